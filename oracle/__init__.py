@@ -1,0 +1,219 @@
+"""Float64 CPU oracle of the TT-EmbeddingBag hot path.
+
+TEST INFRASTRUCTURE ONLY: only ``tests/``, ``__graft_entry__.smoke()`` and the
+CPU-baseline leg of ``bench.py`` may import this package.  The product library
+never loads it, and it imports nothing from the product package.
+
+The arithmetic lives in ``tt_oracle.c`` (plain C, float64, definition written
+out per lookup, see its header).  This module compiles it with gcc, promotes
+the float32 cores to float64 and marshals arrays; the SGD step
+``G <- G - lr dG`` (FBTT README, "Fused Kernel": the update is applied inside
+the backward pass; every gradient is taken at the pre-update cores) is the one
+line of arithmetic done here.
+
+Tables are any objects with ``num_embeddings``, ``p``, ``q`` and ``ranks``
+attributes; cores are ``[p_k, r_{k-1}, q_k, r_k]`` arrays.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import subprocess
+import threading
+
+import numpy as np
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+_SRC = os.path.join(_HERE, "tt_oracle.c")
+_OUT_DIR = os.path.join(_HERE, "_build")
+_LIB_PATH = os.path.join(_OUT_DIR, "libtt_oracle.so")
+_lock = threading.Lock()
+_lib = None
+
+
+class _Table(ctypes.Structure):
+    _fields_ = [
+        ("E", ctypes.c_int64),
+        ("p", ctypes.c_int64 * 3),
+        ("q", ctypes.c_int64 * 3),
+        ("r", ctypes.c_int64 * 2),
+        ("G", ctypes.c_void_p * 3),
+    ]
+
+
+def build(force: bool = False) -> str:
+    """Compile ``tt_oracle.c`` into ``oracle/_build/libtt_oracle.so``."""
+    os.makedirs(_OUT_DIR, exist_ok=True)
+    if not force and os.path.exists(_LIB_PATH) and os.path.getmtime(_LIB_PATH) >= os.path.getmtime(_SRC):
+        return _LIB_PATH
+    tmp = _LIB_PATH + f".tmp{os.getpid()}"
+    base = ["gcc", "-O2", "-std=c99", "-shared", "-fPIC", "-o", tmp, _SRC, "-lm"]
+    try:
+        subprocess.run(base[:1] + ["-fopenmp"] + base[1:], check=True, capture_output=True)
+    except subprocess.CalledProcessError:
+        subprocess.run(base, check=True, capture_output=True)
+    os.replace(tmp, _LIB_PATH)
+    return _LIB_PATH
+
+
+def _load():
+    global _lib
+    with _lock:
+        if _lib is None:
+            lib = ctypes.CDLL(build())
+            i64p = ctypes.POINTER(ctypes.c_int64)
+            lib.tto_num_threads.restype = ctypes.c_int
+            lib.tto_decode.argtypes = [ctypes.c_void_p, ctypes.c_int, ctypes.c_int64, ctypes.c_int64,
+                                       i64p, i64p, i64p, i64p, i64p, i64p]
+            lib.tto_forward.argtypes = [ctypes.c_void_p, ctypes.c_int, ctypes.c_int64, ctypes.c_int64,
+                                        i64p, i64p, ctypes.c_void_p, ctypes.c_int, ctypes.c_int64,
+                                        ctypes.c_void_p, ctypes.c_void_p]
+            lib.tto_backward_core.argtypes = [ctypes.c_void_p, ctypes.c_int, ctypes.c_int64, ctypes.c_int64,
+                                              i64p, i64p, ctypes.c_void_p, ctypes.c_int, ctypes.c_void_p,
+                                              ctypes.c_int, ctypes.c_int, ctypes.c_int64, ctypes.c_void_p,
+                                              ctypes.c_void_p]
+            _lib = lib
+    return _lib
+
+
+def num_threads() -> int:
+    """Threads the oracle's OpenMP loops use."""
+    return int(_load().tto_num_threads())
+
+
+def _i64(a):
+    return np.ascontiguousarray(a, dtype=np.int64)
+
+
+def _ptr(a, ctype=ctypes.c_int64):
+    return a.ctypes.data_as(ctypes.POINTER(ctype))
+
+
+class _Tables:
+    """ctypes table array with float64 copies of the cores kept alive."""
+
+    def __init__(self, tables, cores):
+        if len(tables) != len(cores):
+            raise ValueError("one core triple per table")
+        self.keep = []
+        self.arr = (_Table * len(tables))()
+        for t, (spec, cs) in enumerate(zip(tables, cores)):
+            tt = self.arr[t]
+            tt.E = int(spec.num_embeddings)
+            for k in range(3):
+                tt.p[k] = int(spec.p[k])
+                tt.q[k] = int(spec.q[k])
+                g = np.ascontiguousarray(cs[k], dtype=np.float64)
+                self.keep.append(g)
+                tt.G[k] = g.ctypes.data
+            tt.r[0], tt.r[1] = int(spec.ranks[0]), int(spec.ranks[1])
+
+
+def _bags_per_table(tables, offsets, bags_per_table):
+    nb = int(offsets.shape[0] - 1)
+    if bags_per_table is None:
+        if nb % len(tables):
+            raise ValueError("number of bags is not a multiple of the number of tables")
+        bags_per_table = nb // len(tables)
+    return int(bags_per_table)
+
+
+def _check(rc, what):
+    if rc == 1:
+        raise IndexError(f"oracle {what}: index out of range")
+    if rc != 0:
+        raise ValueError(f"oracle {what}: invalid arguments (code {rc})")
+
+
+def decode(tables, indices, offsets, bags_per_table=None):
+    """(i1, i2, i3, bag) of every lookup, int64 arrays."""
+    lib = _load()
+    idx, off = _i64(indices), _i64(offsets)
+    bpt = _bags_per_table(tables, off, bags_per_table)
+    zero = [np.zeros((1, 1, 1, 1)) for _ in range(3)]
+    tabs = _Tables(tables, [zero] * len(tables))
+    outs = [np.full(idx.shape[0], -1, dtype=np.int64) for _ in range(4)]
+    rc = lib.tto_decode(ctypes.byref(tabs.arr), len(tables), bpt, idx.shape[0], _ptr(idx), _ptr(off),
+                        *[_ptr(o) for o in outs])
+    _check(rc, "decode")
+    return tuple(outs)
+
+
+def forward(tables, cores, indices, offsets, weights=None, mode="sum", bags_per_table=None, bags=None):
+    """Pooled output, float64 ``[num_bags or len(bags), D]``."""
+    lib = _load()
+    idx, off = _i64(indices), _i64(offsets)
+    bpt = _bags_per_table(tables, off, bags_per_table)
+    tabs = _Tables(tables, cores)
+    D = int(np.prod(tables[0].q))
+    w = None if weights is None else np.ascontiguousarray(weights, dtype=np.float64)
+    sel = None if bags is None else _i64(bags)
+    nout = (off.shape[0] - 1) if sel is None else sel.shape[0]
+    out = np.zeros((nout, D), dtype=np.float64)
+    rc = lib.tto_forward(ctypes.byref(tabs.arr), len(tables), bpt, idx.shape[0], _ptr(idx), _ptr(off),
+                         None if w is None else w.ctypes.data, 1 if mode == "mean" else 0,
+                         0 if sel is None else sel.shape[0], None if sel is None else sel.ctypes.data,
+                         out.ctypes.data)
+    _check(rc, "forward")
+    return out
+
+
+def backward_core(tables, cores, indices, offsets, grad_out, table, core, weights=None, mode="sum",
+                  bags_per_table=None, slices=None):
+    """Gradient of core ``core`` of ``table`` for ``slices`` (default: all).
+
+    Returns float64 ``[len(slices), r_{k-1}, q_k, r_k]``.
+    """
+    lib = _load()
+    idx, off = _i64(indices), _i64(offsets)
+    bpt = _bags_per_table(tables, off, bags_per_table)
+    tabs = _Tables(tables, cores)
+    spec = tables[table]
+    rk = [1, int(spec.ranks[0]), int(spec.ranks[1]), 1]
+    shape = (rk[core], int(spec.q[core]), rk[core + 1])
+    sl = np.arange(int(spec.p[core]), dtype=np.int64) if slices is None else _i64(slices)
+    go = np.ascontiguousarray(grad_out, dtype=np.float64)
+    w = None if weights is None else np.ascontiguousarray(weights, dtype=np.float64)
+    dG = np.zeros((sl.shape[0],) + shape, dtype=np.float64)
+    rc = lib.tto_backward_core(ctypes.byref(tabs.arr), len(tables), bpt, idx.shape[0], _ptr(idx), _ptr(off),
+                               None if w is None else w.ctypes.data, 1 if mode == "mean" else 0,
+                               go.ctypes.data, int(table), int(core), sl.shape[0], sl.ctypes.data,
+                               dG.ctypes.data)
+    _check(rc, "backward")
+    return dG
+
+
+def sgd_slices(tables, cores, indices, offsets, grad_out, lr, table, core, weights=None, mode="sum",
+               bags_per_table=None, slices=None):
+    """Updated slices ``G_k[s] - lr dG_k[s]`` in float64 (gradients at the pre-update cores)."""
+    spec = tables[table]
+    sl = np.arange(int(spec.p[core]), dtype=np.int64) if slices is None else _i64(slices)
+    dG = backward_core(tables, cores, indices, offsets, grad_out, table, core, weights, mode,
+                       bags_per_table, sl)
+    return np.asarray(cores[table][core], dtype=np.float64)[sl] - float(lr) * dG
+
+
+def sgd_step(tables, cores, indices, offsets, grad_out, lr, weights=None, mode="sum", bags_per_table=None):
+    """Every core of every table after one fused SGD step, float64."""
+    return [
+        [sgd_slices(tables, cores, indices, offsets, grad_out, lr, t, k, weights, mode, bags_per_table)
+         for k in range(3)]
+        for t in range(len(tables))
+    ]
+
+
+def workload_forward(w, bags=None, cores=None):
+    """``forward`` on a ``tt_inputs.Workload``."""
+    return forward(w.tables, cores or w.cores, w.indices, w.offsets, w.weights, w.mode, w.batch, bags)
+
+
+def workload_backward_core(w, table, core, slices=None, cores=None):
+    """``backward_core`` on a ``tt_inputs.Workload``."""
+    return backward_core(w.tables, cores or w.cores, w.indices, w.offsets, w.grad_out, table, core,
+                         w.weights, w.mode, w.batch, slices)
+
+
+def workload_sgd_slices(w, table, core, slices=None, cores=None):
+    """``sgd_slices`` on a ``tt_inputs.Workload`` with its learning rate."""
+    return sgd_slices(w.tables, cores or w.cores, w.indices, w.offsets, w.grad_out, w.lr, table, core,
+                      w.weights, w.mode, w.batch, slices)

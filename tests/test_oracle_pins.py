@@ -1,0 +1,291 @@
+"""Pins of the float64 oracle against what the pages and the mathematics fix.
+
+None of these checks retypes the oracle's formula: each one compares it with
+an independent route to the same numbers.
+
+* TT-SVD: any E x D matrix has an exact tensor-train form at full ranks
+  (Oseledets, 2011).  Decomposing a random matrix with numpy's SVD and feeding
+  the cores back must reproduce the matrix row for row.  This pins the row
+  decode i = i1 p2 p3 + i2 p3 + i3, the column order j = j1 q2 q3 + j2 q3 + j3
+  and the [p_k, r_{k-1}, q_k, r_k] core layout.
+* Rank 1: with r1 = r2 = 1 a row is the Kronecker product of three vectors.
+* Plain EmbeddingBag: p = [E,1,1], q = [D,1,1], r = [1,1] with unit G2, G3
+  leaves W = G1, which must match torch.nn.functional.embedding_bag (the
+  FBTT README presents the layer as a drop-in for it).
+* Finite differences: L = <out, grad_out> is linear in every single core
+  element, so a central difference with step 1 is exact up to rounding.
+* torch autograd through an einsum of the cores gives the same gradients.
+* Invariants: duplicates act as weight 2, order inside a bag does not
+  matter, mean = sum / L_b, linearity in grad_out, untouched slices keep
+  their exact bits under SGD, batched tables equal separate tables.
+"""
+import itertools
+import json
+import os
+
+import numpy as np
+import pytest
+import torch
+
+import oracle
+from tt_inputs import TableSpec, config
+
+GOLDEN = os.path.join(os.path.dirname(__file__), "golden")
+
+
+def rand_cores(rng, spec, sigma=0.5):
+    return [rng.normal(0, sigma, size=s) for s in spec.core_shapes()]
+
+
+def one_hot_rows(spec, cores, rows=None):
+    rows = np.arange(spec.num_embeddings) if rows is None else np.asarray(rows)
+    off = np.arange(rows.shape[0] + 1)
+    return oracle.forward([spec], [cores], rows, off)
+
+
+def tt_svd(W, p, q):
+    """Exact (full-rank) TT decomposition of W[E, D], cores in [p_k, r_{k-1}, q_k, r_k]."""
+    p1, p2, p3 = p
+    q1, q2, q3 = q
+    X = W.reshape(p1, p2, p3, q1, q2, q3).transpose(0, 3, 1, 4, 2, 5)  # (i1,j1,i2,j2,i3,j3)
+    U, S, Vt = np.linalg.svd(X.reshape(p1 * q1, -1), full_matrices=False)
+    r1 = U.shape[1]
+    G1 = U.reshape(p1, q1, r1)[:, None, :, :]
+    R = (S[:, None] * Vt).reshape(r1 * p2 * q2, p3 * q3)  # rows (a, i2, j2)
+    U2, S2, Vt2 = np.linalg.svd(R, full_matrices=False)
+    r2 = U2.shape[1]
+    G2 = U2.reshape(r1, p2, q2, r2).transpose(1, 0, 2, 3)
+    G3 = (S2[:, None] * Vt2).reshape(r2, p3, q3).transpose(1, 0, 2)[..., None]
+    return [np.ascontiguousarray(G1), np.ascontiguousarray(G2), np.ascontiguousarray(G3)], (r1, r2)
+
+
+@pytest.mark.parametrize("p,q", [([3, 2, 4], [2, 3, 2]), ([2, 5, 3], [4, 1, 3]), ([4, 3, 2], [3, 2, 2])])
+def test_tt_svd_reconstructs_arbitrary_matrix(p, q):
+    rng = np.random.default_rng(1)
+    E, D = int(np.prod(p)), int(np.prod(q))
+    W = rng.standard_normal((E, D))
+    cores, (r1, r2) = tt_svd(W, p, q)
+    spec = TableSpec(E, p, q, [r1, r2])
+    got = one_hot_rows(spec, cores)
+    np.testing.assert_allclose(got, W, rtol=0, atol=1e-12 * np.abs(W).max())
+
+
+def test_rank_one_is_kronecker_product():
+    rng = np.random.default_rng(2)
+    p, q = [3, 4, 5], [2, 3, 2]
+    spec = TableSpec(60, p, q, [1, 1])
+    cores = rand_cores(rng, spec)
+    got = one_hot_rows(spec, cores)
+    for i, (a, b, c) in enumerate(itertools.product(range(p[0]), range(p[1]), range(p[2]))):
+        want = np.kron(np.kron(cores[0][a, 0, :, 0], cores[1][b, 0, :, 0]), cores[2][c, 0, :, 0])
+        np.testing.assert_allclose(got[i], want, rtol=1e-14, atol=1e-15)
+
+
+def test_decode_follows_enumeration_order():
+    p = [3, 4, 5]
+    spec = TableSpec(60, p, [1, 1, 1], [1, 1])
+    idx = np.arange(60)
+    i1, i2, i3, bag = oracle.decode([spec], idx, np.arange(61))
+    want = np.array(list(itertools.product(range(p[0]), range(p[1]), range(p[2]))))
+    np.testing.assert_array_equal(np.stack([i1, i2, i3], 1), want)
+    np.testing.assert_array_equal(bag, idx)
+
+
+def test_padding_rows_rejected():
+    spec = TableSpec(50, [3, 4, 5], [1, 1, 1], [1, 1])  # 60 slots, 50 rows
+    cores = rand_cores(np.random.default_rng(0), spec)
+    with pytest.raises(IndexError):
+        oracle.forward([spec], [cores], np.array([50]), np.array([0, 1]))
+    with pytest.raises(IndexError):
+        oracle.forward([spec], [cores], np.array([-1]), np.array([0, 1]))
+
+
+def _plain_bag_case(rng, E=37, D=6, B=9):
+    spec = TableSpec(E, [E, 1, 1], [D, 1, 1], [1, 1])
+    G1 = rng.standard_normal((E, 1, D, 1))
+    cores = [G1, np.ones((1, 1, 1, 1)), np.ones((1, 1, 1, 1))]
+    lengths = rng.integers(0, 6, size=B)
+    off = np.concatenate([[0], np.cumsum(lengths)])
+    idx = rng.integers(0, E, size=int(off[-1]))
+    w = rng.random(idx.shape[0])
+    return spec, cores, G1[:, 0, :, 0], idx, off, w
+
+
+@pytest.mark.parametrize("mode", ["sum", "mean"])
+def test_plain_embedding_bag_matches_torch(mode):
+    rng = np.random.default_rng(3)
+    spec, cores, W, idx, off, w = _plain_bag_case(rng)
+    got = oracle.forward([spec], [cores], idx, off, mode=mode)
+    want = torch.nn.functional.embedding_bag(
+        torch.from_numpy(idx), torch.from_numpy(W), torch.from_numpy(off[:-1]), mode=mode
+    ).numpy()
+    np.testing.assert_allclose(got, want, rtol=1e-14, atol=1e-14)
+
+
+def test_plain_embedding_bag_weights_and_gradient_match_torch():
+    rng = np.random.default_rng(4)
+    spec, cores, W, idx, off, w = _plain_bag_case(rng)
+    go = rng.standard_normal((off.shape[0] - 1, W.shape[1]))
+    Wt = torch.from_numpy(W.copy()).requires_grad_(True)
+    out = torch.nn.functional.embedding_bag(
+        torch.from_numpy(idx), Wt, torch.from_numpy(off[:-1]), mode="sum",
+        per_sample_weights=torch.from_numpy(w),
+    )
+    (out * torch.from_numpy(go)).sum().backward()
+    got = oracle.forward([spec], [cores], idx, off, weights=w)
+    np.testing.assert_allclose(got, out.detach().numpy(), rtol=1e-14, atol=1e-14)
+    dG1 = oracle.backward_core([spec], [cores], idx, off, go, 0, 0, weights=w)
+    np.testing.assert_allclose(dG1[:, 0, :, 0], Wt.grad.numpy(), rtol=1e-13, atol=1e-13)
+
+
+def _loss(spec, cores, idx, off, go, w, mode):
+    return float((oracle.forward([spec], [cores], idx, off, weights=w, mode=mode) * go).sum())
+
+
+@pytest.mark.parametrize("mode,weighted", [("sum", False), ("mean", True)])
+def test_backward_matches_exact_finite_differences(mode, weighted):
+    wl = config(1)
+    spec, cores = wl.tables[0], [c.astype(np.float64) for c in wl.cores[0]]
+    rng = np.random.default_rng(5)
+    w = rng.random(wl.nnz) if weighted else None
+    go = wl.grad_out.astype(np.float64)
+    for k in range(3):
+        dG = oracle.backward_core([spec], [cores], wl.indices, wl.offsets, go, 0, k, weights=w, mode=mode)
+        fd = np.zeros_like(cores[k])
+        flat = cores[k].reshape(-1)
+        for e in range(flat.shape[0]):
+            keep = flat[e]
+            flat[e] = keep + 1.0
+            lp = _loss(spec, cores, wl.indices, wl.offsets, go, w, mode)
+            flat[e] = keep - 1.0
+            lm = _loss(spec, cores, wl.indices, wl.offsets, go, w, mode)
+            flat[e] = keep
+            fd.reshape(-1)[e] = 0.5 * (lp - lm)
+        np.testing.assert_allclose(dG, fd, rtol=1e-10, atol=1e-11)
+
+
+def test_backward_matches_torch_autograd():
+    rng = np.random.default_rng(6)
+    spec = TableSpec(100, [5, 4, 6], [2, 3, 2], [3, 5])
+    cores = rand_cores(rng, spec)
+    B = 7
+    lengths = rng.integers(0, 5, size=B)
+    off = np.concatenate([[0], np.cumsum(lengths)])
+    idx = rng.integers(0, 100, size=int(off[-1]))
+    w = rng.random(idx.shape[0])
+    go = rng.standard_normal((B, 12))
+    gt = [torch.from_numpy(c.copy()).requires_grad_(True) for c in cores]
+    full = torch.einsum("xja,yakc,zcl->xyzjkl", gt[0][:, 0], gt[1], gt[2][..., 0]).reshape(120, 12)
+    bag = torch.from_numpy(np.repeat(np.arange(B), lengths))
+    L = torch.from_numpy(lengths).double()
+    s = torch.from_numpy(w) / L[bag]
+    out = torch.zeros(B, 12, dtype=torch.float64).index_add_(0, bag, s[:, None] * full[torch.from_numpy(idx)])
+    (out * torch.from_numpy(go)).sum().backward()
+    np.testing.assert_allclose(
+        oracle.forward([spec], [cores], idx, off, weights=w, mode="mean"), out.detach().numpy(), rtol=1e-12, atol=1e-13
+    )
+    for k in range(3):
+        dG = oracle.backward_core([spec], [cores], idx, off, go, 0, k, weights=w, mode="mean")
+        np.testing.assert_allclose(dG, gt[k].grad.numpy(), rtol=1e-12, atol=1e-13)
+
+
+def test_pooling_invariants():
+    rng = np.random.default_rng(7)
+    spec = TableSpec(100, [5, 4, 5], [2, 2, 2], [3, 4])
+    cores = rand_cores(rng, spec)
+    # a duplicated index is the same as weight 2
+    a = oracle.forward([spec], [cores], np.array([3, 3, 17]), np.array([0, 3]))
+    b = oracle.forward([spec], [cores], np.array([3, 17]), np.array([0, 2]), weights=np.array([2.0, 1.0]))
+    np.testing.assert_allclose(a, b, rtol=1e-14, atol=1e-15)
+    # order inside a bag does not matter
+    idx = rng.integers(0, 100, size=9)
+    a = oracle.forward([spec], [cores], idx, np.array([0, 9]))
+    b = oracle.forward([spec], [cores], idx[::-1].copy(), np.array([0, 9]))
+    np.testing.assert_allclose(a, b, rtol=1e-13, atol=1e-14)
+    # mean = sum / L, and an empty bag is a zero row
+    off = np.array([0, 4, 4, 9])
+    s = oracle.forward([spec], [cores], idx, off)
+    m = oracle.forward([spec], [cores], idx, off, mode="mean")
+    np.testing.assert_allclose(m[0], s[0] / 4, rtol=1e-14)
+    np.testing.assert_allclose(m[2], s[2] / 5, rtol=1e-14)
+    assert not s[1].any() and not m[1].any()
+    # the selected-bag path gives the same rows
+    np.testing.assert_array_equal(oracle.forward([spec], [cores], idx, off, bags=[2, 0]), s[[2, 0]])
+
+
+def test_backward_invariants():
+    wl = config(1)
+    spec, cores = wl.tables[0], wl.cores[0]
+    rng = np.random.default_rng(8)
+    g1 = rng.standard_normal(wl.grad_out.shape)
+    g2 = rng.standard_normal(wl.grad_out.shape)
+    for k in range(3):
+        d1 = oracle.backward_core([spec], [cores], wl.indices, wl.offsets, g1, 0, k)
+        d2 = oracle.backward_core([spec], [cores], wl.indices, wl.offsets, g2, 0, k)
+        d12 = oracle.backward_core([spec], [cores], wl.indices, wl.offsets, 2 * g1 - 3 * g2, 0, k)
+        np.testing.assert_allclose(d12, 2 * d1 - 3 * d2, rtol=1e-12, atol=1e-13)
+    # untouched slices keep their exact bits, touched ones move
+    i1, i2, i3, _ = oracle.decode([spec], wl.indices, wl.offsets)
+    new = oracle.sgd_step([spec], [cores], wl.indices, wl.offsets, wl.grad_out, wl.lr)[0]
+    for k, ik in enumerate([i1, i2, i3]):
+        untouched = np.setdiff1d(np.arange(spec.p[k]), ik)
+        np.testing.assert_array_equal(new[k][untouched], cores[k][untouched].astype(np.float64))
+        touched = np.unique(ik)
+        assert np.abs(new[k][touched] - cores[k][touched]).max() > 0
+
+
+def test_batched_tables_equal_separate_tables():
+    rng = np.random.default_rng(9)
+    specs = [TableSpec(60, [3, 4, 5], [2, 2, 2], [2, 3]), TableSpec(30, [2, 3, 5], [4, 1, 2], [4, 2])]
+    cores = [rand_cores(rng, s) for s in specs]
+    B = 5
+    parts, offs = [], [0]
+    for s in specs:
+        lengths = rng.integers(0, 4, size=B)
+        parts.append(rng.integers(0, s.num_embeddings, size=int(lengths.sum())))
+        offs.extend(offs[-1] + np.cumsum(lengths))
+    idx, off = np.concatenate(parts), np.array(offs)
+    go = rng.standard_normal((2 * B, 8))
+    both = oracle.forward(specs, cores, idx, off)
+    for t in range(2):
+        sub_off = off[t * B : (t + 1) * B + 1] - off[t * B]
+        sub_idx = idx[off[t * B] : off[(t + 1) * B]]
+        np.testing.assert_array_equal(both[t * B : (t + 1) * B], oracle.forward([specs[t]], [cores[t]], sub_idx, sub_off))
+        for k in range(3):
+            np.testing.assert_array_equal(
+                oracle.backward_core(specs, cores, idx, off, go, t, k),
+                oracle.backward_core([specs[t]], [cores[t]], sub_idx, sub_off, go[t * B : (t + 1) * B], 0, k),
+            )
+
+
+def test_page_usage_example_offsets_convention():
+    """FBTT README usage example: 10 rows of width 3, two bags of four lookups.
+
+    The page prints values drawn from a random initialisation, so only the
+    shape and the bag split given by start-position offsets are pinned.
+    """
+    with open(os.path.join(GOLDEN, "fbtt_readme_usage_example.json")) as f:
+        ex = json.load(f)
+    idx = np.array(ex["input"])
+    csr = np.concatenate([ex["offsets"], [idx.shape[0]]])
+    spec = TableSpec(ex["num_embeddings"], ex["p_shapes_used_here"], ex["q_shapes_used_here"], ex["tt_ranks"])
+    cores = rand_cores(np.random.default_rng(10), spec)
+    out = oracle.forward([spec], [cores], idx, csr)
+    assert list(out.shape) == ex["output_shape"]
+    rows = one_hot_rows(spec, cores)
+    for b, members in enumerate(ex["bag_members"]):
+        np.testing.assert_allclose(out[b], rows[members].sum(0), rtol=1e-14, atol=1e-15)
+
+
+def test_tiny_workload_golden():
+    """Regression fixture written by tests/golden/make_golden.py (oracle only)."""
+    with open(os.path.join(GOLDEN, "config1_oracle.json")) as f:
+        g = json.load(f)
+    wl = config(1)
+    np.testing.assert_array_equal(wl.indices, g["indices"])
+    np.testing.assert_array_equal(wl.offsets, g["offsets"])
+    np.testing.assert_allclose(oracle.workload_forward(wl), np.array(g["out"]), rtol=1e-15, atol=1e-15)
+    for k in range(3):
+        np.testing.assert_allclose(
+            oracle.workload_sgd_slices(wl, 0, k), np.array(g["updated_cores"][k]), rtol=1e-15, atol=1e-15
+        )
