@@ -1,0 +1,411 @@
+"""TT-EmbeddingBag forward + backward (fused SGD) throughput on GB300.
+
+Workload: the FBTT README sample configuration, p = [200, 220, 250]
+(E = 11,000,000), q = [4, 4, 4] (D = 64), ranks [32, 32], 512 bags of exactly
+20 uniform lookups (nnz = 10,240), sum pooling, SGD lr = 0.1; seeded synthetic
+data resident in HBM.  One step = forward + backward with the in-place core
+update, through the C ABI.
+
+Default arm prints one JSON line with the device-timed throughput (value,
+lookups/s), the end-to-end number through the C ABI with host buffers (e2e),
+the roofline of the dominant kernel from live CUDA events, clocks sampled
+during the timed region and the float64 oracle timed on the host cores
+(cpu_baseline).  ``--impl reference`` times that oracle alone on bounded
+samples of the same workload.
+
+Launch: ``python bench.py --gpus 1 --steps K --warmup W``; for N > 1 under
+``torch.distributed.run`` every rank runs an independent replica on its own
+GPU (weak scaling, no collective on the data path); rank 0 prints.
+"""
+import argparse
+import json
+import os
+import statistics
+import subprocess
+import sys
+import tempfile
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+METRIC = "TT-EmbeddingBag fwd+bwd ns/nnz (lookups/s) and % of roofline, 1×GB300"
+WORKLOAD = "TT-EmbeddingBag 11M x 64 rank-32 (p=[200,220,250], q=[4,4,4]), B=512 x 20 uniform lookups, sum, fused SGD"
+SM_COUNT = 152
+FP32_LANES_PER_SM = 128
+SM_MAX_MHZ = 2070.0
+L2_FLUSH_BYTES = 256 << 20
+
+
+def peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            d = json.load(f)
+        return d, "measured"
+    except OSError:
+        return {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "sm_max_mhz": SM_MAX_MHZ}, "fallback"
+
+
+def fp32_peak_tflops(sm_mhz):
+    # FFMA: 128 lanes x 2 FLOP per SM per clock
+    return SM_COUNT * FP32_LANES_PER_SM * 2 * sm_mhz * 1e6 / 1e12
+
+
+def flops_per_lookup(spec):
+    q1, q2, q3 = spec.q
+    r1, r2 = spec.ranks
+    A = q1 * r1 * q2 * r2
+    Bc = q1 * q2 * r2 * q3
+    return A, Bc
+
+
+def dist_env():
+    ws = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return ws, rank, local
+
+
+class ClockSampler:
+    """nvidia-smi samples of the SM clock and throttle reasons during a region."""
+
+    FIELDS = ("clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index):
+        self.gpu = gpu_index
+        self.proc = None
+        self.file = None
+
+    def start(self):
+        try:
+            self.file = tempfile.TemporaryFile(mode="w+")
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.gpu), f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits",
+                 "-lms", "50"], stdout=self.file, stderr=subprocess.DEVNULL)
+        except (OSError, ValueError):
+            self.proc = None
+
+    def stop(self):
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"], "samples": 0}
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+        self.file.seek(0)
+        sm, smax, reasons, n = [], [], set(), 0
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for line in self.file:
+            parts = [p.strip() for p in line.split(",")]
+            if len(parts) < 8:
+                continue
+            try:
+                sm.append(float(parts[0]))
+                smax.append(float(parts[1]))
+            except ValueError:
+                continue
+            n += 1
+            for name, v in zip(names, parts[4:8]):
+                if v.lower() == "active":
+                    reasons.add(name)
+        self.file.close()
+        return {
+            "sm_mhz": statistics.median(sm) if sm else None,
+            "sm_max_mhz": max(smax) if smax else None,
+            "reasons": sorted(reasons),
+            "samples": n,
+        }
+
+
+# ---------------------------------------------------------------- reference arm (oracle)
+
+
+def sub_workload(wl, nbags):
+    from tt_inputs import Workload
+
+    n = int(wl.offsets[nbags])
+    return Workload(**{**wl.__dict__, "indices": wl.indices[:n], "offsets": wl.offsets[: nbags + 1],
+                       "grad_out": wl.grad_out[:nbags], "batch": nbags})
+
+
+def oracle_step(sub):
+    import oracle
+
+    oracle.workload_forward(sub)
+    for k in range(3):
+        oracle.workload_sgd_slices(sub, 0, k)
+
+
+def cpu_baseline(wl, nbags=None):
+    """One oracle fwd + bwd + SGD step on the first `nbags` bags, timed on the host."""
+    import oracle
+
+    nbags = nbags or wl.num_bags
+    sub = sub_workload(wl, nbags)
+    oracle.build()
+    t0 = time.perf_counter()
+    oracle_step(sub)
+    dt = time.perf_counter() - t0
+    return {
+        "value": sub.nnz / dt,
+        "unit": "lookups/s",
+        "cores": oracle.num_threads(),
+        "kind": "oracle",
+        "sample": f"{nbags} of {wl.num_bags} bags ({sub.nnz} lookups), one forward + backward + SGD step, "
+                  f"float64, {dt:.2f} s",
+    }
+
+
+def run_reference(args):
+    ws, rank, _ = dist_env()
+    if rank != 0:
+        return 0
+    import oracle
+    import tt_inputs
+
+    wl = tt_inputs.config(2)
+    oracle.build()
+    # size each step's sample so that warmup + steps finish in about two minutes
+    budget = max(0.05, min(2.0, 120.0 / max(1, args.steps + args.warmup)))
+    probe = sub_workload(wl, 8)
+    t0 = time.perf_counter()
+    oracle_step(probe)
+    per_bag = (time.perf_counter() - t0) / 8
+    nbags = int(max(1, min(wl.num_bags, budget / max(per_bag, 1e-9))))
+    sub = sub_workload(wl, nbags)
+    for _ in range(args.warmup):
+        oracle_step(sub)
+    t0 = time.perf_counter()
+    for _ in range(args.steps):
+        oracle_step(sub)
+    dt = time.perf_counter() - t0
+    value = sub.nnz * args.steps / dt
+    line = {
+        "impl": "reference",
+        "metric": METRIC,
+        "value": value,
+        "unit": "lookups/s",
+        "n_gpus": ws,
+        "steps": args.steps,
+        "warmup": args.warmup,
+        "ms_per_step": dt / args.steps * 1e3,
+        "ns_per_nnz": 1e9 * dt / (sub.nnz * args.steps),
+        "higher_is_better": True,
+        "scaling": "weak",
+        "vs_baseline": None,
+        "dtype": "f64",
+        "data": "synthetic",
+        "config": {"workload": WORKLOAD, "sample_bags": nbags, "sample_nnz": sub.nnz},
+        "cpu_baseline": {
+            "value": value, "unit": "lookups/s", "cores": oracle.num_threads(), "kind": "oracle",
+            "sample": f"first {nbags} of 512 bags ({sub.nnz} lookups) per step, forward + backward + SGD, float64",
+        },
+        "e2e": {"value": value, "unit": "lookups/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+    return 0
+
+
+# ---------------------------------------------------------------- GPU arm
+
+
+def run_gpu(args):
+    import torch
+    import torch.distributed as dist
+
+    import tensor_train_compressed_embeddingbag_gb300 as tt
+    import tt_inputs
+
+    ws, rank, local = dist_env()
+    if ws > 1:
+        dist.init_process_group("nccl", device_id=torch.device("cuda", local))
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    tt.build()
+    tt.load_library()
+
+    wl = tt_inputs.config(2)
+    spec = wl.tables[0]
+    D, nnz, B = spec.embedding_dim, wl.nnz, wl.num_bags
+    cores = [torch.from_numpy(c).to(dev) for c in wl.cores[0]]
+    h = tt.tt_emb_create(spec.num_embeddings, spec.p, spec.q, spec.ranks, cores)
+    tt.tt_emb_reserve(h, nnz, B)
+    idx = torch.from_numpy(wl.indices).to(dev)
+    off = torch.from_numpy(wl.offsets).to(dev)
+    go = torch.from_numpy(wl.grad_out).to(dev)
+    out = torch.empty((B, D), dtype=torch.float32, device=dev)
+    flush = torch.empty(L2_FLUSH_BYTES // 4, dtype=torch.float32, device=dev)
+    stream = torch.cuda.current_stream(dev)
+    lr = wl.lr
+
+    def step():
+        tt.tt_emb_forward(h, idx, off, None, tt.TT_POOL_SUM, out, stream)
+        tt.tt_emb_backward(h, go, lr, stream)
+
+    def barrier():
+        torch.cuda.synchronize(dev)
+        if ws > 1:
+            dist.barrier()
+        torch.cuda.synchronize(dev)
+
+    def timed(fn, steps):
+        """Sum of per-step device times (ms), L2 flushed before every step outside the events."""
+        ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(steps)]
+        barrier()
+        for s, e in ev:
+            flush.fill_(1.0)
+            s.record(stream)
+            fn()
+            e.record(stream)
+        barrier()
+        return sum(s.elapsed_time(e) for s, e in ev)
+
+    for _ in range(max(3, args.warmup)):
+        step()
+    err = tt.tt_emb_get_last_error(h)
+    if err != tt.TT_OK:
+        raise RuntimeError(f"device error during warm-up: {tt.tt_emb_status_string(err)}")
+    launches_per_step = tt.tt_emb_last_launch_count(h, 0) + tt.tt_emb_last_launch_count(h, 1)
+
+    vis = [v for v in os.environ.get("CUDA_VISIBLE_DEVICES", "").split(",") if v.strip()]
+    sampler = ClockSampler(vis[local] if local < len(vis) else str(local))
+    sampler.start()
+    time.sleep(0.2)
+    ms_total = timed(step, args.steps)
+    clocks = sampler.stop()
+    t = torch.tensor([ms_total], dtype=torch.float64, device=dev)
+    if ws > 1:
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    ms_total = float(t.item())
+    if tt.tt_emb_get_last_error(h) != tt.TT_OK:
+        raise RuntimeError("device error in the timed region")
+
+    # forward alone
+    ms_fwd = timed(lambda: tt.tt_emb_forward(h, idx, off, None, tt.TT_POOL_SUM, out, stream), args.steps)
+
+    # per-kernel durations from the library's stage events (same stream, same steps)
+    tt.tt_emb_set_stage_timing(h, True)
+    kstats = {}
+    nstage = min(args.steps, 400)
+    barrier()
+    for _ in range(nstage):
+        flush.fill_(1.0)
+        step()
+        for which in (0, 1):
+            for name, ms in tt.tt_emb_stage_times(h, which):
+                kstats.setdefault(name, []).append(ms)
+    tt.tt_emb_set_stage_timing(h, False)
+    kavg = {k: sum(v) / len(v) for k, v in kstats.items()}
+
+    # end to end through the C ABI with host buffers: inputs copied in, result copied out, every step
+    idx_h = torch.from_numpy(wl.indices).pin_memory()
+    off_h = torch.from_numpy(wl.offsets).pin_memory()
+    go_h = torch.from_numpy(wl.grad_out).pin_memory()
+    out_h = torch.empty((B, D), dtype=torch.float32).pin_memory()
+    h2d = idx_h.numel() * 8 + off_h.numel() * 8 + go_h.numel() * 4
+    d2h = out_h.numel() * 4
+
+    def e2e_step():
+        idx.copy_(idx_h, non_blocking=True)
+        off.copy_(off_h, non_blocking=True)
+        go.copy_(go_h, non_blocking=True)
+        step()
+        out_h.copy_(out, non_blocking=True)
+
+    ms_e2e = timed(e2e_step, args.steps)
+    te = torch.tensor([ms_e2e, ms_fwd], dtype=torch.float64, device=dev)
+    if ws > 1:
+        dist.all_reduce(te, op=dist.ReduceOp.MAX)
+    ms_e2e, ms_fwd = float(te[0].item()), float(te[1].item())
+
+    result = None
+    if rank == 0:
+        pk, pk_kind = peaks()
+        A, Bc = flops_per_lookup(spec)
+        total_lookups = nnz * args.steps * ws
+        value = total_lookups / (ms_total / 1e3)
+        # dominant kernel and its algorithmic FLOPs per launch (per-lookup figures x nnz)
+        kernel_flops = {
+            "tile_fwd": 2 * A * nnz,            # T = G1 G2, per lookup 2 q1 r1 q2 r2
+            "pool": 2 * Bc * nnz,               # row = T G3, per lookup 2 q1 q2 r2 q3
+            "tile_bwd": 4 * (A + Bc) * nnz,     # dT, dG3, dG1, dG2, per lookup 4 (A + Bc)
+        }
+        dom = max(kavg, key=kavg.get)
+        sm_mhz = SM_MAX_MHZ
+        peak_tf = fp32_peak_tflops(sm_mhz)
+        if dom in kernel_flops:
+            ach = kernel_flops[dom] / (kavg[dom] * 1e-3) / 1e12
+            roof = {"bound": "alu", "achieved": ach, "peak": peak_tf, "unit": "TFLOP/s", "frac": ach / peak_tf,
+                    "traffic": None, "kernel": dom, "avg_ms": kavg[dom],
+                    "peak_source": "FP32 FFMA: 152 SMs x 128 lanes x 2 FLOP x 2070 MHz"}
+        else:
+            roof = {"bound": "hbm", "achieved": None, "peak": pk["hbm_gbs"], "unit": "GB/s", "frac": None,
+                    "traffic": None, "kernel": dom, "avg_ms": kavg[dom]}
+        step_flops = 6 * (A + Bc) * nnz
+        step_tf = step_flops / (ms_total / args.steps * 1e-3) / 1e12
+        result = {
+            "metric": METRIC,
+            "value": value,
+            "unit": "lookups/s",
+            "n_gpus": ws,
+            "steps": args.steps,
+            "warmup": max(3, args.warmup),
+            "ms_per_step": ms_total / args.steps,
+            "ns_per_nnz": 1e6 * ms_total / (nnz * args.steps),
+            "higher_is_better": True,
+            "scaling": "weak",
+            "vs_baseline": None,
+            "dtype": "f32",
+            "data": "synthetic",
+            "config": {
+                "workload": WORKLOAD,
+                "nnz": nnz,
+                "bags": B,
+                "p": spec.p, "q": spec.q, "ranks": spec.ranks,
+                "l2": f"flushed before every timed step ({L2_FLUSH_BYTES >> 20} MiB write, outside the events)",
+                "replicas": ws,
+            },
+            "forward": {"ns_per_nnz": 1e6 * ms_fwd / (nnz * args.steps),
+                        "lookups_per_s": nnz * args.steps * ws / (ms_fwd / 1e3)},
+            "step_roofline": {"flops_per_step": step_flops, "achieved_tflops": step_tf, "peak_tflops": peak_tf,
+                              "frac": step_tf / peak_tf, "flop_formula": "6 (q1 r1 q2 r2 + q1 q2 r2 q3) per lookup"},
+            "roofline": roof,
+            "kernels_ms": kavg,
+            "gpu_launches": launches_per_step * args.steps,
+            "clocks": clocks,
+            "peaks_source": pk_kind,
+            "e2e": {"value": total_lookups / (ms_e2e / 1e3), "unit": "lookups/s",
+                    "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h},
+        }
+    tt.tt_emb_destroy(h)
+    if rank == 0 and not args.no_cpu_baseline:
+        result["cpu_baseline"] = cpu_baseline(wl)
+    if rank == 0:
+        print(json.dumps(result), flush=True)
+    if ws > 1:
+        dist.barrier()
+        dist.destroy_process_group()
+    return 0
+
+
+def main():
+    ap = argparse.ArgumentParser(description=__doc__, formatter_class=argparse.RawDescriptionHelpFormatter)
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=3000)
+    ap.add_argument("--warmup", type=int, default=20)
+    ap.add_argument("--impl", choices=["gb300", "reference"], default="gb300")
+    ap.add_argument("--no-cpu-baseline", action="store_true", help="skip the oracle timing")
+    args = ap.parse_args()
+    if args.impl == "reference":
+        return run_reference(args)
+    return run_gpu(args)
+
+
+if __name__ == "__main__":
+    sys.exit(main())

@@ -1,0 +1,189 @@
+/*
+ * tt_emb.h -- C ABI of the GB300 (sm_103a) TT-EmbeddingBag library, libttemb.so.
+ *
+ * A TT-EmbeddingBag is a drop-in EmbeddingBag whose E x D table is held as
+ * three tensor-train cores (TT-Rec / FBTT-Embedding pages; FBTT README,
+ * opening paragraph and "How FBTT-Embedding works").  Row i, decoded as
+ * i = i1 p2 p3 + i2 p3 + i3, is the chain product G1[i1] G2[i2] G3[i3]; the
+ * rows named by each bag are sum- or mean-pooled (optionally weighted) into
+ * one output row, and the backward pass applies a fused sparse SGD update to
+ * the touched core slices (FBTT README, "Fused Kernel", sparse=True).
+ *
+ * Conventions for every entry point:
+ *   - Pointers named *_dev are CUDA device pointers; the caller owns them and
+ *     keeps them valid until the work queued on `stream` has completed.
+ *   - Core k of a table is float32 [p_k][r_{k-1}][q_k][r_k] (r_0 = r_3 = 1),
+ *     C-contiguous, so slice G_k[i_k] is contiguous.  The FBTT README's
+ *     "Initialization" section gives the cores as r_{k-1} x p_k x q_k x r_k;
+ *     the slice index is moved first here, which changes no value.
+ *   - Column j of a row is j = j1 q2 q3 + j2 q3 + j3.
+ *   - Bags are CSR: offsets_dev has num_bags + 1 int64 entries, offsets[0] = 0,
+ *     offsets[num_bags] = nnz, non-decreasing; bag g holds the lookups
+ *     offsets[g] .. offsets[g+1]-1.  (PyTorch's EmbeddingBag passes the B
+ *     start positions only; append nnz to convert.)
+ *   - A handle is not thread-safe; calls on one handle must be issued from
+ *     one host thread and be ordered on the streams they are given.
+ *   - No call throws; each returns a tt_status.  Host-side validation runs
+ *     before anything is queued, and on failure nothing is modified.  Errors
+ *     found on the device (an index outside [0, E), malformed offsets) are
+ *     recorded in a sticky per-handle flag read by tt_emb_get_last_error();
+ *     the offending lookups contribute nothing to the output, and a backward
+ *     pass that follows such a forward pass leaves every core unchanged.
+ */
+#ifndef TT_EMB_H
+#define TT_EMB_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef struct tt_emb tt_emb;          /* opaque handle */
+typedef struct CUstream_st* tt_stream; /* same type as cudaStream_t; NULL = legacy default stream */
+
+typedef enum {
+    TT_OK = 0,
+    TT_ERR_ARG = 1,     /* bad argument: null pointer, negative size, unknown mode */
+    TT_ERR_SHAPE = 2,   /* inconsistent TT shape: p1 p2 p3 < E, q1 q2 q3 != D, rank <= 0, limits */
+    TT_ERR_INDEX = 3,   /* device found an index outside [0, E) */
+    TT_ERR_CUDA = 4,    /* a CUDA runtime call failed */
+    TT_ERR_STATE = 5,   /* call out of order, e.g. backward without a forward */
+    TT_ERR_TIMEOUT = 6, /* a bounded device wait gave up */
+    TT_ERR_NOMEM = 7    /* device workspace allocation failed */
+} tt_status;
+
+typedef enum { TT_POOL_SUM = 0, TT_POOL_MEAN = 1 } tt_pool;
+
+/* Limits checked by the create calls. */
+#define TT_MAX_P 1048576 /* each p_k */
+#define TT_MAX_Q 64      /* each q_k */
+#define TT_MAX_RANK 128  /* each r_k */
+#define TT_MAX_D 256     /* q1 q2 q3 */
+
+/* One table of a table-batched handle (FBTT README, "TableBatchedTTEmbeddingBag"). */
+typedef struct {
+    int64_t num_embeddings; /* E: rows of this table */
+    int64_t p[3];           /* row factorisation, p1 p2 p3 >= E (FBTT README, "Parameters": tt_p_shapes) */
+    int32_t q[3];           /* column factorisation, q1 q2 q3 = D (tt_q_shapes) */
+    int32_t ranks[2];       /* r1, r2 (tt_ranks) */
+    float* cores_dev[3];    /* caller-owned device cores, updated in place by tt_emb_backward */
+} tt_table_desc;
+
+/*
+ * Create a single-table handle.  FBTT README, "Parameters" (num_embeddings,
+ * tt_p_shapes, tt_q_shapes, tt_ranks).  cores_dev[k] must hold
+ * p_k * r_{k-1} * q_k * r_k floats.  The handle keeps the core pointers (not
+ * the data); the caller keeps the cores alive while the handle is used.
+ * Device memory for the handle's fixed tables is allocated on the current
+ * CUDA device, which every later call on the handle must also use.
+ * Returns TT_ERR_ARG (null out/cores), TT_ERR_SHAPE (see limits above).
+ */
+tt_status tt_emb_create(int64_t num_embeddings, const int64_t p[3], const int32_t q[3],
+                        const int32_t ranks[2], float* const cores_dev[3], tt_emb** out);
+
+/*
+ * Create a table-batched handle over num_tables >= 1 tables that share D
+ * (FBTT README, "TableBatchedTTEmbeddingBag": many tables in one call; unlike
+ * the README's version, the tables may differ in E, p, q and ranks).  Bags of
+ * a batched call are ordered table-major: bag g = t * B + b is sample b of
+ * table t, and its indices are row ids of table t.
+ */
+tt_status tt_emb_batch_create(int32_t num_tables, const tt_table_desc* descs, tt_emb** out);
+
+/* Release the handle's device memory (not the caller's cores).  NULL is a no-op. */
+void tt_emb_destroy(tt_emb* h);
+
+/*
+ * Size the handle's workspace for up to max_nnz lookups and max_bags bags, so
+ * that later forward/backward calls within those sizes allocate nothing (and
+ * may be captured in a CUDA graph).  Forward calls beyond the reserved sizes
+ * grow the workspace themselves.
+ */
+tt_status tt_emb_reserve(tt_emb* h, int64_t max_nnz, int64_t max_bags);
+
+/*
+ * Forward pass (FBTT README, "How FBTT-Embedding works": forward(input,
+ * offsets); the pooling of PyTorch's EmbeddingBag).
+ *   indices_dev          int64 [nnz]          row ids (of the bag's table)
+ *   offsets_dev          int64 [num_bags + 1] CSR bag boundaries
+ *   per_sample_weights   float [nnz] or NULL   (NULL: every weight is 1)
+ *   mode                 TT_POOL_SUM: out[g] = sum_n w_n row_n
+ *                        TT_POOL_MEAN: out[g] = (1/L_g) sum_n w_n row_n, L_g = bag length
+ *   out_dev              float [num_bags][D], written completely (empty bag: zeros)
+ * num_bags must be a multiple of the handle's table count.  The decoded
+ * lookups, their grouping and the partial products G1[i1] G2[i2] are kept in
+ * the handle for the next tt_emb_backward().  Asynchronous on `stream`.
+ * Returns TT_ERR_ARG (null pointers with nnz > 0, negative sizes, bad mode,
+ * num_bags not a multiple of the table count), TT_ERR_NOMEM, TT_ERR_CUDA.
+ */
+tt_status tt_emb_forward(tt_emb* h, const int64_t* indices_dev, int64_t nnz,
+                         const int64_t* offsets_dev, int64_t num_bags,
+                         const float* per_sample_weights_dev, tt_pool mode, float* out_dev,
+                         tt_stream stream);
+
+/*
+ * Backward pass fused with SGD (FBTT README, "Fused Kernel", sparse=True with
+ * OptimType.SGD): for L = sum_g <out[g], grad_out[g]> of the most recent
+ * forward pass on this handle, every touched slice becomes
+ * G_k[s] - lr * dL/dG_k[s], all gradients taken at the pre-update cores;
+ * no gradient is returned.  grad_out_dev is float [num_bags][D] of that
+ * forward pass.  Consumes the saved forward state: a second backward without
+ * a new forward returns TT_ERR_STATE.  If the forward pass recorded a device
+ * error, no core is changed.  Asynchronous on `stream`.
+ */
+tt_status tt_emb_backward(tt_emb* h, const float* grad_out_dev, float lr, tt_stream stream);
+
+/*
+ * Hot-row cache (FBTT README, "Software Cache"): decompress the n rows of
+ * table 0 listed in rows_dev (int64, distinct, within [0, E)) into a
+ * device-resident fp32 cache.  Later forward passes read a cached row instead
+ * of contracting it, as long as its three core slices have not changed since
+ * it was filled; a backward pass marks the rows whose slices it updated as
+ * stale and the next forward pass recomputes those rows and writes them back
+ * into the cache.  Results are the same as without a cache.  Replaces any
+ * previous cache content.  Single-table handles only (TT_ERR_STATE otherwise).
+ */
+tt_status tt_emb_cache_populate(tt_emb* h, const int64_t* rows_dev, int64_t n, tt_stream stream);
+
+/* Drop the cache and free its memory. */
+tt_status tt_emb_cache_disable(tt_emb* h);
+
+/*
+ * Copy the decode of the most recent forward pass: for every lookup its
+ * table, its slice indices (i1, i2, i3) and its bag.  Each *_dev is a
+ * caller-owned int32 [nnz] device buffer; any may be NULL.  For checks.
+ */
+tt_status tt_emb_get_decoded(tt_emb* h, int32_t* table_dev, int32_t* i1_dev, int32_t* i2_dev,
+                             int32_t* i3_dev, int32_t* bag_dev, tt_stream stream);
+
+/*
+ * Wait for the handle's queued work, then return and clear the sticky device
+ * error (TT_ERR_INDEX, TT_ERR_ARG for malformed offsets, TT_ERR_TIMEOUT) or
+ * TT_OK.  Returns TT_ERR_CUDA if the wait itself fails.
+ */
+tt_status tt_emb_get_last_error(tt_emb* h);
+
+/*
+ * Stage timing: when enabled, each forward/backward records a CUDA event
+ * after each of its kernels on the call's stream.  tt_emb_stage_times()
+ * waits for the last call and writes up to cap per-kernel durations in
+ * milliseconds (kernel order of that call) with their names; returns the
+ * number of kernels the call launched, or -1 on error.
+ */
+tt_status tt_emb_set_stage_timing(tt_emb* h, int enable);
+int tt_emb_stage_times(tt_emb* h, int which /* 0 forward, 1 backward */, float* ms, const char** names,
+                       int cap);
+
+/* Kernels launched by the most recent forward (which = 0) or backward (1). */
+int tt_emb_last_launch_count(tt_emb* h, int which);
+
+/* Static description of a status code; never NULL. */
+const char* tt_emb_status_string(tt_status s);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* TT_EMB_H */

@@ -1,0 +1,382 @@
+"""GB300 (sm_103a) TT-EmbeddingBag: Python binding of libttemb.so.
+
+A drop-in EmbeddingBag whose E x D table is stored as three tensor-train cores
+(TT-Rec / FBTT-Embedding pages).  Every step of the computation runs in the
+CUDA kernels of ``libttemb.so``; this module only marshals arguments: torch
+supplies device memory and the current stream.  There is no CPU fallback:
+without the built library every call raises.
+
+Low-level functions carry the C ABI's names (``include/tt_emb.h``):
+``tt_emb_create``, ``tt_emb_batch_create``, ``tt_emb_forward``,
+``tt_emb_backward``, ``tt_emb_cache_populate`` ...  ``TTEmbeddingBag`` and
+``TableBatchedTTEmbeddingBag`` wrap them as ``torch.nn.Module`` s whose
+backward pass applies the fused SGD update to the cores and returns no
+gradient for them (FBTT README, "Fused Kernel", sparse=True).
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import threading
+from typing import List, Optional, Sequence
+
+import torch
+
+from ._nvcc_build import LIB as _LIB_PATH
+from ._nvcc_build import build
+
+__all__ = [
+    "TTError",
+    "build",
+    "load_library",
+    "library_path",
+    "tt_emb_create",
+    "tt_emb_batch_create",
+    "tt_emb_destroy",
+    "tt_emb_reserve",
+    "tt_emb_forward",
+    "tt_emb_backward",
+    "tt_emb_cache_populate",
+    "tt_emb_cache_disable",
+    "tt_emb_get_decoded",
+    "tt_emb_get_last_error",
+    "tt_emb_set_stage_timing",
+    "tt_emb_stage_times",
+    "tt_emb_last_launch_count",
+    "tt_emb_status_string",
+    "EXPORTED_SYMBOLS",
+    "TTEmbeddingBag",
+    "TableBatchedTTEmbeddingBag",
+]
+
+TT_OK, TT_ERR_ARG, TT_ERR_SHAPE, TT_ERR_INDEX, TT_ERR_CUDA, TT_ERR_STATE, TT_ERR_TIMEOUT, TT_ERR_NOMEM = range(8)
+TT_POOL_SUM, TT_POOL_MEAN = 0, 1
+
+EXPORTED_SYMBOLS = (
+    "tt_emb_create",
+    "tt_emb_batch_create",
+    "tt_emb_destroy",
+    "tt_emb_reserve",
+    "tt_emb_forward",
+    "tt_emb_backward",
+    "tt_emb_cache_populate",
+    "tt_emb_cache_disable",
+    "tt_emb_get_decoded",
+    "tt_emb_get_last_error",
+    "tt_emb_set_stage_timing",
+    "tt_emb_stage_times",
+    "tt_emb_last_launch_count",
+    "tt_emb_status_string",
+)
+
+
+class TTError(RuntimeError):
+    """A tt_status other than TT_OK."""
+
+    def __init__(self, code: int, what: str):
+        self.code = code
+        super().__init__(f"{what}: {tt_emb_status_string(code)} (tt_status {code})")
+
+
+class _Desc(ctypes.Structure):
+    _fields_ = [
+        ("num_embeddings", ctypes.c_int64),
+        ("p", ctypes.c_int64 * 3),
+        ("q", ctypes.c_int32 * 3),
+        ("ranks", ctypes.c_int32 * 2),
+        ("cores_dev", ctypes.c_void_p * 3),
+    ]
+
+
+_lib = None
+_lock = threading.Lock()
+
+
+def library_path() -> str:
+    return _LIB_PATH
+
+
+def load_library():
+    """Load libttemb.so (it must have been built with ``build()``)."""
+    global _lib
+    with _lock:
+        if _lib is not None:
+            return _lib
+        if not os.path.exists(_LIB_PATH):
+            raise RuntimeError(
+                f"{_LIB_PATH} is missing: build it with "
+                "tensor_train_compressed_embeddingbag_gb300.build() (nvcc, sm_103a)"
+            )
+        lib = ctypes.CDLL(_LIB_PATH)
+        vp, i64, i32, f32 = ctypes.c_void_p, ctypes.c_int64, ctypes.c_int32, ctypes.c_float
+        sig = {
+            "tt_emb_create": (ctypes.c_int, [i64, ctypes.POINTER(i64), ctypes.POINTER(i32), ctypes.POINTER(i32),
+                                             ctypes.POINTER(vp), ctypes.POINTER(vp)]),
+            "tt_emb_batch_create": (ctypes.c_int, [i32, ctypes.POINTER(_Desc), ctypes.POINTER(vp)]),
+            "tt_emb_destroy": (None, [vp]),
+            "tt_emb_reserve": (ctypes.c_int, [vp, i64, i64]),
+            "tt_emb_forward": (ctypes.c_int, [vp, vp, i64, vp, i64, vp, ctypes.c_int, vp, vp]),
+            "tt_emb_backward": (ctypes.c_int, [vp, vp, f32, vp]),
+            "tt_emb_cache_populate": (ctypes.c_int, [vp, vp, i64, vp]),
+            "tt_emb_cache_disable": (ctypes.c_int, [vp]),
+            "tt_emb_get_decoded": (ctypes.c_int, [vp, vp, vp, vp, vp, vp, vp]),
+            "tt_emb_get_last_error": (ctypes.c_int, [vp]),
+            "tt_emb_set_stage_timing": (ctypes.c_int, [vp, ctypes.c_int]),
+            "tt_emb_stage_times": (ctypes.c_int, [vp, ctypes.c_int, ctypes.POINTER(f32),
+                                                  ctypes.POINTER(ctypes.c_char_p), ctypes.c_int]),
+            "tt_emb_last_launch_count": (ctypes.c_int, [vp, ctypes.c_int]),
+            "tt_emb_status_string": (ctypes.c_char_p, [ctypes.c_int]),
+        }
+        for name, (res, args) in sig.items():
+            fn = getattr(lib, name)
+            fn.restype = res
+            fn.argtypes = args
+        _lib = lib
+        return lib
+
+
+def _check(st: int, what: str):
+    if st != TT_OK:
+        raise TTError(st, what)
+
+
+def _ptr(t: Optional[torch.Tensor]):
+    return None if t is None else ctypes.c_void_p(t.data_ptr())
+
+
+def _stream(stream) -> ctypes.c_void_p:
+    if stream is None:
+        stream = torch.cuda.current_stream()
+    return ctypes.c_void_p(stream.cuda_stream if hasattr(stream, "cuda_stream") else int(stream))
+
+
+def _cuda_f32(t: torch.Tensor, what: str):
+    if not (t.is_cuda and t.dtype == torch.float32 and t.is_contiguous()):
+        raise TTError(TT_ERR_ARG, f"{what} must be a contiguous float32 CUDA tensor")
+
+
+def tt_emb_status_string(code: int) -> str:
+    return load_library().tt_emb_status_string(int(code)).decode()
+
+
+def tt_emb_create(num_embeddings: int, p: Sequence[int], q: Sequence[int], ranks: Sequence[int],
+                  cores: Sequence[torch.Tensor]) -> ctypes.c_void_p:
+    lib = load_library()
+    for k, c in enumerate(cores):
+        _cuda_f32(c, f"core {k}")
+    h = ctypes.c_void_p()
+    ptrs = (ctypes.c_void_p * 3)(*[c.data_ptr() for c in cores])
+    st = lib.tt_emb_create(int(num_embeddings), (ctypes.c_int64 * 3)(*p), (ctypes.c_int32 * 3)(*q),
+                           (ctypes.c_int32 * 2)(*ranks), ptrs, ctypes.byref(h))
+    _check(st, "tt_emb_create")
+    return h
+
+
+def tt_emb_batch_create(tables) -> ctypes.c_void_p:
+    """tables: sequence of (num_embeddings, p, q, ranks, cores)."""
+    lib = load_library()
+    arr = (_Desc * len(tables))()
+    for i, (E, p, q, r, cores) in enumerate(tables):
+        for k, c in enumerate(cores):
+            _cuda_f32(c, f"table {i} core {k}")
+        arr[i].num_embeddings = int(E)
+        for k in range(3):
+            arr[i].p[k] = int(p[k])
+            arr[i].q[k] = int(q[k])
+            arr[i].cores_dev[k] = cores[k].data_ptr()
+        arr[i].ranks[0], arr[i].ranks[1] = int(r[0]), int(r[1])
+    h = ctypes.c_void_p()
+    _check(lib.tt_emb_batch_create(len(tables), arr, ctypes.byref(h)), "tt_emb_batch_create")
+    return h
+
+
+def tt_emb_destroy(h):
+    if h:
+        load_library().tt_emb_destroy(h)
+
+
+def tt_emb_reserve(h, max_nnz: int, max_bags: int):
+    _check(load_library().tt_emb_reserve(h, int(max_nnz), int(max_bags)), "tt_emb_reserve")
+
+
+def tt_emb_forward(h, indices: torch.Tensor, offsets: torch.Tensor, weights: Optional[torch.Tensor], mode: int,
+                   out: torch.Tensor, stream=None):
+    """indices int64 [nnz], offsets int64 [num_bags + 1] (CSR), out float32 [num_bags, D]."""
+    nb = offsets.numel() - 1
+    st = load_library().tt_emb_forward(h, _ptr(indices), indices.numel(), _ptr(offsets), nb, _ptr(weights),
+                                       int(mode), _ptr(out), _stream(stream))
+    _check(st, "tt_emb_forward")
+
+
+def tt_emb_backward(h, grad_out: torch.Tensor, lr: float, stream=None):
+    _check(load_library().tt_emb_backward(h, _ptr(grad_out), float(lr), _stream(stream)), "tt_emb_backward")
+
+
+def tt_emb_cache_populate(h, rows: torch.Tensor, stream=None):
+    _check(load_library().tt_emb_cache_populate(h, _ptr(rows), rows.numel(), _stream(stream)), "tt_emb_cache_populate")
+
+
+def tt_emb_cache_disable(h):
+    _check(load_library().tt_emb_cache_disable(h), "tt_emb_cache_disable")
+
+
+def tt_emb_get_decoded(h, nnz: int, device, stream=None):
+    """(table, i1, i2, i3, bag) int32 CUDA tensors of the last forward pass."""
+    outs = [torch.empty(nnz, dtype=torch.int32, device=device) for _ in range(5)]
+    _check(load_library().tt_emb_get_decoded(h, *[_ptr(o) for o in outs], _stream(stream)), "tt_emb_get_decoded")
+    return tuple(outs)
+
+
+def tt_emb_get_last_error(h) -> int:
+    return int(load_library().tt_emb_get_last_error(h))
+
+
+def tt_emb_set_stage_timing(h, enable: bool):
+    _check(load_library().tt_emb_set_stage_timing(h, 1 if enable else 0), "tt_emb_set_stage_timing")
+
+
+def tt_emb_stage_times(h, which: int, cap: int = 16):
+    """[(kernel name, ms), ...] of the last forward (0) or backward (1) call."""
+    ms = (ctypes.c_float * cap)()
+    names = (ctypes.c_char_p * cap)()
+    n = load_library().tt_emb_stage_times(h, int(which), ms, names, cap)
+    if n < 0:
+        raise TTError(TT_ERR_CUDA, "tt_emb_stage_times")
+    return [(names[i].decode() if names[i] else "?", float(ms[i])) for i in range(min(n, cap)) if names[i]]
+
+
+def tt_emb_last_launch_count(h, which: int) -> int:
+    return int(load_library().tt_emb_last_launch_count(h, int(which)))
+
+
+# ---------------------------------------------------------------- modules
+
+
+def _csr_offsets(offsets: torch.Tensor, nnz: int, include_last_offset: bool) -> torch.Tensor:
+    offsets = offsets.to(torch.int64).contiguous()
+    if include_last_offset:
+        return offsets
+    tail = torch.full((1,), nnz, dtype=torch.int64, device=offsets.device)
+    return torch.cat([offsets, tail])
+
+
+class _TTBagFunction(torch.autograd.Function):
+    @staticmethod
+    def forward(ctx, module, indices, offsets, weights, mode, *cores):
+        D = module.embedding_dim
+        out = torch.empty((offsets.numel() - 1, D), dtype=torch.float32, device=indices.device)
+        tt_emb_forward(module._h, indices, offsets, weights, mode, out)
+        ctx.module = module
+        return out
+
+    @staticmethod
+    def backward(ctx, grad_out):
+        m = ctx.module
+        tt_emb_backward(m._h, grad_out.contiguous(), m.learning_rate)
+        return (None,) * (5 + len(m._core_list()))
+
+
+class _TTBase(torch.nn.Module):
+    _h = None
+
+    def _core_list(self) -> List[torch.Tensor]:
+        raise NotImplementedError
+
+    def _run(self, indices, offsets, per_sample_weights, mode, include_last_offset):
+        if mode not in ("sum", "mean"):
+            raise ValueError("mode must be 'sum' or 'mean'")
+        indices = indices.to(torch.int64).contiguous()
+        offsets = _csr_offsets(offsets, indices.numel(), include_last_offset)
+        w = None if per_sample_weights is None else per_sample_weights.to(torch.float32).contiguous()
+        return _TTBagFunction.apply(self, indices, offsets, w, TT_POOL_MEAN if mode == "mean" else TT_POOL_SUM,
+                                    *self._core_list())
+
+    def last_error(self) -> int:
+        return tt_emb_get_last_error(self._h)
+
+    def __del__(self):
+        try:
+            if self._h:
+                tt_emb_destroy(self._h)
+                self._h = None
+        except Exception:
+            pass
+
+
+class TTEmbeddingBag(_TTBase):
+    """TT-compressed EmbeddingBag with fused SGD (FBTT README, "Parameters" and "Fused Kernel").
+
+    cores: optional initial cores ``[G1, G2, G3]`` with shapes
+    ``[p_k, r_{k-1}, q_k, r_k]``; default i.i.d. N(0, sigma).
+    """
+
+    def __init__(self, num_embeddings: int, embedding_dim: int, tt_ranks: Sequence[int],
+                 tt_p_shapes: Sequence[int], tt_q_shapes: Sequence[int], learning_rate: float = 0.1,
+                 cores: Optional[Sequence[torch.Tensor]] = None, sigma: float = 0.1, device=None,
+                 use_cache: bool = False, cache_rows: Optional[torch.Tensor] = None):
+        super().__init__()
+        device = torch.device(device or "cuda")
+        q = list(tt_q_shapes)
+        if q[0] * q[1] * q[2] != embedding_dim:
+            raise ValueError("prod(tt_q_shapes) must equal embedding_dim")
+        self.num_embeddings, self.embedding_dim = int(num_embeddings), int(embedding_dim)
+        self.p, self.q, self.ranks = list(tt_p_shapes), q, list(tt_ranks)
+        self.learning_rate = float(learning_rate)
+        r = [1, self.ranks[0], self.ranks[1], 1]
+        shapes = [(self.p[k], r[k], q[k], r[k + 1]) for k in range(3)]
+        if cores is None:
+            cores = [torch.randn(s, device=device) * sigma for s in shapes]
+        self.G1, self.G2, self.G3 = (
+            torch.nn.Parameter(c.to(device=device, dtype=torch.float32).contiguous().clone()) for c in cores
+        )
+        for k, c in enumerate(self._core_list()):
+            if tuple(c.shape) != shapes[k]:
+                raise ValueError(f"core {k} has shape {tuple(c.shape)}, expected {shapes[k]}")
+        self._h = tt_emb_create(self.num_embeddings, self.p, self.q, self.ranks, self._core_list())
+        if use_cache and cache_rows is not None:
+            self.cache_populate(cache_rows)
+
+    def _core_list(self):
+        return [self.G1, self.G2, self.G3]
+
+    def cache_populate(self, rows: torch.Tensor):
+        """Fill the hot-row cache with these rows (FBTT README, "Software Cache")."""
+        tt_emb_cache_populate(self._h, rows.to(torch.int64).contiguous())
+
+    def forward(self, input, offsets, per_sample_weights=None, mode: str = "sum", include_last_offset=False):
+        return self._run(input, offsets, per_sample_weights, mode, include_last_offset)
+
+
+class TableBatchedTTEmbeddingBag(_TTBase):
+    """Several TT tables in one call (FBTT README, "TableBatchedTTEmbeddingBag").
+
+    tables: sequence of dicts with num_embeddings, p, q, ranks and optional cores.
+    Bags are ordered table-major: offsets cover num_tables * B bags, bag
+    t * B + b is sample b of table t; the output is [num_tables * B, D].
+    """
+
+    def __init__(self, tables, learning_rate: float = 0.1, sigma: float = 0.1, device=None):
+        super().__init__()
+        device = torch.device(device or "cuda")
+        self.learning_rate = float(learning_rate)
+        self.specs = []
+        params = []
+        for i, t in enumerate(tables):
+            p, q, rk = list(t["p"]), list(t["q"]), list(t["ranks"])
+            r = [1, rk[0], rk[1], 1]
+            shapes = [(p[k], r[k], q[k], r[k + 1]) for k in range(3)]
+            cores = t.get("cores") or [torch.randn(s, device=device) * sigma for s in shapes]
+            cs = [torch.nn.Parameter(c.to(device=device, dtype=torch.float32).contiguous().clone()) for c in cores]
+            for k in range(3):
+                self.register_parameter(f"t{i}_G{k + 1}", cs[k])
+            params.append(cs)
+            self.specs.append((int(t["num_embeddings"]), p, q, rk))
+        self.embedding_dim = int(self.specs[0][2][0] * self.specs[0][2][1] * self.specs[0][2][2])
+        self._cores = params
+        self._h = tt_emb_batch_create([(E, p, q, r, params[i]) for i, (E, p, q, r) in enumerate(self.specs)])
+
+    def _core_list(self):
+        return [c for cs in self._cores for c in cs]
+
+    def forward(self, input, offsets, per_sample_weights=None, mode: str = "sum", include_last_offset=True):
+        return self._run(input, offsets, per_sample_weights, mode, include_last_offset)

@@ -1,0 +1,549 @@
+// tt_api.cu -- the C ABI of libttemb.so (declarations and contracts in include/tt_emb.h).
+//
+// Host side only: argument validation, the handle's device tables, the
+// workspace, and the order of the kernel launches of one forward or backward
+// call.  Every step of the computation runs in the kernels of tt_sort.cu and
+// tt_compute.cu.
+#include <algorithm>
+#include <cstdio>
+#include <cstring>
+#include <new>
+#include <vector>
+
+#include "../../include/tt_emb.h"
+#include "tt_internal.cuh"
+
+using namespace ttemb;
+
+namespace {
+
+constexpr int kMaxStages = 16;
+
+struct Arena {
+    char* base = nullptr;
+    size_t used = 0;
+    size_t cap = 0;
+    template <class T>
+    T* take(size_t count) {
+        size_t off = (used + 255) & ~(size_t)255;
+        used = off + sizeof(T) * count;
+        return base ? reinterpret_cast<T*>(base + off) : nullptr;
+    }
+};
+
+}  // namespace
+
+struct tt_emb {
+    int device = 0;
+    int ntab = 0;
+    std::vector<TableDev> tabs;  // host copy
+    TableDev* d_tables = nullptr;
+    int* d_bins = nullptr;       // bin -> table for the three digits
+    int* d_fixed = nullptr;      // err, counters[2], ntiles, grp_done[n2]
+    float* d_tbuf = nullptr;
+    int64_t tbuf_floats = 0;
+    Params P{};                  // constants + workspace pointers
+    // workspace
+    void* d_ws = nullptr;
+    size_t ws_bytes = 0;
+    int64_t cap_nnz = -1, cap_bags = -1;
+    // forward state
+    bool has_fwd = false;
+    cudaStream_t last_stream = nullptr;
+    // stage timing
+    bool timing = false;
+    cudaEvent_t ev[2][kMaxStages + 1] = {};
+    const char* names[2][kMaxStages] = {};
+    int nstage[2] = {0, 0};
+    int launches[2] = {0, 0};
+    // cache
+    int64_t* d_cache_rows = nullptr;
+    float* d_cache_vals = nullptr;
+    int* d_cache_stamp = nullptr;
+    int* d_slice_stamp = nullptr;
+    int64_t cache_n = 0;
+    int step = 0;
+};
+
+namespace {
+
+tt_status cuda_status(cudaError_t e) { return e == cudaSuccess ? TT_OK : TT_ERR_CUDA; }
+
+// Workspace carve-up for up to `nnz` lookups; base == nullptr only measures.
+size_t carve(tt_emb* h, void* base, int64_t nnz, bool assign) {
+    Arena A;
+    A.base = static_cast<char*>(base);
+    Params& P = h->P;
+    const int64_t N = std::max<int64_t>(nnz, 1);
+    const int nch = (int)((N + kChunk - 1) / kChunk);
+    const int max_tiles = (int)((N + P.tile_cap - 1) / P.tile_cap) + P.n2;
+    int* lk_i1 = A.take<int>(N);
+    int* lk_i2 = A.take<int>(N);
+    int* lk_i3 = A.take<int>(N);
+    int* lk_bag = A.take<int>(N);
+    float* lk_s = A.take<float>(N);
+    int* H1 = A.take<int>((size_t)P.n1 * nch);
+    int* H3 = A.take<int>((size_t)P.n3 * nch);
+    int* H2 = A.take<int>((size_t)P.n2 * nch);
+    int* pi1 = A.take<int>(N);
+    int* pi3 = A.take<int>(N);
+    int* pi21 = A.take<int>(N);
+    int* sigma = A.take<int>(N);
+    int4* tiles = A.take<int4>(max_tiles);
+    int* grp_first = A.take<int>(P.n2);
+    int* grp_ntiles = A.take<int>(P.n2);
+    int* rep_pair = A.take<int>(N);
+    int* rep_row = A.take<int>(N);
+    float* Qbuf = A.take<float>((size_t)N * P.qs_max);
+    float* Pbuf = A.take<float>((size_t)N * P.ps_max);
+    float* dG2part = A.take<float>((size_t)max_tiles * P.s2_max);
+    if (assign) {
+        P.lk_i1 = lk_i1; P.lk_i2 = lk_i2; P.lk_i3 = lk_i3; P.lk_bag = lk_bag; P.lk_s = lk_s;
+        P.H1 = H1; P.H3 = H3; P.H2 = H2;
+        P.pi1 = pi1; P.pi3 = pi3; P.pi21 = pi21; P.sigma = sigma;
+        P.tiles = tiles; P.grp_first = grp_first; P.grp_ntiles = grp_ntiles;
+        P.rep_pair = rep_pair; P.rep_row = rep_row;
+        P.Qbuf = Qbuf; P.Pbuf = Pbuf; P.dG2part = dG2part;
+    }
+    return A.used + 256;
+}
+
+tt_status ensure_workspace(tt_emb* h, int64_t nnz, int64_t nbags) {
+    if (nnz <= h->cap_nnz && nbags <= h->cap_bags && h->d_ws) {
+        carve(h, h->d_ws, h->cap_nnz, true);
+        return TT_OK;
+    }
+    const int64_t cap = std::max<int64_t>({nnz, h->cap_nnz, 1});
+    const size_t bytes = carve(h, nullptr, cap, false);
+    if (h->d_ws) {
+        cudaError_t e = cudaDeviceSynchronize();
+        if (e != cudaSuccess) return TT_ERR_CUDA;
+        cudaFree(h->d_ws);
+        h->d_ws = nullptr;
+    }
+    if (cudaMalloc(&h->d_ws, bytes) != cudaSuccess) {
+        cudaGetLastError();
+        h->d_ws = nullptr;
+        h->cap_nnz = h->cap_bags = -1;
+        return TT_ERR_NOMEM;
+    }
+    h->ws_bytes = bytes;
+    h->cap_nnz = cap;
+    h->cap_bags = std::max<int64_t>(nbags, h->cap_bags);
+    carve(h, h->d_ws, cap, true);
+    return TT_OK;
+}
+
+tt_status validate_table(int64_t E, const int64_t p[3], const int32_t q[3], const int32_t r[2]) {
+    if (E <= 0) return TT_ERR_SHAPE;
+    double prod = 1.0;
+    for (int k = 0; k < 3; ++k) {
+        if (p[k] <= 0 || p[k] > TT_MAX_P) return TT_ERR_SHAPE;
+        if (q[k] <= 0 || q[k] > TT_MAX_Q) return TT_ERR_SHAPE;
+        prod *= (double)p[k];
+    }
+    if (prod < (double)E) return TT_ERR_SHAPE;
+    if (p[0] * p[1] * p[2] < E) return TT_ERR_SHAPE;
+    for (int k = 0; k < 2; ++k)
+        if (r[k] <= 0 || r[k] > TT_MAX_RANK) return TT_ERR_SHAPE;
+    const int64_t D = (int64_t)q[0] * q[1] * q[2];
+    if (D > TT_MAX_D) return TT_ERR_SHAPE;
+    // per-thread accumulator limits of the tile and reduce kernels
+    if ((int64_t)r[0] * q[1] * r[1] > 64 * kTileThreads) return TT_ERR_SHAPE;
+    if ((int64_t)q[0] * r[0] > 32 * kTileThreads || (int64_t)r[1] * q[2] > 32 * kTileThreads) return TT_ERR_SHAPE;
+    if ((int64_t)q[0] * q[1] * r[1] > 8192) return TT_ERR_SHAPE;  // one partial product T
+    if ((int64_t)p[0] * p[1] > (int64_t)1 << 30) return TT_ERR_SHAPE;
+    return TT_OK;
+}
+
+tt_status build_handle(tt_emb* h, int ntab, const tt_table_desc* d) {
+    // every host-side check comes before the first CUDA call
+    for (int t = 0; t < ntab; ++t) {
+        tt_status st = validate_table(d[t].num_embeddings, d[t].p, d[t].q, d[t].ranks);
+        if (st != TT_OK) return st;
+        if (d[t].q[0] * d[t].q[1] * d[t].q[2] != d[0].q[0] * d[0].q[1] * d[0].q[2]) return TT_ERR_SHAPE;
+        for (int k = 0; k < 3; ++k)
+            if (!d[t].cores_dev[k]) return TT_ERR_ARG;
+    }
+    {
+        int64_t s1 = 0, s2 = 0, s3 = 0;
+        for (int t = 0; t < ntab; ++t) { s1 += d[t].p[0]; s2 += d[t].p[1]; s3 += d[t].p[2]; }
+        if (s1 > kMaxBinsPerDigit || s2 > kMaxBinsPerDigit || s3 > kMaxBinsPerDigit) return TT_ERR_SHAPE;
+    }
+    if (cudaGetDevice(&h->device) != cudaSuccess) return TT_ERR_CUDA;
+    h->ntab = ntab;
+    const int D = d[0].q[0] * d[0].q[1] * d[0].q[2];
+    int n1 = 0, n2 = 0, n3 = 0, qs = 1, ps = 1, s2 = 1, r1m = 1, Nm = 1, q1Nm = 1;
+    int64_t tb = 0;
+    for (int t = 0; t < ntab; ++t) {
+        TableDev T{};
+        T.E = d[t].num_embeddings;
+        T.p1 = (int)d[t].p[0]; T.p2 = (int)d[t].p[1]; T.p3 = (int)d[t].p[2];
+        T.q1 = d[t].q[0]; T.q2 = d[t].q[1]; T.q3 = d[t].q[2];
+        T.r1 = d[t].ranks[0]; T.r2 = d[t].ranks[1];
+        T.D = D;
+        T.G1 = d[t].cores_dev[0]; T.G2 = d[t].cores_dev[1]; T.G3 = d[t].cores_dev[2];
+        T.tbase = tb;
+        tb += (int64_t)T.p1 * T.p2 * T.q1 * T.q2 * T.r2;
+        T.base1 = n1; T.base2 = n2; T.base3 = n3;
+        n1 += T.p1; n2 += T.p2; n3 += T.p3;
+        qs = std::max(qs, T.q1 * T.r1);
+        ps = std::max(ps, T.r2 * T.q3);
+        s2 = std::max(s2, T.r1 * T.q2 * T.r2);
+        r1m = std::max(r1m, T.r1);
+        Nm = std::max(Nm, T.q2 * T.r2);
+        q1Nm = std::max(q1Nm, T.q1 * T.q2 * T.r2);
+        h->tabs.push_back(T);
+    }
+    if (n1 > kMaxBinsPerDigit || n2 > kMaxBinsPerDigit || n3 > kMaxBinsPerDigit) return TT_ERR_SHAPE;
+    Params& P = h->P;
+    P.ntab = ntab;
+    P.n1 = n1; P.n2 = n2; P.n3 = n3;
+    P.D = D;
+    P.qs_max = qs; P.ps_max = ps; P.s2_max = s2;
+    P.r1_max = r1m; P.N_max = Nm; P.q1N_max = q1Nm;
+    // tile size: the summed upstream gradient of a tile (tile_cap x D floats) stays <= 64 KB
+    {
+        const int lim = std::min(kTileThreads, 16384 / D);
+        int cap = 1;
+        while (cap * 2 <= lim) cap *= 2;
+        P.tile_cap = cap;
+    }
+    // device tables
+    std::vector<int> bins(n1 + n2 + n3);
+    for (int t = 0; t < ntab; ++t) {
+        const TableDev& T = h->tabs[t];
+        for (int i = 0; i < T.p1; ++i) bins[T.base1 + i] = t;
+        for (int i = 0; i < T.p2; ++i) bins[n1 + T.base2 + i] = t;
+        for (int i = 0; i < T.p3; ++i) bins[n1 + n2 + T.base3 + i] = t;
+    }
+    if (cudaMalloc(&h->d_tables, sizeof(TableDev) * ntab) != cudaSuccess) return TT_ERR_NOMEM;
+    if (cudaMalloc(&h->d_bins, sizeof(int) * bins.size()) != cudaSuccess) return TT_ERR_NOMEM;
+    const int nfixed = 8 + n2;
+    if (cudaMalloc(&h->d_fixed, sizeof(int) * nfixed) != cudaSuccess) return TT_ERR_NOMEM;
+    if (cudaMalloc(&h->d_tbuf, sizeof(float) * std::max<int64_t>(tb, 1)) != cudaSuccess) return TT_ERR_NOMEM;
+    h->tbuf_floats = tb;
+    if (cudaMemcpy(h->d_tables, h->tabs.data(), sizeof(TableDev) * ntab, cudaMemcpyHostToDevice) != cudaSuccess ||
+        cudaMemcpy(h->d_bins, bins.data(), sizeof(int) * bins.size(), cudaMemcpyHostToDevice) != cudaSuccess ||
+        cudaMemset(h->d_fixed, 0, sizeof(int) * nfixed) != cudaSuccess)
+        return TT_ERR_CUDA;
+    P.tables = h->d_tables;
+    P.bin1_tab = h->d_bins;
+    P.bin2_tab = h->d_bins + n1;
+    P.bin3_tab = h->d_bins + n1 + n2;
+    P.err = h->d_fixed;
+    P.counters = h->d_fixed + 1;
+    P.ntiles = h->d_fixed + 3;
+    P.grp_done = h->d_fixed + 8;
+    P.Tbuf = h->d_tbuf;
+    return TT_OK;
+}
+
+void free_handle(tt_emb* h) {
+    if (!h) return;
+    cudaFree(h->d_tables);
+    cudaFree(h->d_bins);
+    cudaFree(h->d_fixed);
+    cudaFree(h->d_tbuf);
+    cudaFree(h->d_ws);
+    cudaFree(h->d_cache_rows);
+    cudaFree(h->d_cache_vals);
+    cudaFree(h->d_cache_stamp);
+    cudaFree(h->d_slice_stamp);
+    for (int w = 0; w < 2; ++w)
+        for (int i = 0; i <= kMaxStages; ++i)
+            if (h->ev[w][i]) cudaEventDestroy(h->ev[w][i]);
+    delete h;
+}
+
+// Launch sequence helper: records stage events when timing is on.
+struct Seq {
+    tt_emb* h;
+    int which;
+    cudaStream_t s;
+    int n = 0;
+    tt_status st = TT_OK;
+    Seq(tt_emb* hh, int w, cudaStream_t ss) : h(hh), which(w), s(ss) {
+        if (h->timing) {
+            if (!h->ev[w][0] && cudaEventCreate(&h->ev[w][0]) != cudaSuccess) st = TT_ERR_CUDA;
+            else if (cudaEventRecord(h->ev[w][0], s) != cudaSuccess) st = TT_ERR_CUDA;
+        }
+    }
+    void run(const char* name, cudaError_t (*fn)(const Params&, cudaStream_t)) {
+        if (st != TT_OK) return;
+        cudaError_t e = fn(h->P, s);
+        if (e != cudaSuccess) { st = TT_ERR_CUDA; return; }
+        if (h->timing && n < kMaxStages) {
+            cudaEvent_t& ev = h->ev[which][n + 1];
+            if (!ev && cudaEventCreate(&ev) != cudaSuccess) { st = TT_ERR_CUDA; return; }
+            if (cudaEventRecord(ev, s) != cudaSuccess) { st = TT_ERR_CUDA; return; }
+            h->names[which][n] = name;
+        }
+        ++n;
+    }
+    tt_status finish() {
+        h->launches[which] = n;
+        h->nstage[which] = h->timing ? std::min(n, kMaxStages) : 0;
+        return st;
+    }
+};
+
+}  // namespace
+
+extern "C" {
+
+const char* tt_emb_status_string(tt_status s) {
+    switch (s) {
+        case TT_OK: return "ok";
+        case TT_ERR_ARG: return "invalid argument";
+        case TT_ERR_SHAPE: return "invalid or unsupported TT shape";
+        case TT_ERR_INDEX: return "index outside [0, num_embeddings)";
+        case TT_ERR_CUDA: return "CUDA runtime error";
+        case TT_ERR_STATE: return "call out of order";
+        case TT_ERR_TIMEOUT: return "bounded device wait gave up";
+        case TT_ERR_NOMEM: return "device memory allocation failed";
+    }
+    return "unknown status";
+}
+
+tt_status tt_emb_create(int64_t num_embeddings, const int64_t p[3], const int32_t q[3], const int32_t ranks[2],
+                        float* const cores_dev[3], tt_emb** out) {
+    if (!out || !p || !q || !ranks || !cores_dev) return TT_ERR_ARG;
+    *out = nullptr;
+    tt_table_desc d{};
+    d.num_embeddings = num_embeddings;
+    for (int k = 0; k < 3; ++k) {
+        d.p[k] = p[k];
+        d.q[k] = q[k];
+        d.cores_dev[k] = cores_dev[k];
+    }
+    d.ranks[0] = ranks[0];
+    d.ranks[1] = ranks[1];
+    return tt_emb_batch_create(1, &d, out);
+}
+
+tt_status tt_emb_batch_create(int32_t num_tables, const tt_table_desc* descs, tt_emb** out) {
+    if (!out || !descs || num_tables <= 0) return TT_ERR_ARG;
+    *out = nullptr;
+    tt_emb* h = new (std::nothrow) tt_emb();
+    if (!h) return TT_ERR_NOMEM;
+    tt_status st = build_handle(h, num_tables, descs);
+    if (st != TT_OK) {
+        free_handle(h);
+        return st;
+    }
+    *out = h;
+    return TT_OK;
+}
+
+void tt_emb_destroy(tt_emb* h) {
+    if (!h) return;
+    cudaDeviceSynchronize();
+    free_handle(h);
+}
+
+tt_status tt_emb_reserve(tt_emb* h, int64_t max_nnz, int64_t max_bags) {
+    if (!h || max_nnz < 0 || max_bags < 0) return TT_ERR_ARG;
+    return ensure_workspace(h, max_nnz, max_bags);
+}
+
+tt_status tt_emb_forward(tt_emb* h, const int64_t* indices, int64_t nnz, const int64_t* offsets, int64_t num_bags,
+                         const float* weights, tt_pool mode, float* out, tt_stream stream) {
+    if (!h || nnz < 0 || num_bags < 0) return TT_ERR_ARG;
+    if (mode != TT_POOL_SUM && mode != TT_POOL_MEAN) return TT_ERR_ARG;
+    if (num_bags % h->ntab) return TT_ERR_ARG;
+    if (nnz > 0 && (!indices || !offsets)) return TT_ERR_ARG;
+    if (num_bags > 0 && (!offsets || !out)) return TT_ERR_ARG;
+    if (num_bags == 0 && nnz > 0) return TT_ERR_ARG;
+    if (nnz >= ((int64_t)1 << 31) - kChunk) return TT_ERR_ARG;
+    cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+    tt_status st = ensure_workspace(h, nnz, num_bags);
+    if (st != TT_OK) return st;
+    Params& P = h->P;
+    P.idx = indices;
+    P.off = offsets;
+    P.w = weights;
+    P.mean = mode == TT_POOL_MEAN;
+    P.nnz = nnz;
+    P.nbags = num_bags;
+    P.bags_per_table = num_bags / h->ntab;
+    P.out = out;
+    P.nch = (int)((std::max<int64_t>(nnz, 1) + kChunk - 1) / kChunk);
+    P.max_tiles = (int)((std::max<int64_t>(nnz, 1) + P.tile_cap - 1) / P.tile_cap) + P.n2;
+    P.cache_rows = h->d_cache_rows;
+    P.cache_n = h->cache_n;
+    P.cache_vals = h->d_cache_vals;
+    P.cache_stamp = h->d_cache_stamp;
+    P.slice_stamp = h->d_slice_stamp;
+    P.step = h->step;
+    h->last_stream = s;
+    h->has_fwd = false;
+    if (num_bags == 0) {
+        h->launches[0] = 0;
+        h->nstage[0] = 0;
+        h->has_fwd = true;
+        return TT_OK;
+    }
+    Seq q(h, 0, s);
+    if (nnz == 0) {
+        if (cudaMemsetAsync(out, 0, sizeof(float) * (size_t)num_bags * P.D, s) != cudaSuccess) return TT_ERR_CUDA;
+    } else {
+        q.run("decode_hist", launch_decode_hist);
+        q.run("scan13", launch_scan13);
+        q.run("scatter13", launch_scatter13);
+        q.run("scan2_tiles", launch_scan2_tiles);
+        q.run("scatter2", launch_scatter2);
+        q.run("tile_fwd", launch_tile_fwd);
+        q.run("pool", launch_pool);
+    }
+    st = q.finish();
+    if (st == TT_OK) h->has_fwd = true;
+    return st;
+}
+
+tt_status tt_emb_backward(tt_emb* h, const float* grad_out, float lr, tt_stream stream) {
+    if (!h) return TT_ERR_ARG;
+    if (!h->has_fwd) return TT_ERR_STATE;
+    Params& P = h->P;
+    if (P.nbags > 0 && !grad_out) return TT_ERR_ARG;
+    cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+    h->has_fwd = false;
+    h->last_stream = s;
+    P.grad_out = grad_out;
+    P.lr = lr;
+    P.step = h->step;
+    P.slice_stamp = h->d_slice_stamp;
+    Seq q(h, 1, s);
+    if (P.nnz > 0) {
+        q.run("tile_bwd", launch_tile_bwd);
+        q.run("reduce13", launch_reduce13);
+    }
+    tt_status st = q.finish();
+    if (h->cache_n > 0) ++h->step;
+    return st;
+}
+
+tt_status tt_emb_cache_populate(tt_emb* h, const int64_t* rows_dev, int64_t n, tt_stream stream) {
+    if (!h || n < 0 || (n > 0 && !rows_dev)) return TT_ERR_ARG;
+    if (h->ntab != 1) return TT_ERR_STATE;
+    cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+    tt_emb_cache_disable(h);
+    if (n == 0) return TT_OK;
+    // rows are sorted on the host once so that lookups can binary-search them
+    std::vector<int64_t> rows(n);
+    if (cudaMemcpyAsync(rows.data(), rows_dev, sizeof(int64_t) * n, cudaMemcpyDeviceToHost, s) != cudaSuccess ||
+        cudaStreamSynchronize(s) != cudaSuccess)
+        return TT_ERR_CUDA;
+    std::sort(rows.begin(), rows.end());
+    const TableDev& T = h->tabs[0];
+    for (int64_t i = 0; i < n; ++i)
+        if (rows[i] < 0 || rows[i] >= T.E || (i > 0 && rows[i] == rows[i - 1])) return TT_ERR_ARG;
+    const int nslice = T.p1 + T.p2 + T.p3;
+    if (cudaMalloc(&h->d_cache_rows, sizeof(int64_t) * n) != cudaSuccess ||
+        cudaMalloc(&h->d_cache_vals, sizeof(float) * (size_t)n * T.D) != cudaSuccess ||
+        cudaMalloc(&h->d_cache_stamp, sizeof(int) * n) != cudaSuccess ||
+        cudaMalloc(&h->d_slice_stamp, sizeof(int) * nslice) != cudaSuccess) {
+        cudaGetLastError();
+        tt_emb_cache_disable(h);
+        return TT_ERR_NOMEM;
+    }
+    if (cudaMemcpyAsync(h->d_cache_rows, rows.data(), sizeof(int64_t) * n, cudaMemcpyHostToDevice, s) != cudaSuccess ||
+        cudaMemsetAsync(h->d_slice_stamp, 0, sizeof(int) * nslice, s) != cudaSuccess)
+        return TT_ERR_CUDA;
+    h->cache_n = n;
+    Params P = h->P;
+    P.cache_rows = h->d_cache_rows;
+    P.cache_n = n;
+    P.cache_vals = h->d_cache_vals;
+    P.cache_stamp = h->d_cache_stamp;
+    P.step = h->step;
+    if (launch_cache_fill(P, s) != cudaSuccess) return TT_ERR_CUDA;
+    // the host vector must outlive the copy
+    if (cudaStreamSynchronize(s) != cudaSuccess) return TT_ERR_CUDA;
+    return TT_OK;
+}
+
+tt_status tt_emb_cache_disable(tt_emb* h) {
+    if (!h) return TT_ERR_ARG;
+    if (h->cache_n > 0 || h->d_cache_rows) cudaDeviceSynchronize();
+    cudaFree(h->d_cache_rows);
+    cudaFree(h->d_cache_vals);
+    cudaFree(h->d_cache_stamp);
+    cudaFree(h->d_slice_stamp);
+    h->d_cache_rows = nullptr;
+    h->d_cache_vals = nullptr;
+    h->d_cache_stamp = nullptr;
+    h->d_slice_stamp = nullptr;
+    h->cache_n = 0;
+    h->P.cache_n = 0;
+    h->P.slice_stamp = nullptr;
+    return TT_OK;
+}
+
+tt_status tt_emb_get_decoded(tt_emb* h, int32_t* table_dev, int32_t* i1_dev, int32_t* i2_dev, int32_t* i3_dev,
+                             int32_t* bag_dev, tt_stream stream) {
+    if (!h) return TT_ERR_ARG;
+    if (!h->has_fwd) return TT_ERR_STATE;
+    const Params& P = h->P;
+    if (P.nnz == 0) return TT_OK;
+    cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+    const size_t bytes = sizeof(int) * (size_t)P.nnz;
+    cudaError_t e = cudaSuccess;
+    if (i1_dev && e == cudaSuccess) e = cudaMemcpyAsync(i1_dev, P.lk_i1, bytes, cudaMemcpyDeviceToDevice, s);
+    if (i2_dev && e == cudaSuccess) e = cudaMemcpyAsync(i2_dev, P.lk_i2, bytes, cudaMemcpyDeviceToDevice, s);
+    if (i3_dev && e == cudaSuccess) e = cudaMemcpyAsync(i3_dev, P.lk_i3, bytes, cudaMemcpyDeviceToDevice, s);
+    if (bag_dev && e == cudaSuccess) e = cudaMemcpyAsync(bag_dev, P.lk_bag, bytes, cudaMemcpyDeviceToDevice, s);
+    if (table_dev && e == cudaSuccess) {
+        // table = bag / bags_per_table; derived on the host side of the copy for 1 table
+        if (h->ntab == 1) {
+            e = cudaMemsetAsync(table_dev, 0, bytes, s);
+        } else {
+            std::vector<int32_t> bag(P.nnz);
+            e = cudaMemcpyAsync(bag.data(), P.lk_bag, bytes, cudaMemcpyDeviceToHost, s);
+            if (e == cudaSuccess) e = cudaStreamSynchronize(s);
+            for (int64_t n = 0; n < P.nnz && e == cudaSuccess; ++n) bag[n] = (int32_t)(bag[n] / P.bags_per_table);
+            if (e == cudaSuccess) e = cudaMemcpyAsync(table_dev, bag.data(), bytes, cudaMemcpyHostToDevice, s);
+            if (e == cudaSuccess) e = cudaStreamSynchronize(s);
+        }
+    }
+    return cuda_status(e);
+}
+
+tt_status tt_emb_get_last_error(tt_emb* h) {
+    if (!h) return TT_ERR_ARG;
+    if (cudaStreamSynchronize(h->last_stream) != cudaSuccess) return TT_ERR_CUDA;
+    int err = 0;
+    if (cudaMemcpy(&err, h->P.err, sizeof(int), cudaMemcpyDeviceToHost) != cudaSuccess) return TT_ERR_CUDA;
+    if (err && cudaMemset(h->P.err, 0, sizeof(int)) != cudaSuccess) return TT_ERR_CUDA;
+    if (err & kErrIndex) return TT_ERR_INDEX;
+    if (err & kErrOffsets) return TT_ERR_ARG;
+    if (err & kErrTimeout) return TT_ERR_TIMEOUT;
+    return TT_OK;
+}
+
+tt_status tt_emb_set_stage_timing(tt_emb* h, int enable) {
+    if (!h) return TT_ERR_ARG;
+    h->timing = enable != 0;
+    return TT_OK;
+}
+
+int tt_emb_stage_times(tt_emb* h, int which, float* ms, const char** names, int cap) {
+    if (!h || which < 0 || which > 1 || cap < 0) return -1;
+    const int n = h->nstage[which];
+    if (n == 0) return h->launches[which];
+    if (cudaEventSynchronize(h->ev[which][n]) != cudaSuccess) return -1;
+    for (int i = 0; i < n && i < cap; ++i) {
+        float t = 0.f;
+        if (cudaEventElapsedTime(&t, h->ev[which][i], h->ev[which][i + 1]) != cudaSuccess) return -1;
+        if (ms) ms[i] = t;
+        if (names) names[i] = h->names[which][i];
+    }
+    return h->launches[which];
+}
+
+int tt_emb_last_launch_count(tt_emb* h, int which) {
+    if (!h || which < 0 || which > 1) return -1;
+    return h->launches[which];
+}
+
+}  // extern "C"
