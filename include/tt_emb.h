@@ -179,6 +179,35 @@ int tt_emb_stage_times(tt_emb* h, int which /* 0 forward, 1 backward */, float* 
 /* Kernels launched by the most recent forward (which = 0) or backward (1). */
 int tt_emb_last_launch_count(tt_emb* h, int which);
 
+/*
+ * Forward pass that allocates no device memory.  The pages have no
+ * counterpart: this entry point exists for callers that cannot call
+ * cudaMalloc -- code running under a memory manager that owns all device
+ * memory (a framework's caching allocator, a serving runtime with a fixed
+ * budget), and code that must not synchronize the device or that runs while a
+ * stream is captured into a CUDA graph.
+ *
+ * It computes what tt_emb_forward() computes for one table, without a handle:
+ * the arguments mean what they mean for tt_emb_create() and tt_emb_forward()
+ * (cores_dev are only read), and the caller owns every buffer.  err_dev, if
+ * not NULL, is a caller-owned device int32 into which the kernel ORs 1 for an
+ * index outside [0, E) (that lookup contributes nothing) and 2 for malformed
+ * offsets; the caller clears it.  The only scratch is a static device array of
+ * TT_NOALLOC_SCRATCH_BYTES that every GPU loading the library holds until the
+ * process exits; one partial product of q1 q2 r2 floats per warp must fit in
+ * it (TT_ERR_SHAPE otherwise).  Calls share that array, so calls whose work
+ * overlaps on the GPU (unordered streams) race and give wrong results.  The
+ * first call on a device looks up the array's device address (a CUDA runtime
+ * call); make that first call before any stream capture.  Calls no cudaMalloc,
+ * cudaFree or allocating library routine.  Asynchronous on `stream`.
+ */
+#define TT_NOALLOC_SCRATCH_BYTES (8 * 1024 * 1024)
+tt_status tt_emb_forward_noalloc(int64_t num_embeddings, const int64_t p[3], const int32_t q[3],
+                                 const int32_t ranks[2], const float* const cores_dev[3],
+                                 const int64_t* indices_dev, int64_t nnz, const int64_t* offsets_dev,
+                                 int64_t num_bags, const float* per_sample_weights_dev, tt_pool mode,
+                                 float* out_dev, int32_t* err_dev, tt_stream stream);
+
 /* Static description of a status code; never NULL. */
 const char* tt_emb_status_string(tt_status s);
 

@@ -44,6 +44,7 @@ __all__ = [
     "tt_emb_stage_times",
     "tt_emb_last_launch_count",
     "tt_emb_status_string",
+    "tt_emb_forward_noalloc",
     "EXPORTED_SYMBOLS",
     "TTEmbeddingBag",
     "TableBatchedTTEmbeddingBag",
@@ -67,6 +68,7 @@ EXPORTED_SYMBOLS = (
     "tt_emb_stage_times",
     "tt_emb_last_launch_count",
     "tt_emb_status_string",
+    "tt_emb_forward_noalloc",
 )
 
 
@@ -126,6 +128,9 @@ def load_library():
                                                   ctypes.POINTER(ctypes.c_char_p), ctypes.c_int]),
             "tt_emb_last_launch_count": (ctypes.c_int, [vp, ctypes.c_int]),
             "tt_emb_status_string": (ctypes.c_char_p, [ctypes.c_int]),
+            "tt_emb_forward_noalloc": (ctypes.c_int, [i64, ctypes.POINTER(i64), ctypes.POINTER(i32),
+                                                      ctypes.POINTER(i32), ctypes.POINTER(vp), vp, i64, vp, i64,
+                                                      vp, ctypes.c_int, vp, vp, vp]),
         }
         for name, (res, args) in sig.items():
             fn = getattr(lib, name)
@@ -247,6 +252,23 @@ def tt_emb_stage_times(h, which: int, cap: int = 16):
 
 def tt_emb_last_launch_count(h, which: int) -> int:
     return int(load_library().tt_emb_last_launch_count(h, int(which)))
+
+
+def tt_emb_forward_noalloc(num_embeddings: int, p: Sequence[int], q: Sequence[int], ranks: Sequence[int],
+                           cores: Sequence[torch.Tensor], indices: torch.Tensor, offsets: torch.Tensor,
+                           weights: Optional[torch.Tensor], mode: int, out: torch.Tensor,
+                           err: Optional[torch.Tensor] = None, stream=None):
+    """Forward pass without a handle that allocates no device memory (see include/tt_emb.h).
+
+    For callers that cannot allocate device memory: every buffer, including
+    ``out`` and the optional int32 error word ``err``, is the caller's.
+    """
+    ptrs = (ctypes.c_void_p * 3)(*[c.data_ptr() for c in cores])
+    st = load_library().tt_emb_forward_noalloc(
+        int(num_embeddings), (ctypes.c_int64 * 3)(*p), (ctypes.c_int32 * 3)(*q), (ctypes.c_int32 * 2)(*ranks),
+        ptrs, _ptr(indices), indices.numel(), _ptr(offsets), offsets.numel() - 1, _ptr(weights), int(mode),
+        _ptr(out), _ptr(err), _stream(stream))
+    _check(st, "tt_emb_forward_noalloc")
 
 
 # ---------------------------------------------------------------- modules
