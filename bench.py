@@ -273,11 +273,29 @@ def run_gpu(args):
         raise RuntimeError(f"device error during warm-up: {tt.tt_emb_status_string(err)}")
     launches_per_step = tt.tt_emb_last_launch_count(h, 0) + tt.tt_emb_last_launch_count(h, 1)
 
+    # the step as a CUDA graph: forward + backward captured once, replayed per step
+    def capture(timing):
+        tt.tt_emb_set_stage_timing(h, timing)
+        step()  # creates the stage events outside the capture
+        torch.cuda.synchronize(dev)
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g):
+            cs = torch.cuda.current_stream(dev)
+            tt.tt_emb_forward(h, idx, off, None, tt.TT_POOL_SUM, out, cs)
+            tt.tt_emb_backward(h, go, lr, cs)
+        tt.tt_emb_set_stage_timing(h, False)
+        return g
+
+    graph = capture(False) if not args.eager else None
+    run_step = graph.replay if graph is not None else step
+    for _ in range(max(3, args.warmup)):
+        run_step()
+
     vis = [v for v in os.environ.get("CUDA_VISIBLE_DEVICES", "").split(",") if v.strip()]
     sampler = ClockSampler(vis[local] if local < len(vis) else str(local))
     sampler.start()
     time.sleep(0.2)
-    ms_total = timed(step, args.steps)
+    ms_total = timed(run_step, args.steps)
     clocks = sampler.stop()
     t = torch.tensor([ms_total], dtype=torch.float64, device=dev)
     if ws > 1:
@@ -286,22 +304,31 @@ def run_gpu(args):
     if tt.tt_emb_get_last_error(h) != tt.TT_OK:
         raise RuntimeError("device error in the timed region")
 
+    # eager launches (no graph), and the host time to enqueue them
+    ms_eager = timed(step, args.steps)
+    torch.cuda.synchronize(dev)
+    t0 = time.perf_counter()
+    for _ in range(200):
+        step()
+    host_us = (time.perf_counter() - t0) / 200 * 1e6
+    torch.cuda.synchronize(dev)
+
     # forward alone
     ms_fwd = timed(lambda: tt.tt_emb_forward(h, idx, off, None, tt.TT_POOL_SUM, out, stream), args.steps)
 
-    # per-kernel durations from the library's stage events (same stream, same steps)
-    tt.tt_emb_set_stage_timing(h, True)
+    # per-kernel durations: a graph of the same step with an event after every kernel
+    gstage = capture(True)
     kstats = {}
     nstage = min(args.steps, 400)
     barrier()
     for _ in range(nstage):
         flush.fill_(1.0)
-        step()
+        gstage.replay()
         for which in (0, 1):
             for name, ms in tt.tt_emb_stage_times(h, which):
                 kstats.setdefault(name, []).append(ms)
-    tt.tt_emb_set_stage_timing(h, False)
     kavg = {k: sum(v) / len(v) for k, v in kstats.items()}
+    del gstage, graph
 
     # end to end through the C ABI with host buffers: inputs copied in, result copied out, every step
     idx_h = torch.from_numpy(wl.indices).pin_memory()
@@ -371,6 +398,8 @@ def run_gpu(args):
                 "l2": f"flushed before every timed step ({L2_FLUSH_BYTES >> 20} MiB write, outside the events)",
                 "replicas": ws,
             },
+            "timing": "CUDA graph of forward + backward replayed per step" if not args.eager else "eager launches",
+            "eager": {"ms_per_step": ms_eager / args.steps, "host_enqueue_us_per_step": host_us},
             "forward": {"ns_per_nnz": 1e6 * ms_fwd / (nnz * args.steps),
                         "lookups_per_s": nnz * args.steps * ws / (ms_fwd / 1e3)},
             "step_roofline": {"flops_per_step": step_flops, "achieved_tflops": step_tf, "peak_tflops": peak_tf,
@@ -401,6 +430,7 @@ def main():
     ap.add_argument("--warmup", type=int, default=20)
     ap.add_argument("--impl", choices=["gb300", "reference"], default="gb300")
     ap.add_argument("--no-cpu-baseline", action="store_true", help="skip the oracle timing")
+    ap.add_argument("--eager", action="store_true", help="time eager launches instead of a CUDA graph replay")
     args = ap.parse_args()
     if args.impl == "reference":
         return run_reference(args)

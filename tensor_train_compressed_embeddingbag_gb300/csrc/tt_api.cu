@@ -6,7 +6,9 @@
 // tt_compute.cu.
 #include <algorithm>
 #include <cstdio>
+#include <cstdlib>
 #include <cstring>
+#include <mutex>
 #include <new>
 #include <vector>
 
@@ -14,6 +16,10 @@
 #include "tt_internal.cuh"
 
 using namespace ttemb;
+
+namespace ttemb {
+bool g_use_pdl = true;
+}
 
 namespace {
 
@@ -42,6 +48,9 @@ struct tt_emb {
     int* d_fixed = nullptr;      // err, counters[2], ntiles, grp_done[n2]
     float* d_tbuf = nullptr;
     int64_t tbuf_floats = 0;
+    int* d_tflag = nullptr;      // dense touched-pair flags
+    int split_small = 1;         // column split of k_tile_bwd on the single-CTA-sort path
+    int cap_small = 64, cap_large = 128;
     Params P{};                  // constants + workspace pointers
     // workspace
     void* d_ws = nullptr;
@@ -69,19 +78,43 @@ namespace {
 
 tt_status cuda_status(cudaError_t e) { return e == cudaSuccess ? TT_OK : TT_ERR_CUDA; }
 
+int pow2_floor(int x) {
+    int p = 1;
+    while (p * 2 <= x) p *= 2;
+    return p;
+}
+
+bool use_small_path(const tt_emb* h, int64_t nnz) {
+    const Params& P = h->P;
+    return nnz <= kSmallMaxNnz && P.n1 <= kSmallMaxBins && P.n2 <= kSmallMaxBins && P.n3 <= kSmallMaxBins;
+}
+
+// Tiles of a call: each (table, i2) group of c lookups gives ceil(c / cap) tiles.
+int max_tiles_for(const tt_emb* h, int64_t nnz, int cap) {
+    return (int)((std::max<int64_t>(nnz, 1) + cap - 1) / cap) + h->P.n2;
+}
+
 // Workspace carve-up for up to `nnz` lookups; base == nullptr only measures.
 size_t carve(tt_emb* h, void* base, int64_t nnz, bool assign) {
     Arena A;
     A.base = static_cast<char*>(base);
     Params& P = h->P;
     const int64_t N = std::max<int64_t>(nnz, 1);
-    const int nch = (int)((N + kChunk - 1) / kChunk);
-    const int max_tiles = (int)((N + P.tile_cap - 1) / P.tile_cap) + P.n2;
+    const int64_t Ns = std::min<int64_t>(N, kSmallMaxNnz);
+    const int nch = std::max((int)((N + kChunk - 1) / kChunk), (int)((Ns + kSmallChunk - 1) / kSmallChunk));
+    const int tiles_small = max_tiles_for(h, Ns, h->cap_small);
+    const int tiles_large = max_tiles_for(h, N, h->cap_large);
+    const int max_tiles = std::max(tiles_small, tiles_large);
+    const size_t part_floats = std::max((size_t)tiles_small * h->split_small, (size_t)tiles_large) * P.s2_max;
+    const size_t qslots = std::max<size_t>((size_t)N, (size_t)Ns * h->split_small);
     int* lk_i1 = A.take<int>(N);
     int* lk_i2 = A.take<int>(N);
     int* lk_i3 = A.take<int>(N);
     int* lk_bag = A.take<int>(N);
     float* lk_s = A.take<float>(N);
+    uint16_t* lr1 = A.take<uint16_t>(Ns);
+    uint16_t* lr2 = A.take<uint16_t>(Ns);
+    uint16_t* lr3 = A.take<uint16_t>(Ns);
     int* H1 = A.take<int>((size_t)P.n1 * nch);
     int* H3 = A.take<int>((size_t)P.n3 * nch);
     int* H2 = A.take<int>((size_t)P.n2 * nch);
@@ -94,11 +127,12 @@ size_t carve(tt_emb* h, void* base, int64_t nnz, bool assign) {
     int* grp_ntiles = A.take<int>(P.n2);
     int* rep_pair = A.take<int>(N);
     int* rep_row = A.take<int>(N);
-    float* Qbuf = A.take<float>((size_t)N * P.qs_max);
+    float* Qbuf = A.take<float>(qslots * P.qs_max);
     float* Pbuf = A.take<float>((size_t)N * P.ps_max);
-    float* dG2part = A.take<float>((size_t)max_tiles * P.s2_max);
+    float* dG2part = A.take<float>(part_floats);
     if (assign) {
         P.lk_i1 = lk_i1; P.lk_i2 = lk_i2; P.lk_i3 = lk_i3; P.lk_bag = lk_bag; P.lk_s = lk_s;
+        P.lr1 = lr1; P.lr2 = lr2; P.lr3 = lr3;
         P.H1 = H1; P.H3 = H3; P.H2 = H2;
         P.pi1 = pi1; P.pi3 = pi3; P.pi21 = pi21; P.sigma = sigma;
         P.tiles = tiles; P.grp_first = grp_first; P.grp_ntiles = grp_ntiles;
@@ -157,6 +191,10 @@ tt_status validate_table(int64_t E, const int64_t p[3], const int32_t q[3], cons
 }
 
 tt_status build_handle(tt_emb* h, int ntab, const tt_table_desc* d) {
+    {
+        const char* e = getenv("TTEMB_PDL");
+        g_use_pdl = !(e && e[0] == '0');
+    }
     // every host-side check comes before the first CUDA call
     for (int t = 0; t < ntab; ++t) {
         tt_status st = validate_table(d[t].num_embeddings, d[t].p, d[t].q, d[t].ranks);
@@ -171,10 +209,24 @@ tt_status build_handle(tt_emb* h, int ntab, const tt_table_desc* d) {
         if (s1 > kMaxBinsPerDigit || s2 > kMaxBinsPerDigit || s3 > kMaxBinsPerDigit) return TT_ERR_SHAPE;
     }
     if (cudaGetDevice(&h->device) != cudaSuccess) return TT_ERR_CUDA;
+    {
+        // kernel attributes are set once per device, never during a launch sequence
+        static std::mutex mu;
+        static std::vector<int> done;
+        std::lock_guard<std::mutex> lock(mu);
+        if (std::find(done.begin(), done.end(), h->device) == done.end()) {
+            int max_smem = 0;
+            if (cudaDeviceGetAttribute(&max_smem, cudaDevAttrMaxSharedMemoryPerBlockOptin, h->device) != cudaSuccess ||
+                set_sort_attributes(max_smem) != cudaSuccess || set_fwd_attributes(max_smem) != cudaSuccess ||
+                set_bwd_attributes(max_smem) != cudaSuccess)
+                return TT_ERR_CUDA;
+            done.push_back(h->device);
+        }
+    }
     h->ntab = ntab;
     const int D = d[0].q[0] * d[0].q[1] * d[0].q[2];
     int n1 = 0, n2 = 0, n3 = 0, qs = 1, ps = 1, s2 = 1, r1m = 1, Nm = 1, q1Nm = 1;
-    int64_t tb = 0;
+    int64_t tb = 0, fb = 0;
     for (int t = 0; t < ntab; ++t) {
         TableDev T{};
         T.E = d[t].num_embeddings;
@@ -185,6 +237,9 @@ tt_status build_handle(tt_emb* h, int ntab, const tt_table_desc* d) {
         T.G1 = d[t].cores_dev[0]; T.G2 = d[t].cores_dev[1]; T.G3 = d[t].cores_dev[2];
         T.tbase = tb;
         tb += (int64_t)T.p1 * T.p2 * T.q1 * T.q2 * T.r2;
+        T.fbase = fb;
+        fb += (int64_t)T.p1 * T.p2;
+        T.dclass = dim_class_of(T.q1, T.q2, T.q3, T.r1, T.r2);
         T.base1 = n1; T.base2 = n2; T.base3 = n3;
         n1 += T.p1; n2 += T.p2; n3 += T.p3;
         qs = std::max(qs, T.q1 * T.r1);
@@ -202,13 +257,21 @@ tt_status build_handle(tt_emb* h, int ntab, const tt_table_desc* d) {
     P.D = D;
     P.qs_max = qs; P.ps_max = ps; P.s2_max = s2;
     P.r1_max = r1m; P.N_max = Nm; P.q1N_max = q1Nm;
-    // tile size: the summed upstream gradient of a tile (tile_cap x D floats) stays <= 64 KB
-    {
-        const int lim = std::min(kTileThreads, 16384 / D);
-        int cap = 1;
-        while (cap * 2 <= lim) cap *= 2;
-        P.tile_cap = cap;
+    // tile caps: the summed upstream gradient of a tile (cap x D floats) stays <= 16 KB on the
+    // single-CTA-sort path (many small tiles) and <= 64 KB on the multi-CTA path
+    h->cap_small = pow2_floor(std::min(kTileThreads, 4096 / D));
+    h->cap_large = pow2_floor(std::min(kTileThreads, 16384 / D));
+    P.tile_cap = h->cap_large;
+    int common = h->tabs[0].dclass, p1m = 1;
+    bool can_split = true;
+    for (const TableDev& T : h->tabs) {
+        if (T.dclass != common) common = -1;
+        p1m = std::max(p1m, T.p1);
+        can_split = can_split && T.r2 % 8 == 0 && T.r2 >= 16;
     }
+    P.dclass_all = common;
+    P.p1_max = p1m;
+    h->split_small = can_split ? 2 : 1;
     // device tables
     std::vector<int> bins(n1 + n2 + n3);
     for (int t = 0; t < ntab; ++t) {
@@ -219,14 +282,20 @@ tt_status build_handle(tt_emb* h, int ntab, const tt_table_desc* d) {
     }
     if (cudaMalloc(&h->d_tables, sizeof(TableDev) * ntab) != cudaSuccess) return TT_ERR_NOMEM;
     if (cudaMalloc(&h->d_bins, sizeof(int) * bins.size()) != cudaSuccess) return TT_ERR_NOMEM;
-    const int nfixed = 8 + n2;
+    const int nfixed = 8 + 2 * n2;
     if (cudaMalloc(&h->d_fixed, sizeof(int) * nfixed) != cudaSuccess) return TT_ERR_NOMEM;
     if (cudaMalloc(&h->d_tbuf, sizeof(float) * std::max<int64_t>(tb, 1)) != cudaSuccess) return TT_ERR_NOMEM;
+    if (cudaMalloc(&h->d_tflag, sizeof(int) * std::max<int64_t>(fb, 1)) != cudaSuccess) return TT_ERR_NOMEM;
+    if (cudaMemset(h->d_tflag, 0, sizeof(int) * std::max<int64_t>(fb, 1)) != cudaSuccess) return TT_ERR_CUDA;
     h->tbuf_floats = tb;
     if (cudaMemcpy(h->d_tables, h->tabs.data(), sizeof(TableDev) * ntab, cudaMemcpyHostToDevice) != cudaSuccess ||
         cudaMemcpy(h->d_bins, bins.data(), sizeof(int) * bins.size(), cudaMemcpyHostToDevice) != cudaSuccess ||
         cudaMemset(h->d_fixed, 0, sizeof(int) * nfixed) != cudaSuccess)
         return TT_ERR_CUDA;
+    {
+        const int one = 1;  // touched flags start at 0: the first epoch is 1
+        if (cudaMemcpy(h->d_fixed + 4, &one, sizeof(int), cudaMemcpyHostToDevice) != cudaSuccess) return TT_ERR_CUDA;
+    }
     P.tables = h->d_tables;
     P.bin1_tab = h->d_bins;
     P.bin2_tab = h->d_bins + n1;
@@ -234,8 +303,10 @@ tt_status build_handle(tt_emb* h, int ntab, const tt_table_desc* d) {
     P.err = h->d_fixed;
     P.counters = h->d_fixed + 1;
     P.ntiles = h->d_fixed + 3;
+    P.epoch = h->d_fixed + 4;
     P.grp_done = h->d_fixed + 8;
     P.Tbuf = h->d_tbuf;
+    P.tflag = h->d_tflag;
     return TT_OK;
 }
 
@@ -245,6 +316,7 @@ void free_handle(tt_emb* h) {
     cudaFree(h->d_bins);
     cudaFree(h->d_fixed);
     cudaFree(h->d_tbuf);
+    cudaFree(h->d_tflag);
     cudaFree(h->d_ws);
     cudaFree(h->d_cache_rows);
     cudaFree(h->d_cache_vals);
@@ -254,6 +326,14 @@ void free_handle(tt_emb* h) {
         for (int i = 0; i <= kMaxStages; ++i)
             if (h->ev[w][i]) cudaEventDestroy(h->ev[w][i]);
     delete h;
+}
+
+// Event record that also works during stream capture (as an event node of the graph).
+cudaError_t record_stage(cudaEvent_t ev, cudaStream_t s) {
+    cudaStreamCaptureStatus cs = cudaStreamCaptureStatusNone;
+    if (cudaStreamIsCapturing(s, &cs) != cudaSuccess) return cudaErrorUnknown;
+    return cs == cudaStreamCaptureStatusActive ? cudaEventRecordWithFlags(ev, s, cudaEventRecordExternal)
+                                               : cudaEventRecord(ev, s);
 }
 
 // Launch sequence helper: records stage events when timing is on.
@@ -266,7 +346,7 @@ struct Seq {
     Seq(tt_emb* hh, int w, cudaStream_t ss) : h(hh), which(w), s(ss) {
         if (h->timing) {
             if (!h->ev[w][0] && cudaEventCreate(&h->ev[w][0]) != cudaSuccess) st = TT_ERR_CUDA;
-            else if (cudaEventRecord(h->ev[w][0], s) != cudaSuccess) st = TT_ERR_CUDA;
+            else if (record_stage(h->ev[w][0], s) != cudaSuccess) st = TT_ERR_CUDA;
         }
     }
     void run(const char* name, cudaError_t (*fn)(const Params&, cudaStream_t)) {
@@ -276,7 +356,7 @@ struct Seq {
         if (h->timing && n < kMaxStages) {
             cudaEvent_t& ev = h->ev[which][n + 1];
             if (!ev && cudaEventCreate(&ev) != cudaSuccess) { st = TT_ERR_CUDA; return; }
-            if (cudaEventRecord(ev, s) != cudaSuccess) { st = TT_ERR_CUDA; return; }
+            if (record_stage(ev, s) != cudaSuccess) { st = TT_ERR_CUDA; return; }
             h->names[which][n] = name;
         }
         ++n;
@@ -368,8 +448,23 @@ tt_status tt_emb_forward(tt_emb* h, const int64_t* indices, int64_t nnz, const i
     P.nbags = num_bags;
     P.bags_per_table = num_bags / h->ntab;
     P.out = out;
-    P.nch = (int)((std::max<int64_t>(nnz, 1) + kChunk - 1) / kChunk);
-    P.max_tiles = (int)((std::max<int64_t>(nnz, 1) + P.tile_cap - 1) / P.tile_cap) + P.n2;
+    const bool small = use_small_path(h, nnz);
+    P.small = small ? 1 : 0;
+    P.split = small ? h->split_small : 1;
+    P.tile_cap = small ? h->cap_small : h->cap_large;
+    P.nch = (int)((std::max<int64_t>(nnz, 1) + (small ? kSmallChunk : kChunk) - 1) / (small ? kSmallChunk : kChunk));
+    P.max_tiles = max_tiles_for(h, nnz, P.tile_cap);
+    {
+        int g1f = 1, dtf = 1;
+        for (const TableDev& T : h->tabs) {
+            const int Ns = T.q2 * (T.r2 / P.split);
+            const int pb = bwd_batch_pairs(T.q1, Ns, T.r1);
+            g1f = std::max(g1f, pb * T.q1 * T.r1);
+            dtf = std::max(dtf, pb * T.q1 * Ns);
+        }
+        P.g1s_floats = g1f;
+        P.dts_floats = dtf;
+    }
     P.cache_rows = h->d_cache_rows;
     P.cache_n = h->cache_n;
     P.cache_vals = h->d_cache_vals;
@@ -388,12 +483,17 @@ tt_status tt_emb_forward(tt_emb* h, const int64_t* indices, int64_t nnz, const i
     if (nnz == 0) {
         if (cudaMemsetAsync(out, 0, sizeof(float) * (size_t)num_bags * P.D, s) != cudaSuccess) return TT_ERR_CUDA;
     } else {
-        q.run("decode_hist", launch_decode_hist);
-        q.run("scan13", launch_scan13);
-        q.run("scatter13", launch_scatter13);
-        q.run("scan2_tiles", launch_scan2_tiles);
-        q.run("scatter2", launch_scatter2);
-        q.run("tile_fwd", launch_tile_fwd);
+        if (small) {
+            q.run("decode", launch_decode_small);
+            q.run("scan3", launch_scan3_small);
+        } else {
+            q.run("decode_hist", launch_decode_hist);
+            q.run("scan13", launch_scan13);
+            q.run("scatter13", launch_scatter13);
+            q.run("scan2_tiles", launch_scan2_tiles);
+            q.run("scatter2", launch_scatter2);
+        }
+        q.run("fwd_T", launch_fwd_T);
         q.run("pool", launch_pool);
     }
     st = q.finish();

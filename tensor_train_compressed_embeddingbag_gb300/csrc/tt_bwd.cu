@@ -1,0 +1,733 @@
+// tt_bwd.cu -- backward contractions, sorted-segment reductions and the fused
+// SGD update (sm_103a, FP32 FFMA).
+//
+// FBTT README, "Software Cache" (the core gradients are a chain of products in
+// reversed order) and "Fused Kernel" (the update is applied inside the
+// backward pass); tensorflow/addons EmbeddingBag issue (gradients are formed
+// after sorting by key so that no two threads write the same entry).
+// Per tile of lookups that share (table, i2), with rows (i1, i2, i3) and pairs
+// (i1, i2) as maximal runs of the sorted tile:
+//   gs  = sum over the row's lookups of s_n grad_out[bag]  (q1 q2 x q3)
+//   P3  = T^T gs                       (r2 x q3)   dG3 partial per row
+//   dT  = sum_rows gs . G3[i3]^T       (q1 x q2 r2) per pair
+//   Q   = dT . G2[i2]^T                (q1 x r1)   dG1 partial per pair
+//   dG2 += G1[i1]^T . dT               (r1 x q2 r2)
+// A column split (SPLIT = 2) gives each of two blocks the columns c of one
+// half of r2: P3, dT and dG2 columns are disjoint, Q is summed over the two
+// halves in k_reduce13.
+#include <algorithm>
+
+#include "tt_dims.cuh"
+
+namespace ttemb {
+
+constexpr int kBwdThreads = 256;
+constexpr int kMaxAcc2 = 64;   // generic path: dG2 accumulators per thread (r1 q2 r2 <= 64 * 256)
+constexpr int kMaxAcc13 = 32;  // k_reduce13: slice <= 32 * 256 floats
+constexpr int kGsUnroll = 4;     // independent gradient rows per thread in flight
+constexpr int kDtUnroll = 4;     // independent dT items per thread in flight
+
+__host__ __device__ inline size_t al16(size_t x) { return (x + 15) & ~(size_t)15; }
+
+// Pairs per batch: dT batch <= 8192 floats, G1 batch <= 8192 floats, and at
+// most 256 threads for the Q register tiles.
+__host__ __device__ inline int bwd_pairs_per_batch(int q1, int Ns, int r1) {
+    int pb = 16;
+    if (pb * q1 * Ns > 8192) pb = 8192 / (q1 * Ns);
+    if (pb * q1 * r1 > 8192) pb = 8192 / (q1 * r1);
+    if (pb * (r1 / 4 > 0 ? r1 / 4 : 1) > 256) pb = 256 / (r1 / 4 > 0 ? r1 / 4 : 1);
+    return pb < 1 ? 1 : pb;
+}
+
+struct BwdLayout {
+    size_t keys, sn, si1, si3, sbag, ss, tbag, ts, rowid, pairid, rowbeg, pairbeg, sh, gs, g2t, g1s, dts, total;
+};
+
+__host__ __device__ inline BwdLayout bwd_layout(int cap, int D, int r1max, int Nmax, int g1f, int dtf) {
+    BwdLayout L;
+    size_t o = 0;
+    L.keys = o;    o = al16(o + sizeof(unsigned long long) * cap);
+    L.sn = o;      o = al16(o + sizeof(int) * cap);
+    L.si1 = o;     o = al16(o + sizeof(int) * cap);
+    L.si3 = o;     o = al16(o + sizeof(int) * cap);
+    L.sbag = o;    o = al16(o + sizeof(int) * cap);
+    L.ss = o;      o = al16(o + sizeof(float) * cap);
+    L.tbag = o;    o = al16(o + sizeof(int) * cap);
+    L.ts = o;      o = al16(o + sizeof(float) * cap);
+    L.rowid = o;   o = al16(o + sizeof(int) * cap);
+    L.pairid = o;  o = al16(o + sizeof(int) * cap);
+    L.rowbeg = o;  o = al16(o + sizeof(int) * (cap + 1));
+    L.pairbeg = o; o = al16(o + sizeof(int) * (cap + 1));
+    L.sh = o;      o = al16(o + sizeof(int) * 64);
+    L.gs = o;      o = al16(o + sizeof(float) * (size_t)cap * D);
+    L.g2t = o;     o = al16(o + sizeof(float) * (size_t)(r1max + 4) * Nmax);  // row stride r1 + 4
+    L.g1s = o;     o = al16(o + sizeof(float) * (size_t)g1f);
+    L.dts = o;     o = al16(o + sizeof(float) * (size_t)dtf);
+    L.total = o;
+    return L;
+}
+
+// The tile's lookups come grouped by (table, i2) (ordered by (i1, pos) on the
+// multi-CTA path, by pos on the small path); sort them by (i1, i3, position) in
+// shared memory.  Bag and scale of each lookup are loaded in the same pass and
+// follow the sort.
+__device__ void load_and_sort_tile(const Params& P, int start, int len, unsigned long long* keys, int* sn,
+                                   int* si1, int* si3, int* sbag, float* ss, int* tbag, float* ts) {
+    int npow = 1;
+    while (npow < len) npow <<= 1;
+    for (int k = threadIdx.x; k < npow; k += blockDim.x) {
+        unsigned long long key = ~0ull;
+        if (k < len) {
+            const int n = P.pi21[start + k];
+            key = ((unsigned long long)P.lk_i1[n] << (2 * kFieldBits)) |
+                  ((unsigned long long)P.lk_i3[n] << kFieldBits) | (unsigned long long)k;
+            tbag[k] = P.lk_bag[n];
+            ts[k] = P.lk_s[n];
+        }
+        keys[k] = key;
+    }
+    block_bitonic_sort(keys, npow);
+    const unsigned long long fmask = (1ull << kFieldBits) - 1;
+    for (int k = threadIdx.x; k < len; k += blockDim.x) {
+        const unsigned long long key = keys[k];
+        const int k0 = (int)(key & fmask);
+        sn[k] = P.pi21[start + k0];
+        si1[k] = (int)(key >> (2 * kFieldBits));
+        si3[k] = (int)((key >> kFieldBits) & fmask);
+        sbag[k] = tbag[k0];
+        ss[k] = ts[k0];
+    }
+    __syncthreads();
+}
+
+template <class Dm, int SPLIT>
+__device__ void tile_bwd_body(const Params& P, const TableDev& T, const Dm dm, unsigned char* smraw) {
+    const BwdLayout L = bwd_layout(P.tile_cap, P.D, P.r1_max, P.N_max, P.g1s_floats, P.dts_floats);
+    unsigned long long* keys = (unsigned long long*)(smraw + L.keys);
+    int* sn = (int*)(smraw + L.sn);
+    int* si1 = (int*)(smraw + L.si1);
+    int* si3 = (int*)(smraw + L.si3);
+    int* sbag = (int*)(smraw + L.sbag);
+    float* ss = (float*)(smraw + L.ss);
+    int* tbag = (int*)(smraw + L.tbag);
+    float* ts = (float*)(smraw + L.ts);
+    int* rowid = (int*)(smraw + L.rowid);
+    int* pairid = (int*)(smraw + L.pairid);
+    int* rowbeg = (int*)(smraw + L.rowbeg);
+    int* pairbeg = (int*)(smraw + L.pairbeg);
+    int* sh = (int*)(smraw + L.sh);
+    float* gs = (float*)(smraw + L.gs);
+    float* g2t = (float*)(smraw + L.g2t);
+    float* g1s = (float*)(smraw + L.g1s);
+    float* dts = (float*)(smraw + L.dts);
+
+    const int tile = blockIdx.x / SPLIT, sp = blockIdx.x % SPLIT;
+    const int4 tl = P.tiles[tile];
+    const int start = tl.x, len = tl.y, g = tl.z;
+    const int i2 = g - T.base2;
+    const int q1 = dm.q1(), q2 = dm.q2(), q3 = dm.q3(), r1 = dm.r1(), r2 = dm.r2();
+    const int D = q1 * q2 * q3, q12 = q1 * q2;
+    const int r2s = r2 / SPLIT, c0 = sp * r2s, Ns = q2 * r2s;
+    const int t = P.bin2_tab[g];
+
+    // ---- lookups of the tile, sorted by (i1, i3, position)
+    load_and_sort_tile(P, start, len, keys, sn, si1, si3, sbag, ss, tbag, ts);
+    const int k = threadIdx.x;  // tile_cap <= blockDim
+    int fr = 0, fp = 0;
+    if (k < len) {
+        fp = (k == 0) || (si1[k] != si1[k - 1]);
+        fr = fp || (si3[k] != si3[k - 1]);
+    }
+    int nrows, npairs;
+    const int rex = block_scan_excl(fr, sh, &nrows);
+    const int pex = block_scan_excl(fp, sh, &npairs);
+    if (k < len) {
+        rowid[k] = rex + fr - 1;
+        pairid[k] = pex + fp - 1;
+        if (fr) rowbeg[rex] = k;
+        if (fp) pairbeg[pex] = k;
+    }
+    if (k == 0) {
+        rowbeg[nrows] = len;
+        pairbeg[npairs] = len;
+    }
+    __syncthreads();
+    // partial slots are numbered by the position of the run's first lookup in the
+    // grouped order, so every run of every tile owns one slot, with no atomics
+    if (sp == 0 && k < len) {
+        const int n = sn[k];
+        P.rep_row[n] = fr ? start + k : -1;
+        P.rep_pair[n] = fp ? start + k : -1;
+    }
+
+    // ---- G2 columns of this split, transposed: g2t[jc'][a], jc' = j2 r2s + c' (8 loads in flight)
+    {
+        const float* src = T.G2 + (int64_t)i2 * r1 * q2 * r2;
+        const int n = r1 * Ns;
+        for (int base = 0; base < n; base += 8 * kBwdThreads) {
+            float v[8];
+#pragma unroll
+            for (int q = 0; q < 8; ++q) {
+                const int e = base + q * kBwdThreads + threadIdx.x;
+                v[q] = 0.f;
+                if (e < n) {
+                    const int a = e / Ns, jc = e - a * Ns;
+                    const int j2 = jc / r2s, c = jc - j2 * r2s;
+                    v[q] = __ldg(src + (a * q2 + j2) * r2 + c0 + c);
+                }
+            }
+#pragma unroll
+            for (int q = 0; q < 8; ++q) {
+                const int e = base + q * kBwdThreads + threadIdx.x;
+                if (e < n) {
+                    const int a = e / Ns, jc = e - a * Ns;
+                    g2t[jc * (r1 + 4) + a] = v[q];
+                }
+            }
+        }
+    }
+    // ---- gs: summed upstream gradient of every tile-row.  Each thread takes
+    // kGsUnroll (row, float4 column) items and loads the first lookup of all of
+    // them before summing; further lookups of a row (repeated rows) follow.
+    {
+        const int D4 = D >> 2;  // every compiled class and every D % 4 == 0 table; else scalar below
+        if ((D & 3) == 0) {
+            const int items = nrows * D4;
+            for (int e0 = threadIdx.x; e0 < items; e0 += kGsUnroll * kBwdThreads) {
+                float4 x[kGsUnroll];
+                int row[kGsUnroll], q4[kGsUnroll];
+#pragma unroll
+                for (int u = 0; u < kGsUnroll; ++u) {
+                    const int e = e0 + u * kBwdThreads;
+                    row[u] = e < items ? e / D4 : -1;
+                    q4[u] = e < items ? e - row[u] * D4 : 0;
+                    x[u] = make_float4(0.f, 0.f, 0.f, 0.f);
+                    if (row[u] >= 0) {
+                        const int kk = rowbeg[row[u]];
+                        x[u] = __ldg(reinterpret_cast<const float4*>(P.grad_out + (int64_t)sbag[kk] * D) + q4[u]);
+                    }
+                }
+#pragma unroll
+                for (int u = 0; u < kGsUnroll; ++u) {
+                    if (row[u] < 0) continue;
+                    const int kb = rowbeg[row[u]];
+                    const float s0 = ss[kb];
+                    float4 a = make_float4(s0 * x[u].x, s0 * x[u].y, s0 * x[u].z, s0 * x[u].w);
+                    for (int kk = kb + 1; kk < rowbeg[row[u] + 1]; ++kk) {
+                        const float4 y = __ldg(reinterpret_cast<const float4*>(P.grad_out + (int64_t)sbag[kk] * D) + q4[u]);
+                        const float sk = ss[kk];
+                        a.x = fmaf(sk, y.x, a.x); a.y = fmaf(sk, y.y, a.y);
+                        a.z = fmaf(sk, y.z, a.z); a.w = fmaf(sk, y.w, a.w);
+                    }
+                    *reinterpret_cast<float4*>(gs + row[u] * D + q4[u] * 4) = a;
+                }
+            }
+        } else {
+            for (int e = threadIdx.x; e < nrows * D; e += blockDim.x) {
+                const int row = e / D, j = e - row * D;
+                float acc = 0.f;
+                for (int kk = rowbeg[row]; kk < rowbeg[row + 1]; ++kk)
+                    acc = fmaf(ss[kk], __ldg(P.grad_out + (int64_t)sbag[kk] * D + j), acc);
+                gs[row * D + j] = acc;
+            }
+        }
+    }
+    __syncthreads();
+
+    // ---- dG3 partial per tile-row, columns c of this split: P3[c][j3] = sum_j12 T[j12][c] gs[j12 q3 + j3]
+    for (int e = threadIdx.x; e < nrows * r2s; e += blockDim.x) {
+        const int row = e / r2s, c = c0 + (e - row * r2s);
+        const int kk = rowbeg[row];
+        const float* Tp = P.Tbuf + T.tbase + ((int64_t)i2 * T.p1 + si1[kk]) * (int64_t)(q12 * r2) + c;
+        const float* gr = gs + row * D;
+        float* dst = P.Pbuf + (int64_t)(start + kk) * P.ps_max + c * q3;
+        if constexpr (Dm::kStatic) {
+            constexpr int Q3 = Dm::q3(), Q12 = Dm::q1() * Dm::q2(), R2 = Dm::r2();
+            float acc[Q3];
+#pragma unroll
+            for (int j3 = 0; j3 < Q3; ++j3) acc[j3] = 0.f;
+#pragma unroll
+            for (int j12 = 0; j12 < Q12; ++j12) {
+                const float tv = __ldg(Tp + j12 * R2);
+#pragma unroll
+                for (int j3 = 0; j3 < Q3; j3 += 4) {
+                    const float4 x = *reinterpret_cast<const float4*>(gr + j12 * Q3 + j3);
+                    acc[j3] = fmaf(tv, x.x, acc[j3]);
+                    acc[j3 + 1] = fmaf(tv, x.y, acc[j3 + 1]);
+                    acc[j3 + 2] = fmaf(tv, x.z, acc[j3 + 2]);
+                    acc[j3 + 3] = fmaf(tv, x.w, acc[j3 + 3]);
+                }
+            }
+#pragma unroll
+            for (int j3 = 0; j3 < Q3; ++j3) dst[j3] = acc[j3];
+        } else {
+            for (int j3 = 0; j3 < q3; ++j3) {
+                float acc = 0.f;
+                for (int j12 = 0; j12 < q12; ++j12) acc = fmaf(Tp[j12 * r2], gr[j12 * q3 + j3], acc);
+                dst[j3] = acc;
+            }
+        }
+    }
+
+    // ---- pairs in batches: dT, dG1 partial (Q), dG2 accumulation
+    const int PB = bwd_pairs_per_batch(q1, Ns, r1);
+    float* G2p = T.G2 + (int64_t)i2 * r1 * q2 * r2;
+
+    if constexpr (Dm::kStatic) {
+        constexpr int R1 = Dm::r1(), Q2 = Dm::q2(), Q3 = Dm::q3(), R2 = Dm::r2();
+        constexpr int R2S = R2 / SPLIT, NS = Q2 * R2S, D_ = 4 * Q2 * Q3;
+        constexpr int PBc = (16 * 4 * NS > 8192) ? 8192 / (4 * NS) : ((16 * 4 * R1 > 8192) ? 8192 / (4 * R1) : 16);
+        constexpr int PBS = (PBc * (R1 / 4) > 256) ? 256 / (R1 / 4) : PBc;
+        // Q tiles: (u, a4, kh); dG2 tiles: (a4, jc4) x K split KS over pairs
+        constexpr int A4 = R1 / 4;
+        constexpr int KH = 256 / (PBS * A4) >= 1 ? 256 / (PBS * A4) : 1;
+        constexpr int TT = A4 * (NS / 4);
+        constexpr int NT = TT >= 256 ? TT / 256 : 1;
+        constexpr int KS = (256 * NT) / TT;
+        static_assert(KH >= 1 && KH <= 32 && (KH & (KH - 1)) == 0, "Q split");
+        static_assert(KS >= 1 && KS <= 32 && (KS & (KS - 1)) == 0, "dG2 split");
+        static_assert(NT * 256 == TT * KS, "dG2 tiles");
+        float acc2[NT][4][4];
+#pragma unroll
+        for (int i = 0; i < NT; ++i)
+#pragma unroll
+            for (int a = 0; a < 4; ++a)
+#pragma unroll
+                for (int c = 0; c < 4; ++c) acc2[i][a][c] = 0.f;
+        const int ks = threadIdx.x % KS, tbase = threadIdx.x / KS;
+        for (int u0 = 0; u0 < npairs; u0 += PBS) {
+            const int nb = min(PBS, npairs - u0);
+            __syncthreads();
+            // g1s[u][a][j1], 8 loads in flight per thread
+            for (int base = 0; base < nb * R1 * 4; base += 8 * kBwdThreads) {
+                float v[8];
+#pragma unroll
+                for (int q = 0; q < 8; ++q) {
+                    const int e = base + q * kBwdThreads + threadIdx.x;
+                    v[q] = 0.f;
+                    if (e < nb * R1 * 4) {
+                        const int u = e / (R1 * 4), rem = e - u * (R1 * 4);
+                        v[q] = __ldg(T.G1 + (int64_t)si1[pairbeg[u0 + u]] * (4 * R1) + (rem & 3) * R1 + (rem >> 2));
+                    }
+                }
+#pragma unroll
+                for (int q = 0; q < 8; ++q) {
+                    const int e = base + q * kBwdThreads + threadIdx.x;
+                    if (e < nb * R1 * 4) g1s[e] = v[q];
+                }
+            }
+            // dts[u][jc'][j1] = sum_rows sum_j3 gs[row][(j1 q2 + j2) q3 + j3] G3[i3][c][j3];
+            // kDtUnroll items per thread load the G3 row of their pair's first row together
+            for (int e0 = threadIdx.x; e0 < nb * NS; e0 += kDtUnroll * kBwdThreads) {
+                float g3v[kDtUnroll][Q3];
+                int uu[kDtUnroll], jj[kDtUnroll];
+#pragma unroll
+                for (int v = 0; v < kDtUnroll; ++v) {
+                    const int e = e0 + v * kBwdThreads;
+                    uu[v] = e < nb * NS ? e / NS : -1;
+                    jj[v] = e < nb * NS ? e - uu[v] * NS : 0;
+                    const int j2 = jj[v] / R2S, c = c0 + (jj[v] - j2 * R2S);
+                    const int kb = uu[v] >= 0 ? pairbeg[u0 + uu[v]] : 0;
+                    const float* g3 = T.G3 + (int64_t)si3[kb] * (R2 * Q3) + c * Q3;
+#pragma unroll
+                    for (int j3 = 0; j3 < Q3; j3 += 4) {
+                        float4 x = make_float4(0.f, 0.f, 0.f, 0.f);
+                        if (uu[v] >= 0) x = __ldg(reinterpret_cast<const float4*>(g3 + j3));
+                        g3v[v][j3] = x.x; g3v[v][j3 + 1] = x.y; g3v[v][j3 + 2] = x.z; g3v[v][j3 + 3] = x.w;
+                    }
+                }
+#pragma unroll
+                for (int v = 0; v < kDtUnroll; ++v) {
+                    if (uu[v] < 0) continue;
+                    const int u = uu[v], jc = jj[v];
+                    const int j2 = jc / R2S, c = c0 + (jc - j2 * R2S);
+                    const int kb = pairbeg[u0 + u], ke = pairbeg[u0 + u + 1];
+                    float a4v[4] = {0.f, 0.f, 0.f, 0.f};
+                    for (int kk = kb; kk < ke; ++kk) {
+                        if (kk != kb && rowid[kk] == rowid[kk - 1]) continue;  // once per tile-row
+                        float g3r[Q3];
+                        if (kk == kb) {
+#pragma unroll
+                            for (int j3 = 0; j3 < Q3; ++j3) g3r[j3] = g3v[v][j3];
+                        } else {
+                            const float* g3 = T.G3 + (int64_t)si3[kk] * (R2 * Q3) + c * Q3;
+#pragma unroll
+                            for (int j3 = 0; j3 < Q3; j3 += 4) {
+                                const float4 x = __ldg(reinterpret_cast<const float4*>(g3 + j3));
+                                g3r[j3] = x.x; g3r[j3 + 1] = x.y; g3r[j3 + 2] = x.z; g3r[j3 + 3] = x.w;
+                            }
+                        }
+                        const float* gr = gs + rowid[kk] * D_ + j2 * Q3;
+#pragma unroll
+                        for (int j1 = 0; j1 < 4; ++j1) {
+#pragma unroll
+                            for (int j3 = 0; j3 < Q3; j3 += 4) {
+                                const float4 x = *reinterpret_cast<const float4*>(gr + j1 * Q2 * Q3 + j3);
+                                a4v[j1] = fmaf(x.x, g3r[j3], a4v[j1]);
+                                a4v[j1] = fmaf(x.y, g3r[j3 + 1], a4v[j1]);
+                                a4v[j1] = fmaf(x.z, g3r[j3 + 2], a4v[j1]);
+                                a4v[j1] = fmaf(x.w, g3r[j3 + 3], a4v[j1]);
+                            }
+                        }
+                    }
+                    *reinterpret_cast<float4*>(dts + (u * NS + jc) * 4) = make_float4(a4v[0], a4v[1], a4v[2], a4v[3]);
+                }
+            }
+            __syncthreads();
+            // Q[u][j1][a] = sum_jc' dts[u][jc'][j1] g2t[jc'][a]: thread (u, a4, kh)
+            {
+                const int kh = threadIdx.x % KH, ua = threadIdx.x / KH;
+                const int u = ua / A4, a4 = ua - u * A4;
+                float q[4][4];
+#pragma unroll
+                for (int j = 0; j < 4; ++j)
+#pragma unroll
+                    for (int a = 0; a < 4; ++a) q[j][a] = 0.f;
+                if (u < PBS) {
+                    const float* dt = dts + u * NS * 4;
+                    const float* gt = g2t + a4 * 4;
+                    constexpr int GS = R1 + 4;
+#pragma unroll 4
+                    for (int jc = kh; jc < NS; jc += KH) {
+                        const float4 x = *reinterpret_cast<const float4*>(dt + jc * 4);
+                        const float4 y = *reinterpret_cast<const float4*>(gt + jc * GS);
+                        const float xv[4] = {x.x, x.y, x.z, x.w};
+                        const float yv[4] = {y.x, y.y, y.z, y.w};
+#pragma unroll
+                        for (int j = 0; j < 4; ++j)
+#pragma unroll
+                            for (int a = 0; a < 4; ++a) q[j][a] = fmaf(xv[j], yv[a], q[j][a]);
+                    }
+                }
+#pragma unroll
+                for (int o = KH / 2; o >= 1; o >>= 1)
+#pragma unroll
+                    for (int j = 0; j < 4; ++j)
+#pragma unroll
+                        for (int a = 0; a < 4; ++a) q[j][a] += __shfl_xor_sync(0xffffffffu, q[j][a], o);
+                if (kh == 0 && u < nb) {
+                    float* dst = P.Qbuf + ((int64_t)(start + pairbeg[u0 + u]) * SPLIT + sp) * P.qs_max + a4 * 4;
+#pragma unroll
+                    for (int j = 0; j < 4; ++j)
+                        *reinterpret_cast<float4*>(dst + j * R1) = make_float4(q[j][0], q[j][1], q[j][2], q[j][3]);
+                }
+            }
+            // dG2[a][jc'] += sum_u sum_j1 g1s[u][a][j1] dts[u][jc'][j1]: tiles (a4, jl) own columns
+            // jc' = jl + (NS/4) c, c < 4 (consecutive lanes read consecutive float4); pairs u = ks mod KS
+#pragma unroll
+            for (int i = 0; i < NT; ++i) {
+                const int ti = tbase + i * (256 / KS);
+                const int a4 = ti / (NS / 4), jc4 = ti - a4 * (NS / 4);
+                for (int u = ks; u < nb; u += KS) {
+                    float gv[4][4], dv[4][4];
+#pragma unroll
+                    for (int a = 0; a < 4; ++a) {
+                        const float4 x = *reinterpret_cast<const float4*>(g1s + (u * R1 + a4 * 4 + a) * 4);
+                        gv[a][0] = x.x; gv[a][1] = x.y; gv[a][2] = x.z; gv[a][3] = x.w;
+                    }
+#pragma unroll
+                    for (int c = 0; c < 4; ++c) {
+                        const float4 x = *reinterpret_cast<const float4*>(dts + (u * NS + jc4 + (NS / 4) * c) * 4);
+                        dv[c][0] = x.x; dv[c][1] = x.y; dv[c][2] = x.z; dv[c][3] = x.w;
+                    }
+#pragma unroll
+                    for (int a = 0; a < 4; ++a)
+#pragma unroll
+                        for (int c = 0; c < 4; ++c)
+#pragma unroll
+                            for (int j = 0; j < 4; ++j) acc2[i][a][c] = fmaf(gv[a][j], dv[c][j], acc2[i][a][c]);
+                }
+            }
+        }
+        // combine the KS pair-parities (butterfly, fixed order)
+#pragma unroll
+        for (int o = KS / 2; o >= 1; o >>= 1)
+#pragma unroll
+            for (int i = 0; i < NT; ++i)
+#pragma unroll
+                for (int a = 0; a < 4; ++a)
+#pragma unroll
+                    for (int c = 0; c < 4; ++c) acc2[i][a][c] += __shfl_xor_sync(0xffffffffu, acc2[i][a][c], o);
+        // dG2 of this split: direct update, or partial + the group's last tile
+        const int nt = P.grp_ntiles[g];
+        float* part = P.dG2part + ((int64_t)tile * SPLIT + sp) * P.s2_max;
+        if (ks == 0) {
+#pragma unroll
+            for (int i = 0; i < NT; ++i) {
+                const int ti = tbase + i * (256 / KS);
+                const int a4 = ti / (NS / 4), jc4 = ti - a4 * (NS / 4);
+#pragma unroll
+                for (int a = 0; a < 4; ++a)
+#pragma unroll
+                    for (int c = 0; c < 4; ++c) {
+                        const int jc = jc4 + (NS / 4) * c, j2 = jc / R2S, cc = c0 + (jc - j2 * R2S);
+                        const int ga = ((a4 * 4 + a) * Q2 + j2) * R2 + cc;
+                        if (nt == 1) G2p[ga] = fmaf(-P.lr, acc2[i][a][c], G2p[ga]);
+                        else part[(a4 * 4 + a) * NS + jc] = acc2[i][a][c];
+                    }
+            }
+        }
+        if (nt == 1) {
+            if (P.slice_stamp && threadIdx.x == 0 && t == 0) P.slice_stamp[T.p1 + i2] = P.step + 1;
+            return;
+        }
+    } else {
+        // generic dimensions
+        float acc2[kMaxAcc2];
+#pragma unroll
+        for (int m = 0; m < kMaxAcc2; ++m) acc2[m] = 0.f;
+        const int S2 = r1 * Ns;
+        for (int u0 = 0; u0 < npairs; u0 += PB) {
+            const int nb = min(PB, npairs - u0);
+            __syncthreads();
+            for (int e = threadIdx.x; e < nb * r1 * q1; e += blockDim.x) {
+                const int u = e / (r1 * q1), rem = e - u * (r1 * q1);
+                const int a = rem / q1, j1 = rem - a * q1;
+                g1s[e] = T.G1[(int64_t)si1[pairbeg[u0 + u]] * (q1 * r1) + j1 * r1 + a];
+            }
+            for (int e = threadIdx.x; e < nb * Ns * q1; e += blockDim.x) {
+                const int u = e / (Ns * q1), rem = e - u * (Ns * q1);
+                const int jc = rem / q1, j1 = rem - jc * q1;
+                const int j2 = jc / r2s, c = c0 + (jc - j2 * r2s);
+                const int kb = pairbeg[u0 + u], ke = pairbeg[u0 + u + 1];
+                float acc = 0.f;
+                for (int kk = kb; kk < ke; ++kk) {
+                    if (kk != kb && rowid[kk] == rowid[kk - 1]) continue;
+                    const float* g3 = T.G3 + (int64_t)si3[kk] * (r2 * q3) + c * q3;
+                    const float* gr = gs + rowid[kk] * D + (j1 * q2 + j2) * q3;
+                    for (int j3 = 0; j3 < q3; ++j3) acc = fmaf(gr[j3], g3[j3], acc);
+                }
+                dts[(u * Ns + jc) * q1 + j1] = acc;
+            }
+            __syncthreads();
+            for (int e = threadIdx.x; e < nb * q1 * r1; e += blockDim.x) {
+                const int u = e / (q1 * r1), ja = e - u * (q1 * r1);
+                const int j1 = ja / r1, a = ja - j1 * r1;
+                float acc = 0.f;
+                for (int jc = 0; jc < Ns; ++jc) acc = fmaf(dts[(u * Ns + jc) * q1 + j1], g2t[jc * (r1 + 4) + a], acc);
+                P.Qbuf[((int64_t)(start + pairbeg[u0 + u]) * SPLIT + sp) * P.qs_max + ja] = acc;
+            }
+#pragma unroll
+            for (int m = 0; m < kMaxAcc2; ++m) {
+                const int e = threadIdx.x + m * kBwdThreads;
+                if (e < S2) {
+                    const int a = e / Ns, jc = e - a * Ns;
+                    float acc = acc2[m];
+                    for (int u = 0; u < nb; ++u)
+                        for (int j1 = 0; j1 < q1; ++j1)
+                            acc = fmaf(g1s[(u * r1 + a) * q1 + j1], dts[(u * Ns + jc) * q1 + j1], acc);
+                    acc2[m] = acc;
+                }
+            }
+        }
+        const int nt = P.grp_ntiles[g];
+        float* part = P.dG2part + ((int64_t)tile * SPLIT + sp) * P.s2_max;
+#pragma unroll
+        for (int m = 0; m < kMaxAcc2; ++m) {
+            const int e = threadIdx.x + m * kBwdThreads;
+            if (e < S2) {
+                const int a = e / Ns, jc = e - a * Ns;
+                const int j2 = jc / r2s, c = c0 + (jc - j2 * r2s);
+                const int ga = (a * q2 + j2) * r2 + c;
+                if (nt == 1) G2p[ga] = fmaf(-P.lr, acc2[m], G2p[ga]);
+                else part[e] = acc2[m];
+            }
+        }
+        if (nt == 1) {
+            if (P.slice_stamp && threadIdx.x == 0 && t == 0) P.slice_stamp[T.p1 + i2] = P.step + 1;
+            return;
+        }
+    }
+
+    // several tiles in the group: the last one (per split) sums the partials in tile order
+    __threadfence();
+    __syncthreads();
+    const int nt = P.grp_ntiles[g];
+    if (threadIdx.x == 0) sh[42] = (atomicAdd(&P.grp_done[g * SPLIT + sp], 1) == nt - 1);
+    __syncthreads();
+    if (!sh[42]) return;
+    __threadfence();
+    const int first = P.grp_first[g];
+    for (int e = threadIdx.x; e < r1 * Ns; e += blockDim.x) {
+        float sum = 0.f;
+        for (int tt = 0; tt < nt; ++tt)
+            sum += __ldcg(P.dG2part + ((int64_t)(first + tt) * SPLIT + sp) * P.s2_max + e);
+        const int a = e / Ns, jc = e - a * Ns;
+        const int j2 = jc / r2s, c = c0 + (jc - j2 * r2s);
+        const int ga = (a * q2 + j2) * r2 + c;
+        G2p[ga] = fmaf(-P.lr, sum, G2p[ga]);
+    }
+    if (threadIdx.x == 0) {
+        P.grp_done[g * SPLIT + sp] = 0;
+        if (P.slice_stamp && t == 0) P.slice_stamp[T.p1 + i2] = P.step + 1;
+    }
+}
+
+template <int DC, int SPLIT>
+__global__ void __launch_bounds__(kBwdThreads) k_tile_bwd(const __grid_constant__ Params P) {
+    pdl_entry();
+    if (*P.err) return;  // a device error was recorded: leave every core unchanged
+    if ((int)(blockIdx.x / SPLIT) >= *P.ntiles) return;
+    extern __shared__ __align__(16) unsigned char smraw[];
+    const int g = P.tiles[blockIdx.x / SPLIT].z;
+    const TableDev& T = P.tables[P.bin2_tab[g]];
+    switch (DC >= 0 ? DC : T.dclass) {
+        case kQ444R32: tile_bwd_body<SDims<4, 4, 4, 32, 32>, SPLIT>(P, T, {}, smraw); break;
+        case kQ444R16: tile_bwd_body<SDims<4, 4, 4, 16, 16>, SPLIT>(P, T, {}, smraw); break;
+        case kQ444R64: tile_bwd_body<SDims<4, 4, 4, 64, 64>, SPLIT>(P, T, {}, smraw); break;
+        case kQ448R64: tile_bwd_body<SDims<4, 4, 8, 64, 64>, SPLIT>(P, T, {}, smraw); break;
+        default: tile_bwd_body<DDims, SPLIT>(P, T, DDims{T.q1, T.q2, T.q3, T.r1, T.r2}, smraw); break;
+    }
+}
+
+// Sum the dG1 (per tile-pair, over the column splits) and dG3 (per tile-row)
+// partials of one slice in sorted-segment order, then apply the SGD update.
+// The slots of the slice are compacted in order; thread (lane group r, element
+// e) loads the slots j = r, r + R, ... all at once and sums them in order, then
+// the R partial sums are added in r order.
+constexpr int kReduceSlots = 1024;   // slots gathered per round
+constexpr int kReducePer = 16;       // loads in flight per thread
+
+__global__ void __launch_bounds__(kBwdThreads) k_reduce13(const __grid_constant__ Params P) {
+    pdl_entry();
+    if (*P.err) return;
+    __shared__ int slots[kReduceSlots];
+    __shared__ int sh[40];
+    int b = blockIdx.x;
+    const bool first_core = b < P.n1;
+    if (!first_core) b -= P.n1;
+    const int nb = first_core ? P.n1 : P.n3;
+    const int* H = first_core ? P.H1 : P.H3;
+    const int* pi = first_core ? P.pi1 : P.pi3;
+    const int* rep = first_core ? P.rep_pair : P.rep_row;
+    const int start = H[(int64_t)b * P.nch];
+    const int end = (b + 1 < nb) ? H[(int64_t)(b + 1) * P.nch] : (int)P.nnz;
+    if (start >= end) return;
+    const int t = first_core ? P.bin1_tab[b] : P.bin3_tab[b];
+    const TableDev& T = P.tables[t];
+    const int slice = b - (first_core ? T.base1 : T.base3);
+    const int S = first_core ? T.q1 * T.r1 : T.r2 * T.q3;
+    const int nsub = first_core ? P.split : 1;  // dG1 partials: one per column split
+    const int stride = first_core ? P.qs_max : P.ps_max;
+    const float* buf = first_core ? P.Qbuf : P.Pbuf;
+    float* G = (first_core ? T.G1 : T.G3) + (int64_t)slice * S;
+    // R lane groups share the slots when the slice is narrower than the block
+    const int R = S >= kBwdThreads ? 1 : kBwdThreads / S;
+    const int r = threadIdx.x / (S >= kBwdThreads ? kBwdThreads : S);
+    extern __shared__ float sacc[];  // [ceil(S / blockDim) * blockDim] running sums
+    for (int e = threadIdx.x; e < kMaxAcc13 * kBwdThreads && e < ((S + kBwdThreads - 1) / kBwdThreads) * kBwdThreads;
+         e += blockDim.x)
+        sacc[e] = 0.f;
+    __syncthreads();
+    for (int base = start; base < end;) {
+        // compact up to kReduceSlots / nsub representatives, in segment order
+        int nslot = 0;
+        while (base < end && nslot + (int)blockDim.x * nsub <= kReduceSlots) {
+            const int kk = base + threadIdx.x;
+            const int rv = kk < end ? rep[pi[kk]] : -1;
+            int tot;
+            const int ex = block_scan_excl(rv >= 0 ? 1 : 0, sh, &tot);
+            if (rv >= 0)
+                for (int q = 0; q < nsub; ++q) slots[nslot + ex * nsub + q] = rv * nsub + q;
+            nslot += tot * nsub;
+            base += blockDim.x;
+        }
+        __syncthreads();
+        if (r < R) {
+            const int e0 = threadIdx.x - r * (S >= kBwdThreads ? kBwdThreads : S);
+#pragma unroll 1
+            for (int m = 0; m < kMaxAcc13 && m * kBwdThreads < S; ++m) {
+                const int e = e0 + m * kBwdThreads;
+                if (e < S) {
+                    float a = 0.f;
+#pragma unroll 1
+                    for (int j0 = r; j0 < nslot; j0 += R * kReducePer) {
+                        float v[kReducePer];
+#pragma unroll
+                        for (int u = 0; u < kReducePer; ++u) {
+                            const int j = j0 + u * R;
+                            v[u] = j < nslot ? __ldg(buf + (int64_t)slots[j] * stride + e) : 0.f;
+                        }
+#pragma unroll
+                        for (int u = 0; u < kReducePer; ++u) a += v[u];
+                    }
+                    sacc[m * kBwdThreads + threadIdx.x] += a;
+                }
+            }
+        }
+        __syncthreads();
+    }
+    if (R == 1) {
+        for (int e = threadIdx.x; e < S; e += blockDim.x) G[e] = fmaf(-P.lr, sacc[e], G[e]);
+    } else {
+        // add the R lane groups' sums in group order
+        if (threadIdx.x < S) {
+            float sum = 0.f;
+            for (int rr = 0; rr < R; ++rr) sum += sacc[rr * S + threadIdx.x];
+            G[threadIdx.x] = fmaf(-P.lr, sum, G[threadIdx.x]);
+        }
+    }
+    if (P.slice_stamp && threadIdx.x == 0 && t == 0)
+        P.slice_stamp[first_core ? slice : T.p1 + T.p2 + slice] = P.step + 1;
+}
+
+// ------------------------------------------------------------------ launchers
+
+size_t tile_bwd_smem(const Params& P) {
+    return bwd_layout(P.tile_cap, P.D, P.r1_max, P.N_max, P.g1s_floats, P.dts_floats).total;
+}
+
+int bwd_batch_pairs(int q1, int Ns, int r1) { return bwd_pairs_per_batch(q1, Ns, r1); }
+
+template <int DC, int SPLIT>
+static cudaError_t launch_tile_bwd_dc(const Params& P, cudaStream_t s) {
+    const size_t smem = tile_bwd_smem(P);
+    cudaError_t le = launch_pdl(k_tile_bwd<DC, SPLIT>, dim3((unsigned)P.max_tiles * SPLIT), dim3(kBwdThreads), smem, s, P);
+    if (le != cudaSuccess) return le;
+    return cudaGetLastError();
+}
+
+template <int SPLIT>
+static cudaError_t launch_tile_bwd_split(const Params& P, cudaStream_t s) {
+    switch (P.dclass_all) {
+        case kQ444R32: return launch_tile_bwd_dc<kQ444R32, SPLIT>(P, s);
+        case kQ444R16: return launch_tile_bwd_dc<kQ444R16, SPLIT>(P, s);
+        case kQ444R64: return launch_tile_bwd_dc<kQ444R64, SPLIT>(P, s);
+        case kQ448R64: return launch_tile_bwd_dc<kQ448R64, SPLIT>(P, s);
+        case kDynamic: return launch_tile_bwd_dc<kDynamic, SPLIT>(P, s);
+        default: return launch_tile_bwd_dc<-1, SPLIT>(P, s);
+    }
+}
+
+cudaError_t launch_tile_bwd(const Params& P, cudaStream_t s) {
+    return P.split == 2 ? launch_tile_bwd_split<2>(P, s) : launch_tile_bwd_split<1>(P, s);
+}
+
+cudaError_t launch_reduce13(const Params& P, cudaStream_t s) {
+    const size_t smem = sizeof(float) * (size_t)kBwdThreads *
+                        (size_t)((std::max(P.qs_max, P.ps_max) + kBwdThreads - 1) / kBwdThreads);
+    cudaError_t le = launch_pdl(k_reduce13, dim3(P.n1 + P.n3), dim3(kBwdThreads), smem, s, P);
+    if (le != cudaSuccess) return le;
+    return cudaGetLastError();
+}
+
+template <int SPLIT>
+static cudaError_t set_tile_attrs(int max_smem) {
+    const void* ks[] = {(const void*)k_tile_bwd<kQ444R32, SPLIT>, (const void*)k_tile_bwd<kQ444R16, SPLIT>,
+                        (const void*)k_tile_bwd<kQ444R64, SPLIT>, (const void*)k_tile_bwd<kQ448R64, SPLIT>,
+                        (const void*)k_tile_bwd<kDynamic, SPLIT>, (const void*)k_tile_bwd<-1, SPLIT>};
+    for (const void* k : ks) {
+        cudaError_t e = allow_max_dynamic_smem(k, max_smem);
+        if (e != cudaSuccess) return e;
+    }
+    return cudaSuccess;
+}
+
+cudaError_t set_bwd_attributes(int max_smem) {
+    cudaError_t e = set_tile_attrs<1>(max_smem);
+    if (e == cudaSuccess) e = set_tile_attrs<2>(max_smem);
+    if (e == cudaSuccess) e = allow_max_dynamic_smem((const void*)k_reduce13, max_smem);
+    return e;
+}
+
+}  // namespace ttemb

@@ -1,0 +1,464 @@
+// tt_fwd.cu -- forward contractions and pooling (sm_103a, FP32 FFMA).
+//
+// FBTT README, "Software Cache": a row is computed from the cores by two
+// consecutive small matrix products; the TT-Rec abstract batches them.  Here
+//   T[i1,i2] = G1[i1] (q1 x r1) . G2[i2] (r1 x q2 r2)   once per touched pair,
+// batched per (table, i2) with the G2 slice in shared memory, and
+//   row = T (q1 q2 x r2) . G3[i3] (r2 x q3)            per lookup, pooled per bag
+// in registers (tensorflow/addons EmbeddingBag issue: the pre-pool rows are
+// never materialised).
+#include "tt_dims.cuh"
+
+namespace ttemb {
+
+constexpr int kFwdThreads = 256;
+constexpr int kListCap = 1024;      // touched i1 handled per round
+constexpr int kPoolWarps = 4;       // warps per bag
+constexpr int kMaxDPerLane = 8;     // generic pool path: D <= 256
+
+// ------------------------------------------------------------------ T per pair
+
+struct FwdSmem {
+    int* ulist;
+    int* sh;
+    float* g2s;
+    float* g1s;
+};
+
+constexpr int kG1Floats = 8192;     // G1 rows gathered at once (pairs x q1 r1 floats)
+
+__host__ __device__ inline size_t fwd_smem_bytes(int r1max, int Nmax) {
+    // ulist + sh, G2 slice, G1 rows of up to kG1Floats / (q1 r1) pairs
+    return sizeof(int) * (kListCap + 64) + sizeof(float) * (size_t)r1max * Nmax + sizeof(float) * kG1Floats;
+}
+
+// Touched i1 of pair block [i2][base .. base + kListCap) into ulist; returns the count.
+__device__ __forceinline__ int touched_list(const Params& P, const TableDev& T, int i2, int base, int* ulist,
+                                            int* sh) {
+    const int* fl = P.tflag + T.fbase + (int64_t)i2 * T.p1;
+    const int end = min(T.p1, base + kListCap);
+    const int epoch = *P.epoch;
+    int m = 0;
+    for (int b = base; b < end; b += blockDim.x) {
+        const int i1 = b + threadIdx.x;
+        const int f = (i1 < end) && (fl[i1] == epoch);
+        int tot;
+        const int ex = block_scan_excl(f, sh, &tot);
+        if (f) ulist[m + ex] = i1;
+        m += tot;
+    }
+    return m;
+}
+
+template <class Dm>
+__device__ void fwd_T_group(const Params& P, const TableDev& T, const Dm dm, int i2, const FwdSmem& S) {
+    const int q1 = dm.q1(), r1 = dm.r1(), N = dm.q2() * dm.r2();
+    bool staged = false;
+    for (int base = 0; base < T.p1; base += kListCap) {
+        const int m = touched_list(P, T, i2, base, S.ulist, S.sh);
+        if (m == 0) continue;
+        if (!staged) {
+            const float* src = T.G2 + (int64_t)i2 * r1 * N;
+            if constexpr (Dm::kStatic) stage_f32x4<4>(S.g2s, src, (r1 * N) / 4);
+            else stage_f32<8>(S.g2s, src, r1 * N);
+            staged = true;
+        }
+        if constexpr (Dm::kStatic) {
+            // every compiled class has q1 = 4 and q2 r2 % 8 == 0.  Register tile: 4 rows (j1) x 8
+            // columns per thread, columns cg*4 .. +3 and NN/2 + cg*4 .. +3 (consecutive lanes read
+            // consecutive float4 of the G2 row), PS pairs per pass
+            constexpr int R1 = Dm::r1(), NN = Dm::q2() * Dm::r2();
+            constexpr int CG = NN / 8;
+            constexpr int PS = kFwdThreads / CG;
+            const int cg = threadIdx.x % CG, ps = threadIdx.x / CG;
+            constexpr int GB = kG1Floats / (4 * R1);  // pairs gathered at once
+            for (int g0 = 0; g0 < m; g0 += GB) {
+                const int gn = min(GB, m - g0);
+                __syncthreads();
+                // g1s[u][a][j1] = G1[i1_u][j1][a] for the gn pairs, 8 loads in flight per thread
+                for (int base = 0; base < gn * R1 * 4; base += 8 * kFwdThreads) {
+                    float v[8];
+#pragma unroll
+                    for (int q = 0; q < 8; ++q) {
+                        const int e = base + q * kFwdThreads + threadIdx.x;
+                        v[q] = 0.f;
+                        if (e < gn * R1 * 4) {
+                            const int u = e / (R1 * 4), rem = e - u * (R1 * 4);
+                            v[q] = __ldg(T.G1 + (int64_t)S.ulist[g0 + u] * (4 * R1) + (rem & 3) * R1 + (rem >> 2));
+                        }
+                    }
+#pragma unroll
+                    for (int q = 0; q < 8; ++q) {
+                        const int e = base + q * kFwdThreads + threadIdx.x;
+                        if (e < gn * R1 * 4) S.g1s[e] = v[q];
+                    }
+                }
+                __syncthreads();
+                for (int u0 = 0; u0 < gn; u0 += PS) {
+                    const int u = u0 + ps;
+                    if (u < gn) {
+                        float acc[4][8];
+#pragma unroll
+                        for (int j = 0; j < 4; ++j)
+#pragma unroll
+                            for (int c = 0; c < 8; ++c) acc[j][c] = 0.f;
+                        const float* g1 = S.g1s + u * R1 * 4;
+                        const float* g2 = S.g2s + cg * 4;
+#pragma unroll 8
+                        for (int a = 0; a < R1; ++a) {
+                            const float4 x = *reinterpret_cast<const float4*>(g1 + a * 4);
+                            const float4 y0 = *reinterpret_cast<const float4*>(g2 + a * NN);
+                            const float4 y1 = *reinterpret_cast<const float4*>(g2 + a * NN + NN / 2);
+                            const float xv[4] = {x.x, x.y, x.z, x.w};
+                            const float yv[8] = {y0.x, y0.y, y0.z, y0.w, y1.x, y1.y, y1.z, y1.w};
+#pragma unroll
+                            for (int j = 0; j < 4; ++j)
+#pragma unroll
+                                for (int c = 0; c < 8; ++c) acc[j][c] = fmaf(xv[j], yv[c], acc[j][c]);
+                        }
+                        float* dst = P.Tbuf + T.tbase + ((int64_t)i2 * T.p1 + S.ulist[g0 + u]) * (4 * NN) + cg * 4;
+#pragma unroll
+                        for (int j = 0; j < 4; ++j) {
+                            *reinterpret_cast<float4*>(dst + j * NN) = make_float4(acc[j][0], acc[j][1], acc[j][2], acc[j][3]);
+                            *reinterpret_cast<float4*>(dst + j * NN + NN / 2) = make_float4(acc[j][4], acc[j][5], acc[j][6], acc[j][7]);
+                        }
+                    }
+                }
+            }
+            __syncthreads();
+        } else {
+            __syncthreads();
+            const int64_t total = (int64_t)m * N;
+            for (int64_t e = threadIdx.x; e < total; e += blockDim.x) {
+                const int u = (int)(e / N), jc = (int)(e % N);
+                const int i1 = S.ulist[u];
+                const float* g1 = T.G1 + (int64_t)i1 * q1 * r1;
+                float* dst = P.Tbuf + T.tbase + ((int64_t)i2 * T.p1 + i1) * (int64_t)(q1 * N);
+                for (int j1 = 0; j1 < q1; ++j1) {
+                    float acc = 0.f;
+                    for (int a = 0; a < r1; ++a) acc = fmaf(g1[j1 * r1 + a], S.g2s[a * N + jc], acc);
+                    dst[j1 * N + jc] = acc;
+                }
+            }
+            __syncthreads();
+        }
+    }
+}
+
+template <int DC>
+__global__ void __launch_bounds__(kFwdThreads) k_fwd_T(const __grid_constant__ Params P) {
+    pdl_entry();
+    extern __shared__ __align__(16) unsigned char smraw[];
+    const int g = blockIdx.x;
+    if (g >= P.n2) {  // small path: extra blocks scatter the lookups of one chunk
+        scatter_chunk(P, g - P.n2);
+        return;
+    }
+    const TableDev& T = P.tables[P.bin2_tab[g]];
+    const int i2 = g - T.base2;
+    FwdSmem S;
+    S.ulist = (int*)smraw;
+    S.sh = S.ulist + kListCap;
+    S.g2s = (float*)(S.sh + 64);
+    S.g1s = S.g2s + (size_t)P.r1_max * P.N_max;
+    switch (DC >= 0 ? DC : T.dclass) {
+        case kQ444R32: fwd_T_group(P, T, SDims<4, 4, 4, 32, 32>{}, i2, S); break;
+        case kQ444R16: fwd_T_group(P, T, SDims<4, 4, 4, 16, 16>{}, i2, S); break;
+        case kQ444R64: fwd_T_group(P, T, SDims<4, 4, 4, 64, 64>{}, i2, S); break;
+        case kQ448R64: fwd_T_group(P, T, SDims<4, 4, 8, 64, 64>{}, i2, S); break;
+        default: fwd_T_group(P, T, DDims{T.q1, T.q2, T.q3, T.r1, T.r2}, i2, S); break;
+    }
+}
+
+// ------------------------------------------------------------------ pooling
+
+__device__ __forceinline__ const float* t_of_pair(const Params& P, const TableDev& T, int i2, int i1) {
+    return P.Tbuf + T.tbase + ((int64_t)i2 * T.p1 + i1) * (int64_t)(T.q1 * T.q2 * T.r2);
+}
+
+// Cache slot of `row` (table 0) or -1.
+__device__ __forceinline__ int64_t cache_find(const Params& P, int64_t row) {
+    int64_t a = 0, b = P.cache_n;
+    while (a < b) {
+        const int64_t m = (a + b) >> 1;
+        if (P.cache_rows[m] < row) a = m + 1; else b = m;
+    }
+    return (a < P.cache_n && P.cache_rows[a] == row) ? a : -1;
+}
+
+// Cached value state of one lookup: slot (or -1) and whether it is current.
+__device__ __forceinline__ int64_t cache_probe(const Params& P, const TableDev& T, int i1, int i2, int i3,
+                                               bool& fresh) {
+    fresh = false;
+    if (P.cache_n == 0) return -1;
+    const int64_t row = ((int64_t)i1 * T.p2 + i2) * T.p3 + i3;
+    const int64_t slot = cache_find(P, row);
+    if (slot >= 0) {
+        const int need = max(max(P.slice_stamp[i1], P.slice_stamp[T.p1 + i2]), P.slice_stamp[T.p1 + T.p2 + i3]);
+        fresh = *(volatile const int*)(P.cache_stamp + slot) >= need;
+        __threadfence();  // a refreshed stamp is seen only after its values
+    }
+    return slot;
+}
+
+// Static fast path: lanes = 2 output halves (lj) x 16 contraction lanes (lc);
+// lane (lj, lc) sums c = lc, lc + 16, ... for the outputs j = lj * D/2 + v.
+// After the bag, a reduce-scatter over the 16 lc lanes leaves V = D/32 sums
+// per lane.
+template <class Dm>
+__device__ void pool_bag_static(const Params& P, const TableDev& T, int64_t bag, int64_t lo, int64_t hi,
+                                float* red) {
+    constexpr int Q3 = Dm::q3(), R2 = Dm::r2(), Q12 = Dm::q1() * Dm::q2();
+    constexpr int D = Q12 * Q3, H = D / 2, J12H = Q12 / 2, NC = R2 / 16;
+    const int lane = threadIdx.x & 31, w = threadIdx.x >> 5;
+    const int lc = lane & 15, lj = lane >> 4;
+    float acc[H];
+#pragma unroll
+    for (int v = 0; v < H; ++v) acc[v] = 0.f;
+    for (int64_t n = lo + w; n < hi; n += kPoolWarps) {
+        const int i1 = P.lk_i1[n], i2 = P.lk_i2[n], i3 = P.lk_i3[n];
+        const float s = P.lk_s[n];
+        bool fresh;
+        const int64_t slot = cache_probe(P, T, i1, i2, i3, fresh);
+        if (fresh) {
+            if (lc == 0) {
+                const float* cv = P.cache_vals + slot * D + lj * H;
+#pragma unroll
+                for (int v = 0; v < H; ++v) acc[v] = fmaf(s, __ldcg(cv + v), acc[v]);
+            }
+            continue;
+        }
+        const float* Tp = t_of_pair(P, T, i2, i1) + lj * J12H * R2;
+        const float* g3 = T.G3 + (int64_t)i3 * R2 * Q3;
+        float tv[J12H][NC], gv[NC][Q3];
+#pragma unroll
+        for (int k = 0; k < NC; ++k) {
+            const int c = lc + 16 * k;
+#pragma unroll
+            for (int j = 0; j < J12H; ++j) tv[j][k] = __ldg(Tp + j * R2 + c);
+#pragma unroll
+            for (int j3 = 0; j3 < Q3; j3 += 4) {
+                const float4 x = __ldg(reinterpret_cast<const float4*>(g3 + c * Q3 + j3));
+                gv[k][j3] = x.x; gv[k][j3 + 1] = x.y; gv[k][j3 + 2] = x.z; gv[k][j3 + 3] = x.w;
+            }
+        }
+#pragma unroll
+        for (int j = 0; j < J12H; ++j)
+#pragma unroll
+            for (int j3 = 0; j3 < Q3; ++j3) {
+                float t = 0.f;
+#pragma unroll
+                for (int k = 0; k < NC; ++k) t = fmaf(tv[j][k], gv[k][j3], t);
+                acc[j * Q3 + j3] = fmaf(s, t, acc[j * Q3 + j3]);
+            }
+        if (slot >= 0) {
+            // refresh a stale cached row: each column summed over the 16 lc lanes
+#pragma unroll
+            for (int j = 0; j < J12H; ++j)
+#pragma unroll
+                for (int j3 = 0; j3 < Q3; ++j3) {
+                    float t = 0.f;
+#pragma unroll
+                    for (int k = 0; k < NC; ++k) t = fmaf(tv[j][k], gv[k][j3], t);
+#pragma unroll
+                    for (int o = 8; o >= 1; o >>= 1) t += __shfl_xor_sync(0xffffffffu, t, o);
+                    if (lc == 0) __stcg(P.cache_vals + slot * D + lj * H + j * Q3 + j3, t);
+                }
+            __threadfence();
+            __syncwarp();
+            if (lane == 0) atomicExch(P.cache_stamp + slot, P.step);
+        }
+    }
+    // reduce-scatter over the 16 lc lanes: each stage halves the vector
+#pragma unroll
+    for (int o = 8, len = H; o >= 1; o >>= 1, len >>= 1) {
+        const bool up = (lc & o) != 0;
+#pragma unroll
+        for (int v = 0; v < len / 2; ++v) {
+            const float send = up ? acc[v] : acc[v + len / 2];
+            const float keep = up ? acc[v + len / 2] : acc[v];
+            acc[v] = keep + __shfl_xor_sync(0xffffffffu, send, o);
+        }
+    }
+    constexpr int V = H / 16;
+#pragma unroll
+    for (int v = 0; v < V; ++v) red[w * D + lj * H + lc * V + v] = acc[v];
+    __syncthreads();
+    for (int j = threadIdx.x; j < D; j += blockDim.x) {
+        float sum = 0.f;
+#pragma unroll
+        for (int ww = 0; ww < kPoolWarps; ++ww) sum += red[ww * D + j];
+        P.out[bag * D + j] = sum;
+    }
+}
+
+// Generic path: lanes over output columns, loop over c.
+__device__ void pool_bag_generic(const Params& P, const TableDev& T, int64_t bag, int64_t lo, int64_t hi,
+                                 float* red) {
+    const int lane = threadIdx.x & 31, w = threadIdx.x >> 5;
+    const int q3 = T.q3, r2 = T.r2, D = T.D;
+    float acc[kMaxDPerLane];
+#pragma unroll
+    for (int m = 0; m < kMaxDPerLane; ++m) acc[m] = 0.f;
+    for (int64_t n = lo + w; n < hi; n += kPoolWarps) {
+        const int i1 = P.lk_i1[n], i2 = P.lk_i2[n], i3 = P.lk_i3[n];
+        const float s = P.lk_s[n];
+        bool fresh;
+        const int64_t slot = cache_probe(P, T, i1, i2, i3, fresh);
+        float v[kMaxDPerLane];
+        if (fresh) {
+#pragma unroll
+            for (int m = 0; m < kMaxDPerLane; ++m) {
+                const int j = lane + 32 * m;
+                v[m] = j < D ? __ldcg(P.cache_vals + slot * D + j) : 0.f;
+            }
+        } else {
+            const float* Tp = t_of_pair(P, T, i2, i1);
+            const float* g3 = T.G3 + (int64_t)i3 * r2 * q3;
+#pragma unroll
+            for (int m = 0; m < kMaxDPerLane; ++m) {
+                const int j = lane + 32 * m;
+                float a = 0.f;
+                if (j < D) {
+                    const int j12 = j / q3, j3 = j - j12 * q3;
+                    for (int c = 0; c < r2; ++c) a = fmaf(Tp[j12 * r2 + c], g3[c * q3 + j3], a);
+                }
+                v[m] = a;
+            }
+            if (slot >= 0) {
+#pragma unroll
+                for (int m = 0; m < kMaxDPerLane; ++m) {
+                    const int j = lane + 32 * m;
+                    if (j < D) __stcg(P.cache_vals + slot * D + j, v[m]);
+                }
+                __threadfence();
+                __syncwarp();
+                if (lane == 0) atomicExch(P.cache_stamp + slot, P.step);
+            }
+        }
+#pragma unroll
+        for (int m = 0; m < kMaxDPerLane; ++m) acc[m] = fmaf(s, v[m], acc[m]);
+    }
+#pragma unroll
+    for (int m = 0; m < kMaxDPerLane; ++m) {
+        const int j = lane + 32 * m;
+        if (j < D) red[w * D + j] = acc[m];
+    }
+    __syncthreads();
+    for (int j = threadIdx.x; j < D; j += blockDim.x) {
+        float sum = 0.f;
+        for (int ww = 0; ww < kPoolWarps; ++ww) sum += red[ww * D + j];
+        P.out[bag * D + j] = sum;
+    }
+}
+
+// One block of kPoolWarps warps per bag; the warps share the bag's lookups.
+// DC >= 0: every table of the handle has dimension class DC; DC < 0: per table.
+template <int DC>
+__global__ void __launch_bounds__(kPoolWarps * 32) k_pool(const __grid_constant__ Params P) {
+    pdl_entry();
+    __shared__ float red[kPoolWarps * kMaxD];
+    const int64_t bag = blockIdx.x;
+    if (bag == 0 && threadIdx.x == 0) atomicAdd(P.epoch, 1);  // k_fwd_T has finished reading it
+    const TableDev& T = P.tables[table_of_bag(P, (int)bag)];
+    int64_t lo = P.off[bag], hi = P.off[bag + 1];
+    lo = lo < 0 ? 0 : (lo > P.nnz ? P.nnz : lo);
+    hi = hi < lo ? lo : (hi > P.nnz ? P.nnz : hi);
+    const int dc = DC >= 0 ? DC : T.dclass;
+    switch (dc) {
+        case kQ444R32: pool_bag_static<SDims<4, 4, 4, 32, 32>>(P, T, bag, lo, hi, red); break;
+        case kQ444R16: pool_bag_static<SDims<4, 4, 4, 16, 16>>(P, T, bag, lo, hi, red); break;
+        case kQ444R64: pool_bag_static<SDims<4, 4, 4, 64, 64>>(P, T, bag, lo, hi, red); break;
+        case kQ448R64: pool_bag_static<SDims<4, 4, 8, 64, 64>>(P, T, bag, lo, hi, red); break;
+        default: pool_bag_generic(P, T, bag, lo, hi, red); break;
+    }
+}
+
+// Decompress the cached rows of table 0 (chain product, fp32).
+__global__ void k_cache_fill(const __grid_constant__ Params P) {
+    pdl_entry();
+    const int lane = threadIdx.x & 31;
+    const int64_t slot = (int64_t)blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5);
+    if (slot >= P.cache_n) return;
+    const TableDev& T = P.tables[0];
+    const int64_t row = P.cache_rows[slot];
+    const int64_t p23 = (int64_t)T.p2 * T.p3;
+    const int i1 = (int)(row / p23), i2 = (int)((row / T.p3) % T.p2), i3 = (int)(row % T.p3);
+    const int q2 = T.q2, q3 = T.q3, r1 = T.r1, r2 = T.r2, D = T.D;
+    const float* g1 = T.G1 + (int64_t)i1 * T.q1 * r1;
+    const float* g2 = T.G2 + (int64_t)i2 * r1 * q2 * r2;
+    const float* g3 = T.G3 + (int64_t)i3 * r2 * q3;
+    for (int j = lane; j < D; j += 32) {
+        const int j3 = j % q3, j12 = j / q3, j2 = j12 % q2, j1 = j12 / q2;
+        float acc = 0.f;
+        for (int c = 0; c < r2; ++c) {
+            float tv = 0.f;
+            for (int a = 0; a < r1; ++a) tv = fmaf(g1[j1 * r1 + a], g2[(a * q2 + j2) * r2 + c], tv);
+            acc = fmaf(tv, g3[c * q3 + j3], acc);
+        }
+        P.cache_vals[slot * D + j] = acc;
+    }
+    if (lane == 0) P.cache_stamp[slot] = P.step;
+}
+
+// ------------------------------------------------------------------ launchers
+
+int dim_class_of(int q1, int q2, int q3, int r1, int r2) { return dim_class(q1, q2, q3, r1, r2); }
+
+
+template <int DC>
+static cudaError_t launch_fwd_T_dc(const Params& P, cudaStream_t s) {
+    const size_t smem = fwd_smem_bytes(P.r1_max, P.N_max);
+    cudaError_t le = launch_pdl(k_fwd_T<DC>, dim3(P.n2 + (P.small ? P.nch : 0)), dim3(kFwdThreads), smem, s, P);
+    if (le != cudaSuccess) return le;
+    return cudaGetLastError();
+}
+
+cudaError_t launch_fwd_T(const Params& P, cudaStream_t s) {
+    switch (P.dclass_all) {
+        case kQ444R32: return launch_fwd_T_dc<kQ444R32>(P, s);
+        case kQ444R16: return launch_fwd_T_dc<kQ444R16>(P, s);
+        case kQ444R64: return launch_fwd_T_dc<kQ444R64>(P, s);
+        case kQ448R64: return launch_fwd_T_dc<kQ448R64>(P, s);
+        case kDynamic: return launch_fwd_T_dc<kDynamic>(P, s);
+        default: return launch_fwd_T_dc<-1>(P, s);
+    }
+}
+
+template <int DC>
+static cudaError_t launch_pool_dc(const Params& P, cudaStream_t s) {
+    cudaError_t le = launch_pdl(k_pool<DC>, dim3((unsigned)P.nbags), dim3(kPoolWarps * 32), 0, s, P);
+    if (le != cudaSuccess) return le;
+    return cudaGetLastError();
+}
+
+cudaError_t launch_pool(const Params& P, cudaStream_t s) {
+    switch (P.dclass_all) {
+        case kQ444R32: return launch_pool_dc<kQ444R32>(P, s);
+        case kQ444R16: return launch_pool_dc<kQ444R16>(P, s);
+        case kQ444R64: return launch_pool_dc<kQ444R64>(P, s);
+        case kQ448R64: return launch_pool_dc<kQ448R64>(P, s);
+        case kDynamic: return launch_pool_dc<kDynamic>(P, s);
+        default: return launch_pool_dc<-1>(P, s);
+    }
+}
+
+cudaError_t launch_cache_fill(const Params& P, cudaStream_t s) {
+    const int64_t blocks = (P.cache_n + 7) / 8;
+    cudaError_t le = launch_pdl(k_cache_fill, dim3((unsigned)blocks), dim3(256), 0, s, P);
+    if (le != cudaSuccess) return le;
+    return cudaGetLastError();
+}
+
+cudaError_t set_fwd_attributes(int max_smem) {
+    const void* ks[] = {(const void*)k_fwd_T<kQ444R32>, (const void*)k_fwd_T<kQ444R16>,
+                        (const void*)k_fwd_T<kQ444R64>, (const void*)k_fwd_T<kQ448R64>,
+                        (const void*)k_fwd_T<kDynamic>, (const void*)k_fwd_T<-1>};
+    for (const void* k : ks) {
+        cudaError_t e = allow_max_dynamic_smem(k, max_smem);
+        if (e != cudaSuccess) return e;
+    }
+    return cudaSuccess;
+}
+
+}  // namespace ttemb

@@ -1,26 +1,26 @@
 // tt_internal.cuh -- shared definitions of the TT-EmbeddingBag CUDA library (sm_103a).
 //
-// The forward pass of one call runs these kernels, in stream order:
-//   k_decode_hist   decode i -> (i1,i2,i3), bag id and pooling scale per lookup,
-//                   per-chunk histograms of the i1 and i3 digits
-//   k_scan13        exclusive scans of those histograms (bin-major)
-//   k_scatter13     stable counting-sort scatter by i1 (pi1) and by i3 (pi3);
-//                   per-chunk histogram of i2 over pi1 order
-//   k_scan2_tiles   exclusive scan of the i2 histogram; tiles of <= tile_cap
-//                   lookups inside each (table, i2) group
-//   k_scatter2      stable scatter of pi1 by i2: pi21, ordered by (table, i2, i1, position)
-//   k_tile_fwd      per tile: local sort by (i1, i3, position) -> sigma; partial
-//                   products T = G1[i1] G2[i2] once per (i1, i2) pair -> Tbuf
+// Forward pass of one call, in stream order:
+//   k_decode_small | k_decode_hist   decode i -> (i1,i2,i3), bag id and pooling
+//                   scale per lookup; mark the touched (i1, i2) pairs
+//   grouping for the backward pass (stable counting sorts), either
+//     nnz <= kSmallMaxNnz: per-chunk ranks in k_decode_small, k_scan3_small,
+//                   scatter by extra blocks of k_fwd_T -> pi1 by (i1, pos),
+//                   pi3 by (i3, pos), pi21 by (i2, pos), tiles
+//     larger nnz:   k_scan13, k_scatter13, k_scan2_tiles, k_scatter2 -> pi1,
+//                   pi3, pi21 by (i2, i1, pos) (pairs contiguous), tiles
+//   k_fwd_T         per (table, i2): T = G1[i1] G2[i2] for every touched pair
 //   k_pool          per bag: row = T G3[i3], pooled in registers -> out
 // and the backward pass:
-//   k_tile_bwd      per tile: summed upstream gradient per row, dG3 partial per
-//                   row, dT per pair, dG1 partial per pair, dG2 of the group
-//                   (reduced across the group's tiles by the last tile, which
-//                   applies the G2 update)
-//   k_reduce13      per i1 / i3 slice: sum of the partials in sorted segment
+//   k_tile_bwd      per tile (x column split), sorted in shared memory by
+//                   (i1, i3, pos): summed upstream gradient per row,
+//                   dG3 partial per row, dT per pair, dG1 partial per pair, dG2
+//                   of the group (reduced over the group's tiles by its last
+//                   tile, which applies the G2 update)
+//   k_reduce13      per i1 / i3 slice: sum of the partials in sorted-segment
 //                   order, G1 / G3 update
-// Every sum runs in an order fixed by the sort keys, so results are
-// bitwise reproducible; no floating-point atomics are used.
+// Every sum runs in an order fixed by the sort keys, so results are bitwise
+// reproducible; no floating-point atomics are used.
 #pragma once
 
 #include <cuda_runtime.h>
@@ -36,6 +36,11 @@ constexpr int kScanThreads = 1024;
 constexpr int kTileThreads = 256;
 constexpr int kMaxBinsPerDigit = 6144;  // per-warp rank tables: 8 x bins x 4 B of shared memory
 constexpr int kFieldBits = 20;          // bits per field of the in-tile sort key
+constexpr int kSmallMaxNnz = 12288;     // small path: lookups
+constexpr int kSmallMaxBins = 1024;     // small path: bins per digit
+constexpr int kSmallChunk = 256;        // small path: lookups per decode block (8 warps)
+constexpr int kDecodeOffs = 1024;       // bag offsets staged per decode block
+constexpr int kMaxD = 256;              // largest q1 q2 q3
 
 enum ErrBits { kErrIndex = 1, kErrOffsets = 2, kErrTimeout = 4 };
 
@@ -49,7 +54,9 @@ struct TableDev {
     float* G2;
     float* G3;
     int64_t tbase;  // float offset of this table's dense (i2, i1) block in Tbuf
+    int64_t fbase;  // offset of this table's dense (i2, i1) touched-flag block
     int base1, base2, base3;  // first global bin of each digit
+    int dclass;     // compiled dimension class (tt_dims.cuh)
 };
 
 struct Params {
@@ -66,6 +73,11 @@ struct Params {
     int s2_max;                     // max r1 q2 r2 (dG2 partial stride)
     int tile_cap;                   // max lookups per tile (power of two, <= kTileThreads)
     int r1_max, N_max, q1N_max;     // max r1, q2 r2 and q1 q2 r2 over the tables
+    int p1_max;
+    int split;                      // column splits of r2 in k_tile_bwd (1 or 2)
+    int small;                      // 1: chunk-rank path (nnz <= kSmallMaxNnz); pi21 is then ordered by (i2, pos)
+    int dclass_all;                 // dimension class shared by every table, or -1 (mixed)
+    int g1s_floats, dts_floats;     // k_tile_bwd batch buffers (max over tables, this call's split)
     // call arguments
     const int64_t* idx;
     const int64_t* off;
@@ -85,6 +97,9 @@ struct Params {
     int* lk_i3;
     int* lk_bag;
     float* lk_s;
+    uint16_t* lr1;                  // small path: rank of the lookup in its chunk among equal i1 / i2 / i3
+    uint16_t* lr2;
+    uint16_t* lr3;
     int* H1;                        // [n1][nch]
     int* H3;                        // [n3][nch]
     int* H2;                        // [n2][nch]
@@ -93,17 +108,20 @@ struct Params {
     int* pi21;
     int* sigma;
     int4* tiles;                    // {start, len, group bin, tile index in group}
+    int* tflag;                     // dense touched-pair flags, == *epoch when touched by this call
+    int* epoch;                     // device counter: advanced by k_pool at the end of every forward pass
     int* ntiles;
     int* grp_first;                 // [n2]
     int* grp_ntiles;                // [n2]
     int* grp_done;                  // [n2], zero between calls
     float* Tbuf;
-    int* rep_pair;                  // [nnz] slot of the tile-pair starting at this lookup, or -1
-    int* rep_row;                   // [nnz] slot of the tile-row starting at this lookup, or -1
+    int* rep_pair;                  // [nnz] partial slot of the tile-pair starting at this lookup, or -1
+    int* rep_row;                   // [nnz] partial slot of the tile-row starting at this lookup, or -1
+                                    // (slot = position of that lookup in pi21)
     float* Qbuf;                    // [nnz][qs_max]
     float* Pbuf;                    // [nnz][ps_max]
     float* dG2part;                 // [max_tiles][s2_max]
-    int* counters;                  // [0] tile-row slots, [1] tile-pair slots
+    int* counters;                  // spare device counters
     int* err;
     // hot-row cache (single table)
     const int64_t* cache_rows;      // sorted row ids, or null
@@ -115,6 +133,16 @@ struct Params {
 };
 
 // ---------------------------------------------------------------- helpers
+
+// Programmatic dependent launch: let the next kernel of the stream launch now
+// (its blocks then wait in pdl_wait), and wait until the previous kernel of the
+// stream has completed and its writes are visible.  Both are no-ops for a
+// kernel launched without the programmatic-serialization attribute.  Every
+// kernel calls this before its first global memory access.
+__device__ __forceinline__ void pdl_entry() {
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+    asm volatile("griddepcontrol.wait;" ::: "memory");
+}
 
 __device__ __forceinline__ unsigned lanemask_lt() {
     unsigned m;
@@ -171,24 +199,147 @@ __device__ __forceinline__ void block_bitonic_sort(unsigned long long* keys, int
     __syncthreads();
 }
 
+// Block-wide copy of n floats from global to shared memory with U loads in
+// flight per thread (a plain strided loop would wait for each load in turn).
+template <int U = 8>
+__device__ __forceinline__ void stage_f32(float* dst, const float* src, int n) {
+    for (int base = 0; base < n; base += U * blockDim.x) {
+        float v[U];
+#pragma unroll
+        for (int u = 0; u < U; ++u) {
+            const int i = base + u * blockDim.x + threadIdx.x;
+            v[u] = i < n ? __ldg(src + i) : 0.f;
+        }
+#pragma unroll
+        for (int u = 0; u < U; ++u) {
+            const int i = base + u * blockDim.x + threadIdx.x;
+            if (i < n) dst[i] = v[u];
+        }
+    }
+}
+
+// Same with float4 (dst, src 16-byte aligned, n4 = number of float4).
+template <int U = 4>
+__device__ __forceinline__ void stage_f32x4(float* dst, const float* src, int n4) {
+    const float4* s4 = reinterpret_cast<const float4*>(src);
+    float4* d4 = reinterpret_cast<float4*>(dst);
+    for (int base = 0; base < n4; base += U * blockDim.x) {
+        float4 v[U];
+#pragma unroll
+        for (int u = 0; u < U; ++u) {
+            const int i = base + u * blockDim.x + threadIdx.x;
+            if (i < n4) v[u] = __ldg(s4 + i);
+        }
+#pragma unroll
+        for (int u = 0; u < U; ++u) {
+            const int i = base + u * blockDim.x + threadIdx.x;
+            if (i < n4) d4[i] = v[u];
+        }
+    }
+}
+
 __device__ __forceinline__ int table_of_bag(const Params& P, int bag) {
     return P.ntab == 1 ? 0 : (int)(bag / P.bags_per_table);
 }
 
+// Largest g in [0, nbags) with off[g] <= n (the bag of lookup n when offsets are valid).
+__device__ __forceinline__ int64_t bag_of(const Params& P, int64_t n) {
+    int64_t a = 0, b = P.nbags;
+    while (b - a > 1) {
+        const int64_t m = (a + b) >> 1;
+        if (P.off[m] <= n) a = m; else b = m;
+    }
+    return a;
+}
+
+// Decode lookup n of bag `bag`: slice indices, pooling scale, touched-pair flag.
+__device__ __forceinline__ void decode_lookup(const Params& P, int64_t n, int bag, int& t, int& i1, int& i2,
+                                              int& i3, int epoch) {
+    t = table_of_bag(P, bag);
+    const TableDev& T = P.tables[t];
+    int64_t row = P.idx[n];
+    float s = P.w ? P.w[n] : 1.0f;
+    if (row < 0 || row >= T.E) {
+        atomicOr(P.err, kErrIndex);
+        row = 0;
+        s = 0.0f;
+    }
+    if (P.mean) {
+        const int64_t L = P.off[bag + 1] - P.off[bag];
+        s = s / (float)(L > 0 ? L : 1);
+    }
+    const int64_t p23 = (int64_t)T.p2 * T.p3;
+    i1 = (int)(row / p23);
+    i2 = (int)((row / T.p3) % T.p2);
+    i3 = (int)(row % T.p3);
+    P.lk_i1[n] = i1;
+    P.lk_i2[n] = i2;
+    P.lk_i3[n] = i3;
+    P.lk_bag[n] = bag;
+    P.lk_s[n] = s;
+    P.tflag[T.fbase + (int64_t)i2 * T.p1 + i1] = epoch;
+}
+
+// Small path, chunk c: position = scanned base of (digit, chunk) + rank in chunk.
+__device__ __forceinline__ void scatter_chunk(const Params& P, int c) {
+    const int64_t n = (int64_t)c * kSmallChunk + threadIdx.x;
+    if (threadIdx.x >= kSmallChunk || n >= P.nnz) return;
+    const TableDev& T = P.tables[table_of_bag(P, P.lk_bag[n])];
+    const int d1 = T.base1 + P.lk_i1[n], d2 = T.base2 + P.lk_i2[n], d3 = T.base3 + P.lk_i3[n];
+    P.pi1[P.H1[(int64_t)d1 * P.nch + c] + P.lr1[n]] = (int)n;
+    P.pi21[P.H2[(int64_t)d2 * P.nch + c] + P.lr2[n]] = (int)n;
+    P.pi3[P.H3[(int64_t)d3 * P.nch + c] + P.lr3[n]] = (int)n;
+}
+
 // ---------------------------------------------------------------- launchers
 // Each returns the cudaError_t of its launch.
+
+extern bool g_use_pdl;  // programmatic dependent launch between the library's kernels
+
+// Allow a kernel the largest dynamic shared memory the device permits next to
+// its static shared memory.
+inline cudaError_t allow_max_dynamic_smem(const void* kernel, int max_smem) {
+    cudaFuncAttributes a;
+    cudaError_t e = cudaFuncGetAttributes(&a, kernel);
+    if (e != cudaSuccess) return e;
+    return cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                max_smem - (int)a.sharedSizeBytes);
+}
+
+// Launch with the programmatic-stream-serialization attribute (see pdl_entry).
+template <class... Args>
+inline cudaError_t launch_pdl(void (*kernel)(Args...), dim3 grid, dim3 block, size_t smem, cudaStream_t s,
+                              const Params& P) {
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = grid;
+    cfg.blockDim = block;
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = s;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = g_use_pdl ? 1 : 0;
+    return cudaLaunchKernelEx(&cfg, kernel, P);
+}
+cudaError_t launch_decode_small(const Params& P, cudaStream_t s);
+cudaError_t launch_scan3_small(const Params& P, cudaStream_t s);
 cudaError_t launch_decode_hist(const Params& P, cudaStream_t s);
 cudaError_t launch_scan13(const Params& P, cudaStream_t s);
 cudaError_t launch_scatter13(const Params& P, cudaStream_t s);
 cudaError_t launch_scan2_tiles(const Params& P, cudaStream_t s);
 cudaError_t launch_scatter2(const Params& P, cudaStream_t s);
-cudaError_t launch_tile_fwd(const Params& P, cudaStream_t s);
+cudaError_t launch_fwd_T(const Params& P, cudaStream_t s);
 cudaError_t launch_pool(const Params& P, cudaStream_t s);
 cudaError_t launch_tile_bwd(const Params& P, cudaStream_t s);
 cudaError_t launch_reduce13(const Params& P, cudaStream_t s);
 cudaError_t launch_cache_fill(const Params& P, cudaStream_t s);
 
-size_t tile_fwd_smem(const Params& P);
 size_t tile_bwd_smem(const Params& P);
+cudaError_t set_sort_attributes(int max_smem);
+cudaError_t set_fwd_attributes(int max_smem);
+cudaError_t set_bwd_attributes(int max_smem);
+int bwd_batch_pairs(int q1, int Ns, int r1);
+int dim_class_of(int q1, int q2, int q3, int r1, int r2);
 
 }  // namespace ttemb

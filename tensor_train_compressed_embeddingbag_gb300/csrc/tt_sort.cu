@@ -11,6 +11,8 @@
 // among the chunk's lookups with the same digit with warp match masks and a
 // per-warp count table, so the scatter is stable without atomics on the
 // output positions.
+#include <algorithm>
+
 #include "tt_internal.cuh"
 
 namespace ttemb {
@@ -18,6 +20,7 @@ namespace ttemb {
 // ------------------------------------------------------------------ decode
 
 __global__ void __launch_bounds__(kSortThreads) k_decode_hist(const __grid_constant__ Params P) {
+    pdl_entry();
     extern __shared__ int sm[];
     int* h1 = sm;           // [n1]
     int* h3 = sm + P.n1;    // [n3]
@@ -44,35 +47,9 @@ __global__ void __launch_bounds__(kSortThreads) k_decode_hist(const __grid_const
     const int64_t lo = (int64_t)c * kChunk;
     const int64_t hi = (lo + kChunk < P.nnz) ? lo + kChunk : P.nnz;
     for (int64_t n = lo + threadIdx.x; n < hi; n += blockDim.x) {
-        // bag = largest g with off[g] <= n
-        int64_t a = 0, b = P.nbags;  // invariant: off[a] <= n (if offsets are valid), answer in [a, b)
-        while (b - a > 1) {
-            int64_t m = (a + b) >> 1;
-            if (P.off[m] <= n) a = m; else b = m;
-        }
-        const int bag = (int)a;
-        const int t = table_of_bag(P, bag);
+        int t, i1, i2, i3;
+        decode_lookup(P, n, (int)bag_of(P, n), t, i1, i2, i3, *P.epoch);
         const TableDev& T = P.tables[t];
-        int64_t row = P.idx[n];
-        float s = P.w ? P.w[n] : 1.0f;
-        if (row < 0 || row >= T.E) {
-            atomicOr(P.err, kErrIndex);
-            row = 0;
-            s = 0.0f;
-        }
-        if (P.mean) {
-            const int64_t L = P.off[bag + 1] - P.off[bag];
-            s = s / (float)(L > 0 ? L : 1);
-        }
-        const int64_t p23 = (int64_t)T.p2 * T.p3;
-        const int i1 = (int)(row / p23);
-        const int i2 = (int)((row / T.p3) % T.p2);
-        const int i3 = (int)(row % T.p3);
-        P.lk_i1[n] = i1;
-        P.lk_i2[n] = i2;
-        P.lk_i3[n] = i3;
-        P.lk_bag[n] = bag;
-        P.lk_s[n] = s;
         atomicAdd(&h1[T.base1 + i1], 1);
         atomicAdd(&h3[T.base3 + i3], 1);
     }
@@ -96,6 +73,7 @@ __device__ void scan_inplace(int* a, int64_t L, int* sh) {
 }
 
 __global__ void __launch_bounds__(kScanThreads) k_scan13(const __grid_constant__ Params P) {
+    pdl_entry();
     __shared__ int sh[33];
     scan_inplace(P.H1, (int64_t)P.n1 * P.nch, sh);
     scan_inplace(P.H3, (int64_t)P.n3 * P.nch, sh);
@@ -104,6 +82,7 @@ __global__ void __launch_bounds__(kScanThreads) k_scan13(const __grid_constant__
 // Exclusive scan of H2, then the tiles: each (table, i2) group of `cnt`
 // lookups (contiguous in pi21) is cut into ceil(cnt / tile_cap) tiles.
 __global__ void __launch_bounds__(kScanThreads) k_scan2_tiles(const __grid_constant__ Params P) {
+    pdl_entry();
     __shared__ int sh[33];
     scan_inplace(P.H2, (int64_t)P.n2 * P.nch, sh);
     __syncthreads();
@@ -179,6 +158,7 @@ __device__ void chunk_stable_ranks(int c, int64_t count, int nb, int* cnt, Digit
 }
 
 __global__ void __launch_bounds__(kSortThreads) k_scatter13(const __grid_constant__ Params P) {
+    pdl_entry();
     extern __shared__ int cnt[];
     const int c = blockIdx.x;
     // by i1 -> pi1, and the i2 histogram of pi1 chunks
@@ -199,6 +179,7 @@ __global__ void __launch_bounds__(kSortThreads) k_scatter13(const __grid_constan
 }
 
 __global__ void __launch_bounds__(kSortThreads) k_scatter2(const __grid_constant__ Params P) {
+    pdl_entry();
     extern __shared__ int cnt[];
     const int c = blockIdx.x;
     chunk_stable_ranks(
@@ -210,40 +191,221 @@ __global__ void __launch_bounds__(kSortThreads) k_scatter2(const __grid_constant
         [&](int64_t k, int d, int rank) { P.pi21[P.H2[(int64_t)d * P.nch + c] + rank] = P.pi1[k]; });
 }
 
+// ------------------------------------------------------------------ small path
+//
+// For nnz <= kSmallMaxNnz the three stable counting sorts (by i1, i2 and i3,
+// each over original order) run with chunks of kSmallChunk lookups:
+//   k_decode_small  one block per chunk: decode, and for every digit the
+//                   chunk histogram and each lookup's stable rank among the
+//                   chunk's lookups with the same digit
+//   k_scan3_small   one block per digit: exclusive scan of [bin][chunk]; the
+//                   i2 block also cuts the (table, i2) groups into tiles
+//   scatter_chunk   position = scanned base + rank (run by extra blocks of
+//                   the k_fwd_T launch)
+
+// Bag offsets covering lookups lo .. hi-1 into soff: all of them when they
+// fit, else offsets b0 .. b1 + 1 of the bags of lo and hi - 1.  Returns the
+// number staged (sb[0] = b0), or 0 when the range does not fit (the caller
+// then searches global memory).
+__device__ int stage_bag_offsets(const Params& P, int64_t lo, int64_t hi, int64_t* soff, int64_t* sb, int cap) {
+    if (P.nbags + 1 <= cap) {
+        for (int i = threadIdx.x; i <= P.nbags; i += blockDim.x) soff[i] = P.off[i];
+        if (threadIdx.x == 0) sb[0] = 0;
+        __syncthreads();
+        return (int)(P.nbags + 1);
+    }
+    if (threadIdx.x == 0) sb[0] = bag_of(P, lo);
+    if (threadIdx.x == 32) sb[1] = bag_of(P, hi - 1);
+    __syncthreads();
+    const int64_t b0 = sb[0], nst = sb[1] - b0 + 2;
+    const bool ok = nst >= 2 && nst <= cap;
+    if (ok)
+        for (int i = threadIdx.x; i < nst; i += blockDim.x) soff[i] = P.off[b0 + i];
+    __syncthreads();
+    return ok ? (int)nst : 0;
+}
+
+__device__ __forceinline__ int64_t staged_bag(const int64_t* soff, int64_t b0, int nst, int64_t n) {
+    int a = 0, b = nst - 1;  // largest a < nst - 1 with soff[a] <= n
+    while (b - a > 1) {
+        const int m = (a + b) >> 1;
+        if (soff[m] <= n) a = m; else b = m;
+    }
+    return b0 + a;
+}
+
+__global__ void __launch_bounds__(kSmallChunk) k_decode_small(const __grid_constant__ Params P) {
+    pdl_entry();
+    __shared__ int64_t soff[kDecodeOffs];
+    __shared__ int64_t sb[2];
+    __shared__ int cnt[kSmallChunk / 32][kSmallMaxBins];
+    const int c = blockIdx.x;
+    const int64_t lo = (int64_t)c * kSmallChunk;
+    const int64_t hi = (lo + kSmallChunk < P.nnz) ? lo + kSmallChunk : P.nnz;
+    if (c == 0 && threadIdx.x == 64 && (P.off[0] != 0 || P.off[P.nbags] != P.nnz)) atomicOr(P.err, kErrOffsets);
+    for (int64_t g = (int64_t)c * blockDim.x + threadIdx.x; g < P.nbags; g += (int64_t)gridDim.x * blockDim.x)
+        if (P.off[g] > P.off[g + 1]) atomicOr(P.err, kErrOffsets);
+    const int nst = stage_bag_offsets(P, lo, hi, soff, sb, kDecodeOffs);
+    const int64_t n = lo + threadIdx.x;
+    int d[3] = {-1, -1, -1};
+    if (n < hi) {
+        const int64_t bag = nst ? staged_bag(soff, sb[0], nst, n) : bag_of(P, n);
+        int t, i1, i2, i3;
+        decode_lookup(P, n, (int)bag, t, i1, i2, i3, *P.epoch);
+        const TableDev& T = P.tables[t];
+        d[0] = T.base1 + i1;
+        d[1] = T.base2 + i2;
+        d[2] = T.base3 + i3;
+    }
+    const int lane = threadIdx.x & 31, w = threadIdx.x >> 5;
+    const int nbs[3] = {P.n1, P.n2, P.n3};
+    int* Hs[3] = {P.H1, P.H2, P.H3};
+    uint16_t* lrs[3] = {P.lr1, P.lr2, P.lr3};
+#pragma unroll
+    for (int k = 0; k < 3; ++k) {
+        const int nb = nbs[k];
+        for (int e = threadIdx.x; e < (kSmallChunk / 32) * nb; e += blockDim.x) cnt[e / nb][e % nb] = 0;
+        __syncthreads();
+        const unsigned m = __match_any_sync(0xffffffffu, d[k]);
+        if (d[k] >= 0 && lane == __ffs(m) - 1) cnt[w][d[k]] = __popc(m);
+        __syncthreads();
+        for (int b = threadIdx.x; b < nb; b += blockDim.x) {
+            int run = 0;
+#pragma unroll
+            for (int ww = 0; ww < kSmallChunk / 32; ++ww) {
+                const int v = cnt[ww][b];
+                cnt[ww][b] = run;
+                run += v;
+            }
+            Hs[k][(int64_t)b * P.nch + c] = run;
+        }
+        __syncthreads();
+        if (d[k] >= 0) lrs[k][n] = (uint16_t)(cnt[w][d[k]] + __popc(m & lanemask_lt()));
+        __syncthreads();
+    }
+}
+
+// Block k scans digit k's [bin][chunk] histogram in shared memory; the i2
+// block then cuts each (table, i2) group into tiles of <= tile_cap lookups.
+__global__ void __launch_bounds__(kScanThreads) k_scan3_small(const __grid_constant__ Params P) {
+    pdl_entry();
+    extern __shared__ int sv[];
+    __shared__ int sh[40];
+    const int k = blockIdx.x;
+    const int nb = k == 0 ? P.n1 : (k == 1 ? P.n2 : P.n3);
+    int* H = k == 0 ? P.H1 : (k == 1 ? P.H2 : P.H3);
+    const int L = nb * P.nch;
+    {
+        constexpr int U = 16;  // loads in flight per thread
+        for (int base = 0; base < L; base += U * blockDim.x) {
+            int v[U];
+#pragma unroll
+            for (int u = 0; u < U; ++u) {
+                const int i = base + u * blockDim.x + threadIdx.x;
+                v[u] = i < L ? H[i] : 0;
+            }
+#pragma unroll
+            for (int u = 0; u < U; ++u) {
+                const int i = base + u * blockDim.x + threadIdx.x;
+                if (i < L) sv[i] = v[u];
+            }
+        }
+    }
+    __syncthreads();
+    const int per = (L + blockDim.x - 1) / blockDim.x;
+    const int i0 = threadIdx.x * per, i1 = min(L, i0 + per);
+    int sum = 0;
+    for (int i = i0; i < i1; ++i) sum += sv[i];
+    int total;
+    int run = block_scan_excl(sum, sh, &total);
+    for (int i = i0; i < i1; ++i) {
+        const int v = sv[i];
+        sv[i] = run;
+        run += v;
+    }
+    __syncthreads();
+    for (int i = threadIdx.x; i < L; i += blockDim.x) H[i] = sv[i];
+    if (k != 1) return;
+    const int cap = P.tile_cap;
+    int carry = 0;
+    for (int base = 0; base < nb; base += blockDim.x) {
+        const int g = base + threadIdx.x;
+        int start = 0, cnt = 0, nt = 0;
+        if (g < nb) {
+            start = sv[g * P.nch];
+            cnt = ((g + 1 < nb) ? sv[(g + 1) * P.nch] : (int)P.nnz) - start;
+            nt = (cnt + cap - 1) / cap;
+        }
+        int tot;
+        const int first = carry + block_scan_excl(nt, sh, &tot);
+        if (g < nb) {
+            P.grp_first[g] = first;
+            P.grp_ntiles[g] = nt;
+            for (int t = 0; t < nt; ++t)
+                P.tiles[first + t] = make_int4(start + t * cap, min(cap, cnt - t * cap), g, t);
+        }
+        carry += tot;
+    }
+    if (threadIdx.x == 0) *P.ntiles = carry;
+}
+
 // ------------------------------------------------------------------ launchers
+
+cudaError_t launch_decode_small(const Params& P, cudaStream_t s) {
+    cudaError_t le = launch_pdl(k_decode_small, dim3((unsigned)P.nch), dim3(kSmallChunk), 0, s, P);
+    if (le != cudaSuccess) return le;
+    return cudaGetLastError();
+}
+
+cudaError_t launch_scan3_small(const Params& P, cudaStream_t s) {
+    const int L = std::max(std::max(P.n1, P.n2), P.n3) * P.nch;
+    const size_t smem = sizeof(int) * (size_t)L;
+    cudaError_t le = launch_pdl(k_scan3_small, dim3(3), dim3(kScanThreads), smem, s, P);
+    if (le != cudaSuccess) return le;
+    return cudaGetLastError();
+}
 
 cudaError_t launch_decode_hist(const Params& P, cudaStream_t s) {
     const size_t smem = sizeof(int) * (size_t)(P.n1 + P.n3);
-    cudaError_t e = cudaFuncSetAttribute(k_decode_hist, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
-    if (e != cudaSuccess) return e;
-    k_decode_hist<<<P.nch, kSortThreads, smem, s>>>(P);
+    cudaError_t le = launch_pdl(k_decode_hist, dim3(P.nch), dim3(kSortThreads), smem, s, P);
+    if (le != cudaSuccess) return le;
     return cudaGetLastError();
 }
 
 cudaError_t launch_scan13(const Params& P, cudaStream_t s) {
-    k_scan13<<<1, kScanThreads, 0, s>>>(P);
+    cudaError_t le = launch_pdl(k_scan13, dim3(1), dim3(kScanThreads), 0, s, P);
+    if (le != cudaSuccess) return le;
     return cudaGetLastError();
 }
 
 cudaError_t launch_scatter13(const Params& P, cudaStream_t s) {
     const size_t smem = sizeof(int) * kSortWarps * (size_t)max(P.n1, P.n3);
-    cudaError_t e = cudaFuncSetAttribute(k_scatter13, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
-    if (e != cudaSuccess) return e;
-    k_scatter13<<<P.nch, kSortThreads, smem, s>>>(P);
+    cudaError_t le = launch_pdl(k_scatter13, dim3(P.nch), dim3(kSortThreads), smem, s, P);
+    if (le != cudaSuccess) return le;
     return cudaGetLastError();
 }
 
 cudaError_t launch_scan2_tiles(const Params& P, cudaStream_t s) {
-    k_scan2_tiles<<<1, kScanThreads, 0, s>>>(P);
+    cudaError_t le = launch_pdl(k_scan2_tiles, dim3(1), dim3(kScanThreads), 0, s, P);
+    if (le != cudaSuccess) return le;
     return cudaGetLastError();
 }
 
 cudaError_t launch_scatter2(const Params& P, cudaStream_t s) {
     const size_t smem = sizeof(int) * kSortWarps * (size_t)P.n2;
-    cudaError_t e = cudaFuncSetAttribute(k_scatter2, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
-    if (e != cudaSuccess) return e;
-    k_scatter2<<<P.nch, kSortThreads, smem, s>>>(P);
+    cudaError_t le = launch_pdl(k_scatter2, dim3(P.nch), dim3(kSortThreads), smem, s, P);
+    if (le != cudaSuccess) return le;
     return cudaGetLastError();
+}
+
+cudaError_t set_sort_attributes(int max_smem) {
+    const void* ks[] = {(const void*)k_decode_hist, (const void*)k_scatter13, (const void*)k_scatter2,
+                        (const void*)k_scan3_small};
+    for (const void* k : ks) {
+        cudaError_t e = allow_max_dynamic_smem(k, max_smem);
+        if (e != cudaSuccess) return e;
+    }
+    return cudaSuccess;
 }
 
 }  // namespace ttemb
