@@ -240,6 +240,7 @@ tt_status build_handle(tt_emb* h, int ntab, const tt_table_desc* d) {
         T.fbase = fb;
         fb += (int64_t)T.p1 * T.p2;
         T.dclass = dim_class_of(T.q1, T.q2, T.q3, T.r1, T.r2);
+        T.idx32 = (int64_t)T.p1 * T.p2 * T.p3 < ((int64_t)1 << 31) ? 1 : 0;
         T.base1 = n1; T.base2 = n2; T.base3 = n3;
         n1 += T.p1; n2 += T.p2; n3 += T.p3;
         qs = std::max(qs, T.q1 * T.r1);
@@ -270,6 +271,11 @@ tt_status build_handle(tt_emb* h, int ntab, const tt_table_desc* d) {
         can_split = can_split && T.r2 % 8 == 0 && T.r2 >= 16;
     }
     P.dclass_all = common;
+    {
+        int sms = 0;  // few i2 groups: two k_fwd_T blocks share each group's pairs
+        if (cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, h->device) != cudaSuccess) return TT_ERR_CUDA;
+        P.fwd_split = n2 < 2 * sms ? 2 : 1;
+    }
     P.p1_max = p1m;
     h->split_small = can_split ? 2 : 1;
     // device tables
@@ -485,7 +491,6 @@ tt_status tt_emb_forward(tt_emb* h, const int64_t* indices, int64_t nnz, const i
     } else {
         if (small) {
             q.run("decode", launch_decode_small);
-            q.run("scan3", launch_scan3_small);
         } else {
             q.run("decode_hist", launch_decode_hist);
             q.run("scan13", launch_scan13);

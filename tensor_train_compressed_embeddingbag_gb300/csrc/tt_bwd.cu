@@ -14,7 +14,8 @@
 //   dG2 += G1[i1]^T . dT               (r1 x q2 r2)
 // A column split (SPLIT = 2) gives each of two blocks the columns c of one
 // half of r2: P3, dT and dG2 columns are disjoint, Q is summed over the two
-// halves in k_reduce13.
+// halves when its G1 slice is reduced.  k_reduce13 then reduces every G1 / G3
+// slice in sorted-segment order, one block per slice.
 #include <algorithm>
 
 #include "tt_dims.cuh"
@@ -23,7 +24,6 @@ namespace ttemb {
 
 constexpr int kBwdThreads = 256;
 constexpr int kMaxAcc2 = 64;   // generic path: dG2 accumulators per thread (r1 q2 r2 <= 64 * 256)
-constexpr int kMaxAcc13 = 32;  // k_reduce13: slice <= 32 * 256 floats
 constexpr int kGsUnroll = 4;     // independent gradient rows per thread in flight
 constexpr int kDtUnroll = 4;     // independent dT items per thread in flight
 
@@ -97,6 +97,86 @@ __device__ void load_and_sort_tile(const Params& P, int start, int len, unsigned
         sbag[k] = tbag[k0];
         ss[k] = ts[k0];
     }
+    __syncthreads();
+}
+
+// Sum the dG1 (per tile-pair, over the column splits) or dG3 (per tile-row)
+// partials of one slice in sorted-segment order, then apply the SGD update to
+// the slice (one block per slice, after every tile block).  The slots of the slice are compacted in segment order; thread
+// (lane group r, element e) loads slots j = r, r + R, ... kReducePer at a time
+// and sums them in order, then the R partial sums are added in r order.
+constexpr int kReduceSlots = 1024;   // slots gathered per round
+constexpr int kReducePer = 16;       // loads in flight per thread
+
+__device__ void reduce_slice(const Params& P, int bglob, int* slots, int* sh, float* sacc) {
+    const bool first_core = bglob < P.n1;
+    const int b = first_core ? bglob : bglob - P.n1;
+    const int nb = first_core ? P.n1 : P.n3;
+    const int* H = first_core ? P.H1 : P.H3;
+    const int* pi = first_core ? P.pi1 : P.pi3;
+    const int* rep = first_core ? P.rep_pair : P.rep_row;
+    const int start = H[(int64_t)b * P.nch];
+    const int end = (b + 1 < nb) ? H[(int64_t)(b + 1) * P.nch] : (int)P.nnz;
+    const int t = first_core ? P.bin1_tab[b] : P.bin3_tab[b];
+    const TableDev& T = P.tables[t];
+    const int slice = b - (first_core ? T.base1 : T.base3);
+    const int S = first_core ? T.q1 * T.r1 : T.r2 * T.q3;
+    const int nsub = first_core ? P.split : 1;  // dG1 partials: one per column split
+    const int stride = first_core ? P.qs_max : P.ps_max;
+    const float* buf = first_core ? P.Qbuf : P.Pbuf;
+    float* G = (first_core ? T.G1 : T.G3) + (int64_t)slice * S;
+    const int W = S >= kBwdThreads ? kBwdThreads : S;  // threads per lane group
+    const int R = S >= kBwdThreads ? 1 : kBwdThreads / S;
+    const int r = threadIdx.x / W;
+    const int nacc = ((S + kBwdThreads - 1) / kBwdThreads) * kBwdThreads;
+    for (int e = threadIdx.x; e < nacc; e += blockDim.x) sacc[e] = 0.f;
+    __syncthreads();
+    for (int base = start; base < end;) {
+        int nslot = 0;
+        while (base < end && nslot + (int)blockDim.x * nsub <= kReduceSlots) {
+            const int kk = base + threadIdx.x;
+            const int rv = kk < end ? rep[pi[kk]] : -1;
+            int tot;
+            const int ex = block_scan_excl(rv >= 0 ? 1 : 0, sh, &tot);
+            if (rv >= 0)
+                for (int q = 0; q < nsub; ++q) slots[nslot + ex * nsub + q] = rv * nsub + q;
+            nslot += tot * nsub;
+            base += blockDim.x;
+        }
+        __syncthreads();
+        if (r < R) {
+            const int e0 = threadIdx.x - r * W;
+#pragma unroll 1
+            for (int m = 0; m * kBwdThreads < S; ++m) {
+                const int e = e0 + m * kBwdThreads;
+                if (e < S) {
+                    float a = 0.f;
+#pragma unroll 1
+                    for (int j0 = r; j0 < nslot; j0 += R * kReducePer) {
+                        float v[kReducePer];
+#pragma unroll
+                        for (int u = 0; u < kReducePer; ++u) {
+                            const int j = j0 + u * R;
+                            v[u] = j < nslot ? __ldg(buf + (int64_t)slots[j] * stride + e) : 0.f;
+                        }
+#pragma unroll
+                        for (int u = 0; u < kReducePer; ++u) a += v[u];
+                    }
+                    sacc[m * kBwdThreads + threadIdx.x] += a;
+                }
+            }
+        }
+        __syncthreads();
+    }
+    if (R == 1) {
+        for (int e = threadIdx.x; e < S; e += blockDim.x) G[e] = fmaf(-P.lr, sacc[e], G[e]);
+    } else if (threadIdx.x < S) {
+        float sum = 0.f;  // the R lane groups' sums in group order
+        for (int rr = 0; rr < R; ++rr) sum += sacc[rr * S + threadIdx.x];
+        G[threadIdx.x] = fmaf(-P.lr, sum, G[threadIdx.x]);
+    }
+    if (P.slice_stamp && threadIdx.x == 0 && t == 0)
+        P.slice_stamp[first_core ? slice : T.p1 + T.p2 + slice] = P.step + 1;
     __syncthreads();
 }
 
@@ -467,10 +547,7 @@ __device__ void tile_bwd_body(const Params& P, const TableDev& T, const Dm dm, u
                     }
             }
         }
-        if (nt == 1) {
-            if (P.slice_stamp && threadIdx.x == 0 && t == 0) P.slice_stamp[T.p1 + i2] = P.step + 1;
-            return;
-        }
+        if (nt == 1 && P.slice_stamp && threadIdx.x == 0 && t == 0) P.slice_stamp[T.p1 + i2] = P.step + 1;
     } else {
         // generic dimensions
         float acc2[kMaxAcc2];
@@ -533,33 +610,34 @@ __device__ void tile_bwd_body(const Params& P, const TableDev& T, const Dm dm, u
                 else part[e] = acc2[m];
             }
         }
-        if (nt == 1) {
-            if (P.slice_stamp && threadIdx.x == 0 && t == 0) P.slice_stamp[T.p1 + i2] = P.step + 1;
-            return;
-        }
+        if (nt == 1 && P.slice_stamp && threadIdx.x == 0 && t == 0) P.slice_stamp[T.p1 + i2] = P.step + 1;
     }
 
-    // several tiles in the group: the last one (per split) sums the partials in tile order
+    // every partial of this block is written: publish them before any arrival count
     __threadfence();
     __syncthreads();
+    // several tiles in the group: the last one (per split) sums the dG2 partials in tile order
     const int nt = P.grp_ntiles[g];
-    if (threadIdx.x == 0) sh[42] = (atomicAdd(&P.grp_done[g * SPLIT + sp], 1) == nt - 1);
-    __syncthreads();
-    if (!sh[42]) return;
-    __threadfence();
-    const int first = P.grp_first[g];
-    for (int e = threadIdx.x; e < r1 * Ns; e += blockDim.x) {
-        float sum = 0.f;
-        for (int tt = 0; tt < nt; ++tt)
-            sum += __ldcg(P.dG2part + ((int64_t)(first + tt) * SPLIT + sp) * P.s2_max + e);
-        const int a = e / Ns, jc = e - a * Ns;
-        const int j2 = jc / r2s, c = c0 + (jc - j2 * r2s);
-        const int ga = (a * q2 + j2) * r2 + c;
-        G2p[ga] = fmaf(-P.lr, sum, G2p[ga]);
-    }
-    if (threadIdx.x == 0) {
-        P.grp_done[g * SPLIT + sp] = 0;
-        if (P.slice_stamp && t == 0) P.slice_stamp[T.p1 + i2] = P.step + 1;
+    if (nt > 1) {
+        if (threadIdx.x == 0) sh[42] = (atomicAdd(&P.grp_done[g * SPLIT + sp], 1) == nt - 1);
+        __syncthreads();
+        if (sh[42]) {
+            __threadfence();
+            const int first = P.grp_first[g];
+            for (int e = threadIdx.x; e < r1 * Ns; e += blockDim.x) {
+                float sum = 0.f;
+                for (int tt = 0; tt < nt; ++tt)
+                    sum += __ldcg(P.dG2part + ((int64_t)(first + tt) * SPLIT + sp) * P.s2_max + e);
+                const int a = e / Ns, jc = e - a * Ns;
+                const int j2 = jc / r2s, c = c0 + (jc - j2 * r2s);
+                const int ga = (a * q2 + j2) * r2 + c;
+                G2p[ga] = fmaf(-P.lr, sum, G2p[ga]);
+            }
+            if (threadIdx.x == 0) {
+                P.grp_done[g * SPLIT + sp] = 0;
+                if (P.slice_stamp && t == 0) P.slice_stamp[T.p1 + i2] = P.step + 1;
+            }
+        }
     }
 }
 
@@ -580,95 +658,20 @@ __global__ void __launch_bounds__(kBwdThreads) k_tile_bwd(const __grid_constant_
     }
 }
 
-// Sum the dG1 (per tile-pair, over the column splits) and dG3 (per tile-row)
-// partials of one slice in sorted-segment order, then apply the SGD update.
-// The slots of the slice are compacted in order; thread (lane group r, element
-// e) loads the slots j = r, r + R, ... all at once and sums them in order, then
-// the R partial sums are added in r order.
-constexpr int kReduceSlots = 1024;   // slots gathered per round
-constexpr int kReducePer = 16;       // loads in flight per thread
-
 __global__ void __launch_bounds__(kBwdThreads) k_reduce13(const __grid_constant__ Params P) {
     pdl_entry();
-    if (*P.err) return;
+    if (*P.err) return;  // a device error was recorded: leave every core unchanged
     __shared__ int slots[kReduceSlots];
     __shared__ int sh[40];
-    int b = blockIdx.x;
-    const bool first_core = b < P.n1;
-    if (!first_core) b -= P.n1;
-    const int nb = first_core ? P.n1 : P.n3;
-    const int* H = first_core ? P.H1 : P.H3;
-    const int* pi = first_core ? P.pi1 : P.pi3;
-    const int* rep = first_core ? P.rep_pair : P.rep_row;
-    const int start = H[(int64_t)b * P.nch];
-    const int end = (b + 1 < nb) ? H[(int64_t)(b + 1) * P.nch] : (int)P.nnz;
+    extern __shared__ float sacc[];
+    const int b = blockIdx.x;
+    const int nb = b < P.n1 ? P.n1 : P.n3;
+    const int bb = b < P.n1 ? b : b - P.n1;
+    const int* H = b < P.n1 ? P.H1 : P.H3;
+    const int start = H[(int64_t)bb * P.nch];
+    const int end = (bb + 1 < nb) ? H[(int64_t)(bb + 1) * P.nch] : (int)P.nnz;
     if (start >= end) return;
-    const int t = first_core ? P.bin1_tab[b] : P.bin3_tab[b];
-    const TableDev& T = P.tables[t];
-    const int slice = b - (first_core ? T.base1 : T.base3);
-    const int S = first_core ? T.q1 * T.r1 : T.r2 * T.q3;
-    const int nsub = first_core ? P.split : 1;  // dG1 partials: one per column split
-    const int stride = first_core ? P.qs_max : P.ps_max;
-    const float* buf = first_core ? P.Qbuf : P.Pbuf;
-    float* G = (first_core ? T.G1 : T.G3) + (int64_t)slice * S;
-    // R lane groups share the slots when the slice is narrower than the block
-    const int R = S >= kBwdThreads ? 1 : kBwdThreads / S;
-    const int r = threadIdx.x / (S >= kBwdThreads ? kBwdThreads : S);
-    extern __shared__ float sacc[];  // [ceil(S / blockDim) * blockDim] running sums
-    for (int e = threadIdx.x; e < kMaxAcc13 * kBwdThreads && e < ((S + kBwdThreads - 1) / kBwdThreads) * kBwdThreads;
-         e += blockDim.x)
-        sacc[e] = 0.f;
-    __syncthreads();
-    for (int base = start; base < end;) {
-        // compact up to kReduceSlots / nsub representatives, in segment order
-        int nslot = 0;
-        while (base < end && nslot + (int)blockDim.x * nsub <= kReduceSlots) {
-            const int kk = base + threadIdx.x;
-            const int rv = kk < end ? rep[pi[kk]] : -1;
-            int tot;
-            const int ex = block_scan_excl(rv >= 0 ? 1 : 0, sh, &tot);
-            if (rv >= 0)
-                for (int q = 0; q < nsub; ++q) slots[nslot + ex * nsub + q] = rv * nsub + q;
-            nslot += tot * nsub;
-            base += blockDim.x;
-        }
-        __syncthreads();
-        if (r < R) {
-            const int e0 = threadIdx.x - r * (S >= kBwdThreads ? kBwdThreads : S);
-#pragma unroll 1
-            for (int m = 0; m < kMaxAcc13 && m * kBwdThreads < S; ++m) {
-                const int e = e0 + m * kBwdThreads;
-                if (e < S) {
-                    float a = 0.f;
-#pragma unroll 1
-                    for (int j0 = r; j0 < nslot; j0 += R * kReducePer) {
-                        float v[kReducePer];
-#pragma unroll
-                        for (int u = 0; u < kReducePer; ++u) {
-                            const int j = j0 + u * R;
-                            v[u] = j < nslot ? __ldg(buf + (int64_t)slots[j] * stride + e) : 0.f;
-                        }
-#pragma unroll
-                        for (int u = 0; u < kReducePer; ++u) a += v[u];
-                    }
-                    sacc[m * kBwdThreads + threadIdx.x] += a;
-                }
-            }
-        }
-        __syncthreads();
-    }
-    if (R == 1) {
-        for (int e = threadIdx.x; e < S; e += blockDim.x) G[e] = fmaf(-P.lr, sacc[e], G[e]);
-    } else {
-        // add the R lane groups' sums in group order
-        if (threadIdx.x < S) {
-            float sum = 0.f;
-            for (int rr = 0; rr < R; ++rr) sum += sacc[rr * S + threadIdx.x];
-            G[threadIdx.x] = fmaf(-P.lr, sum, G[threadIdx.x]);
-        }
-    }
-    if (P.slice_stamp && threadIdx.x == 0 && t == 0)
-        P.slice_stamp[first_core ? slice : T.p1 + T.p2 + slice] = P.step + 1;
+    reduce_slice(P, b, slots, sh, sacc);
 }
 
 // ------------------------------------------------------------------ launchers
@@ -703,13 +706,6 @@ cudaError_t launch_tile_bwd(const Params& P, cudaStream_t s) {
     return P.split == 2 ? launch_tile_bwd_split<2>(P, s) : launch_tile_bwd_split<1>(P, s);
 }
 
-cudaError_t launch_reduce13(const Params& P, cudaStream_t s) {
-    const size_t smem = sizeof(float) * (size_t)kBwdThreads *
-                        (size_t)((std::max(P.qs_max, P.ps_max) + kBwdThreads - 1) / kBwdThreads);
-    cudaError_t le = launch_pdl(k_reduce13, dim3(P.n1 + P.n3), dim3(kBwdThreads), smem, s, P);
-    if (le != cudaSuccess) return le;
-    return cudaGetLastError();
-}
 
 template <int SPLIT>
 static cudaError_t set_tile_attrs(int max_smem) {
@@ -721,6 +717,14 @@ static cudaError_t set_tile_attrs(int max_smem) {
         if (e != cudaSuccess) return e;
     }
     return cudaSuccess;
+}
+
+cudaError_t launch_reduce13(const Params& P, cudaStream_t s) {
+    const size_t smem = sizeof(float) * (size_t)kBwdThreads *
+                        (size_t)((std::max(P.qs_max, P.ps_max) + kBwdThreads - 1) / kBwdThreads);
+    cudaError_t le = launch_pdl(k_reduce13, dim3(P.n1 + P.n3), dim3(kBwdThreads), smem, s, P);
+    if (le != cudaSuccess) return le;
+    return cudaGetLastError();
 }
 
 cudaError_t set_bwd_attributes(int max_smem) {

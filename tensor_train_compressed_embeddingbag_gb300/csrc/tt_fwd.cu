@@ -51,11 +51,17 @@ __device__ __forceinline__ int touched_list(const Params& P, const TableDev& T, 
 }
 
 template <class Dm>
-__device__ void fwd_T_group(const Params& P, const TableDev& T, const Dm dm, int i2, const FwdSmem& S) {
+__device__ void fwd_T_group(const Params& P, const TableDev& T, const Dm dm, int i2, int half, FwdSmem S) {
     const int q1 = dm.q1(), r1 = dm.r1(), N = dm.q2() * dm.r2();
     bool staged = false;
+    int* list0 = S.ulist;
     for (int base = 0; base < T.p1; base += kListCap) {
-        const int m = touched_list(P, T, i2, base, S.ulist, S.sh);
+        int m = touched_list(P, T, i2, base, list0, S.sh);
+        if (P.fwd_split == 2) {  // this block takes one half of the touched pairs
+            const int m2 = (m + 1) / 2;
+            S.ulist = list0 + half * m2;
+            m = half ? m - m2 : m2;
+        }
         if (m == 0) continue;
         if (!staged) {
             const float* src = T.G2 + (int64_t)i2 * r1 * N;
@@ -149,9 +155,9 @@ template <int DC>
 __global__ void __launch_bounds__(kFwdThreads) k_fwd_T(const __grid_constant__ Params P) {
     pdl_entry();
     extern __shared__ __align__(16) unsigned char smraw[];
-    const int g = blockIdx.x;
-    if (g >= P.n2) {  // small path: extra blocks scatter the lookups of one chunk
-        scatter_chunk(P, g - P.n2);
+    const int g = blockIdx.x / P.fwd_split, half = blockIdx.x % P.fwd_split;
+    if ((int)blockIdx.x >= P.n2 * P.fwd_split) {  // small path: three extra blocks scan the grouping histograms
+        scan_digit_block(P, blockIdx.x - P.n2 * P.fwd_split, (int*)smraw);
         return;
     }
     const TableDev& T = P.tables[P.bin2_tab[g]];
@@ -162,11 +168,11 @@ __global__ void __launch_bounds__(kFwdThreads) k_fwd_T(const __grid_constant__ P
     S.g2s = (float*)(S.sh + 64);
     S.g1s = S.g2s + (size_t)P.r1_max * P.N_max;
     switch (DC >= 0 ? DC : T.dclass) {
-        case kQ444R32: fwd_T_group(P, T, SDims<4, 4, 4, 32, 32>{}, i2, S); break;
-        case kQ444R16: fwd_T_group(P, T, SDims<4, 4, 4, 16, 16>{}, i2, S); break;
-        case kQ444R64: fwd_T_group(P, T, SDims<4, 4, 4, 64, 64>{}, i2, S); break;
-        case kQ448R64: fwd_T_group(P, T, SDims<4, 4, 8, 64, 64>{}, i2, S); break;
-        default: fwd_T_group(P, T, DDims{T.q1, T.q2, T.q3, T.r1, T.r2}, i2, S); break;
+        case kQ444R32: fwd_T_group(P, T, SDims<4, 4, 4, 32, 32>{}, i2, half, S); break;
+        case kQ444R16: fwd_T_group(P, T, SDims<4, 4, 4, 16, 16>{}, i2, half, S); break;
+        case kQ444R64: fwd_T_group(P, T, SDims<4, 4, 4, 64, 64>{}, i2, half, S); break;
+        case kQ448R64: fwd_T_group(P, T, SDims<4, 4, 8, 64, 64>{}, i2, half, S); break;
+        default: fwd_T_group(P, T, DDims{T.q1, T.q2, T.q3, T.r1, T.r2}, i2, half, S); break;
     }
 }
 
@@ -215,44 +221,77 @@ __device__ void pool_bag_static(const Params& P, const TableDev& T, int64_t bag,
     float acc[H];
 #pragma unroll
     for (int v = 0; v < H; ++v) acc[v] = 0.f;
-    for (int64_t n = lo + w; n < hi; n += kPoolWarps) {
-        const int i1 = P.lk_i1[n], i2 = P.lk_i2[n], i3 = P.lk_i3[n];
-        const float s = P.lk_s[n];
-        bool fresh;
-        const int64_t slot = cache_probe(P, T, i1, i2, i3, fresh);
-        if (fresh) {
-            if (lc == 0) {
-                const float* cv = P.cache_vals + slot * D + lj * H;
+    if (P.cache_n == 0) {
+        // two lookups per warp in flight: indices of both, then their T and G3 values
+        for (int64_t n = lo + w; n < hi; n += 2 * kPoolWarps) {
+            const int64_t n2 = n + kPoolWarps;
+            const bool two = n2 < hi;
+            const int i1a = P.lk_i1[n], i2a = P.lk_i2[n], i3a = P.lk_i3[n];
+            const float sa = P.lk_s[n];
+            const int i1b = two ? P.lk_i1[n2] : i1a, i2b = two ? P.lk_i2[n2] : i2a, i3b = two ? P.lk_i3[n2] : i3a;
+            const float sb = two ? P.lk_s[n2] : 0.f;
+            const float* Tpa = t_of_pair(P, T, i2a, i1a) + lj * J12H * R2;
+            const float* Tpb = t_of_pair(P, T, i2b, i1b) + lj * J12H * R2;
+            const float* g3a = T.G3 + (int64_t)i3a * R2 * Q3;
+            const float* g3b = T.G3 + (int64_t)i3b * R2 * Q3;
+            float ta[J12H][NC], tb[J12H][NC], ga[NC][Q3], gb[NC][Q3];
 #pragma unroll
-                for (int v = 0; v < H; ++v) acc[v] = fmaf(s, __ldcg(cv + v), acc[v]);
+            for (int k = 0; k < NC; ++k) {
+                const int c = lc + 16 * k;
+#pragma unroll
+                for (int j = 0; j < J12H; ++j) {
+                    ta[j][k] = __ldg(Tpa + j * R2 + c);
+                    tb[j][k] = __ldg(Tpb + j * R2 + c);
+                }
+#pragma unroll
+                for (int j3 = 0; j3 < Q3; j3 += 4) {
+                    const float4 x = __ldg(reinterpret_cast<const float4*>(g3a + c * Q3 + j3));
+                    const float4 y = __ldg(reinterpret_cast<const float4*>(g3b + c * Q3 + j3));
+                    ga[k][j3] = x.x; ga[k][j3 + 1] = x.y; ga[k][j3 + 2] = x.z; ga[k][j3 + 3] = x.w;
+                    gb[k][j3] = y.x; gb[k][j3 + 1] = y.y; gb[k][j3 + 2] = y.z; gb[k][j3 + 3] = y.w;
+                }
             }
-            continue;
+#pragma unroll
+            for (int j = 0; j < J12H; ++j)
+#pragma unroll
+                for (int j3 = 0; j3 < Q3; ++j3) {
+                    float x = 0.f, y = 0.f;
+#pragma unroll
+                    for (int k = 0; k < NC; ++k) {
+                        x = fmaf(ta[j][k], ga[k][j3], x);
+                        y = fmaf(tb[j][k], gb[k][j3], y);
+                    }
+                    acc[j * Q3 + j3] = fmaf(sb, y, fmaf(sa, x, acc[j * Q3 + j3]));
+                }
         }
-        const float* Tp = t_of_pair(P, T, i2, i1) + lj * J12H * R2;
-        const float* g3 = T.G3 + (int64_t)i3 * R2 * Q3;
-        float tv[J12H][NC], gv[NC][Q3];
+    } else {
+        for (int64_t n = lo + w; n < hi; n += kPoolWarps) {
+            const int i1 = P.lk_i1[n], i2 = P.lk_i2[n], i3 = P.lk_i3[n];
+            const float s = P.lk_s[n];
+            bool fresh;
+            const int64_t slot = cache_probe(P, T, i1, i2, i3, fresh);
+            if (fresh) {
+                if (lc == 0) {
+                    const float* cv = P.cache_vals + slot * D + lj * H;
 #pragma unroll
-        for (int k = 0; k < NC; ++k) {
-            const int c = lc + 16 * k;
-#pragma unroll
-            for (int j = 0; j < J12H; ++j) tv[j][k] = __ldg(Tp + j * R2 + c);
-#pragma unroll
-            for (int j3 = 0; j3 < Q3; j3 += 4) {
-                const float4 x = __ldg(reinterpret_cast<const float4*>(g3 + c * Q3 + j3));
-                gv[k][j3] = x.x; gv[k][j3 + 1] = x.y; gv[k][j3 + 2] = x.z; gv[k][j3 + 3] = x.w;
+                    for (int v = 0; v < H; ++v) acc[v] = fmaf(s, __ldcg(cv + v), acc[v]);
+                }
+                continue;
             }
-        }
+            const float* Tp = t_of_pair(P, T, i2, i1) + lj * J12H * R2;
+            const float* g3 = T.G3 + (int64_t)i3 * R2 * Q3;
+            float tv[J12H][NC], gv[NC][Q3];
 #pragma unroll
-        for (int j = 0; j < J12H; ++j)
+            for (int k = 0; k < NC; ++k) {
+                const int c = lc + 16 * k;
 #pragma unroll
-            for (int j3 = 0; j3 < Q3; ++j3) {
-                float t = 0.f;
+                for (int j = 0; j < J12H; ++j) tv[j][k] = __ldg(Tp + j * R2 + c);
 #pragma unroll
-                for (int k = 0; k < NC; ++k) t = fmaf(tv[j][k], gv[k][j3], t);
-                acc[j * Q3 + j3] = fmaf(s, t, acc[j * Q3 + j3]);
+                for (int j3 = 0; j3 < Q3; j3 += 4) {
+                    const float4 x = __ldg(reinterpret_cast<const float4*>(g3 + c * Q3 + j3));
+                    gv[k][j3] = x.x; gv[k][j3 + 1] = x.y; gv[k][j3 + 2] = x.z; gv[k][j3 + 3] = x.w;
+                }
             }
-        if (slot >= 0) {
-            // refresh a stale cached row: each column summed over the 16 lc lanes
 #pragma unroll
             for (int j = 0; j < J12H; ++j)
 #pragma unroll
@@ -260,13 +299,25 @@ __device__ void pool_bag_static(const Params& P, const TableDev& T, int64_t bag,
                     float t = 0.f;
 #pragma unroll
                     for (int k = 0; k < NC; ++k) t = fmaf(tv[j][k], gv[k][j3], t);
-#pragma unroll
-                    for (int o = 8; o >= 1; o >>= 1) t += __shfl_xor_sync(0xffffffffu, t, o);
-                    if (lc == 0) __stcg(P.cache_vals + slot * D + lj * H + j * Q3 + j3, t);
+                    acc[j * Q3 + j3] = fmaf(s, t, acc[j * Q3 + j3]);
                 }
-            __threadfence();
-            __syncwarp();
-            if (lane == 0) atomicExch(P.cache_stamp + slot, P.step);
+            if (slot >= 0) {
+                // refresh a stale cached row: each column summed over the 16 lc lanes
+#pragma unroll
+                for (int j = 0; j < J12H; ++j)
+#pragma unroll
+                    for (int j3 = 0; j3 < Q3; ++j3) {
+                        float t = 0.f;
+#pragma unroll
+                        for (int k = 0; k < NC; ++k) t = fmaf(tv[j][k], gv[k][j3], t);
+#pragma unroll
+                        for (int o = 8; o >= 1; o >>= 1) t += __shfl_xor_sync(0xffffffffu, t, o);
+                        if (lc == 0) __stcg(P.cache_vals + slot * D + lj * H + j * Q3 + j3, t);
+                    }
+                __threadfence();
+                __syncwarp();
+                if (lane == 0) atomicExch(P.cache_stamp + slot, P.step);
+            }
         }
     }
     // reduce-scatter over the 16 lc lanes: each stage halves the vector
@@ -359,6 +410,10 @@ __global__ void __launch_bounds__(kPoolWarps * 32) k_pool(const __grid_constant_
     pdl_entry();
     __shared__ float red[kPoolWarps * kMaxD];
     const int64_t bag = blockIdx.x;
+    if (bag >= P.nbags) {  // small path: extra blocks scatter the lookups of one chunk
+        scatter_chunk(P, (int)(bag - P.nbags));
+        return;
+    }
     if (bag == 0 && threadIdx.x == 0) atomicAdd(P.epoch, 1);  // k_fwd_T has finished reading it
     const TableDev& T = P.tables[table_of_bag(P, (int)bag)];
     int64_t lo = P.off[bag], hi = P.off[bag + 1];
@@ -409,7 +464,7 @@ int dim_class_of(int q1, int q2, int q3, int r1, int r2) { return dim_class(q1, 
 template <int DC>
 static cudaError_t launch_fwd_T_dc(const Params& P, cudaStream_t s) {
     const size_t smem = fwd_smem_bytes(P.r1_max, P.N_max);
-    cudaError_t le = launch_pdl(k_fwd_T<DC>, dim3(P.n2 + (P.small ? P.nch : 0)), dim3(kFwdThreads), smem, s, P);
+    cudaError_t le = launch_pdl(k_fwd_T<DC>, dim3(P.n2 * P.fwd_split + (P.small ? 3 : 0)), dim3(kFwdThreads), smem, s, P);
     if (le != cudaSuccess) return le;
     return cudaGetLastError();
 }
@@ -427,7 +482,7 @@ cudaError_t launch_fwd_T(const Params& P, cudaStream_t s) {
 
 template <int DC>
 static cudaError_t launch_pool_dc(const Params& P, cudaStream_t s) {
-    cudaError_t le = launch_pdl(k_pool<DC>, dim3((unsigned)P.nbags), dim3(kPoolWarps * 32), 0, s, P);
+    cudaError_t le = launch_pdl(k_pool<DC>, dim3((unsigned)(P.nbags + (P.small ? P.nch : 0))), dim3(kPoolWarps * 32), 0, s, P);
     if (le != cudaSuccess) return le;
     return cudaGetLastError();
 }

@@ -4,8 +4,8 @@
 //   k_decode_small | k_decode_hist   decode i -> (i1,i2,i3), bag id and pooling
 //                   scale per lookup; mark the touched (i1, i2) pairs
 //   grouping for the backward pass (stable counting sorts), either
-//     nnz <= kSmallMaxNnz: per-chunk ranks in k_decode_small, k_scan3_small,
-//                   scatter by extra blocks of k_fwd_T -> pi1 by (i1, pos),
+//     nnz <= kSmallMaxNnz: per-chunk ranks in k_decode_small, scans by extra
+//                   blocks of k_fwd_T, scatter by extra blocks of k_pool -> pi1 by (i1, pos),
 //                   pi3 by (i3, pos), pi21 by (i2, pos), tiles
 //     larger nnz:   k_scan13, k_scatter13, k_scan2_tiles, k_scatter2 -> pi1,
 //                   pi3, pi21 by (i2, i1, pos) (pairs contiguous), tiles
@@ -57,6 +57,7 @@ struct TableDev {
     int64_t fbase;  // offset of this table's dense (i2, i1) touched-flag block
     int base1, base2, base3;  // first global bin of each digit
     int dclass;     // compiled dimension class (tt_dims.cuh)
+    int idx32;      // p1 p2 p3 < 2^31: rows decode with 32-bit arithmetic
 };
 
 struct Params {
@@ -77,6 +78,7 @@ struct Params {
     int split;                      // column splits of r2 in k_tile_bwd (1 or 2)
     int small;                      // 1: chunk-rank path (nnz <= kSmallMaxNnz); pi21 is then ordered by (i2, pos)
     int dclass_all;                 // dimension class shared by every table, or -1 (mixed)
+    int fwd_split;                  // k_fwd_T blocks per (table, i2) group (1 or 2)
     int g1s_floats, dts_floats;     // k_tile_bwd batch buffers (max over tables, this call's split)
     // call arguments
     const int64_t* idx;
@@ -268,10 +270,17 @@ __device__ __forceinline__ void decode_lookup(const Params& P, int64_t n, int ba
         const int64_t L = P.off[bag + 1] - P.off[bag];
         s = s / (float)(L > 0 ? L : 1);
     }
-    const int64_t p23 = (int64_t)T.p2 * T.p3;
-    i1 = (int)(row / p23);
-    i2 = (int)((row / T.p3) % T.p2);
-    i3 = (int)(row % T.p3);
+    if (T.idx32) {
+        const unsigned r = (unsigned)row, p3 = (unsigned)T.p3, q = r / p3;
+        i3 = (int)(r - q * p3);
+        i2 = (int)(q % (unsigned)T.p2);
+        i1 = (int)(q / (unsigned)T.p2);
+    } else {
+        const int64_t p23 = (int64_t)T.p2 * T.p3;
+        i1 = (int)(row / p23);
+        i2 = (int)((row / T.p3) % T.p2);
+        i3 = (int)(row % T.p3);
+    }
     P.lk_i1[n] = i1;
     P.lk_i2[n] = i2;
     P.lk_i3[n] = i3;
@@ -282,13 +291,73 @@ __device__ __forceinline__ void decode_lookup(const Params& P, int64_t n, int ba
 
 // Small path, chunk c: position = scanned base of (digit, chunk) + rank in chunk.
 __device__ __forceinline__ void scatter_chunk(const Params& P, int c) {
-    const int64_t n = (int64_t)c * kSmallChunk + threadIdx.x;
-    if (threadIdx.x >= kSmallChunk || n >= P.nnz) return;
-    const TableDev& T = P.tables[table_of_bag(P, P.lk_bag[n])];
-    const int d1 = T.base1 + P.lk_i1[n], d2 = T.base2 + P.lk_i2[n], d3 = T.base3 + P.lk_i3[n];
-    P.pi1[P.H1[(int64_t)d1 * P.nch + c] + P.lr1[n]] = (int)n;
-    P.pi21[P.H2[(int64_t)d2 * P.nch + c] + P.lr2[n]] = (int)n;
-    P.pi3[P.H3[(int64_t)d3 * P.nch + c] + P.lr3[n]] = (int)n;
+    const int64_t lo = (int64_t)c * kSmallChunk;
+    const int64_t hi = (lo + kSmallChunk < P.nnz) ? lo + kSmallChunk : P.nnz;
+    for (int64_t n = lo + threadIdx.x; n < hi; n += blockDim.x) {
+        const TableDev& T = P.tables[table_of_bag(P, P.lk_bag[n])];
+        const int d1 = T.base1 + P.lk_i1[n], d2 = T.base2 + P.lk_i2[n], d3 = T.base3 + P.lk_i3[n];
+        P.pi1[P.H1[(int64_t)d1 * P.nch + c] + P.lr1[n]] = (int)n;
+        P.pi21[P.H2[(int64_t)d2 * P.nch + c] + P.lr2[n]] = (int)n;
+        P.pi3[P.H3[(int64_t)d3 * P.nch + c] + P.lr3[n]] = (int)n;
+    }
+}
+
+// Small path: exclusive scan of digit k's [bin][chunk] histogram (k = 0: i1,
+// 1: i2, 2: i3) by one block, in place in global memory: each thread owns a
+// contiguous range, sums it (16 loads in flight), the block scans the sums,
+// and each thread rewrites its range.  The i2 block then cuts every
+// (table, i2) group into tiles of <= tile_cap lookups.
+__device__ __forceinline__ void scan_digit_block(const Params& P, int k, int* sh) {
+    constexpr int U = 16;
+    const int nb = k == 0 ? P.n1 : (k == 1 ? P.n2 : P.n3);
+    int* H = k == 0 ? P.H1 : (k == 1 ? P.H2 : P.H3);
+    const int L = nb * P.nch;
+    const int per = (L + blockDim.x - 1) / blockDim.x;
+    const int i0 = min(L, (int)threadIdx.x * per), i1 = min(L, i0 + per);
+    int sum = 0;
+    for (int base = i0; base < i1; base += U) {
+        int v[U];
+#pragma unroll
+        for (int u = 0; u < U; ++u) v[u] = base + u < i1 ? H[base + u] : 0;
+#pragma unroll
+        for (int u = 0; u < U; ++u) sum += v[u];
+    }
+    int total;
+    int run = block_scan_excl(sum, sh, &total);
+    for (int base = i0; base < i1; base += U) {
+        int v[U];
+#pragma unroll
+        for (int u = 0; u < U; ++u) v[u] = base + u < i1 ? H[base + u] : 0;
+#pragma unroll
+        for (int u = 0; u < U; ++u)
+            if (base + u < i1) {
+                H[base + u] = run;
+                run += v[u];
+            }
+    }
+    if (k != 1) return;
+    __syncthreads();  // the block's writes of H are visible to the block after this
+    const int cap = P.tile_cap;
+    int carry = 0;
+    for (int base = 0; base < nb; base += blockDim.x) {
+        const int g = base + threadIdx.x;
+        int start = 0, cnt = 0, nt = 0;
+        if (g < nb) {
+            start = H[g * P.nch];
+            cnt = ((g + 1 < nb) ? H[(g + 1) * P.nch] : (int)P.nnz) - start;
+            nt = (cnt + cap - 1) / cap;
+        }
+        int tot;
+        const int first = carry + block_scan_excl(nt, sh, &tot);
+        if (g < nb) {
+            P.grp_first[g] = first;
+            P.grp_ntiles[g] = nt;
+            for (int t = 0; t < nt; ++t)
+                P.tiles[first + t] = make_int4(start + t * cap, min(cap, cnt - t * cap), g, t);
+        }
+        carry += tot;
+    }
+    if (threadIdx.x == 0) *P.ntiles = carry;
 }
 
 // ---------------------------------------------------------------- launchers
@@ -323,7 +392,6 @@ inline cudaError_t launch_pdl(void (*kernel)(Args...), dim3 grid, dim3 block, si
     return cudaLaunchKernelEx(&cfg, kernel, P);
 }
 cudaError_t launch_decode_small(const Params& P, cudaStream_t s);
-cudaError_t launch_scan3_small(const Params& P, cudaStream_t s);
 cudaError_t launch_decode_hist(const Params& P, cudaStream_t s);
 cudaError_t launch_scan13(const Params& P, cudaStream_t s);
 cudaError_t launch_scatter13(const Params& P, cudaStream_t s);

@@ -198,10 +198,11 @@ __global__ void __launch_bounds__(kSortThreads) k_scatter2(const __grid_constant
 //   k_decode_small  one block per chunk: decode, and for every digit the
 //                   chunk histogram and each lookup's stable rank among the
 //                   chunk's lookups with the same digit
-//   k_scan3_small   one block per digit: exclusive scan of [bin][chunk]; the
-//                   i2 block also cuts the (table, i2) groups into tiles
-//   scatter_chunk   position = scanned base + rank (run by extra blocks of
-//                   the k_fwd_T launch)
+//   scan_digit_block  one block per digit: exclusive scan of [bin][chunk]; the
+//                   i2 block also cuts the (table, i2) groups into tiles (run by
+//                   three extra blocks of the k_fwd_T launch)
+//   scatter_chunk   position = scanned base + rank (run by extra blocks of the
+//                   k_pool launch)
 
 // Bag offsets covering lookups lo .. hi-1 into soff: all of them when they
 // fit, else offsets b0 .. b1 + 1 of the bags of lo and hi - 1.  Returns the
@@ -209,7 +210,20 @@ __global__ void __launch_bounds__(kSortThreads) k_scatter2(const __grid_constant
 // then searches global memory).
 __device__ int stage_bag_offsets(const Params& P, int64_t lo, int64_t hi, int64_t* soff, int64_t* sb, int cap) {
     if (P.nbags + 1 <= cap) {
-        for (int i = threadIdx.x; i <= P.nbags; i += blockDim.x) soff[i] = P.off[i];
+        const int nst = (int)(P.nbags + 1);
+        for (int base = 0; base < nst; base += 4 * blockDim.x) {  // 4 loads in flight per thread
+            int64_t v[4];
+#pragma unroll
+            for (int u = 0; u < 4; ++u) {
+                const int i = base + u * blockDim.x + threadIdx.x;
+                v[u] = i < nst ? P.off[i] : 0;
+            }
+#pragma unroll
+            for (int u = 0; u < 4; ++u) {
+                const int i = base + u * blockDim.x + threadIdx.x;
+                if (i < nst) soff[i] = v[u];
+            }
+        }
         if (threadIdx.x == 0) sb[0] = 0;
         __syncthreads();
         return (int)(P.nbags + 1);
@@ -285,82 +299,10 @@ __global__ void __launch_bounds__(kSmallChunk) k_decode_small(const __grid_const
     }
 }
 
-// Block k scans digit k's [bin][chunk] histogram in shared memory; the i2
-// block then cuts each (table, i2) group into tiles of <= tile_cap lookups.
-__global__ void __launch_bounds__(kScanThreads) k_scan3_small(const __grid_constant__ Params P) {
-    pdl_entry();
-    extern __shared__ int sv[];
-    __shared__ int sh[40];
-    const int k = blockIdx.x;
-    const int nb = k == 0 ? P.n1 : (k == 1 ? P.n2 : P.n3);
-    int* H = k == 0 ? P.H1 : (k == 1 ? P.H2 : P.H3);
-    const int L = nb * P.nch;
-    {
-        constexpr int U = 16;  // loads in flight per thread
-        for (int base = 0; base < L; base += U * blockDim.x) {
-            int v[U];
-#pragma unroll
-            for (int u = 0; u < U; ++u) {
-                const int i = base + u * blockDim.x + threadIdx.x;
-                v[u] = i < L ? H[i] : 0;
-            }
-#pragma unroll
-            for (int u = 0; u < U; ++u) {
-                const int i = base + u * blockDim.x + threadIdx.x;
-                if (i < L) sv[i] = v[u];
-            }
-        }
-    }
-    __syncthreads();
-    const int per = (L + blockDim.x - 1) / blockDim.x;
-    const int i0 = threadIdx.x * per, i1 = min(L, i0 + per);
-    int sum = 0;
-    for (int i = i0; i < i1; ++i) sum += sv[i];
-    int total;
-    int run = block_scan_excl(sum, sh, &total);
-    for (int i = i0; i < i1; ++i) {
-        const int v = sv[i];
-        sv[i] = run;
-        run += v;
-    }
-    __syncthreads();
-    for (int i = threadIdx.x; i < L; i += blockDim.x) H[i] = sv[i];
-    if (k != 1) return;
-    const int cap = P.tile_cap;
-    int carry = 0;
-    for (int base = 0; base < nb; base += blockDim.x) {
-        const int g = base + threadIdx.x;
-        int start = 0, cnt = 0, nt = 0;
-        if (g < nb) {
-            start = sv[g * P.nch];
-            cnt = ((g + 1 < nb) ? sv[(g + 1) * P.nch] : (int)P.nnz) - start;
-            nt = (cnt + cap - 1) / cap;
-        }
-        int tot;
-        const int first = carry + block_scan_excl(nt, sh, &tot);
-        if (g < nb) {
-            P.grp_first[g] = first;
-            P.grp_ntiles[g] = nt;
-            for (int t = 0; t < nt; ++t)
-                P.tiles[first + t] = make_int4(start + t * cap, min(cap, cnt - t * cap), g, t);
-        }
-        carry += tot;
-    }
-    if (threadIdx.x == 0) *P.ntiles = carry;
-}
-
 // ------------------------------------------------------------------ launchers
 
 cudaError_t launch_decode_small(const Params& P, cudaStream_t s) {
     cudaError_t le = launch_pdl(k_decode_small, dim3((unsigned)P.nch), dim3(kSmallChunk), 0, s, P);
-    if (le != cudaSuccess) return le;
-    return cudaGetLastError();
-}
-
-cudaError_t launch_scan3_small(const Params& P, cudaStream_t s) {
-    const int L = std::max(std::max(P.n1, P.n2), P.n3) * P.nch;
-    const size_t smem = sizeof(int) * (size_t)L;
-    cudaError_t le = launch_pdl(k_scan3_small, dim3(3), dim3(kScanThreads), smem, s, P);
     if (le != cudaSuccess) return le;
     return cudaGetLastError();
 }
@@ -399,8 +341,7 @@ cudaError_t launch_scatter2(const Params& P, cudaStream_t s) {
 }
 
 cudaError_t set_sort_attributes(int max_smem) {
-    const void* ks[] = {(const void*)k_decode_hist, (const void*)k_scatter13, (const void*)k_scatter2,
-                        (const void*)k_scan3_small};
+    const void* ks[] = {(const void*)k_decode_hist, (const void*)k_scatter13, (const void*)k_scatter2};
     for (const void* k : ks) {
         cudaError_t e = allow_max_dynamic_smem(k, max_smem);
         if (e != cudaSuccess) return e;
