@@ -461,15 +461,19 @@ tt_status tt_emb_forward(tt_emb* h, const int64_t* indices, int64_t nnz, const i
     P.nch = (int)((std::max<int64_t>(nnz, 1) + (small ? kSmallChunk : kChunk) - 1) / (small ? kSmallChunk : kChunk));
     P.max_tiles = max_tiles_for(h, nnz, P.tile_cap);
     {
-        int g1f = 1, dtf = 1;
+        // k_tile_bwd pads the dT rows of each pair by up to 16 floats and the G2 rows
+        // by up to 32 floats (bank spreading), on top of the plain sizes
+        int g1f = 1, dtf = 1, g2f = 1;
         for (const TableDev& T : h->tabs) {
             const int Ns = T.q2 * (T.r2 / P.split);
             const int pb = bwd_batch_pairs(T.q1, Ns, T.r1);
             g1f = std::max(g1f, pb * T.q1 * T.r1);
-            dtf = std::max(dtf, pb * T.q1 * Ns);
+            dtf = std::max(dtf, pb * (T.q1 * Ns + 16));
+            g2f = std::max(g2f, (T.r1 + 32) * Ns);
         }
         P.g1s_floats = g1f;
         P.dts_floats = dtf;
+        P.g2s_floats = g2f;
     }
     P.cache_rows = h->d_cache_rows;
     P.cache_n = h->cache_n;

@@ -43,7 +43,7 @@ struct BwdLayout {
     size_t keys, sn, si1, si3, sbag, ss, tbag, ts, rowid, pairid, rowbeg, pairbeg, sh, gs, g2t, g1s, dts, total;
 };
 
-__host__ __device__ inline BwdLayout bwd_layout(int cap, int D, int r1max, int Nmax, int g1f, int dtf) {
+__host__ __device__ inline BwdLayout bwd_layout(int cap, int D, int g2f, int g1f, int dtf) {
     BwdLayout L;
     size_t o = 0;
     L.keys = o;    o = al16(o + sizeof(unsigned long long) * cap);
@@ -60,7 +60,7 @@ __host__ __device__ inline BwdLayout bwd_layout(int cap, int D, int r1max, int N
     L.pairbeg = o; o = al16(o + sizeof(int) * (cap + 1));
     L.sh = o;      o = al16(o + sizeof(int) * 64);
     L.gs = o;      o = al16(o + sizeof(float) * (size_t)cap * D);
-    L.g2t = o;     o = al16(o + sizeof(float) * (size_t)(r1max + 4) * Nmax);  // row stride r1 + 4
+    L.g2t = o;     o = al16(o + sizeof(float) * (size_t)g2f);  // G2 columns of the split, padded rows
     L.g1s = o;     o = al16(o + sizeof(float) * (size_t)g1f);
     L.dts = o;     o = al16(o + sizeof(float) * (size_t)dtf);
     L.total = o;
@@ -180,9 +180,43 @@ __device__ void reduce_slice(const Params& P, int bglob, int* slots, int* sh, fl
     __syncthreads();
 }
 
+// Register tiling of the batch loop for the compiled classes (q1 = 4, r1 % 16 == 0).
+//   Q   = dT . G2^T : thread (kh, a4, u) owns a 4 (j1) x 4 (a) tile summed over the columns
+//                     jc = kh mod KH; a warp spans KH x AL x UL threads, so one shared load
+//                     touches at most 8 distinct 16-byte words (dT pairs US floats apart,
+//                     G2 rows GS floats apart, both strides chosen to spread the banks);
+//   dG2 = G1^T . dT : thread owns a = ag + A4 i, jc = jg + JG c (i, c < 4); a warp spans
+//                     AG x JL such tiles (AG consecutive G1 words, JL consecutive dT words);
+//                     the pairs are split over KS warp groups when one group covers all tiles.
+template <class Dm, int SPLIT>
+struct BwdTiling {
+    static constexpr int R1 = Dm::r1(), Q2 = Dm::q2(), Q3 = Dm::q3(), R2 = Dm::r2();
+    static constexpr int R2S = R2 / SPLIT, NS = Q2 * R2S, D = 4 * Q2 * Q3;
+    static constexpr int PBc = (16 * 4 * NS > 8192) ? 8192 / (4 * NS) : ((16 * 4 * R1 > 8192) ? 8192 / (4 * R1) : 16);
+    static constexpr int PBS = (PBc * (R1 / 4) > 256) ? 256 / (R1 / 4) : PBc;
+    static constexpr int A4 = R1 / 4;
+    static constexpr int KH = 256 / (PBS * A4) >= 1 ? 256 / (PBS * A4) : 1;
+    static constexpr int AL = (KH == 1 ? 8 : 4) < A4 ? (KH == 1 ? 8 : 4) : A4;
+    static constexpr int UL = 32 / (KH * AL);
+    static constexpr int US = 4 * NS + 4 * KH;  // dts pair stride (floats)
+    static constexpr int GS = KH == 1 ? R1 + 4 : R1 + (((4 * AL - R1) % 32) + 32) % 32;  // g2t row stride
+    static constexpr int JG = NS / 4;
+    static constexpr int AG = A4 < 8 ? A4 : 8;
+    static constexpr int JL = 32 / AG;
+    static constexpr int WT = (A4 / AG) * (JG / JL);  // warps that cover every dG2 tile once
+    static constexpr int NT = WT >= 8 ? WT / 8 : 1;   // tile sets per warp
+    static constexpr int KS = WT >= 8 ? 1 : 8 / WT;   // warp groups splitting the pairs
+    static_assert(kBwdThreads == 256, "tiling assumes 8 warps");
+    static_assert(KH >= 1 && KH <= 4 && (KH & (KH - 1)) == 0 && KH * AL * UL == 32, "Q lanes");
+    static_assert(A4 % AL == 0 && PBS % UL == 0 && (A4 / AL) * (PBS / UL) == 8, "Q warps");
+    static_assert(PBS <= 16 && US <= 4 * NS + 16 && GS <= R1 + 32, "padding within the host sizes");
+    static_assert(A4 % AG == 0 && JG % JL == 0 && (NT * 8 == WT || KS * WT == 8), "dG2 tiles");
+    static_assert(KS == 1 || D * (4096 / D) >= 4096, "cross-warp dG2 sums fit in gs");
+};
+
 template <class Dm, int SPLIT>
 __device__ void tile_bwd_body(const Params& P, const TableDev& T, const Dm dm, unsigned char* smraw) {
-    const BwdLayout L = bwd_layout(P.tile_cap, P.D, P.r1_max, P.N_max, P.g1s_floats, P.dts_floats);
+    const BwdLayout L = bwd_layout(P.tile_cap, P.D, P.g2s_floats, P.g1s_floats, P.dts_floats);
     unsigned long long* keys = (unsigned long long*)(smraw + L.keys);
     int* sn = (int*)(smraw + L.sn);
     int* si1 = (int*)(smraw + L.si1);
@@ -244,6 +278,8 @@ __device__ void tile_bwd_body(const Params& P, const TableDev& T, const Dm dm, u
     {
         const float* src = T.G2 + (int64_t)i2 * r1 * q2 * r2;
         const int n = r1 * Ns;
+        int gstride = r1 + 4;
+        if constexpr (Dm::kStatic) gstride = BwdTiling<Dm, SPLIT>::GS;
         for (int base = 0; base < n; base += 8 * kBwdThreads) {
             float v[8];
 #pragma unroll
@@ -261,7 +297,7 @@ __device__ void tile_bwd_body(const Params& P, const TableDev& T, const Dm dm, u
                 const int e = base + q * kBwdThreads + threadIdx.x;
                 if (e < n) {
                     const int a = e / Ns, jc = e - a * Ns;
-                    g2t[jc * (r1 + 4) + a] = v[q];
+                    g2t[jc * gstride + a] = v[q];
                 }
             }
         }
@@ -315,32 +351,53 @@ __device__ void tile_bwd_body(const Params& P, const TableDev& T, const Dm dm, u
     __syncthreads();
 
     // ---- dG3 partial per tile-row, columns c of this split: P3[c][j3] = sum_j12 T[j12][c] gs[j12 q3 + j3]
-    for (int e = threadIdx.x; e < nrows * r2s; e += blockDim.x) {
-        const int row = e / r2s, c = c0 + (e - row * r2s);
-        const int kk = rowbeg[row];
-        const float* Tp = P.Tbuf + T.tbase + ((int64_t)i2 * T.p1 + si1[kk]) * (int64_t)(q12 * r2) + c;
-        const float* gr = gs + row * D;
-        float* dst = P.Pbuf + (int64_t)(start + kk) * P.ps_max + c * q3;
-        if constexpr (Dm::kStatic) {
-            constexpr int Q3 = Dm::q3(), Q12 = Dm::q1() * Dm::q2(), R2 = Dm::r2();
-            float acc[Q3];
+    if constexpr (Dm::kStatic) {
+        // two items per thread: the T columns of both are loaded before either is summed
+        constexpr int Q3 = Dm::q3(), Q12 = Dm::q1() * Dm::q2(), R2 = Dm::r2();
+        const int items = nrows * r2s;
+        for (int e0 = threadIdx.x; e0 < items; e0 += 2 * kBwdThreads) {
+            float tv[2][Q12];
+            int rowv[2], cv[2];
 #pragma unroll
-            for (int j3 = 0; j3 < Q3; ++j3) acc[j3] = 0.f;
+            for (int v = 0; v < 2; ++v) {
+                const int e = e0 + v * kBwdThreads;
+                rowv[v] = e < items ? e / r2s : -1;
+                cv[v] = e < items ? c0 + (e - rowv[v] * r2s) : 0;
+                const int kk = rowv[v] >= 0 ? rowbeg[rowv[v]] : 0;
+                const float* Tp = P.Tbuf + T.tbase + ((int64_t)i2 * T.p1 + si1[kk]) * (int64_t)(Q12 * R2) + cv[v];
 #pragma unroll
-            for (int j12 = 0; j12 < Q12; ++j12) {
-                const float tv = __ldg(Tp + j12 * R2);
-#pragma unroll
-                for (int j3 = 0; j3 < Q3; j3 += 4) {
-                    const float4 x = *reinterpret_cast<const float4*>(gr + j12 * Q3 + j3);
-                    acc[j3] = fmaf(tv, x.x, acc[j3]);
-                    acc[j3 + 1] = fmaf(tv, x.y, acc[j3 + 1]);
-                    acc[j3 + 2] = fmaf(tv, x.z, acc[j3 + 2]);
-                    acc[j3 + 3] = fmaf(tv, x.w, acc[j3 + 3]);
-                }
+                for (int j12 = 0; j12 < Q12; ++j12) tv[v][j12] = rowv[v] >= 0 ? __ldg(Tp + j12 * R2) : 0.f;
             }
 #pragma unroll
-            for (int j3 = 0; j3 < Q3; ++j3) dst[j3] = acc[j3];
-        } else {
+            for (int v = 0; v < 2; ++v) {
+                if (rowv[v] < 0) continue;
+                const float* gr = gs + rowv[v] * D;
+                float acc[Q3];
+#pragma unroll
+                for (int j3 = 0; j3 < Q3; ++j3) acc[j3] = 0.f;
+#pragma unroll
+                for (int j12 = 0; j12 < Q12; ++j12) {
+#pragma unroll
+                    for (int j3 = 0; j3 < Q3; j3 += 4) {
+                        const float4 x = *reinterpret_cast<const float4*>(gr + j12 * Q3 + j3);
+                        acc[j3] = fmaf(tv[v][j12], x.x, acc[j3]);
+                        acc[j3 + 1] = fmaf(tv[v][j12], x.y, acc[j3 + 1]);
+                        acc[j3 + 2] = fmaf(tv[v][j12], x.z, acc[j3 + 2]);
+                        acc[j3 + 3] = fmaf(tv[v][j12], x.w, acc[j3 + 3]);
+                    }
+                }
+                float* dst = P.Pbuf + (int64_t)(start + rowbeg[rowv[v]]) * P.ps_max + cv[v] * Q3;
+#pragma unroll
+                for (int j3 = 0; j3 < Q3; ++j3) dst[j3] = acc[j3];
+            }
+        }
+    } else {
+        for (int e = threadIdx.x; e < nrows * r2s; e += blockDim.x) {
+            const int row = e / r2s, c = c0 + (e - row * r2s);
+            const int kk = rowbeg[row];
+            const float* Tp = P.Tbuf + T.tbase + ((int64_t)i2 * T.p1 + si1[kk]) * (int64_t)(q12 * r2) + c;
+            const float* gr = gs + row * D;
+            float* dst = P.Pbuf + (int64_t)(start + kk) * P.ps_max + c * q3;
             for (int j3 = 0; j3 < q3; ++j3) {
                 float acc = 0.f;
                 for (int j12 = 0; j12 < q12; ++j12) acc = fmaf(Tp[j12 * r2], gr[j12 * q3 + j3], acc);
@@ -354,19 +411,12 @@ __device__ void tile_bwd_body(const Params& P, const TableDev& T, const Dm dm, u
     float* G2p = T.G2 + (int64_t)i2 * r1 * q2 * r2;
 
     if constexpr (Dm::kStatic) {
-        constexpr int R1 = Dm::r1(), Q2 = Dm::q2(), Q3 = Dm::q3(), R2 = Dm::r2();
-        constexpr int R2S = R2 / SPLIT, NS = Q2 * R2S, D_ = 4 * Q2 * Q3;
-        constexpr int PBc = (16 * 4 * NS > 8192) ? 8192 / (4 * NS) : ((16 * 4 * R1 > 8192) ? 8192 / (4 * R1) : 16);
-        constexpr int PBS = (PBc * (R1 / 4) > 256) ? 256 / (R1 / 4) : PBc;
-        // Q tiles: (u, a4, kh); dG2 tiles: (a4, jc4) x K split KS over pairs
-        constexpr int A4 = R1 / 4;
-        constexpr int KH = 256 / (PBS * A4) >= 1 ? 256 / (PBS * A4) : 1;
-        constexpr int TT = A4 * (NS / 4);
-        constexpr int NT = TT >= 256 ? TT / 256 : 1;
-        constexpr int KS = (256 * NT) / TT;
-        static_assert(KH >= 1 && KH <= 32 && (KH & (KH - 1)) == 0, "Q split");
-        static_assert(KS >= 1 && KS <= 32 && (KS & (KS - 1)) == 0, "dG2 split");
-        static_assert(NT * 256 == TT * KS, "dG2 tiles");
+        using BT = BwdTiling<Dm, SPLIT>;
+        constexpr int R1 = BT::R1, Q2 = BT::Q2, Q3 = BT::Q3, R2 = BT::R2;
+        constexpr int R2S = BT::R2S, NS = BT::NS, D_ = BT::D, PBS = BT::PBS, A4 = BT::A4;
+        constexpr int KH = BT::KH, AL = BT::AL, UL = BT::UL, US = BT::US, GS = BT::GS;
+        constexpr int JG = BT::JG, AG = BT::AG, JL = BT::JL, WT = BT::WT, NT = BT::NT, KS = BT::KS;
+        const int lane = threadIdx.x & 31, w = threadIdx.x >> 5;
         float acc2[NT][4][4];
 #pragma unroll
         for (int i = 0; i < NT; ++i)
@@ -374,7 +424,8 @@ __device__ void tile_bwd_body(const Params& P, const TableDev& T, const Dm dm, u
             for (int a = 0; a < 4; ++a)
 #pragma unroll
                 for (int c = 0; c < 4; ++c) acc2[i][a][c] = 0.f;
-        const int ks = threadIdx.x % KS, tbase = threadIdx.x / KS;
+        // dG2 tile of this thread (tile set i adds 8 i to the warp's tile index)
+        const int ks = KS > 1 ? w / WT : 0, wt0 = KS > 1 ? w % WT : w;
         for (int u0 = 0; u0 < npairs; u0 += PBS) {
             const int nb = min(PBS, npairs - u0);
             __syncthreads();
@@ -450,34 +501,31 @@ __device__ void tile_bwd_body(const Params& P, const TableDev& T, const Dm dm, u
                             }
                         }
                     }
-                    *reinterpret_cast<float4*>(dts + (u * NS + jc) * 4) = make_float4(a4v[0], a4v[1], a4v[2], a4v[3]);
+                    *reinterpret_cast<float4*>(dts + u * US + jc * 4) = make_float4(a4v[0], a4v[1], a4v[2], a4v[3]);
                 }
             }
             __syncthreads();
-            // Q[u][j1][a] = sum_jc' dts[u][jc'][j1] g2t[jc'][a]: thread (u, a4, kh)
+            // Q[u][j1][a] = sum_jc' dts[u][jc'][j1] g2t[jc'][a]: thread (kh, a4, u)
             {
-                const int kh = threadIdx.x % KH, ua = threadIdx.x / KH;
-                const int u = ua / A4, a4 = ua - u * A4;
+                const int kh = lane % KH, al = (lane / KH) % AL, ul = lane / (KH * AL);
+                const int a4 = (w % (A4 / AL)) * AL + al, u = (w / (A4 / AL)) * UL + ul;
                 float q[4][4];
 #pragma unroll
                 for (int j = 0; j < 4; ++j)
 #pragma unroll
                     for (int a = 0; a < 4; ++a) q[j][a] = 0.f;
-                if (u < PBS) {
-                    const float* dt = dts + u * NS * 4;
-                    const float* gt = g2t + a4 * 4;
-                    constexpr int GS = R1 + 4;
+                const float* dt = dts + u * US;
+                const float* gt = g2t + a4 * 4;
 #pragma unroll 4
-                    for (int jc = kh; jc < NS; jc += KH) {
-                        const float4 x = *reinterpret_cast<const float4*>(dt + jc * 4);
-                        const float4 y = *reinterpret_cast<const float4*>(gt + jc * GS);
-                        const float xv[4] = {x.x, x.y, x.z, x.w};
-                        const float yv[4] = {y.x, y.y, y.z, y.w};
+                for (int jc = kh; jc < NS; jc += KH) {
+                    const float4 x = *reinterpret_cast<const float4*>(dt + jc * 4);
+                    const float4 y = *reinterpret_cast<const float4*>(gt + jc * GS);
+                    const float xv[4] = {x.x, x.y, x.z, x.w};
+                    const float yv[4] = {y.x, y.y, y.z, y.w};
 #pragma unroll
-                        for (int j = 0; j < 4; ++j)
+                    for (int j = 0; j < 4; ++j)
 #pragma unroll
-                            for (int a = 0; a < 4; ++a) q[j][a] = fmaf(xv[j], yv[a], q[j][a]);
-                    }
+                        for (int a = 0; a < 4; ++a) q[j][a] = fmaf(xv[j], yv[a], q[j][a]);
                 }
 #pragma unroll
                 for (int o = KH / 2; o >= 1; o >>= 1)
@@ -492,22 +540,21 @@ __device__ void tile_bwd_body(const Params& P, const TableDev& T, const Dm dm, u
                         *reinterpret_cast<float4*>(dst + j * R1) = make_float4(q[j][0], q[j][1], q[j][2], q[j][3]);
                 }
             }
-            // dG2[a][jc'] += sum_u sum_j1 g1s[u][a][j1] dts[u][jc'][j1]: tiles (a4, jl) own columns
-            // jc' = jl + (NS/4) c, c < 4 (consecutive lanes read consecutive float4); pairs u = ks mod KS
+            // dG2[a][jc'] += sum_u sum_j1 g1s[u][a][j1] dts[u][jc'][j1] over the pairs u = ks mod KS
 #pragma unroll
             for (int i = 0; i < NT; ++i) {
-                const int ti = tbase + i * (256 / KS);
-                const int a4 = ti / (NS / 4), jc4 = ti - a4 * (NS / 4);
+                const int wt = wt0 + 8 * i;
+                const int ag = (wt % (A4 / AG)) * AG + lane % AG, jg = (wt / (A4 / AG)) * JL + lane / AG;
                 for (int u = ks; u < nb; u += KS) {
                     float gv[4][4], dv[4][4];
 #pragma unroll
                     for (int a = 0; a < 4; ++a) {
-                        const float4 x = *reinterpret_cast<const float4*>(g1s + (u * R1 + a4 * 4 + a) * 4);
+                        const float4 x = *reinterpret_cast<const float4*>(g1s + (u * R1 + ag + A4 * a) * 4);
                         gv[a][0] = x.x; gv[a][1] = x.y; gv[a][2] = x.z; gv[a][3] = x.w;
                     }
 #pragma unroll
                     for (int c = 0; c < 4; ++c) {
-                        const float4 x = *reinterpret_cast<const float4*>(dts + (u * NS + jc4 + (NS / 4) * c) * 4);
+                        const float4 x = *reinterpret_cast<const float4*>(dts + u * US + (jg + JG * c) * 4);
                         dv[c][0] = x.x; dv[c][1] = x.y; dv[c][2] = x.z; dv[c][3] = x.w;
                     }
 #pragma unroll
@@ -519,31 +566,41 @@ __device__ void tile_bwd_body(const Params& P, const TableDev& T, const Dm dm, u
                 }
             }
         }
-        // combine the KS pair-parities (butterfly, fixed order)
-#pragma unroll
-        for (int o = KS / 2; o >= 1; o >>= 1)
-#pragma unroll
-            for (int i = 0; i < NT; ++i)
+        // add the KS warp groups' sums in group order (gs is free after the last batch)
+        if constexpr (KS > 1) {
+            __syncthreads();
+            float* red = gs;
+            if (ks > 0) {
 #pragma unroll
                 for (int a = 0; a < 4; ++a)
 #pragma unroll
-                    for (int c = 0; c < 4; ++c) acc2[i][a][c] += __shfl_xor_sync(0xffffffffu, acc2[i][a][c], o);
+                    for (int c = 0; c < 4; ++c) red[(((ks - 1) * WT + wt0) * 16 + a * 4 + c) * 32 + lane] = acc2[0][a][c];
+            }
+            __syncthreads();
+            if (ks == 0) {
+                for (int k2 = 1; k2 < KS; ++k2)
+#pragma unroll
+                    for (int a = 0; a < 4; ++a)
+#pragma unroll
+                        for (int c = 0; c < 4; ++c) acc2[0][a][c] += red[(((k2 - 1) * WT + wt0) * 16 + a * 4 + c) * 32 + lane];
+            }
+        }
         // dG2 of this split: direct update, or partial + the group's last tile
         const int nt = P.grp_ntiles[g];
         float* part = P.dG2part + ((int64_t)tile * SPLIT + sp) * P.s2_max;
         if (ks == 0) {
 #pragma unroll
             for (int i = 0; i < NT; ++i) {
-                const int ti = tbase + i * (256 / KS);
-                const int a4 = ti / (NS / 4), jc4 = ti - a4 * (NS / 4);
+                const int wt = wt0 + 8 * i;
+                const int ag = (wt % (A4 / AG)) * AG + lane % AG, jg = (wt / (A4 / AG)) * JL + lane / AG;
 #pragma unroll
                 for (int a = 0; a < 4; ++a)
 #pragma unroll
                     for (int c = 0; c < 4; ++c) {
-                        const int jc = jc4 + (NS / 4) * c, j2 = jc / R2S, cc = c0 + (jc - j2 * R2S);
-                        const int ga = ((a4 * 4 + a) * Q2 + j2) * R2 + cc;
+                        const int aa = ag + A4 * a, jc = jg + JG * c, j2 = jc / R2S, cc = c0 + (jc - j2 * R2S);
+                        const int ga = (aa * Q2 + j2) * R2 + cc;
                         if (nt == 1) G2p[ga] = fmaf(-P.lr, acc2[i][a][c], G2p[ga]);
-                        else part[(a4 * 4 + a) * NS + jc] = acc2[i][a][c];
+                        else part[aa * NS + jc] = acc2[i][a][c];
                     }
             }
         }
@@ -677,7 +734,7 @@ __global__ void __launch_bounds__(kBwdThreads) k_reduce13(const __grid_constant_
 // ------------------------------------------------------------------ launchers
 
 size_t tile_bwd_smem(const Params& P) {
-    return bwd_layout(P.tile_cap, P.D, P.r1_max, P.N_max, P.g1s_floats, P.dts_floats).total;
+    return bwd_layout(P.tile_cap, P.D, P.g2s_floats, P.g1s_floats, P.dts_floats).total;
 }
 
 int bwd_batch_pairs(int q1, int Ns, int r1) { return bwd_pairs_per_batch(q1, Ns, r1); }

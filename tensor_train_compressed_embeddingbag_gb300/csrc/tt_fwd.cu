@@ -29,7 +29,7 @@ constexpr int kG1Floats = 8192;     // G1 rows gathered at once (pairs x q1 r1 f
 
 __host__ __device__ inline size_t fwd_smem_bytes(int r1max, int Nmax) {
     // ulist + sh, G2 slice, G1 rows of up to kG1Floats / (q1 r1) pairs
-    return sizeof(int) * (kListCap + 64) + sizeof(float) * (size_t)r1max * Nmax + sizeof(float) * kG1Floats;
+    return sizeof(int) * (kListCap + 64) + sizeof(float) * (size_t)(r1max + 4) * Nmax + sizeof(float) * kG1Floats;
 }
 
 // Touched i1 of pair block [i2][base .. base + kListCap) into ulist; returns the count.
@@ -50,6 +50,28 @@ __device__ __forceinline__ int touched_list(const Params& P, const TableDev& T, 
     return m;
 }
 
+// g1s[u][0 .. 4 R1) = G1 slice of pair u (contiguous [j1][a]), float4 loads, 4 in flight.
+// Pair u starts at u (4 R1 + 4) floats: the pairs read together by one warp fall in
+// distinct banks.
+template <int R1>
+__device__ __forceinline__ void stage_g1_rows(float* g1s, const float* G1, const int* ulist, int gn) {
+    constexpr int F4 = R1;  // float4 per slice (4 R1 floats)
+    const int n4 = gn * F4;
+    for (int base = 0; base < n4; base += 4 * kFwdThreads) {
+        float4 v[4];
+#pragma unroll
+        for (int q = 0; q < 4; ++q) {
+            const int e = base + q * kFwdThreads + threadIdx.x;
+            if (e < n4) v[q] = __ldg(reinterpret_cast<const float4*>(G1 + (int64_t)ulist[e / F4] * (4 * R1)) + e % F4);
+        }
+#pragma unroll
+        for (int q = 0; q < 4; ++q) {
+            const int e = base + q * kFwdThreads + threadIdx.x;
+            if (e < n4) reinterpret_cast<float4*>(g1s)[(e / F4) * (F4 + 1) + e % F4] = v[q];
+        }
+    }
+}
+
 template <class Dm>
 __device__ void fwd_T_group(const Params& P, const TableDev& T, const Dm dm, int i2, int half, FwdSmem S) {
     const int q1 = dm.q1(), r1 = dm.r1(), N = dm.q2() * dm.r2();
@@ -65,69 +87,78 @@ __device__ void fwd_T_group(const Params& P, const TableDev& T, const Dm dm, int
         if (m == 0) continue;
         if (!staged) {
             const float* src = T.G2 + (int64_t)i2 * r1 * N;
-            if constexpr (Dm::kStatic) stage_f32x4<4>(S.g2s, src, (r1 * N) / 4);
-            else stage_f32<8>(S.g2s, src, r1 * N);
-            staged = true;
-        }
-        if constexpr (Dm::kStatic) {
-            // every compiled class has q1 = 4 and q2 r2 % 8 == 0.  Register tile: 4 rows (j1) x 8
-            // columns per thread, columns cg*4 .. +3 and NN/2 + cg*4 .. +3 (consecutive lanes read
-            // consecutive float4 of the G2 row), PS pairs per pass
-            constexpr int R1 = Dm::r1(), NN = Dm::q2() * Dm::r2();
-            constexpr int CG = NN / 8;
-            constexpr int PS = kFwdThreads / CG;
-            const int cg = threadIdx.x % CG, ps = threadIdx.x / CG;
-            constexpr int GB = kG1Floats / (4 * R1);  // pairs gathered at once
-            for (int g0 = 0; g0 < m; g0 += GB) {
-                const int gn = min(GB, m - g0);
-                __syncthreads();
-                // g1s[u][a][j1] = G1[i1_u][j1][a] for the gn pairs, 8 loads in flight per thread
-                for (int base = 0; base < gn * R1 * 4; base += 8 * kFwdThreads) {
+            if constexpr (Dm::kStatic) {
+                // transposed: g2t[jc][a] with row stride r1 + 4 (8 loads in flight per thread)
+                for (int base = 0; base < r1 * N; base += 8 * kFwdThreads) {
                     float v[8];
 #pragma unroll
                     for (int q = 0; q < 8; ++q) {
                         const int e = base + q * kFwdThreads + threadIdx.x;
-                        v[q] = 0.f;
-                        if (e < gn * R1 * 4) {
-                            const int u = e / (R1 * 4), rem = e - u * (R1 * 4);
-                            v[q] = __ldg(T.G1 + (int64_t)S.ulist[g0 + u] * (4 * R1) + (rem & 3) * R1 + (rem >> 2));
-                        }
+                        v[q] = e < r1 * N ? __ldg(src + e) : 0.f;
                     }
 #pragma unroll
                     for (int q = 0; q < 8; ++q) {
                         const int e = base + q * kFwdThreads + threadIdx.x;
-                        if (e < gn * R1 * 4) S.g1s[e] = v[q];
+                        if (e < r1 * N) S.g2s[(e % N) * (r1 + 4) + e / N] = v[q];
                     }
                 }
+            } else {
+                stage_f32<8>(S.g2s, src, r1 * N);
+            }
+            staged = true;
+        }
+        if constexpr (Dm::kStatic) {
+            // every compiled class has q1 = 4 and q2 r2 % 4 == 0.  Register tile: 4 rows (j1) x 4
+            // columns jc = cg + CG c per thread, PS pairs per pass.  A warp covers CL column
+            // groups x PL pairs, so each of its shared loads touches at most 8 distinct 16-byte
+            // words (G2 rows of stride r1 + 4 and G1 slices of stride 4 r1 + 4 hit distinct
+            // banks): one wavefront per load.  Paired FFMA over a: even / odd partial sums.
+            constexpr int R1 = Dm::r1(), NN = Dm::q2() * Dm::r2();
+            constexpr int CG = NN / 4;
+            constexpr int PS = kFwdThreads / CG;
+            constexpr int CL = CG < 8 ? CG : 8, PL = 32 / CL, WC = CG / CL;  // lanes: CL x PL; warps: WC per pair block
+            static_assert(CG % CL == 0 && (kFwdThreads / 32) % WC == 0 && PS == (kFwdThreads / 32 / WC) * PL, "fwd_T tiles");
+            constexpr int GS = R1 + 4;      // g2t row stride
+            constexpr int US = 4 * R1 + 4;  // g1s pair stride
+            const int lane = threadIdx.x & 31, w = threadIdx.x >> 5;
+            const int cg = (w % WC) * CL + lane % CL, ps = (w / WC) * PL + lane / CL;
+            constexpr int GB = kG1Floats / US;  // pairs gathered at once
+            for (int g0 = 0; g0 < m; g0 += GB) {
+                const int gn = min(GB, m - g0);
+                __syncthreads();
+                // g1s[u][j1][a] = G1[i1_u][j1][a]: the pair's contiguous slice, 4 float4 loads in flight
+                stage_g1_rows<R1>(S.g1s, T.G1, S.ulist + g0, gn);
                 __syncthreads();
                 for (int u0 = 0; u0 < gn; u0 += PS) {
                     const int u = u0 + ps;
                     if (u < gn) {
-                        float acc[4][8];
+                        float2 acc[4][4];
 #pragma unroll
                         for (int j = 0; j < 4; ++j)
 #pragma unroll
-                            for (int c = 0; c < 8; ++c) acc[j][c] = 0.f;
-                        const float* g1 = S.g1s + u * R1 * 4;
-                        const float* g2 = S.g2s + cg * 4;
-#pragma unroll 8
-                        for (int a = 0; a < R1; ++a) {
-                            const float4 x = *reinterpret_cast<const float4*>(g1 + a * 4);
-                            const float4 y0 = *reinterpret_cast<const float4*>(g2 + a * NN);
-                            const float4 y1 = *reinterpret_cast<const float4*>(g2 + a * NN + NN / 2);
-                            const float xv[4] = {x.x, x.y, x.z, x.w};
-                            const float yv[8] = {y0.x, y0.y, y0.z, y0.w, y1.x, y1.y, y1.z, y1.w};
+                            for (int c = 0; c < 4; ++c) acc[j][c] = make_float2(0.f, 0.f);
+                        const float* g1 = S.g1s + u * US;
+                        const float* g2 = S.g2s + cg * GS;
+#pragma unroll 2
+                        for (int a = 0; a < R1; a += 4) {
+                            float4 x[4], y[4];
+#pragma unroll
+                            for (int j = 0; j < 4; ++j) x[j] = *reinterpret_cast<const float4*>(g1 + j * R1 + a);
+#pragma unroll
+                            for (int c = 0; c < 4; ++c) y[c] = *reinterpret_cast<const float4*>(g2 + c * CG * GS + a);
 #pragma unroll
                             for (int j = 0; j < 4; ++j)
 #pragma unroll
-                                for (int c = 0; c < 8; ++c) acc[j][c] = fmaf(xv[j], yv[c], acc[j][c]);
+                                for (int c = 0; c < 4; ++c) {
+                                    acc[j][c] = __ffma2_rn(make_float2(x[j].x, x[j].y), make_float2(y[c].x, y[c].y), acc[j][c]);
+                                    acc[j][c] = __ffma2_rn(make_float2(x[j].z, x[j].w), make_float2(y[c].z, y[c].w), acc[j][c]);
+                                }
                         }
-                        float* dst = P.Tbuf + T.tbase + ((int64_t)i2 * T.p1 + S.ulist[g0 + u]) * (4 * NN) + cg * 4;
+                        float* dst = P.Tbuf + T.tbase + ((int64_t)i2 * T.p1 + S.ulist[g0 + u]) * (4 * NN) + cg;
 #pragma unroll
-                        for (int j = 0; j < 4; ++j) {
-                            *reinterpret_cast<float4*>(dst + j * NN) = make_float4(acc[j][0], acc[j][1], acc[j][2], acc[j][3]);
-                            *reinterpret_cast<float4*>(dst + j * NN + NN / 2) = make_float4(acc[j][4], acc[j][5], acc[j][6], acc[j][7]);
-                        }
+                        for (int j = 0; j < 4; ++j)
+#pragma unroll
+                            for (int c = 0; c < 4; ++c) dst[j * NN + c * CG] = acc[j][c].x + acc[j][c].y;
                     }
                 }
             }
@@ -152,21 +183,24 @@ __device__ void fwd_T_group(const Params& P, const TableDev& T, const Dm dm, int
 }
 
 template <int DC>
-__global__ void __launch_bounds__(kFwdThreads) k_fwd_T(const __grid_constant__ Params P) {
+__global__ void __launch_bounds__(kFwdThreads, 3) k_fwd_T(const __grid_constant__ Params P) {
     pdl_entry();
     extern __shared__ __align__(16) unsigned char smraw[];
-    const int g = blockIdx.x / P.fwd_split, half = blockIdx.x % P.fwd_split;
-    if ((int)blockIdx.x >= P.n2 * P.fwd_split) {  // small path: three extra blocks scan the grouping histograms
-        scan_digit_block(P, blockIdx.x - P.n2 * P.fwd_split, (int*)smraw);
+    // small path: the first three blocks scan the grouping histograms (first, so
+    // that they are resident from the start; they are the longest blocks)
+    const int nscan = P.small ? 3 : 0;
+    if ((int)blockIdx.x < nscan) {
+        scan_digit_block(P, blockIdx.x, (int*)smraw);
         return;
     }
+    const int g = (blockIdx.x - nscan) / P.fwd_split, half = (blockIdx.x - nscan) % P.fwd_split;
     const TableDev& T = P.tables[P.bin2_tab[g]];
     const int i2 = g - T.base2;
     FwdSmem S;
     S.ulist = (int*)smraw;
     S.sh = S.ulist + kListCap;
     S.g2s = (float*)(S.sh + 64);
-    S.g1s = S.g2s + (size_t)P.r1_max * P.N_max;
+    S.g1s = S.g2s + (size_t)(P.r1_max + 4) * P.N_max;
     switch (DC >= 0 ? DC : T.dclass) {
         case kQ444R32: fwd_T_group(P, T, SDims<4, 4, 4, 32, 32>{}, i2, half, S); break;
         case kQ444R16: fwd_T_group(P, T, SDims<4, 4, 4, 16, 16>{}, i2, half, S); break;
@@ -508,7 +542,10 @@ cudaError_t launch_cache_fill(const Params& P, cudaStream_t s) {
 cudaError_t set_fwd_attributes(int max_smem) {
     const void* ks[] = {(const void*)k_fwd_T<kQ444R32>, (const void*)k_fwd_T<kQ444R16>,
                         (const void*)k_fwd_T<kQ444R64>, (const void*)k_fwd_T<kQ448R64>,
-                        (const void*)k_fwd_T<kDynamic>, (const void*)k_fwd_T<-1>};
+                        (const void*)k_fwd_T<kDynamic>, (const void*)k_fwd_T<-1>,
+                        (const void*)k_pool<kQ444R32>, (const void*)k_pool<kQ444R16>,
+                        (const void*)k_pool<kQ444R64>, (const void*)k_pool<kQ448R64>,
+                        (const void*)k_pool<kDynamic>, (const void*)k_pool<-1>, (const void*)k_cache_fill};
     for (const void* k : ks) {
         cudaError_t e = allow_max_dynamic_smem(k, max_smem);
         if (e != cudaSuccess) return e;

@@ -80,6 +80,7 @@ struct Params {
     int dclass_all;                 // dimension class shared by every table, or -1 (mixed)
     int fwd_split;                  // k_fwd_T blocks per (table, i2) group (1 or 2)
     int g1s_floats, dts_floats;     // k_tile_bwd batch buffers (max over tables, this call's split)
+    int g2s_floats;                 // k_tile_bwd G2 columns of one split, padded rows (max over tables)
     // call arguments
     const int64_t* idx;
     const int64_t* off;
@@ -303,61 +304,52 @@ __device__ __forceinline__ void scatter_chunk(const Params& P, int c) {
 }
 
 // Small path: exclusive scan of digit k's [bin][chunk] histogram (k = 0: i1,
-// 1: i2, 2: i3) by one block, in place in global memory: each thread owns a
-// contiguous range, sums it (16 loads in flight), the block scans the sums,
-// and each thread rewrites its range.  The i2 block then cuts every
-// (table, i2) group into tiles of <= tile_cap lookups.
+// 1: i2, 2: i3) by one block, in place in global memory.  Thread per bin: it
+// loads the bin's nch chunk counts together (they are contiguous), the block
+// scans the bin totals, and the thread writes the bin's running prefix.  The
+// i2 block then cuts every (table, i2) group into tiles of <= tile_cap lookups.
+constexpr int kScanChunkMax = 48;  // >= kSmallMaxNnz / kSmallChunk
 __device__ __forceinline__ void scan_digit_block(const Params& P, int k, int* sh) {
-    constexpr int U = 16;
     const int nb = k == 0 ? P.n1 : (k == 1 ? P.n2 : P.n3);
     int* H = k == 0 ? P.H1 : (k == 1 ? P.H2 : P.H3);
-    const int L = nb * P.nch;
-    const int per = (L + blockDim.x - 1) / blockDim.x;
-    const int i0 = min(L, (int)threadIdx.x * per), i1 = min(L, i0 + per);
-    int sum = 0;
-    for (int base = i0; base < i1; base += U) {
-        int v[U];
+    const int nch = P.nch;  // <= kScanChunkMax on this path
+    int carry = 0, tcarry = 0;
+    for (int b0 = 0; b0 < nb; b0 += blockDim.x) {
+        const int b = b0 + threadIdx.x;
+        int v[kScanChunkMax];
+        int tot = 0;
 #pragma unroll
-        for (int u = 0; u < U; ++u) v[u] = base + u < i1 ? H[base + u] : 0;
+        for (int c = 0; c < kScanChunkMax; ++c) {
+            v[c] = (b < nb && c < nch) ? H[(int64_t)b * nch + c] : 0;
+            tot += v[c];
+        }
+        int total;
+        const int start = carry + block_scan_excl(tot, sh, &total);
+        if (b < nb) {
+            int run = start;
 #pragma unroll
-        for (int u = 0; u < U; ++u) sum += v[u];
-    }
-    int total;
-    int run = block_scan_excl(sum, sh, &total);
-    for (int base = i0; base < i1; base += U) {
-        int v[U];
-#pragma unroll
-        for (int u = 0; u < U; ++u) v[u] = base + u < i1 ? H[base + u] : 0;
-#pragma unroll
-        for (int u = 0; u < U; ++u)
-            if (base + u < i1) {
-                H[base + u] = run;
-                run += v[u];
+            for (int c = 0; c < kScanChunkMax; ++c)
+                if (c < nch) {
+                    H[(int64_t)b * nch + c] = run;
+                    run += v[c];
+                }
+        }
+        carry += total;
+        if (k == 1) {  // tiles of the (table, i2) groups of this round of bins
+            const int cap = P.tile_cap;
+            const int nt = b < nb ? (tot + cap - 1) / cap : 0;
+            int ttot;
+            const int first = tcarry + block_scan_excl(nt, sh, &ttot);
+            if (b < nb) {
+                P.grp_first[b] = first;
+                P.grp_ntiles[b] = nt;
+                for (int t = 0; t < nt; ++t)
+                    P.tiles[first + t] = make_int4(start + t * cap, min(cap, tot - t * cap), b, t);
             }
-    }
-    if (k != 1) return;
-    __syncthreads();  // the block's writes of H are visible to the block after this
-    const int cap = P.tile_cap;
-    int carry = 0;
-    for (int base = 0; base < nb; base += blockDim.x) {
-        const int g = base + threadIdx.x;
-        int start = 0, cnt = 0, nt = 0;
-        if (g < nb) {
-            start = H[g * P.nch];
-            cnt = ((g + 1 < nb) ? H[(g + 1) * P.nch] : (int)P.nnz) - start;
-            nt = (cnt + cap - 1) / cap;
+            tcarry += ttot;
         }
-        int tot;
-        const int first = carry + block_scan_excl(nt, sh, &tot);
-        if (g < nb) {
-            P.grp_first[g] = first;
-            P.grp_ntiles[g] = nt;
-            for (int t = 0; t < nt; ++t)
-                P.tiles[first + t] = make_int4(start + t * cap, min(cap, cnt - t * cap), g, t);
-        }
-        carry += tot;
     }
-    if (threadIdx.x == 0) *P.ntiles = carry;
+    if (k == 1 && threadIdx.x == 0) *P.ntiles = tcarry;
 }
 
 // ---------------------------------------------------------------- launchers
@@ -366,13 +358,19 @@ __device__ __forceinline__ void scan_digit_block(const Params& P, int k, int* sh
 extern bool g_use_pdl;  // programmatic dependent launch between the library's kernels
 
 // Allow a kernel the largest dynamic shared memory the device permits next to
-// its static shared memory.
+// its static shared memory, and ask for the largest shared-memory carve-out.
+// The carve-out matters for the overlap of consecutive kernels: an SM whose
+// L1/shared split was chosen for a kernel with little shared memory cannot take
+// a block that needs more until it has drained, so every kernel of the library
+// asks for the same (maximal) split and the blocks of the next kernel can move
+// in next to those of the previous one.
 inline cudaError_t allow_max_dynamic_smem(const void* kernel, int max_smem) {
     cudaFuncAttributes a;
     cudaError_t e = cudaFuncGetAttributes(&a, kernel);
     if (e != cudaSuccess) return e;
-    return cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                max_smem - (int)a.sharedSizeBytes);
+    e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, max_smem - (int)a.sharedSizeBytes);
+    if (e != cudaSuccess) return e;
+    return cudaFuncSetAttribute(kernel, cudaFuncAttributePreferredSharedMemoryCarveout, cudaSharedmemCarveoutMaxShared);
 }
 
 // Launch with the programmatic-stream-serialization attribute (see pdl_entry).

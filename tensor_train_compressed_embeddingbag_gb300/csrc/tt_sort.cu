@@ -341,7 +341,8 @@ cudaError_t launch_scatter2(const Params& P, cudaStream_t s) {
 }
 
 cudaError_t set_sort_attributes(int max_smem) {
-    const void* ks[] = {(const void*)k_decode_hist, (const void*)k_scatter13, (const void*)k_scatter2};
+    const void* ks[] = {(const void*)k_decode_hist, (const void*)k_scatter13, (const void*)k_scatter2,
+                        (const void*)k_decode_small, (const void*)k_scan13, (const void*)k_scan2_tiles};
     for (const void* k : ks) {
         cudaError_t e = allow_max_dynamic_smem(k, max_smem);
         if (e != cudaSuccess) return e;
