@@ -68,17 +68,20 @@ typedef struct {
     int64_t p[3];           /* row factorisation, p1 p2 p3 >= E (FBTT README, "Parameters": tt_p_shapes) */
     int32_t q[3];           /* column factorisation, q1 q2 q3 = D (tt_q_shapes) */
     int32_t ranks[2];       /* r1, r2 (tt_ranks) */
-    float* cores_dev[3];    /* caller-owned device cores, updated in place by tt_emb_backward */
+    float* cores_dev[3];    /* caller-owned, 16-byte aligned device cores, updated in place by tt_emb_backward */
 } tt_table_desc;
 
 /*
  * Create a single-table handle.  FBTT README, "Parameters" (num_embeddings,
  * tt_p_shapes, tt_q_shapes, tt_ranks).  cores_dev[k] must hold
- * p_k * r_{k-1} * q_k * r_k floats.  The handle keeps the core pointers (not
+ * p_k * r_{k-1} * q_k * r_k floats and be 16-byte aligned (the kernels read
+ * the cores as float4; a fresh cudaMalloc or torch allocation always is).
+ * The handle keeps the core pointers (not
  * the data); the caller keeps the cores alive while the handle is used.
  * Device memory for the handle's fixed tables is allocated on the current
  * CUDA device, which every later call on the handle must also use.
- * Returns TT_ERR_ARG (null out/cores), TT_ERR_SHAPE (see limits above).
+ * Returns TT_ERR_ARG (null out/cores, misaligned cores), TT_ERR_SHAPE (see
+ * limits above).
  */
 tt_status tt_emb_create(int64_t num_embeddings, const int64_t p[3], const int32_t q[3],
                         const int32_t ranks[2], float* const cores_dev[3], tt_emb** out);

@@ -200,8 +200,8 @@ tt_status build_handle(tt_emb* h, int ntab, const tt_table_desc* d) {
         tt_status st = validate_table(d[t].num_embeddings, d[t].p, d[t].q, d[t].ranks);
         if (st != TT_OK) return st;
         if (d[t].q[0] * d[t].q[1] * d[t].q[2] != d[0].q[0] * d[0].q[1] * d[0].q[2]) return TT_ERR_SHAPE;
-        for (int k = 0; k < 3; ++k)
-            if (!d[t].cores_dev[k]) return TT_ERR_ARG;
+        for (int k = 0; k < 3; ++k)  // the kernels read the cores as float4
+            if (!d[t].cores_dev[k] || ((uintptr_t)d[t].cores_dev[k] & 15u) != 0) return TT_ERR_ARG;
     }
     {
         int64_t s1 = 0, s2 = 0, s3 = 0;
@@ -225,7 +225,7 @@ tt_status build_handle(tt_emb* h, int ntab, const tt_table_desc* d) {
     }
     h->ntab = ntab;
     const int D = d[0].q[0] * d[0].q[1] * d[0].q[2];
-    int n1 = 0, n2 = 0, n3 = 0, qs = 1, ps = 1, s2 = 1, r1m = 1, Nm = 1, q1Nm = 1;
+    int n1 = 0, n2 = 0, n3 = 0, qs = 1, ps = 1, s2 = 1, r1m = 1, Nm = 1, q1Nm = 1, tcf = 0;
     int64_t tb = 0, fb = 0;
     for (int t = 0; t < ntab; ++t) {
         TableDev T{};
@@ -249,6 +249,7 @@ tt_status build_handle(tt_emb* h, int ntab, const tt_table_desc* d) {
         r1m = std::max(r1m, T.r1);
         Nm = std::max(Nm, T.q2 * T.r2);
         q1Nm = std::max(q1Nm, T.q1 * T.q2 * T.r2);
+        tcf = std::max(tcf, fwd_tc_floats_of(T.dclass, T.r1, T.q2 * T.r2));
         h->tabs.push_back(T);
     }
     if (n1 > kMaxBinsPerDigit || n2 > kMaxBinsPerDigit || n3 > kMaxBinsPerDigit) return TT_ERR_SHAPE;
@@ -257,7 +258,7 @@ tt_status build_handle(tt_emb* h, int ntab, const tt_table_desc* d) {
     P.n1 = n1; P.n2 = n2; P.n3 = n3;
     P.D = D;
     P.qs_max = qs; P.ps_max = ps; P.s2_max = s2;
-    P.r1_max = r1m; P.N_max = Nm; P.q1N_max = q1Nm;
+    P.r1_max = r1m; P.N_max = Nm; P.q1N_max = q1Nm; P.fwd_tc_floats = tcf;
     // tile caps: the summed upstream gradient of a tile (cap x D floats) stays <= 16 KB on the
     // single-CTA-sort path (many small tiles) and <= 64 KB on the multi-CTA path
     h->cap_small = pow2_floor(std::min(kTileThreads, 4096 / D));
@@ -274,7 +275,10 @@ tt_status build_handle(tt_emb* h, int ntab, const tt_table_desc* d) {
     {
         int sms = 0;  // few i2 groups: two k_fwd_T blocks share each group's pairs
         if (cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, h->device) != cudaSuccess) return TT_ERR_CUDA;
-        P.fwd_split = n2 < 2 * sms ? 2 : 1;
+        // the tensor-core T path takes a whole (table, i2) group per block
+        bool all_tc = true;
+        for (const TableDev& T : h->tabs) all_tc = all_tc && fwd_tc_floats_of(T.dclass, T.r1, T.q2 * T.r2) > 0;
+        P.fwd_split = (!all_tc && n2 < 2 * sms) ? 2 : 1;
     }
     P.p1_max = p1m;
     h->split_small = can_split ? 2 : 1;

@@ -8,6 +8,7 @@
 // in registers (tensorflow/addons EmbeddingBag issue: the pre-pool rows are
 // never materialised).
 #include "tt_dims.cuh"
+#include "tt_tc.cuh"
 
 namespace ttemb {
 
@@ -23,13 +24,35 @@ struct FwdSmem {
     int* sh;
     float* g2s;
     float* g1s;
+    unsigned char* tc;  // tensor-core path: operand tiles, mbarrier, tensor-memory address
 };
 
 constexpr int kG1Floats = 8192;     // G1 rows gathered at once (pairs x q1 r1 floats)
+constexpr size_t kFwdTcBase = 5120;  // byte offset of the tensor-core region (after ulist + sh)
+constexpr int kTcTiles = 2;          // 128-row tensor-core tiles per batch (64 pairs)
 
-__host__ __device__ inline size_t fwd_smem_bytes(int r1max, int Nmax) {
-    // ulist + sh, G2 slice, G1 rows of up to kG1Floats / (q1 r1) pairs
-    return sizeof(int) * (kListCap + 64) + sizeof(float) * (size_t)(r1max + 4) * Nmax + sizeof(float) * kG1Floats;
+// Dimension classes whose T = G1 G2 runs on the tensor cores (3xTF32): q1 = 4,
+// r1 <= 32, q2 r2 <= 128 (one MMA covers every column; operand tiles fit three
+// blocks per SM).
+__host__ __device__ constexpr bool fwd_tc_class(int dclass) { return dclass == kQ444R32 || dclass == kQ444R16; }
+
+// fp32 words of the operand tiles: A (kTcTiles x 128 rows x r1) and B (N rows x r1), hi and lo.
+int fwd_tc_floats_of(int dclass, int r1, int N) { return fwd_tc_class(dclass) ? 2 * r1 * (kTcTiles * kTcM + N) : 0; }
+
+constexpr size_t kFwdTcCtl = 128;  // mbarrier, tensor-memory address and flag ahead of the tiles
+
+__host__ __device__ inline size_t fwd_smem_bytes(int r1max, int Nmax, int tc_floats) {
+    // ulist + sh, G2 slice, G1 rows of up to kG1Floats / (q1 r1) pairs; or the tensor-core tiles
+    const size_t ffma = sizeof(int) * (kListCap + 64) + sizeof(float) * (size_t)(r1max + 4) * Nmax + sizeof(float) * kG1Floats;
+    const size_t tc = tc_floats > 0 ? kFwdTcBase + kFwdTcCtl + sizeof(float) * (size_t)tc_floats : 0;
+    const size_t scan = sizeof(int) * (size_t)kScanSmemInts;  // the small path's histogram-scan blocks
+    const size_t m = ffma > tc ? ffma : tc;
+    return m > scan ? m : scan;
+}
+
+// Tensor-memory columns a tensor-core k_fwd_T block holds: kTcTiles accumulators of q2 r2 columns.
+__host__ __device__ constexpr uint32_t fwd_tc_cols(int dclass) {
+    return dclass == kQ444R32 ? kTcTiles * 128u : (dclass == kQ444R16 ? kTcTiles * 64u : 0u);
 }
 
 // Touched i1 of pair block [i2][base .. base + kListCap) into ulist; returns the count.
@@ -72,8 +95,161 @@ __device__ __forceinline__ void stage_g1_rows(float* g1s, const float* G1, const
     }
 }
 
+// T = G1 G2 for the touched pairs of (table, i2) on the tensor cores.  Batches of
+// up to kTcTiles x 32 pairs: A = their G1 slices as rows (u, j1) x r1 (128 rows per
+// tile), B = G2^T (q2 r2 rows x r1), D_t = A_t . B^T = 32 T blocks per tile in
+// tensor memory (columns [t N, t N + N)); three TF32 MMAs per K step (hi.hi +
+// hi.lo + lo.hi).  The G2 loads are issued before the touched-pair scan so that
+// the two latencies overlap.
+// The block's tensor memory (fwd_tc_cols columns) is allocated at kernel entry.
+template <int R1, int NN>
+__device__ void fwd_T_group_tc(const Params& P, const TableDev& T, int i2, int half, FwdSmem S) {
+    static_assert(R1 % 8 == 0 && R1 <= 32 && NN % 32 == 0 && NN <= 128, "tensor-core tile shapes");
+    constexpr uint32_t kIdesc = tc_idesc_tf32(kTcM, NN);
+    constexpr uint32_t kLbo = 128, kSbo = R1 * 32;  // K core matrices / 8-row groups, bytes
+    constexpr int kBQ = (R1 / 4) * NN;              // float4 quads of B
+    constexpr int kBPer = (kBQ + kFwdThreads - 1) / kFwdThreads;
+    constexpr int kPairs = kTcTiles * kTcM / 4;     // pairs per batch
+    uint64_t* bar = reinterpret_cast<uint64_t*>(S.tc);
+    uint32_t* tslot = reinterpret_cast<uint32_t*>(bar + 1);
+    int* okflag = reinterpret_cast<int*>(tslot + 1);
+    float* Ah = reinterpret_cast<float*>(S.tc + kFwdTcCtl);
+    float* Al = Ah + kTcTiles * kTcM * R1;
+    float* Bh = Al + kTcTiles * kTcM * R1;
+    float* Bl = Bh + NN * R1;
+    const int lane = threadIdx.x & 31, w = threadIdx.x >> 5;
+
+    // G2 of this i2, element (jc, a) of B = G2[i2][a][jc]: loads in flight during the scan
+    float bx[kBPer][4];
+    {
+        const float* src = T.G2 + (int64_t)i2 * R1 * NN;
+#pragma unroll
+        for (int q = 0; q < kBPer; ++q) {
+            const int e = threadIdx.x + q * kFwdThreads;
+            const int jc = e % NN, a4 = e / NN;
+#pragma unroll
+            for (int i = 0; i < 4; ++i) bx[q][i] = e < kBQ ? __ldg(src + (4 * a4 + i) * NN + jc) : 0.f;
+        }
+    }
+    bool staged = false;
+    int nbatch = 0;
+    int* list0 = S.ulist;
+    for (int base = 0; base < T.p1; base += kListCap) {
+        int m = touched_list(P, T, i2, base, list0, S.sh);
+        if (P.fwd_split == 2) {
+            const int m2 = (m + 1) / 2;
+            S.ulist = list0 + half * m2;
+            m = half ? m - m2 : m2;
+        }
+        if (m == 0) continue;
+        if (!staged) {
+#pragma unroll
+            for (int q = 0; q < kBPer; ++q) {
+                const int e = threadIdx.x + q * kFwdThreads;
+                if (e < kBQ) {
+                    const int jc = e % NN, a4 = e / NN;
+                    float hi[4];
+#pragma unroll
+                    for (int i = 0; i < 4; ++i) hi[i] = tf32_round(bx[q][i]);
+                    const int o = tc_off(jc, 4 * a4, R1);
+                    *reinterpret_cast<float4*>(Bh + o) = make_float4(hi[0], hi[1], hi[2], hi[3]);
+                    *reinterpret_cast<float4*>(Bl + o) =
+                        make_float4(bx[q][0] - hi[0], bx[q][1] - hi[1], bx[q][2] - hi[2], bx[q][3] - hi[3]);
+                }
+            }
+            if (threadIdx.x == 32) mbar_init(bar, 1);
+            staged = true;
+        }
+        for (int g0 = 0; g0 < m; g0 += kPairs) {
+            const int gn = min(kPairs, m - g0);
+            const int ntl = (gn + kTcM / 4 - 1) / (kTcM / 4);  // tiles of this batch
+            tc_fence_before();
+            __syncthreads();  // the previous batch's tensor-memory reads and A reads are done
+            // A: row (u, j1) = G1[i1_u][j1][0 .. r1) (tile u / 32); lanes take 8 rows x 4
+            // column quads (rows counted up to a multiple of 8; rows past 4 gn are skipped)
+            // (every load of the batch is issued before the first store)
+            const int rows8 = (4 * gn + 7) & ~7;
+            constexpr int kAPer = kTcTiles * kTcM * (R1 / 4) / kFwdThreads;
+            float4 xa[kAPer];
+            int oa[kAPer];
+#pragma unroll
+            for (int q = 0; q < kAPer; ++q) {
+                const int e4 = threadIdx.x + q * kFwdThreads;
+                const int rl = e4 & 7, a4 = (e4 >> 3) % (R1 / 4), rh = (e4 >> 3) / (R1 / 4);
+                const int row = rh * 8 + rl;
+                oa[q] = -1;
+                xa[q] = make_float4(0.f, 0.f, 0.f, 0.f);
+                if (e4 < rows8 * (R1 / 4) && row < 4 * gn) {
+                    const int u = row >> 2, j1 = row & 3;
+                    xa[q] = __ldg(reinterpret_cast<const float4*>(T.G1 + (int64_t)S.ulist[g0 + u] * (4 * R1) + j1 * R1) + a4);
+                    oa[q] = (row / kTcM) * (kTcM * R1) + tc_off(row % kTcM, 4 * a4, R1);
+                }
+            }
+#pragma unroll
+            for (int q = 0; q < kAPer; ++q) {
+                if (oa[q] < 0) continue;
+                const float4 x = xa[q];
+                const float4 hi = make_float4(tf32_round(x.x), tf32_round(x.y), tf32_round(x.z), tf32_round(x.w));
+                *reinterpret_cast<float4*>(Ah + oa[q]) = hi;
+                *reinterpret_cast<float4*>(Al + oa[q]) = make_float4(x.x - hi.x, x.y - hi.y, x.z - hi.z, x.w - hi.w);
+            }
+            tc_fence_smem();
+            tc_fence_before();
+            __syncthreads();
+            tc_fence_after();
+            if (threadIdx.x == 0) {
+                const uint32_t bh = smem_addr(Bh), bl = smem_addr(Bl);
+                for (int t = 0; t < ntl; ++t) {
+                    const uint32_t d = *tslot + (uint32_t)(t * NN);
+                    const uint32_t ah = smem_addr(Ah + t * kTcM * R1), al = smem_addr(Al + t * kTcM * R1);
+#pragma unroll
+                    for (int ks = 0; ks < R1 / 8; ++ks) {
+                        const uint32_t ko = ks * 256;
+                        tc_mma_tf32(d, tc_desc(ah + ko, kLbo, kSbo), tc_desc(bh + ko, kLbo, kSbo), kIdesc, ks > 0);
+                        tc_mma_tf32(d, tc_desc(ah + ko, kLbo, kSbo), tc_desc(bl + ko, kLbo, kSbo), kIdesc, true);
+                        tc_mma_tf32(d, tc_desc(al + ko, kLbo, kSbo), tc_desc(bh + ko, kLbo, kSbo), kIdesc, true);
+                    }
+                }
+                tc_commit(bar);
+                *okflag = mbar_wait(bar, nbatch & 1) ? 1 : 0;
+                if (!*okflag) atomicOr(P.err, kErrTimeout);
+            }
+            __syncthreads();
+            tc_fence_after();
+            // warp w reads tile w / 4, lanes 32 (w % 4) .. + 31 (its rows), all N columns
+            const int t = w >> 2;
+            if (*okflag && t < ntl) {
+                const int row = 32 * (w & 3) + lane, u = t * (kTcM / 4) + (row >> 2), j1 = row & 3;
+                const uint32_t taddr = *tslot + ((uint32_t)(32 * (w & 3)) << 16) + (uint32_t)(t * NN);
+                float* dst = nullptr;
+                if (u < gn) dst = P.Tbuf + T.tbase + (((int64_t)i2 * T.p1 + S.ulist[g0 + u]) * 4 + j1) * NN;
+#pragma unroll
+                for (int c0 = 0; c0 < NN; c0 += 32) {
+                    float v[32];
+                    tc_ld32(taddr + c0, v);
+                    if (dst) {
+#pragma unroll
+                        for (int i = 0; i < 32; i += 4)
+                            *reinterpret_cast<float4*>(dst + c0 + i) = make_float4(v[i], v[i + 1], v[i + 2], v[i + 3]);
+                    }
+                }
+            }
+            ++nbatch;
+        }
+    }
+    tc_fence_before();
+    __syncthreads();
+    if (w == 0) tc_dealloc(*tslot, kTcTiles * NN);
+}
+
 template <class Dm>
 __device__ void fwd_T_group(const Params& P, const TableDev& T, const Dm dm, int i2, int half, FwdSmem S) {
+    if constexpr (Dm::kStatic) {
+        if constexpr (Dm::r1() <= 32 && Dm::q2() * Dm::r2() <= 128) {
+            fwd_T_group_tc<Dm::r1(), Dm::q2() * Dm::r2()>(P, T, i2, half, S);
+            return;
+        }
+    }
     const int q1 = dm.q1(), r1 = dm.r1(), N = dm.q2() * dm.r2();
     bool staged = false;
     int* list0 = S.ulist;
@@ -183,24 +359,32 @@ __device__ void fwd_T_group(const Params& P, const TableDev& T, const Dm dm, int
 }
 
 template <int DC>
-__global__ void __launch_bounds__(kFwdThreads, 3) k_fwd_T(const __grid_constant__ Params P) {
-    pdl_entry();
+__global__ void __launch_bounds__(kFwdThreads, 2) k_fwd_T(const __grid_constant__ Params P) {
     extern __shared__ __align__(16) unsigned char smraw[];
     // small path: the first three blocks scan the grouping histograms (first, so
     // that they are resident from the start; they are the longest blocks)
     const int nscan = P.small ? 3 : 0;
     if ((int)blockIdx.x < nscan) {
+        pdl_entry();
         scan_digit_block(P, blockIdx.x, (int*)smraw);
         return;
     }
+    // the handle's constant tables may be read before the previous kernel completes
     const int g = (blockIdx.x - nscan) / P.fwd_split, half = (blockIdx.x - nscan) % P.fwd_split;
     const TableDev& T = P.tables[P.bin2_tab[g]];
     const int i2 = g - T.base2;
+    // Tensor memory first: while a block holds its allocation permit, no further
+    // block of a tensor-memory kernel is placed on the SM, so the permit is
+    // released at once.  (The previous kernels of the library hold no tensor memory.)
+    const uint32_t tcols = fwd_tc_cols(DC >= 0 ? DC : T.dclass);
+    if (tcols != 0 && threadIdx.x < 32) tc_alloc(reinterpret_cast<uint32_t*>(smraw + kFwdTcBase + 8), tcols);
+    pdl_entry();
     FwdSmem S;
     S.ulist = (int*)smraw;
     S.sh = S.ulist + kListCap;
     S.g2s = (float*)(S.sh + 64);
     S.g1s = S.g2s + (size_t)(P.r1_max + 4) * P.N_max;
+    S.tc = smraw + kFwdTcBase;
     switch (DC >= 0 ? DC : T.dclass) {
         case kQ444R32: fwd_T_group(P, T, SDims<4, 4, 4, 32, 32>{}, i2, half, S); break;
         case kQ444R16: fwd_T_group(P, T, SDims<4, 4, 4, 16, 16>{}, i2, half, S); break;
@@ -497,7 +681,7 @@ int dim_class_of(int q1, int q2, int q3, int r1, int r2) { return dim_class(q1, 
 
 template <int DC>
 static cudaError_t launch_fwd_T_dc(const Params& P, cudaStream_t s) {
-    const size_t smem = fwd_smem_bytes(P.r1_max, P.N_max);
+    const size_t smem = fwd_smem_bytes(P.r1_max, P.N_max, P.fwd_tc_floats);
     cudaError_t le = launch_pdl(k_fwd_T<DC>, dim3(P.n2 * P.fwd_split + (P.small ? 3 : 0)), dim3(kFwdThreads), smem, s, P);
     if (le != cudaSuccess) return le;
     return cudaGetLastError();

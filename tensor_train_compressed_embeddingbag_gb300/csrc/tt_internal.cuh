@@ -74,6 +74,7 @@ struct Params {
     int s2_max;                     // max r1 q2 r2 (dG2 partial stride)
     int tile_cap;                   // max lookups per tile (power of two, <= kTileThreads)
     int r1_max, N_max, q1N_max;     // max r1, q2 r2 and q1 q2 r2 over the tables
+    int fwd_tc_floats;              // k_fwd_T tensor-core operand tiles (max over the tables that use them)
     int p1_max;
     int split;                      // column splits of r2 in k_tile_bwd (1 or 2)
     int small;                      // 1: chunk-rank path (nnz <= kSmallMaxNnz); pi21 is then ordered by (i2, pos)
@@ -304,43 +305,62 @@ __device__ __forceinline__ void scatter_chunk(const Params& P, int c) {
 }
 
 // Small path: exclusive scan of digit k's [bin][chunk] histogram (k = 0: i1,
-// 1: i2, 2: i3) by one block, in place in global memory.  Thread per bin: it
-// loads the bin's nch chunk counts together (they are contiguous), the block
-// scans the bin totals, and the thread writes the bin's running prefix.  The
-// i2 block then cuts every (table, i2) group into tiles of <= tile_cap lookups.
+// 1: i2, 2: i3) by one block, in place in global memory.  Rounds of blockDim
+// bins: the round's rows (contiguous) are copied to shared memory with coalesced
+// int4 loads, eight in flight per thread; a thread per bin sums its row, the
+// block scans the bin totals, the thread rewrites its row as running prefixes,
+// and the rows go back with coalesced stores.  The i2 block then cuts every
+// (table, i2) group into tiles of <= tile_cap lookups.  sm: kScanSmemInts ints.
 constexpr int kScanChunkMax = 48;  // >= kSmallMaxNnz / kSmallChunk
-__device__ __forceinline__ void scan_digit_block(const Params& P, int k, int* sh) {
+constexpr int kScanBlock = 256;    // threads of the scanning block
+constexpr int kScanSmemInts = 64 + kScanBlock * kScanChunkMax;
+__device__ __forceinline__ void scan_digit_block(const Params& P, int k, int* sm) {
+    int* sh = sm;
+    int* hs = sm + 64;  // 16-byte aligned when sm is
     const int nb = k == 0 ? P.n1 : (k == 1 ? P.n2 : P.n3);
     int* H = k == 0 ? P.H1 : (k == 1 ? P.H2 : P.H3);
     const int nch = P.nch;  // <= kScanChunkMax on this path
     int carry = 0, tcarry = 0;
-    for (int b0 = 0; b0 < nb; b0 += blockDim.x) {
-        const int b = b0 + threadIdx.x;
-        int v[kScanChunkMax];
-        int tot = 0;
+    for (int b0 = 0; b0 < nb; b0 += kScanBlock) {
+        const int nbr = min(kScanBlock, nb - b0);
+        const int n = nbr * nch, n4 = n >> 2;
+        int* src = H + (int64_t)b0 * nch;  // 16-byte aligned: H is, and b0 nch is a multiple of 256
+        for (int base = 0; base < n4; base += 8 * kScanBlock) {
+            int4 v[8];
 #pragma unroll
-        for (int c = 0; c < kScanChunkMax; ++c) {
-            v[c] = (b < nb && c < nch) ? H[(int64_t)b * nch + c] : 0;
-            tot += v[c];
+            for (int q = 0; q < 8; ++q) {
+                const int e = base + q * kScanBlock + threadIdx.x;
+                if (e < n4) v[q] = reinterpret_cast<const int4*>(src)[e];
+            }
+#pragma unroll
+            for (int q = 0; q < 8; ++q) {
+                const int e = base + q * kScanBlock + threadIdx.x;
+                if (e < n4) reinterpret_cast<int4*>(hs)[e] = v[q];
+            }
         }
+        for (int e = 4 * n4 + threadIdx.x; e < n; e += kScanBlock) hs[e] = src[e];
+        __syncthreads();
+        const int bl = threadIdx.x, b = b0 + bl;
+        int tot = 0;
+        if (bl < nbr)
+            for (int c = 0; c < nch; ++c) tot += hs[bl * nch + c];
         int total;
         const int start = carry + block_scan_excl(tot, sh, &total);
-        if (b < nb) {
+        if (bl < nbr) {
             int run = start;
-#pragma unroll
-            for (int c = 0; c < kScanChunkMax; ++c)
-                if (c < nch) {
-                    H[(int64_t)b * nch + c] = run;
-                    run += v[c];
-                }
+            for (int c = 0; c < nch; ++c) {
+                const int x = hs[bl * nch + c];
+                hs[bl * nch + c] = run;
+                run += x;
+            }
         }
         carry += total;
         if (k == 1) {  // tiles of the (table, i2) groups of this round of bins
             const int cap = P.tile_cap;
-            const int nt = b < nb ? (tot + cap - 1) / cap : 0;
+            const int nt = bl < nbr ? (tot + cap - 1) / cap : 0;
             int ttot;
             const int first = tcarry + block_scan_excl(nt, sh, &ttot);
-            if (b < nb) {
+            if (bl < nbr) {
                 P.grp_first[b] = first;
                 P.grp_ntiles[b] = nt;
                 for (int t = 0; t < nt; ++t)
@@ -348,6 +368,10 @@ __device__ __forceinline__ void scan_digit_block(const Params& P, int k, int* sh
             }
             tcarry += ttot;
         }
+        __syncthreads();
+        for (int e = threadIdx.x; e < n4; e += kScanBlock) reinterpret_cast<int4*>(src)[e] = reinterpret_cast<const int4*>(hs)[e];
+        for (int e = 4 * n4 + threadIdx.x; e < n; e += kScanBlock) src[e] = hs[e];
+        __syncthreads();  // the next round reuses hs
     }
     if (k == 1 && threadIdx.x == 0) *P.ntiles = tcarry;
 }
@@ -396,6 +420,7 @@ cudaError_t launch_scatter13(const Params& P, cudaStream_t s);
 cudaError_t launch_scan2_tiles(const Params& P, cudaStream_t s);
 cudaError_t launch_scatter2(const Params& P, cudaStream_t s);
 cudaError_t launch_fwd_T(const Params& P, cudaStream_t s);
+int fwd_tc_floats_of(int dclass, int r1, int N);
 cudaError_t launch_pool(const Params& P, cudaStream_t s);
 cudaError_t launch_tile_bwd(const Params& P, cudaStream_t s);
 cudaError_t launch_reduce13(const Params& P, cudaStream_t s);

@@ -50,7 +50,7 @@ def test_status_strings(lib):
     assert "index" in tt.tt_emb_status_string(tt.TT_ERR_INDEX)
 
 
-def _create(lib, E, p, q, r, cores=(1, 1, 1)):
+def _create(lib, E, p, q, r, cores=(256, 512, 768)):
     h = ctypes.c_void_p()
     ptrs = (ctypes.c_void_p * 3)(*cores)
     st = lib.tt_emb_create(E, (ctypes.c_int64 * 3)(*p), (ctypes.c_int32 * 3)(*q), (ctypes.c_int32 * 2)(*r),
@@ -76,8 +76,12 @@ def test_bad_shapes_rejected_before_any_cuda_call(lib, E, p, q, r):
 
 
 def test_null_arguments_rejected(lib):
-    st, h = _create(lib, 120, [4, 5, 6], [2, 2, 2], [4, 4], cores=(1, 0, 1))
+    st, h = _create(lib, 120, [4, 5, 6], [2, 2, 2], [4, 4], cores=(256, 0, 256))
     assert st == tt.TT_ERR_ARG
+    # cores must be 16-byte aligned (the kernels read them as float4)
+    st, h = _create(lib, 120, [4, 5, 6], [2, 2, 2], [4, 4], cores=(256, 260, 256))
+    assert st == tt.TT_ERR_ARG
+    assert not h.value
     h = ctypes.c_void_p()
     assert lib.tt_emb_batch_create(0, None, ctypes.byref(h)) == tt.TT_ERR_ARG
     assert lib.tt_emb_forward(None, None, 0, None, 0, None, 0, None, None) == tt.TT_ERR_ARG
