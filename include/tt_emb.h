@@ -56,6 +56,15 @@ typedef enum {
 
 typedef enum { TT_POOL_SUM = 0, TT_POOL_MEAN = 1 } tt_pool;
 
+/* What tt_emb_backward does with the gradient g of each element of every
+ * touched core slice (FBTT README, "Parameters": sparse, optimizer,
+ * learning_rate, eps; "Fused Kernel"). */
+typedef enum {
+    TT_OPT_SGD = 0,     /* sparse=True, SGD:     G -= lr g                                   */
+    TT_OPT_ADAGRAD = 1, /* sparse=True, Adagrad: s += g^2; G -= lr g / (sqrt(s) + eps)       */
+    TT_OPT_GRAD = 2     /* sparse=False: the gradient is written out, the cores stay as they are */
+} tt_optim;
+
 /* Limits checked by the create calls. */
 #define TT_MAX_P 1048576 /* each p_k */
 #define TT_MAX_Q 64      /* each q_k */
@@ -137,6 +146,29 @@ tt_status tt_emb_forward(tt_emb* h, const int64_t* indices_dev, int64_t nnz,
  * error, no core is changed.  Asynchronous on `stream`.
  */
 tt_status tt_emb_backward(tt_emb* h, const float* grad_out_dev, float lr, tt_stream stream);
+
+/*
+ * Choose the update that tt_emb_backward applies (default TT_OPT_SGD; the
+ * tt_emb_backward description above is the SGD case).  FBTT README,
+ * "Parameters": sparse selects between the fused update and returning the
+ * core gradients to an external optimizer; optimizer and eps configure the
+ * fused update.  No page fixes the Adagrad variant: this is element-wise
+ * Adagrad with one accumulator per core element, lr_decay and weight decay 0.
+ *   optim  TT_OPT_SGD, TT_OPT_ADAGRAD or TT_OPT_GRAD
+ *   eps    Adagrad denominator term, finite and >= 0 (ignored otherwise)
+ *   aux    3 * num_tables caller-owned device pointers, table-major
+ *          (aux[3 t + k] belongs to core k of table t), each with the shape of
+ *          that core, 16-byte aligned; NULL for TT_OPT_SGD.
+ *            TT_OPT_ADAGRAD: the accumulators s, read and updated in place
+ *              (a new run starts them at 0, or at an initial value >= 0);
+ *            TT_OPT_GRAD: every tt_emb_backward overwrites the whole buffer
+ *              with dL/dG_k (zeros for untouched slices).
+ * The handle keeps the pointers, which must stay valid while it is used.
+ * Synchronous (copies the handle's device tables); not for stream capture.
+ * Returns TT_ERR_ARG (null handle, unknown optim, bad eps, null or misaligned
+ * aux), TT_ERR_CUDA.
+ */
+tt_status tt_emb_set_optimizer(tt_emb* h, int32_t optim, float eps, float* const* aux);
 
 /*
  * Hot-row cache (FBTT README, "Software Cache"): decompress the n rows of

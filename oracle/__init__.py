@@ -6,10 +6,15 @@ never loads it, and it imports nothing from the product package.
 
 The arithmetic lives in ``tt_oracle.c`` (plain C, float64, definition written
 out per lookup, see its header).  This module compiles it with gcc, promotes
-the float32 cores to float64 and marshals arrays; the SGD step
-``G <- G - lr dG`` (FBTT README, "Fused Kernel": the update is applied inside
-the backward pass; every gradient is taken at the pre-update cores) is the one
-line of arithmetic done here.
+the float32 cores to float64 and marshals arrays; the optimizer steps are the
+only arithmetic done here (FBTT README, "Fused Kernel": the update is applied
+inside the backward pass; every gradient is taken at the pre-update cores;
+"Parameters": optimizer, learning_rate, eps):
+
+* SGD: ``G <- G - lr dG``;
+* Adagrad, element-wise (the pages name the optimizer and its eps but no
+  variant; the plainest reading is the textbook one, one accumulator per core
+  element): ``s <- s + dG^2``, ``G <- G - lr dG / (sqrt(s) + eps)``.
 
 Tables are any objects with ``num_embeddings``, ``p``, ``q`` and ``ranks``
 attributes; cores are ``[p_k, r_{k-1}, q_k, r_k]`` arrays.
@@ -193,6 +198,21 @@ def sgd_slices(tables, cores, indices, offsets, grad_out, lr, table, core, weigh
     return np.asarray(cores[table][core], dtype=np.float64)[sl] - float(lr) * dG
 
 
+def adagrad_slices(tables, cores, indices, offsets, grad_out, lr, eps, state, table, core, weights=None,
+                   mode="sum", bags_per_table=None, slices=None):
+    """Element-wise Adagrad on ``slices`` of core ``core`` of ``table``; ``state`` is that core's accumulator.
+
+    Returns float64 ``(updated slices, updated accumulator slices)``.
+    """
+    spec = tables[table]
+    sl = np.arange(int(spec.p[core]), dtype=np.int64) if slices is None else _i64(slices)
+    dG = backward_core(tables, cores, indices, offsets, grad_out, table, core, weights, mode,
+                       bags_per_table, sl)
+    s_new = np.asarray(state, dtype=np.float64)[sl] + dG * dG
+    g_new = np.asarray(cores[table][core], dtype=np.float64)[sl] - float(lr) * dG / (np.sqrt(s_new) + float(eps))
+    return g_new, s_new
+
+
 def sgd_step(tables, cores, indices, offsets, grad_out, lr, weights=None, mode="sum", bags_per_table=None):
     """Every core of every table after one fused SGD step, float64."""
     return [
@@ -211,6 +231,12 @@ def workload_backward_core(w, table, core, slices=None, cores=None):
     """``backward_core`` on a ``tt_inputs.Workload``."""
     return backward_core(w.tables, cores or w.cores, w.indices, w.offsets, w.grad_out, table, core,
                          w.weights, w.mode, w.batch, slices)
+
+
+def workload_adagrad_slices(w, table, core, state, eps, slices=None, cores=None):
+    """``adagrad_slices`` on a ``tt_inputs.Workload`` with its learning rate."""
+    return adagrad_slices(w.tables, cores or w.cores, w.indices, w.offsets, w.grad_out, w.lr, eps, state, table,
+                          core, w.weights, w.mode, w.batch, slices)
 
 
 def workload_sgd_slices(w, table, core, slices=None, cores=None):

@@ -9,9 +9,11 @@ without the built library every call raises.
 Low-level functions carry the C ABI's names (``include/tt_emb.h``):
 ``tt_emb_create``, ``tt_emb_batch_create``, ``tt_emb_forward``,
 ``tt_emb_backward``, ``tt_emb_cache_populate`` ...  ``TTEmbeddingBag`` and
-``TableBatchedTTEmbeddingBag`` wrap them as ``torch.nn.Module`` s whose
-backward pass applies the fused SGD update to the cores and returns no
-gradient for them (FBTT README, "Fused Kernel", sparse=True).
+``TableBatchedTTEmbeddingBag`` wrap them as ``torch.nn.Module`` s.  With
+``sparse=True`` (default) the backward pass applies the fused update (SGD or
+Adagrad) to the cores and returns no gradient for them (FBTT README, "Fused
+Kernel"); with ``sparse=False`` the cores' gradients are returned to autograd
+for an external optimizer (FBTT README, "Parameters": sparse).
 """
 from __future__ import annotations
 
@@ -36,6 +38,7 @@ __all__ = [
     "tt_emb_reserve",
     "tt_emb_forward",
     "tt_emb_backward",
+    "tt_emb_set_optimizer",
     "tt_emb_cache_populate",
     "tt_emb_cache_disable",
     "tt_emb_get_decoded",
@@ -52,6 +55,7 @@ __all__ = [
 
 TT_OK, TT_ERR_ARG, TT_ERR_SHAPE, TT_ERR_INDEX, TT_ERR_CUDA, TT_ERR_STATE, TT_ERR_TIMEOUT, TT_ERR_NOMEM = range(8)
 TT_POOL_SUM, TT_POOL_MEAN = 0, 1
+TT_OPT_SGD, TT_OPT_ADAGRAD, TT_OPT_GRAD = 0, 1, 2
 
 EXPORTED_SYMBOLS = (
     "tt_emb_create",
@@ -60,6 +64,7 @@ EXPORTED_SYMBOLS = (
     "tt_emb_reserve",
     "tt_emb_forward",
     "tt_emb_backward",
+    "tt_emb_set_optimizer",
     "tt_emb_cache_populate",
     "tt_emb_cache_disable",
     "tt_emb_get_decoded",
@@ -119,6 +124,7 @@ def load_library():
             "tt_emb_reserve": (ctypes.c_int, [vp, i64, i64]),
             "tt_emb_forward": (ctypes.c_int, [vp, vp, i64, vp, i64, vp, ctypes.c_int, vp, vp]),
             "tt_emb_backward": (ctypes.c_int, [vp, vp, f32, vp]),
+            "tt_emb_set_optimizer": (ctypes.c_int, [vp, i32, f32, ctypes.POINTER(vp)]),
             "tt_emb_cache_populate": (ctypes.c_int, [vp, vp, i64, vp]),
             "tt_emb_cache_disable": (ctypes.c_int, [vp]),
             "tt_emb_get_decoded": (ctypes.c_int, [vp, vp, vp, vp, vp, vp, vp]),
@@ -217,6 +223,20 @@ def tt_emb_backward(h, grad_out: torch.Tensor, lr: float, stream=None):
     _check(load_library().tt_emb_backward(h, _ptr(grad_out), float(lr), _stream(stream)), "tt_emb_backward")
 
 
+def tt_emb_set_optimizer(h, optim: int, eps: float = 0.0, aux: Optional[Sequence[torch.Tensor]] = None):
+    """What tt_emb_backward does with the core gradients (TT_OPT_SGD / TT_OPT_ADAGRAD / TT_OPT_GRAD).
+
+    aux: 3 * num_tables float32 device tensors shaped like the cores (table-major):
+    the Adagrad accumulators, or the gradient buffers for TT_OPT_GRAD.
+    """
+    arr = None
+    if aux is not None:
+        for t in aux:
+            _cuda_f32(t, "aux")
+        arr = (ctypes.c_void_p * len(aux))(*[t.data_ptr() for t in aux])
+    _check(load_library().tt_emb_set_optimizer(h, int(optim), float(eps), arr), "tt_emb_set_optimizer")
+
+
 def tt_emb_cache_populate(h, rows: torch.Tensor, stream=None):
     _check(load_library().tt_emb_cache_populate(h, _ptr(rows), rows.numel(), _stream(stream)), "tt_emb_cache_populate")
 
@@ -295,14 +315,38 @@ class _TTBagFunction(torch.autograd.Function):
     def backward(ctx, grad_out):
         m = ctx.module
         tt_emb_backward(m._h, grad_out.contiguous(), m.learning_rate)
-        return (None,) * (5 + len(m._core_list()))
+        if m.sparse:  # fused update: no gradient leaves the module
+            return (None,) * (5 + len(m._core_list()))
+        return (None,) * 5 + tuple(m._grad_bufs)
 
 
 class _TTBase(torch.nn.Module):
     _h = None
+    sparse = True
 
     def _core_list(self) -> List[torch.Tensor]:
         raise NotImplementedError
+
+    def _set_optimizer(self, sparse: bool, optimizer: str, eps: float):
+        """FBTT README, "Parameters": sparse, optimizer, eps."""
+        opt = optimizer.lower()
+        if opt not in ("sgd", "adagrad"):
+            raise ValueError("optimizer must be 'sgd' or 'adagrad'")
+        self.sparse, self.optimizer, self.eps = bool(sparse), opt, float(eps)
+        self._grad_bufs = []
+        if not self.sparse:
+            self._grad_bufs = [torch.zeros_like(c) for c in self._core_list()]
+            tt_emb_set_optimizer(self._h, TT_OPT_GRAD, 0.0, self._grad_bufs)
+        elif opt == "adagrad":
+            for i, c in enumerate(self._core_list()):
+                self.register_buffer(f"adagrad_state{i}", torch.zeros_like(c.detach()))
+            tt_emb_set_optimizer(self._h, TT_OPT_ADAGRAD, self.eps, self.adagrad_states())
+        else:
+            tt_emb_set_optimizer(self._h, TT_OPT_SGD)
+
+    def adagrad_states(self) -> List[torch.Tensor]:
+        """The per-element Adagrad accumulators, one per core (sparse=True, optimizer='adagrad')."""
+        return [getattr(self, f"adagrad_state{i}") for i in range(len(self._core_list()))]
 
     def _run(self, indices, offsets, per_sample_weights, mode, include_last_offset):
         if mode not in ("sum", "mean"):
@@ -326,7 +370,10 @@ class _TTBase(torch.nn.Module):
 
 
 class TTEmbeddingBag(_TTBase):
-    """TT-compressed EmbeddingBag with fused SGD (FBTT README, "Parameters" and "Fused Kernel").
+    """TT-compressed EmbeddingBag (FBTT README, "Parameters" and "Fused Kernel").
+
+    sparse=True fuses the update (optimizer 'sgd' or 'adagrad', learning_rate,
+    eps) into the backward pass; sparse=False returns the cores' gradients.
 
     cores: optional initial cores ``[G1, G2, G3]`` with shapes
     ``[p_k, r_{k-1}, q_k, r_k]``; default i.i.d. N(0, sigma).
@@ -335,7 +382,8 @@ class TTEmbeddingBag(_TTBase):
     def __init__(self, num_embeddings: int, embedding_dim: int, tt_ranks: Sequence[int],
                  tt_p_shapes: Sequence[int], tt_q_shapes: Sequence[int], learning_rate: float = 0.1,
                  cores: Optional[Sequence[torch.Tensor]] = None, sigma: float = 0.1, device=None,
-                 use_cache: bool = False, cache_rows: Optional[torch.Tensor] = None):
+                 use_cache: bool = False, cache_rows: Optional[torch.Tensor] = None,
+                 sparse: bool = True, optimizer: str = "sgd", eps: float = 1.0e-10):
         super().__init__()
         device = torch.device(device or "cuda")
         q = list(tt_q_shapes)
@@ -355,6 +403,7 @@ class TTEmbeddingBag(_TTBase):
             if tuple(c.shape) != shapes[k]:
                 raise ValueError(f"core {k} has shape {tuple(c.shape)}, expected {shapes[k]}")
         self._h = tt_emb_create(self.num_embeddings, self.p, self.q, self.ranks, self._core_list())
+        self._set_optimizer(sparse, optimizer, eps)
         if use_cache and cache_rows is not None:
             self.cache_populate(cache_rows)
 
@@ -377,7 +426,8 @@ class TableBatchedTTEmbeddingBag(_TTBase):
     t * B + b is sample b of table t; the output is [num_tables * B, D].
     """
 
-    def __init__(self, tables, learning_rate: float = 0.1, sigma: float = 0.1, device=None):
+    def __init__(self, tables, learning_rate: float = 0.1, sigma: float = 0.1, device=None,
+                 sparse: bool = True, optimizer: str = "sgd", eps: float = 1.0e-10):
         super().__init__()
         device = torch.device(device or "cuda")
         self.learning_rate = float(learning_rate)
@@ -396,6 +446,7 @@ class TableBatchedTTEmbeddingBag(_TTBase):
         self.embedding_dim = int(self.specs[0][2][0] * self.specs[0][2][1] * self.specs[0][2][2])
         self._cores = params
         self._h = tt_emb_batch_create([(E, p, q, r, params[i]) for i, (E, p, q, r) in enumerate(self.specs)])
+        self._set_optimizer(sparse, optimizer, eps)
 
     def _core_list(self):
         return [c for cs in self._cores for c in cs]

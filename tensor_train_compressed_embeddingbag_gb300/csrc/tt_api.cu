@@ -527,6 +527,14 @@ tt_status tt_emb_backward(tt_emb* h, const float* grad_out, float lr, tt_stream 
     P.step = h->step;
     P.slice_stamp = h->d_slice_stamp;
     Seq q(h, 1, s);
+    if (P.opt == TT_OPT_GRAD) {  // untouched slices have a zero gradient
+        for (const TableDev& T : h->tabs) {
+            const size_t n[3] = {(size_t)T.p1 * T.q1 * T.r1, (size_t)T.p2 * T.r1 * T.q2 * T.r2,
+                                 (size_t)T.p3 * T.r2 * T.q3};
+            for (int k = 0; k < 3; ++k)
+                if (cudaMemsetAsync(T.aux[k], 0, sizeof(float) * n[k], s) != cudaSuccess) return TT_ERR_CUDA;
+        }
+    }
     if (P.nnz > 0) {
         q.run("tile_bwd", launch_tile_bwd);
         q.run("reduce13", launch_reduce13);
@@ -534,6 +542,29 @@ tt_status tt_emb_backward(tt_emb* h, const float* grad_out, float lr, tt_stream 
     tt_status st = q.finish();
     if (h->cache_n > 0) ++h->step;
     return st;
+}
+
+tt_status tt_emb_set_optimizer(tt_emb* h, int32_t optim, float eps, float* const* aux) {
+    if (!h) return TT_ERR_ARG;
+    if (optim != TT_OPT_SGD && optim != TT_OPT_ADAGRAD && optim != TT_OPT_GRAD) return TT_ERR_ARG;
+    if (optim == TT_OPT_ADAGRAD && !(eps >= 0.f && eps <= 3.0e38f)) return TT_ERR_ARG;
+    if (optim != TT_OPT_SGD) {
+        if (!aux) return TT_ERR_ARG;
+        for (int i = 0; i < 3 * h->ntab; ++i)
+            if (!aux[i] || ((uintptr_t)aux[i] & 15u) != 0) return TT_ERR_ARG;
+    }
+    std::vector<TableDev> tabs = h->tabs;
+    for (int t = 0; t < h->ntab; ++t)
+        for (int k = 0; k < 3; ++k) tabs[t].aux[k] = optim == TT_OPT_SGD ? nullptr : aux[3 * t + k];
+    if (cudaSetDevice(h->device) != cudaSuccess ||
+        cudaMemcpy(h->d_tables, tabs.data(), sizeof(TableDev) * tabs.size(), cudaMemcpyHostToDevice) != cudaSuccess) {
+        cudaGetLastError();
+        return TT_ERR_CUDA;
+    }
+    h->tabs = tabs;
+    h->P.opt = optim;
+    h->P.eps = eps;
+    return TT_OK;
 }
 
 tt_status tt_emb_cache_populate(tt_emb* h, const int64_t* rows_dev, int64_t n, tt_stream stream) {

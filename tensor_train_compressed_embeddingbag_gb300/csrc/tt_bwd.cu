@@ -125,6 +125,8 @@ __device__ void reduce_slice(const Params& P, int bglob, int* slots, int* sh, fl
     const int stride = first_core ? P.qs_max : P.ps_max;
     const float* buf = first_core ? P.Qbuf : P.Pbuf;
     float* G = (first_core ? T.G1 : T.G3) + (int64_t)slice * S;
+    float* A = (first_core ? T.aux[0] : T.aux[2]);
+    if (A) A += (int64_t)slice * S;
     const int W = S >= kBwdThreads ? kBwdThreads : S;  // threads per lane group
     const int R = S >= kBwdThreads ? 1 : kBwdThreads / S;
     const int r = threadIdx.x / W;
@@ -169,13 +171,13 @@ __device__ void reduce_slice(const Params& P, int bglob, int* slots, int* sh, fl
         __syncthreads();
     }
     if (R == 1) {
-        for (int e = threadIdx.x; e < S; e += blockDim.x) G[e] = fmaf(-P.lr, sacc[e], G[e]);
+        for (int e = threadIdx.x; e < S; e += blockDim.x) core_update(P, G, A, e, sacc[e]);
     } else if (threadIdx.x < S) {
         float sum = 0.f;  // the R lane groups' sums in group order
         for (int rr = 0; rr < R; ++rr) sum += sacc[rr * S + threadIdx.x];
-        G[threadIdx.x] = fmaf(-P.lr, sum, G[threadIdx.x]);
+        core_update(P, G, A, threadIdx.x, sum);
     }
-    if (P.slice_stamp && threadIdx.x == 0 && t == 0)
+    if (P.slice_stamp && P.opt != TT_OPT_GRAD && threadIdx.x == 0 && t == 0)
         P.slice_stamp[first_core ? slice : T.p1 + T.p2 + slice] = P.step + 1;
     __syncthreads();
 }
@@ -409,6 +411,7 @@ __device__ void tile_bwd_body(const Params& P, const TableDev& T, const Dm dm, u
     // ---- pairs in batches: dT, dG1 partial (Q), dG2 accumulation
     const int PB = bwd_pairs_per_batch(q1, Ns, r1);
     float* G2p = T.G2 + (int64_t)i2 * r1 * q2 * r2;
+    float* A2p = T.aux[1] ? T.aux[1] + (int64_t)i2 * r1 * q2 * r2 : nullptr;
 
     if constexpr (Dm::kStatic) {
         using BT = BwdTiling<Dm, SPLIT>;
@@ -599,12 +602,12 @@ __device__ void tile_bwd_body(const Params& P, const TableDev& T, const Dm dm, u
                     for (int c = 0; c < 4; ++c) {
                         const int aa = ag + A4 * a, jc = jg + JG * c, j2 = jc / R2S, cc = c0 + (jc - j2 * R2S);
                         const int ga = (aa * Q2 + j2) * R2 + cc;
-                        if (nt == 1) G2p[ga] = fmaf(-P.lr, acc2[i][a][c], G2p[ga]);
+                        if (nt == 1) core_update(P, G2p, A2p, ga, acc2[i][a][c]);
                         else part[aa * NS + jc] = acc2[i][a][c];
                     }
             }
         }
-        if (nt == 1 && P.slice_stamp && threadIdx.x == 0 && t == 0) P.slice_stamp[T.p1 + i2] = P.step + 1;
+        if (nt == 1 && P.slice_stamp && P.opt != TT_OPT_GRAD && threadIdx.x == 0 && t == 0) P.slice_stamp[T.p1 + i2] = P.step + 1;
     } else {
         // generic dimensions
         float acc2[kMaxAcc2];
@@ -663,11 +666,11 @@ __device__ void tile_bwd_body(const Params& P, const TableDev& T, const Dm dm, u
                 const int a = e / Ns, jc = e - a * Ns;
                 const int j2 = jc / r2s, c = c0 + (jc - j2 * r2s);
                 const int ga = (a * q2 + j2) * r2 + c;
-                if (nt == 1) G2p[ga] = fmaf(-P.lr, acc2[m], G2p[ga]);
+                if (nt == 1) core_update(P, G2p, A2p, ga, acc2[m]);
                 else part[e] = acc2[m];
             }
         }
-        if (nt == 1 && P.slice_stamp && threadIdx.x == 0 && t == 0) P.slice_stamp[T.p1 + i2] = P.step + 1;
+        if (nt == 1 && P.slice_stamp && P.opt != TT_OPT_GRAD && threadIdx.x == 0 && t == 0) P.slice_stamp[T.p1 + i2] = P.step + 1;
     }
 
     // every partial of this block is written: publish them before any arrival count
@@ -688,11 +691,11 @@ __device__ void tile_bwd_body(const Params& P, const TableDev& T, const Dm dm, u
                 const int a = e / Ns, jc = e - a * Ns;
                 const int j2 = jc / r2s, c = c0 + (jc - j2 * r2s);
                 const int ga = (a * q2 + j2) * r2 + c;
-                G2p[ga] = fmaf(-P.lr, sum, G2p[ga]);
+                core_update(P, G2p, A2p, ga, sum);
             }
             if (threadIdx.x == 0) {
                 P.grp_done[g * SPLIT + sp] = 0;
-                if (P.slice_stamp && t == 0) P.slice_stamp[T.p1 + i2] = P.step + 1;
+                if (P.slice_stamp && P.opt != TT_OPT_GRAD && t == 0) P.slice_stamp[T.p1 + i2] = P.step + 1;
             }
         }
     }

@@ -26,6 +26,8 @@
 #include <cuda_runtime.h>
 #include <stdint.h>
 
+#include "../../include/tt_emb.h"
+
 namespace ttemb {
 
 constexpr int kChunk = 2048;        // lookups per counting-sort chunk
@@ -58,6 +60,7 @@ struct TableDev {
     int base1, base2, base3;  // first global bin of each digit
     int dclass;     // compiled dimension class (tt_dims.cuh)
     int idx32;      // p1 p2 p3 < 2^31: rows decode with 32-bit arithmetic
+    float* aux[3];  // per core: Adagrad state or gradient buffer (tt_emb_set_optimizer), else null
 };
 
 struct Params {
@@ -93,6 +96,8 @@ struct Params {
     float* out;
     const float* grad_out;
     float lr;
+    int opt;                        // tt_optim of the backward: what happens to each core gradient
+    float eps;                      // Adagrad denominator term
     int nch;                        // chunks of kChunk lookups
     int max_tiles;
     // workspace
@@ -143,6 +148,24 @@ struct Params {
 // stream has completed and its writes are visible.  Both are no-ops for a
 // kernel launched without the programmatic-serialization attribute.  Every
 // kernel calls this before its first global memory access.
+// The one write of core element i (of the slice at G, aux) with its gradient g,
+// after every gradient of the step has been taken (FBTT README, "Parameters":
+// sparse, optimizer, learning_rate, eps):
+//   TT_OPT_SGD      G -= lr g
+//   TT_OPT_ADAGRAD  s += g^2;  G -= lr g / (sqrt(s) + eps)      (s = aux, per element)
+//   TT_OPT_GRAD     aux = g, G unchanged                         (sparse = False)
+__device__ __forceinline__ void core_update(const Params& P, float* G, float* aux, int64_t i, float g) {
+    if (P.opt == TT_OPT_SGD) {
+        G[i] = fmaf(-P.lr, g, G[i]);
+    } else if (P.opt == TT_OPT_ADAGRAD) {
+        const float st = fmaf(g, g, aux[i]);
+        aux[i] = st;
+        G[i] -= P.lr * g / (sqrtf(st) + P.eps);
+    } else {
+        aux[i] = g;
+    }
+}
+
 __device__ __forceinline__ void pdl_entry() {
     asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
     asm volatile("griddepcontrol.wait;" ::: "memory");

@@ -86,6 +86,7 @@ def test_null_arguments_rejected(lib):
     assert lib.tt_emb_batch_create(0, None, ctypes.byref(h)) == tt.TT_ERR_ARG
     assert lib.tt_emb_forward(None, None, 0, None, 0, None, 0, None, None) == tt.TT_ERR_ARG
     assert lib.tt_emb_backward(None, None, ctypes.c_float(0.1), None) == tt.TT_ERR_ARG
+    assert lib.tt_emb_set_optimizer(None, tt.TT_OPT_SGD, ctypes.c_float(0.0), None) == tt.TT_ERR_ARG
     assert lib.tt_emb_reserve(None, 1, 1) == tt.TT_ERR_ARG
     assert lib.tt_emb_get_last_error(None) == tt.TT_ERR_ARG
     assert lib.tt_emb_last_launch_count(None, 0) == -1

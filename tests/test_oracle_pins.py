@@ -18,6 +18,8 @@ an independent route to the same numbers.
 * Invariants: duplicates act as weight 2, order inside a bag does not
   matter, mean = sum / L_b, linearity in grad_out, untouched slices keep
   their exact bits under SGD, batched tables equal separate tables.
+* Adagrad: two oracle steps equal torch.optim.Adagrad fed the same
+  gradients, from a zero and from a warm accumulator.
 """
 import itertools
 import json
@@ -289,3 +291,32 @@ def test_tiny_workload_golden():
         np.testing.assert_allclose(
             oracle.workload_sgd_slices(wl, 0, k), np.array(g["updated_cores"][k]), rtol=1e-15, atol=1e-15
         )
+
+
+@pytest.mark.parametrize("init", [0.0, 0.7])
+def test_adagrad_matches_torch_optim(init):
+    """Two fused element-wise Adagrad steps of the oracle (gradients at the
+    pre-update cores of each step) equal torch.optim.Adagrad fed the same
+    gradients: the update rule is pinned to an independent implementation."""
+    rng = np.random.default_rng(11)
+    spec = TableSpec(100, [5, 4, 6], [2, 3, 2], [3, 5])
+    cores = rand_cores(rng, spec)
+    B = 6
+    lengths = rng.integers(1, 5, size=B)
+    off = np.concatenate([[0], np.cumsum(lengths)])
+    idx = rng.integers(0, 100, size=int(off[-1]))
+    go = rng.standard_normal((B, 12))
+    lr, eps = 0.05, 1e-10
+    params = [torch.from_numpy(c.copy()).requires_grad_(True) for c in cores]
+    opt = torch.optim.Adagrad(params, lr=lr, eps=eps, initial_accumulator_value=init)
+    cur = [c.copy() for c in cores]
+    state = [np.full(c.shape, init) for c in cores]
+    for _ in range(2):
+        upd = [oracle.adagrad_slices([spec], [cur], idx, off, go, lr, eps, state[k], 0, k) for k in range(3)]
+        for k in range(3):
+            params[k].grad = torch.from_numpy(oracle.backward_core([spec], [cur], idx, off, go, 0, k))
+        opt.step()
+        cur, state = [u[0] for u in upd], [u[1] for u in upd]
+        for k in range(3):
+            np.testing.assert_allclose(cur[k], params[k].detach().numpy(), rtol=1e-12, atol=1e-14)
+            np.testing.assert_allclose(state[k], opt.state[params[k]]["sum"].numpy(), rtol=1e-12, atol=1e-14)
