@@ -105,6 +105,7 @@ __device__ __forceinline__ void stage_g1_rows(float* g1s, const float* G1, const
 template <int R1, int NN>
 __device__ void fwd_T_group_tc(const Params& P, const TableDev& T, int i2, int half, FwdSmem S) {
     static_assert(R1 % 8 == 0 && R1 <= 32 && NN % 32 == 0 && NN <= 128, "tensor-core tile shapes");
+    static_assert(2 * kTcTiles * kTcM * R1 >= (kFwdThreads / 32) * 1024, "write-out buffers fit in the A tiles (hi and lo)");
     constexpr uint32_t kIdesc = tc_idesc_tf32(kTcM, NN);
     constexpr uint32_t kLbo = 128, kSbo = R1 * 32;  // K core matrices / 8-row groups, bytes
     constexpr int kBQ = (R1 / 4) * NN;              // float4 quads of B
@@ -216,22 +217,36 @@ __device__ void fwd_T_group_tc(const Params& P, const TableDev& T, int i2, int h
             }
             __syncthreads();
             tc_fence_after();
-            // warp w reads tile w / 4, lanes 32 (w % 4) .. + 31 (its rows), all N columns
+            // warp w reads tile w / 4, lanes 32 (w % 4) .. + 31 (its 32 rows), all N columns, 32 at
+            // a time; each 32 x 32 block goes through a private shared buffer (the A tiles are free
+            // now; float4 chunk q of row r sits at chunk q ^ (r & 7), so neither side has bank
+            // conflicts) and leaves as four full 128-byte row segments per store instruction.
             const int t = w >> 2;
             if (*okflag && t < ntl) {
-                const int row = 32 * (w & 3) + lane, u = t * (kTcM / 4) + (row >> 2), j1 = row & 3;
-                const uint32_t taddr = *tslot + ((uint32_t)(32 * (w & 3)) << 16) + (uint32_t)(t * NN);
-                float* dst = nullptr;
-                if (u < gn) dst = P.Tbuf + T.tbase + (((int64_t)i2 * T.p1 + S.ulist[g0 + u]) * 4 + j1) * NN;
-#pragma unroll
+                const int rbase = 32 * (w & 3);  // first row (tensor-memory lane) of this warp in tile t
+                const uint32_t taddr = *tslot + ((uint32_t)rbase << 16) + (uint32_t)(t * NN);
+                float* buf = Ah + w * 1024;
+                const int q = lane & 7;
+#pragma unroll 1
                 for (int c0 = 0; c0 < NN; c0 += 32) {
                     float v[32];
                     tc_ld32(taddr + c0, v);
-                    if (dst) {
 #pragma unroll
-                        for (int i = 0; i < 32; i += 4)
-                            *reinterpret_cast<float4*>(dst + c0 + i) = make_float4(v[i], v[i + 1], v[i + 2], v[i + 3]);
+                    for (int k = 0; k < 8; ++k)
+                        *reinterpret_cast<float4*>(buf + lane * 32 + ((k ^ (lane & 7)) << 2)) =
+                            make_float4(v[4 * k], v[4 * k + 1], v[4 * k + 2], v[4 * k + 3]);
+                    __syncwarp();
+#pragma unroll
+                    for (int i = 0; i < 8; ++i) {
+                        const int r = 4 * i + (lane >> 3);
+                        const int row = rbase + r, u = t * (kTcM / 4) + (row >> 2), j1 = row & 3;
+                        const float4 x = *reinterpret_cast<const float4*>(buf + r * 32 + ((q ^ (r & 7)) << 2));
+                        if (u < gn)
+                            *reinterpret_cast<float4*>(P.Tbuf + T.tbase +
+                                                       (((int64_t)i2 * T.p1 + S.ulist[g0 + u]) * 4 + j1) * NN + c0 +
+                                                       4 * q) = x;
                     }
+                    __syncwarp();
                 }
             }
             ++nbatch;
