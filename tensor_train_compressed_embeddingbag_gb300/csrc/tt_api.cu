@@ -257,7 +257,8 @@ tt_status build_handle(tt_emb* h, int ntab, const tt_table_desc* d) {
     P.ntab = ntab;
     P.n1 = n1; P.n2 = n2; P.n3 = n3;
     P.D = D;
-    P.qs_max = qs; P.ps_max = ps; P.s2_max = s2;
+    // slot strides in whole 16-byte words: the kernels store the Q and P3 partials as float4
+    P.qs_max = (qs + 3) & ~3; P.ps_max = (ps + 3) & ~3; P.s2_max = s2;
     P.r1_max = r1m; P.N_max = Nm; P.q1N_max = q1Nm; P.fwd_tc_floats = tcf;
     // tile caps: the summed upstream gradient of a tile (cap x D floats) stays <= 16 KB on the
     // single-CTA-sort path (many small tiles) and <= 64 KB on the multi-CTA path

@@ -389,8 +389,14 @@ __device__ void tile_bwd_body(const Params& P, const TableDev& T, const Dm dm, u
                     }
                 }
                 float* dst = P.Pbuf + (int64_t)(start + rowbeg[rowv[v]]) * P.ps_max + cv[v] * Q3;
+                if constexpr (Q3 % 4 == 0) {  // whole 16-byte words: lanes of consecutive c fill whole sectors
 #pragma unroll
-                for (int j3 = 0; j3 < Q3; ++j3) dst[j3] = acc[j3];
+                    for (int j3 = 0; j3 < Q3; j3 += 4)
+                        *reinterpret_cast<float4*>(dst + j3) = make_float4(acc[j3], acc[j3 + 1], acc[j3 + 2], acc[j3 + 3]);
+                } else {
+#pragma unroll
+                    for (int j3 = 0; j3 < Q3; ++j3) dst[j3] = acc[j3];
+                }
             }
         }
     } else {
@@ -429,27 +435,33 @@ __device__ void tile_bwd_body(const Params& P, const TableDev& T, const Dm dm, u
                 for (int c = 0; c < 4; ++c) acc2[i][a][c] = 0.f;
         // dG2 tile of this thread (tile set i adds 8 i to the warp's tile index)
         const int ks = KS > 1 ? w / WT : 0, wt0 = KS > 1 ? w % WT : w;
+        // g1s[u][a][j1] of a batch: GPT values per thread (every compiled class: PBS R1 4 <= 16 kBwdThreads);
+        // the next batch's values are loaded into registers while this batch computes
+        constexpr int GPT = (PBS * R1 * 4 + kBwdThreads - 1) / kBwdThreads;
+        static_assert(GPT <= 16, "G1 prefetch registers");
+        float g1n[GPT];
+        auto load_g1 = [&](int ub) {
+            const int nbb = min(PBS, npairs - ub);
+#pragma unroll
+            for (int q = 0; q < GPT; ++q) {
+                const int e = q * kBwdThreads + threadIdx.x;
+                g1n[q] = 0.f;
+                if (e < nbb * R1 * 4) {
+                    const int u = e / (R1 * 4), rem = e - u * (R1 * 4);
+                    g1n[q] = __ldg(T.G1 + (int64_t)si1[pairbeg[ub + u]] * (4 * R1) + (rem & 3) * R1 + (rem >> 2));
+                }
+            }
+        };
+        if (npairs > 0) load_g1(0);
         for (int u0 = 0; u0 < npairs; u0 += PBS) {
             const int nb = min(PBS, npairs - u0);
             __syncthreads();
-            // g1s[u][a][j1], 8 loads in flight per thread
-            for (int base = 0; base < nb * R1 * 4; base += 8 * kBwdThreads) {
-                float v[8];
 #pragma unroll
-                for (int q = 0; q < 8; ++q) {
-                    const int e = base + q * kBwdThreads + threadIdx.x;
-                    v[q] = 0.f;
-                    if (e < nb * R1 * 4) {
-                        const int u = e / (R1 * 4), rem = e - u * (R1 * 4);
-                        v[q] = __ldg(T.G1 + (int64_t)si1[pairbeg[u0 + u]] * (4 * R1) + (rem & 3) * R1 + (rem >> 2));
-                    }
-                }
-#pragma unroll
-                for (int q = 0; q < 8; ++q) {
-                    const int e = base + q * kBwdThreads + threadIdx.x;
-                    if (e < nb * R1 * 4) g1s[e] = v[q];
-                }
+            for (int q = 0; q < GPT; ++q) {
+                const int e = q * kBwdThreads + threadIdx.x;
+                if (e < nb * R1 * 4) g1s[e] = g1n[q];
             }
+            if (u0 + PBS < npairs) load_g1(u0 + PBS);
             // dts[u][jc'][j1] = sum_rows sum_j3 gs[row][(j1 q2 + j2) q3 + j3] G3[i3][c][j3];
             // kDtUnroll items per thread load the G3 row of their pair's first row together
             for (int e0 = threadIdx.x; e0 < nb * NS; e0 += kDtUnroll * kBwdThreads) {
@@ -597,14 +609,24 @@ __device__ void tile_bwd_body(const Params& P, const TableDev& T, const Dm dm, u
                 const int wt = wt0 + 8 * i;
                 const int ag = (wt % (A4 / AG)) * AG + lane % AG, jg = (wt / (A4 / AG)) * JL + lane / AG;
 #pragma unroll
-                for (int a = 0; a < 4; ++a)
+                for (int ah = 0; ah < 4; ah += 2) {  // two halves of 8 elements (register pressure)
+                    int gidx[8];
+                    float gv[8];
 #pragma unroll
-                    for (int c = 0; c < 4; ++c) {
-                        const int aa = ag + A4 * a, jc = jg + JG * c, j2 = jc / R2S, cc = c0 + (jc - j2 * R2S);
-                        const int ga = (aa * Q2 + j2) * R2 + cc;
-                        if (nt == 1) core_update(P, G2p, A2p, ga, acc2[i][a][c]);
-                        else part[aa * NS + jc] = acc2[i][a][c];
+                    for (int a = ah; a < ah + 2; ++a)
+#pragma unroll
+                        for (int c = 0; c < 4; ++c) {
+                            const int aa = ag + A4 * a, jc = jg + JG * c, j2 = jc / R2S, cc = c0 + (jc - j2 * R2S);
+                            gidx[(a - ah) * 4 + c] = nt == 1 ? (aa * Q2 + j2) * R2 + cc : aa * NS + jc;
+                            gv[(a - ah) * 4 + c] = acc2[i][a][c];
+                        }
+                    if (nt == 1) {
+                        core_update_n<8>(P, G2p, A2p, gidx, gv);  // 8 loads in flight, then the stores
+                    } else {
+#pragma unroll
+                        for (int e = 0; e < 8; ++e) part[gidx[e]] = gv[e];
                     }
+                }
             }
         }
         if (nt == 1 && P.slice_stamp && P.opt != TT_OPT_GRAD && threadIdx.x == 0 && t == 0) P.slice_stamp[T.p1 + i2] = P.step + 1;
@@ -701,8 +723,9 @@ __device__ void tile_bwd_body(const Params& P, const TableDev& T, const Dm dm, u
     }
 }
 
+// Column-split kernels: three blocks per SM for the rank-16/32 classes (registers capped at 80), two otherwise.
 template <int DC, int SPLIT>
-__global__ void __launch_bounds__(kBwdThreads) k_tile_bwd(const __grid_constant__ Params P) {
+__global__ void __launch_bounds__(kBwdThreads, SPLIT == 2 ? ((DC == kQ444R32 || DC == kQ444R16) ? 3 : 2) : 1) k_tile_bwd(const __grid_constant__ Params P) {
     pdl_entry();
     if (*P.err) return;  // a device error was recorded: leave every core unchanged
     if ((int)(blockIdx.x / SPLIT) >= *P.ntiles) return;

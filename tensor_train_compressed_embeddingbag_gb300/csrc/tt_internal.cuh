@@ -166,6 +166,32 @@ __device__ __forceinline__ void core_update(const Params& P, float* G, float* au
     }
 }
 
+// core_update of n elements, every load issued before the first store (the
+// elements are distinct, so the order of the writes does not matter).
+template <int N>
+__device__ __forceinline__ void core_update_n(const Params& P, float* G, float* aux, const int* idx, const float* g) {
+    if (P.opt == TT_OPT_GRAD) {
+#pragma unroll
+        for (int i = 0; i < N; ++i) aux[idx[i]] = g[i];
+        return;
+    }
+    float w[N], st[N];
+#pragma unroll
+    for (int i = 0; i < N; ++i) w[i] = G[idx[i]];
+    if (P.opt == TT_OPT_ADAGRAD) {
+#pragma unroll
+        for (int i = 0; i < N; ++i) st[i] = fmaf(g[i], g[i], aux[idx[i]]);
+#pragma unroll
+        for (int i = 0; i < N; ++i) {
+            aux[idx[i]] = st[i];
+            G[idx[i]] = w[i] - P.lr * g[i] / (sqrtf(st[i]) + P.eps);
+        }
+    } else {
+#pragma unroll
+        for (int i = 0; i < N; ++i) G[idx[i]] = fmaf(-P.lr, g[i], w[i]);
+    }
+}
+
 __device__ __forceinline__ void pdl_entry() {
     asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
     asm volatile("griddepcontrol.wait;" ::: "memory");
