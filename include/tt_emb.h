@@ -171,6 +171,18 @@ tt_status tt_emb_backward(tt_emb* h, const float* grad_out_dev, float lr, tt_str
 tt_status tt_emb_set_optimizer(tt_emb* h, int32_t optim, float eps, float* const* aux);
 
 /*
+ * Expand rows [row0, row0 + nrows) of table `table` (0 for a single-table
+ * handle) to a dense float [nrows][D] block (FBTT README,
+ * "TableBatchedTTEmbeddingBag": expanding to full weight).  Row i of the table
+ * is G1[i1] G2[i2] G3[i3] with i = i1 p2 p3 + i2 p3 + i3, read from the cores
+ * as they are when the kernel runs.  out_dev is caller-owned, nrows * D
+ * floats.  Asynchronous on `stream`.  Returns TT_ERR_ARG (null handle, null
+ * out with nrows > 0, table out of range, rows outside [0, E)), TT_ERR_CUDA.
+ */
+tt_status tt_emb_full_weight(tt_emb* h, int32_t table, int64_t row0, int64_t nrows, float* out_dev,
+                             tt_stream stream);
+
+/*
  * Hot-row cache (FBTT README, "Software Cache"): decompress the n rows of
  * table 0 listed in rows_dev (int64, distinct, within [0, E)) into a
  * device-resident fp32 cache.  Later forward passes read a cached row instead

@@ -30,6 +30,8 @@ from ._nvcc_build import build
 __all__ = [
     "TTError",
     "build",
+    "suggested_tt_shapes",
+    "tt_init_cores",
     "load_library",
     "library_path",
     "tt_emb_create",
@@ -39,6 +41,7 @@ __all__ = [
     "tt_emb_forward",
     "tt_emb_backward",
     "tt_emb_set_optimizer",
+    "tt_emb_full_weight",
     "tt_emb_cache_populate",
     "tt_emb_cache_disable",
     "tt_emb_get_decoded",
@@ -65,6 +68,7 @@ EXPORTED_SYMBOLS = (
     "tt_emb_forward",
     "tt_emb_backward",
     "tt_emb_set_optimizer",
+    "tt_emb_full_weight",
     "tt_emb_cache_populate",
     "tt_emb_cache_disable",
     "tt_emb_get_decoded",
@@ -125,6 +129,7 @@ def load_library():
             "tt_emb_forward": (ctypes.c_int, [vp, vp, i64, vp, i64, vp, ctypes.c_int, vp, vp]),
             "tt_emb_backward": (ctypes.c_int, [vp, vp, f32, vp]),
             "tt_emb_set_optimizer": (ctypes.c_int, [vp, i32, f32, ctypes.POINTER(vp)]),
+            "tt_emb_full_weight": (ctypes.c_int, [vp, i32, i64, i64, vp, vp]),
             "tt_emb_cache_populate": (ctypes.c_int, [vp, vp, i64, vp]),
             "tt_emb_cache_disable": (ctypes.c_int, [vp]),
             "tt_emb_get_decoded": (ctypes.c_int, [vp, vp, vp, vp, vp, vp, vp]),
@@ -237,6 +242,15 @@ def tt_emb_set_optimizer(h, optim: int, eps: float = 0.0, aux: Optional[Sequence
     _check(load_library().tt_emb_set_optimizer(h, int(optim), float(eps), arr), "tt_emb_set_optimizer")
 
 
+def tt_emb_full_weight(h, table: int, row0: int, nrows: int, out: torch.Tensor, stream=None):
+    """Rows [row0, row0 + nrows) of `table` as dense float [nrows][D] into `out`."""
+    _cuda_f32(out, "out")
+    if out.numel() < nrows * (out.shape[-1] if out.dim() else 0):
+        raise TTError(TT_ERR_ARG, "out is too small")
+    _check(load_library().tt_emb_full_weight(h, int(table), int(row0), int(nrows), _ptr(out), _stream(stream)),
+           "tt_emb_full_weight")
+
+
 def tt_emb_cache_populate(h, rows: torch.Tensor, stream=None):
     _check(load_library().tt_emb_cache_populate(h, _ptr(rows), rows.numel(), _stream(stream)), "tt_emb_cache_populate")
 
@@ -292,6 +306,79 @@ def tt_emb_forward_noalloc(num_embeddings: int, p: Sequence[int], q: Sequence[in
 
 
 # ---------------------------------------------------------------- modules
+
+
+WEIGHT_DISTS = ("uniform", "naive-uniform", "approx-uniform", "normal", "approx-normal")
+
+
+def suggested_tt_shapes(num_embeddings: int, embedding_dim: int):
+    """Factor E and D when tt_p_shapes / tt_q_shapes are None (FBTT README, "Initialization").
+
+    The pages ask only that prod(p) >= E and prod(q) == D.  Read here as the
+    balanced choice: p1 = p2 = max(1, round(E^(1/3))), p3 = ceil(E / (p1 p2));
+    q = the three factors of D with product exactly D whose largest factor is
+    smallest (then whose smallest factor is largest), in ascending order
+    (64 -> [4, 4, 4], 128 -> [4, 4, 8]).
+    """
+    E, D = int(num_embeddings), int(embedding_dim)
+    if E < 1 or D < 1:
+        raise ValueError("num_embeddings and embedding_dim must be positive")
+    c = max(1, int(round(E ** (1.0 / 3.0))))
+    p = [c, c, -(-E // (c * c))]
+    best = None
+    for a in range(1, D + 1):
+        if D % a:
+            continue
+        for b in range(a, D // a + 1):
+            if (D // a) % b:
+                continue
+            cc = D // (a * b)
+            if cc < b:
+                continue
+            key = (cc, -a)
+            if best is None or key < best[0]:
+                best = (key, [a, b, cc])
+    return p, best[1]
+
+
+def tt_init_cores(p: Sequence[int], q: Sequence[int], ranks: Sequence[int], weight_dist: str = "normal",
+                  sigma: float = 1.0, generator: Optional[torch.Generator] = None, device=None) -> List[torch.Tensor]:
+    """Initial cores [p_k, r_{k-1}, q_k, r_k] (FBTT README, "Parameters": weight_dist).
+
+    sigma is the standard deviation of the target distribution X: N(0, sigma^2)
+    or U(-sqrt(3) sigma, sqrt(3) sigma).  Readings of the pages:
+      "normal", "uniform"   cores i.i.d. from X;
+      "approx-normal"       cores i.i.d. N(0, s^2), s^6 r1 r2 = sigma^2, so a full-table
+                            entry (a sum of r1 r2 products of three core entries) has X's
+                            mean and variance and is near-normal;
+      "approx-uniform"      cores i.i.d. U(-c, c), (c^2 / 3)^3 r1 r2 = sigma^2 (X's mean
+                            and variance for the full-table entries);
+      "naive-uniform"       cores i.i.d. U(-b, b), b^3 = sqrt(3) sigma: X's bound split
+                            evenly over the three cores, ignoring the r1 r2 summed terms.
+    """
+    dist = weight_dist.lower()
+    if dist not in WEIGHT_DISTS:
+        raise ValueError(f"weight_dist must be one of {WEIGHT_DISTS}")
+    r = [1, int(ranks[0]), int(ranks[1]), 1]
+    shapes = [(int(p[k]), r[k], int(q[k]), r[k + 1]) for k in range(3)]
+    terms = r[1] * r[2]
+    sigma = float(sigma)
+    out = []
+    for sh in shapes:
+        if dist == "normal":
+            t = torch.randn(sh, generator=generator) * sigma
+        elif dist == "approx-normal":
+            t = torch.randn(sh, generator=generator) * (sigma ** 2 / terms) ** (1.0 / 6.0)
+        else:
+            if dist == "uniform":
+                bound = 3.0 ** 0.5 * sigma
+            elif dist == "approx-uniform":
+                bound = 3.0 ** 0.5 * (sigma ** 2 / terms) ** (1.0 / 6.0)
+            else:
+                bound = (3.0 ** 0.5 * sigma) ** (1.0 / 3.0)
+            t = (torch.rand(sh, generator=generator) * 2.0 - 1.0) * bound
+        out.append(t.to(device=device, dtype=torch.float32).contiguous())
+    return out
 
 
 def _csr_offsets(offsets: torch.Tensor, nnz: int, include_last_offset: bool) -> torch.Tensor:
@@ -380,12 +467,17 @@ class TTEmbeddingBag(_TTBase):
     """
 
     def __init__(self, num_embeddings: int, embedding_dim: int, tt_ranks: Sequence[int],
-                 tt_p_shapes: Sequence[int], tt_q_shapes: Sequence[int], learning_rate: float = 0.1,
-                 cores: Optional[Sequence[torch.Tensor]] = None, sigma: float = 0.1, device=None,
-                 use_cache: bool = False, cache_rows: Optional[torch.Tensor] = None,
-                 sparse: bool = True, optimizer: str = "sgd", eps: float = 1.0e-10):
+                 tt_p_shapes: Optional[Sequence[int]] = None, tt_q_shapes: Optional[Sequence[int]] = None,
+                 learning_rate: float = 0.1, cores: Optional[Sequence[torch.Tensor]] = None, sigma: float = 0.1,
+                 device=None, use_cache: bool = False, cache_rows: Optional[torch.Tensor] = None,
+                 sparse: bool = True, optimizer: str = "sgd", eps: float = 1.0e-10, weight_dist: str = "normal",
+                 generator: Optional[torch.Generator] = None):
         super().__init__()
         device = torch.device(device or "cuda")
+        if tt_p_shapes is None or tt_q_shapes is None:
+            ps, qs = suggested_tt_shapes(num_embeddings, embedding_dim)
+            tt_p_shapes = ps if tt_p_shapes is None else tt_p_shapes
+            tt_q_shapes = qs if tt_q_shapes is None else tt_q_shapes
         q = list(tt_q_shapes)
         if q[0] * q[1] * q[2] != embedding_dim:
             raise ValueError("prod(tt_q_shapes) must equal embedding_dim")
@@ -395,7 +487,7 @@ class TTEmbeddingBag(_TTBase):
         r = [1, self.ranks[0], self.ranks[1], 1]
         shapes = [(self.p[k], r[k], q[k], r[k + 1]) for k in range(3)]
         if cores is None:
-            cores = [torch.randn(s, device=device) * sigma for s in shapes]
+            cores = tt_init_cores(self.p, q, self.ranks, weight_dist, sigma, generator, device)
         self.G1, self.G2, self.G3 = (
             torch.nn.Parameter(c.to(device=device, dtype=torch.float32).contiguous().clone()) for c in cores
         )
@@ -410,6 +502,13 @@ class TTEmbeddingBag(_TTBase):
     def _core_list(self):
         return [self.G1, self.G2, self.G3]
 
+    def full_weight(self, row0: int = 0, nrows: Optional[int] = None) -> torch.Tensor:
+        """Rows [row0, row0 + nrows) of the E x D table, expanded from the cores (default: all rows)."""
+        n = self.num_embeddings - row0 if nrows is None else int(nrows)
+        out = torch.empty((n, self.embedding_dim), dtype=torch.float32, device=self.G1.device)
+        tt_emb_full_weight(self._h, 0, row0, n, out)
+        return out
+
     def cache_populate(self, rows: torch.Tensor):
         """Fill the hot-row cache with these rows (FBTT README, "Software Cache")."""
         tt_emb_cache_populate(self._h, rows.to(torch.int64).contiguous())
@@ -421,23 +520,27 @@ class TTEmbeddingBag(_TTBase):
 class TableBatchedTTEmbeddingBag(_TTBase):
     """Several TT tables in one call (FBTT README, "TableBatchedTTEmbeddingBag").
 
-    tables: sequence of dicts with num_embeddings, p, q, ranks and optional cores.
+    tables: sequence of dicts with num_embeddings, ranks, optional p and q (None:
+    suggested_tt_shapes, which then needs embedding_dim) and optional cores.
     Bags are ordered table-major: offsets cover num_tables * B bags, bag
     t * B + b is sample b of table t; the output is [num_tables * B, D].
     """
 
     def __init__(self, tables, learning_rate: float = 0.1, sigma: float = 0.1, device=None,
-                 sparse: bool = True, optimizer: str = "sgd", eps: float = 1.0e-10):
+                 sparse: bool = True, optimizer: str = "sgd", eps: float = 1.0e-10, weight_dist: str = "normal",
+                 generator: Optional[torch.Generator] = None):
         super().__init__()
         device = torch.device(device or "cuda")
         self.learning_rate = float(learning_rate)
         self.specs = []
         params = []
         for i, t in enumerate(tables):
-            p, q, rk = list(t["p"]), list(t["q"]), list(t["ranks"])
-            r = [1, rk[0], rk[1], 1]
-            shapes = [(p[k], r[k], q[k], r[k + 1]) for k in range(3)]
-            cores = t.get("cores") or [torch.randn(s, device=device) * sigma for s in shapes]
+            p, q, rk = t.get("p"), t.get("q"), list(t["ranks"])
+            if p is None or q is None:
+                ps, qs = suggested_tt_shapes(t["num_embeddings"], t["embedding_dim"])
+                p, q = (ps if p is None else p), (qs if q is None else q)
+            p, q = list(p), list(q)
+            cores = t.get("cores") or tt_init_cores(p, q, rk, weight_dist, sigma, generator, device)
             cs = [torch.nn.Parameter(c.to(device=device, dtype=torch.float32).contiguous().clone()) for c in cores]
             for k in range(3):
                 self.register_parameter(f"t{i}_G{k + 1}", cs[k])
@@ -450,6 +553,14 @@ class TableBatchedTTEmbeddingBag(_TTBase):
 
     def _core_list(self):
         return [c for cs in self._cores for c in cs]
+
+    def full_weight(self, table: int, row0: int = 0, nrows: Optional[int] = None) -> torch.Tensor:
+        """Rows of table `table` expanded from its cores (default: all rows)."""
+        E = self.specs[table][0]
+        n = E - row0 if nrows is None else int(nrows)
+        out = torch.empty((n, self.embedding_dim), dtype=torch.float32, device=self._cores[table][0].device)
+        tt_emb_full_weight(self._h, table, row0, n, out)
+        return out
 
     def forward(self, input, offsets, per_sample_weights=None, mode: str = "sum", include_last_offset=True):
         return self._run(input, offsets, per_sample_weights, mode, include_last_offset)

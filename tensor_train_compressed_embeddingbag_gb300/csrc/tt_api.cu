@@ -557,8 +557,7 @@ tt_status tt_emb_set_optimizer(tt_emb* h, int32_t optim, float eps, float* const
     std::vector<TableDev> tabs = h->tabs;
     for (int t = 0; t < h->ntab; ++t)
         for (int k = 0; k < 3; ++k) tabs[t].aux[k] = optim == TT_OPT_SGD ? nullptr : aux[3 * t + k];
-    if (cudaSetDevice(h->device) != cudaSuccess ||
-        cudaMemcpy(h->d_tables, tabs.data(), sizeof(TableDev) * tabs.size(), cudaMemcpyHostToDevice) != cudaSuccess) {
+    if (cudaMemcpy(h->d_tables, tabs.data(), sizeof(TableDev) * tabs.size(), cudaMemcpyHostToDevice) != cudaSuccess) {
         cudaGetLastError();
         return TT_ERR_CUDA;
     }
@@ -566,6 +565,17 @@ tt_status tt_emb_set_optimizer(tt_emb* h, int32_t optim, float eps, float* const
     h->P.opt = optim;
     h->P.eps = eps;
     return TT_OK;
+}
+
+tt_status tt_emb_full_weight(tt_emb* h, int32_t table, int64_t row0, int64_t nrows, float* out_dev,
+                             tt_stream stream) {
+    if (!h || table < 0 || table >= h->ntab || row0 < 0 || nrows < 0 || (nrows > 0 && !out_dev)) return TT_ERR_ARG;
+    const TableDev& T = h->tabs[table];
+    if (row0 > T.E || nrows > T.E - row0) return TT_ERR_ARG;
+    if (nrows == 0) return TT_OK;
+    if (nrows > (int64_t)8 * 0x7fffffff) return TT_ERR_ARG;  // grid limit of the warp-per-row launch
+    const cudaError_t e = launch_full_weight(h->d_tables, table, row0, nrows, out_dev, reinterpret_cast<cudaStream_t>(stream));
+    return e == cudaSuccess ? TT_OK : TT_ERR_CUDA;
 }
 
 tt_status tt_emb_cache_populate(tt_emb* h, const int64_t* rows_dev, int64_t n, tt_stream stream) {

@@ -731,6 +731,40 @@ cudaError_t launch_pool(const Params& P, cudaStream_t s) {
     }
 }
 
+// Rows [row0, row0 + nrows) of one table as dense rows (warp per row, chain
+// product G1[i1] G2[i2] G3[i3], fp32); rows are independent.
+__global__ void k_full_weight(const TableDev* __restrict__ tables, int t, int64_t row0, int64_t nrows,
+                              float* __restrict__ out) {
+    const int lane = threadIdx.x & 31;
+    const int64_t k = (int64_t)blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5);
+    if (k >= nrows) return;
+    const TableDev& T = tables[t];
+    const int64_t row = row0 + k;
+    const int64_t p23 = (int64_t)T.p2 * T.p3;
+    const int i1 = (int)(row / p23), i2 = (int)((row / T.p3) % T.p2), i3 = (int)(row % T.p3);
+    const int q2 = T.q2, q3 = T.q3, r1 = T.r1, r2 = T.r2, D = T.D;
+    const float* g1 = T.G1 + (int64_t)i1 * T.q1 * r1;
+    const float* g2 = T.G2 + (int64_t)i2 * r1 * q2 * r2;
+    const float* g3 = T.G3 + (int64_t)i3 * r2 * q3;
+    for (int j = lane; j < D; j += 32) {
+        const int j3 = j % q3, j12 = j / q3, j2 = j12 % q2, j1 = j12 / q2;
+        float acc = 0.f;
+        for (int c = 0; c < r2; ++c) {
+            float tv = 0.f;
+            for (int a = 0; a < r1; ++a) tv = fmaf(g1[j1 * r1 + a], g2[(a * q2 + j2) * r2 + c], tv);
+            acc = fmaf(tv, g3[c * q3 + j3], acc);
+        }
+        out[k * D + j] = acc;
+    }
+}
+
+cudaError_t launch_full_weight(const TableDev* tables, int t, int64_t row0, int64_t nrows, float* out,
+                               cudaStream_t s) {
+    const int64_t blocks = (nrows + 7) / 8;
+    k_full_weight<<<dim3((unsigned)blocks), dim3(256), 0, s>>>(tables, t, row0, nrows, out);
+    return cudaGetLastError();
+}
+
 cudaError_t launch_cache_fill(const Params& P, cudaStream_t s) {
     const int64_t blocks = (P.cache_n + 7) / 8;
     cudaError_t le = launch_pdl(k_cache_fill, dim3((unsigned)blocks), dim3(256), 0, s, P);

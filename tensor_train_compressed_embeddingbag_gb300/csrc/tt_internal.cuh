@@ -474,6 +474,7 @@ cudaError_t launch_pool(const Params& P, cudaStream_t s);
 cudaError_t launch_tile_bwd(const Params& P, cudaStream_t s);
 cudaError_t launch_reduce13(const Params& P, cudaStream_t s);
 cudaError_t launch_cache_fill(const Params& P, cudaStream_t s);
+cudaError_t launch_full_weight(const TableDev* tables, int t, int64_t row0, int64_t nrows, float* out, cudaStream_t s);
 
 size_t tile_bwd_smem(const Params& P);
 cudaError_t set_sort_attributes(int max_smem);
