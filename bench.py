@@ -248,6 +248,13 @@ def run_gpu(args):
     D, nnz, B = spec.embedding_dim, wl.nnz, wl.num_bags
     cores = [torch.from_numpy(c).to(dev) for c in wl.cores[0]]
     h = tt.tt_emb_create(spec.num_embeddings, spec.p, spec.q, spec.ranks, cores)
+    aux = None
+    if args.optimizer == "adagrad":  # fused element-wise Adagrad, accumulators starting at 0
+        aux = [torch.zeros_like(c) for c in cores]
+        tt.tt_emb_set_optimizer(h, tt.TT_OPT_ADAGRAD, 1.0e-10, aux)
+    elif args.optimizer == "grad":  # sparse=False: the gradients are written out, the cores stay
+        aux = [torch.zeros_like(c) for c in cores]
+        tt.tt_emb_set_optimizer(h, tt.TT_OPT_GRAD, 0.0, aux)
     tt.tt_emb_reserve(h, nnz, B)
     idx = torch.from_numpy(wl.indices).to(dev)
     off = torch.from_numpy(wl.offsets).to(dev)
@@ -399,11 +406,14 @@ def run_gpu(args):
             "dtype": "f32",
             "data": "synthetic",
             "config": {
-                "workload": WORKLOAD,
+                "workload": WORKLOAD if args.optimizer == "sgd" else WORKLOAD.replace(
+                    "fused SGD", {"adagrad": "fused Adagrad", "grad": "sparse=False gradients"}[args.optimizer]),
                 "nnz": nnz,
                 "bags": B,
                 "p": spec.p, "q": spec.q, "ranks": spec.ranks,
                 "l2": f"flushed before every timed step ({L2_FLUSH_BYTES >> 20} MiB write, outside the events)",
+                "optimizer": {"sgd": "fused SGD", "adagrad": "fused element-wise Adagrad",
+                              "grad": "sparse=False (gradients written out)"}[args.optimizer],
                 "replicas": ws,
             },
             "timing": "CUDA graph of forward + backward replayed per step" if not args.eager else "eager launches",
@@ -439,6 +449,8 @@ def main():
     ap.add_argument("--impl", choices=["gb300", "reference"], default="gb300")
     ap.add_argument("--no-cpu-baseline", action="store_true", help="skip the oracle timing")
     ap.add_argument("--eager", action="store_true", help="time eager launches instead of a CUDA graph replay")
+    ap.add_argument("--optimizer", choices=["sgd", "adagrad", "grad"], default="sgd",
+                    help="what the backward does with the core gradients (default: fused SGD)")
     args = ap.parse_args()
     if args.impl == "reference":
         return run_reference(args)

@@ -198,6 +198,45 @@ tt_status tt_emb_cache_populate(tt_emb* h, const int64_t* rows_dev, int64_t n, t
 tt_status tt_emb_cache_disable(tt_emb* h);
 
 /*
+ * LFU cache policy (FBTT README, "Parameters": use_cache, cache_size,
+ * hashtbl_size; "Software Cache": access frequencies are counted in an
+ * open-addressing hash table during forward propagation, the cache is a
+ * 32-way set-associative least-frequently-used cache, and it changes only
+ * when it is populated, with values initialised from the TT cores).
+ * Single-table handles only (TT_ERR_STATE otherwise).
+ *
+ * tt_emb_lfu_enable: allocate a frequency table of hashtbl_size entries (a
+ *   power of two, 32 .. 2^30) and size the cache at cache_size rows rounded up
+ *   to a multiple of 32 (cache_size / 32 sets of 32 ways).  From then on every
+ *   forward pass counts each lookup's row: hash h = SplitMix64(row) (the first
+ *   output of a SplitMix64 generator seeded with row), entry h mod hashtbl_size,
+ *   linear probing over at most 64 entries; a row that finds no free or
+ *   matching entry there is not counted.  Counting uses integer atomics, so
+ *   the counts do not depend on the order of the lookups while the table has
+ *   room.  Replaces any previous frequency table (counts start at 0).
+ * tt_emb_lfu_populate: rebuild the cache from the counts: set k (k =
+ *   (h >> 32) mod sets) holds the 32 most frequently counted rows whose hash
+ *   maps to k (ties: the smaller row id); each cached value is computed from
+ *   the cores.  Cached rows are exact copies of TT rows: gradients go to the
+ *   cores and a row whose slices change is recomputed on its next hit, so
+ *   results equal the no-cache results (FBTT's trainable cache rows are not
+ *   built).  Synchronous.
+ * tt_emb_lfu_read: copy the counted (row, count) pairs, sorted by row, into
+ *   caller-owned host arrays of cap entries; *n_out = number of pairs.
+ * tt_emb_lfu_cached_rows: copy the cache's rows per slot (slot = set * 32 +
+ *   way, -1 = empty way; or the sorted rows of tt_emb_cache_populate) into a
+ *   host array of cap entries; *n_out = number of slots.  Synchronous.
+ * tt_emb_lfu_disable: stop counting and free the frequency table.
+ * Return TT_ERR_ARG (bad sizes, null pointers), TT_ERR_STATE (batched handle;
+ * populate or read before enable), TT_ERR_NOMEM, TT_ERR_CUDA.
+ */
+tt_status tt_emb_lfu_enable(tt_emb* h, int64_t cache_size, int64_t hashtbl_size);
+tt_status tt_emb_lfu_populate(tt_emb* h, tt_stream stream);
+tt_status tt_emb_lfu_read(tt_emb* h, int64_t* rows_host, uint32_t* counts_host, int64_t cap, int64_t* n_out);
+tt_status tt_emb_lfu_cached_rows(tt_emb* h, int64_t* rows_host, int64_t cap, int64_t* n_out);
+tt_status tt_emb_lfu_disable(tt_emb* h);
+
+/*
  * Copy the decode of the most recent forward pass: for every lookup its
  * table, its slice indices (i1, i2, i3) and its bag.  Each *_dev is a
  * caller-owned int32 [nnz] device buffer; any may be NULL.  For checks.

@@ -243,3 +243,43 @@ def workload_sgd_slices(w, table, core, slices=None, cores=None):
     """``sgd_slices`` on a ``tt_inputs.Workload`` with its learning rate."""
     return sgd_slices(w.tables, cores or w.cores, w.indices, w.offsets, w.grad_out, w.lr, table, core,
                       w.weights, w.mode, w.batch, slices)
+
+
+# ---------------------------------------------------------------- LFU cache policy
+# FBTT README, "Software Cache": access frequencies are counted in a hash table
+# during the forward passes; cache_populate() fills a 32-way set-associative
+# least-frequently-used cache from them.  Written from those statements and the
+# published SplitMix64 definition (the row hash), independently of the library.
+
+_M64 = (1 << 64) - 1
+LFU_WAYS = 32
+
+
+def splitmix64(x: int) -> int:
+    """First output of a SplitMix64 generator seeded with x (Steele, Lea and Flood, OOPSLA 2014)."""
+    z = (int(x) + 0x9E3779B97F4A7C15) & _M64
+    z = ((z ^ (z >> 30)) * 0xBF58476D1CE4E5B9) & _M64
+    z = ((z ^ (z >> 27)) * 0x94D049BB133111EB) & _M64
+    return z ^ (z >> 31)
+
+
+def lfu_counts(*index_arrays):
+    """Access count of every row over the given lookups (all forward passes since counting began)."""
+    rows, counts = np.unique(np.concatenate([np.asarray(a, dtype=np.int64) for a in index_arrays]),
+                             return_counts=True)
+    return rows, counts
+
+
+def lfu_select(rows, counts, cache_size):
+    """Cache content per slot (set * 32 + way, -1 = empty): set k holds the 32 most
+    frequent rows r with (splitmix64(r) >> 32) mod sets == k, ties to the smaller row."""
+    sets = -(-int(cache_size) // LFU_WAYS)
+    members = [[] for _ in range(sets)]
+    for r, c in zip(np.asarray(rows).tolist(), np.asarray(counts).tolist()):
+        members[(splitmix64(r) >> 32) % sets].append((-int(c), int(r)))
+    out = np.full(sets * LFU_WAYS, -1, dtype=np.int64)
+    for k, m in enumerate(members):
+        m.sort()
+        for w, (_, r) in enumerate(m[:LFU_WAYS]):
+            out[k * LFU_WAYS + w] = r
+    return out

@@ -42,6 +42,11 @@ __all__ = [
     "tt_emb_backward",
     "tt_emb_set_optimizer",
     "tt_emb_full_weight",
+    "tt_emb_lfu_enable",
+    "tt_emb_lfu_populate",
+    "tt_emb_lfu_read",
+    "tt_emb_lfu_cached_rows",
+    "tt_emb_lfu_disable",
     "tt_emb_cache_populate",
     "tt_emb_cache_disable",
     "tt_emb_get_decoded",
@@ -69,6 +74,11 @@ EXPORTED_SYMBOLS = (
     "tt_emb_backward",
     "tt_emb_set_optimizer",
     "tt_emb_full_weight",
+    "tt_emb_lfu_enable",
+    "tt_emb_lfu_populate",
+    "tt_emb_lfu_read",
+    "tt_emb_lfu_cached_rows",
+    "tt_emb_lfu_disable",
     "tt_emb_cache_populate",
     "tt_emb_cache_disable",
     "tt_emb_get_decoded",
@@ -130,6 +140,11 @@ def load_library():
             "tt_emb_backward": (ctypes.c_int, [vp, vp, f32, vp]),
             "tt_emb_set_optimizer": (ctypes.c_int, [vp, i32, f32, ctypes.POINTER(vp)]),
             "tt_emb_full_weight": (ctypes.c_int, [vp, i32, i64, i64, vp, vp]),
+            "tt_emb_lfu_enable": (ctypes.c_int, [vp, i64, i64]),
+            "tt_emb_lfu_populate": (ctypes.c_int, [vp, vp]),
+            "tt_emb_lfu_read": (ctypes.c_int, [vp, vp, vp, i64, ctypes.POINTER(i64)]),
+            "tt_emb_lfu_cached_rows": (ctypes.c_int, [vp, vp, i64, ctypes.POINTER(i64)]),
+            "tt_emb_lfu_disable": (ctypes.c_int, [vp]),
             "tt_emb_cache_populate": (ctypes.c_int, [vp, vp, i64, vp]),
             "tt_emb_cache_disable": (ctypes.c_int, [vp]),
             "tt_emb_get_decoded": (ctypes.c_int, [vp, vp, vp, vp, vp, vp, vp]),
@@ -249,6 +264,43 @@ def tt_emb_full_weight(h, table: int, row0: int, nrows: int, out: torch.Tensor, 
         raise TTError(TT_ERR_ARG, "out is too small")
     _check(load_library().tt_emb_full_weight(h, int(table), int(row0), int(nrows), _ptr(out), _stream(stream)),
            "tt_emb_full_weight")
+
+
+def tt_emb_lfu_enable(h, cache_size: int, hashtbl_size: int):
+    """Count row accesses in every forward pass and size a 32-way set-associative LFU cache."""
+    _check(load_library().tt_emb_lfu_enable(h, int(cache_size), int(hashtbl_size)), "tt_emb_lfu_enable")
+
+
+def tt_emb_lfu_populate(h, stream=None):
+    """Rebuild the cache from the access counts (per set: the 32 most frequent rows)."""
+    _check(load_library().tt_emb_lfu_populate(h, _stream(stream)), "tt_emb_lfu_populate")
+
+
+def tt_emb_lfu_read(h):
+    """(rows, counts) of the frequency table, sorted by row (numpy int64 / uint32)."""
+    import numpy as np
+    lib = load_library()
+    n = ctypes.c_int64()
+    _check(lib.tt_emb_lfu_read(h, None, None, 0, ctypes.byref(n)), "tt_emb_lfu_read")
+    rows = np.empty(n.value, dtype=np.int64)
+    counts = np.empty(n.value, dtype=np.uint32)
+    _check(lib.tt_emb_lfu_read(h, rows.ctypes.data, counts.ctypes.data, n.value, ctypes.byref(n)), "tt_emb_lfu_read")
+    return rows, counts
+
+
+def tt_emb_lfu_cached_rows(h):
+    """The cache's row per slot (set * 32 + way; -1 = empty), numpy int64."""
+    import numpy as np
+    lib = load_library()
+    n = ctypes.c_int64()
+    _check(lib.tt_emb_lfu_cached_rows(h, None, 0, ctypes.byref(n)), "tt_emb_lfu_cached_rows")
+    rows = np.empty(n.value, dtype=np.int64)
+    _check(lib.tt_emb_lfu_cached_rows(h, rows.ctypes.data, n.value, ctypes.byref(n)), "tt_emb_lfu_cached_rows")
+    return rows
+
+
+def tt_emb_lfu_disable(h):
+    _check(load_library().tt_emb_lfu_disable(h), "tt_emb_lfu_disable")
 
 
 def tt_emb_cache_populate(h, rows: torch.Tensor, stream=None):
@@ -471,7 +523,7 @@ class TTEmbeddingBag(_TTBase):
                  learning_rate: float = 0.1, cores: Optional[Sequence[torch.Tensor]] = None, sigma: float = 0.1,
                  device=None, use_cache: bool = False, cache_rows: Optional[torch.Tensor] = None,
                  sparse: bool = True, optimizer: str = "sgd", eps: float = 1.0e-10, weight_dist: str = "normal",
-                 generator: Optional[torch.Generator] = None):
+                 generator: Optional[torch.Generator] = None, cache_size: int = 0, hashtbl_size: int = 0):
         super().__init__()
         device = torch.device(device or "cuda")
         if tt_p_shapes is None or tt_q_shapes is None:
@@ -498,6 +550,11 @@ class TTEmbeddingBag(_TTBase):
         self._set_optimizer(sparse, optimizer, eps)
         if use_cache and cache_rows is not None:
             self.cache_populate(cache_rows)
+        elif use_cache and cache_size > 0:
+            # FBTT README, "Software Cache": count accesses, cache the most frequent rows on populate
+            hsize = hashtbl_size if hashtbl_size > 0 else max(32, 4 * cache_size)
+            hsize = 1 << max(5, (int(hsize) - 1).bit_length())
+            tt_emb_lfu_enable(self._h, cache_size, hsize)
 
     def _core_list(self):
         return [self.G1, self.G2, self.G3]
@@ -509,9 +566,13 @@ class TTEmbeddingBag(_TTBase):
         tt_emb_full_weight(self._h, 0, row0, n, out)
         return out
 
-    def cache_populate(self, rows: torch.Tensor):
-        """Fill the hot-row cache with these rows (FBTT README, "Software Cache")."""
-        tt_emb_cache_populate(self._h, rows.to(torch.int64).contiguous())
+    def cache_populate(self, rows: Optional[torch.Tensor] = None):
+        """Fill the hot-row cache (FBTT README, "Software Cache"): with `rows`, exactly those
+        rows; without, by the LFU policy from the access counts of the forward passes so far."""
+        if rows is None:
+            tt_emb_lfu_populate(self._h)
+        else:
+            tt_emb_cache_populate(self._h, rows.to(torch.int64).contiguous())
 
     def forward(self, input, offsets, per_sample_weights=None, mode: str = "sum", include_last_offset=False):
         return self._run(input, offsets, per_sample_weights, mode, include_last_offset)

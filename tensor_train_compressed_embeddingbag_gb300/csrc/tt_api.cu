@@ -70,6 +70,11 @@ struct tt_emb {
     float* d_cache_vals = nullptr;
     int* d_cache_stamp = nullptr;
     int* d_slice_stamp = nullptr;
+    // LFU policy (tt_emb_lfu_enable)
+    unsigned long long* d_freq_keys = nullptr;
+    unsigned* d_freq_counts = nullptr;
+    int64_t freq_size = 0;
+    int64_t lfu_slots = 0;  // cache rows (a multiple of kLfuWays)
     int64_t cache_n = 0;
     int step = 0;
 };
@@ -333,6 +338,8 @@ void free_handle(tt_emb* h) {
     cudaFree(h->d_cache_vals);
     cudaFree(h->d_cache_stamp);
     cudaFree(h->d_slice_stamp);
+    cudaFree(h->d_freq_keys);
+    cudaFree(h->d_freq_counts);
     for (int w = 0; w < 2; ++w)
         for (int i = 0; i <= kMaxStages; ++i)
             if (h->ev[w][i]) cudaEventDestroy(h->ev[w][i]);
@@ -578,6 +585,137 @@ tt_status tt_emb_full_weight(tt_emb* h, int32_t table, int64_t row0, int64_t nro
     return e == cudaSuccess ? TT_OK : TT_ERR_CUDA;
 }
 
+// Allocate the cache arrays for n slots of table 0 and fill them from host row ids
+// (-1 = empty slot); `sets` > 0 selects the set-associative layout.
+static tt_status cache_install(tt_emb* h, const std::vector<int64_t>& rows, int sets, cudaStream_t s) {
+    const int64_t n = (int64_t)rows.size();
+    const TableDev& T = h->tabs[0];
+    const int nslice = T.p1 + T.p2 + T.p3;
+    if (cudaMalloc(&h->d_cache_rows, sizeof(int64_t) * n) != cudaSuccess ||
+        cudaMalloc(&h->d_cache_vals, sizeof(float) * (size_t)n * T.D) != cudaSuccess ||
+        cudaMalloc(&h->d_cache_stamp, sizeof(int) * n) != cudaSuccess ||
+        cudaMalloc(&h->d_slice_stamp, sizeof(int) * nslice) != cudaSuccess) {
+        cudaGetLastError();
+        tt_emb_cache_disable(h);
+        return TT_ERR_NOMEM;
+    }
+    if (cudaMemcpyAsync(h->d_cache_rows, rows.data(), sizeof(int64_t) * n, cudaMemcpyHostToDevice, s) != cudaSuccess ||
+        cudaMemsetAsync(h->d_slice_stamp, 0, sizeof(int) * nslice, s) != cudaSuccess)
+        return TT_ERR_CUDA;
+    h->cache_n = n;
+    h->P.cache_sets = sets;
+    Params P = h->P;
+    P.cache_rows = h->d_cache_rows;
+    P.cache_n = n;
+    P.cache_vals = h->d_cache_vals;
+    P.cache_stamp = h->d_cache_stamp;
+    P.step = h->step;
+    if (launch_cache_fill(P, s) != cudaSuccess) return TT_ERR_CUDA;
+    // the host vector must outlive the copy
+    if (cudaStreamSynchronize(s) != cudaSuccess) return TT_ERR_CUDA;
+    return TT_OK;
+}
+
+tt_status tt_emb_lfu_enable(tt_emb* h, int64_t cache_size, int64_t hashtbl_size) {
+    if (!h || cache_size < 1 || hashtbl_size < 32 || (hashtbl_size & (hashtbl_size - 1)) != 0 ||
+        hashtbl_size > ((int64_t)1 << 30) || cache_size > ((int64_t)1 << 30))
+        return TT_ERR_ARG;
+    if (h->ntab != 1) return TT_ERR_STATE;
+    tt_emb_lfu_disable(h);
+    if (cudaMalloc(&h->d_freq_keys, sizeof(unsigned long long) * hashtbl_size) != cudaSuccess ||
+        cudaMalloc(&h->d_freq_counts, sizeof(unsigned) * hashtbl_size) != cudaSuccess) {
+        cudaGetLastError();
+        tt_emb_lfu_disable(h);
+        return TT_ERR_NOMEM;
+    }
+    if (cudaMemset(h->d_freq_keys, 0xFF, sizeof(unsigned long long) * hashtbl_size) != cudaSuccess ||
+        cudaMemset(h->d_freq_counts, 0, sizeof(unsigned) * hashtbl_size) != cudaSuccess)
+        return TT_ERR_CUDA;
+    h->freq_size = hashtbl_size;
+    h->lfu_slots = (cache_size + kLfuWays - 1) / kLfuWays * kLfuWays;
+    h->P.freq_keys = h->d_freq_keys;
+    h->P.freq_counts = h->d_freq_counts;
+    h->P.freq_mask = (int)(hashtbl_size - 1);
+    return TT_OK;
+}
+
+tt_status tt_emb_lfu_disable(tt_emb* h) {
+    if (!h) return TT_ERR_ARG;
+    if (h->d_freq_keys) cudaDeviceSynchronize();
+    cudaFree(h->d_freq_keys);
+    cudaFree(h->d_freq_counts);
+    h->d_freq_keys = nullptr;
+    h->d_freq_counts = nullptr;
+    h->freq_size = 0;
+    h->lfu_slots = 0;
+    h->P.freq_keys = nullptr;
+    h->P.freq_counts = nullptr;
+    h->P.freq_mask = 0;
+    return TT_OK;
+}
+
+// The frequency table's (row, count) entries, sorted by row.
+static tt_status lfu_entries(tt_emb* h, std::vector<std::pair<int64_t, unsigned>>& out) {
+    std::vector<unsigned long long> keys(h->freq_size);
+    std::vector<unsigned> counts(h->freq_size);
+    if (cudaDeviceSynchronize() != cudaSuccess ||
+        cudaMemcpy(keys.data(), h->d_freq_keys, sizeof(unsigned long long) * h->freq_size, cudaMemcpyDeviceToHost) != cudaSuccess ||
+        cudaMemcpy(counts.data(), h->d_freq_counts, sizeof(unsigned) * h->freq_size, cudaMemcpyDeviceToHost) != cudaSuccess)
+        return TT_ERR_CUDA;
+    out.clear();
+    for (int64_t i = 0; i < h->freq_size; ++i)
+        if (keys[i] != ~0ull) out.emplace_back((int64_t)keys[i], counts[i]);
+    std::sort(out.begin(), out.end());
+    return TT_OK;
+}
+
+tt_status tt_emb_lfu_read(tt_emb* h, int64_t* rows_host, uint32_t* counts_host, int64_t cap, int64_t* n_out) {
+    if (!h || !n_out || cap < 0 || (cap > 0 && (!rows_host || !counts_host))) return TT_ERR_ARG;
+    if (!h->d_freq_keys) return TT_ERR_STATE;
+    std::vector<std::pair<int64_t, unsigned>> e;
+    tt_status st = lfu_entries(h, e);
+    if (st != TT_OK) return st;
+    *n_out = (int64_t)e.size();
+    for (int64_t i = 0; i < (int64_t)e.size() && i < cap; ++i) {
+        rows_host[i] = e[i].first;
+        counts_host[i] = e[i].second;
+    }
+    return TT_OK;
+}
+
+tt_status tt_emb_lfu_populate(tt_emb* h, tt_stream stream) {
+    if (!h) return TT_ERR_ARG;
+    if (!h->d_freq_keys) return TT_ERR_STATE;
+    cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+    std::vector<std::pair<int64_t, unsigned>> e;
+    tt_status st = lfu_entries(h, e);
+    if (st != TT_OK) return st;
+    tt_emb_cache_disable(h);
+    const int sets = (int)(h->lfu_slots / kLfuWays);
+    // per set: the kLfuWays most frequent counted rows (ties: the smaller row id)
+    std::vector<std::vector<std::pair<int64_t, int64_t>>> by_set(sets);  // (-count, row)
+    for (const auto& x : e) by_set[lfu_set_of(x.first, sets)].emplace_back(-(int64_t)x.second, x.first);
+    std::vector<int64_t> rows((size_t)sets * kLfuWays, -1);
+    for (int k = 0; k < sets; ++k) {
+        auto& v = by_set[k];
+        const size_t take = std::min(v.size(), (size_t)kLfuWays);
+        std::partial_sort(v.begin(), v.begin() + take, v.end());
+        for (size_t w = 0; w < take; ++w) rows[(size_t)k * kLfuWays + w] = v[w].second;
+    }
+    return cache_install(h, rows, sets, s);
+}
+
+tt_status tt_emb_lfu_cached_rows(tt_emb* h, int64_t* rows_host, int64_t cap, int64_t* n_out) {
+    if (!h || !n_out || cap < 0 || (cap > 0 && !rows_host)) return TT_ERR_ARG;
+    *n_out = h->cache_n;
+    if (h->cache_n == 0) return TT_OK;
+    if (cudaDeviceSynchronize() != cudaSuccess ||
+        cudaMemcpy(rows_host, h->d_cache_rows, sizeof(int64_t) * (size_t)std::min(cap, h->cache_n),
+                   cudaMemcpyDeviceToHost) != cudaSuccess)
+        return TT_ERR_CUDA;
+    return TT_OK;
+}
+
 tt_status tt_emb_cache_populate(tt_emb* h, const int64_t* rows_dev, int64_t n, tt_stream stream) {
     if (!h || n < 0 || (n > 0 && !rows_dev)) return TT_ERR_ARG;
     if (h->ntab != 1) return TT_ERR_STATE;
@@ -593,29 +731,7 @@ tt_status tt_emb_cache_populate(tt_emb* h, const int64_t* rows_dev, int64_t n, t
     const TableDev& T = h->tabs[0];
     for (int64_t i = 0; i < n; ++i)
         if (rows[i] < 0 || rows[i] >= T.E || (i > 0 && rows[i] == rows[i - 1])) return TT_ERR_ARG;
-    const int nslice = T.p1 + T.p2 + T.p3;
-    if (cudaMalloc(&h->d_cache_rows, sizeof(int64_t) * n) != cudaSuccess ||
-        cudaMalloc(&h->d_cache_vals, sizeof(float) * (size_t)n * T.D) != cudaSuccess ||
-        cudaMalloc(&h->d_cache_stamp, sizeof(int) * n) != cudaSuccess ||
-        cudaMalloc(&h->d_slice_stamp, sizeof(int) * nslice) != cudaSuccess) {
-        cudaGetLastError();
-        tt_emb_cache_disable(h);
-        return TT_ERR_NOMEM;
-    }
-    if (cudaMemcpyAsync(h->d_cache_rows, rows.data(), sizeof(int64_t) * n, cudaMemcpyHostToDevice, s) != cudaSuccess ||
-        cudaMemsetAsync(h->d_slice_stamp, 0, sizeof(int) * nslice, s) != cudaSuccess)
-        return TT_ERR_CUDA;
-    h->cache_n = n;
-    Params P = h->P;
-    P.cache_rows = h->d_cache_rows;
-    P.cache_n = n;
-    P.cache_vals = h->d_cache_vals;
-    P.cache_stamp = h->d_cache_stamp;
-    P.step = h->step;
-    if (launch_cache_fill(P, s) != cudaSuccess) return TT_ERR_CUDA;
-    // the host vector must outlive the copy
-    if (cudaStreamSynchronize(s) != cudaSuccess) return TT_ERR_CUDA;
-    return TT_OK;
+    return cache_install(h, rows, 0, s);
 }
 
 tt_status tt_emb_cache_disable(tt_emb* h) {
@@ -631,6 +747,7 @@ tt_status tt_emb_cache_disable(tt_emb* h) {
     h->d_slice_stamp = nullptr;
     h->cache_n = 0;
     h->P.cache_n = 0;
+    h->P.cache_sets = 0;
     h->P.slice_stamp = nullptr;
     return TT_OK;
 }

@@ -417,6 +417,12 @@ __device__ __forceinline__ const float* t_of_pair(const Params& P, const TableDe
 
 // Cache slot of `row` (table 0) or -1.
 __device__ __forceinline__ int64_t cache_find(const Params& P, int64_t row) {
+    if (P.cache_sets > 0) {  // set-associative: the kLfuWays ways of the row's set
+        const int64_t base = lfu_set_of(row, P.cache_sets) * kLfuWays;
+        for (int w = 0; w < kLfuWays; ++w)
+            if (P.cache_rows[base + w] == row) return base + w;
+        return -1;
+    }
     int64_t a = 0, b = P.cache_n;
     while (a < b) {
         const int64_t m = (a + b) >> 1;
@@ -670,6 +676,7 @@ __global__ void k_cache_fill(const __grid_constant__ Params P) {
     if (slot >= P.cache_n) return;
     const TableDev& T = P.tables[0];
     const int64_t row = P.cache_rows[slot];
+    if (row < 0) return;  // empty way of a set-associative cache
     const int64_t p23 = (int64_t)T.p2 * T.p3;
     const int i1 = (int)(row / p23), i2 = (int)((row / T.p3) % T.p2), i3 = (int)(row % T.p3);
     const int q2 = T.q2, q3 = T.q3, r1 = T.r1, r2 = T.r2, D = T.D;

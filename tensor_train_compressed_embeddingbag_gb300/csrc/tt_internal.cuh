@@ -139,6 +139,13 @@ struct Params {
     int* cache_stamp;               // [cache_n] step at which the row was computed
     int* slice_stamp;               // [p1 + p2 + p3] step at which each slice last changed
     int step;
+    // FBTT README, "Software Cache": access-frequency table (open addressing, linear
+    // probing) updated by every forward pass, and the set-associative layout of the
+    // cache (cache_sets > 0: slot = set * kLfuWays + way; 0: cache_rows sorted)
+    unsigned long long* freq_keys;  // [freq_mask + 1], ~0 = empty
+    unsigned* freq_counts;          // [freq_mask + 1]
+    int freq_mask;
+    int cache_sets;
 };
 
 // ---------------------------------------------------------------- helpers
@@ -306,6 +313,38 @@ __device__ __forceinline__ int64_t bag_of(const Params& P, int64_t n) {
 }
 
 // Decode lookup n of bag `bag`: slice indices, pooling scale, touched-pair flag.
+// SplitMix64 output function (Steele, Lea and Flood, "Fast splittable pseudorandom
+// number generators", OOPSLA 2014): the first output of a generator seeded with x.
+// Hashes row ids for the frequency table (low bits) and the cache sets (high bits).
+__host__ __device__ __forceinline__ uint64_t mix64(uint64_t x) {
+    uint64_t z = x + 0x9E3779B97F4A7C15ull;
+    z = (z ^ (z >> 30)) * 0xBF58476D1CE4E5B9ull;
+    z = (z ^ (z >> 27)) * 0x94D049BB133111EBull;
+    return z ^ (z >> 31);
+}
+
+constexpr int kLfuWays = 32;      // cache associativity
+constexpr int kLfuMaxProbe = 64;  // frequency-table probes before a lookup goes uncounted
+
+__host__ __device__ __forceinline__ int64_t lfu_set_of(int64_t row, int sets) {
+    return (int64_t)((mix64((uint64_t)row) >> 32) % (uint64_t)sets);
+}
+
+// Count one access of `row` in the frequency table (integer atomics: the final
+// counts do not depend on the order of the lookups while the table has room).
+__device__ __forceinline__ void lfu_count(const Params& P, int64_t row) {
+    unsigned slot = (unsigned)mix64((uint64_t)row) & (unsigned)P.freq_mask;
+    for (int probe = 0; probe < kLfuMaxProbe; ++probe) {
+        unsigned long long k = P.freq_keys[slot];
+        if (k == ~0ull) k = atomicCAS(P.freq_keys + slot, ~0ull, (unsigned long long)row);
+        if (k == ~0ull || k == (unsigned long long)row) {
+            atomicAdd(P.freq_counts + slot, 1u);
+            return;
+        }
+        slot = (slot + 1) & (unsigned)P.freq_mask;
+    }
+}
+
 __device__ __forceinline__ void decode_lookup(const Params& P, int64_t n, int bag, int& t, int& i1, int& i2,
                                               int& i3, int epoch) {
     t = table_of_bag(P, bag);
@@ -316,6 +355,8 @@ __device__ __forceinline__ void decode_lookup(const Params& P, int64_t n, int ba
         atomicOr(P.err, kErrIndex);
         row = 0;
         s = 0.0f;
+    } else if (P.freq_keys) {  // FBTT README, "Software Cache": every forward counts its rows
+        lfu_count(P, row);
     }
     if (P.mean) {
         const int64_t L = P.off[bag + 1] - P.off[bag];

@@ -87,6 +87,10 @@ def test_null_arguments_rejected(lib):
     assert lib.tt_emb_forward(None, None, 0, None, 0, None, 0, None, None) == tt.TT_ERR_ARG
     assert lib.tt_emb_backward(None, None, ctypes.c_float(0.1), None) == tt.TT_ERR_ARG
     assert lib.tt_emb_set_optimizer(None, tt.TT_OPT_SGD, ctypes.c_float(0.0), None) == tt.TT_ERR_ARG
+    assert lib.tt_emb_full_weight(None, 0, 0, 1, None, None) == tt.TT_ERR_ARG
+    assert lib.tt_emb_lfu_enable(None, 64, 64) == tt.TT_ERR_ARG
+    assert lib.tt_emb_lfu_populate(None, None) == tt.TT_ERR_ARG
+    assert lib.tt_emb_lfu_disable(None) == tt.TT_ERR_ARG
     assert lib.tt_emb_reserve(None, 1, 1) == tt.TT_ERR_ARG
     assert lib.tt_emb_get_last_error(None) == tt.TT_ERR_ARG
     assert lib.tt_emb_last_launch_count(None, 0) == -1

@@ -320,3 +320,30 @@ def test_adagrad_matches_torch_optim(init):
         for k in range(3):
             np.testing.assert_allclose(cur[k], params[k].detach().numpy(), rtol=1e-12, atol=1e-14)
             np.testing.assert_allclose(state[k], opt.state[params[k]]["sum"].numpy(), rtol=1e-12, atol=1e-14)
+
+
+def test_splitmix64_published_outputs():
+    """The row hash of the LFU policy: SplitMix64's published outputs (seed 0; seed 1234567, three steps)."""
+    assert oracle.splitmix64(0) == 0xE220A8397B1DCDAF
+    golden = 0x9E3779B97F4A7C15
+    s, out = 1234567, []
+    for _ in range(3):
+        out.append(oracle.splitmix64(s))
+        s = (s + golden) & ((1 << 64) - 1)
+    assert out == [6457827717110365317, 3203168211198807973, 9817491932198370423]
+
+
+def test_lfu_select_brute_force():
+    """Per set, the selection equals a brute-force ranking of that set's rows."""
+    rng = np.random.default_rng(9)
+    rows = rng.choice(100000, 3000, replace=False)
+    counts = rng.integers(1, 6, size=rows.shape[0])  # many ties
+    sel = oracle.lfu_select(rows, counts, 40 * 32)
+    sets = 40
+    for k in range(sets):
+        mine = [(-int(c), int(r)) for r, c in zip(rows, counts) if (oracle.splitmix64(int(r)) >> 32) % sets == k]
+        want = [r for _, r in sorted(mine)[:32]]
+        got = [r for r in sel[k * 32:(k + 1) * 32] if r >= 0]
+        assert got == want
+    r2, c2 = oracle.lfu_counts([5, 3, 5, 9], np.array([5]))
+    assert r2.tolist() == [3, 5, 9] and c2.tolist() == [1, 3, 1]
