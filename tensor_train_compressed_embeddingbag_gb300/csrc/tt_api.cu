@@ -126,6 +126,10 @@ size_t carve(tt_emb* h, void* base, int64_t nnz, bool assign) {
     int* pi1 = A.take<int>(N);
     int* pi3 = A.take<int>(N);
     int* pi21 = A.take<int>(N);
+    int* g_i1 = A.take<int>(N);
+    int* g_i3 = A.take<int>(N);
+    int* g_bag = A.take<int>(N);
+    float* g_s = A.take<float>(N);
     int* sigma = A.take<int>(N);
     int4* tiles = A.take<int4>(max_tiles);
     int* grp_first = A.take<int>(P.n2);
@@ -140,6 +144,7 @@ size_t carve(tt_emb* h, void* base, int64_t nnz, bool assign) {
         P.lr1 = lr1; P.lr2 = lr2; P.lr3 = lr3;
         P.H1 = H1; P.H3 = H3; P.H2 = H2;
         P.pi1 = pi1; P.pi3 = pi3; P.pi21 = pi21; P.sigma = sigma;
+        P.g_i1 = g_i1; P.g_i3 = g_i3; P.g_bag = g_bag; P.g_s = g_s;
         P.tiles = tiles; P.grp_first = grp_first; P.grp_ntiles = grp_ntiles;
         P.rep_pair = rep_pair; P.rep_row = rep_row;
         P.Qbuf = Qbuf; P.Pbuf = Pbuf; P.dG2part = dG2part;

@@ -40,7 +40,7 @@ __host__ __device__ inline int bwd_pairs_per_batch(int q1, int Ns, int r1) {
 }
 
 struct BwdLayout {
-    size_t keys, sn, si1, si3, sbag, ss, tbag, ts, rowid, pairid, rowbeg, pairbeg, sh, gs, g2t, g1s, dts, total;
+    size_t keys, sn, si1, si3, sbag, ss, rowid, pairid, rowbeg, pairbeg, sh, gs, g2t, g1s, dts, total;
 };
 
 __host__ __device__ inline BwdLayout bwd_layout(int cap, int D, int g2f, int g1f, int dtf) {
@@ -52,8 +52,6 @@ __host__ __device__ inline BwdLayout bwd_layout(int cap, int D, int g2f, int g1f
     L.si3 = o;     o = al16(o + sizeof(int) * cap);
     L.sbag = o;    o = al16(o + sizeof(int) * cap);
     L.ss = o;      o = al16(o + sizeof(float) * cap);
-    L.tbag = o;    o = al16(o + sizeof(int) * cap);
-    L.ts = o;      o = al16(o + sizeof(float) * cap);
     L.rowid = o;   o = al16(o + sizeof(int) * cap);
     L.pairid = o;  o = al16(o + sizeof(int) * cap);
     L.rowbeg = o;  o = al16(o + sizeof(int) * (cap + 1));
@@ -69,33 +67,35 @@ __host__ __device__ inline BwdLayout bwd_layout(int cap, int D, int g2f, int g1f
 
 // The tile's lookups come grouped by (table, i2) (ordered by (i1, pos) on the
 // multi-CTA path, by pos on the small path); sort them by (i1, i3, position) in
-// shared memory.  Bag and scale of each lookup are loaded in the same pass and
-// follow the sort.
+// shared memory.  Bag and scale of each lookup are read in the same pass (from
+// the grouped-order copies the scatter wrote) and follow the sort.
 __device__ void load_and_sort_tile(const Params& P, int start, int len, unsigned long long* keys, int* sn,
-                                   int* si1, int* si3, int* sbag, float* ss, int* tbag, float* ts) {
-    int npow = 1;
-    while (npow < len) npow <<= 1;
-    for (int k = threadIdx.x; k < npow; k += blockDim.x) {
-        unsigned long long key = ~0ull;
-        if (k < len) {
-            const int n = P.pi21[start + k];
-            key = ((unsigned long long)P.lk_i1[n] << (2 * kFieldBits)) |
-                  ((unsigned long long)P.lk_i3[n] << kFieldBits) | (unsigned long long)k;
-            tbag[k] = P.lk_bag[n];
-            ts[k] = P.lk_s[n];
-        }
+                                   int* si1, int* si3, int* sbag, float* ss) {
+    // len <= blockDim: thread k holds lookup k of the tile.  The keys (i1, i3, k) are
+    // distinct, so a key's rank is the number of smaller keys: every thread counts its
+    // own with broadcast shared-memory reads and writes its lookup at that rank.
+    const int k = threadIdx.x;
+    unsigned long long key = ~0ull;
+    int n = 0, i1 = 0, i3 = 0, bag = 0;
+    float sc = 0.f;
+    if (k < len) {  // grouped-order copies: one coalesced pass, no dependent loads
+        n = P.pi21[start + k];
+        i1 = P.g_i1[start + k];
+        i3 = P.g_i3[start + k];
+        bag = P.g_bag[start + k];
+        sc = P.g_s[start + k];
+        key = ((unsigned long long)i1 << (2 * kFieldBits)) | ((unsigned long long)i3 << kFieldBits) | (unsigned long long)k;
         keys[k] = key;
     }
-    block_bitonic_sort(keys, npow);
-    const unsigned long long fmask = (1ull << kFieldBits) - 1;
-    for (int k = threadIdx.x; k < len; k += blockDim.x) {
-        const unsigned long long key = keys[k];
-        const int k0 = (int)(key & fmask);
-        sn[k] = P.pi21[start + k0];
-        si1[k] = (int)(key >> (2 * kFieldBits));
-        si3[k] = (int)((key >> kFieldBits) & fmask);
-        sbag[k] = tbag[k0];
-        ss[k] = ts[k0];
+    __syncthreads();
+    if (k < len) {
+        int r = 0;
+        for (int j = 0; j < len; ++j) r += keys[j] < key ? 1 : 0;
+        sn[r] = n;
+        si1[r] = i1;
+        si3[r] = i3;
+        sbag[r] = bag;
+        ss[r] = sc;
     }
     __syncthreads();
 }
@@ -225,8 +225,6 @@ __device__ void tile_bwd_body(const Params& P, const TableDev& T, const Dm dm, u
     int* si3 = (int*)(smraw + L.si3);
     int* sbag = (int*)(smraw + L.sbag);
     float* ss = (float*)(smraw + L.ss);
-    int* tbag = (int*)(smraw + L.tbag);
-    float* ts = (float*)(smraw + L.ts);
     int* rowid = (int*)(smraw + L.rowid);
     int* pairid = (int*)(smraw + L.pairid);
     int* rowbeg = (int*)(smraw + L.rowbeg);
@@ -247,7 +245,7 @@ __device__ void tile_bwd_body(const Params& P, const TableDev& T, const Dm dm, u
     const int t = P.bin2_tab[g];
 
     // ---- lookups of the tile, sorted by (i1, i3, position)
-    load_and_sort_tile(P, start, len, keys, sn, si1, si3, sbag, ss, tbag, ts);
+    load_and_sort_tile(P, start, len, keys, sn, si1, si3, sbag, ss);
     const int k = threadIdx.x;  // tile_cap <= blockDim
     int fr = 0, fp = 0;
     if (k < len) {

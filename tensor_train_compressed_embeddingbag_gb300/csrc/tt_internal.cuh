@@ -115,6 +115,12 @@ struct Params {
     int* pi1;
     int* pi3;
     int* pi21;
+    // the lookups' (i1, i3, bag, scale) in the (table, i2)-grouped order of pi21,
+    // written by the grouping scatter so that k_tile_bwd reads a tile in one pass
+    int* g_i1;
+    int* g_i3;
+    int* g_bag;
+    float* g_s;
     int* sigma;
     int4* tiles;                    // {start, len, group bin, tile index in group}
     int* tflag;                     // dense touched-pair flags, == *epoch when touched by this call
@@ -237,26 +243,6 @@ __device__ __forceinline__ int block_scan_excl(int x, int* sh, int* total) {
     *total = sh[32];
     __syncthreads();
     return res;
-}
-
-// Ascending bitonic sort of n (power of two) keys in shared memory.
-__device__ __forceinline__ void block_bitonic_sort(unsigned long long* keys, int n) {
-    for (int size = 2; size <= n; size <<= 1) {
-        for (int stride = size >> 1; stride > 0; stride >>= 1) {
-            __syncthreads();
-            for (int i = threadIdx.x; i < (n >> 1); i += blockDim.x) {
-                int lo = 2 * i - (i & (stride - 1));
-                int hi = lo + stride;
-                bool asc = (lo & size) == 0;
-                unsigned long long a = keys[lo], b = keys[hi];
-                if ((a > b) == asc) {
-                    keys[lo] = b;
-                    keys[hi] = a;
-                }
-            }
-        }
-    }
-    __syncthreads();
 }
 
 // Block-wide copy of n floats from global to shared memory with U loads in
@@ -389,7 +375,12 @@ __device__ __forceinline__ void scatter_chunk(const Params& P, int c) {
         const TableDev& T = P.tables[table_of_bag(P, P.lk_bag[n])];
         const int d1 = T.base1 + P.lk_i1[n], d2 = T.base2 + P.lk_i2[n], d3 = T.base3 + P.lk_i3[n];
         P.pi1[P.H1[(int64_t)d1 * P.nch + c] + P.lr1[n]] = (int)n;
-        P.pi21[P.H2[(int64_t)d2 * P.nch + c] + P.lr2[n]] = (int)n;
+        const int pos = P.H2[(int64_t)d2 * P.nch + c] + P.lr2[n];
+        P.pi21[pos] = (int)n;
+        P.g_i1[pos] = P.lk_i1[n];
+        P.g_i3[pos] = P.lk_i3[n];
+        P.g_bag[pos] = P.lk_bag[n];
+        P.g_s[pos] = P.lk_s[n];
         P.pi3[P.H3[(int64_t)d3 * P.nch + c] + P.lr3[n]] = (int)n;
     }
 }

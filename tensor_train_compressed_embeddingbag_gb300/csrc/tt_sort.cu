@@ -188,7 +188,14 @@ __global__ void __launch_bounds__(kSortThreads) k_scatter2(const __grid_constant
             const int n = P.pi1[k];
             return P.tables[table_of_bag(P, P.lk_bag[n])].base2 + P.lk_i2[n];
         },
-        [&](int64_t k, int d, int rank) { P.pi21[P.H2[(int64_t)d * P.nch + c] + rank] = P.pi1[k]; });
+        [&](int64_t k, int d, int rank) {
+            const int n = P.pi1[k], pos = P.H2[(int64_t)d * P.nch + c] + rank;
+            P.pi21[pos] = n;
+            P.g_i1[pos] = P.lk_i1[n];
+            P.g_i3[pos] = P.lk_i3[n];
+            P.g_bag[pos] = P.lk_bag[n];
+            P.g_s[pos] = P.lk_s[n];
+        });
 }
 
 // ------------------------------------------------------------------ small path
