@@ -134,8 +134,11 @@ size_t carve(tt_emb* h, void* base, int64_t nnz, bool assign) {
     int4* tiles = A.take<int4>(max_tiles);
     int* grp_first = A.take<int>(P.n2);
     int* grp_ntiles = A.take<int>(P.n2);
-    int* rep_pair = A.take<int>(N);
-    int* rep_row = A.take<int>(N);
+    int* rep1 = A.take<int>(N);
+    int* rep3 = A.take<int>(N);
+    int* g_p1 = A.take<int>(N);
+    int* g_p3 = A.take<int>(N);
+    int* inv3 = A.take<int>(N);
     float* Qbuf = A.take<float>(qslots * P.qs_max);
     float* Pbuf = A.take<float>((size_t)N * P.ps_max);
     float* dG2part = A.take<float>(part_floats);
@@ -146,7 +149,7 @@ size_t carve(tt_emb* h, void* base, int64_t nnz, bool assign) {
         P.pi1 = pi1; P.pi3 = pi3; P.pi21 = pi21; P.sigma = sigma;
         P.g_i1 = g_i1; P.g_i3 = g_i3; P.g_bag = g_bag; P.g_s = g_s;
         P.tiles = tiles; P.grp_first = grp_first; P.grp_ntiles = grp_ntiles;
-        P.rep_pair = rep_pair; P.rep_row = rep_row;
+        P.rep1 = rep1; P.rep3 = rep3; P.g_p1 = g_p1; P.g_p3 = g_p3; P.inv3 = inv3;
         P.Qbuf = Qbuf; P.Pbuf = Pbuf; P.dG2part = dG2part;
     }
     return A.used + 256;

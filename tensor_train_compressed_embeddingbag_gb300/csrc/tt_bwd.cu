@@ -40,14 +40,15 @@ __host__ __device__ inline int bwd_pairs_per_batch(int q1, int Ns, int r1) {
 }
 
 struct BwdLayout {
-    size_t keys, sn, si1, si3, sbag, ss, rowid, pairid, rowbeg, pairbeg, sh, gs, g2t, g1s, dts, total;
+    size_t keys, sp1, sp3, si1, si3, sbag, ss, rowid, pairid, rowbeg, pairbeg, sh, gs, g2t, g1s, dts, total;
 };
 
 __host__ __device__ inline BwdLayout bwd_layout(int cap, int D, int g2f, int g1f, int dtf) {
     BwdLayout L;
     size_t o = 0;
     L.keys = o;    o = al16(o + sizeof(unsigned long long) * cap);
-    L.sn = o;      o = al16(o + sizeof(int) * cap);
+    L.sp1 = o;     o = al16(o + sizeof(int) * cap);
+    L.sp3 = o;     o = al16(o + sizeof(int) * cap);
     L.si1 = o;     o = al16(o + sizeof(int) * cap);
     L.si3 = o;     o = al16(o + sizeof(int) * cap);
     L.sbag = o;    o = al16(o + sizeof(int) * cap);
@@ -69,17 +70,18 @@ __host__ __device__ inline BwdLayout bwd_layout(int cap, int D, int g2f, int g1f
 // multi-CTA path, by pos on the small path); sort them by (i1, i3, position) in
 // shared memory.  Bag and scale of each lookup are read in the same pass (from
 // the grouped-order copies the scatter wrote) and follow the sort.
-__device__ void load_and_sort_tile(const Params& P, int start, int len, unsigned long long* keys, int* sn,
-                                   int* si1, int* si3, int* sbag, float* ss) {
+__device__ void load_and_sort_tile(const Params& P, int start, int len, unsigned long long* keys, int* sp1,
+                                   int* sp3, int* si1, int* si3, int* sbag, float* ss) {
     // len <= blockDim: thread k holds lookup k of the tile.  The keys (i1, i3, k) are
     // distinct, so a key's rank is the number of smaller keys: every thread counts its
     // own with broadcast shared-memory reads and writes its lookup at that rank.
     const int k = threadIdx.x;
     unsigned long long key = ~0ull;
-    int n = 0, i1 = 0, i3 = 0, bag = 0;
+    int p1 = 0, p3 = 0, i1 = 0, i3 = 0, bag = 0;
     float sc = 0.f;
     if (k < len) {  // grouped-order copies: one coalesced pass, no dependent loads
-        n = P.pi21[start + k];
+        p1 = P.g_p1[start + k];
+        p3 = P.g_p3[start + k];
         i1 = P.g_i1[start + k];
         i3 = P.g_i3[start + k];
         bag = P.g_bag[start + k];
@@ -91,7 +93,8 @@ __device__ void load_and_sort_tile(const Params& P, int start, int len, unsigned
     if (k < len) {
         int r = 0;
         for (int j = 0; j < len; ++j) r += keys[j] < key ? 1 : 0;
-        sn[r] = n;
+        sp1[r] = p1;
+        sp3[r] = p3;
         si1[r] = i1;
         si3[r] = i3;
         sbag[r] = bag;
@@ -106,15 +109,14 @@ __device__ void load_and_sort_tile(const Params& P, int start, int len, unsigned
 // (lane group r, element e) loads slots j = r, r + R, ... kReducePer at a time
 // and sums them in order, then the R partial sums are added in r order.
 constexpr int kReduceSlots = 1024;   // slots gathered per round
-constexpr int kReducePer = 16;       // loads in flight per thread
+constexpr int kReducePer = 32;       // loads in flight per thread
 
 __device__ void reduce_slice(const Params& P, int bglob, int* slots, int* sh, float* sacc) {
     const bool first_core = bglob < P.n1;
     const int b = first_core ? bglob : bglob - P.n1;
     const int nb = first_core ? P.n1 : P.n3;
     const int* H = first_core ? P.H1 : P.H3;
-    const int* pi = first_core ? P.pi1 : P.pi3;
-    const int* rep = first_core ? P.rep_pair : P.rep_row;
+    const int* rep = first_core ? P.rep1 : P.rep3;  // indexed by position in the i1 / i3 order
     const int start = H[(int64_t)b * P.nch];
     const int end = (b + 1 < nb) ? H[(int64_t)(b + 1) * P.nch] : (int)P.nnz;
     const int t = first_core ? P.bin1_tab[b] : P.bin3_tab[b];
@@ -137,7 +139,7 @@ __device__ void reduce_slice(const Params& P, int bglob, int* slots, int* sh, fl
         int nslot = 0;
         while (base < end && nslot + (int)blockDim.x * nsub <= kReduceSlots) {
             const int kk = base + threadIdx.x;
-            const int rv = kk < end ? rep[pi[kk]] : -1;
+            const int rv = kk < end ? rep[kk] : -1;
             int tot;
             const int ex = block_scan_excl(rv >= 0 ? 1 : 0, sh, &tot);
             if (rv >= 0)
@@ -220,7 +222,8 @@ template <class Dm, int SPLIT>
 __device__ void tile_bwd_body(const Params& P, const TableDev& T, const Dm dm, unsigned char* smraw) {
     const BwdLayout L = bwd_layout(P.tile_cap, P.D, P.g2s_floats, P.g1s_floats, P.dts_floats);
     unsigned long long* keys = (unsigned long long*)(smraw + L.keys);
-    int* sn = (int*)(smraw + L.sn);
+    int* sp1 = (int*)(smraw + L.sp1);
+    int* sp3 = (int*)(smraw + L.sp3);
     int* si1 = (int*)(smraw + L.si1);
     int* si3 = (int*)(smraw + L.si3);
     int* sbag = (int*)(smraw + L.sbag);
@@ -245,7 +248,7 @@ __device__ void tile_bwd_body(const Params& P, const TableDev& T, const Dm dm, u
     const int t = P.bin2_tab[g];
 
     // ---- lookups of the tile, sorted by (i1, i3, position)
-    load_and_sort_tile(P, start, len, keys, sn, si1, si3, sbag, ss);
+    load_and_sort_tile(P, start, len, keys, sp1, sp3, si1, si3, sbag, ss);
     const int k = threadIdx.x;  // tile_cap <= blockDim
     int fr = 0, fp = 0;
     if (k < len) {
@@ -269,9 +272,8 @@ __device__ void tile_bwd_body(const Params& P, const TableDev& T, const Dm dm, u
     // partial slots are numbered by the position of the run's first lookup in the
     // grouped order, so every run of every tile owns one slot, with no atomics
     if (sp == 0 && k < len) {
-        const int n = sn[k];
-        P.rep_row[n] = fr ? start + k : -1;
-        P.rep_pair[n] = fp ? start + k : -1;
+        P.rep3[sp3[k]] = fr ? start + k : -1;
+        P.rep1[sp1[k]] = fp ? start + k : -1;
     }
 
     // ---- G2 columns of this split, transposed: g2t[jc'][a], jc' = j2 r2s + c' (8 loads in flight)

@@ -16,6 +16,8 @@ constexpr int kFwdThreads = 256;
 constexpr int kListCap = 1024;      // touched i1 handled per round
 constexpr int kPoolWarps = 4;       // warps per bag
 constexpr int kMaxDPerLane = 8;     // generic pool path: D <= 256
+constexpr int kScatterParts = kSmallChunk / (kPoolWarps * 32);  // grouping-scatter blocks per chunk
+static_assert(kScatterParts * kPoolWarps * 32 == kSmallChunk, "scatter parts cover a chunk");
 
 // ------------------------------------------------------------------ T per pair
 
@@ -649,8 +651,9 @@ __global__ void __launch_bounds__(kPoolWarps * 32) k_pool(const __grid_constant_
     pdl_entry();
     __shared__ float red[kPoolWarps * kMaxD];
     const int64_t bag = blockIdx.x;
-    if (bag >= P.nbags) {  // small path: extra blocks scatter the lookups of one chunk
-        scatter_chunk(P, (int)(bag - P.nbags));
+    if (bag >= P.nbags) {  // small path: extra blocks scatter the lookups of part of a chunk
+        const int e = (int)(bag - P.nbags);
+        scatter_chunk(P, e / kScatterParts, e % kScatterParts);
         return;
     }
     if (bag == 0 && threadIdx.x == 0) atomicAdd(P.epoch, 1);  // k_fwd_T has finished reading it
@@ -722,7 +725,8 @@ cudaError_t launch_fwd_T(const Params& P, cudaStream_t s) {
 
 template <int DC>
 static cudaError_t launch_pool_dc(const Params& P, cudaStream_t s) {
-    cudaError_t le = launch_pdl(k_pool<DC>, dim3((unsigned)(P.nbags + (P.small ? P.nch : 0))), dim3(kPoolWarps * 32), 0, s, P);
+    cudaError_t le = launch_pdl(k_pool<DC>, dim3((unsigned)(P.nbags + (P.small ? (int64_t)P.nch * kScatterParts : 0))),
+                                dim3(kPoolWarps * 32), 0, s, P);
     if (le != cudaSuccess) return le;
     return cudaGetLastError();
 }

@@ -121,6 +121,9 @@ struct Params {
     int* g_i3;
     int* g_bag;
     float* g_s;
+    int* g_p1;                      // grouped order: the lookup's position in pi1
+    int* g_p3;                      // grouped order: the lookup's position in pi3
+    int* inv3;                      // [nnz] position of lookup n in pi3 (multi-CTA grouping)
     int* sigma;
     int4* tiles;                    // {start, len, group bin, tile index in group}
     int* tflag;                     // dense touched-pair flags, == *epoch when touched by this call
@@ -130,8 +133,8 @@ struct Params {
     int* grp_ntiles;                // [n2]
     int* grp_done;                  // [n2], zero between calls
     float* Tbuf;
-    int* rep_pair;                  // [nnz] partial slot of the tile-pair starting at this lookup, or -1
-    int* rep_row;                   // [nnz] partial slot of the tile-row starting at this lookup, or -1
+    int* rep1;                      // [nnz] by position in pi1: partial slot of the tile-pair starting at that lookup, or -1
+    int* rep3;                      // [nnz] by position in pi3: partial slot of the tile-row starting at that lookup, or -1
                                     // (slot = position of that lookup in pi21)
     float* Qbuf;                    // [nnz][qs_max]
     float* Pbuf;                    // [nnz][ps_max]
@@ -367,21 +370,27 @@ __device__ __forceinline__ void decode_lookup(const Params& P, int64_t n, int ba
     P.tflag[T.fbase + (int64_t)i2 * T.p1 + i1] = epoch;
 }
 
-// Small path, chunk c: position = scanned base of (digit, chunk) + rank in chunk.
-__device__ __forceinline__ void scatter_chunk(const Params& P, int c) {
-    const int64_t lo = (int64_t)c * kSmallChunk;
-    const int64_t hi = (lo + kSmallChunk < P.nnz) ? lo + kSmallChunk : P.nnz;
-    for (int64_t n = lo + threadIdx.x; n < hi; n += blockDim.x) {
+// Small path, part `part` (of kSmallChunk / blockDim) of chunk c: position =
+// scanned base of (digit, chunk) + rank in chunk; a thread per lookup.
+__device__ __forceinline__ void scatter_chunk(const Params& P, int c, int part) {
+    const int64_t lo = (int64_t)c * kSmallChunk + (int64_t)part * blockDim.x;
+    const int64_t cend = (int64_t)(c + 1) * kSmallChunk;
+    const int64_t hi = (cend < P.nnz) ? cend : P.nnz;
+    for (int64_t n = lo + threadIdx.x; n < hi && n < lo + blockDim.x; n += blockDim.x) {
         const TableDev& T = P.tables[table_of_bag(P, P.lk_bag[n])];
         const int d1 = T.base1 + P.lk_i1[n], d2 = T.base2 + P.lk_i2[n], d3 = T.base3 + P.lk_i3[n];
-        P.pi1[P.H1[(int64_t)d1 * P.nch + c] + P.lr1[n]] = (int)n;
+        const int p1 = P.H1[(int64_t)d1 * P.nch + c] + P.lr1[n];
+        const int p3 = P.H3[(int64_t)d3 * P.nch + c] + P.lr3[n];
         const int pos = P.H2[(int64_t)d2 * P.nch + c] + P.lr2[n];
+        P.pi1[p1] = (int)n;
+        P.pi3[p3] = (int)n;
         P.pi21[pos] = (int)n;
         P.g_i1[pos] = P.lk_i1[n];
         P.g_i3[pos] = P.lk_i3[n];
         P.g_bag[pos] = P.lk_bag[n];
         P.g_s[pos] = P.lk_s[n];
-        P.pi3[P.H3[(int64_t)d3 * P.nch + c] + P.lr3[n]] = (int)n;
+        P.g_p1[pos] = p1;
+        P.g_p3[pos] = p3;
     }
 }
 

@@ -175,7 +175,11 @@ __global__ void __launch_bounds__(kSortThreads) k_scatter13(const __grid_constan
     chunk_stable_ranks(
         c, P.nnz, P.n3, cnt,
         [&](int64_t n) { return P.tables[table_of_bag(P, P.lk_bag[n])].base3 + P.lk_i3[n]; },
-        [&](int64_t n, int d, int rank) { P.pi3[P.H3[(int64_t)d * P.nch + c] + rank] = (int)n; });
+        [&](int64_t n, int d, int rank) {
+            const int pos = P.H3[(int64_t)d * P.nch + c] + rank;
+            P.pi3[pos] = (int)n;
+            P.inv3[n] = pos;
+        });
 }
 
 __global__ void __launch_bounds__(kSortThreads) k_scatter2(const __grid_constant__ Params P) {
@@ -195,6 +199,8 @@ __global__ void __launch_bounds__(kSortThreads) k_scatter2(const __grid_constant
             P.g_i3[pos] = P.lk_i3[n];
             P.g_bag[pos] = P.lk_bag[n];
             P.g_s[pos] = P.lk_s[n];
+            P.g_p1[pos] = (int)k;
+            P.g_p3[pos] = P.inv3[n];
         });
 }
 
