@@ -247,6 +247,22 @@ __device__ void tile_bwd_body(const Params& P, const TableDev& T, const Dm dm, u
     const int r2s = r2 / SPLIT, c0 = sp * r2s, Ns = q2 * r2s;
     const int t = P.bin2_tab[g];
 
+    // ---- the first 8 G2 values of this thread (the G2 slice depends only on i2): their
+    // loads are in flight while the tile's lookups are read and sorted
+    const float* g2src = T.G2 + (int64_t)i2 * r1 * q2 * r2;
+    const int g2n = r1 * Ns;
+    float g2v[8];
+#pragma unroll
+    for (int q = 0; q < 8; ++q) {
+        const int e = q * kBwdThreads + threadIdx.x;
+        g2v[q] = 0.f;
+        if (e < g2n) {
+            const int a = e / Ns, jc = e - a * Ns;
+            const int j2 = jc / r2s, c = jc - j2 * r2s;
+            g2v[q] = __ldg(g2src + (a * q2 + j2) * r2 + c0 + c);
+        }
+    }
+
     // ---- lookups of the tile, sorted by (i1, i3, position)
     load_and_sort_tile(P, start, len, keys, sp1, sp3, si1, si3, sbag, ss);
     const int k = threadIdx.x;  // tile_cap <= blockDim
@@ -276,10 +292,11 @@ __device__ void tile_bwd_body(const Params& P, const TableDev& T, const Dm dm, u
         P.rep1[sp1[k]] = fp ? start + k : -1;
     }
 
-    // ---- G2 columns of this split, transposed: g2t[jc'][a], jc' = j2 r2s + c' (8 loads in flight)
+    // ---- G2 columns of this split, transposed: g2t[jc'][a], jc' = j2 r2s + c' (8 loads in flight;
+    // the first round was loaded before the sort)
     {
-        const float* src = T.G2 + (int64_t)i2 * r1 * q2 * r2;
-        const int n = r1 * Ns;
+        const float* src = g2src;
+        const int n = g2n;
         int gstride = r1 + 4;
         if constexpr (Dm::kStatic) gstride = BwdTiling<Dm, SPLIT>::GS;
         for (int base = 0; base < n; base += 8 * kBwdThreads) {
@@ -288,7 +305,9 @@ __device__ void tile_bwd_body(const Params& P, const TableDev& T, const Dm dm, u
             for (int q = 0; q < 8; ++q) {
                 const int e = base + q * kBwdThreads + threadIdx.x;
                 v[q] = 0.f;
-                if (e < n) {
+                if (base == 0) {
+                    v[q] = g2v[q];
+                } else if (e < n) {
                     const int a = e / Ns, jc = e - a * Ns;
                     const int j2 = jc / r2s, c = jc - j2 * r2s;
                     v[q] = __ldg(src + (a * q2 + j2) * r2 + c0 + c);
