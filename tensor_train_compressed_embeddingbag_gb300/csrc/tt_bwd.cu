@@ -109,7 +109,8 @@ __device__ void load_and_sort_tile(const Params& P, int start, int len, unsigned
 // (lane group r, element e) loads slots j = r, r + R, ... kReducePer at a time
 // and sums them in order, then the R partial sums are added in r order.
 constexpr int kReduceSlots = 1024;   // slots gathered per round
-constexpr int kReducePer = 32;       // loads in flight per thread
+constexpr int kReducePer = 32;       // loads in flight per thread (scalar columns)
+constexpr int kReducePer4 = 16;      // float4 loads in flight per thread
 
 __device__ void reduce_slice(const Params& P, int bglob, int* slots, int* sh, float* sacc) {
     const bool first_core = bglob < P.n1;
@@ -129,10 +130,15 @@ __device__ void reduce_slice(const Params& P, int bglob, int* slots, int* sh, fl
     float* G = (first_core ? T.G1 : T.G3) + (int64_t)slice * S;
     float* A = (first_core ? T.aux[0] : T.aux[2]);
     if (A) A += (int64_t)slice * S;
-    const int W = S >= kBwdThreads ? kBwdThreads : S;  // threads per lane group
-    const int R = S >= kBwdThreads ? 1 : kBwdThreads / S;
+    // Lanes: groups of W threads; thread (r, e) sums element column e (float4 when S % 4 == 0:
+    // four elements per thread, every slot row read in 16-byte words) over the slots
+    // j = r, r + R, ..., kReducePer loads in flight; the R group sums are added in group order.
+    const bool v4 = (S & 3) == 0;  // slot strides are whole 16-byte words (rounded on the host)
+    const int SE = v4 ? S >> 2 : S;  // element columns (float4 or float)
+    const int W = SE >= kBwdThreads ? kBwdThreads : SE;
+    const int R = kBwdThreads / W;
     const int r = threadIdx.x / W;
-    const int nacc = ((S + kBwdThreads - 1) / kBwdThreads) * kBwdThreads;
+    const int nacc = R * S > S ? R * S : S;  // group sums, or S when one group walks every column
     for (int e = threadIdx.x; e < nacc; e += blockDim.x) sacc[e] = 0.f;
     __syncthreads();
     for (int base = start; base < end;) {
@@ -151,9 +157,26 @@ __device__ void reduce_slice(const Params& P, int bglob, int* slots, int* sh, fl
         if (r < R) {
             const int e0 = threadIdx.x - r * W;
 #pragma unroll 1
-            for (int m = 0; m * kBwdThreads < S; ++m) {
-                const int e = e0 + m * kBwdThreads;
-                if (e < S) {
+            for (int e = e0; e < SE; e += W) {
+                if (v4) {
+                    float4 a = make_float4(0.f, 0.f, 0.f, 0.f);
+#pragma unroll 1
+                    for (int j0 = r; j0 < nslot; j0 += R * kReducePer4) {
+                        float4 v[kReducePer4];
+#pragma unroll
+                        for (int u = 0; u < kReducePer4; ++u) {
+                            const int j = j0 + u * R;
+                            v[u] = j < nslot ? __ldg(reinterpret_cast<const float4*>(buf + (int64_t)slots[j] * stride) + e)
+                                             : make_float4(0.f, 0.f, 0.f, 0.f);
+                        }
+#pragma unroll
+                        for (int u = 0; u < kReducePer4; ++u) {
+                            a.x += v[u].x; a.y += v[u].y; a.z += v[u].z; a.w += v[u].w;
+                        }
+                    }
+                    float* dst = sacc + (R > 1 ? r * S : 0) + 4 * e;
+                    dst[0] += a.x; dst[1] += a.y; dst[2] += a.z; dst[3] += a.w;
+                } else {
                     float a = 0.f;
 #pragma unroll 1
                     for (int j0 = r; j0 < nslot; j0 += R * kReducePer) {
@@ -166,18 +189,16 @@ __device__ void reduce_slice(const Params& P, int bglob, int* slots, int* sh, fl
 #pragma unroll
                         for (int u = 0; u < kReducePer; ++u) a += v[u];
                     }
-                    sacc[m * kBwdThreads + threadIdx.x] += a;
+                    sacc[(R > 1 ? r * S : 0) + e] += a;
                 }
             }
         }
         __syncthreads();
     }
-    if (R == 1) {
-        for (int e = threadIdx.x; e < S; e += blockDim.x) core_update(P, G, A, e, sacc[e]);
-    } else if (threadIdx.x < S) {
+    for (int e = threadIdx.x; e < S; e += blockDim.x) {
         float sum = 0.f;  // the R lane groups' sums in group order
-        for (int rr = 0; rr < R; ++rr) sum += sacc[rr * S + threadIdx.x];
-        core_update(P, G, A, threadIdx.x, sum);
+        for (int rr = 0; rr < R; ++rr) sum += sacc[(R > 1 ? rr * S : 0) + e];
+        core_update(P, G, A, e, sum);
     }
     if (P.slice_stamp && P.opt != TT_OPT_GRAD && threadIdx.x == 0 && t == 0)
         P.slice_stamp[first_core ? slice : T.p1 + T.p2 + slice] = P.step + 1;
@@ -760,7 +781,9 @@ __global__ void __launch_bounds__(kBwdThreads, SPLIT == 2 ? ((DC == kQ444R32 || 
     }
 }
 
-__global__ void __launch_bounds__(kBwdThreads) k_reduce13(const __grid_constant__ Params P) {
+// Three blocks per SM (the slice count of the workloads fits one wave); without a minimum
+// the register target is so low that the partial loads of a thread no longer overlap.
+__global__ void __launch_bounds__(kBwdThreads, 3) k_reduce13(const __grid_constant__ Params P) {
     pdl_entry();
     if (*P.err) return;  // a device error was recorded: leave every core unchanged
     __shared__ int slots[kReduceSlots];
@@ -822,8 +845,8 @@ static cudaError_t set_tile_attrs(int max_smem) {
 }
 
 cudaError_t launch_reduce13(const Params& P, cudaStream_t s) {
-    const size_t smem = sizeof(float) * (size_t)kBwdThreads *
-                        (size_t)((std::max(P.qs_max, P.ps_max) + kBwdThreads - 1) / kBwdThreads);
+    // per-group sums: R S <= 4 kBwdThreads floats while one group's columns fit the block, else S
+    const size_t smem = sizeof(float) * std::max<size_t>(4 * kBwdThreads, (size_t)std::max(P.qs_max, P.ps_max));
     cudaError_t le = launch_pdl(k_reduce13, dim3(P.n1 + P.n3), dim3(kBwdThreads), smem, s, P);
     if (le != cudaSuccess) return le;
     return cudaGetLastError();
