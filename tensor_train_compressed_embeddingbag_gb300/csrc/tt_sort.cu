@@ -19,7 +19,7 @@ namespace ttemb {
 
 // ------------------------------------------------------------------ decode
 
-__global__ void __launch_bounds__(kSortThreads) k_decode_hist(const __grid_constant__ Params P) {
+__global__ void __launch_bounds__(kSortThreads, 1) k_decode_hist(const __grid_constant__ Params P) {
     pdl_entry();
     extern __shared__ int sm[];
     int* h1 = sm;           // [n1]
@@ -157,7 +157,7 @@ __device__ void chunk_stable_ranks(int c, int64_t count, int nb, int* cnt, Digit
     __syncthreads();
 }
 
-__global__ void __launch_bounds__(kSortThreads) k_scatter13(const __grid_constant__ Params P) {
+__global__ void __launch_bounds__(kSortThreads, 1) k_scatter13(const __grid_constant__ Params P) {
     pdl_entry();
     extern __shared__ int cnt[];
     const int c = blockIdx.x;
@@ -182,7 +182,7 @@ __global__ void __launch_bounds__(kSortThreads) k_scatter13(const __grid_constan
         });
 }
 
-__global__ void __launch_bounds__(kSortThreads) k_scatter2(const __grid_constant__ Params P) {
+__global__ void __launch_bounds__(kSortThreads, 1) k_scatter2(const __grid_constant__ Params P) {
     pdl_entry();
     extern __shared__ int cnt[];
     const int c = blockIdx.x;
