@@ -15,6 +15,7 @@ namespace ttemb {
 constexpr int kFwdThreads = 256;
 constexpr int kListCap = 1024;      // touched i1 handled per round
 constexpr int kPoolWarps = 4;       // warps per bag
+constexpr int kPoolPer = 3;         // lookups of a warp whose T and G3 loads are in flight together
 constexpr int kMaxDPerLane = 8;     // generic pool path: D <= 256
 constexpr int kScatterParts = kSmallChunk / (kPoolWarps * 32);  // grouping-scatter blocks per chunk
 static_assert(kScatterParts * kPoolWarps * 32 == kSmallChunk, "scatter parts cover a chunk");
@@ -464,8 +465,7 @@ __device__ void pool_bag_static(const Params& P, const TableDev& T, int64_t bag,
     for (int v = 0; v < H; ++v) acc[v] = 0.f;
     if (P.cache_n == 0) {
         // warp w takes lookups lo + w + kPoolWarps l; lane l first loads the indices of the
-        // warp's l-th lookup of a round (one pass), then the warp walks them two at a time:
-        // both lookups' T and G3 values are in flight together
+        // warp's l-th lookup of a round (one pass), then the warp walks them kPoolPer at a time
         for (int64_t nb0 = lo; nb0 < hi; nb0 += 32 * kPoolWarps) {
             const int64_t nl = nb0 + w + (int64_t)kPoolWarps * lane;
             int i1l = 0, i2l = 0, i3l = 0;
@@ -479,47 +479,50 @@ __device__ void pool_bag_static(const Params& P, const TableDev& T, int64_t bag,
             const int64_t left = hi - nb0 - w;  // this warp's lookups nb0 + w + kPoolWarps l < hi
             const int64_t c64 = left <= 0 ? 0 : (left + kPoolWarps - 1) / kPoolWarps;
             const int cnt = c64 > 32 ? 32 : (int)c64;
-            for (int l = 0; l < cnt; l += 2) {
-                const bool two = l + 1 < cnt;
-                const int lb = two ? l + 1 : l;
-                const int i1a = __shfl_sync(0xffffffffu, i1l, l), i2a = __shfl_sync(0xffffffffu, i2l, l);
-                const int i3a = __shfl_sync(0xffffffffu, i3l, l);
-                const float sa = __shfl_sync(0xffffffffu, sl, l);
-                const int i1b = __shfl_sync(0xffffffffu, i1l, lb), i2b = __shfl_sync(0xffffffffu, i2l, lb);
-                const int i3b = __shfl_sync(0xffffffffu, i3l, lb);
-                const float sb = two ? __shfl_sync(0xffffffffu, sl, lb) : 0.f;
-                const float* Tpa = t_of_pair(P, T, i2a, i1a) + lj * J12H * R2;
-                const float* Tpb = t_of_pair(P, T, i2b, i1b) + lj * J12H * R2;
-                const float* g3a = T.G3 + (int64_t)i3a * R2 * Q3;
-                const float* g3b = T.G3 + (int64_t)i3b * R2 * Q3;
-                float ta[J12H][NC], tb[J12H][NC], ga[NC][Q3], gb[NC][Q3];
+            for (int l = 0; l < cnt; l += kPoolPer) {
+                // kPoolPer lookups of this warp: their T and G3 values are all in flight together
+                int li[kPoolPer];
+                float sv[kPoolPer];
+                const float* Tp[kPoolPer];
+                const float* g3p[kPoolPer];
 #pragma unroll
-                for (int k = 0; k < NC; ++k) {
-                    const int c = lc + 16 * k;
-#pragma unroll
-                    for (int j = 0; j < J12H; ++j) {
-                        ta[j][k] = __ldg(Tpa + j * R2 + c);
-                        tb[j][k] = __ldg(Tpb + j * R2 + c);
-                    }
-#pragma unroll
-                    for (int j3 = 0; j3 < Q3; j3 += 4) {
-                        const float4 x = __ldg(reinterpret_cast<const float4*>(g3a + c * Q3 + j3));
-                        const float4 y = __ldg(reinterpret_cast<const float4*>(g3b + c * Q3 + j3));
-                        ga[k][j3] = x.x; ga[k][j3 + 1] = x.y; ga[k][j3 + 2] = x.z; ga[k][j3 + 3] = x.w;
-                        gb[k][j3] = y.x; gb[k][j3 + 1] = y.y; gb[k][j3 + 2] = y.z; gb[k][j3 + 3] = y.w;
-                    }
+                for (int q = 0; q < kPoolPer; ++q) {
+                    const bool valid = l + q < cnt;
+                    li[q] = valid ? l + q : l;
+                    const int i1q = __shfl_sync(0xffffffffu, i1l, li[q]), i2q = __shfl_sync(0xffffffffu, i2l, li[q]);
+                    const int i3q = __shfl_sync(0xffffffffu, i3l, li[q]);
+                    const float sq = __shfl_sync(0xffffffffu, sl, li[q]);
+                    sv[q] = valid ? sq : 0.f;
+                    Tp[q] = t_of_pair(P, T, i2q, i1q) + lj * J12H * R2;
+                    g3p[q] = T.G3 + (int64_t)i3q * R2 * Q3;
                 }
+                float tv[kPoolPer][J12H][NC], gv[kPoolPer][NC][Q3];
+#pragma unroll
+                for (int q = 0; q < kPoolPer; ++q)
+#pragma unroll
+                    for (int k = 0; k < NC; ++k) {
+                        const int c = lc + 16 * k;
+#pragma unroll
+                        for (int j = 0; j < J12H; ++j) tv[q][j][k] = __ldg(Tp[q] + j * R2 + c);
+#pragma unroll
+                        for (int j3 = 0; j3 < Q3; j3 += 4) {
+                            const float4 x = __ldg(reinterpret_cast<const float4*>(g3p[q] + c * Q3 + j3));
+                            gv[q][k][j3] = x.x; gv[q][k][j3 + 1] = x.y; gv[q][k][j3 + 2] = x.z; gv[q][k][j3 + 3] = x.w;
+                        }
+                    }
 #pragma unroll
                 for (int j = 0; j < J12H; ++j)
 #pragma unroll
                     for (int j3 = 0; j3 < Q3; ++j3) {
-                        float x = 0.f, y = 0.f;
+                        float a = acc[j * Q3 + j3];
 #pragma unroll
-                        for (int k = 0; k < NC; ++k) {
-                            x = fmaf(ta[j][k], ga[k][j3], x);
-                            y = fmaf(tb[j][k], gb[k][j3], y);
+                        for (int q = 0; q < kPoolPer; ++q) {
+                            float x = 0.f;
+#pragma unroll
+                            for (int k = 0; k < NC; ++k) x = fmaf(tv[q][j][k], gv[q][k][j3], x);
+                            a = fmaf(sv[q], x, a);
                         }
-                        acc[j * Q3 + j3] = fmaf(sb, y, fmaf(sa, x, acc[j * Q3 + j3]));
+                        acc[j * Q3 + j3] = a;
                     }
             }
         }

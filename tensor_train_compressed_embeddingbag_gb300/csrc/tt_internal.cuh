@@ -334,12 +334,13 @@ __device__ __forceinline__ void lfu_count(const Params& P, int64_t row) {
     }
 }
 
-__device__ __forceinline__ void decode_lookup(const Params& P, int64_t n, int bag, int& t, int& i1, int& i2,
-                                              int& i3, int epoch) {
+// Lookup n with its index `row` and weight `w` (loaded by the caller, so that the
+// loads can be issued early).
+__device__ __forceinline__ void decode_lookup(const Params& P, int64_t n, int bag, int64_t row, float w, int& t,
+                                              int& i1, int& i2, int& i3, int epoch) {
     t = table_of_bag(P, bag);
     const TableDev& T = P.tables[t];
-    int64_t row = P.idx[n];
-    float s = P.w ? P.w[n] : 1.0f;
+    float s = w;
     if (row < 0 || row >= T.E) {
         atomicOr(P.err, kErrIndex);
         row = 0;

@@ -48,7 +48,7 @@ __global__ void __launch_bounds__(kSortThreads, 1) k_decode_hist(const __grid_co
     const int64_t hi = (lo + kChunk < P.nnz) ? lo + kChunk : P.nnz;
     for (int64_t n = lo + threadIdx.x; n < hi; n += blockDim.x) {
         int t, i1, i2, i3;
-        decode_lookup(P, n, (int)bag_of(P, n), t, i1, i2, i3, *P.epoch);
+        decode_lookup(P, n, (int)bag_of(P, n), P.idx[n], P.w ? P.w[n] : 1.0f, t, i1, i2, i3, *P.epoch);
         const TableDev& T = P.tables[t];
         atomicAdd(&h1[T.base1 + i1], 1);
         atomicAdd(&h3[T.base3 + i3], 1);
@@ -269,16 +269,20 @@ __global__ void __launch_bounds__(kSmallChunk) k_decode_small(const __grid_const
     const int c = blockIdx.x;
     const int64_t lo = (int64_t)c * kSmallChunk;
     const int64_t hi = (lo + kSmallChunk < P.nnz) ? lo + kSmallChunk : P.nnz;
+    // this thread's index, weight and the epoch: in flight while the offsets are checked and staged
+    const int64_t n = lo + threadIdx.x;
+    const int64_t row = n < hi ? P.idx[n] : 0;
+    const float wv = (n < hi && P.w) ? P.w[n] : 1.0f;
+    const int epoch = *P.epoch;
     if (c == 0 && threadIdx.x == 64 && (P.off[0] != 0 || P.off[P.nbags] != P.nnz)) atomicOr(P.err, kErrOffsets);
     for (int64_t g = (int64_t)c * blockDim.x + threadIdx.x; g < P.nbags; g += (int64_t)gridDim.x * blockDim.x)
         if (P.off[g] > P.off[g + 1]) atomicOr(P.err, kErrOffsets);
     const int nst = stage_bag_offsets(P, lo, hi, soff, sb, kDecodeOffs);
-    const int64_t n = lo + threadIdx.x;
     int d[3] = {-1, -1, -1};
     if (n < hi) {
         const int64_t bag = nst ? staged_bag(soff, sb[0], nst, n) : bag_of(P, n);
         int t, i1, i2, i3;
-        decode_lookup(P, n, (int)bag, t, i1, i2, i3, *P.epoch);
+        decode_lookup(P, n, (int)bag, row, wv, t, i1, i2, i3, epoch);
         const TableDev& T = P.tables[t];
         d[0] = T.base1 + i1;
         d[1] = T.base2 + i2;
