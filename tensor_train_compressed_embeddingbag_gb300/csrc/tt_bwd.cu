@@ -111,6 +111,7 @@ __device__ void load_and_sort_tile(const Params& P, int start, int len, unsigned
 constexpr int kReduceSlots = 1024;   // slots gathered per round
 constexpr int kReducePer = 32;       // loads in flight per thread (scalar columns)
 constexpr int kReducePer4 = 16;      // float4 loads in flight per thread
+constexpr int kP3Items = 3;          // P3 items per thread whose T loads are in flight together
 
 __device__ void reduce_slice(const Params& P, int bglob, int* slots, int* sh, float* sacc) {
     const bool first_core = bglob < P.n1;
@@ -394,14 +395,14 @@ __device__ void tile_bwd_body(const Params& P, const TableDev& T, const Dm dm, u
 
     // ---- dG3 partial per tile-row, columns c of this split: P3[c][j3] = sum_j12 T[j12][c] gs[j12 q3 + j3]
     if constexpr (Dm::kStatic) {
-        // two items per thread: the T columns of both are loaded before either is summed
+        // kP3Items items per thread: the T columns of all are loaded before any is summed
         constexpr int Q3 = Dm::q3(), Q12 = Dm::q1() * Dm::q2(), R2 = Dm::r2();
         const int items = nrows * r2s;
-        for (int e0 = threadIdx.x; e0 < items; e0 += 2 * kBwdThreads) {
-            float tv[2][Q12];
-            int rowv[2], cv[2];
+        for (int e0 = threadIdx.x; e0 < items; e0 += kP3Items * kBwdThreads) {
+            float tv[kP3Items][Q12];
+            int rowv[kP3Items], cv[kP3Items];
 #pragma unroll
-            for (int v = 0; v < 2; ++v) {
+            for (int v = 0; v < kP3Items; ++v) {
                 const int e = e0 + v * kBwdThreads;
                 rowv[v] = e < items ? e / r2s : -1;
                 cv[v] = e < items ? c0 + (e - rowv[v] * r2s) : 0;
@@ -411,7 +412,7 @@ __device__ void tile_bwd_body(const Params& P, const TableDev& T, const Dm dm, u
                 for (int j12 = 0; j12 < Q12; ++j12) tv[v][j12] = rowv[v] >= 0 ? __ldg(Tp + j12 * R2) : 0.f;
             }
 #pragma unroll
-            for (int v = 0; v < 2; ++v) {
+            for (int v = 0; v < kP3Items; ++v) {
                 if (rowv[v] < 0) continue;
                 const float* gr = gs + rowv[v] * D;
                 float acc[Q3];
@@ -561,7 +562,7 @@ __device__ void tile_bwd_body(const Params& P, const TableDev& T, const Dm dm, u
             }
             __syncthreads();
             // Q[u][j1][a] = sum_jc' dts[u][jc'][j1] g2t[jc'][a]: thread (kh, a4, u)
-            {
+            if ((w / (A4 / AL)) * UL < nb) {  // warps whose pairs all lie past the batch skip it
                 const int kh = lane % KH, al = (lane / KH) % AL, ul = lane / (KH * AL);
                 const int a4 = (w % (A4 / AL)) * AL + al, u = (w / (A4 / AL)) * UL + ul;
                 float q[4][4];
