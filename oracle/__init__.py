@@ -283,3 +283,70 @@ def lfu_select(rows, counts, cache_size):
         for w, (_, r) in enumerate(m[:LFU_WAYS]):
             out[k * LFU_WAYS + w] = r
     return out
+
+
+# ---------------------------------------------------------------- trainable cache rows
+# FBTT README, "Parameters": sparse (backward gives the gradient w.r.t. the TT cores or
+# the cache); "Software Cache": a cached row is read from the cache, without
+# decompressing it.  Reading: a row that sits in the cache takes the cached value in
+# place of its TT row, so the output is linear in the cached values and the cores see
+# only the lookups of rows outside the cache.
+
+def _cache_split(cache_rows, indices, offsets, weights, mode):
+    """(slot of every lookup or -1, pooling scale, bag) for a single table."""
+    idx, off = _i64(indices), _i64(offsets)
+    slot_of = {r: k for k, r in enumerate(np.asarray(cache_rows, dtype=np.int64).tolist()) if r >= 0}
+    slot = np.array([slot_of.get(r, -1) for r in idx.tolist()], dtype=np.int64)
+    lengths = np.diff(off)
+    bag = np.repeat(np.arange(lengths.shape[0]), lengths)
+    w = np.ones(idx.shape[0]) if weights is None else np.asarray(weights, dtype=np.float64)
+    scale = w / np.maximum(lengths[bag], 1) if mode == "mean" else w
+    return slot, scale, bag
+
+
+def cache_miss_weights(cache_rows, indices, offsets, weights=None):
+    """Per-sample weights with every cached lookup's weight set to 0: with them the
+    plain TT functions give the cores' share of a step (the mean-mode divisor still
+    counts every lookup of the bag)."""
+    slot, _, _ = _cache_split(cache_rows, indices, offsets, None, "sum")
+    w = np.ones(slot.shape[0]) if weights is None else np.asarray(weights, dtype=np.float64)
+    return np.where(slot >= 0, 0.0, w)
+
+
+def cached_forward(tables, cores, cache_rows, cache_vals, indices, offsets, weights=None, mode="sum", bags=None):
+    """Pooled output with trainable cache rows, float64 (single table; ``bags``: a subset)."""
+    slot, scale, bag = _cache_split(cache_rows, indices, offsets, weights, mode)
+    out = forward(tables, cores, indices, offsets, cache_miss_weights(cache_rows, indices, offsets, weights), mode)
+    hit = slot >= 0
+    np.add.at(out, bag[hit], scale[hit, None] * np.asarray(cache_vals, dtype=np.float64)[slot[hit]])
+    return out if bags is None else out[_i64(bags)]
+
+
+def cache_grad(cache_rows, indices, offsets, grad_out, weights=None, mode="sum"):
+    """(dL/d cached value ``[slots, D]``, touched flag per slot): the sum over the lookups
+    of each cached row of pooling scale x grad_out of the bag."""
+    slot, scale, bag = _cache_split(cache_rows, indices, offsets, weights, mode)
+    go = np.asarray(grad_out, dtype=np.float64)
+    n = np.asarray(cache_rows).shape[0]
+    d = np.zeros((n, go.shape[1]))
+    hit = slot >= 0
+    np.add.at(d, slot[hit], scale[hit, None] * go[bag[hit]])
+    touched = np.zeros(n, dtype=bool)
+    touched[slot[hit]] = True
+    return d, touched
+
+
+def cache_sgd(vals, grad, touched, lr):
+    """SGD on the touched cached values."""
+    v = np.array(vals, dtype=np.float64)
+    v[touched] -= float(lr) * grad[touched]
+    return v
+
+
+def cache_adagrad(vals, state, grad, touched, lr, eps):
+    """Element-wise Adagrad (the cores' rule) on the touched cached values: (values, state)."""
+    v = np.array(vals, dtype=np.float64)
+    s = np.array(state, dtype=np.float64)
+    s[touched] += grad[touched] ** 2
+    v[touched] -= float(lr) * grad[touched] / (np.sqrt(s[touched]) + float(eps))
+    return v, s

@@ -347,3 +347,69 @@ def test_lfu_select_brute_force():
         assert got == want
     r2, c2 = oracle.lfu_counts([5, 3, 5, 9], np.array([5]))
     assert r2.tolist() == [3, 5, 9] and c2.tolist() == [1, 3, 1]
+
+
+@pytest.mark.parametrize("mode,weighted", [("sum", True), ("mean", False), ("mean", True)])
+def test_trainable_cache_matches_torch_autograd(mode, weighted):
+    """Trainable cache rows: a table whose cached rows are separate parameters.  The
+    oracle's output, cache gradient and (miss-only) core gradients equal torch
+    autograd through the full table with those rows swapped in."""
+    rng = np.random.default_rng(13)
+    spec = TableSpec(100, [5, 4, 6], [2, 3, 2], [3, 5])
+    cores = rand_cores(rng, spec)
+    B = 9
+    lengths = rng.integers(0, 7, size=B)
+    off = np.concatenate([[0], np.cumsum(lengths)])
+    hot = np.array([3, 17, 42, 99, 64], dtype=np.int64)
+    idx = np.where(rng.random(int(off[-1])) < 0.5, rng.choice(hot, int(off[-1])), rng.integers(0, 100, int(off[-1])))
+    w = rng.random(idx.shape[0]) if weighted else None
+    go = rng.standard_normal((B, 12))
+    cache_rows = np.array([17, -1, 3, 64, 55], dtype=np.int64)  # 55 is never looked up, slot 1 empty
+    vals = rng.standard_normal((5, 12))
+    gt = [torch.from_numpy(c.copy()).requires_grad_(True) for c in cores]
+    cv = torch.from_numpy(vals.copy()).requires_grad_(True)
+    full = torch.einsum("xja,yakc,zcl->xyzjkl", gt[0][:, 0], gt[1], gt[2][..., 0]).reshape(120, 12)
+    rows = [cv[k] if k >= 0 else full[r] for r, k in
+            ((r, list(cache_rows).index(r) if r in cache_rows else -1) for r in range(100))]
+    table = torch.stack(rows)
+    bag = torch.from_numpy(np.repeat(np.arange(B), lengths))
+    wt = torch.ones(idx.shape[0], dtype=torch.float64) if w is None else torch.from_numpy(w)
+    if mode == "mean":
+        wt = wt / torch.from_numpy(np.maximum(lengths, 1)).double()[bag]
+    out = torch.zeros(B, 12, dtype=torch.float64).index_add_(0, bag, wt[:, None] * table[torch.from_numpy(idx)])
+    (out * torch.from_numpy(go)).sum().backward()
+    np.testing.assert_allclose(oracle.cached_forward([spec], [cores], cache_rows, vals, idx, off, w, mode),
+                               out.detach().numpy(), rtol=1e-12, atol=1e-13)
+    d, touched = oracle.cache_grad(cache_rows, idx, off, go, w, mode)
+    np.testing.assert_allclose(d, cv.grad.numpy(), rtol=1e-12, atol=1e-13)
+    assert touched.tolist() == [r in set(idx.tolist()) for r in cache_rows]
+    mw = oracle.cache_miss_weights(cache_rows, idx, off, w)
+    for k in range(3):
+        dG = oracle.backward_core([spec], [cores], idx, off, go, 0, k, weights=mw, mode=mode)
+        np.testing.assert_allclose(dG, gt[k].grad.numpy(), rtol=1e-12, atol=1e-13)
+
+
+def test_trainable_cache_updates_match_torch_optim():
+    """The cached values' SGD and Adagrad steps equal torch.optim on a parameter whose
+    untouched rows get a zero gradient (with eps > 0 such rows do not move)."""
+    rng = np.random.default_rng(14)
+    vals = rng.standard_normal((6, 4))
+    grad = rng.standard_normal((6, 4))
+    touched = np.array([True, False, True, True, False, True])
+    grad[~touched] = 0.0
+    lr, eps = 0.07, 1e-10
+    p = torch.from_numpy(vals.copy()).requires_grad_(True)
+    p.grad = torch.from_numpy(grad.copy())
+    torch.optim.SGD([p], lr=lr).step()
+    np.testing.assert_allclose(oracle.cache_sgd(vals, grad, touched, lr), p.detach().numpy(), rtol=1e-14)
+    state0 = rng.uniform(0.0, 1.0, size=vals.shape)
+    state0[1] = 0.0  # an untouched row with an empty accumulator stays put
+    p = torch.from_numpy(vals.copy()).requires_grad_(True)
+    opt = torch.optim.Adagrad([p], lr=lr, eps=eps)
+    opt.state[p]["sum"] = torch.from_numpy(state0.copy())
+    opt.state[p]["step"] = torch.tensor(0.0)
+    p.grad = torch.from_numpy(grad.copy())
+    opt.step()
+    v, s = oracle.cache_adagrad(vals, state0, grad, touched, lr, eps)
+    np.testing.assert_allclose(v, p.detach().numpy(), rtol=1e-13)
+    np.testing.assert_allclose(s, opt.state[p]["sum"].numpy(), rtol=1e-13)
