@@ -166,7 +166,7 @@ tt_status tt_emb_backward(tt_emb* h, const float* grad_out_dev, float lr, tt_str
  * The handle keeps the pointers, which must stay valid while it is used.
  * Synchronous (copies the handle's device tables); not for stream capture.
  * Returns TT_ERR_ARG (null handle, unknown optim, bad eps, null or misaligned
- * aux), TT_ERR_CUDA.
+ * aux, Adagrad with eps = 0 while the cache rows are trainable), TT_ERR_CUDA.
  */
 tt_status tt_emb_set_optimizer(tt_emb* h, int32_t optim, float eps, float* const* aux);
 
@@ -217,10 +217,11 @@ tt_status tt_emb_cache_disable(tt_emb* h);
  * tt_emb_lfu_populate: rebuild the cache from the counts: set k (k =
  *   (h >> 32) mod sets) holds the 32 most frequently counted rows whose hash
  *   maps to k (ties: the smaller row id); each cached value is computed from
- *   the cores.  Cached rows are exact copies of TT rows: gradients go to the
- *   cores and a row whose slices change is recomputed on its next hit, so
- *   results equal the no-cache results (FBTT's trainable cache rows are not
- *   built).  Synchronous.
+ *   the cores.  By default cached rows are exact copies of TT rows: gradients
+ *   go to the cores and a row whose slices change is recomputed on its next
+ *   hit, so results equal the no-cache results.  With
+ *   tt_emb_cache_set_trainable the cached rows are parameters of their own
+ *   (see there).  Synchronous.
  * tt_emb_lfu_read: copy the counted (row, count) pairs, sorted by row, into
  *   caller-owned host arrays of cap entries; *n_out = number of pairs.
  * tt_emb_lfu_cached_rows: copy the cache's rows per slot (slot = set * 32 +
@@ -235,6 +236,43 @@ tt_status tt_emb_lfu_populate(tt_emb* h, tt_stream stream);
 tt_status tt_emb_lfu_read(tt_emb* h, int64_t* rows_host, uint32_t* counts_host, int64_t cap, int64_t* n_out);
 tt_status tt_emb_lfu_cached_rows(tt_emb* h, int64_t* rows_host, int64_t cap, int64_t* n_out);
 tt_status tt_emb_lfu_disable(tt_emb* h);
+
+/*
+ * Trainable cache rows (FBTT README, "Parameters": sparse, where backward
+ * gives the gradient w.r.t. the TT cores or the cache; "Software Cache":
+ * cached rows are loaded without decompressing them).  Single-table handles
+ * only (TT_ERR_STATE otherwise).
+ *
+ * tt_emb_cache_set_trainable(h, 1): from the next forward pass on, a lookup
+ *   whose row is cached (a hit) reads the cached value instead of its TT row,
+ *   and backward gives the hit's gradient to the cached value and none to the
+ *   cores: the gradient of cached value [slot][j] is the sum over the hits of
+ *   that slot of (the lookup's pooling scale: weight, divided by the bag
+ *   length in mean mode) x grad_out[bag][j].  The sum is taken in 64-bit fixed
+ *   point with integer atomics, so it does not depend on the order of the
+ *   hits (each term is rounded to a step of 2^-S with |sum| < 2^62, S set by
+ *   the step's largest term and lookup count).  The optimizer of
+ *   tt_emb_set_optimizer then updates the cached values that some hit touched
+ *   (SGD; Adagrad with its own state per cached value, zero at populate; or
+ *   TT_OPT_GRAD, which keeps the gradient for tt_emb_cache_read and gives
+ *   untouched values 0); misses train the cores as before.  The cache state
+ *   (installed now or later by a populate call) is initialised from the cores.
+ *   Adagrad with eps = 0 is refused (TT_ERR_ARG): a slice that only hits touch
+ *   gets a zero gradient.  (h, 0): back to exact-copy rows, recomputed from
+ *   the cores now.  Synchronous.
+ * tt_emb_cache_read: copy the cached values ([slots][D] fp32, slot order of
+ *   tt_emb_lfu_cached_rows) into vals_dev and, trainable mode only, the last
+ *   gradients of TT_OPT_GRAD into grads_dev (caller-owned device buffers; either
+ *   may be NULL).  Stream-ordered.
+ * tt_emb_cache_write: overwrite the cached values from vals_dev (same layout;
+ *   trainable mode only: an external optimizer's step on the values after
+ *   TT_OPT_GRAD).  Stream-ordered.
+ * Return TT_ERR_ARG, TT_ERR_STATE (batched handle; grads_dev or a write
+ * outside trainable mode), TT_ERR_NOMEM, TT_ERR_CUDA.
+ */
+tt_status tt_emb_cache_set_trainable(tt_emb* h, int32_t trainable, tt_stream stream);
+tt_status tt_emb_cache_read(tt_emb* h, float* vals_dev, float* grads_dev, tt_stream stream);
+tt_status tt_emb_cache_write(tt_emb* h, const float* vals_dev, tt_stream stream);
 
 /*
  * Copy the decode of the most recent forward pass: for every lookup its

@@ -49,6 +49,9 @@ __all__ = [
     "tt_emb_lfu_disable",
     "tt_emb_cache_populate",
     "tt_emb_cache_disable",
+    "tt_emb_cache_set_trainable",
+    "tt_emb_cache_read",
+    "tt_emb_cache_write",
     "tt_emb_get_decoded",
     "tt_emb_get_last_error",
     "tt_emb_set_stage_timing",
@@ -81,6 +84,9 @@ EXPORTED_SYMBOLS = (
     "tt_emb_lfu_disable",
     "tt_emb_cache_populate",
     "tt_emb_cache_disable",
+    "tt_emb_cache_set_trainable",
+    "tt_emb_cache_read",
+    "tt_emb_cache_write",
     "tt_emb_get_decoded",
     "tt_emb_get_last_error",
     "tt_emb_set_stage_timing",
@@ -147,6 +153,9 @@ def load_library():
             "tt_emb_lfu_disable": (ctypes.c_int, [vp]),
             "tt_emb_cache_populate": (ctypes.c_int, [vp, vp, i64, vp]),
             "tt_emb_cache_disable": (ctypes.c_int, [vp]),
+            "tt_emb_cache_set_trainable": (ctypes.c_int, [vp, i32, vp]),
+            "tt_emb_cache_read": (ctypes.c_int, [vp, vp, vp, vp]),
+            "tt_emb_cache_write": (ctypes.c_int, [vp, vp, vp]),
             "tt_emb_get_decoded": (ctypes.c_int, [vp, vp, vp, vp, vp, vp, vp]),
             "tt_emb_get_last_error": (ctypes.c_int, [vp]),
             "tt_emb_set_stage_timing": (ctypes.c_int, [vp, ctypes.c_int]),
@@ -309,6 +318,21 @@ def tt_emb_cache_populate(h, rows: torch.Tensor, stream=None):
 
 def tt_emb_cache_disable(h):
     _check(load_library().tt_emb_cache_disable(h), "tt_emb_cache_disable")
+
+
+def tt_emb_cache_set_trainable(h, trainable: bool, stream=None):
+    _check(load_library().tt_emb_cache_set_trainable(h, 1 if trainable else 0, _stream(stream)),
+           "tt_emb_cache_set_trainable")
+
+
+def tt_emb_cache_read(h, vals: Optional[torch.Tensor], grads: Optional[torch.Tensor] = None, stream=None):
+    """Copy the cached values (and, trainable rows, their last gradients) into [slots, D] fp32 CUDA tensors."""
+    _check(load_library().tt_emb_cache_read(h, _ptr(vals), _ptr(grads), _stream(stream)), "tt_emb_cache_read")
+
+
+def tt_emb_cache_write(h, vals: torch.Tensor, stream=None):
+    """Overwrite the trainable cached values from a [slots, D] fp32 CUDA tensor."""
+    _check(load_library().tt_emb_cache_write(h, _ptr(vals), _stream(stream)), "tt_emb_cache_write")
 
 
 def tt_emb_get_decoded(h, nnz: int, device, stream=None):
@@ -514,6 +538,13 @@ class TTEmbeddingBag(_TTBase):
     sparse=True fuses the update (optimizer 'sgd' or 'adagrad', learning_rate,
     eps) into the backward pass; sparse=False returns the cores' gradients.
 
+    use_cache: a hot-row cache, filled by ``cache_populate()`` (with ``cache_size``
+    rows by the LFU policy, or the given ``cache_rows``).  cache_trainable=True
+    (FBTT's cache): cached rows are parameters of their own, initialised from the
+    cores; their gradient updates them with the module's optimizer (sparse=True)
+    or is read with ``cache_grad()`` (sparse=False).  False: cached rows are exact
+    copies of TT rows and all gradients go to the cores.
+
     cores: optional initial cores ``[G1, G2, G3]`` with shapes
     ``[p_k, r_{k-1}, q_k, r_k]``; default i.i.d. N(0, sigma).
     """
@@ -523,7 +554,8 @@ class TTEmbeddingBag(_TTBase):
                  learning_rate: float = 0.1, cores: Optional[Sequence[torch.Tensor]] = None, sigma: float = 0.1,
                  device=None, use_cache: bool = False, cache_rows: Optional[torch.Tensor] = None,
                  sparse: bool = True, optimizer: str = "sgd", eps: float = 1.0e-10, weight_dist: str = "normal",
-                 generator: Optional[torch.Generator] = None, cache_size: int = 0, hashtbl_size: int = 0):
+                 generator: Optional[torch.Generator] = None, cache_size: int = 0, hashtbl_size: int = 0,
+                 cache_trainable: bool = True):
         super().__init__()
         device = torch.device(device or "cuda")
         if tt_p_shapes is None or tt_q_shapes is None:
@@ -548,6 +580,9 @@ class TTEmbeddingBag(_TTBase):
                 raise ValueError(f"core {k} has shape {tuple(c.shape)}, expected {shapes[k]}")
         self._h = tt_emb_create(self.num_embeddings, self.p, self.q, self.ranks, self._core_list())
         self._set_optimizer(sparse, optimizer, eps)
+        self.cache_trainable = bool(use_cache and cache_trainable)
+        if self.cache_trainable:
+            tt_emb_cache_set_trainable(self._h, True)
         if use_cache and cache_rows is not None:
             self.cache_populate(cache_rows)
         elif use_cache and cache_size > 0:
@@ -573,6 +608,26 @@ class TTEmbeddingBag(_TTBase):
             tt_emb_lfu_populate(self._h)
         else:
             tt_emb_cache_populate(self._h, rows.to(torch.int64).contiguous())
+
+    def cache_rows(self):
+        """Row per cache slot (set * 32 + way for the LFU policy; -1 = empty), numpy int64."""
+        return tt_emb_lfu_cached_rows(self._h)
+
+    def cache_values(self) -> torch.Tensor:
+        """Copy of the cached values, [slots, embedding_dim]."""
+        out = torch.empty((self.cache_rows().shape[0], self.embedding_dim), dtype=torch.float32, device=self.G1.device)
+        tt_emb_cache_read(self._h, out)
+        return out
+
+    def cache_grad(self) -> torch.Tensor:
+        """Gradient of the cached values from the last backward (sparse=False, trainable cache)."""
+        out = torch.empty((self.cache_rows().shape[0], self.embedding_dim), dtype=torch.float32, device=self.G1.device)
+        tt_emb_cache_read(self._h, None, out)
+        return out
+
+    def cache_write(self, vals: torch.Tensor):
+        """Set the trainable cached values (an external optimizer's step, sparse=False)."""
+        tt_emb_cache_write(self._h, vals.to(device=self.G1.device, dtype=torch.float32).contiguous())
 
     def forward(self, input, offsets, per_sample_weights=None, mode: str = "sum", include_last_offset=False):
         return self._run(input, offsets, per_sample_weights, mode, include_last_offset)

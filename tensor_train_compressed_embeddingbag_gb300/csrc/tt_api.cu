@@ -70,6 +70,13 @@ struct tt_emb {
     float* d_cache_vals = nullptr;
     int* d_cache_stamp = nullptr;
     int* d_slice_stamp = nullptr;
+    // trainable cache rows (tt_emb_cache_set_trainable)
+    bool cache_train = false;
+    unsigned long long* d_cache_acc = nullptr;
+    float* d_cache_state = nullptr;
+    float* d_cache_grad = nullptr;
+    unsigned* d_cache_gmax = nullptr;
+    int* d_cache_touch = nullptr;
     // LFU policy (tt_emb_lfu_enable)
     unsigned long long* d_freq_keys = nullptr;
     unsigned* d_freq_counts = nullptr;
@@ -117,6 +124,8 @@ size_t carve(tt_emb* h, void* base, int64_t nnz, bool assign) {
     int* lk_i3 = A.take<int>(N);
     int* lk_bag = A.take<int>(N);
     float* lk_s = A.take<float>(N);
+    int* lk_hit = A.take<int>(N);
+    float* lk_sh = A.take<float>(N);
     uint16_t* lr1 = A.take<uint16_t>(Ns);
     uint16_t* lr2 = A.take<uint16_t>(Ns);
     uint16_t* lr3 = A.take<uint16_t>(Ns);
@@ -144,6 +153,7 @@ size_t carve(tt_emb* h, void* base, int64_t nnz, bool assign) {
     float* dG2part = A.take<float>(part_floats);
     if (assign) {
         P.lk_i1 = lk_i1; P.lk_i2 = lk_i2; P.lk_i3 = lk_i3; P.lk_bag = lk_bag; P.lk_s = lk_s;
+        P.lk_hit = lk_hit; P.lk_sh = lk_sh;
         P.lr1 = lr1; P.lr2 = lr2; P.lr3 = lr3;
         P.H1 = H1; P.H3 = H3; P.H2 = H2;
         P.pi1 = pi1; P.pi3 = pi3; P.pi21 = pi21; P.sigma = sigma;
@@ -346,6 +356,11 @@ void free_handle(tt_emb* h) {
     cudaFree(h->d_cache_vals);
     cudaFree(h->d_cache_stamp);
     cudaFree(h->d_slice_stamp);
+    cudaFree(h->d_cache_acc);
+    cudaFree(h->d_cache_state);
+    cudaFree(h->d_cache_grad);
+    cudaFree(h->d_cache_gmax);
+    cudaFree(h->d_cache_touch);
     cudaFree(h->d_freq_keys);
     cudaFree(h->d_freq_counts);
     for (int w = 0; w < 2; ++w)
@@ -501,6 +516,12 @@ tt_status tt_emb_forward(tt_emb* h, const int64_t* indices, int64_t nnz, const i
     P.cache_stamp = h->d_cache_stamp;
     P.slice_stamp = h->d_slice_stamp;
     P.step = h->step;
+    P.cache_train = (h->cache_train && h->cache_n > 0) ? 1 : 0;
+    P.cache_acc = h->d_cache_acc;
+    P.cache_state = h->d_cache_state;
+    P.cache_grad = h->d_cache_grad;
+    P.cache_gmax = h->d_cache_gmax;
+    P.cache_touch = h->d_cache_touch;
     h->last_stream = s;
     h->has_fwd = false;
     if (num_bags == 0) {
@@ -554,6 +575,14 @@ tt_status tt_emb_backward(tt_emb* h, const float* grad_out, float lr, tt_stream 
     if (P.nnz > 0) {
         q.run("tile_bwd", launch_tile_bwd);
         q.run("reduce13", launch_reduce13);
+        if (P.cache_train) {
+            q.run("cache_gmax", launch_cache_gmax);
+            q.run("cache_acc", launch_cache_acc);
+            q.run("cache_apply", launch_cache_apply);
+        }
+    } else if (P.cache_train && P.opt == TT_OPT_GRAD) {
+        if (cudaMemsetAsync(h->d_cache_grad, 0, sizeof(float) * (size_t)h->cache_n * P.D, s) != cudaSuccess)
+            return TT_ERR_CUDA;
     }
     tt_status st = q.finish();
     if (h->cache_n > 0) ++h->step;
@@ -564,6 +593,8 @@ tt_status tt_emb_set_optimizer(tt_emb* h, int32_t optim, float eps, float* const
     if (!h) return TT_ERR_ARG;
     if (optim != TT_OPT_SGD && optim != TT_OPT_ADAGRAD && optim != TT_OPT_GRAD) return TT_ERR_ARG;
     if (optim == TT_OPT_ADAGRAD && !(eps >= 0.f && eps <= 3.0e38f)) return TT_ERR_ARG;
+    // a slice that only trainable cache hits touch gets a zero gradient: 0 / 0 with eps = 0
+    if (optim == TT_OPT_ADAGRAD && eps == 0.f && h->cache_train) return TT_ERR_ARG;
     if (optim != TT_OPT_SGD) {
         if (!aux) return TT_ERR_ARG;
         for (int i = 0; i < 3 * h->ntab; ++i)
@@ -593,6 +624,41 @@ tt_status tt_emb_full_weight(tt_emb* h, int32_t table, int64_t row0, int64_t nro
     return e == cudaSuccess ? TT_OK : TT_ERR_CUDA;
 }
 
+static void cache_train_free(tt_emb* h) {
+    cudaFree(h->d_cache_acc);
+    cudaFree(h->d_cache_state);
+    cudaFree(h->d_cache_grad);
+    cudaFree(h->d_cache_gmax);
+    cudaFree(h->d_cache_touch);
+    h->d_cache_acc = nullptr;
+    h->d_cache_state = nullptr;
+    h->d_cache_grad = nullptr;
+    h->d_cache_gmax = nullptr;
+    h->d_cache_touch = nullptr;
+}
+
+// Gradient state of the trainable cache rows, zeroed: fixed-point sums, Adagrad
+// accumulators, last gradients, the two gmax words and the touch flags.
+static tt_status cache_train_alloc(tt_emb* h, cudaStream_t s) {
+    const size_t nd = (size_t)h->cache_n * h->tabs[0].D;
+    if (cudaMalloc(&h->d_cache_acc, sizeof(unsigned long long) * nd) != cudaSuccess ||
+        cudaMalloc(&h->d_cache_state, sizeof(float) * nd) != cudaSuccess ||
+        cudaMalloc(&h->d_cache_grad, sizeof(float) * nd) != cudaSuccess ||
+        cudaMalloc(&h->d_cache_gmax, sizeof(unsigned) * 2) != cudaSuccess ||
+        cudaMalloc(&h->d_cache_touch, sizeof(int) * (size_t)h->cache_n) != cudaSuccess) {
+        cudaGetLastError();
+        cache_train_free(h);
+        return TT_ERR_NOMEM;
+    }
+    if (cudaMemsetAsync(h->d_cache_acc, 0, sizeof(unsigned long long) * nd, s) != cudaSuccess ||
+        cudaMemsetAsync(h->d_cache_state, 0, sizeof(float) * nd, s) != cudaSuccess ||
+        cudaMemsetAsync(h->d_cache_grad, 0, sizeof(float) * nd, s) != cudaSuccess ||
+        cudaMemsetAsync(h->d_cache_gmax, 0, sizeof(unsigned) * 2, s) != cudaSuccess ||
+        cudaMemsetAsync(h->d_cache_touch, 0, sizeof(int) * (size_t)h->cache_n, s) != cudaSuccess)
+        return TT_ERR_CUDA;
+    return TT_OK;
+}
+
 // Allocate the cache arrays for n slots of table 0 and fill them from host row ids
 // (-1 = empty slot); `sets` > 0 selects the set-associative layout.
 static tt_status cache_install(tt_emb* h, const std::vector<int64_t>& rows, int sets, cudaStream_t s) {
@@ -607,10 +673,17 @@ static tt_status cache_install(tt_emb* h, const std::vector<int64_t>& rows, int 
         tt_emb_cache_disable(h);
         return TT_ERR_NOMEM;
     }
+    h->cache_n = n;
+    if (h->cache_train) {
+        const tt_status st = cache_train_alloc(h, s);
+        if (st != TT_OK) {
+            tt_emb_cache_disable(h);
+            return st;
+        }
+    }
     if (cudaMemcpyAsync(h->d_cache_rows, rows.data(), sizeof(int64_t) * n, cudaMemcpyHostToDevice, s) != cudaSuccess ||
         cudaMemsetAsync(h->d_slice_stamp, 0, sizeof(int) * nslice, s) != cudaSuccess)
         return TT_ERR_CUDA;
-    h->cache_n = n;
     h->P.cache_sets = sets;
     Params P = h->P;
     P.cache_rows = h->d_cache_rows;
@@ -745,6 +818,11 @@ tt_status tt_emb_cache_populate(tt_emb* h, const int64_t* rows_dev, int64_t n, t
 tt_status tt_emb_cache_disable(tt_emb* h) {
     if (!h) return TT_ERR_ARG;
     if (h->cache_n > 0 || h->d_cache_rows) cudaDeviceSynchronize();
+    if (h->P.cache_train) {  // the last forward's hit slots refer to this cache
+        h->P.cache_train = 0;
+        h->has_fwd = false;
+    }
+    cache_train_free(h);
     cudaFree(h->d_cache_rows);
     cudaFree(h->d_cache_vals);
     cudaFree(h->d_cache_stamp);
@@ -758,6 +836,59 @@ tt_status tt_emb_cache_disable(tt_emb* h) {
     h->P.cache_sets = 0;
     h->P.slice_stamp = nullptr;
     return TT_OK;
+}
+
+tt_status tt_emb_cache_set_trainable(tt_emb* h, int32_t trainable, tt_stream stream) {
+    if (!h || (trainable != 0 && trainable != 1)) return TT_ERR_ARG;
+    if (h->ntab != 1) return TT_ERR_STATE;
+    if (trainable && h->P.opt == TT_OPT_ADAGRAD && h->P.eps == 0.f) return TT_ERR_ARG;
+    cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+    if (h->cache_n > 0) cudaDeviceSynchronize();
+    if (h->P.cache_train) {  // the last forward's hit slots refer to this cache state
+        h->P.cache_train = 0;
+        h->has_fwd = false;
+    }
+    cache_train_free(h);
+    h->cache_train = trainable != 0;
+    if (h->cache_n == 0) return TT_OK;
+    if (h->cache_train) {
+        const tt_status st = cache_train_alloc(h, s);
+        if (st != TT_OK) {
+            tt_emb_cache_disable(h);
+            return st;
+        }
+    }
+    // the cached values start again from the cores
+    Params P = h->P;
+    P.cache_rows = h->d_cache_rows;
+    P.cache_n = h->cache_n;
+    P.cache_vals = h->d_cache_vals;
+    P.cache_stamp = h->d_cache_stamp;
+    P.step = h->step;
+    if (launch_cache_fill(P, s) != cudaSuccess) return TT_ERR_CUDA;
+    return cudaStreamSynchronize(s) == cudaSuccess ? TT_OK : TT_ERR_CUDA;
+}
+
+tt_status tt_emb_cache_read(tt_emb* h, float* vals_dev, float* grads_dev, tt_stream stream) {
+    if (!h) return TT_ERR_ARG;
+    if (grads_dev && !h->cache_train) return TT_ERR_STATE;
+    if (h->cache_n == 0) return TT_OK;
+    cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+    const size_t bytes = sizeof(float) * (size_t)h->cache_n * h->tabs[0].D;
+    if (vals_dev && cudaMemcpyAsync(vals_dev, h->d_cache_vals, bytes, cudaMemcpyDeviceToDevice, s) != cudaSuccess)
+        return TT_ERR_CUDA;
+    if (grads_dev && cudaMemcpyAsync(grads_dev, h->d_cache_grad, bytes, cudaMemcpyDeviceToDevice, s) != cudaSuccess)
+        return TT_ERR_CUDA;
+    return TT_OK;
+}
+
+tt_status tt_emb_cache_write(tt_emb* h, const float* vals_dev, tt_stream stream) {
+    if (!h || !vals_dev) return TT_ERR_ARG;
+    if (!h->cache_train) return TT_ERR_STATE;
+    if (h->cache_n == 0) return TT_OK;
+    const size_t bytes = sizeof(float) * (size_t)h->cache_n * h->tabs[0].D;
+    return cudaMemcpyAsync(h->d_cache_vals, vals_dev, bytes, cudaMemcpyDeviceToDevice,
+                           reinterpret_cast<cudaStream_t>(stream)) == cudaSuccess ? TT_OK : TT_ERR_CUDA;
 }
 
 tt_status tt_emb_get_decoded(tt_emb* h, int32_t* table_dev, int32_t* i1_dev, int32_t* i2_dev, int32_t* i3_dev,

@@ -418,27 +418,11 @@ __device__ __forceinline__ const float* t_of_pair(const Params& P, const TableDe
     return P.Tbuf + T.tbase + ((int64_t)i2 * T.p1 + i1) * (int64_t)(T.q1 * T.q2 * T.r2);
 }
 
-// Cache slot of `row` (table 0) or -1.
-__device__ __forceinline__ int64_t cache_find(const Params& P, int64_t row) {
-    if (P.cache_sets > 0) {  // set-associative: the kLfuWays ways of the row's set
-        const int64_t base = lfu_set_of(row, P.cache_sets) * kLfuWays;
-        for (int w = 0; w < kLfuWays; ++w)
-            if (P.cache_rows[base + w] == row) return base + w;
-        return -1;
-    }
-    int64_t a = 0, b = P.cache_n;
-    while (a < b) {
-        const int64_t m = (a + b) >> 1;
-        if (P.cache_rows[m] < row) a = m + 1; else b = m;
-    }
-    return (a < P.cache_n && P.cache_rows[a] == row) ? a : -1;
-}
-
 // Cached value state of one lookup: slot (or -1) and whether it is current.
 __device__ __forceinline__ int64_t cache_probe(const Params& P, const TableDev& T, int i1, int i2, int i3,
                                                bool& fresh) {
     fresh = false;
-    if (P.cache_n == 0) return -1;
+    if (P.cache_n == 0 || P.cache_train) return -1;  // trainable rows are added separately
     const int64_t row = ((int64_t)i1 * T.p2 + i2) * T.p3 + i3;
     const int64_t slot = cache_find(P, row);
     if (slot >= 0) {
@@ -463,7 +447,7 @@ __device__ void pool_bag_static(const Params& P, const TableDev& T, int64_t bag,
     float acc[H];
 #pragma unroll
     for (int v = 0; v < H; ++v) acc[v] = 0.f;
-    if (P.cache_n == 0) {
+    if (P.cache_n == 0 || P.cache_train) {
         // warp w takes lookups lo + w + kPoolWarps l; lane l first loads the indices of the
         // warp's l-th lookup of a round (one pass), then the warp walks them kPoolPer at a time
         for (int64_t nb0 = lo; nb0 < hi; nb0 += 32 * kPoolWarps) {
@@ -594,6 +578,16 @@ __device__ void pool_bag_static(const Params& P, const TableDev& T, int64_t bag,
         }
     }
     constexpr int V = H / 16;
+    if (P.cache_train) {  // trainable cache rows: s times the cached value, V columns a lane
+        for (int64_t n = lo + w; n < hi; n += kPoolWarps) {
+            const int slot = P.lk_hit[n];
+            if (slot < 0) continue;
+            const float sh = P.lk_sh[n];
+            const float* cv = P.cache_vals + (int64_t)slot * D + lj * H + lc * V;
+#pragma unroll
+            for (int v = 0; v < V; ++v) acc[v] = fmaf(sh, __ldcg(cv + v), acc[v]);
+        }
+    }
 #pragma unroll
     for (int v = 0; v < V; ++v) red[w * D + lj * H + lc * V + v] = acc[v];
     __syncthreads();
@@ -651,6 +645,17 @@ __device__ void pool_bag_generic(const Params& P, const TableDev& T, int64_t bag
         }
 #pragma unroll
         for (int m = 0; m < kMaxDPerLane; ++m) acc[m] = fmaf(s, v[m], acc[m]);
+        if (P.cache_train) {  // trainable cache rows: s times the cached value
+            const int slot2 = P.lk_hit[n];
+            if (slot2 >= 0) {
+                const float sh = P.lk_sh[n];
+#pragma unroll
+                for (int m = 0; m < kMaxDPerLane; ++m) {
+                    const int j = lane + 32 * m;
+                    if (j < D) acc[m] = fmaf(sh, __ldcg(P.cache_vals + (int64_t)slot2 * D + j), acc[m]);
+                }
+            }
+        }
     }
 #pragma unroll
     for (int m = 0; m < kMaxDPerLane; ++m) {
@@ -797,11 +802,127 @@ cudaError_t launch_full_weight(const TableDev* tables, int t, int64_t row0, int6
     return cudaGetLastError();
 }
 
+// Trainable cache rows, backward (FBTT README, "Parameters": sparse, the gradient
+// w.r.t. the cache).  The gradient of cached value [slot][j] is the sum, over the hits n
+// of the slot, of sh_n * grad_out[bag_n][j].  The sum is taken in 64-bit fixed point with
+// integer atomics, so it does not depend on the order of the hits: each term (exact in
+// double) is rounded to a multiple of 2^-S.  With every |term| < 2^e and at most 2^k
+// terms, S = 61 - e - k keeps every partial sum below 2^62.
+
+// 2^x as a double (x within the normal exponent range).
+__device__ __forceinline__ double pow2d(int x) { return __longlong_as_double((long long)(x + 1023) << 52); }
+
+// S of the step from the largest term, or INT_MIN when that is not finite.
+__device__ __forceinline__ int cache_fixed_shift(const Params& P) {
+    const unsigned gb = P.cache_gmax[0];
+    const int E = (int)((gb >> 23) & 255u);
+    if (E == 255) return INT_MIN;
+    const int e = (E == 0 ? 1 : E) - 126;  // |term| <= largest < 2^e
+    int k = 0;
+    while (((int64_t)1 << k) < P.nnz) ++k;
+    return 61 - e - k;
+}
+
+// Largest |sh * grad_out| over the hits of the step (a non-finite term counts as
+// infinity) into cache_gmax[0], which the previous step's k_cache_apply left at 0;
+// clears the touch flags of the previous step.
+__global__ void __launch_bounds__(256) k_cache_gmax(const __grid_constant__ Params P) {
+    pdl_entry();
+    const int lane = threadIdx.x & 31, D = P.D;
+    const int64_t gt = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
+    for (int64_t i = gt; i < P.cache_n; i += (int64_t)gridDim.x * blockDim.x) P.cache_touch[i] = 0;
+    float m = 0.f;
+    const int64_t warps = (int64_t)gridDim.x * (blockDim.x >> 5);
+    for (int64_t n = gt >> 5; n < P.nnz; n += warps) {
+        if (P.lk_hit[n] < 0) continue;
+        const float sh = P.lk_sh[n];
+        const float* g = P.grad_out + (int64_t)P.lk_bag[n] * D;
+        for (int j = lane; j < D; j += 32) {
+            const float a = fabsf(sh * g[j]);
+            m = fmaxf(m, a <= 3.402823466e38f ? a : __int_as_float(0x7f800000));
+        }
+    }
+#pragma unroll
+    for (int o = 16; o >= 1; o >>= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, o));
+    if (lane == 0 && m > 0.f) atomicMax(P.cache_gmax, __float_as_uint(m));
+}
+
+// Fixed-point sum of the hit terms into cache_acc; marks the touched slots and
+// passes S on in cache_gmax[1].
+__global__ void __launch_bounds__(256) k_cache_acc(const __grid_constant__ Params P) {
+    pdl_entry();
+    const int S = cache_fixed_shift(P);
+    if (blockIdx.x == 0 && threadIdx.x == 0) P.cache_gmax[1] = (unsigned)S;
+    if (S == INT_MIN) return;
+    const double scale = pow2d(S);
+    const int lane = threadIdx.x & 31, D = P.D;
+    const int64_t warps = (int64_t)gridDim.x * (blockDim.x >> 5);
+    for (int64_t n = ((int64_t)blockIdx.x * blockDim.x + threadIdx.x) >> 5; n < P.nnz; n += warps) {
+        const int slot = P.lk_hit[n];
+        if (slot < 0) continue;
+        const double sh = P.lk_sh[n];
+        const float* g = P.grad_out + (int64_t)P.lk_bag[n] * D;
+        unsigned long long* acc = P.cache_acc + (int64_t)slot * D;
+        for (int j = lane; j < D; j += 32)
+            atomicAdd(acc + j, (unsigned long long)__double2ll_rn(sh * (double)g[j] * scale));
+        if (lane == 0) P.cache_touch[slot] = 1;
+    }
+}
+
+// The optimizer step of the touched cached values (SGD, Adagrad, or the gradient kept
+// for reading); the accumulators and cache_gmax[0] return to zero.
+__global__ void __launch_bounds__(256) k_cache_apply(const __grid_constant__ Params P) {
+    pdl_entry();
+    const int S = (int)P.cache_gmax[1];
+    if (blockIdx.x == 0 && threadIdx.x == 0) P.cache_gmax[0] = 0u;
+    const double unscale = S == INT_MIN ? 0.0 : pow2d(-S);
+    const int64_t total = P.cache_n * P.D;
+    for (int64_t e = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; e < total; e += (int64_t)gridDim.x * blockDim.x) {
+        if (!P.cache_touch[e / P.D]) {
+            if (P.opt == TT_OPT_GRAD) P.cache_grad[e] = 0.f;
+            continue;
+        }
+        const float g = S == INT_MIN ? __int_as_float(0x7fffffff) : (float)((double)(long long)P.cache_acc[e] * unscale);
+        P.cache_acc[e] = 0ull;
+        if (P.opt == TT_OPT_SGD) {
+            P.cache_vals[e] = fmaf(-P.lr, g, P.cache_vals[e]);
+        } else if (P.opt == TT_OPT_ADAGRAD) {
+            const float st = fmaf(g, g, P.cache_state[e]);
+            P.cache_state[e] = st;
+            P.cache_vals[e] -= P.lr * g / (sqrtf(st) + P.eps);
+        } else {
+            P.cache_grad[e] = g;
+        }
+    }
+}
+
 cudaError_t launch_cache_fill(const Params& P, cudaStream_t s) {
     const int64_t blocks = (P.cache_n + 7) / 8;
     cudaError_t le = launch_pdl(k_cache_fill, dim3((unsigned)blocks), dim3(256), 0, s, P);
     if (le != cudaSuccess) return le;
     return cudaGetLastError();
+}
+
+static int64_t grid_for(int64_t units, int per_block, int64_t cap) {
+    const int64_t b = (units + per_block - 1) / per_block;
+    return b < 1 ? 1 : (b > cap ? cap : b);
+}
+
+cudaError_t launch_cache_gmax(const Params& P, cudaStream_t s) {
+    const int64_t b = std::max(grid_for(P.nnz, 8, 152 * 8), grid_for(P.cache_n, 256, 152 * 8));
+    cudaError_t le = launch_pdl(k_cache_gmax, dim3((unsigned)b), dim3(256), 0, s, P);
+    return le != cudaSuccess ? le : cudaGetLastError();
+}
+
+cudaError_t launch_cache_acc(const Params& P, cudaStream_t s) {
+    cudaError_t le = launch_pdl(k_cache_acc, dim3((unsigned)grid_for(P.nnz, 8, 152 * 8)), dim3(256), 0, s, P);
+    return le != cudaSuccess ? le : cudaGetLastError();
+}
+
+cudaError_t launch_cache_apply(const Params& P, cudaStream_t s) {
+    const int64_t b = grid_for(P.cache_n * P.D, 256, 152 * 16);
+    cudaError_t le = launch_pdl(k_cache_apply, dim3((unsigned)b), dim3(256), 0, s, P);
+    return le != cudaSuccess ? le : cudaGetLastError();
 }
 
 cudaError_t set_fwd_attributes(int max_smem) {

@@ -155,6 +155,16 @@ struct Params {
     unsigned* freq_counts;          // [freq_mask + 1]
     int freq_mask;
     int cache_sets;
+    // trainable cache rows (FBTT README, "Parameters": sparse, the gradient w.r.t. the
+    // cache): a hit reads the cached value and its gradient goes to that value
+    int cache_train;
+    int* lk_hit;                    // [nnz] cache slot of the lookup, or -1
+    float* lk_sh;                   // [nnz] pooling scale of a hit (its TT scale is 0)
+    unsigned long long* cache_acc;  // [cache_n][D] fixed-point gradient sums
+    float* cache_state;             // [cache_n][D] Adagrad accumulators of the cached values
+    float* cache_grad;              // [cache_n][D] last gradient of the cached values (sparse=False)
+    unsigned* cache_gmax;           // [2]: max |hit term| of the step (float bits), its shift S
+    int* cache_touch;               // [cache_n] 1 once a hit of this step touched the slot
 };
 
 // ---------------------------------------------------------------- helpers
@@ -336,6 +346,23 @@ __device__ __forceinline__ void lfu_count(const Params& P, int64_t row) {
 
 // Lookup n with its index `row` and weight `w` (loaded by the caller, so that the
 // loads can be issued early).
+// Cache slot of `row` (table 0) or -1: set-associative (the kLfuWays ways of the row's
+// set) or a binary search of the sorted rows.
+__device__ __forceinline__ int64_t cache_find(const Params& P, int64_t row) {
+    if (P.cache_sets > 0) {
+        const int64_t base = lfu_set_of(row, P.cache_sets) * kLfuWays;
+        for (int w = 0; w < kLfuWays; ++w)
+            if (P.cache_rows[base + w] == row) return base + w;
+        return -1;
+    }
+    int64_t a = 0, b = P.cache_n;
+    while (a < b) {
+        const int64_t m = (a + b) >> 1;
+        if (P.cache_rows[m] < row) a = m + 1; else b = m;
+    }
+    return (a < P.cache_n && P.cache_rows[a] == row) ? a : -1;
+}
+
 __device__ __forceinline__ void decode_lookup(const Params& P, int64_t n, int bag, int64_t row, float w, int& t,
                                               int& i1, int& i2, int& i3, int epoch) {
     t = table_of_bag(P, bag);
@@ -351,6 +378,14 @@ __device__ __forceinline__ void decode_lookup(const Params& P, int64_t n, int ba
     if (P.mean) {
         const int64_t L = P.off[bag + 1] - P.off[bag];
         s = s / (float)(L > 0 ? L : 1);
+    }
+    if (P.cache_train) {  // a hit leaves the TT path (scale 0 there) for its cached value
+        const int64_t slot = cache_find(P, row);
+        P.lk_hit[n] = (int)slot;
+        if (slot >= 0) {
+            P.lk_sh[n] = s;
+            s = 0.0f;
+        }
     }
     if (T.idx32) {
         const unsigned r = (unsigned)row, p3 = (unsigned)T.p3, q = r / p3;
@@ -516,6 +551,9 @@ cudaError_t launch_pool(const Params& P, cudaStream_t s);
 cudaError_t launch_tile_bwd(const Params& P, cudaStream_t s);
 cudaError_t launch_reduce13(const Params& P, cudaStream_t s);
 cudaError_t launch_cache_fill(const Params& P, cudaStream_t s);
+cudaError_t launch_cache_gmax(const Params& P, cudaStream_t s);
+cudaError_t launch_cache_acc(const Params& P, cudaStream_t s);
+cudaError_t launch_cache_apply(const Params& P, cudaStream_t s);
 cudaError_t launch_full_weight(const TableDev* tables, int t, int64_t row0, int64_t nrows, float* out, cudaStream_t s);
 
 size_t tile_bwd_smem(const Params& P);
