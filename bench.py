@@ -16,6 +16,11 @@ samples of the same workload.
 Launch: ``python bench.py --gpus 1 --steps K --warmup W``; for N > 1 under
 ``torch.distributed.run`` every rank runs an independent replica on its own
 GPU (weak scaling, no collective on the data path); rank 0 prints.
+
+``--config N`` times another of the seeded workloads instead (1 tiny, 3 Zipf
+weighted-mean with its 110,000 hot rows, 4 40M x 128 rank-64, 5 26 tables);
+``--cache coherent|trainable`` adds the hot-row cache (single-table workloads
+with hot rows: config 3) in its exact-copy or trainable-row mode.
 """
 import argparse
 import json
@@ -62,6 +67,17 @@ def flops_per_lookup(spec):
     A = q1 * r1 * q2 * r2
     Bc = q1 * q2 * r2 * q3
     return A, Bc
+
+
+def lookup_flops(wl):
+    """(sum over lookups of A, sum over lookups of Bc): per-table figures times the table's lookups."""
+    sa = sb = 0
+    for t, spec in enumerate(wl.tables):
+        n = int(wl.offsets[(t + 1) * wl.batch] - wl.offsets[t * wl.batch])
+        A, Bc = flops_per_lookup(spec)
+        sa += A * n
+        sb += Bc * n
+    return sa, sb
 
 
 def max_over_ranks(values, device=None):
@@ -151,17 +167,24 @@ def oracle_step(sub):
     import oracle
 
     oracle.workload_forward(sub)
-    for k in range(3):
-        oracle.workload_sgd_slices(sub, 0, k)
+    for t in range(sub.num_tables):
+        for k in range(3):
+            oracle.workload_sgd_slices(sub, t, k)
 
 
-def cpu_baseline(wl, nbags=None):
-    """One oracle fwd + bwd + SGD step on the first `nbags` bags, timed on the host."""
+def cpu_baseline(wl, nbags=None, budget_s=10.0):
+    """One oracle fwd + bwd + SGD step on the first `nbags` bags (default: as many as fit
+    about `budget_s` seconds, at most all), timed on the host."""
     import oracle
 
-    nbags = nbags or wl.num_bags
-    sub = sub_workload(wl, nbags)
     oracle.build()
+    if nbags is None:
+        probe = sub_workload(wl, min(8, wl.num_bags))
+        t0 = time.perf_counter()
+        oracle_step(probe)
+        per_bag = (time.perf_counter() - t0) / probe.num_bags
+        nbags = int(max(1, min(wl.num_bags, budget_s / max(per_bag, 1e-9))))
+    sub = sub_workload(wl, nbags)
     t0 = time.perf_counter()
     oracle_step(sub)
     dt = time.perf_counter() - t0
@@ -228,6 +251,19 @@ def run_reference(args):
 # ---------------------------------------------------------------- GPU arm
 
 
+def workload_name(args):
+    import tt_inputs
+
+    name = WORKLOAD if args.config == 2 else "TT-EmbeddingBag " + tt_inputs.CONFIG_NAMES[args.config]
+    opt = {"sgd": "fused SGD", "adagrad": "fused Adagrad", "grad": "sparse=False gradients"}[args.optimizer]
+    name = name.replace("fused SGD", opt) if args.config == 2 else f"{name}, {opt}"
+    if args.cache != "none":
+        name += f", {args.cache} hot-row cache"
+    elif args.config == 3:
+        name = name.replace(", hot-row cache", ", no cache")
+    return name
+
+
 def run_gpu(args):
     import torch
     import torch.distributed as dist
@@ -243,11 +279,15 @@ def run_gpu(args):
     tt.build()
     tt.load_library()
 
-    wl = tt_inputs.config(2)
+    wl = tt_inputs.config(args.config)
     spec = wl.tables[0]
     D, nnz, B = spec.embedding_dim, wl.nnz, wl.num_bags
-    cores = [torch.from_numpy(c).to(dev) for c in wl.cores[0]]
-    h = tt.tt_emb_create(spec.num_embeddings, spec.p, spec.q, spec.ranks, cores)
+    cores = [torch.from_numpy(c).to(dev) for t in wl.cores for c in t]
+    if wl.num_tables == 1:
+        h = tt.tt_emb_create(spec.num_embeddings, spec.p, spec.q, spec.ranks, cores)
+    else:
+        h = tt.tt_emb_batch_create([(s.num_embeddings, s.p, s.q, s.ranks, cores[3 * t:3 * t + 3])
+                                    for t, s in enumerate(wl.tables)])
     aux = None
     if args.optimizer == "adagrad":  # fused element-wise Adagrad, accumulators starting at 0
         aux = [torch.zeros_like(c) for c in cores]
@@ -255,17 +295,25 @@ def run_gpu(args):
     elif args.optimizer == "grad":  # sparse=False: the gradients are written out, the cores stay
         aux = [torch.zeros_like(c) for c in cores]
         tt.tt_emb_set_optimizer(h, tt.TT_OPT_GRAD, 0.0, aux)
+    if args.cache != "none":
+        if wl.num_tables != 1 or wl.cache_rows is None:
+            raise SystemExit("--cache needs a single-table workload with hot rows (--config 3)")
+        if args.cache == "trainable":
+            tt.tt_emb_cache_set_trainable(h, True)
+        tt.tt_emb_cache_populate(h, torch.from_numpy(wl.cache_rows).to(dev))
     tt.tt_emb_reserve(h, nnz, B)
     idx = torch.from_numpy(wl.indices).to(dev)
     off = torch.from_numpy(wl.offsets).to(dev)
     go = torch.from_numpy(wl.grad_out).to(dev)
+    wts = None if wl.weights is None else torch.from_numpy(wl.weights).to(dev)
+    mode = tt.TT_POOL_MEAN if wl.mode == "mean" else tt.TT_POOL_SUM
     out = torch.empty((B, D), dtype=torch.float32, device=dev)
     flush = torch.empty(L2_FLUSH_BYTES // 4, dtype=torch.float32, device=dev)
     stream = torch.cuda.current_stream(dev)
     lr = wl.lr
 
     def step():
-        tt.tt_emb_forward(h, idx, off, None, tt.TT_POOL_SUM, out, stream)
+        tt.tt_emb_forward(h, idx, off, wts, mode, out, stream)
         tt.tt_emb_backward(h, go, lr, stream)
 
     def barrier():
@@ -301,7 +349,7 @@ def run_gpu(args):
         g = torch.cuda.CUDAGraph()
         with torch.cuda.graph(g):
             cs = torch.cuda.current_stream(dev)
-            tt.tt_emb_forward(h, idx, off, None, tt.TT_POOL_SUM, out, cs)
+            tt.tt_emb_forward(h, idx, off, wts, mode, out, cs)
             tt.tt_emb_backward(h, go, lr, cs)
         tt.tt_emb_set_stage_timing(h, False)
         return g
@@ -331,7 +379,7 @@ def run_gpu(args):
     torch.cuda.synchronize(dev)
 
     # forward alone
-    ms_fwd = timed(lambda: tt.tt_emb_forward(h, idx, off, None, tt.TT_POOL_SUM, out, stream), args.steps)
+    ms_fwd = timed(lambda: tt.tt_emb_forward(h, idx, off, wts, mode, out, stream), args.steps)
 
     # per-kernel durations: a graph of the same step with an event after every kernel
     gstage = capture(True)
@@ -351,14 +399,17 @@ def run_gpu(args):
     idx_h = torch.from_numpy(wl.indices).pin_memory()
     off_h = torch.from_numpy(wl.offsets).pin_memory()
     go_h = torch.from_numpy(wl.grad_out).pin_memory()
+    w_h = None if wts is None else torch.from_numpy(wl.weights).pin_memory()
     out_h = torch.empty((B, D), dtype=torch.float32).pin_memory()
-    h2d = idx_h.numel() * 8 + off_h.numel() * 8 + go_h.numel() * 4
+    h2d = idx_h.numel() * 8 + off_h.numel() * 8 + go_h.numel() * 4 + (0 if w_h is None else w_h.numel() * 4)
     d2h = out_h.numel() * 4
 
     def e2e_step():
         idx.copy_(idx_h, non_blocking=True)
         off.copy_(off_h, non_blocking=True)
         go.copy_(go_h, non_blocking=True)
+        if w_h is not None:
+            wts.copy_(w_h, non_blocking=True)
         step()
         out_h.copy_(out, non_blocking=True)
 
@@ -368,14 +419,14 @@ def run_gpu(args):
     result = None
     if rank == 0:
         pk, pk_kind = peaks()
-        A, Bc = flops_per_lookup(spec)
+        sA, sB = lookup_flops(wl)
         total_lookups = nnz * args.steps * ws
         value = total_lookups / (ms_total / 1e3)
-        # dominant kernel and its algorithmic FLOPs per launch (per-lookup figures x nnz)
+        # dominant kernel and its algorithmic FLOPs per launch (per-lookup figures x lookups)
         kernel_flops = {
-            "tile_fwd": 2 * A * nnz,            # T = G1 G2, per lookup 2 q1 r1 q2 r2
-            "pool": 2 * Bc * nnz,               # row = T G3, per lookup 2 q1 q2 r2 q3
-            "tile_bwd": 4 * (A + Bc) * nnz,     # dT, dG3, dG1, dG2, per lookup 4 (A + Bc)
+            "fwd_T": 2 * sA,                    # T = G1 G2, per lookup 2 q1 r1 q2 r2
+            "pool": 2 * sB,                     # row = T G3, per lookup 2 q1 q2 r2 q3
+            "tile_bwd": 4 * (sA + sB),          # dT, dG3, dG1, dG2, per lookup 4 (A + Bc)
         }
         dom = max(kavg, key=kavg.get)
         sm_mhz = SM_MAX_MHZ
@@ -388,7 +439,7 @@ def run_gpu(args):
         else:
             roof = {"bound": "hbm", "achieved": None, "peak": pk["hbm_gbs"], "unit": "GB/s", "frac": None,
                     "traffic": None, "kernel": dom, "avg_ms": kavg[dom]}
-        step_flops = 6 * (A + Bc) * nnz
+        step_flops = 6 * (sA + sB)
         step_tf = step_flops / (ms_total / args.steps * 1e-3) / 1e12
         result = {
             "metric": METRIC,
@@ -401,13 +452,13 @@ def run_gpu(args):
             "ns_per_nnz": 1e6 * ms_total / (nnz * args.steps),
             "higher_is_better": True,
             "scaling": "weak",
-            "vs_baseline": value / (1e9 / PAGES_NS_PER_NNZ),
-            "vs_baseline_note": "value / (1e9 / 416 ns), the FBTT README sample line for this workload (GPU not stated)",
+            "vs_baseline": value / (1e9 / PAGES_NS_PER_NNZ) if args.config == 2 else None,
+            "vs_baseline_note": ("value / (1e9 / 416 ns), the FBTT README sample line for this workload (GPU not stated)"
+                                 if args.config == 2 else "the pages give no figure for this workload"),
             "dtype": "f32",
             "data": "synthetic",
             "config": {
-                "workload": WORKLOAD if args.optimizer == "sgd" else WORKLOAD.replace(
-                    "fused SGD", {"adagrad": "fused Adagrad", "grad": "sparse=False gradients"}[args.optimizer]),
+                "workload": workload_name(args),
                 "nnz": nnz,
                 "bags": B,
                 "p": spec.p, "q": spec.q, "ranks": spec.ranks,
@@ -415,6 +466,8 @@ def run_gpu(args):
                 "optimizer": {"sgd": "fused SGD", "adagrad": "fused element-wise Adagrad",
                               "grad": "sparse=False (gradients written out)"}[args.optimizer],
                 "replicas": ws,
+                "cache": {"none": "none", "coherent": "110,000 hot rows, exact copies",
+                          "trainable": "110,000 hot rows, trainable"}[args.cache],
             },
             "timing": "CUDA graph of forward + backward replayed per step" if not args.eager else "eager launches",
             "eager": {"ms_per_step": ms_eager / args.steps, "host_enqueue_us_per_step": host_us},
@@ -431,8 +484,13 @@ def run_gpu(args):
                     "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h},
         }
     tt.tt_emb_destroy(h)
-    if rank == 0 and not args.no_cpu_baseline:
+    if rank == 0 and not args.no_cpu_baseline and wl.num_tables > 1:
+        result["cpu_baseline"] = {"value": None, "unit": "lookups/s", "kind": "oracle",
+                                  "sample": "not sampled: the bag sampler takes single-table workloads"}
+    elif rank == 0 and not args.no_cpu_baseline:
         result["cpu_baseline"] = cpu_baseline(wl)
+        if args.cache != "none":
+            result["cpu_baseline"]["sample"] += " (the oracle without the cache)"
     if rank == 0:
         print(json.dumps(result), flush=True)
     if ws > 1:
@@ -451,6 +509,10 @@ def main():
     ap.add_argument("--eager", action="store_true", help="time eager launches instead of a CUDA graph replay")
     ap.add_argument("--optimizer", choices=["sgd", "adagrad", "grad"], default="sgd",
                     help="what the backward does with the core gradients (default: fused SGD)")
+    ap.add_argument("--config", type=int, choices=[1, 2, 3, 4, 5], default=2,
+                    help="seeded workload (default 2: the FBTT README sample configuration)")
+    ap.add_argument("--cache", choices=["none", "coherent", "trainable"], default="none",
+                    help="hot-row cache mode (config 3's hot rows)")
     args = ap.parse_args()
     if args.impl == "reference":
         return run_reference(args)

@@ -83,7 +83,6 @@ struct tt_emb {
     int64_t freq_size = 0;
     int64_t lfu_slots = 0;  // cache rows (a multiple of kLfuWays)
     int64_t cache_n = 0;
-    int step = 0;
 };
 
 namespace {
@@ -338,6 +337,7 @@ tt_status build_handle(tt_emb* h, int ntab, const tt_table_desc* d) {
     P.counters = h->d_fixed + 1;
     P.ntiles = h->d_fixed + 3;
     P.epoch = h->d_fixed + 4;
+    P.dstep = h->d_fixed + 5;
     P.grp_done = h->d_fixed + 8;
     P.Tbuf = h->d_tbuf;
     P.tflag = h->d_tflag;
@@ -515,7 +515,6 @@ tt_status tt_emb_forward(tt_emb* h, const int64_t* indices, int64_t nnz, const i
     P.cache_vals = h->d_cache_vals;
     P.cache_stamp = h->d_cache_stamp;
     P.slice_stamp = h->d_slice_stamp;
-    P.step = h->step;
     P.cache_train = (h->cache_train && h->cache_n > 0) ? 1 : 0;
     P.cache_acc = h->d_cache_acc;
     P.cache_state = h->d_cache_state;
@@ -561,7 +560,6 @@ tt_status tt_emb_backward(tt_emb* h, const float* grad_out, float lr, tt_stream 
     h->last_stream = s;
     P.grad_out = grad_out;
     P.lr = lr;
-    P.step = h->step;
     P.slice_stamp = h->d_slice_stamp;
     Seq q(h, 1, s);
     if (P.opt == TT_OPT_GRAD) {  // untouched slices have a zero gradient
@@ -585,7 +583,6 @@ tt_status tt_emb_backward(tt_emb* h, const float* grad_out, float lr, tt_stream 
             return TT_ERR_CUDA;
     }
     tt_status st = q.finish();
-    if (h->cache_n > 0) ++h->step;
     return st;
 }
 
@@ -690,7 +687,6 @@ static tt_status cache_install(tt_emb* h, const std::vector<int64_t>& rows, int 
     P.cache_n = n;
     P.cache_vals = h->d_cache_vals;
     P.cache_stamp = h->d_cache_stamp;
-    P.step = h->step;
     if (launch_cache_fill(P, s) != cudaSuccess) return TT_ERR_CUDA;
     // the host vector must outlive the copy
     if (cudaStreamSynchronize(s) != cudaSuccess) return TT_ERR_CUDA;
@@ -864,7 +860,6 @@ tt_status tt_emb_cache_set_trainable(tt_emb* h, int32_t trainable, tt_stream str
     P.cache_n = h->cache_n;
     P.cache_vals = h->d_cache_vals;
     P.cache_stamp = h->d_cache_stamp;
-    P.step = h->step;
     if (launch_cache_fill(P, s) != cudaSuccess) return TT_ERR_CUDA;
     return cudaStreamSynchronize(s) == cudaSuccess ? TT_OK : TT_ERR_CUDA;
 }

@@ -202,7 +202,7 @@ __device__ void reduce_slice(const Params& P, int bglob, int* slots, int* sh, fl
         core_update(P, G, A, e, sum);
     }
     if (P.slice_stamp && P.opt != TT_OPT_GRAD && threadIdx.x == 0 && t == 0)
-        P.slice_stamp[first_core ? slice : T.p1 + T.p2 + slice] = P.step + 1;
+        P.slice_stamp[first_core ? slice : T.p1 + T.p2 + slice] = *P.dstep + 1;
     __syncthreads();
 }
 
@@ -670,7 +670,7 @@ __device__ void tile_bwd_body(const Params& P, const TableDev& T, const Dm dm, u
                 }
             }
         }
-        if (nt == 1 && P.slice_stamp && P.opt != TT_OPT_GRAD && threadIdx.x == 0 && t == 0) P.slice_stamp[T.p1 + i2] = P.step + 1;
+        if (nt == 1 && P.slice_stamp && P.opt != TT_OPT_GRAD && threadIdx.x == 0 && t == 0) P.slice_stamp[T.p1 + i2] = *P.dstep + 1;
     } else {
         // generic dimensions
         float acc2[kMaxAcc2];
@@ -733,7 +733,7 @@ __device__ void tile_bwd_body(const Params& P, const TableDev& T, const Dm dm, u
                 else part[e] = acc2[m];
             }
         }
-        if (nt == 1 && P.slice_stamp && P.opt != TT_OPT_GRAD && threadIdx.x == 0 && t == 0) P.slice_stamp[T.p1 + i2] = P.step + 1;
+        if (nt == 1 && P.slice_stamp && P.opt != TT_OPT_GRAD && threadIdx.x == 0 && t == 0) P.slice_stamp[T.p1 + i2] = *P.dstep + 1;
     }
 
     // every partial of this block is written: publish them before any arrival count
@@ -758,7 +758,7 @@ __device__ void tile_bwd_body(const Params& P, const TableDev& T, const Dm dm, u
             }
             if (threadIdx.x == 0) {
                 P.grp_done[g * SPLIT + sp] = 0;
-                if (P.slice_stamp && P.opt != TT_OPT_GRAD && t == 0) P.slice_stamp[T.p1 + i2] = P.step + 1;
+                if (P.slice_stamp && P.opt != TT_OPT_GRAD && t == 0) P.slice_stamp[T.p1 + i2] = *P.dstep + 1;
             }
         }
     }

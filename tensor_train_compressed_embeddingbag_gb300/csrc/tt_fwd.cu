@@ -562,7 +562,7 @@ __device__ void pool_bag_static(const Params& P, const TableDev& T, int64_t bag,
                     }
                 __threadfence();
                 __syncwarp();
-                if (lane == 0) atomicExch(P.cache_stamp + slot, P.step);
+                if (lane == 0) atomicExch(P.cache_stamp + slot, *P.dstep);
             }
         }
     }
@@ -640,7 +640,7 @@ __device__ void pool_bag_generic(const Params& P, const TableDev& T, int64_t bag
                 }
                 __threadfence();
                 __syncwarp();
-                if (lane == 0) atomicExch(P.cache_stamp + slot, P.step);
+                if (lane == 0) atomicExch(P.cache_stamp + slot, *P.dstep);
             }
         }
 #pragma unroll
@@ -722,7 +722,7 @@ __global__ void k_cache_fill(const __grid_constant__ Params P) {
         }
         P.cache_vals[slot * D + j] = acc;
     }
-    if (lane == 0) P.cache_stamp[slot] = P.step;
+    if (lane == 0) P.cache_stamp[slot] = *P.dstep;
 }
 
 // ------------------------------------------------------------------ launchers

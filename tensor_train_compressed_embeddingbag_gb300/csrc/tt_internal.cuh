@@ -145,9 +145,9 @@ struct Params {
     const int64_t* cache_rows;      // sorted row ids, or null
     int64_t cache_n;
     float* cache_vals;              // [cache_n][D]
-    int* cache_stamp;               // [cache_n] step at which the row was computed
-    int* slice_stamp;               // [p1 + p2 + p3] step at which each slice last changed
-    int step;
+    int* cache_stamp;               // [cache_n] *dstep when the row was computed
+    int* slice_stamp;               // [p1 + p2 + p3] *dstep + 1 of the backward that last changed the slice
+    int* dstep;                     // device counter: advanced by the decode kernel of every forward pass
     // FBTT README, "Software Cache": access-frequency table (open addressing, linear
     // probing) updated by every forward pass, and the set-associative layout of the
     // cache (cache_sets > 0: slot = set * kLfuWays + way; 0: cache_rows sorted)

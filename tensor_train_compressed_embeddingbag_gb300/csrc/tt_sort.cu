@@ -21,6 +21,7 @@ namespace ttemb {
 
 __global__ void __launch_bounds__(kSortThreads, 1) k_decode_hist(const __grid_constant__ Params P) {
     pdl_entry();
+    if (blockIdx.x == 0 && threadIdx.x == 0) atomicAdd(P.dstep, 1);  // the pass's cache stamp
     extern __shared__ int sm[];
     int* h1 = sm;           // [n1]
     int* h3 = sm + P.n1;    // [n3]
@@ -263,6 +264,7 @@ __device__ __forceinline__ int64_t staged_bag(const int64_t* soff, int64_t b0, i
 
 __global__ void __launch_bounds__(kSmallChunk) k_decode_small(const __grid_constant__ Params P) {
     pdl_entry();
+    if (blockIdx.x == 0 && threadIdx.x == 0) atomicAdd(P.dstep, 1);  // the pass's cache stamp
     __shared__ int64_t soff[kDecodeOffs];
     __shared__ int64_t sb[2];
     __shared__ int cnt[kSmallChunk / 32][kSmallMaxBins];
