@@ -184,7 +184,7 @@ tt_status tt_emb_full_weight(tt_emb* h, int32_t table, int64_t row0, int64_t nro
 
 /*
  * Hot-row cache (FBTT README, "Software Cache"): decompress the n rows of
- * table 0 listed in rows_dev (int64, distinct, within [0, E)) into a
+ * table 0 listed in rows_dev (n <= 2^29 int64 rows, distinct, within [0, E)) into a
  * device-resident fp32 cache.  Later forward passes read a cached row instead
  * of contracting it, as long as its three core slices have not changed since
  * it was filled; a backward pass marks the rows whose slices it updated as
@@ -250,8 +250,8 @@ tt_status tt_emb_lfu_disable(tt_emb* h);
  *   that slot of (the lookup's pooling scale: weight, divided by the bag
  *   length in mean mode) x grad_out[bag][j].  The sum is taken in 64-bit fixed
  *   point with integer atomics, so it does not depend on the order of the
- *   hits (each term is rounded to a step of 2^-S with |sum| < 2^62, S set by
- *   the step's largest term and lookup count).  The optimizer of
+ *   hits (each term, the fp32 product, is rounded to a step of 2^-S with
+ *   |sum| < 2^62, S set by the step's largest term and lookup count).  The optimizer of
  *   tt_emb_set_optimizer then updates the cached values that some hit touched
  *   (SGD; Adagrad with its own state per cached value, zero at populate; or
  *   TT_OPT_GRAD, which keeps the gradient for tt_emb_cache_read and gives

@@ -77,6 +77,10 @@ struct tt_emb {
     float* d_cache_grad = nullptr;
     unsigned* d_cache_gmax = nullptr;
     int* d_cache_touch = nullptr;
+    int* d_cache_list = nullptr;
+    // explicit rows (tt_emb_cache_populate): open-addressing index row -> slot
+    longlong2* d_cache_hidx = nullptr;
+    int* d_cache_claim = nullptr;
     // LFU policy (tt_emb_lfu_enable)
     unsigned long long* d_freq_keys = nullptr;
     unsigned* d_freq_counts = nullptr;
@@ -361,6 +365,9 @@ void free_handle(tt_emb* h) {
     cudaFree(h->d_cache_grad);
     cudaFree(h->d_cache_gmax);
     cudaFree(h->d_cache_touch);
+    cudaFree(h->d_cache_list);
+    cudaFree(h->d_cache_hidx);
+    cudaFree(h->d_cache_claim);
     cudaFree(h->d_freq_keys);
     cudaFree(h->d_freq_counts);
     for (int w = 0; w < 2; ++w)
@@ -513,6 +520,8 @@ tt_status tt_emb_forward(tt_emb* h, const int64_t* indices, int64_t nnz, const i
     P.cache_rows = h->d_cache_rows;
     P.cache_n = h->cache_n;
     P.cache_vals = h->d_cache_vals;
+    P.cache_hidx = h->d_cache_hidx;
+    P.cache_claim = h->d_cache_claim;
     P.cache_stamp = h->d_cache_stamp;
     P.slice_stamp = h->d_slice_stamp;
     P.cache_train = (h->cache_train && h->cache_n > 0) ? 1 : 0;
@@ -521,6 +530,7 @@ tt_status tt_emb_forward(tt_emb* h, const int64_t* indices, int64_t nnz, const i
     P.cache_grad = h->d_cache_grad;
     P.cache_gmax = h->d_cache_gmax;
     P.cache_touch = h->d_cache_touch;
+    P.cache_list = h->d_cache_list;
     h->last_stream = s;
     h->has_fwd = false;
     if (num_bags == 0) {
@@ -570,6 +580,9 @@ tt_status tt_emb_backward(tt_emb* h, const float* grad_out, float lr, tt_stream 
                 if (cudaMemsetAsync(T.aux[k], 0, sizeof(float) * n[k], s) != cudaSuccess) return TT_ERR_CUDA;
         }
     }
+    if (P.cache_train && P.opt == TT_OPT_GRAD &&
+        cudaMemsetAsync(h->d_cache_grad, 0, sizeof(float) * (size_t)h->cache_n * P.D, s) != cudaSuccess)
+        return TT_ERR_CUDA;
     if (P.nnz > 0) {
         q.run("tile_bwd", launch_tile_bwd);
         q.run("reduce13", launch_reduce13);
@@ -578,9 +591,6 @@ tt_status tt_emb_backward(tt_emb* h, const float* grad_out, float lr, tt_stream 
             q.run("cache_acc", launch_cache_acc);
             q.run("cache_apply", launch_cache_apply);
         }
-    } else if (P.cache_train && P.opt == TT_OPT_GRAD) {
-        if (cudaMemsetAsync(h->d_cache_grad, 0, sizeof(float) * (size_t)h->cache_n * P.D, s) != cudaSuccess)
-            return TT_ERR_CUDA;
     }
     tt_status st = q.finish();
     return st;
@@ -627,6 +637,8 @@ static void cache_train_free(tt_emb* h) {
     cudaFree(h->d_cache_grad);
     cudaFree(h->d_cache_gmax);
     cudaFree(h->d_cache_touch);
+    cudaFree(h->d_cache_list);
+    h->d_cache_list = nullptr;
     h->d_cache_acc = nullptr;
     h->d_cache_state = nullptr;
     h->d_cache_grad = nullptr;
@@ -641,8 +653,9 @@ static tt_status cache_train_alloc(tt_emb* h, cudaStream_t s) {
     if (cudaMalloc(&h->d_cache_acc, sizeof(unsigned long long) * nd) != cudaSuccess ||
         cudaMalloc(&h->d_cache_state, sizeof(float) * nd) != cudaSuccess ||
         cudaMalloc(&h->d_cache_grad, sizeof(float) * nd) != cudaSuccess ||
-        cudaMalloc(&h->d_cache_gmax, sizeof(unsigned) * 2) != cudaSuccess ||
-        cudaMalloc(&h->d_cache_touch, sizeof(int) * (size_t)h->cache_n) != cudaSuccess) {
+        cudaMalloc(&h->d_cache_gmax, sizeof(unsigned) * 4) != cudaSuccess ||
+        cudaMalloc(&h->d_cache_touch, sizeof(int) * (size_t)h->cache_n) != cudaSuccess ||
+        cudaMalloc(&h->d_cache_list, sizeof(int) * (size_t)h->cache_n) != cudaSuccess) {
         cudaGetLastError();
         cache_train_free(h);
         return TT_ERR_NOMEM;
@@ -650,7 +663,7 @@ static tt_status cache_train_alloc(tt_emb* h, cudaStream_t s) {
     if (cudaMemsetAsync(h->d_cache_acc, 0, sizeof(unsigned long long) * nd, s) != cudaSuccess ||
         cudaMemsetAsync(h->d_cache_state, 0, sizeof(float) * nd, s) != cudaSuccess ||
         cudaMemsetAsync(h->d_cache_grad, 0, sizeof(float) * nd, s) != cudaSuccess ||
-        cudaMemsetAsync(h->d_cache_gmax, 0, sizeof(unsigned) * 2, s) != cudaSuccess ||
+        cudaMemsetAsync(h->d_cache_gmax, 0, sizeof(unsigned) * 4, s) != cudaSuccess ||
         cudaMemsetAsync(h->d_cache_touch, 0, sizeof(int) * (size_t)h->cache_n, s) != cudaSuccess)
         return TT_ERR_CUDA;
     return TT_OK;
@@ -665,6 +678,7 @@ static tt_status cache_install(tt_emb* h, const std::vector<int64_t>& rows, int 
     if (cudaMalloc(&h->d_cache_rows, sizeof(int64_t) * n) != cudaSuccess ||
         cudaMalloc(&h->d_cache_vals, sizeof(float) * (size_t)n * T.D) != cudaSuccess ||
         cudaMalloc(&h->d_cache_stamp, sizeof(int) * n) != cudaSuccess ||
+        cudaMalloc(&h->d_cache_claim, sizeof(int) * n) != cudaSuccess ||
         cudaMalloc(&h->d_slice_stamp, sizeof(int) * nslice) != cudaSuccess) {
         cudaGetLastError();
         tt_emb_cache_disable(h);
@@ -679,9 +693,37 @@ static tt_status cache_install(tt_emb* h, const std::vector<int64_t>& rows, int 
         }
     }
     if (cudaMemcpyAsync(h->d_cache_rows, rows.data(), sizeof(int64_t) * n, cudaMemcpyHostToDevice, s) != cudaSuccess ||
-        cudaMemsetAsync(h->d_slice_stamp, 0, sizeof(int) * nslice, s) != cudaSuccess)
+        cudaMemsetAsync(h->d_slice_stamp, 0, sizeof(int) * nslice, s) != cudaSuccess ||
+        cudaMemsetAsync(h->d_cache_claim, 0, sizeof(int) * n, s) != cudaSuccess)  // epochs start at 1
         return TT_ERR_CUDA;
     h->P.cache_sets = sets;
+    if (sets == 0) {
+        // explicit rows: open-addressing index (load <= 1/2, linear probing from mix64(row))
+        int64_t M = 32;
+        while (M < 2 * n) M <<= 1;
+        std::vector<longlong2> hx((size_t)M, longlong2{-1, 0});
+        int maxp = 1;
+        for (int64_t i = 0; i < n; ++i) {
+            uint64_t e = mix64((uint64_t)rows[i]) & (uint64_t)(M - 1);
+            int p = 1;
+            while (hx[e].x >= 0) {
+                e = (e + 1) & (uint64_t)(M - 1);
+                ++p;
+            }
+            hx[e] = longlong2{(long long)rows[i], (long long)i};
+            maxp = std::max(maxp, p);
+        }
+        if (cudaMalloc(&h->d_cache_hidx, sizeof(longlong2) * M) != cudaSuccess) {
+            cudaGetLastError();
+            tt_emb_cache_disable(h);
+            return TT_ERR_NOMEM;
+        }
+        if (cudaMemcpyAsync(h->d_cache_hidx, hx.data(), sizeof(longlong2) * M, cudaMemcpyHostToDevice, s) != cudaSuccess ||
+            cudaStreamSynchronize(s) != cudaSuccess)
+            return TT_ERR_CUDA;
+        h->P.cache_hmask = (int)(M - 1);
+        h->P.cache_hprobe = maxp;
+    }
     Params P = h->P;
     P.cache_rows = h->d_cache_rows;
     P.cache_n = n;
@@ -794,7 +836,7 @@ tt_status tt_emb_lfu_cached_rows(tt_emb* h, int64_t* rows_host, int64_t cap, int
 }
 
 tt_status tt_emb_cache_populate(tt_emb* h, const int64_t* rows_dev, int64_t n, tt_stream stream) {
-    if (!h || n < 0 || (n > 0 && !rows_dev)) return TT_ERR_ARG;
+    if (!h || n < 0 || (n > 0 && !rows_dev) || n > ((int64_t)1 << 29)) return TT_ERR_ARG;
     if (h->ntab != 1) return TT_ERR_STATE;
     cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
     tt_emb_cache_disable(h);
@@ -823,6 +865,12 @@ tt_status tt_emb_cache_disable(tt_emb* h) {
     cudaFree(h->d_cache_vals);
     cudaFree(h->d_cache_stamp);
     cudaFree(h->d_slice_stamp);
+    cudaFree(h->d_cache_hidx);
+    cudaFree(h->d_cache_claim);
+    h->d_cache_hidx = nullptr;
+    h->d_cache_claim = nullptr;
+    h->P.cache_hmask = 0;
+    h->P.cache_hprobe = 0;
     h->d_cache_rows = nullptr;
     h->d_cache_vals = nullptr;
     h->d_cache_stamp = nullptr;

@@ -418,19 +418,26 @@ __device__ __forceinline__ const float* t_of_pair(const Params& P, const TableDe
     return P.Tbuf + T.tbase + ((int64_t)i2 * T.p1 + i1) * (int64_t)(T.q1 * T.q2 * T.r2);
 }
 
-// Cached value state of one lookup: slot (or -1) and whether it is current.
-__device__ __forceinline__ int64_t cache_probe(const Params& P, const TableDev& T, int i1, int i2, int i3,
-                                               bool& fresh) {
-    fresh = false;
-    if (P.cache_n == 0 || P.cache_train) return -1;  // trainable rows are added separately
-    const int64_t row = ((int64_t)i1 * T.p2 + i2) * T.p3 + i3;
-    const int64_t slot = cache_find(P, row);
-    if (slot >= 0) {
-        const int need = max(max(P.slice_stamp[i1], P.slice_stamp[T.p1 + i2]), P.slice_stamp[T.p1 + T.p2 + i3]);
-        fresh = *(volatile const int*)(P.cache_stamp + slot) >= need;
-        __threadfence();  // a refreshed stamp is seen only after its values
+// Exact-copy cache: the lookups that the decode chose to refresh a stale cached row
+// (one per row and pass, lk_hit = -2 - slot) recompute the row from T and G3 and
+// write it back with the pass's stamp.  A warp per lookup, lanes over columns.
+__device__ void cache_refresh_rows(const Params& P, const TableDev& T, int64_t lo, int64_t hi) {
+    const int lane = threadIdx.x & 31, w = threadIdx.x >> 5;
+    const int q3 = T.q3, r2 = T.r2, D = T.D;
+    for (int64_t n = lo + w; n < hi; n += kPoolWarps) {
+        const int code = P.lk_hit[n];
+        if (code > -2) continue;
+        const int64_t slot = -2 - (int64_t)code;
+        const float* Tp = t_of_pair(P, T, P.lk_i2[n], P.lk_i1[n]);
+        const float* g3 = T.G3 + (int64_t)P.lk_i3[n] * r2 * q3;
+        for (int j = lane; j < D; j += 32) {
+            const int j12 = j / q3, j3 = j - j12 * q3;
+            float a = 0.f;
+            for (int c = 0; c < r2; ++c) a = fmaf(Tp[j12 * r2 + c], g3[c * q3 + j3], a);
+            __stcg(P.cache_vals + slot * D + j, a);
+        }
+        if (lane == 0) P.cache_stamp[slot] = *P.dstep;
     }
-    return slot;
 }
 
 // Static fast path: lanes = 2 output halves (lj) x 16 contraction lanes (lc);
@@ -447,7 +454,7 @@ __device__ void pool_bag_static(const Params& P, const TableDev& T, int64_t bag,
     float acc[H];
 #pragma unroll
     for (int v = 0; v < H; ++v) acc[v] = 0.f;
-    if (P.cache_n == 0 || P.cache_train) {
+    {
         // warp w takes lookups lo + w + kPoolWarps l; lane l first loads the indices of the
         // warp's l-th lookup of a round (one pass), then the warp walks them kPoolPer at a time
         for (int64_t nb0 = lo; nb0 < hi; nb0 += 32 * kPoolWarps) {
@@ -459,6 +466,7 @@ __device__ void pool_bag_static(const Params& P, const TableDev& T, int64_t bag,
                 i2l = P.lk_i2[nl];
                 i3l = P.lk_i3[nl];
                 sl = P.lk_s[nl];
+                if (P.cache_n > 0 && P.lk_hit[nl] >= 0) sl = 0.f;  // read from the cache below
             }
             const int64_t left = hi - nb0 - w;  // this warp's lookups nb0 + w + kPoolWarps l < hi
             const int64_t c64 = left <= 0 ? 0 : (left + kPoolWarps - 1) / kPoolWarps;
@@ -510,61 +518,6 @@ __device__ void pool_bag_static(const Params& P, const TableDev& T, int64_t bag,
                     }
             }
         }
-    } else {
-        for (int64_t n = lo + w; n < hi; n += kPoolWarps) {
-            const int i1 = P.lk_i1[n], i2 = P.lk_i2[n], i3 = P.lk_i3[n];
-            const float s = P.lk_s[n];
-            bool fresh;
-            const int64_t slot = cache_probe(P, T, i1, i2, i3, fresh);
-            if (fresh) {
-                if (lc == 0) {
-                    const float* cv = P.cache_vals + slot * D + lj * H;
-#pragma unroll
-                    for (int v = 0; v < H; ++v) acc[v] = fmaf(s, __ldcg(cv + v), acc[v]);
-                }
-                continue;
-            }
-            const float* Tp = t_of_pair(P, T, i2, i1) + lj * J12H * R2;
-            const float* g3 = T.G3 + (int64_t)i3 * R2 * Q3;
-            float tv[J12H][NC], gv[NC][Q3];
-#pragma unroll
-            for (int k = 0; k < NC; ++k) {
-                const int c = lc + 16 * k;
-#pragma unroll
-                for (int j = 0; j < J12H; ++j) tv[j][k] = __ldg(Tp + j * R2 + c);
-#pragma unroll
-                for (int j3 = 0; j3 < Q3; j3 += 4) {
-                    const float4 x = __ldg(reinterpret_cast<const float4*>(g3 + c * Q3 + j3));
-                    gv[k][j3] = x.x; gv[k][j3 + 1] = x.y; gv[k][j3 + 2] = x.z; gv[k][j3 + 3] = x.w;
-                }
-            }
-#pragma unroll
-            for (int j = 0; j < J12H; ++j)
-#pragma unroll
-                for (int j3 = 0; j3 < Q3; ++j3) {
-                    float t = 0.f;
-#pragma unroll
-                    for (int k = 0; k < NC; ++k) t = fmaf(tv[j][k], gv[k][j3], t);
-                    acc[j * Q3 + j3] = fmaf(s, t, acc[j * Q3 + j3]);
-                }
-            if (slot >= 0) {
-                // refresh a stale cached row: each column summed over the 16 lc lanes
-#pragma unroll
-                for (int j = 0; j < J12H; ++j)
-#pragma unroll
-                    for (int j3 = 0; j3 < Q3; ++j3) {
-                        float t = 0.f;
-#pragma unroll
-                        for (int k = 0; k < NC; ++k) t = fmaf(tv[j][k], gv[k][j3], t);
-#pragma unroll
-                        for (int o = 8; o >= 1; o >>= 1) t += __shfl_xor_sync(0xffffffffu, t, o);
-                        if (lc == 0) __stcg(P.cache_vals + slot * D + lj * H + j * Q3 + j3, t);
-                    }
-                __threadfence();
-                __syncwarp();
-                if (lane == 0) atomicExch(P.cache_stamp + slot, *P.dstep);
-            }
-        }
     }
     // reduce-scatter over the 16 lc lanes: each stage halves the vector
 #pragma unroll
@@ -578,7 +531,7 @@ __device__ void pool_bag_static(const Params& P, const TableDev& T, int64_t bag,
         }
     }
     constexpr int V = H / 16;
-    if (P.cache_train) {  // trainable cache rows: s times the cached value, V columns a lane
+    if (P.cache_n > 0) {  // cache hits: s times the cached value, V columns a lane
         for (int64_t n = lo + w; n < hi; n += kPoolWarps) {
             const int slot = P.lk_hit[n];
             if (slot < 0) continue;
@@ -588,6 +541,7 @@ __device__ void pool_bag_static(const Params& P, const TableDev& T, int64_t bag,
             for (int v = 0; v < V; ++v) acc[v] = fmaf(sh, __ldcg(cv + v), acc[v]);
         }
     }
+    if (P.cache_n > 0 && !P.cache_train) cache_refresh_rows(P, T, lo, hi);
 #pragma unroll
     for (int v = 0; v < V; ++v) red[w * D + lj * H + lc * V + v] = acc[v];
     __syncthreads();
@@ -609,43 +563,20 @@ __device__ void pool_bag_generic(const Params& P, const TableDev& T, int64_t bag
     for (int m = 0; m < kMaxDPerLane; ++m) acc[m] = 0.f;
     for (int64_t n = lo + w; n < hi; n += kPoolWarps) {
         const int i1 = P.lk_i1[n], i2 = P.lk_i2[n], i3 = P.lk_i3[n];
-        const float s = P.lk_s[n];
-        bool fresh;
-        const int64_t slot = cache_probe(P, T, i1, i2, i3, fresh);
-        float v[kMaxDPerLane];
-        if (fresh) {
+        const float s = (P.cache_n > 0 && P.lk_hit[n] >= 0) ? 0.f : P.lk_s[n];  // a hit reads the cache below
+        const float* Tp = t_of_pair(P, T, i2, i1);
+        const float* g3 = T.G3 + (int64_t)i3 * r2 * q3;
 #pragma unroll
-            for (int m = 0; m < kMaxDPerLane; ++m) {
-                const int j = lane + 32 * m;
-                v[m] = j < D ? __ldcg(P.cache_vals + slot * D + j) : 0.f;
+        for (int m = 0; m < kMaxDPerLane; ++m) {
+            const int j = lane + 32 * m;
+            float a = 0.f;
+            if (j < D) {
+                const int j12 = j / q3, j3 = j - j12 * q3;
+                for (int c = 0; c < r2; ++c) a = fmaf(Tp[j12 * r2 + c], g3[c * q3 + j3], a);
             }
-        } else {
-            const float* Tp = t_of_pair(P, T, i2, i1);
-            const float* g3 = T.G3 + (int64_t)i3 * r2 * q3;
-#pragma unroll
-            for (int m = 0; m < kMaxDPerLane; ++m) {
-                const int j = lane + 32 * m;
-                float a = 0.f;
-                if (j < D) {
-                    const int j12 = j / q3, j3 = j - j12 * q3;
-                    for (int c = 0; c < r2; ++c) a = fmaf(Tp[j12 * r2 + c], g3[c * q3 + j3], a);
-                }
-                v[m] = a;
-            }
-            if (slot >= 0) {
-#pragma unroll
-                for (int m = 0; m < kMaxDPerLane; ++m) {
-                    const int j = lane + 32 * m;
-                    if (j < D) __stcg(P.cache_vals + slot * D + j, v[m]);
-                }
-                __threadfence();
-                __syncwarp();
-                if (lane == 0) atomicExch(P.cache_stamp + slot, *P.dstep);
-            }
+            acc[m] = fmaf(s, a, acc[m]);
         }
-#pragma unroll
-        for (int m = 0; m < kMaxDPerLane; ++m) acc[m] = fmaf(s, v[m], acc[m]);
-        if (P.cache_train) {  // trainable cache rows: s times the cached value
+        if (P.cache_n > 0) {  // a cache hit: s times the cached value
             const int slot2 = P.lk_hit[n];
             if (slot2 >= 0) {
                 const float sh = P.lk_sh[n];
@@ -657,6 +588,7 @@ __device__ void pool_bag_generic(const Params& P, const TableDev& T, int64_t bag
             }
         }
     }
+    if (P.cache_n > 0 && !P.cache_train) cache_refresh_rows(P, T, lo, hi);
 #pragma unroll
     for (int m = 0; m < kMaxDPerLane; ++m) {
         const int j = lane + 32 * m;
@@ -809,80 +741,205 @@ cudaError_t launch_full_weight(const TableDev* tables, int t, int64_t row0, int6
 // double) is rounded to a multiple of 2^-S.  With every |term| < 2^e and at most 2^k
 // terms, S = 61 - e - k keeps every partial sum below 2^62.
 
-// 2^x as a double (x within the normal exponent range).
-__device__ __forceinline__ double pow2d(int x) { return __longlong_as_double((long long)(x + 1023) << 52); }
+// 2^x as a float (x within the normal exponent range).
+__device__ __forceinline__ float pow2f(int x) { return __int_as_float((x + 127) << 23); }
 
-// S of the step from the largest term, or INT_MIN when that is not finite.
+// v * 2^x, exact for the ranges used here: two power-of-two factors within the
+// normal exponent range, so neither product overflows while |v * 2^x| < 2^62.
+__device__ __forceinline__ float scale2(float v, int x) {
+    const int a = x / 2;
+    return v * pow2f(a) * pow2f(x - a);
+}
+
+// S of the step, or INT_MIN when a bound is not finite.  Every hit term satisfies
+// |sh * g| <= max|sh| * max|g| < 2^(eS + eG) (the exponents of the two maxima); fp32
+// terms are 0 or >= 2^-149, so e = max(eS + eG, -149) and S = 61 - e - k, nnz <= 2^k.
 __device__ __forceinline__ int cache_fixed_shift(const Params& P) {
-    const unsigned gb = P.cache_gmax[0];
-    const int E = (int)((gb >> 23) & 255u);
-    if (E == 255) return INT_MIN;
-    const int e = (E == 0 ? 1 : E) - 126;  // |term| <= largest < 2^e
+    const int EG = (int)((P.cache_gmax[0] >> 23) & 255u), ES = (int)((P.cache_gmax[3] >> 23) & 255u);
+    if (EG == 255 || ES == 255) return INT_MIN;
+    int e = ((EG == 0 ? 1 : EG) - 126) + ((ES == 0 ? 1 : ES) - 126);
+    e = e < -149 ? -149 : e;
     int k = 0;
     while (((int64_t)1 << k) < P.nnz) ++k;
     return 61 - e - k;
 }
 
-// Largest |sh * grad_out| over the hits of the step (a non-finite term counts as
-// infinity) into cache_gmax[0], which the previous step's k_cache_apply left at 0;
-// clears the touch flags of the previous step.
+// max|grad_out| into cache_gmax[0] and max|sh| over the hits into cache_gmax[3]
+// (a non-finite value counts as infinity; both words were left at 0 by the previous
+// step's k_cache_apply); the touched-slot list starts empty.
 __global__ void __launch_bounds__(256) k_cache_gmax(const __grid_constant__ Params P) {
     pdl_entry();
-    const int lane = threadIdx.x & 31, D = P.D;
-    const int64_t gt = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
-    for (int64_t i = gt; i < P.cache_n; i += (int64_t)gridDim.x * blockDim.x) P.cache_touch[i] = 0;
-    float m = 0.f;
-    const int64_t warps = (int64_t)gridDim.x * (blockDim.x >> 5);
-    for (int64_t n = gt >> 5; n < P.nnz; n += warps) {
-        if (P.lk_hit[n] < 0) continue;
-        const float sh = P.lk_sh[n];
-        const float* g = P.grad_out + (int64_t)P.lk_bag[n] * D;
-        for (int j = lane; j < D; j += 32) {
-            const float a = fabsf(sh * g[j]);
-            m = fmaxf(m, a <= 3.402823466e38f ? a : __int_as_float(0x7f800000));
-        }
+    __shared__ float wm[2][8];
+    const int lane = threadIdx.x & 31, w = threadIdx.x >> 5;
+    const int64_t gt = (int64_t)blockIdx.x * blockDim.x + threadIdx.x, stride = (int64_t)gridDim.x * blockDim.x;
+    if (gt == 0) P.cache_gmax[2] = 0u;
+    const float inf = __int_as_float(0x7f800000);
+    float mg = 0.f, ms = 0.f;
+    const int64_t ng = (int64_t)P.nbags * P.D;
+    for (int64_t i = gt; i < ng; i += stride) {
+        const float a = fabsf(__ldg(P.grad_out + i));
+        mg = fmaxf(mg, a <= 3.402823466e38f ? a : inf);
+    }
+    for (int64_t n = gt; n < P.nnz; n += stride) {
+        const float a = P.lk_hit[n] >= 0 ? fabsf(P.lk_sh[n]) : 0.f;
+        ms = fmaxf(ms, a <= 3.402823466e38f ? a : inf);
     }
 #pragma unroll
-    for (int o = 16; o >= 1; o >>= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, o));
-    if (lane == 0 && m > 0.f) atomicMax(P.cache_gmax, __float_as_uint(m));
+    for (int o = 16; o >= 1; o >>= 1) {
+        mg = fmaxf(mg, __shfl_xor_sync(0xffffffffu, mg, o));
+        ms = fmaxf(ms, __shfl_xor_sync(0xffffffffu, ms, o));
+    }
+    if (lane == 0) {
+        wm[0][w] = mg;
+        wm[1][w] = ms;
+    }
+    __syncthreads();
+    if (threadIdx.x == 0) {
+        for (int v = 1; v < (int)(blockDim.x >> 5); ++v) {
+            mg = fmaxf(mg, wm[0][v]);
+            ms = fmaxf(ms, wm[1][v]);
+        }
+        if (mg > 0.f) atomicMax(P.cache_gmax, __float_as_uint(mg));
+        if (ms > 0.f) atomicMax(P.cache_gmax + 3, __float_as_uint(ms));
+    }
 }
 
-// Fixed-point sum of the hit terms into cache_acc; marks the touched slots and
-// passes S on in cache_gmax[1].
-__global__ void __launch_bounds__(256) k_cache_acc(const __grid_constant__ Params P) {
+// Fixed-point sums of the hit terms into cache_acc.  A block takes kCacheChunk
+// consecutive lookups and sorts its hits by slot in shared memory; a warp sums each
+// slot's run in registers (term = round(fl(sh * g) * 2^S), four hits' loads in
+// flight at a time) and adds it with one integer atomic per column, so a hot row
+// costs one atomic per block and column.  The first block to touch a slot appends it
+// to the touched list (one list reservation per block).  Block 0 passes S on in
+// cache_gmax[1].  DPL = columns per lane (D <= 32 DPL).
+constexpr int kCacheChunk = 256;
+
+template <int DPL>
+__global__ void __launch_bounds__(kCacheChunk) k_cache_acc(const __grid_constant__ Params P) {
     pdl_entry();
+    __shared__ unsigned long long key[kCacheChunk];  // (slot << 32) | position in the chunk
+    __shared__ float shs[kCacheChunk];
+    __shared__ int bags[kCacheChunk];
+    __shared__ int heads[kCacheChunk];
+    __shared__ int fresh[kCacheChunk];  // slots this block touched first
+    __shared__ int wcnt[2][kCacheChunk / 32];
+    __shared__ int nhead, nhit, nfresh, fbase;
     const int S = cache_fixed_shift(P);
     if (blockIdx.x == 0 && threadIdx.x == 0) P.cache_gmax[1] = (unsigned)S;
-    if (S == INT_MIN) return;
-    const double scale = pow2d(S);
-    const int lane = threadIdx.x & 31, D = P.D;
-    const int64_t warps = (int64_t)gridDim.x * (blockDim.x >> 5);
-    for (int64_t n = ((int64_t)blockIdx.x * blockDim.x + threadIdx.x) >> 5; n < P.nnz; n += warps) {
-        const int slot = P.lk_hit[n];
-        if (slot < 0) continue;
-        const double sh = P.lk_sh[n];
-        const float* g = P.grad_out + (int64_t)P.lk_bag[n] * D;
-        unsigned long long* acc = P.cache_acc + (int64_t)slot * D;
-        for (int j = lane; j < D; j += 32)
-            atomicAdd(acc + j, (unsigned long long)__double2ll_rn(sh * (double)g[j] * scale));
-        if (lane == 0) P.cache_touch[slot] = 1;
+    const bool finite = S != INT_MIN;  // else the touched slots get NaN from k_cache_apply
+    const int tid = threadIdx.x, lane = tid & 31, w = tid >> 5, D = P.D;
+    for (int64_t c0 = (int64_t)blockIdx.x * kCacheChunk; c0 < P.nnz; c0 += (int64_t)gridDim.x * kCacheChunk) {
+        const int64_t n = c0 + tid;
+        const int slot = n < P.nnz ? P.lk_hit[n] : -1;
+        if (slot >= 0) {
+            shs[tid] = P.lk_sh[n];
+            bags[tid] = P.lk_bag[n];
+        }
+        key[tid] = ((unsigned long long)(slot >= 0 ? (unsigned)slot : 0xffffffffu) << 32) | (unsigned)tid;
+        if (tid == 0) nfresh = 0;
+        __syncthreads();
+        // bitonic sort of the chunk's keys, ascending: hits first, runs of equal slots
+        for (int k = 2; k <= kCacheChunk; k <<= 1)
+            for (int j = k >> 1; j > 0; j >>= 1) {
+                const int o = tid ^ j;
+                if (o > tid) {
+                    const unsigned long long a = key[tid], b = key[o];
+                    if (((tid & k) == 0) == (a > b)) {
+                        key[tid] = b;
+                        key[o] = a;
+                    }
+                }
+                __syncthreads();
+            }
+        // run heads in sorted order (ballot + prefix over the warps)
+        const unsigned ks = (unsigned)(key[tid] >> 32);
+        const bool hit = ks != 0xffffffffu;
+        const bool head = hit && (tid == 0 || (unsigned)(key[tid - 1] >> 32) != ks);
+        const unsigned hb = __ballot_sync(0xffffffffu, head), xb = __ballot_sync(0xffffffffu, hit);
+        if (lane == 0) {
+            wcnt[0][w] = __popc(hb);
+            wcnt[1][w] = __popc(xb);
+        }
+        __syncthreads();
+        int off = 0;
+        for (int v = 0; v < w; ++v) off += wcnt[0][v];
+        if (head) heads[off + __popc(hb & lanemask_lt())] = tid;
+        if (tid == 0) {
+            int a = 0, b = 0;
+            for (int v = 0; v < kCacheChunk / 32; ++v) {
+                a += wcnt[0][v];
+                b += wcnt[1][v];
+            }
+            nhead = a;
+            nhit = b;
+        }
+        __syncthreads();
+        for (int h = w; h < nhead; h += kCacheChunk / 32) {
+            const int i0 = heads[h], i1 = h + 1 < nhead ? heads[h + 1] : nhit;
+            const unsigned sl = (unsigned)(key[i0] >> 32);
+            long long acc[DPL];
+#pragma unroll
+            for (int m = 0; m < DPL; ++m) acc[m] = 0;
+            int i = i0;
+            if (finite) {
+                for (; i + 4 <= i1; i += 4) {
+                    float gv[4][DPL], sv[4];
+#pragma unroll
+                    for (int q = 0; q < 4; ++q) {
+                        const int t = (int)(key[i + q] & 0xffffffffu);
+                        sv[q] = shs[t];
+                        const float* g = P.grad_out + (int64_t)bags[t] * D;
+#pragma unroll
+                        for (int m = 0; m < DPL; ++m) gv[q][m] = lane + 32 * m < D ? g[lane + 32 * m] : 0.f;
+                    }
+#pragma unroll
+                    for (int q = 0; q < 4; ++q)
+#pragma unroll
+                        for (int m = 0; m < DPL; ++m) acc[m] += __float2ll_rn(scale2(sv[q] * gv[q][m], S));
+                }
+                for (; i < i1; ++i) {
+                    const int t = (int)(key[i] & 0xffffffffu);
+                    const float sh = shs[t];
+                    const float* g = P.grad_out + (int64_t)bags[t] * D;
+#pragma unroll
+                    for (int m = 0; m < DPL; ++m)
+                        if (lane + 32 * m < D) acc[m] += __float2ll_rn(scale2(sh * g[lane + 32 * m], S));
+                }
+            }
+            unsigned long long* dst = P.cache_acc + (int64_t)sl * D;
+#pragma unroll
+            for (int m = 0; m < DPL; ++m)
+                if (lane + 32 * m < D) atomicAdd(dst + lane + 32 * m, (unsigned long long)acc[m]);
+        }
+        // touched-slot bookkeeping, a thread per run
+        if (tid < nhead) {
+            const int sl = (int)(key[heads[tid]] >> 32);
+            if (P.cache_touch[sl] == 0 && atomicExch(P.cache_touch + sl, 1) == 0) fresh[atomicAdd(&nfresh, 1)] = sl;
+        }
+        __syncthreads();
+        if (tid == 0 && nfresh > 0) fbase = (int)atomicAdd(P.cache_gmax + 2, (unsigned)nfresh);
+        __syncthreads();
+        if (tid < nfresh) P.cache_list[fbase + tid] = fresh[tid];
+        __syncthreads();
     }
 }
 
 // The optimizer step of the touched cached values (SGD, Adagrad, or the gradient kept
-// for reading); the accumulators and cache_gmax[0] return to zero.
+// for reading), a thread per (listed slot, column); the accumulators, touch flags
+// and the two bound words return to zero.
 __global__ void __launch_bounds__(256) k_cache_apply(const __grid_constant__ Params P) {
     pdl_entry();
     const int S = (int)P.cache_gmax[1];
-    if (blockIdx.x == 0 && threadIdx.x == 0) P.cache_gmax[0] = 0u;
-    const double unscale = S == INT_MIN ? 0.0 : pow2d(-S);
-    const int64_t total = P.cache_n * P.D;
-    for (int64_t e = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; e < total; e += (int64_t)gridDim.x * blockDim.x) {
-        if (!P.cache_touch[e / P.D]) {
-            if (P.opt == TT_OPT_GRAD) P.cache_grad[e] = 0.f;
-            continue;
-        }
-        const float g = S == INT_MIN ? __int_as_float(0x7fffffff) : (float)((double)(long long)P.cache_acc[e] * unscale);
+    const int64_t total = (int64_t)P.cache_gmax[2] * P.D;
+    if (blockIdx.x == 0 && threadIdx.x == 0) {
+        P.cache_gmax[0] = 0u;
+        P.cache_gmax[3] = 0u;
+    }
+    for (int64_t f = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; f < total; f += (int64_t)gridDim.x * blockDim.x) {
+        const int64_t i = f / P.D;
+        const int j = (int)(f - i * P.D);
+        const int slot = P.cache_list[i];
+        const int64_t e = (int64_t)slot * P.D + j;
+        const float g = S == INT_MIN ? __int_as_float(0x7fffffff) : scale2(__ll2float_rn((long long)P.cache_acc[e]), -S);
         P.cache_acc[e] = 0ull;
         if (P.opt == TT_OPT_SGD) {
             P.cache_vals[e] = fmaf(-P.lr, g, P.cache_vals[e]);
@@ -893,6 +950,7 @@ __global__ void __launch_bounds__(256) k_cache_apply(const __grid_constant__ Par
         } else {
             P.cache_grad[e] = g;
         }
+        if (j == 0) P.cache_touch[slot] = 0;
     }
 }
 
@@ -909,18 +967,21 @@ static int64_t grid_for(int64_t units, int per_block, int64_t cap) {
 }
 
 cudaError_t launch_cache_gmax(const Params& P, cudaStream_t s) {
-    const int64_t b = std::max(grid_for(P.nnz, 8, 152 * 8), grid_for(P.cache_n, 256, 152 * 8));
+    const int64_t b = grid_for(std::max<int64_t>(P.nnz, (int64_t)P.nbags * P.D), 256 * 4, 152 * 2);
     cudaError_t le = launch_pdl(k_cache_gmax, dim3((unsigned)b), dim3(256), 0, s, P);
     return le != cudaSuccess ? le : cudaGetLastError();
 }
 
 cudaError_t launch_cache_acc(const Params& P, cudaStream_t s) {
-    cudaError_t le = launch_pdl(k_cache_acc, dim3((unsigned)grid_for(P.nnz, 8, 152 * 8)), dim3(256), 0, s, P);
+    const int64_t b = grid_for(P.nnz, kCacheChunk, 152 * 8);
+    cudaError_t le = P.D <= 64 ? launch_pdl(k_cache_acc<2>, dim3((unsigned)b), dim3(kCacheChunk), 0, s, P)
+                   : P.D <= 128 ? launch_pdl(k_cache_acc<4>, dim3((unsigned)b), dim3(kCacheChunk), 0, s, P)
+                                : launch_pdl(k_cache_acc<8>, dim3((unsigned)b), dim3(kCacheChunk), 0, s, P);
     return le != cudaSuccess ? le : cudaGetLastError();
 }
 
 cudaError_t launch_cache_apply(const Params& P, cudaStream_t s) {
-    const int64_t b = grid_for(P.cache_n * P.D, 256, 152 * 16);
+    const int64_t b = grid_for(P.cache_n * P.D, 256, 152 * 8);
     cudaError_t le = launch_pdl(k_cache_apply, dim3((unsigned)b), dim3(256), 0, s, P);
     return le != cudaSuccess ? le : cudaGetLastError();
 }

@@ -142,10 +142,14 @@ struct Params {
     int* counters;                  // spare device counters
     int* err;
     // hot-row cache (single table)
-    const int64_t* cache_rows;      // sorted row ids, or null
+    const int64_t* cache_rows;      // row id per slot (-1 = empty way)
+    const longlong2* cache_hidx;    // explicit rows: open-addressing index, (row id or -1, slot)
+    int cache_hmask;                //   entries - 1 (a power of two minus one)
+    int cache_hprobe;               //   longest probe sequence of the index
     int64_t cache_n;
     float* cache_vals;              // [cache_n][D]
     int* cache_stamp;               // [cache_n] *dstep when the row was computed
+    int* cache_claim;               // [cache_n] epoch of the pass whose decode chose the row's refresher
     int* slice_stamp;               // [p1 + p2 + p3] *dstep + 1 of the backward that last changed the slice
     int* dstep;                     // device counter: advanced by the decode kernel of every forward pass
     // FBTT README, "Software Cache": access-frequency table (open addressing, linear
@@ -163,8 +167,9 @@ struct Params {
     unsigned long long* cache_acc;  // [cache_n][D] fixed-point gradient sums
     float* cache_state;             // [cache_n][D] Adagrad accumulators of the cached values
     float* cache_grad;              // [cache_n][D] last gradient of the cached values (sparse=False)
-    unsigned* cache_gmax;           // [2]: max |hit term| of the step (float bits), its shift S
+    unsigned* cache_gmax;           // [4]: max|grad_out| (float bits), shift S, touched slots, max|hit scale|
     int* cache_touch;               // [cache_n] 1 once a hit of this step touched the slot
+    int* cache_list;                // [cache_n] the touched slots of the step
 };
 
 // ---------------------------------------------------------------- helpers
@@ -346,21 +351,33 @@ __device__ __forceinline__ void lfu_count(const Params& P, int64_t row) {
 
 // Lookup n with its index `row` and weight `w` (loaded by the caller, so that the
 // loads can be issued early).
-// Cache slot of `row` (table 0) or -1: set-associative (the kLfuWays ways of the row's
-// set) or a binary search of the sorted rows.
-__device__ __forceinline__ int64_t cache_find(const Params& P, int64_t row) {
+// Cache slot of `row` (table 0) or -1.  Set-associative cache: the kLfuWays ways of
+// the row's set, all loaded at once (16-byte loads of a 256-byte aligned set).
+// Explicit rows: linear probing in the open-addressing index from entry
+// mix64(row) mod size, at most the index's longest probe sequence.
+__device__ __forceinline__ int cache_find(const Params& P, int64_t row) {
     if (P.cache_sets > 0) {
-        const int64_t base = lfu_set_of(row, P.cache_sets) * kLfuWays;
-        for (int w = 0; w < kLfuWays; ++w)
-            if (P.cache_rows[base + w] == row) return base + w;
-        return -1;
+        const longlong2* set = reinterpret_cast<const longlong2*>(P.cache_rows + lfu_set_of(row, P.cache_sets) * kLfuWays);
+        long long w[kLfuWays];
+#pragma unroll
+        for (int v = 0; v < kLfuWays / 2; ++v) {
+            const longlong2 x = __ldg(set + v);
+            w[2 * v] = x.x;
+            w[2 * v + 1] = x.y;
+        }
+        int found = -1;
+#pragma unroll
+        for (int v = 0; v < kLfuWays; ++v) found = (w[v] == row) ? v : found;
+        return found < 0 ? -1 : (int)(lfu_set_of(row, P.cache_sets) * kLfuWays) + found;
     }
-    int64_t a = 0, b = P.cache_n;
-    while (a < b) {
-        const int64_t m = (a + b) >> 1;
-        if (P.cache_rows[m] < row) a = m + 1; else b = m;
+    unsigned e = (unsigned)mix64((uint64_t)row) & (unsigned)P.cache_hmask;
+    for (int k = 0; k < P.cache_hprobe; ++k) {
+        const longlong2 x = __ldg(P.cache_hidx + e);
+        if (x.x == row) return (int)x.y;
+        if (x.x < 0) return -1;
+        e = (e + 1) & (unsigned)P.cache_hmask;
     }
-    return (a < P.cache_n && P.cache_rows[a] == row) ? a : -1;
+    return -1;
 }
 
 __device__ __forceinline__ void decode_lookup(const Params& P, int64_t n, int bag, int64_t row, float w, int& t,
@@ -368,7 +385,8 @@ __device__ __forceinline__ void decode_lookup(const Params& P, int64_t n, int ba
     t = table_of_bag(P, bag);
     const TableDev& T = P.tables[t];
     float s = w;
-    if (row < 0 || row >= T.E) {
+    const bool valid = row >= 0 && row < T.E;
+    if (!valid) {
         atomicOr(P.err, kErrIndex);
         row = 0;
         s = 0.0f;
@@ -378,14 +396,6 @@ __device__ __forceinline__ void decode_lookup(const Params& P, int64_t n, int ba
     if (P.mean) {
         const int64_t L = P.off[bag + 1] - P.off[bag];
         s = s / (float)(L > 0 ? L : 1);
-    }
-    if (P.cache_train) {  // a hit leaves the TT path (scale 0 there) for its cached value
-        const int64_t slot = cache_find(P, row);
-        P.lk_hit[n] = (int)slot;
-        if (slot >= 0) {
-            P.lk_sh[n] = s;
-            s = 0.0f;
-        }
     }
     if (T.idx32) {
         const unsigned r = (unsigned)row, p3 = (unsigned)T.p3, q = r / p3;
@@ -397,6 +407,26 @@ __device__ __forceinline__ void decode_lookup(const Params& P, int64_t n, int ba
         i1 = (int)(row / p23);
         i2 = (int)((row / T.p3) % T.p2);
         i3 = (int)(row % T.p3);
+    }
+    // cache: lk_hit = slot for a lookup that reads its cached value (the pool gives its
+    // TT path scale 0), -2 - slot for the one lookup of a pass that refreshes a stale
+    // exact copy, -1 otherwise.  A trainable hit takes no part in the cores' gradient
+    // (lk_s = 0); an exact-copy hit keeps it.
+    if (P.cache_n > 0) {
+        int slot = valid ? cache_find(P, row) : -1;
+        if (slot >= 0) {
+            if (P.cache_train) {
+                P.lk_sh[n] = s;
+                s = 0.0f;
+            } else {
+                const int need = max(max(P.slice_stamp[i1], P.slice_stamp[T.p1 + i2]), P.slice_stamp[T.p1 + T.p2 + i3]);
+                if (P.cache_stamp[slot] >= need)
+                    P.lk_sh[n] = s;
+                else
+                    slot = atomicExch(P.cache_claim + slot, epoch) != epoch ? -2 - slot : -1;
+            }
+        }
+        P.lk_hit[n] = slot;
     }
     P.lk_i1[n] = i1;
     P.lk_i2[n] = i2;

@@ -63,10 +63,22 @@ def _lfu_run(wl, cache_size=1024):
     return run, tt.tt_emb_lfu_cached_rows(run.h)
 
 
-def test_two_sgd_steps_lfu(workloads):
-    """Zipf weighted-mean workload (11M x 64, rank 32), 512 bags: forward, SGD step, forward."""
+def _rows_run(wl):
+    """Handle with the workload's 110,000 hot rows cached explicitly (hash index), trainable."""
+    run = GpuRun(wl)
+    tt.tt_emb_cache_set_trainable(run.h, True)
+    tt.tt_emb_cache_populate(run.h, dev(wl.cache_rows))
+    rows = tt.tt_emb_lfu_cached_rows(run.h)
+    np.testing.assert_array_equal(rows, np.sort(wl.cache_rows))
+    return run, rows
+
+
+@pytest.mark.parametrize("policy", ["lfu", "rows"])
+def test_two_sgd_steps(workloads, policy):
+    """Zipf weighted-mean workload (11M x 64, rank 32), 512 bags: forward, SGD step, forward;
+    an LFU cache of 1024 rows, or the 110,000 hot rows given explicitly."""
     wl = workloads(3, 512)
-    run, rows = _lfu_run(wl)
+    run, rows = _lfu_run(wl) if policy == "lfu" else _rows_run(wl)
     live = rows >= 0
     assert np.isin(wl.indices, rows[live]).mean() > 0.3
     vals0 = _initial_values(wl, rows)
