@@ -166,7 +166,7 @@ tt_status tt_emb_backward(tt_emb* h, const float* grad_out_dev, float lr, tt_str
  * The handle keeps the pointers, which must stay valid while it is used.
  * Synchronous (copies the handle's device tables); not for stream capture.
  * Returns TT_ERR_ARG (null handle, unknown optim, bad eps, null or misaligned
- * aux, Adagrad with eps = 0 while the cache rows are trainable), TT_ERR_CUDA.
+ * aux), TT_ERR_CUDA.
  */
 tt_status tt_emb_set_optimizer(tt_emb* h, int32_t optim, float eps, float* const* aux);
 
@@ -255,11 +255,11 @@ tt_status tt_emb_lfu_disable(tt_emb* h);
  *   tt_emb_set_optimizer then updates the cached values that some hit touched
  *   (SGD; Adagrad with its own state per cached value, zero at populate; or
  *   TT_OPT_GRAD, which keeps the gradient for tt_emb_cache_read and gives
- *   untouched values 0); misses train the cores as before.  The cache state
- *   (installed now or later by a populate call) is initialised from the cores.
- *   Adagrad with eps = 0 is refused (TT_ERR_ARG): a slice that only hits touch
- *   gets a zero gradient.  (h, 0): back to exact-copy rows, recomputed from
- *   the cores now.  Synchronous.
+ *   untouched values 0); misses train the cores as before.  Hits take no part
+ *   in the TT contractions or their grouping: a core slice that only hits use
+ *   is not touched.  The cache state (installed now or later by a populate
+ *   call) is initialised from the cores.  (h, 0): back to exact-copy rows,
+ *   recomputed from the cores now.  Synchronous.
  * tt_emb_cache_read: copy the cached values ([slots][D] fp32, slot order of
  *   tt_emb_lfu_cached_rows) into vals_dev and, trainable mode only, the last
  *   gradients of TT_OPT_GRAD into grads_dev (caller-owned device buffers; either

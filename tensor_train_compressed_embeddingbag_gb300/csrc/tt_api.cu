@@ -324,6 +324,9 @@ tt_status build_handle(tt_emb* h, int ntab, const tt_table_desc* d) {
     if (cudaMalloc(&h->d_tbuf, sizeof(float) * std::max<int64_t>(tb, 1)) != cudaSuccess) return TT_ERR_NOMEM;
     if (cudaMalloc(&h->d_tflag, sizeof(int) * std::max<int64_t>(fb, 1)) != cudaSuccess) return TT_ERR_NOMEM;
     if (cudaMemset(h->d_tflag, 0, sizeof(int) * std::max<int64_t>(fb, 1)) != cudaSuccess) return TT_ERR_CUDA;
+    // T of a pair that no lookup of a pass touched is read (times 0) by the trainable
+    // cache hits of that pass: the buffer must hold finite values from the start
+    if (cudaMemset(h->d_tbuf, 0, sizeof(float) * std::max<int64_t>(tb, 1)) != cudaSuccess) return TT_ERR_CUDA;
     h->tbuf_floats = tb;
     if (cudaMemcpy(h->d_tables, h->tabs.data(), sizeof(TableDev) * ntab, cudaMemcpyHostToDevice) != cudaSuccess ||
         cudaMemcpy(h->d_bins, bins.data(), sizeof(int) * bins.size(), cudaMemcpyHostToDevice) != cudaSuccess ||
@@ -342,6 +345,7 @@ tt_status build_handle(tt_emb* h, int ntab, const tt_table_desc* d) {
     P.ntiles = h->d_fixed + 3;
     P.epoch = h->d_fixed + 4;
     P.dstep = h->d_fixed + 5;
+    P.nincl = h->d_fixed + 6;
     P.grp_done = h->d_fixed + 8;
     P.Tbuf = h->d_tbuf;
     P.tflag = h->d_tflag;
@@ -600,8 +604,6 @@ tt_status tt_emb_set_optimizer(tt_emb* h, int32_t optim, float eps, float* const
     if (!h) return TT_ERR_ARG;
     if (optim != TT_OPT_SGD && optim != TT_OPT_ADAGRAD && optim != TT_OPT_GRAD) return TT_ERR_ARG;
     if (optim == TT_OPT_ADAGRAD && !(eps >= 0.f && eps <= 3.0e38f)) return TT_ERR_ARG;
-    // a slice that only trainable cache hits touch gets a zero gradient: 0 / 0 with eps = 0
-    if (optim == TT_OPT_ADAGRAD && eps == 0.f && h->cache_train) return TT_ERR_ARG;
     if (optim != TT_OPT_SGD) {
         if (!aux) return TT_ERR_ARG;
         for (int i = 0; i < 3 * h->ntab; ++i)
@@ -885,7 +887,6 @@ tt_status tt_emb_cache_disable(tt_emb* h) {
 tt_status tt_emb_cache_set_trainable(tt_emb* h, int32_t trainable, tt_stream stream) {
     if (!h || (trainable != 0 && trainable != 1)) return TT_ERR_ARG;
     if (h->ntab != 1) return TT_ERR_STATE;
-    if (trainable && h->P.opt == TT_OPT_ADAGRAD && h->P.eps == 0.f) return TT_ERR_ARG;
     cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
     if (h->cache_n > 0) cudaDeviceSynchronize();
     if (h->P.cache_train) {  // the last forward's hit slots refer to this cache state

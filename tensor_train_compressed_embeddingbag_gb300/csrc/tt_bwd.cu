@@ -120,7 +120,7 @@ __device__ void reduce_slice(const Params& P, int bglob, int* slots, int* sh, fl
     const int* H = first_core ? P.H1 : P.H3;
     const int* rep = first_core ? P.rep1 : P.rep3;  // indexed by position in the i1 / i3 order
     const int start = H[(int64_t)b * P.nch];
-    const int end = (b + 1 < nb) ? H[(int64_t)(b + 1) * P.nch] : (int)P.nnz;
+    const int end = (b + 1 < nb) ? H[(int64_t)(b + 1) * P.nch] : *P.nincl;
     const int t = first_core ? P.bin1_tab[b] : P.bin3_tab[b];
     const TableDev& T = P.tables[t];
     const int slice = b - (first_core ? T.base1 : T.base3);
@@ -795,7 +795,7 @@ __global__ void __launch_bounds__(kBwdThreads, 3) k_reduce13(const __grid_consta
     const int bb = b < P.n1 ? b : b - P.n1;
     const int* H = b < P.n1 ? P.H1 : P.H3;
     const int start = H[(int64_t)bb * P.nch];
-    const int end = (bb + 1 < nb) ? H[(int64_t)(bb + 1) * P.nch] : (int)P.nnz;
+    const int end = (bb + 1 < nb) ? H[(int64_t)(bb + 1) * P.nch] : *P.nincl;
     if (start >= end) return;
     reduce_slice(P, b, slots, sh, sacc);
 }

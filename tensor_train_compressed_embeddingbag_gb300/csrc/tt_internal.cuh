@@ -140,6 +140,7 @@ struct Params {
     float* Pbuf;                    // [nnz][ps_max]
     float* dG2part;                 // [max_tiles][s2_max]
     int* counters;                  // spare device counters
+    int* nincl;                     // lookups in the sorted orders (all but the trainable cache hits)
     int* err;
     // hot-row cache (single table)
     const int64_t* cache_rows;      // row id per slot (-1 = empty way)
@@ -380,7 +381,9 @@ __device__ __forceinline__ int cache_find(const Params& P, int64_t row) {
     return -1;
 }
 
-__device__ __forceinline__ void decode_lookup(const Params& P, int64_t n, int bag, int64_t row, float w, int& t,
+// Returns false for a lookup that stays out of the TT path and its grouping (a
+// trainable cache hit), true otherwise.
+__device__ __forceinline__ bool decode_lookup(const Params& P, int64_t n, int bag, int64_t row, float w, int& t,
                                               int& i1, int& i2, int& i3, int epoch) {
     t = table_of_bag(P, bag);
     const TableDev& T = P.tables[t];
@@ -433,7 +436,14 @@ __device__ __forceinline__ void decode_lookup(const Params& P, int64_t n, int ba
     P.lk_i3[n] = i3;
     P.lk_bag[n] = bag;
     P.lk_s[n] = s;
+    if (P.cache_train && P.lk_hit[n] >= 0) return false;
     P.tflag[T.fbase + (int64_t)i2 * T.p1 + i1] = epoch;
+    return true;
+}
+
+// The lookup stays out of the sorted orders (a trainable cache hit).
+__device__ __forceinline__ bool excluded(const Params& P, int64_t n) {
+    return P.cache_train && P.lk_hit[n] >= 0;
 }
 
 // Small path, part `part` (of kSmallChunk / blockDim) of chunk c: position =
@@ -443,6 +453,7 @@ __device__ __forceinline__ void scatter_chunk(const Params& P, int c, int part) 
     const int64_t cend = (int64_t)(c + 1) * kSmallChunk;
     const int64_t hi = (cend < P.nnz) ? cend : P.nnz;
     for (int64_t n = lo + threadIdx.x; n < hi && n < lo + blockDim.x; n += blockDim.x) {
+        if (excluded(P, n)) continue;
         const TableDev& T = P.tables[table_of_bag(P, P.lk_bag[n])];
         const int d1 = T.base1 + P.lk_i1[n], d2 = T.base2 + P.lk_i2[n], d3 = T.base3 + P.lk_i3[n];
         const int p1 = P.H1[(int64_t)d1 * P.nch + c] + P.lr1[n];
@@ -530,6 +541,7 @@ __device__ __forceinline__ void scan_digit_block(const Params& P, int k, int* sm
         __syncthreads();  // the next round reuses hs
     }
     if (k == 1 && threadIdx.x == 0) *P.ntiles = tcarry;
+    if (k == 0 && threadIdx.x == 0) *P.nincl = carry;
 }
 
 // ---------------------------------------------------------------- launchers

@@ -49,7 +49,8 @@ __global__ void __launch_bounds__(kSortThreads, 1) k_decode_hist(const __grid_co
     const int64_t hi = (lo + kChunk < P.nnz) ? lo + kChunk : P.nnz;
     for (int64_t n = lo + threadIdx.x; n < hi; n += blockDim.x) {
         int t, i1, i2, i3;
-        decode_lookup(P, n, (int)bag_of(P, n), P.idx[n], P.w ? P.w[n] : 1.0f, t, i1, i2, i3, *P.epoch);
+        if (!decode_lookup(P, n, (int)bag_of(P, n), P.idx[n], P.w ? P.w[n] : 1.0f, t, i1, i2, i3, *P.epoch))
+            continue;
         const TableDev& T = P.tables[t];
         atomicAdd(&h1[T.base1 + i1], 1);
         atomicAdd(&h3[T.base3 + i3], 1);
@@ -61,7 +62,8 @@ __global__ void __launch_bounds__(kSortThreads, 1) k_decode_hist(const __grid_co
 
 // ------------------------------------------------------------------ scans
 
-__device__ void scan_inplace(int* a, int64_t L, int* sh) {
+// Returns the total.
+__device__ int scan_inplace(int* a, int64_t L, int* sh) {
     int carry = 0;
     for (int64_t base = 0; base < L; base += blockDim.x) {
         const int64_t i = base + threadIdx.x;
@@ -71,13 +73,15 @@ __device__ void scan_inplace(int* a, int64_t L, int* sh) {
         if (i < L) a[i] = carry + ex;
         carry += total;
     }
+    return carry;
 }
 
 __global__ void __launch_bounds__(kScanThreads) k_scan13(const __grid_constant__ Params P) {
     pdl_entry();
     __shared__ int sh[33];
-    scan_inplace(P.H1, (int64_t)P.n1 * P.nch, sh);
+    const int total = scan_inplace(P.H1, (int64_t)P.n1 * P.nch, sh);
     scan_inplace(P.H3, (int64_t)P.n3 * P.nch, sh);
+    if (threadIdx.x == 0) *P.nincl = total;
 }
 
 // Exclusive scan of H2, then the tiles: each (table, i2) group of `cnt`
@@ -93,7 +97,7 @@ __global__ void __launch_bounds__(kScanThreads) k_scan2_tiles(const __grid_const
         int start = 0, cnt = 0, nt = 0;
         if (g < P.n2) {
             start = P.H2[(int64_t)g * P.nch];
-            const int end = (g + 1 < P.n2) ? P.H2[(int64_t)(g + 1) * P.nch] : (int)P.nnz;
+            const int end = (g + 1 < P.n2) ? P.H2[(int64_t)(g + 1) * P.nch] : *P.nincl;
             cnt = end - start;
             nt = (cnt + P.tile_cap - 1) / P.tile_cap;
         }
@@ -165,7 +169,7 @@ __global__ void __launch_bounds__(kSortThreads, 1) k_scatter13(const __grid_cons
     // by i1 -> pi1, and the i2 histogram of pi1 chunks
     chunk_stable_ranks(
         c, P.nnz, P.n1, cnt,
-        [&](int64_t n) { return P.tables[table_of_bag(P, P.lk_bag[n])].base1 + P.lk_i1[n]; },
+        [&](int64_t n) { return excluded(P, n) ? -1 : P.tables[table_of_bag(P, P.lk_bag[n])].base1 + P.lk_i1[n]; },
         [&](int64_t n, int d, int rank) {
             const int pos = P.H1[(int64_t)d * P.nch + c] + rank;
             P.pi1[pos] = (int)n;
@@ -175,7 +179,7 @@ __global__ void __launch_bounds__(kSortThreads, 1) k_scatter13(const __grid_cons
     // by i3 -> pi3
     chunk_stable_ranks(
         c, P.nnz, P.n3, cnt,
-        [&](int64_t n) { return P.tables[table_of_bag(P, P.lk_bag[n])].base3 + P.lk_i3[n]; },
+        [&](int64_t n) { return excluded(P, n) ? -1 : P.tables[table_of_bag(P, P.lk_bag[n])].base3 + P.lk_i3[n]; },
         [&](int64_t n, int d, int rank) {
             const int pos = P.H3[(int64_t)d * P.nch + c] + rank;
             P.pi3[pos] = (int)n;
@@ -187,9 +191,11 @@ __global__ void __launch_bounds__(kSortThreads, 1) k_scatter2(const __grid_const
     pdl_entry();
     extern __shared__ int cnt[];
     const int c = blockIdx.x;
+    const int nincl = *P.nincl;  // positions of the i1 order in use
     chunk_stable_ranks(
         c, P.nnz, P.n2, cnt,
         [&](int64_t k) {
+            if (k >= nincl) return -1;
             const int n = P.pi1[k];
             return P.tables[table_of_bag(P, P.lk_bag[n])].base2 + P.lk_i2[n];
         },
@@ -284,11 +290,12 @@ __global__ void __launch_bounds__(kSmallChunk) k_decode_small(const __grid_const
     if (n < hi) {
         const int64_t bag = nst ? staged_bag(soff, sb[0], nst, n) : bag_of(P, n);
         int t, i1, i2, i3;
-        decode_lookup(P, n, (int)bag, row, wv, t, i1, i2, i3, epoch);
-        const TableDev& T = P.tables[t];
-        d[0] = T.base1 + i1;
-        d[1] = T.base2 + i2;
-        d[2] = T.base3 + i3;
+        if (decode_lookup(P, n, (int)bag, row, wv, t, i1, i2, i3, epoch)) {
+            const TableDev& T = P.tables[t];
+            d[0] = T.base1 + i1;
+            d[1] = T.base2 + i2;
+            d[2] = T.base3 + i3;
+        }
     }
     const int lane = threadIdx.x & 31, w = threadIdx.x >> 5;
     const int nbs[3] = {P.n1, P.n2, P.n3};

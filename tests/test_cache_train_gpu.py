@@ -73,11 +73,12 @@ def _rows_run(wl):
     return run, rows
 
 
-@pytest.mark.parametrize("policy", ["lfu", "rows"])
-def test_two_sgd_steps(workloads, policy):
-    """Zipf weighted-mean workload (11M x 64, rank 32), 512 bags: forward, SGD step, forward;
-    an LFU cache of 1024 rows, or the 110,000 hot rows given explicitly."""
-    wl = workloads(3, 512)
+@pytest.mark.parametrize("policy,batch", [("lfu", 512), ("rows", 512), ("rows", None)])
+def test_two_sgd_steps(workloads, policy, batch):
+    """Zipf weighted-mean workload (11M x 64, rank 32): forward, SGD step, forward; an LFU
+    cache of 1024 rows or the 110,000 hot rows given explicitly; 512 bags (10k lookups,
+    the small grouping path) or all 4096 bags (82k lookups, the large one)."""
+    wl = workloads(3, batch)
     run, rows = _lfu_run(wl) if policy == "lfu" else _rows_run(wl)
     live = rows >= 0
     assert np.isin(wl.indices, rows[live]).mean() > 0.3
@@ -214,10 +215,6 @@ def test_trainable_cache_argument_and_state_errors(workloads):
     assert lib.tt_emb_cache_set_trainable(run.h, 2, None) == tt.TT_ERR_ARG
     assert lib.tt_emb_cache_read(run.h, None, tt._ptr(buf), None) == tt.TT_ERR_STATE  # not trainable
     assert lib.tt_emb_cache_write(run.h, tt._ptr(buf), None) == tt.TT_ERR_STATE
-    state = [torch.zeros_like(c) for c in run.cores[0]]
-    tt.tt_emb_set_optimizer(run.h, tt.TT_OPT_ADAGRAD, 0.0, state)
-    assert lib.tt_emb_cache_set_trainable(run.h, 1, None) == tt.TT_ERR_ARG  # Adagrad with eps = 0
-    tt.tt_emb_set_optimizer(run.h, tt.TT_OPT_SGD)
     assert lib.tt_emb_cache_set_trainable(run.h, 1, None) == tt.TT_OK
     assert lib.tt_emb_cache_write(run.h, None, None) == tt.TT_ERR_ARG
     run.close()
