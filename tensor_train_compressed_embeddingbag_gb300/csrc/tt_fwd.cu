@@ -16,6 +16,7 @@ constexpr int kFwdThreads = 256;
 constexpr int kListCap = 1024;      // touched i1 handled per round
 constexpr int kPoolWarps = 4;       // warps per bag
 constexpr int kPoolPer = 3;         // lookups of a warp whose T and G3 loads are in flight together
+constexpr int kPoolWarpBag = 4;     // average bag length up to which a warp takes a whole bag
 constexpr int kMaxDPerLane = 8;     // generic pool path: D <= 256
 constexpr int kScatterParts = kSmallChunk / (kPoolWarps * 32);  // grouping-scatter blocks per chunk
 static_assert(kScatterParts * kPoolWarps * 32 == kSmallChunk, "scatter parts cover a chunk");
@@ -421,10 +422,11 @@ __device__ __forceinline__ const float* t_of_pair(const Params& P, const TableDe
 // Exact-copy cache: the lookups that the decode chose to refresh a stale cached row
 // (one per row and pass, lk_hit = -2 - slot) recompute the row from T and G3 and
 // write it back with the pass's stamp.  A warp per lookup, lanes over columns.
-__device__ void cache_refresh_rows(const Params& P, const TableDev& T, int64_t lo, int64_t hi) {
-    const int lane = threadIdx.x & 31, w = threadIdx.x >> 5;
+// first / step: the warp's share of the bag's lookups.
+__device__ void cache_refresh_rows(const Params& P, const TableDev& T, int64_t first, int64_t hi, int step) {
+    const int lane = threadIdx.x & 31;
     const int q3 = T.q3, r2 = T.r2, D = T.D;
-    for (int64_t n = lo + w; n < hi; n += kPoolWarps) {
+    for (int64_t n = first; n < hi; n += step) {
         const int code = P.lk_hit[n];
         if (code > -2) continue;
         const int64_t slot = -2 - (int64_t)code;
@@ -443,8 +445,9 @@ __device__ void cache_refresh_rows(const Params& P, const TableDev& T, int64_t l
 // Static fast path: lanes = 2 output halves (lj) x 16 contraction lanes (lc);
 // lane (lj, lc) sums c = lc, lc + 16, ... for the outputs j = lj * D/2 + v.
 // After the bag, a reduce-scatter over the 16 lc lanes leaves V = D/32 sums
-// per lane.
-template <class Dm>
+// per lane.  WARP: one warp takes the whole bag and stores its row (short bags);
+// else the block's kPoolWarps warps share the bag and sum through `red`.
+template <class Dm, bool WARP>
 __device__ void pool_bag_static(const Params& P, const TableDev& T, int64_t bag, int64_t lo, int64_t hi,
                                 float* red) {
     constexpr int Q3 = Dm::q3(), R2 = Dm::r2(), Q12 = Dm::q1() * Dm::q2();
@@ -457,8 +460,10 @@ __device__ void pool_bag_static(const Params& P, const TableDev& T, int64_t bag,
     {
         // warp w takes lookups lo + w + kPoolWarps l; lane l first loads the indices of the
         // warp's l-th lookup of a round (one pass), then the warp walks them kPoolPer at a time
-        for (int64_t nb0 = lo; nb0 < hi; nb0 += 32 * kPoolWarps) {
-            const int64_t nl = nb0 + w + (int64_t)kPoolWarps * lane;
+        constexpr int NW = WARP ? 1 : kPoolWarps;  // warps sharing the bag
+        const int wb = WARP ? 0 : w;                // this warp's rank among them
+        for (int64_t nb0 = lo; nb0 < hi; nb0 += 32 * NW) {
+            const int64_t nl = nb0 + wb + (int64_t)NW * lane;
             int i1l = 0, i2l = 0, i3l = 0;
             float sl = 0.f;
             if (nl < hi) {
@@ -468,8 +473,8 @@ __device__ void pool_bag_static(const Params& P, const TableDev& T, int64_t bag,
                 sl = P.lk_s[nl];
                 if (P.cache_n > 0 && P.lk_hit[nl] >= 0) sl = 0.f;  // read from the cache below
             }
-            const int64_t left = hi - nb0 - w;  // this warp's lookups nb0 + w + kPoolWarps l < hi
-            const int64_t c64 = left <= 0 ? 0 : (left + kPoolWarps - 1) / kPoolWarps;
+            const int64_t left = hi - nb0 - wb;  // this warp's lookups nb0 + wb + NW l < hi
+            const int64_t c64 = left <= 0 ? 0 : (left + NW - 1) / NW;
             const int cnt = c64 > 32 ? 32 : (int)c64;
             for (int l = 0; l < cnt; l += kPoolPer) {
                 // kPoolPer lookups of this warp: their T and G3 values are all in flight together
@@ -531,8 +536,10 @@ __device__ void pool_bag_static(const Params& P, const TableDev& T, int64_t bag,
         }
     }
     constexpr int V = H / 16;
+    const int64_t first = lo + (WARP ? 0 : w);
+    const int step = WARP ? 1 : kPoolWarps;
     if (P.cache_n > 0) {  // cache hits: s times the cached value, V columns a lane
-        for (int64_t n = lo + w; n < hi; n += kPoolWarps) {
+        for (int64_t n = first; n < hi; n += step) {
             const int slot = P.lk_hit[n];
             if (slot < 0) continue;
             const float sh = P.lk_sh[n];
@@ -541,27 +548,36 @@ __device__ void pool_bag_static(const Params& P, const TableDev& T, int64_t bag,
             for (int v = 0; v < V; ++v) acc[v] = fmaf(sh, __ldcg(cv + v), acc[v]);
         }
     }
-    if (P.cache_n > 0 && !P.cache_train) cache_refresh_rows(P, T, lo, hi);
+    if (P.cache_n > 0 && !P.cache_train) cache_refresh_rows(P, T, first, hi, step);
+    if constexpr (WARP) {
+        float* o = P.out + bag * D + lj * H + lc * V;
 #pragma unroll
-    for (int v = 0; v < V; ++v) red[w * D + lj * H + lc * V + v] = acc[v];
-    __syncthreads();
-    for (int j = threadIdx.x; j < D; j += blockDim.x) {
-        float sum = 0.f;
+        for (int v = 0; v < V; ++v) o[v] = acc[v];
+    } else {
 #pragma unroll
-        for (int ww = 0; ww < kPoolWarps; ++ww) sum += red[ww * D + j];
-        P.out[bag * D + j] = sum;
+        for (int v = 0; v < V; ++v) red[w * D + lj * H + lc * V + v] = acc[v];
+        __syncthreads();
+        for (int j = threadIdx.x; j < D; j += blockDim.x) {
+            float sum = 0.f;
+#pragma unroll
+            for (int ww = 0; ww < kPoolWarps; ++ww) sum += red[ww * D + j];
+            P.out[bag * D + j] = sum;
+        }
     }
 }
 
-// Generic path: lanes over output columns, loop over c.
+// Generic path: lanes over output columns, loop over c.  WARP as for the static path.
+template <bool WARP>
 __device__ void pool_bag_generic(const Params& P, const TableDev& T, int64_t bag, int64_t lo, int64_t hi,
                                  float* red) {
     const int lane = threadIdx.x & 31, w = threadIdx.x >> 5;
     const int q3 = T.q3, r2 = T.r2, D = T.D;
+    const int64_t first = lo + (WARP ? 0 : w);
+    const int step = WARP ? 1 : kPoolWarps;
     float acc[kMaxDPerLane];
 #pragma unroll
     for (int m = 0; m < kMaxDPerLane; ++m) acc[m] = 0.f;
-    for (int64_t n = lo + w; n < hi; n += kPoolWarps) {
+    for (int64_t n = first; n < hi; n += step) {
         const int i1 = P.lk_i1[n], i2 = P.lk_i2[n], i3 = P.lk_i3[n];
         const float s = (P.cache_n > 0 && P.lk_hit[n] >= 0) ? 0.f : P.lk_s[n];  // a hit reads the cache below
         const float* Tp = t_of_pair(P, T, i2, i1);
@@ -588,44 +604,66 @@ __device__ void pool_bag_generic(const Params& P, const TableDev& T, int64_t bag
             }
         }
     }
-    if (P.cache_n > 0 && !P.cache_train) cache_refresh_rows(P, T, lo, hi);
+    if (P.cache_n > 0 && !P.cache_train) cache_refresh_rows(P, T, first, hi, step);
+    if constexpr (WARP) {
 #pragma unroll
-    for (int m = 0; m < kMaxDPerLane; ++m) {
-        const int j = lane + 32 * m;
-        if (j < D) red[w * D + j] = acc[m];
-    }
-    __syncthreads();
-    for (int j = threadIdx.x; j < D; j += blockDim.x) {
-        float sum = 0.f;
-        for (int ww = 0; ww < kPoolWarps; ++ww) sum += red[ww * D + j];
-        P.out[bag * D + j] = sum;
+        for (int m = 0; m < kMaxDPerLane; ++m) {
+            const int j = lane + 32 * m;
+            if (j < D) P.out[bag * D + j] = acc[m];
+        }
+    } else {
+#pragma unroll
+        for (int m = 0; m < kMaxDPerLane; ++m) {
+            const int j = lane + 32 * m;
+            if (j < D) red[w * D + j] = acc[m];
+        }
+        __syncthreads();
+        for (int j = threadIdx.x; j < D; j += blockDim.x) {
+            float sum = 0.f;
+            for (int ww = 0; ww < kPoolWarps; ++ww) sum += red[ww * D + j];
+            P.out[bag * D + j] = sum;
+        }
     }
 }
 
-// One block of kPoolWarps warps per bag; the warps share the bag's lookups.
-// DC >= 0: every table of the handle has dimension class DC; DC < 0: per table.
-template <int DC>
-__global__ void __launch_bounds__(kPoolWarps * 32) k_pool(const __grid_constant__ Params P) {
-    pdl_entry();
-    __shared__ float red[kPoolWarps * kMaxD];
-    const int64_t bag = blockIdx.x;
-    if (bag >= P.nbags) {  // small path: extra blocks scatter the lookups of part of a chunk
-        const int e = (int)(bag - P.nbags);
-        scatter_chunk(P, e / kScatterParts, e % kScatterParts);
-        return;
-    }
-    if (bag == 0 && threadIdx.x == 0) atomicAdd(P.epoch, 1);  // k_fwd_T has finished reading it
+template <int DC, bool WARP>
+__device__ __forceinline__ void pool_one_bag(const Params& P, int64_t bag, float* red) {
     const TableDev& T = P.tables[table_of_bag(P, (int)bag)];
     int64_t lo = P.off[bag], hi = P.off[bag + 1];
     lo = lo < 0 ? 0 : (lo > P.nnz ? P.nnz : lo);
     hi = hi < lo ? lo : (hi > P.nnz ? P.nnz : hi);
+    // DC = -1: mixed classes of width 64 (no q3 = 8 class); -2: mixed, another width
     const int dc = DC >= 0 ? DC : T.dclass;
     switch (dc) {
-        case kQ444R32: pool_bag_static<SDims<4, 4, 4, 32, 32>>(P, T, bag, lo, hi, red); break;
-        case kQ444R16: pool_bag_static<SDims<4, 4, 4, 16, 16>>(P, T, bag, lo, hi, red); break;
-        case kQ444R64: pool_bag_static<SDims<4, 4, 4, 64, 64>>(P, T, bag, lo, hi, red); break;
-        case kQ448R64: pool_bag_static<SDims<4, 4, 8, 64, 64>>(P, T, bag, lo, hi, red); break;
-        default: pool_bag_generic(P, T, bag, lo, hi, red); break;
+        case kQ444R32: if constexpr (DC != -2) pool_bag_static<SDims<4, 4, 4, 32, 32>, WARP>(P, T, bag, lo, hi, red); break;
+        case kQ444R16: if constexpr (DC != -2) pool_bag_static<SDims<4, 4, 4, 16, 16>, WARP>(P, T, bag, lo, hi, red); break;
+        case kQ444R64: if constexpr (DC != -2) pool_bag_static<SDims<4, 4, 4, 64, 64>, WARP>(P, T, bag, lo, hi, red); break;
+        case kQ448R64: if constexpr (DC != -1) pool_bag_static<SDims<4, 4, 8, 64, 64>, WARP>(P, T, bag, lo, hi, red); break;
+        default: pool_bag_generic<WARP>(P, T, bag, lo, hi, red); break;
+    }
+}
+
+// Bags of more than kPoolWarpBag lookups on average: one block of kPoolWarps warps per
+// bag, the warps share the bag's lookups; shorter bags: one warp per bag.  Blocks past
+// the bags' run the grouping scatter of the small path.  DC >= 0: every table of the
+// handle has dimension class DC; DC < 0: per table.
+template <int DC>
+__global__ void __launch_bounds__(kPoolWarps * 32) k_pool(const __grid_constant__ Params P) {
+    pdl_entry();
+    __shared__ float red[kPoolWarps * kMaxD];
+    const bool warp_mode = P.nnz <= (int64_t)kPoolWarpBag * P.nbags;
+    const int64_t nbb = warp_mode ? (P.nbags + kPoolWarps - 1) / kPoolWarps : P.nbags;  // bag blocks
+    if ((int64_t)blockIdx.x >= nbb) {  // small path: extra blocks scatter the lookups of part of a chunk
+        const int e = (int)(blockIdx.x - nbb);
+        scatter_chunk(P, e / kScatterParts, e % kScatterParts);
+        return;
+    }
+    if (blockIdx.x == 0 && threadIdx.x == 0) atomicAdd(P.epoch, 1);  // k_fwd_T has finished reading it
+    if (warp_mode) {
+        const int64_t bag = (int64_t)blockIdx.x * kPoolWarps + (threadIdx.x >> 5);
+        if (bag < P.nbags) pool_one_bag<DC, true>(P, bag, red);
+    } else {
+        pool_one_bag<DC, false>(P, blockIdx.x, red);
     }
 }
 
@@ -683,7 +721,9 @@ cudaError_t launch_fwd_T(const Params& P, cudaStream_t s) {
 
 template <int DC>
 static cudaError_t launch_pool_dc(const Params& P, cudaStream_t s) {
-    cudaError_t le = launch_pdl(k_pool<DC>, dim3((unsigned)(P.nbags + (P.small ? (int64_t)P.nch * kScatterParts : 0))),
+    const bool warp_mode = P.nnz <= (int64_t)kPoolWarpBag * P.nbags;
+    const int64_t nbb = warp_mode ? (P.nbags + kPoolWarps - 1) / kPoolWarps : P.nbags;
+    cudaError_t le = launch_pdl(k_pool<DC>, dim3((unsigned)(nbb + (P.small ? (int64_t)P.nch * kScatterParts : 0))),
                                 dim3(kPoolWarps * 32), 0, s, P);
     if (le != cudaSuccess) return le;
     return cudaGetLastError();
@@ -696,7 +736,7 @@ cudaError_t launch_pool(const Params& P, cudaStream_t s) {
         case kQ444R64: return launch_pool_dc<kQ444R64>(P, s);
         case kQ448R64: return launch_pool_dc<kQ448R64>(P, s);
         case kDynamic: return launch_pool_dc<kDynamic>(P, s);
-        default: return launch_pool_dc<-1>(P, s);
+        default: return P.D == 64 ? launch_pool_dc<-1>(P, s) : launch_pool_dc<-2>(P, s);
     }
 }
 
@@ -992,7 +1032,7 @@ cudaError_t set_fwd_attributes(int max_smem) {
                         (const void*)k_fwd_T<kDynamic>, (const void*)k_fwd_T<-1>,
                         (const void*)k_pool<kQ444R32>, (const void*)k_pool<kQ444R16>,
                         (const void*)k_pool<kQ444R64>, (const void*)k_pool<kQ448R64>,
-                        (const void*)k_pool<kDynamic>, (const void*)k_pool<-1>, (const void*)k_cache_fill};
+                        (const void*)k_pool<kDynamic>, (const void*)k_pool<-1>, (const void*)k_pool<-2>, (const void*)k_cache_fill};
     for (const void* k : ks) {
         cudaError_t e = allow_max_dynamic_smem(k, max_smem);
         if (e != cudaSuccess) return e;

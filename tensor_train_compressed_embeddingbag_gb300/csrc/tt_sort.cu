@@ -62,16 +62,46 @@ __global__ void __launch_bounds__(kSortThreads, 1) k_decode_hist(const __grid_co
 
 // ------------------------------------------------------------------ scans
 
-// Returns the total.
+// Exclusive scan of a[0, L) in place by one block; returns the total.  Each thread
+// takes kScanPer consecutive elements per round (int4 loads; `a` is 16-byte aligned),
+// so one block scan covers blockDim * kScanPer elements.
+constexpr int kScanPer = 16;
+
 __device__ int scan_inplace(int* a, int64_t L, int* sh) {
     int carry = 0;
-    for (int64_t base = 0; base < L; base += blockDim.x) {
-        const int64_t i = base + threadIdx.x;
-        const int v = i < L ? a[i] : 0;
+    for (int64_t base = 0; base < L; base += (int64_t)blockDim.x * kScanPer) {
+        const int64_t i0 = base + (int64_t)threadIdx.x * kScanPer;
+        int v[kScanPer];
+        if (i0 + kScanPer <= L) {
+#pragma unroll
+            for (int q = 0; q < kScanPer / 4; ++q) {
+                const int4 x = reinterpret_cast<const int4*>(a + i0)[q];
+                v[4 * q] = x.x; v[4 * q + 1] = x.y; v[4 * q + 2] = x.z; v[4 * q + 3] = x.w;
+            }
+        } else {
+#pragma unroll
+            for (int e = 0; e < kScanPer; ++e) v[e] = i0 + e < L ? a[i0 + e] : 0;
+        }
+        int tot = 0;
+#pragma unroll
+        for (int e = 0; e < kScanPer; ++e) {
+            const int x = v[e];
+            v[e] = tot;
+            tot += x;
+        }
         int total;
-        const int ex = block_scan_excl(v, sh, &total);
-        if (i < L) a[i] = carry + ex;
+        const int ex = carry + block_scan_excl(tot, sh, &total);
+        if (i0 + kScanPer <= L) {
+#pragma unroll
+            for (int q = 0; q < kScanPer / 4; ++q)
+                reinterpret_cast<int4*>(a + i0)[q] = make_int4(ex + v[4 * q], ex + v[4 * q + 1], ex + v[4 * q + 2], ex + v[4 * q + 3]);
+        } else {
+#pragma unroll
+            for (int e = 0; e < kScanPer; ++e)
+                if (i0 + e < L) a[i0 + e] = ex + v[e];
+        }
         carry += total;
+        __syncthreads();  // sh is reused by the next round's block scan
     }
     return carry;
 }

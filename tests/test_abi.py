@@ -91,6 +91,11 @@ def test_null_arguments_rejected(lib):
     assert lib.tt_emb_lfu_enable(None, 64, 64) == tt.TT_ERR_ARG
     assert lib.tt_emb_lfu_populate(None, None) == tt.TT_ERR_ARG
     assert lib.tt_emb_lfu_disable(None) == tt.TT_ERR_ARG
+    assert lib.tt_emb_cache_set_trainable(None, 1, None) == tt.TT_ERR_ARG
+    assert lib.tt_emb_cache_read(None, None, None, None) == tt.TT_ERR_ARG
+    assert lib.tt_emb_cache_write(None, None, None) == tt.TT_ERR_ARG
+    assert lib.tt_emb_cache_populate(None, None, 0, None) == tt.TT_ERR_ARG
+    assert lib.tt_emb_cache_disable(None) == tt.TT_ERR_ARG
     assert lib.tt_emb_reserve(None, 1, 1) == tt.TT_ERR_ARG
     assert lib.tt_emb_get_last_error(None) == tt.TT_ERR_ARG
     assert lib.tt_emb_last_launch_count(None, 0) == -1
