@@ -151,6 +151,7 @@ size_t carve(tt_emb* h, void* base, int64_t nnz, bool assign) {
     int* g_p1 = A.take<int>(N);
     int* g_p3 = A.take<int>(N);
     int* inv3 = A.take<int>(N);
+    int* segsum = A.take<int>((size_t)(((int64_t)(P.n1 + P.n2 + P.n3) * nch) / kScanSeg + 4));
     float* Qbuf = A.take<float>(qslots * P.qs_max);
     float* Pbuf = A.take<float>((size_t)N * P.ps_max);
     float* dG2part = A.take<float>(part_floats);
@@ -162,7 +163,7 @@ size_t carve(tt_emb* h, void* base, int64_t nnz, bool assign) {
         P.pi1 = pi1; P.pi3 = pi3; P.pi21 = pi21; P.sigma = sigma;
         P.g_i1 = g_i1; P.g_i3 = g_i3; P.g_bag = g_bag; P.g_s = g_s;
         P.tiles = tiles; P.grp_first = grp_first; P.grp_ntiles = grp_ntiles;
-        P.rep1 = rep1; P.rep3 = rep3; P.g_p1 = g_p1; P.g_p3 = g_p3; P.inv3 = inv3;
+        P.rep1 = rep1; P.rep3 = rep3; P.g_p1 = g_p1; P.g_p3 = g_p3; P.inv3 = inv3; P.segsum = segsum;
         P.Qbuf = Qbuf; P.Pbuf = Pbuf; P.dG2part = dG2part;
     }
     return A.used + 256;
@@ -346,6 +347,7 @@ tt_status build_handle(tt_emb* h, int ntab, const tt_table_desc* d) {
     P.epoch = h->d_fixed + 4;
     P.dstep = h->d_fixed + 5;
     P.nincl = h->d_fixed + 6;
+    P.scan_done = h->d_fixed + 7;
     P.grp_done = h->d_fixed + 8;
     P.Tbuf = h->d_tbuf;
     P.tflag = h->d_tflag;
@@ -551,8 +553,10 @@ tt_status tt_emb_forward(tt_emb* h, const int64_t* indices, int64_t nnz, const i
             q.run("decode", launch_decode_small);
         } else {
             q.run("decode_hist", launch_decode_hist);
+            if (scan_segments(P, 0) > 2) q.run("scan_sums13", launch_scan_sums13);
             q.run("scan13", launch_scan13);
             q.run("scatter13", launch_scatter13);
+            if (scan_segments(P, 1) > 1) q.run("scan_sums2", launch_scan_sums2);
             q.run("scan2_tiles", launch_scan2_tiles);
             q.run("scatter2", launch_scatter2);
         }

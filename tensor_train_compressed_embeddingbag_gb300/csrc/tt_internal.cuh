@@ -35,6 +35,8 @@ constexpr int kSortThreads = 256;   // 8 warps; each warp owns kChunk/8 consecut
 constexpr int kSortWarps = kSortThreads / 32;
 constexpr int kWarpSpan = kChunk / kSortWarps;
 constexpr int kScanThreads = 1024;
+constexpr int kScanPer = 16;                       // histogram elements per thread and round of a scan
+constexpr int kScanSeg = kScanThreads * kScanPer;  // histogram elements per block of the scans
 constexpr int kTileThreads = 256;
 constexpr int kMaxBinsPerDigit = 6144;  // per-warp rank tables: 8 x bins x 4 B of shared memory
 constexpr int kFieldBits = 20;          // bits per field of the in-tile sort key
@@ -141,6 +143,8 @@ struct Params {
     float* dG2part;                 // [max_tiles][s2_max]
     int* counters;                  // spare device counters
     int* nincl;                     // lookups in the sorted orders (all but the trainable cache hits)
+    int* segsum;                    // segment totals of the multi-block histogram scans
+    int* scan_done;                 // blocks of the H2 scan that have finished (0 between passes)
     int* err;
     // hot-row cache (single table)
     const int64_t* cache_rows;      // row id per slot (-1 = empty way)
@@ -584,6 +588,10 @@ inline cudaError_t launch_pdl(void (*kernel)(Args...), dim3 grid, dim3 block, si
 cudaError_t launch_decode_small(const Params& P, cudaStream_t s);
 cudaError_t launch_decode_hist(const Params& P, cudaStream_t s);
 cudaError_t launch_scan13(const Params& P, cudaStream_t s);
+cudaError_t launch_scan_sums13(const Params& P, cudaStream_t s);
+cudaError_t launch_scan_sums2(const Params& P, cudaStream_t s);
+// Blocks of the histogram scans: W = 0 the H1 and H3 segments (*s1 = H1's), W = 1 H2's.
+int scan_segments(const Params& P, int W, int* s1 = nullptr);
 cudaError_t launch_scatter13(const Params& P, cudaStream_t s);
 cudaError_t launch_scan2_tiles(const Params& P, cudaStream_t s);
 cudaError_t launch_scatter2(const Params& P, cudaStream_t s);

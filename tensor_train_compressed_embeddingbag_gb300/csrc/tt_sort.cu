@@ -62,13 +62,10 @@ __global__ void __launch_bounds__(kSortThreads, 1) k_decode_hist(const __grid_co
 
 // ------------------------------------------------------------------ scans
 
-// Exclusive scan of a[0, L) in place by one block; returns the total.  Each thread
-// takes kScanPer consecutive elements per round (int4 loads; `a` is 16-byte aligned),
-// so one block scan covers blockDim * kScanPer elements.
-constexpr int kScanPer = 16;
-
-__device__ int scan_inplace(int* a, int64_t L, int* sh) {
-    int carry = 0;
+// Exclusive scan of a[0, L) in place by one block, starting from `carry`; returns
+// carry + the total.  Each thread takes kScanPer consecutive elements per round (int4
+// loads; `a` is 16-byte aligned), so one block scan covers blockDim * kScanPer elements.
+__device__ int scan_inplace(int* a, int64_t L, int* sh, int carry) {
     for (int64_t base = 0; base < L; base += (int64_t)blockDim.x * kScanPer) {
         const int64_t i0 = base + (int64_t)threadIdx.x * kScanPer;
         int v[kScanPer];
@@ -106,29 +103,94 @@ __device__ int scan_inplace(int* a, int64_t L, int* sh) {
     return carry;
 }
 
-__global__ void __launch_bounds__(kScanThreads) k_scan13(const __grid_constant__ Params P) {
-    pdl_entry();
-    __shared__ int sh[33];
-    const int total = scan_inplace(P.H1, (int64_t)P.n1 * P.nch, sh);
-    scan_inplace(P.H3, (int64_t)P.n3 * P.nch, sh);
-    if (threadIdx.x == 0) *P.nincl = total;
+// The [digit][chunk] histograms are scanned in segments of kScanSeg elements, a block
+// per segment: W = 0 covers H1 then H3 (the sorts by i1 and i3), W = 1 covers H2.
+// Block b's array, its length, the segment's index in it and the index of the
+// array's first segment.
+int scan_segments(const Params& P, int W, int* s1) {
+    const auto segs = [](int64_t L) { return (int)std::max<int64_t>(1, (L + kScanSeg - 1) / kScanSeg); };
+    const int a = segs((int64_t)(W == 0 ? P.n1 : P.n2) * P.nch);
+    if (s1) *s1 = a;
+    return W == 0 ? a + segs((int64_t)P.n3 * P.nch) : a;
 }
 
-// Exclusive scan of H2, then the tiles: each (table, i2) group of `cnt`
-// lookups (contiguous in pi21) is cut into ceil(cnt / tile_cap) tiles.
-__global__ void __launch_bounds__(kScanThreads) k_scan2_tiles(const __grid_constant__ Params P) {
+template <int W>
+__device__ __forceinline__ void scan_segment_of(const Params& P, int b, int*& a, int64_t& L, int& seg, int& base) {
+    const int64_t L1 = (int64_t)(W == 0 ? P.n1 : P.n2) * P.nch;
+    const int s1 = (int)((L1 + kScanSeg - 1) / kScanSeg);
+    if (W == 1 || b < (s1 > 0 ? s1 : 1)) {
+        a = W == 0 ? P.H1 : P.H2;
+        L = L1;
+        seg = b;
+        base = 0;
+    } else {
+        a = P.H3;
+        L = (int64_t)P.n3 * P.nch;
+        seg = b - (s1 > 0 ? s1 : 1);
+        base = s1 > 0 ? s1 : 1;
+    }
+}
+
+// Pass 1 (only when some array has several segments): each block's segment total
+// into segsum.
+template <int W>
+__global__ void __launch_bounds__(kScanThreads) k_scan_sums(const __grid_constant__ Params P) {
     pdl_entry();
     __shared__ int sh[33];
-    scan_inplace(P.H2, (int64_t)P.n2 * P.nch, sh);
+    int* a;
+    int64_t L;
+    int seg, base;
+    scan_segment_of<W>(P, blockIdx.x, a, L, seg, base);
+    const int64_t lo = (int64_t)seg * kScanSeg, hi = lo + kScanSeg < L ? lo + kScanSeg : L;
+    int sum = 0;
+    for (int64_t i = lo + threadIdx.x; i < hi; i += blockDim.x) sum += a[i];
+    int total;
+    block_scan_excl(sum, sh, &total);
+    if (threadIdx.x == 0) P.segsum[blockIdx.x] = total;
+}
+
+// Pass 2: each block scans its segment from the sum of the earlier segments of its
+// array.  W = 0: the block with H1's last segment stores the count of lookups in the
+// sorted orders.  W = 1: the last block to finish (a counter, no waiting) cuts each
+// (table, i2) group of `cnt` lookups (contiguous in pi21) into ceil(cnt / tile_cap)
+// tiles.
+template <int W>
+__global__ void __launch_bounds__(kScanThreads) k_scan_apply(const __grid_constant__ Params P) {
+    pdl_entry();
+    __shared__ int sh[33];
+    __shared__ int last;
+    int* a;
+    int64_t L;
+    int seg, base;
+    scan_segment_of<W>(P, blockIdx.x, a, L, seg, base);
+    int part = 0;
+    for (int k = threadIdx.x; k < seg; k += blockDim.x) part += P.segsum[base + k];
+    int offset;
+    block_scan_excl(part, sh, &offset);
     __syncthreads();
+    const int64_t lo = (int64_t)seg * kScanSeg;
+    const int64_t n = lo < L ? (lo + kScanSeg < L ? kScanSeg : L - lo) : 0;
+    const int end = scan_inplace(a + lo, n, sh, offset);
+    if (W == 0) {
+        if (a == P.H1 && lo + kScanSeg >= L && threadIdx.x == 0) *P.nincl = end;
+        return;
+    }
+    __syncthreads();
+    if (threadIdx.x == 0) {
+        __threadfence();
+        last = atomicAdd(P.scan_done, 1) == (int)gridDim.x - 1;
+    }
+    __syncthreads();
+    if (!last) return;
+    __threadfence();
     int carry = 0;
-    for (int base = 0; base < P.n2; base += blockDim.x) {
-        const int g = base + threadIdx.x;
+    for (int gb = 0; gb < P.n2; gb += blockDim.x) {
+        const int g = gb + threadIdx.x;
         int start = 0, cnt = 0, nt = 0;
         if (g < P.n2) {
-            start = P.H2[(int64_t)g * P.nch];
-            const int end = (g + 1 < P.n2) ? P.H2[(int64_t)(g + 1) * P.nch] : *P.nincl;
-            cnt = end - start;
+            start = __ldcg(P.H2 + (int64_t)g * P.nch);
+            const int e = (g + 1 < P.n2) ? __ldcg(P.H2 + (int64_t)(g + 1) * P.nch) : *P.nincl;
+            cnt = e - start;
             nt = (cnt + P.tile_cap - 1) / P.tile_cap;
         }
         int total;
@@ -140,8 +202,12 @@ __global__ void __launch_bounds__(kScanThreads) k_scan2_tiles(const __grid_const
                 P.tiles[first + k] = make_int4(start + k * P.tile_cap, min(P.tile_cap, cnt - k * P.tile_cap), g, k);
         }
         carry += total;
+        __syncthreads();
     }
-    if (threadIdx.x == 0) *P.ntiles = carry;
+    if (threadIdx.x == 0) {
+        *P.ntiles = carry;
+        *P.scan_done = 0;  // ready for the next pass
+    }
 }
 
 // ------------------------------------------------------------------ scatters
@@ -370,8 +436,20 @@ cudaError_t launch_decode_hist(const Params& P, cudaStream_t s) {
     return cudaGetLastError();
 }
 
+cudaError_t launch_scan_sums13(const Params& P, cudaStream_t s) {
+    cudaError_t le = launch_pdl(k_scan_sums<0>, dim3(scan_segments(P, 0)), dim3(kScanThreads), 0, s, P);
+    if (le != cudaSuccess) return le;
+    return cudaGetLastError();
+}
+
 cudaError_t launch_scan13(const Params& P, cudaStream_t s) {
-    cudaError_t le = launch_pdl(k_scan13, dim3(1), dim3(kScanThreads), 0, s, P);
+    cudaError_t le = launch_pdl(k_scan_apply<0>, dim3(scan_segments(P, 0)), dim3(kScanThreads), 0, s, P);
+    if (le != cudaSuccess) return le;
+    return cudaGetLastError();
+}
+
+cudaError_t launch_scan_sums2(const Params& P, cudaStream_t s) {
+    cudaError_t le = launch_pdl(k_scan_sums<1>, dim3(scan_segments(P, 1)), dim3(kScanThreads), 0, s, P);
     if (le != cudaSuccess) return le;
     return cudaGetLastError();
 }
@@ -384,7 +462,7 @@ cudaError_t launch_scatter13(const Params& P, cudaStream_t s) {
 }
 
 cudaError_t launch_scan2_tiles(const Params& P, cudaStream_t s) {
-    cudaError_t le = launch_pdl(k_scan2_tiles, dim3(1), dim3(kScanThreads), 0, s, P);
+    cudaError_t le = launch_pdl(k_scan_apply<1>, dim3(scan_segments(P, 1)), dim3(kScanThreads), 0, s, P);
     if (le != cudaSuccess) return le;
     return cudaGetLastError();
 }
@@ -398,7 +476,8 @@ cudaError_t launch_scatter2(const Params& P, cudaStream_t s) {
 
 cudaError_t set_sort_attributes(int max_smem) {
     const void* ks[] = {(const void*)k_decode_hist, (const void*)k_scatter13, (const void*)k_scatter2,
-                        (const void*)k_decode_small, (const void*)k_scan13, (const void*)k_scan2_tiles};
+                        (const void*)k_decode_small, (const void*)k_scan_sums<0>, (const void*)k_scan_sums<1>,
+                        (const void*)k_scan_apply<0>, (const void*)k_scan_apply<1>};
     for (const void* k : ks) {
         cudaError_t e = allow_max_dynamic_smem(k, max_smem);
         if (e != cudaSuccess) return e;
