@@ -108,20 +108,20 @@ def check_forward(out_gpu, wl, bags=None):
     assert_rows_close(got, ref, "forward")
 
 
-def check_cores(run, wl, dec, slices=None, before=None):
-    """Updated cores vs oracle on `slices` (per table, per core; None = all);
-    slices no lookup touched must keep their exact bits."""
+def check_cores(run, wl, dec, slices=None):
+    """Updated cores vs oracle on `slices` (per table, per core; None = all) after one
+    step from the workload's cores; slices no lookup touched must keep their exact bits."""
     after = run.cores_host()
     touched = touched_slices(wl, dec)
     for t in range(wl.num_tables):
         for k in range(3):
-            init = wl.cores[t][k] if before is None else before[t][k]
+            init = wl.cores[t][k]
             un = np.setdiff1d(np.arange(wl.tables[t].p[k]), touched[t][k])
             np.testing.assert_array_equal(after[t][k][un], init[un], err_msg=f"untouched slices t{t} G{k + 1}")
             sl = touched[t][k] if slices is None else np.asarray(slices[t][k], dtype=np.int64)
             if sl.size == 0:
                 continue
-            ref = oracle.workload_sgd_slices(wl, t, k, sl, cores=before)
+            ref = oracle.workload_sgd_slices(wl, t, k, sl)
             assert_rows_close(after[t][k][sl], ref, f"table {t} core G{k + 1}")
 
 

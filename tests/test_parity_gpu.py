@@ -10,6 +10,7 @@ import numpy as np
 import pytest
 import torch
 
+import oracle
 import tensor_train_compressed_embeddingbag_gb300 as tt
 from tt_inputs import TableSpec, Workload, config
 
@@ -86,12 +87,13 @@ def test_table_batched_full_sampled(workloads):
 
 @pytest.mark.parametrize("batch", [64, 4096])
 def test_cache_gives_same_results(workloads, batch):
-    """With the hot-row cache (Zipf, weighted mean), two steps match the oracle."""
+    """With the hot-row cache (Zipf, weighted mean), two steps match the oracle (at 64 bags
+    the oracle's own cores after each step, every bag and slice) and the run without cache."""
     wl = workloads(3, batch)
     run = GpuRun(wl, cache=True)
     ref_run = GpuRun(wl, cache=False)
+    ref_cores = [c.astype(np.float64) for c in wl.cores[0]]
     for step in range(2):
-        before = run.cores_host()
         out = run.forward().cpu().numpy()
         ref = ref_run.forward().cpu().numpy()
         dec = check_decode(run, wl)
@@ -100,12 +102,15 @@ def test_cache_gives_same_results(workloads, batch):
         assert run.error() == tt.TT_OK and ref_run.error() == tt.TT_OK
         assert_rows_close(out, ref, f"cache vs no cache, step {step}")
         if batch <= 64:
-            check_forward(out, Workload(**{**wl.__dict__, "cores": before}))
-            check_cores(run, wl, dec, before=before)
+            assert_rows_close(out, oracle.workload_forward(wl, cores=[ref_cores]), f"forward, step {step}")
         else:
-            rng = np.random.default_rng(step)
-            bags = rng.choice(wl.num_bags, 128, replace=False)
-            check_forward(out, Workload(**{**wl.__dict__, "cores": before}), bags)
+            bags = np.random.default_rng(step).choice(wl.num_bags, 128, replace=False)
+            assert_rows_close(out[bags], oracle.workload_forward(wl, bags=bags, cores=[ref_cores]), f"forward, step {step}")
+        ref_cores = oracle.sgd_step(wl.tables, [ref_cores], wl.indices, wl.offsets, wl.grad_out, wl.lr,
+                                    wl.weights, wl.mode)[0]
+        got = run.cores_host()[0]
+        for k in range(3):
+            assert_rows_close(got[k], ref_cores[k], f"step {step} G{k + 1}")
     run.close()
     ref_run.close()
 
@@ -150,6 +155,32 @@ def test_repeated_rows_span_tiles():
 def test_odd_shapes(q, r):
     rng = np.random.default_rng(3)
     full_parity(synthetic([5, 7, 3], q, r, rng.integers(0, 6, size=40), seed=3, E=100, weights=True))
+
+
+@pytest.mark.parametrize("q,r", [([2, 2, 2], [4, 4]), ([4, 4, 4], [32, 32])])
+def test_cache_short_bags(q, r):
+    """Bags of 1-3 lookups (a warp per bag in the pool; generic and rank-32 paths) with the
+    exact-copy cache of the 40 most frequent rows: three SGD steps, each checked twice
+    (stale rows refreshed, then read fresh) against the oracle's own chain of steps."""
+    rng = np.random.default_rng(5)
+    wl = synthetic([6, 5, 7], q, r, rng.integers(1, 4, size=300), seed=5, weights=True, mode="mean")
+    rows, counts = np.unique(wl.indices, return_counts=True)
+    hot = rows[np.argsort(-counts, kind="stable")[:40]]
+    run = GpuRun(wl)
+    tt.tt_emb_cache_populate(run.h, dev(hot))
+    ref_cores = [c.astype(np.float64) for c in wl.cores[0]]
+    for step in range(3):
+        ref = oracle.workload_forward(wl, cores=[ref_cores])
+        assert_rows_close(run.forward().cpu().numpy(), ref, f"step {step}, rows refreshed")
+        assert_rows_close(run.forward().cpu().numpy(), ref, f"step {step}, rows read")
+        run.backward()
+        assert run.error() == tt.TT_OK
+        ref_cores = oracle.sgd_step(wl.tables, [ref_cores], wl.indices, wl.offsets, wl.grad_out, wl.lr,
+                                    wl.weights, wl.mode)[0]
+        got = run.cores_host()[0]
+        for k in range(3):
+            assert_rows_close(got[k], ref_cores[k], f"step {step} G{k + 1}")
+    run.close()
 
 
 def test_padding_rows_and_last_row():
@@ -250,12 +281,17 @@ def test_workspace_reuse_across_sizes(workloads):
     """One handle, calls of growing and shrinking sizes (workspace regrowth)."""
     small, big = workloads(3, 64), workloads(3, 512)
     run = GpuRun(small)
-    for wl in (small, big, small):
+    ref_cores = [c.astype(np.float64) for c in small.cores[0]]
+    for i, wl in enumerate((small, big, small)):
         run.wl = wl
         run.idx, run.off, run.w, run.go = dev(wl.indices), dev(wl.offsets), dev(wl.weights), dev(wl.grad_out)
-        before = run.cores_host()
         out = run.forward().cpu().numpy()
-        check_forward(out, Workload(**{**wl.__dict__, "cores": before}))
+        assert_rows_close(out, oracle.workload_forward(wl, cores=[ref_cores]), f"call {i}")
         run.backward()
         assert run.error() == tt.TT_OK
+        ref_cores = oracle.sgd_step(wl.tables, [ref_cores], wl.indices, wl.offsets, wl.grad_out, wl.lr,
+                                    wl.weights, wl.mode)[0]
+    got = run.cores_host()[0]
+    for k in range(3):
+        assert_rows_close(got[k], ref_cores[k], f"G{k + 1} after three calls")
     run.close()
