@@ -447,7 +447,7 @@ __device__ void cache_refresh_rows(const Params& P, const TableDev& T, int64_t f
 // After the bag, a reduce-scatter over the 16 lc lanes leaves V = D/32 sums
 // per lane.  WARP: one warp takes the whole bag and stores its row (short bags);
 // else the block's kPoolWarps warps share the bag and sum through `red`.
-template <class Dm, bool WARP>
+template <class Dm, bool WARP, bool CACHE>
 __device__ void pool_bag_static(const Params& P, const TableDev& T, int64_t bag, int64_t lo, int64_t hi,
                                 float* red) {
     constexpr int Q3 = Dm::q3(), R2 = Dm::r2(), Q12 = Dm::q1() * Dm::q2();
@@ -471,7 +471,7 @@ __device__ void pool_bag_static(const Params& P, const TableDev& T, int64_t bag,
                 i2l = P.lk_i2[nl];
                 i3l = P.lk_i3[nl];
                 sl = P.lk_s[nl];
-                if (P.cache_n > 0 && P.lk_hit[nl] >= 0) sl = 0.f;  // read from the cache below
+                if (CACHE && P.lk_hit[nl] >= 0) sl = 0.f;  // read from the cache below
             }
             const int64_t left = hi - nb0 - wb;  // this warp's lookups nb0 + wb + NW l < hi
             const int64_t c64 = left <= 0 ? 0 : (left + NW - 1) / NW;
@@ -538,7 +538,7 @@ __device__ void pool_bag_static(const Params& P, const TableDev& T, int64_t bag,
     constexpr int V = H / 16;
     const int64_t first = lo + (WARP ? 0 : w);
     const int step = WARP ? 1 : kPoolWarps;
-    if (P.cache_n > 0) {  // cache hits: s times the cached value, V columns a lane
+    if (CACHE) {  // cache hits: s times the cached value, V columns a lane
         for (int64_t n = first; n < hi; n += step) {
             const int slot = P.lk_hit[n];
             if (slot < 0) continue;
@@ -548,7 +548,7 @@ __device__ void pool_bag_static(const Params& P, const TableDev& T, int64_t bag,
             for (int v = 0; v < V; ++v) acc[v] = fmaf(sh, __ldcg(cv + v), acc[v]);
         }
     }
-    if (P.cache_n > 0 && !P.cache_train) cache_refresh_rows(P, T, first, hi, step);
+    if (CACHE && !P.cache_train) cache_refresh_rows(P, T, first, hi, step);
     if constexpr (WARP) {
         float* o = P.out + bag * D + lj * H + lc * V;
 #pragma unroll
@@ -567,7 +567,7 @@ __device__ void pool_bag_static(const Params& P, const TableDev& T, int64_t bag,
 }
 
 // Generic path: lanes over output columns, loop over c.  WARP as for the static path.
-template <bool WARP>
+template <bool WARP, bool CACHE>
 __device__ void pool_bag_generic(const Params& P, const TableDev& T, int64_t bag, int64_t lo, int64_t hi,
                                  float* red) {
     const int lane = threadIdx.x & 31, w = threadIdx.x >> 5;
@@ -579,7 +579,7 @@ __device__ void pool_bag_generic(const Params& P, const TableDev& T, int64_t bag
     for (int m = 0; m < kMaxDPerLane; ++m) acc[m] = 0.f;
     for (int64_t n = first; n < hi; n += step) {
         const int i1 = P.lk_i1[n], i2 = P.lk_i2[n], i3 = P.lk_i3[n];
-        const float s = (P.cache_n > 0 && P.lk_hit[n] >= 0) ? 0.f : P.lk_s[n];  // a hit reads the cache below
+        const float s = (CACHE && P.lk_hit[n] >= 0) ? 0.f : P.lk_s[n];  // a hit reads the cache below
         const float* Tp = t_of_pair(P, T, i2, i1);
         const float* g3 = T.G3 + (int64_t)i3 * r2 * q3;
 #pragma unroll
@@ -592,7 +592,7 @@ __device__ void pool_bag_generic(const Params& P, const TableDev& T, int64_t bag
             }
             acc[m] = fmaf(s, a, acc[m]);
         }
-        if (P.cache_n > 0) {  // a cache hit: s times the cached value
+        if (CACHE) {  // a cache hit: s times the cached value
             const int slot2 = P.lk_hit[n];
             if (slot2 >= 0) {
                 const float sh = P.lk_sh[n];
@@ -604,7 +604,7 @@ __device__ void pool_bag_generic(const Params& P, const TableDev& T, int64_t bag
             }
         }
     }
-    if (P.cache_n > 0 && !P.cache_train) cache_refresh_rows(P, T, first, hi, step);
+    if (CACHE && !P.cache_train) cache_refresh_rows(P, T, first, hi, step);
     if constexpr (WARP) {
 #pragma unroll
         for (int m = 0; m < kMaxDPerLane; ++m) {
@@ -626,7 +626,7 @@ __device__ void pool_bag_generic(const Params& P, const TableDev& T, int64_t bag
     }
 }
 
-template <int DC, bool WARP>
+template <int DC, bool WARP, bool CACHE>
 __device__ __forceinline__ void pool_one_bag(const Params& P, int64_t bag, float* red) {
     const TableDev& T = P.tables[table_of_bag(P, (int)bag)];
     int64_t lo = P.off[bag], hi = P.off[bag + 1];
@@ -635,35 +635,36 @@ __device__ __forceinline__ void pool_one_bag(const Params& P, int64_t bag, float
     // DC = -1: mixed classes of width 64 (no q3 = 8 class); -2: mixed, another width
     const int dc = DC >= 0 ? DC : T.dclass;
     switch (dc) {
-        case kQ444R32: if constexpr (DC != -2) pool_bag_static<SDims<4, 4, 4, 32, 32>, WARP>(P, T, bag, lo, hi, red); break;
-        case kQ444R16: if constexpr (DC != -2) pool_bag_static<SDims<4, 4, 4, 16, 16>, WARP>(P, T, bag, lo, hi, red); break;
-        case kQ444R64: if constexpr (DC != -2) pool_bag_static<SDims<4, 4, 4, 64, 64>, WARP>(P, T, bag, lo, hi, red); break;
-        case kQ448R64: if constexpr (DC != -1) pool_bag_static<SDims<4, 4, 8, 64, 64>, WARP>(P, T, bag, lo, hi, red); break;
-        default: pool_bag_generic<WARP>(P, T, bag, lo, hi, red); break;
+        case kQ444R32: if constexpr (DC != -2) pool_bag_static<SDims<4, 4, 4, 32, 32>, WARP, CACHE>(P, T, bag, lo, hi, red); break;
+        case kQ444R16: if constexpr (DC != -2) pool_bag_static<SDims<4, 4, 4, 16, 16>, WARP, CACHE>(P, T, bag, lo, hi, red); break;
+        case kQ444R64: if constexpr (DC != -2) pool_bag_static<SDims<4, 4, 4, 64, 64>, WARP, CACHE>(P, T, bag, lo, hi, red); break;
+        case kQ448R64: if constexpr (DC != -1) pool_bag_static<SDims<4, 4, 8, 64, 64>, WARP, CACHE>(P, T, bag, lo, hi, red); break;
+        default: pool_bag_generic<WARP, CACHE>(P, T, bag, lo, hi, red); break;
     }
 }
 
-// Bags of more than kPoolWarpBag lookups on average: one block of kPoolWarps warps per
-// bag, the warps share the bag's lookups; shorter bags: one warp per bag.  Blocks past
-// the bags' run the grouping scatter of the small path.  DC >= 0: every table of the
-// handle has dimension class DC; DC < 0: per table.
-template <int DC>
+// MODE & 1 (short bags, on average at most kPoolWarpBag lookups): one warp per bag;
+// else one block of kPoolWarps warps per bag, the warps share the bag's lookups.
+// MODE & 2: the handle has a hot-row cache.  Blocks past the bags' run the grouping
+// scatter of the small path.  DC >= 0: every table of the handle has dimension class
+// DC; DC < 0: per table.
+template <int DC, int MODE>
 __global__ void __launch_bounds__(kPoolWarps * 32) k_pool(const __grid_constant__ Params P) {
     pdl_entry();
     __shared__ float red[kPoolWarps * kMaxD];
-    const bool warp_mode = P.nnz <= (int64_t)kPoolWarpBag * P.nbags;
-    const int64_t nbb = warp_mode ? (P.nbags + kPoolWarps - 1) / kPoolWarps : P.nbags;  // bag blocks
+    constexpr bool WARP = (MODE & 1) != 0, CACHE = (MODE & 2) != 0;
+    const int64_t nbb = WARP ? (P.nbags + kPoolWarps - 1) / kPoolWarps : P.nbags;  // bag blocks
     if ((int64_t)blockIdx.x >= nbb) {  // small path: extra blocks scatter the lookups of part of a chunk
         const int e = (int)(blockIdx.x - nbb);
         scatter_chunk(P, e / kScatterParts, e % kScatterParts);
         return;
     }
     if (blockIdx.x == 0 && threadIdx.x == 0) atomicAdd(P.epoch, 1);  // k_fwd_T has finished reading it
-    if (warp_mode) {
+    if constexpr (WARP) {
         const int64_t bag = (int64_t)blockIdx.x * kPoolWarps + (threadIdx.x >> 5);
-        if (bag < P.nbags) pool_one_bag<DC, true>(P, bag, red);
+        if (bag < P.nbags) pool_one_bag<DC, true, CACHE>(P, bag, red);
     } else {
-        pool_one_bag<DC, false>(P, blockIdx.x, red);
+        pool_one_bag<DC, false, CACHE>(P, blockIdx.x, red);
     }
 }
 
@@ -719,14 +720,24 @@ cudaError_t launch_fwd_T(const Params& P, cudaStream_t s) {
     }
 }
 
-template <int DC>
-static cudaError_t launch_pool_dc(const Params& P, cudaStream_t s) {
-    const bool warp_mode = P.nnz <= (int64_t)kPoolWarpBag * P.nbags;
-    const int64_t nbb = warp_mode ? (P.nbags + kPoolWarps - 1) / kPoolWarps : P.nbags;
-    cudaError_t le = launch_pdl(k_pool<DC>, dim3((unsigned)(nbb + (P.small ? (int64_t)P.nch * kScatterParts : 0))),
+template <int DC, int MODE>
+static cudaError_t launch_pool_mode(const Params& P, cudaStream_t s) {
+    const int64_t nbb = (MODE & 1) ? (P.nbags + kPoolWarps - 1) / kPoolWarps : P.nbags;
+    cudaError_t le = launch_pdl(k_pool<DC, MODE>, dim3((unsigned)(nbb + (P.small ? (int64_t)P.nch * kScatterParts : 0))),
                                 dim3(kPoolWarps * 32), 0, s, P);
     if (le != cudaSuccess) return le;
     return cudaGetLastError();
+}
+
+// The hot-row cache exists on single-table handles only: no cached variant of the
+// mixed-class kernels.
+template <int DC>
+static cudaError_t launch_pool_dc(const Params& P, cudaStream_t s) {
+    const int warp = P.nnz <= (int64_t)kPoolWarpBag * P.nbags ? 1 : 0;
+    if constexpr (DC >= 0) {
+        if (P.cache_n > 0) return warp ? launch_pool_mode<DC, 3>(P, s) : launch_pool_mode<DC, 2>(P, s);
+    }
+    return warp ? launch_pool_mode<DC, 1>(P, s) : launch_pool_mode<DC, 0>(P, s);
 }
 
 cudaError_t launch_pool(const Params& P, cudaStream_t s) {
@@ -1030,9 +1041,13 @@ cudaError_t set_fwd_attributes(int max_smem) {
     const void* ks[] = {(const void*)k_fwd_T<kQ444R32>, (const void*)k_fwd_T<kQ444R16>,
                         (const void*)k_fwd_T<kQ444R64>, (const void*)k_fwd_T<kQ448R64>,
                         (const void*)k_fwd_T<kDynamic>, (const void*)k_fwd_T<-1>,
-                        (const void*)k_pool<kQ444R32>, (const void*)k_pool<kQ444R16>,
-                        (const void*)k_pool<kQ444R64>, (const void*)k_pool<kQ448R64>,
-                        (const void*)k_pool<kDynamic>, (const void*)k_pool<-1>, (const void*)k_pool<-2>, (const void*)k_cache_fill};
+#define TT_POOL4(DC) (const void*)k_pool<DC, 0>, (const void*)k_pool<DC, 1>, (const void*)k_pool<DC, 2>, (const void*)k_pool<DC, 3>
+                        TT_POOL4(kQ444R32), TT_POOL4(kQ444R16), TT_POOL4(kQ444R64), TT_POOL4(kQ448R64), TT_POOL4(kDynamic),
+#undef TT_POOL4
+                        (const void*)k_pool<-1, 0>, (const void*)k_pool<-1, 1>, (const void*)k_pool<-2, 0>,
+                        (const void*)k_pool<-2, 1>, (const void*)k_cache_fill, (const void*)k_cache_gmax,
+                        (const void*)k_cache_acc<2>, (const void*)k_cache_acc<4>, (const void*)k_cache_acc<8>,
+                        (const void*)k_cache_apply};
     for (const void* k : ks) {
         cudaError_t e = allow_max_dynamic_smem(k, max_smem);
         if (e != cudaSuccess) return e;

@@ -386,7 +386,8 @@ __device__ __forceinline__ int cache_find(const Params& P, int64_t row) {
 }
 
 // Returns false for a lookup that stays out of the TT path and its grouping (a
-// trainable cache hit), true otherwise.
+// trainable cache hit), true otherwise.  CACHE: the handle has a hot-row cache.
+template <bool CACHE>
 __device__ __forceinline__ bool decode_lookup(const Params& P, int64_t n, int bag, int64_t row, float w, int& t,
                                               int& i1, int& i2, int& i3, int epoch) {
     t = table_of_bag(P, bag);
@@ -419,7 +420,7 @@ __device__ __forceinline__ bool decode_lookup(const Params& P, int64_t n, int ba
     // TT path scale 0), -2 - slot for the one lookup of a pass that refreshes a stale
     // exact copy, -1 otherwise.  A trainable hit takes no part in the cores' gradient
     // (lk_s = 0); an exact-copy hit keeps it.
-    if (P.cache_n > 0) {
+    if constexpr (CACHE) {
         int slot = valid ? cache_find(P, row) : -1;
         if (slot >= 0) {
             if (P.cache_train) {
@@ -440,7 +441,7 @@ __device__ __forceinline__ bool decode_lookup(const Params& P, int64_t n, int ba
     P.lk_i3[n] = i3;
     P.lk_bag[n] = bag;
     P.lk_s[n] = s;
-    if (P.cache_train && P.lk_hit[n] >= 0) return false;
+    if (CACHE && P.cache_train && P.lk_hit[n] >= 0) return false;
     P.tflag[T.fbase + (int64_t)i2 * T.p1 + i1] = epoch;
     return true;
 }

@@ -19,6 +19,7 @@ namespace ttemb {
 
 // ------------------------------------------------------------------ decode
 
+template <bool CACHE>
 __global__ void __launch_bounds__(kSortThreads, 1) k_decode_hist(const __grid_constant__ Params P) {
     pdl_entry();
     if (blockIdx.x == 0 && threadIdx.x == 0) atomicAdd(P.dstep, 1);  // the pass's cache stamp
@@ -49,7 +50,7 @@ __global__ void __launch_bounds__(kSortThreads, 1) k_decode_hist(const __grid_co
     const int64_t hi = (lo + kChunk < P.nnz) ? lo + kChunk : P.nnz;
     for (int64_t n = lo + threadIdx.x; n < hi; n += blockDim.x) {
         int t, i1, i2, i3;
-        if (!decode_lookup(P, n, (int)bag_of(P, n), P.idx[n], P.w ? P.w[n] : 1.0f, t, i1, i2, i3, *P.epoch))
+        if (!decode_lookup<CACHE>(P, n, (int)bag_of(P, n), P.idx[n], P.w ? P.w[n] : 1.0f, t, i1, i2, i3, *P.epoch))
             continue;
         const TableDev& T = P.tables[t];
         atomicAdd(&h1[T.base1 + i1], 1);
@@ -364,6 +365,7 @@ __device__ __forceinline__ int64_t staged_bag(const int64_t* soff, int64_t b0, i
     return b0 + a;
 }
 
+template <bool CACHE>
 __global__ void __launch_bounds__(kSmallChunk) k_decode_small(const __grid_constant__ Params P) {
     pdl_entry();
     if (blockIdx.x == 0 && threadIdx.x == 0) atomicAdd(P.dstep, 1);  // the pass's cache stamp
@@ -386,7 +388,7 @@ __global__ void __launch_bounds__(kSmallChunk) k_decode_small(const __grid_const
     if (n < hi) {
         const int64_t bag = nst ? staged_bag(soff, sb[0], nst, n) : bag_of(P, n);
         int t, i1, i2, i3;
-        if (decode_lookup(P, n, (int)bag, row, wv, t, i1, i2, i3, epoch)) {
+        if (decode_lookup<CACHE>(P, n, (int)bag, row, wv, t, i1, i2, i3, epoch)) {
             const TableDev& T = P.tables[t];
             d[0] = T.base1 + i1;
             d[1] = T.base2 + i2;
@@ -424,14 +426,16 @@ __global__ void __launch_bounds__(kSmallChunk) k_decode_small(const __grid_const
 // ------------------------------------------------------------------ launchers
 
 cudaError_t launch_decode_small(const Params& P, cudaStream_t s) {
-    cudaError_t le = launch_pdl(k_decode_small, dim3((unsigned)P.nch), dim3(kSmallChunk), 0, s, P);
+    cudaError_t le = P.cache_n > 0 ? launch_pdl(k_decode_small<true>, dim3((unsigned)P.nch), dim3(kSmallChunk), 0, s, P)
+                                   : launch_pdl(k_decode_small<false>, dim3((unsigned)P.nch), dim3(kSmallChunk), 0, s, P);
     if (le != cudaSuccess) return le;
     return cudaGetLastError();
 }
 
 cudaError_t launch_decode_hist(const Params& P, cudaStream_t s) {
     const size_t smem = sizeof(int) * (size_t)(P.n1 + P.n3);
-    cudaError_t le = launch_pdl(k_decode_hist, dim3(P.nch), dim3(kSortThreads), smem, s, P);
+    cudaError_t le = P.cache_n > 0 ? launch_pdl(k_decode_hist<true>, dim3(P.nch), dim3(kSortThreads), smem, s, P)
+                                   : launch_pdl(k_decode_hist<false>, dim3(P.nch), dim3(kSortThreads), smem, s, P);
     if (le != cudaSuccess) return le;
     return cudaGetLastError();
 }
@@ -475,8 +479,9 @@ cudaError_t launch_scatter2(const Params& P, cudaStream_t s) {
 }
 
 cudaError_t set_sort_attributes(int max_smem) {
-    const void* ks[] = {(const void*)k_decode_hist, (const void*)k_scatter13, (const void*)k_scatter2,
-                        (const void*)k_decode_small, (const void*)k_scan_sums<0>, (const void*)k_scan_sums<1>,
+    const void* ks[] = {(const void*)k_decode_hist<false>, (const void*)k_decode_hist<true>,
+                        (const void*)k_scatter13, (const void*)k_scatter2,
+                        (const void*)k_decode_small<false>, (const void*)k_decode_small<true>, (const void*)k_scan_sums<0>, (const void*)k_scan_sums<1>,
                         (const void*)k_scan_apply<0>, (const void*)k_scan_apply<1>};
     for (const void* k : ks) {
         cudaError_t e = allow_max_dynamic_smem(k, max_smem);
