@@ -975,33 +975,64 @@ __global__ void __launch_bounds__(kCacheChunk) k_cache_acc(const __grid_constant
 }
 
 // The optimizer step of the touched cached values (SGD, Adagrad, or the gradient kept
-// for reading), a thread per (listed slot, column); the accumulators, touch flags
-// and the two bound words return to zero.
+// for reading): a warp per listed slot, lanes over columns, two slots' loads in flight;
+// the accumulators, touch flags and the two bound words return to zero.  DPL =
+// columns per lane (D <= 32 DPL).
+template <int DPL>
+__device__ __forceinline__ void cache_apply_slot(const Params& P, int slot, int S, const unsigned long long* a,
+                                                 const float* v, const float* st) {
+    const int lane = threadIdx.x & 31, D = P.D;
+#pragma unroll
+    for (int m = 0; m < DPL; ++m) {
+        const int j = lane + 32 * m;
+        if (j >= D) continue;
+        const int64_t e = (int64_t)slot * D + j;
+        const float g = S == INT_MIN ? __int_as_float(0x7fffffff) : scale2(__ll2float_rn((long long)a[m]), -S);
+        P.cache_acc[e] = 0ull;
+        if (P.opt == TT_OPT_SGD) {
+            P.cache_vals[e] = fmaf(-P.lr, g, v[m]);
+        } else if (P.opt == TT_OPT_ADAGRAD) {
+            const float t = fmaf(g, g, st[m]);
+            P.cache_state[e] = t;
+            P.cache_vals[e] = v[m] - P.lr * g / (sqrtf(t) + P.eps);
+        } else {
+            P.cache_grad[e] = g;
+        }
+    }
+    if (lane == 0) P.cache_touch[slot] = 0;
+}
+
+template <int DPL>
 __global__ void __launch_bounds__(256) k_cache_apply(const __grid_constant__ Params P) {
     pdl_entry();
     const int S = (int)P.cache_gmax[1];
-    const int64_t total = (int64_t)P.cache_gmax[2] * P.D;
+    const int cnt = (int)P.cache_gmax[2];
     if (blockIdx.x == 0 && threadIdx.x == 0) {
         P.cache_gmax[0] = 0u;
         P.cache_gmax[3] = 0u;
     }
-    for (int64_t f = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; f < total; f += (int64_t)gridDim.x * blockDim.x) {
-        const int64_t i = f / P.D;
-        const int j = (int)(f - i * P.D);
-        const int slot = P.cache_list[i];
-        const int64_t e = (int64_t)slot * P.D + j;
-        const float g = S == INT_MIN ? __int_as_float(0x7fffffff) : scale2(__ll2float_rn((long long)P.cache_acc[e]), -S);
-        P.cache_acc[e] = 0ull;
-        if (P.opt == TT_OPT_SGD) {
-            P.cache_vals[e] = fmaf(-P.lr, g, P.cache_vals[e]);
-        } else if (P.opt == TT_OPT_ADAGRAD) {
-            const float st = fmaf(g, g, P.cache_state[e]);
-            P.cache_state[e] = st;
-            P.cache_vals[e] -= P.lr * g / (sqrtf(st) + P.eps);
-        } else {
-            P.cache_grad[e] = g;
+    const int lane = threadIdx.x & 31, D = P.D;
+    const int nw = gridDim.x * (blockDim.x >> 5);
+    const bool adagrad = P.opt == TT_OPT_ADAGRAD, update = P.opt != TT_OPT_GRAD;
+    for (int i = (blockIdx.x * blockDim.x + threadIdx.x) >> 5; i < cnt; i += 2 * nw) {
+        const int s0 = P.cache_list[i];
+        const int s1 = i + nw < cnt ? P.cache_list[i + nw] : -1;
+        unsigned long long a0[DPL], a1[DPL];
+        float v0[DPL], v1[DPL], t0[DPL], t1[DPL];
+#pragma unroll
+        for (int m = 0; m < DPL; ++m) {
+            const int j = lane + 32 * m;
+            const bool in = j < D;
+            const int64_t e0 = (int64_t)s0 * D + j, e1 = (int64_t)s1 * D + j;
+            a0[m] = in ? P.cache_acc[e0] : 0ull;
+            v0[m] = in && update ? P.cache_vals[e0] : 0.f;
+            t0[m] = in && adagrad ? P.cache_state[e0] : 0.f;
+            a1[m] = in && s1 >= 0 ? P.cache_acc[e1] : 0ull;
+            v1[m] = in && s1 >= 0 && update ? P.cache_vals[e1] : 0.f;
+            t1[m] = in && s1 >= 0 && adagrad ? P.cache_state[e1] : 0.f;
         }
-        if (j == 0) P.cache_touch[slot] = 0;
+        cache_apply_slot<DPL>(P, s0, S, a0, v0, t0);
+        if (s1 >= 0) cache_apply_slot<DPL>(P, s1, S, a1, v1, t1);
     }
 }
 
@@ -1032,8 +1063,10 @@ cudaError_t launch_cache_acc(const Params& P, cudaStream_t s) {
 }
 
 cudaError_t launch_cache_apply(const Params& P, cudaStream_t s) {
-    const int64_t b = grid_for(P.cache_n * P.D, 256, 152 * 8);
-    cudaError_t le = launch_pdl(k_cache_apply, dim3((unsigned)b), dim3(256), 0, s, P);
+    const int64_t b = grid_for(P.cache_n, 8, 152 * 8);
+    cudaError_t le = P.D <= 64 ? launch_pdl(k_cache_apply<2>, dim3((unsigned)b), dim3(256), 0, s, P)
+                   : P.D <= 128 ? launch_pdl(k_cache_apply<4>, dim3((unsigned)b), dim3(256), 0, s, P)
+                                : launch_pdl(k_cache_apply<8>, dim3((unsigned)b), dim3(256), 0, s, P);
     return le != cudaSuccess ? le : cudaGetLastError();
 }
 
@@ -1047,7 +1080,7 @@ cudaError_t set_fwd_attributes(int max_smem) {
                         (const void*)k_pool<-1, 0>, (const void*)k_pool<-1, 1>, (const void*)k_pool<-2, 0>,
                         (const void*)k_pool<-2, 1>, (const void*)k_cache_fill, (const void*)k_cache_gmax,
                         (const void*)k_cache_acc<2>, (const void*)k_cache_acc<4>, (const void*)k_cache_acc<8>,
-                        (const void*)k_cache_apply};
+                        (const void*)k_cache_apply<2>, (const void*)k_cache_apply<4>, (const void*)k_cache_apply<8>};
     for (const void* k : ks) {
         cudaError_t e = allow_max_dynamic_smem(k, max_smem);
         if (e != cudaSuccess) return e;

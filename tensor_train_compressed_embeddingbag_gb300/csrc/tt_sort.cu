@@ -19,11 +19,58 @@ namespace ttemb {
 
 // ------------------------------------------------------------------ decode
 
+// Bag offsets covering lookups lo .. hi-1 into soff: all of them when they
+// fit, else offsets b0 .. b1 + 1 of the bags of lo and hi - 1.  Returns the
+// number staged (sb[0] = b0), or 0 when the range does not fit (the caller
+// then searches global memory).
+__device__ int stage_bag_offsets(const Params& P, int64_t lo, int64_t hi, int64_t* soff, int64_t* sb, int cap) {
+    if (P.nbags + 1 <= cap) {
+        const int nst = (int)(P.nbags + 1);
+        for (int base = 0; base < nst; base += 4 * blockDim.x) {  // 4 loads in flight per thread
+            int64_t v[4];
+#pragma unroll
+            for (int u = 0; u < 4; ++u) {
+                const int i = base + u * blockDim.x + threadIdx.x;
+                v[u] = i < nst ? P.off[i] : 0;
+            }
+#pragma unroll
+            for (int u = 0; u < 4; ++u) {
+                const int i = base + u * blockDim.x + threadIdx.x;
+                if (i < nst) soff[i] = v[u];
+            }
+        }
+        if (threadIdx.x == 0) sb[0] = 0;
+        __syncthreads();
+        return (int)(P.nbags + 1);
+    }
+    if (threadIdx.x == 0) sb[0] = bag_of(P, lo);
+    if (threadIdx.x == 32) sb[1] = bag_of(P, hi - 1);
+    __syncthreads();
+    const int64_t b0 = sb[0], nst = sb[1] - b0 + 2;
+    const bool ok = nst >= 2 && nst <= cap;
+    if (ok)
+        for (int i = threadIdx.x; i < nst; i += blockDim.x) soff[i] = P.off[b0 + i];
+    __syncthreads();
+    return ok ? (int)nst : 0;
+}
+
+__device__ __forceinline__ int64_t staged_bag(const int64_t* soff, int64_t b0, int nst, int64_t n) {
+    int a = 0, b = nst - 1;  // largest a < nst - 1 with soff[a] <= n
+    while (b - a > 1) {
+        const int m = (a + b) >> 1;
+        if (soff[m] <= n) a = m; else b = m;
+    }
+    return b0 + a;
+}
+
+
 template <bool CACHE>
 __global__ void __launch_bounds__(kSortThreads, 1) k_decode_hist(const __grid_constant__ Params P) {
     pdl_entry();
     if (blockIdx.x == 0 && threadIdx.x == 0) atomicAdd(P.dstep, 1);  // the pass's cache stamp
     extern __shared__ int sm[];
+    __shared__ int64_t soff[kChunk + 2];
+    __shared__ int64_t sb[2];
     int* h1 = sm;           // [n1]
     int* h3 = sm + P.n1;    // [n3]
     const int c = blockIdx.x;
@@ -48,10 +95,26 @@ __global__ void __launch_bounds__(kSortThreads, 1) k_decode_hist(const __grid_co
 
     const int64_t lo = (int64_t)c * kChunk;
     const int64_t hi = (lo + kChunk < P.nnz) ? lo + kChunk : P.nnz;
-    for (int64_t n = lo + threadIdx.x; n < hi; n += blockDim.x) {
+    // this thread's indices and weights, all in flight while the chunk's bag offsets
+    // are staged in shared memory (bag search there rather than in global memory)
+    constexpr int kPer = kChunk / kSortThreads;
+    int64_t rows[kPer];
+    float wts[kPer];
+#pragma unroll
+    for (int u = 0; u < kPer; ++u) {
+        const int64_t n = lo + threadIdx.x + (int64_t)u * kSortThreads;
+        rows[u] = n < hi ? P.idx[n] : 0;
+        wts[u] = (n < hi && P.w) ? P.w[n] : 1.0f;
+    }
+    const int epoch = *P.epoch;
+    const int nst = stage_bag_offsets(P, lo, hi, soff, sb, kChunk + 2);
+#pragma unroll
+    for (int u = 0; u < kPer; ++u) {
+        const int64_t n = lo + threadIdx.x + (int64_t)u * kSortThreads;
+        if (n >= hi) break;
+        const int64_t bag = nst ? staged_bag(soff, sb[0], nst, n) : bag_of(P, n);
         int t, i1, i2, i3;
-        if (!decode_lookup<CACHE>(P, n, (int)bag_of(P, n), P.idx[n], P.w ? P.w[n] : 1.0f, t, i1, i2, i3, *P.epoch))
-            continue;
+        if (!decode_lookup<CACHE>(P, n, (int)bag, rows[u], wts[u], t, i1, i2, i3, epoch)) continue;
         const TableDev& T = P.tables[t];
         atomicAdd(&h1[T.base1 + i1], 1);
         atomicAdd(&h3[T.base3 + i3], 1);
@@ -320,50 +383,6 @@ __global__ void __launch_bounds__(kSortThreads, 1) k_scatter2(const __grid_const
 //                   three extra blocks of the k_fwd_T launch)
 //   scatter_chunk   position = scanned base + rank (run by extra blocks of the
 //                   k_pool launch)
-
-// Bag offsets covering lookups lo .. hi-1 into soff: all of them when they
-// fit, else offsets b0 .. b1 + 1 of the bags of lo and hi - 1.  Returns the
-// number staged (sb[0] = b0), or 0 when the range does not fit (the caller
-// then searches global memory).
-__device__ int stage_bag_offsets(const Params& P, int64_t lo, int64_t hi, int64_t* soff, int64_t* sb, int cap) {
-    if (P.nbags + 1 <= cap) {
-        const int nst = (int)(P.nbags + 1);
-        for (int base = 0; base < nst; base += 4 * blockDim.x) {  // 4 loads in flight per thread
-            int64_t v[4];
-#pragma unroll
-            for (int u = 0; u < 4; ++u) {
-                const int i = base + u * blockDim.x + threadIdx.x;
-                v[u] = i < nst ? P.off[i] : 0;
-            }
-#pragma unroll
-            for (int u = 0; u < 4; ++u) {
-                const int i = base + u * blockDim.x + threadIdx.x;
-                if (i < nst) soff[i] = v[u];
-            }
-        }
-        if (threadIdx.x == 0) sb[0] = 0;
-        __syncthreads();
-        return (int)(P.nbags + 1);
-    }
-    if (threadIdx.x == 0) sb[0] = bag_of(P, lo);
-    if (threadIdx.x == 32) sb[1] = bag_of(P, hi - 1);
-    __syncthreads();
-    const int64_t b0 = sb[0], nst = sb[1] - b0 + 2;
-    const bool ok = nst >= 2 && nst <= cap;
-    if (ok)
-        for (int i = threadIdx.x; i < nst; i += blockDim.x) soff[i] = P.off[b0 + i];
-    __syncthreads();
-    return ok ? (int)nst : 0;
-}
-
-__device__ __forceinline__ int64_t staged_bag(const int64_t* soff, int64_t b0, int nst, int64_t n) {
-    int a = 0, b = nst - 1;  // largest a < nst - 1 with soff[a] <= n
-    while (b - a > 1) {
-        const int m = (a + b) >> 1;
-        if (soff[m] <= n) a = m; else b = m;
-    }
-    return b0 + a;
-}
 
 template <bool CACHE>
 __global__ void __launch_bounds__(kSmallChunk) k_decode_small(const __grid_constant__ Params P) {
