@@ -221,3 +221,43 @@ def test_trainable_cache_argument_and_state_errors(workloads):
     run = GpuRun(workloads(5, 8))
     assert lib.tt_emb_cache_set_trainable(run.h, 1, None) == tt.TT_ERR_STATE  # table-batched handle
     run.close()
+
+
+def test_trainable_short_bags_rank32():
+    """Bags of 1-3 lookups (a warp per bag; the rank-32 pool path) with the 40 most
+    frequent rows trainable: three SGD steps, every output, core and cached value
+    against the oracle's own chain of steps."""
+    from tt_inputs import TableSpec, Workload
+
+    rng = np.random.default_rng(21)
+    spec = TableSpec(210, [6, 5, 7], [4, 4, 4], [32, 32])
+    cores = [rng.normal(0, 0.3, size=sh).astype(np.float32) for sh in spec.core_shapes()]
+    lengths = rng.integers(1, 4, size=300)
+    off = np.concatenate([[0], np.cumsum(lengths)]).astype(np.int64)
+    idx = rng.integers(0, spec.num_embeddings, size=int(off[-1]), dtype=np.int64)
+    w = rng.random(idx.shape[0], dtype=np.float32)
+    go = rng.standard_normal((lengths.shape[0], spec.embedding_dim), dtype=np.float32)
+    wl = Workload("short bags", [spec], [cores], idx, off, w, "mean", 0.1, lengths.shape[0], go)
+    uniq, counts = np.unique(idx, return_counts=True)
+    hot = np.sort(uniq[np.argsort(-counts, kind="stable")[:40]])
+    run = GpuRun(wl)
+    tt.tt_emb_cache_set_trainable(run.h, True)
+    tt.tt_emb_cache_populate(run.h, dev(hot))
+    rows = tt.tt_emb_lfu_cached_rows(run.h)
+    np.testing.assert_array_equal(rows, hot)
+    ref = [c.astype(np.float64) for c in cores]
+    vals = _initial_values(wl, rows)
+    mw = oracle.cache_miss_weights(rows, idx, off, w)
+    for step in range(3):
+        out = run.forward().cpu().numpy()
+        assert_rows_close(out, oracle.cached_forward(wl.tables, [ref], rows, vals, idx, off, w, "mean"), f"forward {step}")
+        run.backward()
+        assert run.error() == tt.TT_OK
+        ref = oracle.sgd_step(wl.tables, [ref], idx, off, go, wl.lr, mw, "mean")[0]
+        d, touched = oracle.cache_grad(rows, idx, off, go, w, "mean")
+        vals = oracle.cache_sgd(vals, d, touched, wl.lr)
+        got = run.cores_host()[0]
+        for k in range(3):
+            assert_rows_close(got[k], ref[k], f"step {step} G{k + 1}")
+        assert_rows_close(_read(run, rows), vals, f"step {step} cached values")
+    run.close()
