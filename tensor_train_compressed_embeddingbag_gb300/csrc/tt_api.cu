@@ -45,7 +45,7 @@ struct tt_emb {
     std::vector<TableDev> tabs;  // host copy
     TableDev* d_tables = nullptr;
     int* d_bins = nullptr;       // bin -> table for the three digits
-    int* d_fixed = nullptr;      // err, counters[2], ntiles, grp_done[n2]
+    int* d_fixed = nullptr;      // err, (spare x2), ntiles, epoch, dstep, nincl, scan_done, grp_done[2 n2]
     float* d_tbuf = nullptr;
     int64_t tbuf_floats = 0;
     int* d_tflag = nullptr;      // dense touched-pair flags
@@ -342,7 +342,6 @@ tt_status build_handle(tt_emb* h, int ntab, const tt_table_desc* d) {
     P.bin2_tab = h->d_bins + n1;
     P.bin3_tab = h->d_bins + n1 + n2;
     P.err = h->d_fixed;
-    P.counters = h->d_fixed + 1;
     P.ntiles = h->d_fixed + 3;
     P.epoch = h->d_fixed + 4;
     P.dstep = h->d_fixed + 5;

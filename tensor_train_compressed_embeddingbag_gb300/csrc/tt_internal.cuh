@@ -7,8 +7,10 @@
 //     nnz <= kSmallMaxNnz: per-chunk ranks in k_decode_small, scans by extra
 //                   blocks of k_fwd_T, scatter by extra blocks of k_pool -> pi1 by (i1, pos),
 //                   pi3 by (i3, pos), pi21 by (i2, pos), tiles
-//     larger nnz:   k_scan13, k_scatter13, k_scan2_tiles, k_scatter2 -> pi1,
-//                   pi3, pi21 by (i2, i1, pos) (pairs contiguous), tiles
+//     larger nnz:   per-chunk histograms in k_decode_hist, segmented scans
+//                   (k_scan_sums, k_scan_apply), k_scatter13, the same scans of
+//                   the i2 histogram (the last block cuts the tiles), k_scatter2
+//                   -> pi1, pi3, pi21 by (i2, i1, pos) (pairs contiguous), tiles
 //   k_fwd_T         per (table, i2): T = G1[i1] G2[i2] for every touched pair
 //   k_pool          per bag: row = T G3[i3], pooled in registers -> out
 // and the backward pass:
@@ -19,8 +21,12 @@
 //                   tile, which applies the G2 update)
 //   k_reduce13      per i1 / i3 slice: sum of the partials in sorted-segment
 //                   order, G1 / G3 update
-// Every sum runs in an order fixed by the sort keys, so results are bitwise
-// reproducible; no floating-point atomics are used.
+//   k_cache_gmax, k_cache_acc, k_cache_apply (trainable cache rows only): the
+//                   hits' gradient per cached value as a 64-bit fixed-point sum,
+//                   then its optimizer step
+// Every floating-point sum runs in an order fixed by the sort keys, so results are
+// bitwise reproducible; no floating-point atomics are used (the trainable rows'
+// sums are integer).
 #pragma once
 
 #include <cuda_runtime.h>
@@ -141,7 +147,6 @@ struct Params {
     float* Qbuf;                    // [nnz][qs_max]
     float* Pbuf;                    // [nnz][ps_max]
     float* dG2part;                 // [max_tiles][s2_max]
-    int* counters;                  // spare device counters
     int* nincl;                     // lookups in the sorted orders (all but the trainable cache hits)
     int* segsum;                    // segment totals of the multi-block histogram scans
     int* scan_done;                 // blocks of the H2 scan that have finished (0 between passes)

@@ -83,8 +83,6 @@ __global__ void __launch_bounds__(kSortThreads, 1) k_decode_hist(const __grid_co
             P.H2[e] = 0;
     }
     if (c == 0 && threadIdx.x == 0) {
-        P.counters[0] = 0;
-        P.counters[1] = 0;
         if (P.off[0] != 0 || P.off[P.nbags] != P.nnz) atomicOr(P.err, kErrOffsets);
     }
     // offsets must be non-decreasing: each block checks a slice of them
