@@ -364,8 +364,10 @@ __device__ __forceinline__ void lfu_count(const Params& P, int64_t row) {
 // Cache slot of `row` (table 0) or -1.  Set-associative cache: the kLfuWays ways of
 // the row's set, all loaded at once (16-byte loads of a 256-byte aligned set).
 // Explicit rows: linear probing in the open-addressing index from entry
-// mix64(row) mod size, at most the index's longest probe sequence.
-__device__ __forceinline__ int cache_find(const Params& P, int64_t row) {
+// mix64(row) mod size, at most the index's longest probe sequence; with has_pre,
+// `pre` is that first entry, already loaded.
+__device__ __forceinline__ int cache_find(const Params& P, int64_t row, bool has_pre = false,
+                                          longlong2 pre = longlong2{-1, 0}) {
     if (P.cache_sets > 0) {
         const longlong2* set = reinterpret_cast<const longlong2*>(P.cache_rows + lfu_set_of(row, P.cache_sets) * kLfuWays);
         long long w[kLfuWays];
@@ -382,7 +384,7 @@ __device__ __forceinline__ int cache_find(const Params& P, int64_t row) {
     }
     unsigned e = (unsigned)mix64((uint64_t)row) & (unsigned)P.cache_hmask;
     for (int k = 0; k < P.cache_hprobe; ++k) {
-        const longlong2 x = __ldg(P.cache_hidx + e);
+        const longlong2 x = (k == 0 && has_pre) ? pre : __ldg(P.cache_hidx + e);
         if (x.x == row) return (int)x.y;
         if (x.x < 0) return -1;
         e = (e + 1) & (unsigned)P.cache_hmask;
@@ -394,7 +396,8 @@ __device__ __forceinline__ int cache_find(const Params& P, int64_t row) {
 // trainable cache hit), true otherwise.  CACHE: the handle has a hot-row cache.
 template <bool CACHE>
 __device__ __forceinline__ bool decode_lookup(const Params& P, int64_t n, int bag, int64_t row, float w, int& t,
-                                              int& i1, int& i2, int& i3, int epoch) {
+                                              int& i1, int& i2, int& i3, int epoch, bool has_pre = false,
+                                              longlong2 pre = longlong2{-1, 0}) {
     t = table_of_bag(P, bag);
     const TableDev& T = P.tables[t];
     float s = w;
@@ -426,7 +429,7 @@ __device__ __forceinline__ bool decode_lookup(const Params& P, int64_t n, int ba
     // exact copy, -1 otherwise.  A trainable hit takes no part in the cores' gradient
     // (lk_s = 0); an exact-copy hit keeps it.
     if constexpr (CACHE) {
-        int slot = valid ? cache_find(P, row) : -1;
+        int slot = valid ? cache_find(P, row, has_pre, pre) : -1;
         if (slot >= 0) {
             if (P.cache_train) {
                 P.lk_sh[n] = s;

@@ -105,6 +105,15 @@ __global__ void __launch_bounds__(kSortThreads, 1) k_decode_hist(const __grid_co
         wts[u] = (n < hi && P.w) ? P.w[n] : 1.0f;
     }
     const int epoch = *P.epoch;
+    // explicit cache rows: the first index entry of every row in flight too
+    longlong2 hx[CACHE ? kPer : 1];
+    const bool pre = CACHE && P.cache_sets == 0;
+    if constexpr (CACHE) {
+#pragma unroll
+        for (int u = 0; u < kPer; ++u)
+            hx[u] = pre ? __ldg(P.cache_hidx + ((unsigned)mix64((uint64_t)rows[u]) & (unsigned)P.cache_hmask))
+                        : longlong2{-1, 0};
+    }
     const int nst = stage_bag_offsets(P, lo, hi, soff, sb, kChunk + 2);
 #pragma unroll
     for (int u = 0; u < kPer; ++u) {
@@ -112,7 +121,8 @@ __global__ void __launch_bounds__(kSortThreads, 1) k_decode_hist(const __grid_co
         if (n >= hi) break;
         const int64_t bag = nst ? staged_bag(soff, sb[0], nst, n) : bag_of(P, n);
         int t, i1, i2, i3;
-        if (!decode_lookup<CACHE>(P, n, (int)bag, rows[u], wts[u], t, i1, i2, i3, epoch)) continue;
+        if (!decode_lookup<CACHE>(P, n, (int)bag, rows[u], wts[u], t, i1, i2, i3, epoch, pre, hx[CACHE ? u : 0]))
+            continue;
         const TableDev& T = P.tables[t];
         atomicAdd(&h1[T.base1 + i1], 1);
         atomicAdd(&h3[T.base3 + i3], 1);
