@@ -488,7 +488,10 @@ def run_gpu(args):
             "timing": "CUDA graph of forward + backward replayed per step" if not args.eager else "eager launches",
             "eager": {"ms_per_step": ms_eager / args.steps, "host_enqueue_us_per_step": host_us},
             "forward": {"ns_per_nnz": 1e6 * ms_fwd / (nnz * args.steps),
-                        "lookups_per_s": nnz * args.steps * ws / (ms_fwd / 1e3)},
+                        "lookups_per_s": nnz * args.steps * ws / (ms_fwd / 1e3),
+                        "achieved_tflops": 2 * (sA + sB) / (ms_fwd / args.steps * 1e-3) / 1e12,
+                        "frac": 2 * (sA + sB) / (ms_fwd / args.steps * 1e-3) / 1e12 / peak_tf,
+                        "flop_formula": "2 (q1 r1 q2 r2 + q1 q2 r2 q3) per lookup, against the FP32 peak"},
             "step_roofline": {"flops_per_step": step_flops, "achieved_tflops": step_tf, "peak_tflops": peak_tf,
                               "frac": step_tf / peak_tf, "flop_formula": "6 (q1 r1 q2 r2 + q1 q2 r2 q3) per lookup"},
             "roofline": roof,
