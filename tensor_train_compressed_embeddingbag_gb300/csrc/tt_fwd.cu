@@ -459,8 +459,10 @@ __device__ void pool_bag_static(const Params& P, const TableDev& T, int64_t bag,
     for (int v = 0; v < H; ++v) acc[v] = 0.f;
     {
         // warp w takes lookups lo + w + kPoolWarps l; lane l first loads the indices of the
-        // warp's l-th lookup of a round (one pass), then the warp walks them kPoolPer at a time
+        // warp's l-th lookup of a round (one pass), then the warp walks them PP at a time
         constexpr int NW = WARP ? 1 : kPoolWarps;  // warps sharing the bag
+        // lookups in flight per warp: short bags (WARP) get one, and more warps per SM
+        constexpr int PP = WARP ? 1 : kPoolPer;
         const int wb = WARP ? 0 : w;                // this warp's rank among them
         for (int64_t nb0 = lo; nb0 < hi; nb0 += 32 * NW) {
             const int64_t nl = nb0 + wb + (int64_t)NW * lane;
@@ -476,14 +478,14 @@ __device__ void pool_bag_static(const Params& P, const TableDev& T, int64_t bag,
             const int64_t left = hi - nb0 - wb;  // this warp's lookups nb0 + wb + NW l < hi
             const int64_t c64 = left <= 0 ? 0 : (left + NW - 1) / NW;
             const int cnt = c64 > 32 ? 32 : (int)c64;
-            for (int l = 0; l < cnt; l += kPoolPer) {
-                // kPoolPer lookups of this warp: their T and G3 values are all in flight together
-                int li[kPoolPer];
-                float sv[kPoolPer];
-                const float* Tp[kPoolPer];
-                const float* g3p[kPoolPer];
+            for (int l = 0; l < cnt; l += PP) {
+                // PP lookups of this warp: their T and G3 values are all in flight together
+                int li[PP];
+                float sv[PP];
+                const float* Tp[PP];
+                const float* g3p[PP];
 #pragma unroll
-                for (int q = 0; q < kPoolPer; ++q) {
+                for (int q = 0; q < PP; ++q) {
                     const bool valid = l + q < cnt;
                     li[q] = valid ? l + q : l;
                     const int i1q = __shfl_sync(0xffffffffu, i1l, li[q]), i2q = __shfl_sync(0xffffffffu, i2l, li[q]);
@@ -493,9 +495,9 @@ __device__ void pool_bag_static(const Params& P, const TableDev& T, int64_t bag,
                     Tp[q] = t_of_pair(P, T, i2q, i1q) + lj * J12H * R2;
                     g3p[q] = T.G3 + (int64_t)i3q * R2 * Q3;
                 }
-                float tv[kPoolPer][J12H][NC], gv[kPoolPer][NC][Q3];
+                float tv[PP][J12H][NC], gv[PP][NC][Q3];
 #pragma unroll
-                for (int q = 0; q < kPoolPer; ++q)
+                for (int q = 0; q < PP; ++q)
 #pragma unroll
                     for (int k = 0; k < NC; ++k) {
                         const int c = lc + 16 * k;
@@ -513,7 +515,7 @@ __device__ void pool_bag_static(const Params& P, const TableDev& T, int64_t bag,
                     for (int j3 = 0; j3 < Q3; ++j3) {
                         float a = acc[j * Q3 + j3];
 #pragma unroll
-                        for (int q = 0; q < kPoolPer; ++q) {
+                        for (int q = 0; q < PP; ++q) {
                             float x = 0.f;
 #pragma unroll
                             for (int k = 0; k < NC; ++k) x = fmaf(tv[q][j][k], gv[q][k][j3], x);
