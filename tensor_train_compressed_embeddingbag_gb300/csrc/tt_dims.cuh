@@ -43,16 +43,4 @@ inline int dim_class(int q1, int q2, int q3, int r1, int r2) {
     return kDynamic;
 }
 
-// Calls body(dims) with the table's dimension type.
-template <class F>
-__device__ __forceinline__ void dispatch_dims(const TableDev& T, F&& body) {
-    switch (T.dclass) {
-        case kQ444R32: body(SDims<4, 4, 4, 32, 32>{}); break;
-        case kQ444R16: body(SDims<4, 4, 4, 16, 16>{}); break;
-        case kQ444R64: body(SDims<4, 4, 4, 64, 64>{}); break;
-        case kQ448R64: body(SDims<4, 4, 8, 64, 64>{}); break;
-        default: body(DDims{T.q1, T.q2, T.q3, T.r1, T.r2}); break;
-    }
-}
-
 }  // namespace ttemb

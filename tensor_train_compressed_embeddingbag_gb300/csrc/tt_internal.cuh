@@ -292,26 +292,6 @@ __device__ __forceinline__ void stage_f32(float* dst, const float* src, int n) {
     }
 }
 
-// Same with float4 (dst, src 16-byte aligned, n4 = number of float4).
-template <int U = 4>
-__device__ __forceinline__ void stage_f32x4(float* dst, const float* src, int n4) {
-    const float4* s4 = reinterpret_cast<const float4*>(src);
-    float4* d4 = reinterpret_cast<float4*>(dst);
-    for (int base = 0; base < n4; base += U * blockDim.x) {
-        float4 v[U];
-#pragma unroll
-        for (int u = 0; u < U; ++u) {
-            const int i = base + u * blockDim.x + threadIdx.x;
-            if (i < n4) v[u] = __ldg(s4 + i);
-        }
-#pragma unroll
-        for (int u = 0; u < U; ++u) {
-            const int i = base + u * blockDim.x + threadIdx.x;
-            if (i < n4) d4[i] = v[u];
-        }
-    }
-}
-
 __device__ __forceinline__ int table_of_bag(const Params& P, int bag) {
     return P.ntab == 1 ? 0 : (int)(bag / P.bags_per_table);
 }
