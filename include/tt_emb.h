@@ -185,16 +185,23 @@ tt_status tt_emb_full_weight(tt_emb* h, int32_t table, int64_t row0, int64_t nro
 /*
  * Hot-row cache (FBTT README, "Software Cache"): decompress the n rows of
  * table 0 listed in rows_dev (n <= 2^29 int64 rows, distinct, within [0, E)) into a
- * device-resident fp32 cache.  Later forward passes read a cached row instead
- * of contracting it, as long as its three core slices have not changed since
- * it was filled; a backward pass marks the rows whose slices it updated as
- * stale and the next forward pass recomputes those rows and writes them back
- * into the cache.  Results are the same as without a cache.  Replaces any
- * previous cache content.  Single-table handles only (TT_ERR_STATE otherwise).
+ * device-resident fp32 cache, slot i holding the i-th smallest row (rows are
+ * found through a hash index).  By default the cached rows are exact copies:
+ * later forward passes read a cached row instead of contracting it, as long as
+ * its three core slices have not changed since it was filled; a backward pass
+ * marks the slices it updated and the next forward pass recomputes a stale row
+ * (one lookup per row) and writes it back into the cache.  Results are the same
+ * as without a cache.  With tt_emb_cache_set_trainable the rows are parameters
+ * of their own, initialised here from the cores.  Replaces any previous cache
+ * content; a forward pass made with the previous cache can no longer be
+ * followed by a backward pass (TT_ERR_STATE) when its rows were trainable.
+ * Synchronous.  Returns TT_ERR_ARG (bad n, rows, or a null pointer),
+ * TT_ERR_STATE (a table-batched handle), TT_ERR_NOMEM, TT_ERR_CUDA.
  */
 tt_status tt_emb_cache_populate(tt_emb* h, const int64_t* rows_dev, int64_t n, tt_stream stream);
 
-/* Drop the cache and free its memory. */
+/* Drop the cache and free its memory (also the LFU policy's cache; the access
+ * counts stay).  Returns TT_ERR_ARG for a null handle. */
 tt_status tt_emb_cache_disable(tt_emb* h);
 
 /*
