@@ -4,12 +4,15 @@ TEST INFRASTRUCTURE ONLY: only ``tests/``, ``__graft_entry__.smoke()`` and the
 CPU-baseline leg of ``bench.py`` may import this package.  The product library
 never loads it, and it imports nothing from the product package.
 
-The arithmetic lives in ``tt_oracle.c`` (plain C, float64, definition written
-out per lookup, see its header).  This module compiles it with gcc, promotes
-the float32 cores to float64 and marshals arrays; the optimizer steps are the
-only arithmetic done here (FBTT README, "Fused Kernel": the update is applied
-inside the backward pass; every gradient is taken at the pre-update cores;
-"Parameters": optimizer, learning_rate, eps):
+The TT arithmetic lives in ``tt_oracle.c`` (plain C, float64, definition
+written out per lookup, see its header).  This module compiles it with gcc,
+promotes the float32 cores to float64 and marshals arrays.  Done here in
+numpy: the LFU policy (row hash, counts, per-set selection), the trainable
+cache rows (a cached row's value replaces its TT row: the hit terms of the
+output and the per-row gradient sums), and the optimizer steps (FBTT README,
+"Fused Kernel": the update is applied inside the backward pass; every
+gradient is taken at the pre-update cores; "Parameters": optimizer,
+learning_rate, eps):
 
 * SGD: ``G <- G - lr dG``;
 * Adagrad, element-wise (the pages name the optimizer and its eps but no
