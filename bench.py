@@ -173,8 +173,9 @@ def oracle_step(sub):
 
 
 def cpu_baseline(wl, nbags=None, budget_s=10.0):
-    """One oracle fwd + bwd + SGD step on the first `nbags` bags (default: as many as fit
-    about `budget_s` seconds, at most all), timed on the host."""
+    """Oracle fwd + bwd + SGD steps on the first `nbags` bags (default: as many as fit
+    about `budget_s` seconds, at most all), repeated while a pass takes less than the
+    budget so that about `budget_s` seconds of host work are timed."""
     import oracle
 
     oracle.build()
@@ -187,14 +188,19 @@ def cpu_baseline(wl, nbags=None, budget_s=10.0):
     sub = sub_workload(wl, nbags)
     t0 = time.perf_counter()
     oracle_step(sub)
+    one = time.perf_counter() - t0
+    reps = int(max(1, min(1000, budget_s / max(one, 1e-9))))
+    t0 = time.perf_counter()
+    for _ in range(reps):
+        oracle_step(sub)
     dt = time.perf_counter() - t0
     return {
-        "value": sub.nnz / dt,
+        "value": sub.nnz * reps / dt,
         "unit": "lookups/s",
         "cores": oracle.num_threads(),
         "kind": "oracle",
-        "sample": f"{nbags} of {wl.num_bags} bags ({sub.nnz} lookups), one forward + backward + SGD step, "
-                  f"float64, {dt:.2f} s",
+        "sample": f"{nbags} of {wl.num_bags} bags ({sub.nnz} lookups), {reps} forward + backward + SGD "
+                  f"steps from the same cores, float64, {dt:.2f} s",
     }
 
 
