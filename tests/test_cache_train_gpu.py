@@ -261,3 +261,20 @@ def test_trainable_short_bags_rank32():
             assert_rows_close(got[k], ref[k], f"step {step} G{k + 1}")
         assert_rows_close(_read(run, rows), vals, f"step {step} cached values")
     run.close()
+
+
+def test_cache_write_then_forward(workloads):
+    """tt_emb_cache_write (an external optimizer's step on the cached values): the values
+    read back bit for bit and the next forward pools them (oracle cached_forward)."""
+    wl = workloads(1)
+    run = GpuRun(wl)
+    tt.tt_emb_cache_set_trainable(run.h, True)
+    rows = np.unique(wl.indices)[::3]
+    tt.tt_emb_cache_populate(run.h, dev(rows))
+    vals = np.random.default_rng(3).standard_normal((rows.shape[0], wl.embedding_dim)).astype(np.float32)
+    tt.tt_emb_cache_write(run.h, dev(vals))
+    np.testing.assert_array_equal(_read(run, rows), vals)
+    out = run.forward().cpu().numpy()
+    assert_rows_close(out, oracle.cached_forward(wl.tables, wl.cores, rows, vals, wl.indices, wl.offsets,
+                                                 wl.weights, wl.mode), "forward after write")
+    run.close()
