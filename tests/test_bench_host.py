@@ -70,3 +70,38 @@ def test_reference_arm_other_ranks_stay_silent():
     out = run_bench(["--impl", "reference", "--steps", "1", "--warmup", "0"],
                     {"RANK": "1", "WORLD_SIZE": "2", "LOCAL_RANK": "1"})
     assert out.strip() == ""
+
+
+def test_flop_accounting_per_table():
+    """The roofline's algorithmic FLOPs: per lookup A = q1 r1 q2 r2 and Bc = q1 q2 r2 q3 of
+    its own table, summed over the lookups (checked by brute force over the bags)."""
+    sys.path.insert(0, ROOT)
+    import bench
+    import tt_inputs
+
+    wl = tt_inputs.config(5, batch=16)
+    sa, sb = bench.lookup_flops(wl)
+    want_a = want_b = 0
+    for g in range(wl.num_bags):
+        spec = wl.tables[g // wl.batch]
+        n = int(wl.offsets[g + 1] - wl.offsets[g])
+        q1, q2, q3 = spec.q
+        r1, r2 = spec.ranks
+        want_a += n * q1 * r1 * q2 * r2
+        want_b += n * q1 * q2 * r2 * q3
+    assert (sa, sb) == (want_a, want_b)
+    spec = tt_inputs.config(2).tables[0]
+    assert bench.flops_per_lookup(spec) == (16384, 2048)  # 11M x 64 rank-32: 4*32*4*32, 4*4*32*4
+
+
+def test_workload_names():
+    sys.path.insert(0, ROOT)
+    import argparse
+
+    import bench
+
+    ns = argparse.Namespace
+    assert bench.workload_name(ns(config=2, optimizer="sgd", cache="none")) == bench.WORKLOAD
+    assert "fused Adagrad" in bench.workload_name(ns(config=2, optimizer="adagrad", cache="none"))
+    assert bench.workload_name(ns(config=3, optimizer="sgd", cache="trainable")).endswith("trainable hot-row cache")
+    assert "no cache" in bench.workload_name(ns(config=3, optimizer="sgd", cache="none"))
