@@ -69,6 +69,20 @@ def flops_per_lookup(spec):
     return A, Bc
 
 
+def dedup_step_flops(wl):
+    """Step FLOPs with the contractions shared per touched (table, i1, i2) pair, as the
+    kernels do them: 6 A per pair (T = G1 G2 forward; Q and dG2 backward) plus 6 Bc
+    per lookup (T G3 forward; dT and the dG3 partial backward)."""
+    total = 0
+    for t, spec in enumerate(wl.tables):
+        lo, hi = int(wl.offsets[t * wl.batch]), int(wl.offsets[(t + 1) * wl.batch])
+        rows = np.asarray(wl.indices[lo:hi], dtype=np.int64)
+        pairs = np.unique(rows // int(spec.p[2])).shape[0] if rows.size else 0  # (i1, i2) = row div p3
+        A, Bc = flops_per_lookup(spec)
+        total += 6 * A * pairs + 6 * Bc * rows.shape[0]
+    return total
+
+
 def lookup_flops(wl):
     """(sum over lookups of A, sum over lookups of Bc): per-table figures times the table's lookups."""
     sa = sb = 0
@@ -461,6 +475,7 @@ def run_gpu(args):
             roof = {"bound": "hbm", "achieved": None, "peak": pk["hbm_gbs"], "unit": "GB/s", "frac": None,
                     "traffic": None, "kernel": dom, "avg_ms": kavg[dom]}
         step_flops = 6 * (sA + sB)
+        dedup_flops = dedup_step_flops(wl)
         step_tf = step_flops / (ms_total / args.steps * 1e-3) / 1e12
         result = {
             "metric": METRIC,
@@ -498,7 +513,10 @@ def run_gpu(args):
                         "frac": 2 * (sA + sB) / (ms_fwd / args.steps * 1e-3) / 1e12 / peak_tf,
                         "flop_formula": "2 (q1 r1 q2 r2 + q1 q2 r2 q3) per lookup, against the FP32 peak"},
             "step_roofline": {"flops_per_step": step_flops, "achieved_tflops": step_tf, "peak_tflops": peak_tf,
-                              "frac": step_tf / peak_tf, "flop_formula": "6 (q1 r1 q2 r2 + q1 q2 r2 q3) per lookup"},
+                              "frac": step_tf / peak_tf, "flop_formula": "6 (q1 r1 q2 r2 + q1 q2 r2 q3) per lookup",
+                              "dedup_flops_per_step": dedup_flops,
+                              "dedup_frac": dedup_flops / (ms_total / args.steps * 1e-3) / 1e12 / peak_tf,
+                              "dedup_formula": "6 q1 r1 q2 r2 per touched (i1, i2) pair + 6 q1 q2 r2 q3 per lookup"},
             "roofline": roof,
             "kernels_ms": kavg,
             "gpu_launches": launches_per_step * args.steps,

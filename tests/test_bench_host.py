@@ -105,3 +105,21 @@ def test_workload_names():
     assert "fused Adagrad" in bench.workload_name(ns(config=2, optimizer="adagrad", cache="none"))
     assert bench.workload_name(ns(config=3, optimizer="sgd", cache="trainable")).endswith("trainable hot-row cache")
     assert "no cache" in bench.workload_name(ns(config=3, optimizer="sgd", cache="none"))
+
+
+def test_dedup_flops_brute_force():
+    """Pairs counted per table from the decoded (i1, i2) of every lookup."""
+    sys.path.insert(0, ROOT)
+    import bench
+    import oracle
+    import tt_inputs
+
+    wl = tt_inputs.config(5, batch=16)
+    i1, i2, i3, bag = oracle.decode(wl.tables, wl.indices, wl.offsets, wl.batch)
+    want = 0
+    for t, spec in enumerate(wl.tables):
+        m = (bag // wl.batch) == t
+        pairs = len(set(zip(i1[m].tolist(), i2[m].tolist())))
+        A, Bc = bench.flops_per_lookup(spec)
+        want += 6 * A * pairs + 6 * Bc * int(m.sum())
+    assert bench.dedup_step_flops(wl) == want
