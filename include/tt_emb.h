@@ -258,7 +258,8 @@ tt_status tt_emb_lfu_disable(tt_emb* h);
  *   length in mean mode) x grad_out[bag][j].  The sum is taken in 64-bit fixed
  *   point with integer atomics, so it does not depend on the order of the
  *   hits (each term, the fp32 product, is rounded to a step of 2^-S with
- *   |sum| < 2^62, S set by the step's largest term and lookup count).  The optimizer of
+ *   |sum| < 2^62, S set by max|grad_out| x max|hit scale| and the lookup
+ *   count).  The optimizer of
  *   tt_emb_set_optimizer then updates the cached values that some hit touched
  *   (SGD; Adagrad with its own state per cached value, zero at populate; or
  *   TT_OPT_GRAD, which keeps the gradient for tt_emb_cache_read and gives

@@ -790,9 +790,9 @@ cudaError_t launch_full_weight(const TableDev* tables, int t, int64_t row0, int6
 // Trainable cache rows, backward (FBTT README, "Parameters": sparse, the gradient
 // w.r.t. the cache).  The gradient of cached value [slot][j] is the sum, over the hits n
 // of the slot, of sh_n * grad_out[bag_n][j].  The sum is taken in 64-bit fixed point with
-// integer atomics, so it does not depend on the order of the hits: each term (exact in
-// double) is rounded to a multiple of 2^-S.  With every |term| < 2^e and at most 2^k
-// terms, S = 61 - e - k keeps every partial sum below 2^62.
+// integer atomics, so it does not depend on the order of the hits: each term (the fp32
+// product) is rounded to a multiple of 2^-S.  With every |term| <= 2^e and at most 2^k
+// terms, S = 61 - e - k keeps every partial sum within 2^61.
 
 // 2^x as a float (x within the normal exponent range).
 __device__ __forceinline__ float pow2f(int x) { return __int_as_float((x + 127) << 23); }
