@@ -191,6 +191,20 @@ def backward_core(tables, cores, indices, offsets, grad_out, table, core, weight
     return dG
 
 
+def sgd_update(G, dG, lr):
+    """One SGD step of a block of core elements, float64: ``G - lr dG``."""
+    return np.asarray(G, dtype=np.float64) - float(lr) * np.asarray(dG, dtype=np.float64)
+
+
+def adagrad_update(G, state, dG, lr, eps):
+    """One element-wise Adagrad step, float64: ``s + dG^2`` and ``G - lr dG / (sqrt(s + dG^2) + eps)``.
+
+    Returns ``(updated G, updated s)``."""
+    dG = np.asarray(dG, dtype=np.float64)
+    s_new = np.asarray(state, dtype=np.float64) + dG * dG
+    return np.asarray(G, dtype=np.float64) - float(lr) * dG / (np.sqrt(s_new) + float(eps)), s_new
+
+
 def sgd_slices(tables, cores, indices, offsets, grad_out, lr, table, core, weights=None, mode="sum",
                bags_per_table=None, slices=None):
     """Updated slices ``G_k[s] - lr dG_k[s]`` in float64 (gradients at the pre-update cores)."""
@@ -198,7 +212,7 @@ def sgd_slices(tables, cores, indices, offsets, grad_out, lr, table, core, weigh
     sl = np.arange(int(spec.p[core]), dtype=np.int64) if slices is None else _i64(slices)
     dG = backward_core(tables, cores, indices, offsets, grad_out, table, core, weights, mode,
                        bags_per_table, sl)
-    return np.asarray(cores[table][core], dtype=np.float64)[sl] - float(lr) * dG
+    return sgd_update(np.asarray(cores[table][core])[sl], dG, lr)
 
 
 def adagrad_slices(tables, cores, indices, offsets, grad_out, lr, eps, state, table, core, weights=None,
@@ -211,9 +225,7 @@ def adagrad_slices(tables, cores, indices, offsets, grad_out, lr, eps, state, ta
     sl = np.arange(int(spec.p[core]), dtype=np.int64) if slices is None else _i64(slices)
     dG = backward_core(tables, cores, indices, offsets, grad_out, table, core, weights, mode,
                        bags_per_table, sl)
-    s_new = np.asarray(state, dtype=np.float64)[sl] + dG * dG
-    g_new = np.asarray(cores[table][core], dtype=np.float64)[sl] - float(lr) * dG / (np.sqrt(s_new) + float(eps))
-    return g_new, s_new
+    return adagrad_update(np.asarray(cores[table][core])[sl], np.asarray(state)[sl], dG, lr, eps)
 
 
 def sgd_step(tables, cores, indices, offsets, grad_out, lr, weights=None, mode="sum", bags_per_table=None):

@@ -20,6 +20,10 @@ an independent route to the same numbers.
   their exact bits under SGD, batched tables equal separate tables.
 * Adagrad: two oracle steps equal torch.optim.Adagrad fed the same
   gradients, from a zero and from a warm accumulator.
+* SGD: two oracle steps (sgd_step over every core of two tables, sgd_slices
+  on a subset of slices) equal torch.optim.SGD stepping the cores of a torch
+  float64 model whose gradients come from autograd through an einsum of the
+  cores, in sum mode and in weighted mean mode.
 """
 import itertools
 import json
@@ -320,6 +324,62 @@ def test_adagrad_matches_torch_optim(init):
         for k in range(3):
             np.testing.assert_allclose(cur[k], params[k].detach().numpy(), rtol=1e-12, atol=1e-14)
             np.testing.assert_allclose(state[k], opt.state[params[k]]["sum"].numpy(), rtol=1e-12, atol=1e-14)
+
+
+def _torch_bag_loss(specs, params, idx, off, go, w, mode, batch):
+    """<out, grad_out> of a table-batched EmbeddingBag over full tables expanded from
+    the cores by einsum (torch float64; autograd gives the core gradients)."""
+    loss = 0.0
+    for t, spec in enumerate(specs):
+        g1, g2, g3 = params[t]
+        p1, p2, p3 = spec.p
+        D = int(np.prod(spec.q))
+        full = torch.einsum("xja,yakc,zcl->xyzjkl", g1[:, 0], g2, g3[..., 0]).reshape(p1 * p2 * p3, D)
+        lo, hi = int(off[t * batch]), int(off[(t + 1) * batch])
+        lengths = np.diff(off[t * batch:(t + 1) * batch + 1])
+        bag = torch.from_numpy(np.repeat(np.arange(batch), lengths))
+        s = torch.ones(hi - lo, dtype=torch.float64) if w is None else torch.from_numpy(w[lo:hi]).clone()
+        if mode == "mean":
+            s = s / torch.from_numpy(np.maximum(lengths, 1)).double()[bag]
+        out = torch.zeros(batch, D, dtype=torch.float64).index_add_(
+            0, bag, s[:, None] * full[torch.from_numpy(idx[lo:hi])])
+        loss = loss + (out * torch.from_numpy(go[t * batch:(t + 1) * batch])).sum()
+    return loss
+
+
+@pytest.mark.parametrize("mode,weighted", [("sum", False), ("mean", True)])
+def test_sgd_matches_torch_optim(mode, weighted):
+    """Two fused SGD steps of the oracle (every gradient at the pre-update cores of its
+    step) equal torch.optim.SGD on a torch model of the same two tables whose gradients
+    come from autograd: pins sgd_update, sgd_slices and sgd_step (a sign error or a
+    doubled learning rate fails here)."""
+    rng = np.random.default_rng(12)
+    specs = [TableSpec(100, [5, 4, 6], [2, 3, 2], [3, 5]), TableSpec(60, [3, 4, 5], [3, 2, 2], [2, 4])]
+    cores = [rand_cores(rng, s) for s in specs]
+    batch = 6
+    lengths = rng.integers(0, 5, size=batch * len(specs))
+    off = np.concatenate([[0], np.cumsum(lengths)])
+    idx = np.concatenate([rng.integers(0, specs[t].num_embeddings, size=int(lengths[t * batch:(t + 1) * batch].sum()))
+                          for t in range(len(specs))])
+    w = rng.random(idx.shape[0]) if weighted else None
+    go = rng.standard_normal((batch * len(specs), 12))
+    lr = 0.07
+    params = [[torch.from_numpy(c.copy()).requires_grad_(True) for c in cs] for cs in cores]
+    opt = torch.optim.SGD([p for ps in params for p in ps], lr=lr)
+    cur = [[c.copy() for c in cs] for cs in cores]
+    for _ in range(2):
+        nxt = oracle.sgd_step(specs, cur, idx, off, go, lr, weights=w, mode=mode, bags_per_table=batch)
+        sl = np.array([0, 2, 3])
+        part = oracle.sgd_slices(specs, cur, idx, off, go, lr, 1, 1, weights=w, mode=mode, bags_per_table=batch,
+                                 slices=sl)
+        opt.zero_grad()
+        _torch_bag_loss(specs, params, idx, off, go, w, mode, batch).backward()
+        opt.step()
+        for t in range(len(specs)):
+            for k in range(3):
+                np.testing.assert_allclose(nxt[t][k], params[t][k].detach().numpy(), rtol=1e-12, atol=1e-14)
+        np.testing.assert_allclose(part, params[1][1].detach().numpy()[sl], rtol=1e-12, atol=1e-14)
+        cur = nxt
 
 
 def test_splitmix64_published_outputs():
