@@ -24,12 +24,13 @@ namespace {
 
 constexpr int64_t kScratchFloats = TT_NOALLOC_SCRATCH_BYTES / sizeof(float);
 constexpr int kWarps = 8;       // warps per block
-constexpr int kMaxGridWarps = 152 * 16;
+constexpr int kWarpsPerSm = 16; // grid cap: resident warps per SM the grid aims for
 constexpr int kMaxDevices = 256;
 
 static __device__ __align__(256) float g_noalloc_scratch[kScratchFloats];
 
 float* g_scratch_addr[kMaxDevices];  // device address of the array, per device
+int g_sm_count[kMaxDevices];         // multiprocessors of the device
 std::mutex g_setup_mutex;
 
 struct NoAllocArgs {
@@ -105,21 +106,26 @@ __global__ void __launch_bounds__(kWarps * 32) k_pool_noalloc(const __grid_const
     }
 }
 
-// Device address of the scratch array on the current device, looked up once per device.
-tt_status scratch_address(float** out) {
+// Device address of the scratch array on the current device and the device's
+// multiprocessor count, looked up once per device.
+tt_status scratch_address(float** out, int* sms) {
     int dev = 0;
     if (cudaGetDevice(&dev) != cudaSuccess) return TT_ERR_CUDA;
     if (dev < 0 || dev >= kMaxDevices) return TT_ERR_CUDA;
     std::lock_guard<std::mutex> lock(g_setup_mutex);
     if (!g_scratch_addr[dev]) {
         void* p = nullptr;
-        if (cudaGetSymbolAddress(&p, g_noalloc_scratch) != cudaSuccess || !p) {
+        int n = 0;
+        if (cudaGetSymbolAddress(&p, g_noalloc_scratch) != cudaSuccess || !p ||
+            cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || n <= 0) {
             cudaGetLastError();
             return TT_ERR_CUDA;
         }
+        g_sm_count[dev] = n;
         g_scratch_addr[dev] = static_cast<float*>(p);
     }
     *out = g_scratch_addr[dev];
+    *sms = g_sm_count[dev];
     return TT_OK;
 }
 
@@ -146,7 +152,8 @@ extern "C" tt_status tt_emb_forward_noalloc(int64_t num_embeddings, const int64_
     const int64_t ts = (int64_t)q[0] * q[1] * ranks[1];
     if (ts * kWarps > kScratchFloats) return TT_ERR_SHAPE;
     float* scratch = nullptr;
-    tt_status st = scratch_address(&scratch);
+    int sms = 0;
+    tt_status st = scratch_address(&scratch, &sms);
     if (st != TT_OK) return st;
     if (num_bags == 0) return TT_OK;
     NoAllocArgs a{};
@@ -166,7 +173,7 @@ extern "C" tt_status tt_emb_forward_noalloc(int64_t num_embeddings, const int64_
     a.err = err_dev;
     // whole blocks of warps, every warp's slot inside the array
     int64_t warps = (num_bags + kWarps - 1) / kWarps * kWarps;
-    if (warps > kMaxGridWarps) warps = kMaxGridWarps;
+    if (warps > (int64_t)sms * kWarpsPerSm) warps = (int64_t)sms * kWarpsPerSm;
     if (warps * ts > kScratchFloats) warps = (kScratchFloats / ts) / kWarps * kWarps;
     const unsigned blocks = (unsigned)(warps / kWarps);
     k_pool_noalloc<<<blocks, kWarps * 32, 0, reinterpret_cast<cudaStream_t>(stream)>>>(a, scratch);

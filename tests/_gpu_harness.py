@@ -6,6 +6,9 @@ max_j |gpu - oracle| <= 1e-4 * max_j |oracle|; for every updated core slice,
 max |gpu - oracle| <= 1e-4 * max |oracle slice|.  Decoded slice indices and
 bag ids must match bit for bit.
 """
+import concurrent.futures as cf
+import os
+
 import numpy as np
 import torch
 
@@ -108,6 +111,48 @@ def check_forward(out_gpu, wl, bags=None):
     assert_rows_close(got, ref, "forward")
 
 
+def _bag_range(wl, b0, b1):
+    """Bags [b0, b1) of every table of `wl` as (indices, offsets, weights, grad_out, batch)."""
+    idx, lens, go, w = [], [], [], []
+    for t in range(wl.num_tables):
+        g0, g1 = t * wl.batch + b0, t * wl.batch + b1
+        lo, hi = int(wl.offsets[g0]), int(wl.offsets[g1])
+        idx.append(wl.indices[lo:hi])
+        lens.append(np.diff(wl.offsets[g0:g1 + 1]))
+        go.append(wl.grad_out[g0:g1])
+        if wl.weights is not None:
+            w.append(wl.weights[lo:hi])
+    off = np.concatenate([[0], np.cumsum(np.concatenate(lens))]).astype(np.int64)
+    return (np.concatenate(idx), off, None if wl.weights is None else np.concatenate(w),
+            np.concatenate(go), b1 - b0)
+
+
+def oracle_grad(wl, t, k, slices, cores=None, chunks=None):
+    """oracle.backward_core of slices `slices` of core k of table t over the whole
+    workload.  The gradient is a sum over bags, so for many lookups the oracle runs on
+    ranges of bags in parallel threads (the C oracle releases the GIL) and the float64
+    partial gradients are added in range order."""
+    cores = cores if cores is not None else wl.cores
+    sl = np.asarray(slices, dtype=np.int64)
+    if chunks is None:
+        chunks = 1 if wl.nnz < 40000 else min(wl.batch, 4 * (os.cpu_count() or 4))
+    if chunks <= 1:
+        return oracle.backward_core(wl.tables, cores, wl.indices, wl.offsets, wl.grad_out, t, k, wl.weights,
+                                    wl.mode, wl.batch, sl)
+    edges = np.linspace(0, wl.batch, chunks + 1).astype(np.int64)
+
+    def part(c):
+        idx, off, w, go, nb = _bag_range(wl, int(edges[c]), int(edges[c + 1]))
+        return oracle.backward_core(wl.tables, cores, idx, off, go, t, k, w, wl.mode, nb, sl)
+
+    with cf.ThreadPoolExecutor(max_workers=min(chunks, os.cpu_count() or 4)) as ex:
+        parts = list(ex.map(part, range(chunks)))
+    total = parts[0]
+    for p in parts[1:]:
+        total = total + p
+    return total
+
+
 def check_cores(run, wl, dec, slices=None):
     """Updated cores vs oracle on `slices` (per table, per core; None = all) after one
     step from the workload's cores; slices no lookup touched must keep their exact bits."""
@@ -121,27 +166,34 @@ def check_cores(run, wl, dec, slices=None):
             sl = touched[t][k] if slices is None else np.asarray(slices[t][k], dtype=np.int64)
             if sl.size == 0:
                 continue
-            ref = oracle.workload_sgd_slices(wl, t, k, sl)
+            ref = oracle.sgd_update(wl.cores[t][k][sl], oracle_grad(wl, t, k, sl), wl.lr)
             assert_rows_close(after[t][k][sl], ref, f"table {t} core G{k + 1}")
 
 
-def sample_slices(wl, dec, rng, per_core=6, max_count=None):
-    """Touched slices with the fewest lookups plus a few random ones (cheap for the oracle)."""
+def sample_slices(wl, dec, rng, per_core=6, max_count=None, hot=2):
+    """Per table and core: the `hot` touched slices with the most lookups (the longest
+    sorted-segment and multi-tile reductions), the touched slices with the fewest
+    lookups, and random ones; `max_count` bounds only the cold and random picks.
+    Every core with a touched slice gets at least one sampled slice."""
     i1, i2, i3, bag = dec
     table = bag // wl.batch
     out = []
     for t in range(wl.num_tables):
         m = table == t
         row = []
-        for ik in (i1[m], i2[m], i3[m]):
-            u, c = np.unique(ik, return_counts=True)
+        for k, ik in enumerate((i1[m], i2[m], i3[m])):
+            u_all, c_all = np.unique(ik, return_counts=True)
+            pick = list(u_all[np.argsort(-c_all, kind="stable")[:hot]])
+            u, c = u_all, c_all
             if max_count is not None:
                 keep = c <= max_count
                 u, c = u[keep], c[keep]
             order = np.argsort(c, kind="stable")
-            pick = list(u[order[: per_core // 2]])
+            pick += list(u[order[: per_core // 2]])
             if u.size:
-                pick += list(rng.choice(u, size=min(per_core - len(pick), u.size), replace=False))
-            row.append(np.unique(np.array(pick, dtype=np.int64)))
+                pick += list(rng.choice(u, size=min(max(per_core - per_core // 2, 0), u.size), replace=False))
+            sel = np.unique(np.array(pick, dtype=np.int64))
+            assert u_all.size == 0 or sel.size > 0, f"no sampled slice for table {t} core G{k + 1}"
+            row.append(sel)
         out.append(row)
     return out

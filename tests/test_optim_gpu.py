@@ -21,7 +21,8 @@ import torch
 import oracle
 import tensor_train_compressed_embeddingbag_gb300 as tt
 
-from _gpu_harness import GpuRun, assert_rows_close, check_decode, check_forward, dev, sample_slices, touched_slices
+from _gpu_harness import (GpuRun, assert_rows_close, check_decode, check_forward, dev, oracle_grad, sample_slices,
+                          touched_slices)
 
 pytestmark = pytest.mark.gpu
 
@@ -65,7 +66,7 @@ def _check_grad(wl, slices=None, bags=None, seed=0):
             assert not g[un].any(), f"untouched slices of t{t} G{k + 1} have a nonzero gradient"
             sl = touched[t][k] if sel is None else sel[t][k]
             if len(sl):
-                ref = oracle.workload_backward_core(wl, t, k, sl)
+                ref = oracle_grad(wl, t, k, sl)
                 assert_rows_close(g[sl], ref, f"gradient t{t} G{k + 1}")
     run.close()
 
@@ -84,7 +85,8 @@ def _check_adagrad(wl, state, slices=None, bags=None):
             np.testing.assert_array_equal(st[un], state[t][k][un], err_msg=f"untouched state t{t} G{k + 1}")
             sl = touched[t][k] if sel is None else sel[t][k]
             if len(sl):
-                ref_g, ref_s = oracle.workload_adagrad_slices(wl, t, k, state[t][k].astype(np.float64), EPS, sl)
+                ref_g, ref_s = oracle.adagrad_update(wl.cores[t][k][sl], state[t][k][sl], oracle_grad(wl, t, k, sl),
+                                                     wl.lr, EPS)
                 assert_rows_close(after[t][k][sl], ref_g, f"Adagrad core t{t} G{k + 1}")
                 assert_rows_close(st[sl], ref_s, f"Adagrad accumulator t{t} G{k + 1}")
     run.close()
@@ -102,6 +104,18 @@ def test_gradient_mode_tiny(workloads):
 def test_gradient_mode_fbtt_sample_sampled(workloads):
     """11M x 64 rank-32, 512 bags: sampled slices; every untouched slice exactly 0."""
     _check_grad(workloads(2), slices=_sampler(1), bags=np.arange(0, 512, 7))
+
+
+def test_gradient_mode_zipf_weighted_mean_full_sampled(workloads):
+    """Zipf weighted mean, 4096 bags (large-path sort): gradients of the hottest,
+    the coldest and random slices against the oracle."""
+    _check_grad(workloads(3), slices=_sampler(11, per_core=6, max_count=2000), bags=np.arange(0, 4096, 37))
+
+
+def test_gradient_mode_large_rank64_scaled(workloads):
+    """40M x 128 rank 64, Zipf, 512 bags (15k lookups: the large-path sort and the
+    rank-64 class): gradients compared directly, not through an update."""
+    _check_grad(workloads(4, 512), slices=_sampler(12, per_core=6), bags=np.arange(0, 512, 11))
 
 
 def test_gradient_mode_table_batched(workloads):
