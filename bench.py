@@ -14,8 +14,11 @@ during the timed region and the float64 oracle timed on the host cores
 samples of the same workload.
 
 Launch: ``python bench.py --gpus 1 --steps K --warmup W``; for N > 1 under
-``torch.distributed.run`` every rank runs an independent replica on its own
-GPU (weak scaling, no collective on the data path); rank 0 prints.
+``torch.distributed.run`` every rank takes its own share of a batch of N times
+the workload's bags (weak scaling), runs forward and backward with the core
+gradients written out, the gradients are summed over the ranks (one NCCL
+all-reduce) and every rank applies the same SGD update; rank 0 prints.
+``--dp`` runs that data-parallel step at N = 1 too.
 
 ``--config N`` times another of the seeded workloads instead (1 tiny, 3 Zipf
 weighted-mean with its 110,000 hot rows, 4 40M x 128 rank-64, 5 26 tables);
@@ -38,12 +41,15 @@ sys.path.insert(0, ROOT)
 
 METRIC = "TT-EmbeddingBag fwd+bwd ns/nnz (lookups/s) and % of roofline, 1×GB300"
 WORKLOAD = "TT-EmbeddingBag 11M x 64 rank-32 (p=[200,220,250], q=[4,4,4]), B=512 x 20 uniform lookups, sum, fused SGD"
-SM_COUNT = 152
 FP32_LANES_PER_SM = 128
 SM_MAX_MHZ = 2070.0
+# nominal dense tensor rates of the part (PFLOP/s): TF32 1.1, BF16 2.25
+TF32_PER_BF16 = 1.1 / 2.25
 L2_FLUSH_BYTES = 256 << 20
 # FBTT README sample output for this exact workload: 0.416 us per lookup, fwd + bwd (GPU not stated)
 PAGES_NS_PER_NNZ = 416.0
+TRAFFIC_FILE = os.path.join(ROOT, "profiles", "dram_traffic.json")
+CSRC = os.path.join(ROOT, "tensor_train_compressed_embeddingbag_gb300", "csrc")
 
 
 def peaks():
@@ -56,9 +62,40 @@ def peaks():
         return {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "sm_max_mhz": SM_MAX_MHZ}, "fallback"
 
 
-def fp32_peak_tflops(sm_mhz):
-    # FFMA: 128 lanes x 2 FLOP per SM per clock
-    return SM_COUNT * FP32_LANES_PER_SM * 2 * sm_mhz * 1e6 / 1e12
+def fp32_peak_tflops(sms, sm_mhz):
+    """FFMA peak: 128 FP32 lanes x 2 FLOP per SM per clock, SM count read from the device."""
+    return sms * FP32_LANES_PER_SM * 2 * sm_mhz * 1e6 / 1e12
+
+
+def tf32x3_peak_tflops(pk):
+    """Useful rate of a 3xTF32 contraction: the measured dense bf16 burst x the nominal
+    TF32:BF16 ratio, / 3 (three TF32 products per useful product)."""
+    return pk["bf16_tflops"] * TF32_PER_BF16 / 3.0
+
+
+def source_sha(files):
+    import hashlib
+
+    h = hashlib.sha256()
+    for f in files:
+        with open(os.path.join(CSRC, f), "rb") as fh:
+            h.update(fh.read())
+    return h.hexdigest()[:16]
+
+
+def measured_traffic(kernel):
+    """DRAM bytes per launch of `kernel` from the committed ncu record, or None when the
+    record is missing or the kernel's sources changed since it was taken."""
+    try:
+        with open(TRAFFIC_FILE) as f:
+            rec = json.load(f).get(kernel)
+    except (OSError, ValueError):
+        return None, "no ncu record"
+    if not rec:
+        return None, "no ncu record"
+    if rec.get("source_sha") != source_sha(rec.get("sources", [])):
+        return None, "kernel changed since the ncu record"
+    return float(rec["bytes_per_launch"]), rec.get("note", "")
 
 
 def flops_per_lookup(spec):
@@ -92,6 +129,41 @@ def lookup_flops(wl):
         sa += A * n
         sb += Bc * n
     return sa, sb
+
+
+# Which pipe runs each kernel's contractions (the rank-16 / rank-32 classes with
+# q = [4, 4, 4] take the tensor-core paths).
+def tc_class(spec):
+    return list(spec.q) == [4, 4, 4] and spec.ranks[0] == spec.ranks[1] and spec.ranks[0] in (16, 32)
+
+
+def kernel_parts(wl):
+    """Per kernel: [(algorithmic FLOPs per launch, pipe)] with the per-lookup counts of
+    the path (A = q1 r1 q2 r2, Bc = q1 q2 r2 q3 per lookup): T = G1 G2 2A; row = T G3
+    2Bc; backward dT and the dG3 partial 4Bc, the dG1 partial and dG2 4A."""
+    out = {"fwd_T": [], "pool": [], "tile_bwd": []}
+    acc = {}
+    for t, spec in enumerate(wl.tables):
+        n = int(wl.offsets[(t + 1) * wl.batch] - wl.offsets[t * wl.batch])
+        A, Bc = flops_per_lookup(spec)
+        tc = tc_class(spec)
+        for k, f, pp in (("fwd_T", 2 * A * n, "tensor" if tc else "fp32"), ("pool", 2 * Bc * n, "fp32"),
+                         ("tile_bwd", 4 * A * n, "fp32"), ("tile_bwd", 4 * Bc * n, "fp32")):
+            acc[(k, pp)] = acc.get((k, pp), 0) + f
+    for (k, pp), f in acc.items():
+        out[k].append((f, pp))
+    return out
+
+
+def peak_source(parts, pipe_peak, sms, sm_mhz, kind):
+    txt = []
+    for f, pp in parts:
+        if pp == "fp32":
+            txt.append(f"{f:.3g} FLOP on FP32 FFMA at {pipe_peak['fp32']:.1f} TFLOP/s ({sms} SMs x 128 x 2 x {sm_mhz:.0f} MHz)")
+        else:
+            txt.append(f"{f:.3g} FLOP on tensor cores (3xTF32) at {pipe_peak['tensor']:.1f} TFLOP/s (bf16 burst of "
+                       f"{kind} peaks x 1.1/2.25 / 3)")
+    return "; ".join(txt) + "; peak = FLOPs / sum(FLOPs_pipe / peak_pipe)"
 
 
 def max_over_ranks(values, device=None):
@@ -319,7 +391,20 @@ def run_gpu(args):
     tt.build()
     tt.load_library()
 
+    # data-parallel step (N > 1, or --dp): every rank takes its own share of a batch of
+    # N times the workload's bags, the core gradients are summed over the ranks (NCCL)
+    # and every rank applies the same update; N = 1 without --dp runs the fused step
+    dp = ws > 1 or args.dp
     wl = tt_inputs.config(args.config)
+    if dp:
+        if args.optimizer == "grad" or args.cache != "none":
+            raise SystemExit("the data-parallel step takes --optimizer sgd|adagrad and no cache")
+        if ws > 1:
+            full = tt_inputs.config(args.config, batch=wl.batch * ws)
+            bags, look, off_r = tt.shard_bags(full.offsets, full.num_tables, rank, ws)
+            wl = tt_inputs.Workload(**{**full.__dict__, "indices": full.indices[look], "offsets": off_r,
+                                       "weights": None if full.weights is None else full.weights[look],
+                                       "grad_out": full.grad_out[bags], "batch": bags.shape[0] // full.num_tables})
     spec = wl.tables[0]
     D, nnz, B = spec.embedding_dim, wl.nnz, wl.num_bags
     cores = [torch.from_numpy(c).to(dev) for t in wl.cores for c in t]
@@ -329,7 +414,12 @@ def run_gpu(args):
         h = tt.tt_emb_batch_create([(s.num_embeddings, s.p, s.q, s.ranks, cores[3 * t:3 * t + 3])
                                     for t, s in enumerate(wl.tables)])
     aux = None
-    if args.optimizer == "adagrad":  # fused element-wise Adagrad, accumulators starting at 0
+    dpstep = None
+    if dp:
+        aux = [torch.zeros_like(c) for c in cores] if args.optimizer == "adagrad" else None
+        dpstep = tt.DataParallelStep(h, cores, optim=tt.TT_OPT_ADAGRAD if aux else tt.TT_OPT_SGD, eps=1.0e-10,
+                                     state=aux)
+    elif args.optimizer == "adagrad":  # fused element-wise Adagrad, accumulators starting at 0
         aux = [torch.zeros_like(c) for c in cores]
         tt.tt_emb_set_optimizer(h, tt.TT_OPT_ADAGRAD, 1.0e-10, aux)
     elif args.optimizer == "grad":  # sparse=False: the gradients are written out, the cores stay
@@ -354,6 +444,9 @@ def run_gpu(args):
     lr = wl.lr
 
     def step():
+        if dpstep is not None:
+            dpstep(idx, off, wts, mode, out, go, lr, stream)
+            return
         tt.tt_emb_forward(h, idx, off, wts, mode, out, stream)
         tt.tt_emb_backward(h, go, lr, stream)
 
@@ -395,7 +488,7 @@ def run_gpu(args):
         tt.tt_emb_set_stage_timing(h, False)
         return g
 
-    graph = capture(False) if not args.eager else None
+    graph = capture(False) if not (args.eager or dp) else None
     run_step = graph.replay if graph is not None else step
     for _ in range(max(3, args.warmup)):
         run_step()
@@ -423,16 +516,22 @@ def run_gpu(args):
     ms_fwd = timed(lambda: tt.tt_emb_forward(h, idx, off, wts, mode, out, stream), args.steps)
 
     # per-kernel durations: a graph of the same step with an event after every kernel
-    gstage = capture(True)
+    gstage = capture(True) if not dp else None
     kstats = {}
     nstage = min(args.steps, 400)
     barrier()
+    if dp:
+        tt.tt_emb_set_stage_timing(h, True)
     for _ in range(nstage):
         flush.fill_(1.0)
-        gstage.replay()
+        if gstage is not None:
+            gstage.replay()
+        else:
+            step()
         for which in (0, 1):
             for name, ms in tt.tt_emb_stage_times(h, which):
                 kstats.setdefault(name, []).append(ms)
+    tt.tt_emb_set_stage_timing(h, False)
     kavg = {k: sum(v) / len(v) for k, v in kstats.items()}
     del gstage, graph
 
@@ -465,6 +564,10 @@ def run_gpu(args):
             out_h.copy_(out, non_blocking=True)
         stream.wait_event(ev_go)
         tt.tt_emb_backward(h, go, lr, stream)
+        if dpstep is not None:  # the rest of the data-parallel step: all-reduce, update
+            if ws > 1:
+                dist.all_reduce(dpstep.flat)
+            tt.tt_emb_apply_gradients(h, dpstep.optim, lr, dpstep.grads, dpstep.state, dpstep.eps, stream)
         ev_bwd.record(stream)
         stream.wait_stream(side)  # the step ends when its output is on the host
 
@@ -474,29 +577,35 @@ def run_gpu(args):
     result = None
     if rank == 0:
         pk, pk_kind = peaks()
+        sms = torch.cuda.get_device_properties(dev).multi_processor_count
         sA, sB = lookup_flops(wl)
         total_lookups = nnz * args.steps * ws
         value = total_lookups / (ms_total / 1e3)
-        # dominant kernel and its algorithmic FLOPs per launch (per-lookup figures x lookups)
-        kernel_flops = {
-            "fwd_T": 2 * sA,                    # T = G1 G2, per lookup 2 q1 r1 q2 r2
-            "pool": 2 * sB,                     # row = T G3, per lookup 2 q1 q2 r2 q3
-            "tile_bwd": 4 * (sA + sB),          # dT, dG3, dG1, dG2, per lookup 4 (A + Bc)
-        }
+        sm_mhz = float(pk.get("sm_max_mhz", SM_MAX_MHZ))
+        pipe_peak = {"fp32": fp32_peak_tflops(sms, sm_mhz), "tensor": tf32x3_peak_tflops(pk)}
+        parts = kernel_parts(wl)
+        step_ms = ms_total / args.steps
+        # ideal time of every kernel: its algorithmic FLOPs at the peak of the pipe that runs them
+        ideal_ms = {k: sum(f / (pipe_peak[pp] * 1e12) for f, pp in v) * 1e3 for k, v in parts.items()}
+        kflops = {k: sum(f for f, _ in v) for k, v in parts.items()}
         dom = max(kavg, key=kavg.get)
-        sm_mhz = SM_MAX_MHZ
-        peak_tf = fp32_peak_tflops(sm_mhz)
-        if dom in kernel_flops:
-            ach = kernel_flops[dom] / (kavg[dom] * 1e-3) / 1e12
-            roof = {"bound": "alu", "achieved": ach, "peak": peak_tf, "unit": "TFLOP/s", "frac": ach / peak_tf,
-                    "traffic": None, "kernel": dom, "avg_ms": kavg[dom],
-                    "peak_source": "FP32 FFMA: 152 SMs x 128 lanes x 2 FLOP x 2070 MHz"}
+        if dom in parts:
+            ach = kflops[dom] / (kavg[dom] * 1e-3) / 1e12
+            eff_peak = kflops[dom] / (ideal_ms[dom] * 1e-3) / 1e12
+            pipes = sorted({pp for _, pp in parts[dom]})
+            traffic, tnote = measured_traffic(dom)
+            roof = {"bound": "tensor" if pipes == ["tensor"] else "alu", "achieved": ach, "peak": eff_peak,
+                    "unit": "TFLOP/s", "frac": ach / eff_peak, "traffic": traffic, "traffic_note": tnote,
+                    "kernel": dom, "avg_ms": kavg[dom], "pipes": {pp: f for f, pp in parts[dom]},
+                    "peak_source": peak_source(parts[dom], pipe_peak, sms, sm_mhz, pk_kind)}
         else:
             roof = {"bound": "hbm", "achieved": None, "peak": pk["hbm_gbs"], "unit": "GB/s", "frac": None,
                     "traffic": None, "kernel": dom, "avg_ms": kavg[dom]}
         step_flops = 6 * (sA + sB)
         dedup_flops = dedup_step_flops(wl)
-        step_tf = step_flops / (ms_total / args.steps * 1e-3) / 1e12
+        step_tf = step_flops / (step_ms * 1e-3) / 1e12
+        fwd_ms = ms_fwd / args.steps
+        fwd_ideal = ideal_ms.get("fwd_T", 0.0) + ideal_ms.get("pool", 0.0)
         result = {
             "metric": METRIC,
             "value": value,
@@ -521,22 +630,38 @@ def run_gpu(args):
                 "l2": f"flushed before every timed step ({L2_FLUSH_BYTES >> 20} MiB write, outside the events)",
                 "optimizer": {"sgd": "fused SGD", "adagrad": "fused element-wise Adagrad",
                               "grad": "sparse=False (gradients written out)"}[args.optimizer],
-                "replicas": ws,
+                "parallelism": (f"data parallel over {ws} GPUs: bags split, NCCL sum all-reduce of the core "
+                                f"gradients, same update on every rank" if dp and ws > 1 else
+                                "data-parallel step on one GPU (gradients out, update), no all-reduce" if dp else
+                                "one GPU, fused update"),
+                "global_bags": B * ws,
                 "cache": {"none": "none", "coherent": "110,000 hot rows, exact copies",
                           "trainable": "110,000 hot rows, trainable"}[args.cache],
             },
-            "timing": "CUDA graph of forward + backward replayed per step" if not args.eager else "eager launches",
+            "timing": ("CUDA graph of forward + backward replayed per step" if not (args.eager or dp) else
+                       "eager launches"),
             "eager": {"ms_per_step": ms_eager / args.steps, "host_enqueue_us_per_step": host_us},
             "forward": {"ns_per_nnz": 1e6 * ms_fwd / (nnz * args.steps),
                         "lookups_per_s": nnz * args.steps * ws / (ms_fwd / 1e3),
-                        "achieved_tflops": 2 * (sA + sB) / (ms_fwd / args.steps * 1e-3) / 1e12,
-                        "frac": 2 * (sA + sB) / (ms_fwd / args.steps * 1e-3) / 1e12 / peak_tf,
-                        "flop_formula": "2 (q1 r1 q2 r2 + q1 q2 r2 q3) per lookup, against the FP32 peak"},
-            "step_roofline": {"flops_per_step": step_flops, "achieved_tflops": step_tf, "peak_tflops": peak_tf,
-                              "frac": step_tf / peak_tf, "flop_formula": "6 (q1 r1 q2 r2 + q1 q2 r2 q3) per lookup",
+                        "achieved_tflops": 2 * (sA + sB) / (fwd_ms * 1e-3) / 1e12,
+                        "frac": fwd_ideal / fwd_ms,
+                        "flop_formula": "2 (q1 r1 q2 r2 + q1 q2 r2 q3) per lookup; frac = sum over the forward "
+                                        "kernels of FLOPs / peak of the pipe that runs them, over the forward time"},
+            "step_roofline": {"flops_per_step": step_flops, "achieved_tflops": step_tf,
+                              "ideal_ms": sum(ideal_ms.values()), "frac": sum(ideal_ms.values()) / step_ms,
+                              "frac_formula": "sum over kernels of (algorithmic FLOPs / peak of the pipe that runs "
+                                              "them), divided by ms_per_step",
+                              "per_kernel": {k: {"flops": kflops[k], "ideal_ms": ideal_ms[k],
+                                                 "avg_ms": kavg.get(k), "pipes": {pp: f for f, pp in parts[k]}}
+                                             for k in parts},
+                              "fp32_frac_of_step": step_tf / pipe_peak["fp32"],
+                              "flop_formula": "6 (q1 r1 q2 r2 + q1 q2 r2 q3) per lookup",
                               "dedup_flops_per_step": dedup_flops,
-                              "dedup_frac": dedup_flops / (ms_total / args.steps * 1e-3) / 1e12 / peak_tf,
                               "dedup_formula": "6 q1 r1 q2 r2 per touched (i1, i2) pair + 6 q1 q2 r2 q3 per lookup"},
+            "peaks": {"sms": sms, "sm_mhz": sm_mhz, "fp32_tflops": pipe_peak["fp32"],
+                      "tf32x3_tflops": pipe_peak["tensor"], "source": pk_kind,
+                      "fp32_formula": f"{sms} SMs (device) x 128 lanes x 2 FLOP x {sm_mhz:.0f} MHz",
+                      "tf32x3_formula": f"measured bf16 burst {pk['bf16_tflops']} x 1.1/2.25 (nominal TF32:BF16) / 3"},
             "roofline": roof,
             "kernels_ms": kavg,
             "gpu_launches": launches_per_step * args.steps,
@@ -573,6 +698,8 @@ def main():
     ap.add_argument("--impl", choices=["gb300", "reference"], default="gb300")
     ap.add_argument("--no-cpu-baseline", action="store_true", help="skip the oracle timing")
     ap.add_argument("--eager", action="store_true", help="time eager launches instead of a CUDA graph replay")
+    ap.add_argument("--dp", action="store_true",
+                    help="run the data-parallel step (gradients out, all-reduce, update) also at N = 1")
     ap.add_argument("--optimizer", choices=["sgd", "adagrad", "grad"], default="sgd",
                     help="what the backward does with the core gradients (default: fused SGD)")
     ap.add_argument("--config", type=int, choices=[1, 2, 3, 4, 5], default=2,

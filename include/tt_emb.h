@@ -171,6 +171,32 @@ tt_status tt_emb_backward(tt_emb* h, const float* grad_out_dev, float lr, tt_str
 tt_status tt_emb_set_optimizer(tt_emb* h, int32_t optim, float eps, float* const* aux);
 
 /*
+ * Update from summed gradients: the data-parallel step.  Bags are independent
+ * in the forward pass and every core gradient is a sum over bags, so ranks that
+ * hold disjoint shares of a batch's bags and identical cores can each run
+ * tt_emb_forward + tt_emb_backward with TT_OPT_GRAD on their share, sum the
+ * gradient buffers over the ranks (one all-reduce, outside this library), and
+ * then apply the same update on every rank with this call; the cores then equal
+ * those of one fused step over the whole batch, up to the order of summation.
+ * The update rules are those of tt_emb_set_optimizer (FBTT README,
+ * "Parameters": optimizer, learning_rate, eps; "Fused Kernel").
+ *   optim      TT_OPT_SGD (G -= lr g) or TT_OPT_ADAGRAD (s += g^2;
+ *              G -= lr g / (sqrt(s) + eps))
+ *   grads_dev  3 * num_tables caller-owned device pointers (table-major, each
+ *              shaped like its core, 16-byte aligned): the summed gradients
+ *   state_dev  3 * num_tables Adagrad accumulators (same layout), updated in
+ *              place; NULL for TT_OPT_SGD
+ * An element whose summed gradient is exactly 0 keeps its bits (as every
+ * element of an untouched slice does in the fused step).  An exact-copy
+ * hot-row cache sees the changed slices as stale.  Allocates nothing;
+ * asynchronous on `stream`.  Returns TT_ERR_ARG (null or misaligned
+ * pointers, unknown optim, bad eps), TT_ERR_STATE (trainable cache rows,
+ * whose gradients this call does not carry), TT_ERR_CUDA.
+ */
+tt_status tt_emb_apply_gradients(tt_emb* h, int32_t optim, float lr, float eps, float* const* grads_dev,
+                                 float* const* state_dev, tt_stream stream);
+
+/*
  * Expand rows [row0, row0 + nrows) of table `table` (0 for a single-table
  * handle) to a dense float [nrows][D] block (FBTT README,
  * "TableBatchedTTEmbeddingBag": expanding to full weight).  Row i of the table
@@ -310,6 +336,19 @@ int tt_emb_stage_times(tt_emb* h, int which /* 0 forward, 1 backward */, float* 
 
 /* Kernels launched by the most recent forward (which = 0) or backward (1). */
 int tt_emb_last_launch_count(tt_emb* h, int which);
+
+/*
+ * Bound of the handle's device waits.  The pages have no counterpart: the
+ * tensor-core kernels wait for their own MMAs on an mbarrier, at most `polls`
+ * polls (default 2^24, far longer than any MMA batch).  A wait that gives up
+ * records TT_ERR_TIMEOUT (read by tt_emb_get_last_error), issues no further
+ * MMA, waits with the default bound for the MMAs already in flight and frees
+ * its tensor memory; the call's results are then undefined and a following
+ * backward changes no core.  polls = 0 makes every such wait give up at once
+ * (a test of that path).  Takes effect from the next call.  Returns
+ * TT_ERR_ARG for a null handle.
+ */
+tt_status tt_emb_set_wait_limit(tt_emb* h, uint32_t polls);
 
 /*
  * Forward pass that allocates no device memory.  The pages have no

@@ -59,6 +59,10 @@ __all__ = [
     "tt_emb_last_launch_count",
     "tt_emb_status_string",
     "tt_emb_forward_noalloc",
+    "tt_emb_apply_gradients",
+    "tt_emb_set_wait_limit",
+    "shard_bags",
+    "DataParallelStep",
     "EXPORTED_SYMBOLS",
     "TTEmbeddingBag",
     "TableBatchedTTEmbeddingBag",
@@ -94,6 +98,8 @@ EXPORTED_SYMBOLS = (
     "tt_emb_last_launch_count",
     "tt_emb_status_string",
     "tt_emb_forward_noalloc",
+    "tt_emb_apply_gradients",
+    "tt_emb_set_wait_limit",
 )
 
 
@@ -166,6 +172,8 @@ def load_library():
             "tt_emb_forward_noalloc": (ctypes.c_int, [i64, ctypes.POINTER(i64), ctypes.POINTER(i32),
                                                       ctypes.POINTER(i32), ctypes.POINTER(vp), vp, i64, vp, i64,
                                                       vp, ctypes.c_int, vp, vp, vp]),
+            "tt_emb_apply_gradients": (ctypes.c_int, [vp, i32, f32, f32, ctypes.POINTER(vp), ctypes.POINTER(vp), vp]),
+            "tt_emb_set_wait_limit": (ctypes.c_int, [vp, ctypes.c_uint32]),
         }
         for name, (res, args) in sig.items():
             fn = getattr(lib, name)
@@ -379,6 +387,94 @@ def tt_emb_forward_noalloc(num_embeddings: int, p: Sequence[int], q: Sequence[in
         ptrs, _ptr(indices), indices.numel(), _ptr(offsets), offsets.numel() - 1, _ptr(weights), int(mode),
         _ptr(out), _ptr(err), _stream(stream))
     _check(st, "tt_emb_forward_noalloc")
+
+
+def tt_emb_apply_gradients(h, optim: int, lr: float, grads: Sequence[torch.Tensor],
+                           state: Optional[Sequence[torch.Tensor]] = None, eps: float = 0.0, stream=None):
+    """The update of the cores from summed gradients (TT_OPT_SGD or TT_OPT_ADAGRAD).
+
+    grads / state: 3 * num_tables float32 device tensors shaped like the cores
+    (table-major); elements with a zero summed gradient keep their bits."""
+    for t in grads:
+        _cuda_f32(t, "grads")
+    garr = (ctypes.c_void_p * len(grads))(*[t.data_ptr() for t in grads])
+    sarr = None
+    if state is not None:
+        for t in state:
+            _cuda_f32(t, "state")
+        sarr = (ctypes.c_void_p * len(state))(*[t.data_ptr() for t in state])
+    _check(load_library().tt_emb_apply_gradients(h, int(optim), float(lr), float(eps), garr, sarr, _stream(stream)),
+           "tt_emb_apply_gradients")
+
+
+def tt_emb_set_wait_limit(h, polls: int):
+    """Polls before a bounded device wait gives up (default 2^24; 0 exercises the give-up path)."""
+    _check(load_library().tt_emb_set_wait_limit(h, int(polls)), "tt_emb_set_wait_limit")
+
+
+# ---------------------------------------------------------------- data-parallel step
+
+
+def shard_bags(offsets, num_tables: int, rank: int, world: int):
+    """This rank's share of a batch (host arrays, bags table-major).
+
+    Every table's B bags are split into `world` contiguous ranges of near-equal
+    size; rank r takes range r of every table.  Returns ``(bag ids, lookup ids,
+    rebased CSR offsets)`` as numpy int64 arrays: the rank's bags in table-major
+    order, the positions of their lookups in the full batch, and the offsets of
+    the rank's own [len(bag ids) + 1] CSR layout.  Slicing indices, weights and
+    grad_out with them gives the rank's call arguments."""
+    import numpy as np
+
+    off = np.asarray(offsets, dtype=np.int64)
+    nb = off.shape[0] - 1
+    if num_tables < 1 or nb % num_tables or not (0 <= rank < world):
+        raise ValueError("bags must be a multiple of the tables and 0 <= rank < world")
+    B = nb // num_tables
+    b0, b1 = (B * rank) // world, (B * (rank + 1)) // world
+    bags = np.concatenate([np.arange(t * B + b0, t * B + b1, dtype=np.int64) for t in range(num_tables)])
+    lens = off[bags + 1] - off[bags]
+    look = np.concatenate([np.arange(off[g], off[g + 1], dtype=np.int64) for g in bags]) if bags.size else \
+        np.zeros(0, dtype=np.int64)
+    return bags, look, np.concatenate([[0], np.cumsum(lens)]).astype(np.int64)
+
+
+class DataParallelStep:
+    """One data-parallel training step of a handle whose cores are replicated on
+    every rank: the rank's share of the bags runs forward and backward with the
+    gradients written out (TT_OPT_GRAD), one all-reduce (sum) of a flat buffer
+    holding every core's gradient goes over ``torch.distributed``, and every
+    rank applies the same update (``tt_emb_apply_gradients``).  The cores then
+    equal one fused step over the whole batch up to the order of summation.
+
+    optim: TT_OPT_SGD or TT_OPT_ADAGRAD (``state``: the accumulators, shaped like
+    the cores, table-major)."""
+
+    def __init__(self, h, cores: Sequence[torch.Tensor], optim: int = TT_OPT_SGD, eps: float = 0.0,
+                 state: Optional[Sequence[torch.Tensor]] = None, group=None):
+        if optim not in (TT_OPT_SGD, TT_OPT_ADAGRAD):
+            raise TTError(TT_ERR_ARG, "DataParallelStep optim")
+        self.h, self.optim, self.eps, self.state, self.group = h, optim, float(eps), state, group
+        sizes = [c.numel() for c in cores]
+        # every gradient view starts 16-byte aligned inside the one flat buffer
+        pad = [(-n) % 4 for n in sizes]
+        self.flat = torch.zeros(sum(n + p for n, p in zip(sizes, pad)), dtype=torch.float32, device=cores[0].device)
+        self.grads, o = [], 0
+        for c, n, p in zip(cores, sizes, pad):
+            self.grads.append(self.flat[o:o + n].view(c.shape))
+            o += n + p
+        tt_emb_set_optimizer(h, TT_OPT_GRAD, 0.0, self.grads)
+
+    def __call__(self, indices, offsets, weights, mode: int, out, grad_out, lr: float, stream=None):
+        import torch.distributed as dist
+
+        tt_emb_forward(self.h, indices, offsets, weights, mode, out, stream)
+        tt_emb_backward(self.h, grad_out, lr, stream)
+        if dist.is_available() and dist.is_initialized() and dist.get_world_size(self.group) > 1:
+            s = torch.cuda.current_stream() if stream is None else stream
+            with torch.cuda.stream(s):
+                dist.all_reduce(self.flat, op=dist.ReduceOp.SUM, group=self.group)
+        tt_emb_apply_gradients(self.h, self.optim, lr, self.grads, self.state, self.eps, stream)
 
 
 # ---------------------------------------------------------------- modules

@@ -303,6 +303,8 @@ tt_status build_handle(tt_emb* h, int ntab, const tt_table_desc* d) {
     {
         int sms = 0;  // few i2 groups: two k_fwd_T blocks share each group's pairs
         if (cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, h->device) != cudaSuccess) return TT_ERR_CUDA;
+        P.sms = sms;
+        P.wait_polls = kTcWaitPolls;
         // the tensor-core T path takes a whole (table, i2) group per block
         bool all_tc = true;
         for (const TableDev& T : h->tabs) all_tc = all_tc && fwd_tc_floats_of(T.dclass, T.r1, T.q2 * T.r2) > 0;
@@ -976,6 +978,55 @@ tt_status tt_emb_get_last_error(tt_emb* h) {
     if (err & kErrIndex) return TT_ERR_INDEX;
     if (err & kErrOffsets) return TT_ERR_ARG;
     if (err & kErrTimeout) return TT_ERR_TIMEOUT;
+    return TT_OK;
+}
+
+tt_status tt_emb_apply_gradients(tt_emb* h, int32_t optim, float lr, float eps, float* const* grads_dev,
+                                 float* const* state_dev, tt_stream stream) {
+    if (!h || !grads_dev) return TT_ERR_ARG;
+    if (optim != TT_OPT_SGD && optim != TT_OPT_ADAGRAD) return TT_ERR_ARG;
+    if (optim == TT_OPT_ADAGRAD && (!state_dev || !(eps >= 0.f && eps <= 3.0e38f))) return TT_ERR_ARG;
+    for (int i = 0; i < 3 * h->ntab; ++i) {
+        if (!grads_dev[i] || ((uintptr_t)grads_dev[i] & 15u) != 0) return TT_ERR_ARG;
+        if (optim == TT_OPT_ADAGRAD && (!state_dev[i] || ((uintptr_t)state_dev[i] & 15u) != 0)) return TT_ERR_ARG;
+    }
+    if (h->cache_train && h->cache_n > 0) return TT_ERR_STATE;  // cached values have gradients of their own
+    cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+    ApplyArgs a{};
+    a.opt = optim;
+    a.lr = lr;
+    a.eps = eps;
+    a.dstep = h->P.dstep;
+    for (int t = 0; t < h->ntab; ++t) {
+        const TableDev& T = h->tabs[t];
+        const int64_t sz[3] = {(int64_t)T.q1 * T.r1, (int64_t)T.r1 * T.q2 * T.r2, (int64_t)T.r2 * T.q3};
+        const int64_t np[3] = {T.p1, T.p2, T.p3};
+        float* G[3] = {T.G1, T.G2, T.G3};
+        const int64_t soff[3] = {0, T.p1, (int64_t)T.p1 + T.p2};
+        for (int k = 0; k < 3; ++k) {
+            const int sg = a.nseg;
+            a.G[sg] = G[k];
+            a.g[sg] = grads_dev[3 * t + k];
+            a.s[sg] = optim == TT_OPT_ADAGRAD ? state_dev[3 * t + k] : nullptr;
+            a.n[sg] = np[k] * sz[k];
+            a.slice_elems[sg] = sz[k];
+            a.stamp[sg] = (t == 0 && h->d_slice_stamp && !h->cache_train) ? h->d_slice_stamp + soff[k] : nullptr;
+            a.start[sg + 1] = a.start[sg] + (a.n[sg] + 3) / 4;
+            ++a.nseg;
+            if (a.nseg == kApplySegs || (t == h->ntab - 1 && k == 2)) {
+                if (launch_apply_grads(a, h->P.sms, s) != cudaSuccess) return TT_ERR_CUDA;
+                a.nseg = 0;
+                a.start[0] = 0;
+            }
+        }
+    }
+    h->last_stream = s;
+    return TT_OK;
+}
+
+tt_status tt_emb_set_wait_limit(tt_emb* h, uint32_t polls) {
+    if (!h) return TT_ERR_ARG;
+    h->P.wait_polls = polls;
     return TT_OK;
 }
 

@@ -800,6 +800,82 @@ __global__ void __launch_bounds__(kBwdThreads, 3) k_reduce13(const __grid_consta
     reduce_slice(P, b, slots, sh, sacc);
 }
 
+// ------------------------------------------------------------------ summed-gradient update
+
+// Data-parallel step: ranks that hold disjoint shares of the bags and the same
+// cores sum their gradients (an all-reduce outside the library); every rank then
+// applies the same update here.  An element whose summed gradient is exactly 0 is
+// left alone (bit-identical to an element of an untouched slice); the others take
+// the optimizer step of core_update.  Four elements per thread (float4 where the
+// four lie inside the segment; every segment starts 16-byte aligned).
+__global__ void __launch_bounds__(256) k_apply_grads(const __grid_constant__ ApplyArgs a) {
+    const int64_t tid = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
+    const int64_t nthreads = (int64_t)gridDim.x * blockDim.x;
+    for (int64_t q = tid; q < a.start[a.nseg]; q += nthreads) {
+        int sg = 0;
+        while (q >= a.start[sg + 1]) ++sg;
+        const int64_t e0 = (q - a.start[sg]) * 4;
+        const int64_t n = a.n[sg];
+        float* G = a.G[sg];
+        const float* g = a.g[sg];
+        float* st = a.s[sg];
+        bool any = false;
+        if (e0 + 4 <= n) {
+            const float4 gv = *reinterpret_cast<const float4*>(g + e0);
+            const float gg[4] = {gv.x, gv.y, gv.z, gv.w};
+            any = gv.x != 0.f || gv.y != 0.f || gv.z != 0.f || gv.w != 0.f;
+            if (any) {
+                float4 w = *reinterpret_cast<const float4*>(G + e0);
+                float ww[4] = {w.x, w.y, w.z, w.w};
+                if (a.opt == TT_OPT_ADAGRAD) {
+                    float4 sv = *reinterpret_cast<const float4*>(st + e0);
+                    float ss[4] = {sv.x, sv.y, sv.z, sv.w};
+#pragma unroll
+                    for (int i = 0; i < 4; ++i)
+                        if (gg[i] != 0.f) {
+                            ss[i] = fmaf(gg[i], gg[i], ss[i]);
+                            ww[i] -= a.lr * gg[i] / (sqrtf(ss[i]) + a.eps);
+                        }
+                    *reinterpret_cast<float4*>(st + e0) = make_float4(ss[0], ss[1], ss[2], ss[3]);
+                } else {
+#pragma unroll
+                    for (int i = 0; i < 4; ++i)
+                        if (gg[i] != 0.f) ww[i] = fmaf(-a.lr, gg[i], ww[i]);
+                }
+                *reinterpret_cast<float4*>(G + e0) = make_float4(ww[0], ww[1], ww[2], ww[3]);
+            }
+        } else {
+            for (int64_t e = e0; e < n; ++e) {
+                const float gi = g[e];
+                if (gi == 0.f) continue;
+                any = true;
+                if (a.opt == TT_OPT_ADAGRAD) {
+                    const float t = fmaf(gi, gi, st[e]);
+                    st[e] = t;
+                    G[e] -= a.lr * gi / (sqrtf(t) + a.eps);
+                } else {
+                    G[e] = fmaf(-a.lr, gi, G[e]);
+                }
+            }
+        }
+        // exact-copy hot-row cache: the slices changed here are stale from the next pass on
+        if (any && a.stamp[sg]) {
+            const int64_t s_lo = e0 / a.slice_elems[sg];
+            const int64_t s_hi = (e0 + 3 < n ? e0 + 3 : n - 1) / a.slice_elems[sg];
+            for (int64_t sl = s_lo; sl <= s_hi; ++sl) a.stamp[sg][sl] = *a.dstep + 1;
+        }
+    }
+}
+
+cudaError_t launch_apply_grads(const ApplyArgs& a, int sms, cudaStream_t s) {
+    if (a.nseg == 0 || a.start[a.nseg] == 0) return cudaSuccess;
+    const int64_t want = (a.start[a.nseg] + 255) / 256;
+    const int64_t cap = (int64_t)sms * 8;
+    const unsigned blocks = (unsigned)(want < cap ? want : cap);
+    k_apply_grads<<<blocks, 256, 0, s>>>(a);
+    return cudaGetLastError();
+}
+
 // ------------------------------------------------------------------ launchers
 
 size_t tile_bwd_smem(const Params& P) {

@@ -136,7 +136,7 @@ __device__ void fwd_T_group_tc(const Params& P, const TableDev& T, int i2, int h
             for (int i = 0; i < 4; ++i) bx[q][i] = e < kBQ ? __ldg(src + (4 * a4 + i) * NN + jc) : 0.f;
         }
     }
-    bool staged = false;
+    bool staged = false, failed = false;
     int nbatch = 0;
     int* list0 = S.ulist;
     for (int base = 0; base < T.p1; base += kListCap) {
@@ -216,11 +216,15 @@ __device__ void fwd_T_group_tc(const Params& P, const TableDev& T, int i2, int h
                     }
                 }
                 tc_commit(bar);
-                *okflag = mbar_wait(bar, nbatch & 1) ? 1 : 0;
+                *okflag = mbar_wait(bar, nbatch & 1, P.wait_polls) ? 1 : 0;
                 if (!*okflag) atomicOr(P.err, kErrTimeout);
             }
             __syncthreads();
             tc_fence_after();
+            if (!*okflag) {  // gave up: no further MMA, no operand rewrite (uniform: shared flag)
+                failed = true;
+                break;
+            }
             // warp w reads tile w / 4, lanes 32 (w % 4) .. + 31 (its 32 rows), all N columns, 32 at
             // a time; each 32 x 32 block goes through a private shared buffer (the A tiles are free
             // now; float4 chunk q of row r sits at chunk q ^ (r & 7), so neither side has bank
@@ -255,7 +259,11 @@ __device__ void fwd_T_group_tc(const Params& P, const TableDev& T, int i2, int h
             }
             ++nbatch;
         }
+        if (failed) break;
     }
+    // after a give-up the MMAs of that batch may still run: wait for them (full
+    // limit) before the tensor memory is freed
+    if (failed && threadIdx.x == 0) mbar_wait(bar, nbatch & 1, kTcWaitLimit);
     tc_fence_before();
     __syncthreads();
     if (w == 0) tc_dealloc(*tslot, kTcTiles * NN);
@@ -1051,13 +1059,13 @@ static int64_t grid_for(int64_t units, int per_block, int64_t cap) {
 }
 
 cudaError_t launch_cache_gmax(const Params& P, cudaStream_t s) {
-    const int64_t b = grid_for(std::max<int64_t>(P.nnz, (int64_t)P.nbags * P.D), 256 * 4, 152 * 2);
+    const int64_t b = grid_for(std::max<int64_t>(P.nnz, (int64_t)P.nbags * P.D), 256 * 4, (int64_t)P.sms * 2);
     cudaError_t le = launch_pdl(k_cache_gmax, dim3((unsigned)b), dim3(256), 0, s, P);
     return le != cudaSuccess ? le : cudaGetLastError();
 }
 
 cudaError_t launch_cache_acc(const Params& P, cudaStream_t s) {
-    const int64_t b = grid_for(P.nnz, kCacheChunk, 152 * 8);
+    const int64_t b = grid_for(P.nnz, kCacheChunk, (int64_t)P.sms * 8);
     cudaError_t le = P.D <= 64 ? launch_pdl(k_cache_acc<2>, dim3((unsigned)b), dim3(kCacheChunk), 0, s, P)
                    : P.D <= 128 ? launch_pdl(k_cache_acc<4>, dim3((unsigned)b), dim3(kCacheChunk), 0, s, P)
                                 : launch_pdl(k_cache_acc<8>, dim3((unsigned)b), dim3(kCacheChunk), 0, s, P);
@@ -1065,7 +1073,7 @@ cudaError_t launch_cache_acc(const Params& P, cudaStream_t s) {
 }
 
 cudaError_t launch_cache_apply(const Params& P, cudaStream_t s) {
-    const int64_t b = grid_for(P.cache_n, 8, 152 * 8);
+    const int64_t b = grid_for(P.cache_n, 8, (int64_t)P.sms * 8);
     cudaError_t le = P.D <= 64 ? launch_pdl(k_cache_apply<2>, dim3((unsigned)b), dim3(256), 0, s, P)
                    : P.D <= 128 ? launch_pdl(k_cache_apply<4>, dim3((unsigned)b), dim3(256), 0, s, P)
                                 : launch_pdl(k_cache_apply<8>, dim3((unsigned)b), dim3(256), 0, s, P);

@@ -54,6 +54,8 @@ constexpr int kMaxD = 256;              // largest q1 q2 q3
 
 enum ErrBits { kErrIndex = 1, kErrOffsets = 2, kErrTimeout = 4 };
 
+constexpr unsigned kTcWaitPolls = 1u << 24;  // default polls of a bounded mbarrier wait
+
 struct TableDev {
     int64_t E;
     int p1, p2, p3;
@@ -91,6 +93,8 @@ struct Params {
     int small;                      // 1: chunk-rank path (nnz <= kSmallMaxNnz); pi21 is then ordered by (i2, pos)
     int dclass_all;                 // dimension class shared by every table, or -1 (mixed)
     int fwd_split;                  // k_fwd_T blocks per (table, i2) group (1 or 2)
+    int sms;                        // multiprocessors of the handle's device (grid sizes)
+    unsigned wait_polls;            // polls before a bounded mbarrier wait gives up (tt_emb_set_wait_limit)
     int g1s_floats, dts_floats;     // k_tile_bwd batch buffers (max over tables, this call's split)
     int g2s_floats;                 // k_tile_bwd G2 columns of one split, padded rows (max over tables)
     // call arguments
@@ -594,6 +598,25 @@ cudaError_t launch_cache_gmax(const Params& P, cudaStream_t s);
 cudaError_t launch_cache_acc(const Params& P, cudaStream_t s);
 cudaError_t launch_cache_apply(const Params& P, cudaStream_t s);
 cudaError_t launch_full_weight(const TableDev* tables, int t, int64_t row0, int64_t nrows, float* out, cudaStream_t s);
+
+// Update of the cores from summed gradients (tt_emb_apply_gradients): up to
+// kApplySegs cores per launch; segment sg has n[sg] elements, float4 groups
+// start[sg] .. start[sg + 1].
+constexpr int kApplySegs = 48;
+struct ApplyArgs {
+    int nseg;
+    int opt;
+    float lr, eps;
+    float* G[kApplySegs];
+    const float* g[kApplySegs];
+    float* s[kApplySegs];
+    int* stamp[kApplySegs];        // slice stamps of an exact-copy cache (table 0), else null
+    int64_t slice_elems[kApplySegs];
+    int64_t n[kApplySegs];
+    int64_t start[kApplySegs + 1];
+    const int* dstep;
+};
+cudaError_t launch_apply_grads(const ApplyArgs& a, int sms, cudaStream_t s);
 
 size_t tile_bwd_smem(const Params& P);
 cudaError_t set_sort_attributes(int max_smem);

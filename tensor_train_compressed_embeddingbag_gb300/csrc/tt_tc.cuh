@@ -15,15 +15,19 @@
 // 0..127, one row per lane, columns [base, base + N).
 //
 // Every wait on an mbarrier is bounded; a wait that gives up reports failure to
-// the caller, which records kErrTimeout and skips the tensor-memory reads.
+// the caller, which records kErrTimeout, issues no further MMA and rewrites no
+// operand tile, and before freeing its tensor memory waits once more (with the
+// full limit) for the MMAs already in flight.
 #pragma once
 
 #include <cstdint>
 
+#include "tt_internal.cuh"
+
 namespace ttemb {
 
 constexpr int kTcM = 128;                 // rows per MMA (one per tensor-memory lane)
-constexpr uint32_t kTcWaitLimit = 1u << 24;  // polls of an mbarrier before giving up
+constexpr uint32_t kTcWaitLimit = kTcWaitPolls;  // polls of an mbarrier before giving up (default)
 
 // Float offset of element (r, k) of an [rows][K] fp32 tile in the canonical layout.
 __host__ __device__ __forceinline__ int tc_off(int r, int k, int K) {
@@ -90,9 +94,10 @@ __device__ __forceinline__ void tc_commit(uint64_t* bar) {
                  : "memory");
 }
 
-// Bounded wait for the phase with the given parity; false if it did not complete.
-__device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity) {
-    for (uint32_t it = 0; it < kTcWaitLimit; ++it) {
+// Bounded wait (at most `limit` polls) for the phase with the given parity; false
+// if it did not complete.
+__device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, uint32_t limit = kTcWaitLimit) {
+    for (uint32_t it = 0; it < limit; ++it) {
         uint32_t ok;
         asm volatile(
             "{\n\t.reg .pred p;\n\tmbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\tselp.u32 %0, 1, 0, p;\n\t}"

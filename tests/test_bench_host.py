@@ -123,3 +123,36 @@ def test_dedup_flops_brute_force():
         A, Bc = bench.flops_per_lookup(spec)
         want += 6 * A * pairs + 6 * Bc * int(m.sum())
     assert bench.dedup_step_flops(wl) == want
+
+
+def test_kernel_parts_cover_the_step_flops():
+    """The per-kernel split of the algorithmic FLOPs adds up to 6 (A + Bc) per lookup, and
+    only the rank-16 / rank-32 q = [4, 4, 4] tables put T = G1 G2 on the tensor pipe."""
+    sys.path.insert(0, ROOT)
+    import bench
+    from tt_inputs import config
+
+    for cid, batch in ((2, None), (5, 64), (4, 64)):
+        wl = config(cid, batch=batch)
+        parts = bench.kernel_parts(wl)
+        sa, sb = bench.lookup_flops(wl)
+        assert sum(f for v in parts.values() for f, _ in v) == 6 * (sa + sb)
+        tensor = sum(f for f, pp in parts["fwd_T"] if pp == "tensor")
+        want = sum(2 * bench.flops_per_lookup(s)[0] * int(wl.offsets[(t + 1) * wl.batch] - wl.offsets[t * wl.batch])
+                   for t, s in enumerate(wl.tables) if bench.tc_class(s))
+        assert tensor == want
+
+
+def test_traffic_record_voided_when_sources_change(tmp_path, monkeypatch):
+    sys.path.insert(0, ROOT)
+    import bench
+
+    rec = {"k_x": {"sources": ["tt_bwd.cu"], "source_sha": bench.source_sha(["tt_bwd.cu"]), "bytes_per_launch": 123.0}}
+    f = tmp_path / "t.json"
+    f.write_text(json.dumps(rec))
+    monkeypatch.setattr(bench, "TRAFFIC_FILE", str(f))
+    assert bench.measured_traffic("k_x")[0] == 123.0
+    rec["k_x"]["source_sha"] = "0" * 16
+    f.write_text(json.dumps(rec))
+    assert bench.measured_traffic("k_x")[0] is None
+    assert bench.measured_traffic("k_missing")[0] is None

@@ -229,6 +229,36 @@ def test_malformed_offsets_reported():
     run.close()
 
 
+@pytest.mark.parametrize("cid,batch", [(2, None), (1, None)])
+def test_tensor_core_wait_give_up(workloads, cid, batch):
+    """With a wait bound of 0 polls every tensor-core wait for its own MMAs gives up at
+    once: the call reports TT_ERR_TIMEOUT, the backward that follows changes no core,
+    and (bound restored) the next step on the same handle matches the oracle.  The
+    MMAs in flight are waited for with the full bound before tensor memory is freed,
+    so the give-up itself leaves nothing running.  (The tiny workload's shape has no
+    tensor-core path: its step must come out clean under the 0 bound.)"""
+    wl = workloads(cid, batch)
+    run = GpuRun(wl)
+    tt.tt_emb_set_wait_limit(run.h, 0)
+    run.forward()
+    run.backward()
+    st = run.error()
+    assert st == (tt.TT_ERR_TIMEOUT if cid == 2 else tt.TT_OK)
+    if st != tt.TT_OK:
+        after = run.cores_host()
+        for k in range(3):
+            np.testing.assert_array_equal(after[0][k], wl.cores[0][k])
+        tt.tt_emb_set_wait_limit(run.h, 1 << 24)
+    out = run.forward().cpu().numpy()
+    dec = check_decode(run, wl)
+    run.backward()
+    assert run.error() == tt.TT_OK
+    if st != tt.TT_OK:
+        check_forward(out, wl)
+        check_cores(run, wl, dec)
+    run.close()
+
+
 def test_call_order_errors():
     wl = synthetic([4, 5, 6], [2, 2, 2], [4, 4], [2, 2])
     run = GpuRun(wl)
