@@ -132,7 +132,9 @@ def lookup_flops(wl):
 
 
 # Which pipe runs each kernel's contractions (the rank-16 / rank-32 classes with
-# q = [4, 4, 4] take the tensor-core paths).
+# q = [4, 4, 4] take the tensor-core paths: T = G1 G2 in the forward; in the backward
+# the pair contractions dG1 = dT G2^T and dG2 = G1^T dT when every table of the
+# handle is of one such class).
 def tc_class(spec):
     return list(spec.q) == [4, 4, 4] and spec.ranks[0] == spec.ranks[1] and spec.ranks[0] in (16, 32)
 
@@ -143,12 +145,14 @@ def kernel_parts(wl):
     2Bc; backward dT and the dG3 partial 4Bc, the dG1 partial and dG2 4A."""
     out = {"fwd_T": [], "pool": [], "tile_bwd": []}
     acc = {}
+    classes = {(tuple(s.q), tuple(s.ranks)) for s in wl.tables}
+    bwd_tc = len(classes) == 1 and tc_class(wl.tables[0]) and os.environ.get("TTEMB_BWD_FFMA") != "1"
     for t, spec in enumerate(wl.tables):
         n = int(wl.offsets[(t + 1) * wl.batch] - wl.offsets[t * wl.batch])
         A, Bc = flops_per_lookup(spec)
         tc = tc_class(spec)
         for k, f, pp in (("fwd_T", 2 * A * n, "tensor" if tc else "fp32"), ("pool", 2 * Bc * n, "fp32"),
-                         ("tile_bwd", 4 * A * n, "fp32"), ("tile_bwd", 4 * Bc * n, "fp32")):
+                         ("tile_bwd", 4 * A * n, "tensor" if bwd_tc else "fp32"), ("tile_bwd", 4 * Bc * n, "fp32")):
             acc[(k, pp)] = acc.get((k, pp), 0) + f
     for (k, pp), f in acc.items():
         out[k].append((f, pp))
@@ -161,8 +165,9 @@ def peak_source(parts, pipe_peak, sms, sm_mhz, kind):
         if pp == "fp32":
             txt.append(f"{f:.3g} FLOP on FP32 FFMA at {pipe_peak['fp32']:.1f} TFLOP/s ({sms} SMs x 128 x 2 x {sm_mhz:.0f} MHz)")
         else:
-            txt.append(f"{f:.3g} FLOP on tensor cores (3xTF32) at {pipe_peak['tensor']:.1f} TFLOP/s (bf16 burst of "
-                       f"{kind} peaks x 1.1/2.25 / 3)")
+            txt.append(f"{f:.3g} FLOP on tensor cores (three products per useful product: 3xTF32, or bf16 pieces "
+                       f"at twice the TF32 rate) at {pipe_peak['tensor']:.1f} TFLOP/s (bf16 burst of {kind} peaks "
+                       f"x 1.1/2.25 / 3)")
     return "; ".join(txt) + "; peak = FLOPs / sum(FLOPs_pipe / peak_pipe)"
 
 

@@ -312,6 +312,17 @@ tt_status build_handle(tt_emb* h, int ntab, const tt_table_desc* d) {
     }
     P.p1_max = p1m;
     h->split_small = can_split ? 2 : 1;
+    {
+        // the backward pair contractions on the tensor cores: one block per tile of at most
+        // bwd_tc_cap() lookups, no column split (TTEMB_BWD_FFMA=1 keeps the FFMA kernel)
+        const char* e = getenv("TTEMB_BWD_FFMA");
+        P.bwd_tc = (bwd_tc_eligible(P.dclass_all) && !(e && e[0] == '1')) ? 1 : 0;
+        if (P.bwd_tc) {
+            h->split_small = 1;
+            h->cap_small = h->cap_large = bwd_tc_cap();
+            P.tile_cap = h->cap_large;
+        }
+    }
     // device tables
     std::vector<int> bins(n1 + n2 + n3);
     for (int t = 0; t < ntab; ++t) {

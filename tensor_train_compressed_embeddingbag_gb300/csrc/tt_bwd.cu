@@ -19,6 +19,7 @@
 #include <algorithm>
 
 #include "tt_dims.cuh"
+#include "tt_tile.cuh"
 
 namespace ttemb {
 
@@ -64,43 +65,6 @@ __host__ __device__ inline BwdLayout bwd_layout(int cap, int D, int g2f, int g1f
     L.dts = o;     o = al16(o + sizeof(float) * (size_t)dtf);
     L.total = o;
     return L;
-}
-
-// The tile's lookups come grouped by (table, i2) (ordered by (i1, pos) on the
-// multi-CTA path, by pos on the small path); sort them by (i1, i3, position) in
-// shared memory.  Bag and scale of each lookup are read in the same pass (from
-// the grouped-order copies the scatter wrote) and follow the sort.
-__device__ void load_and_sort_tile(const Params& P, int start, int len, unsigned long long* keys, int* sp1,
-                                   int* sp3, int* si1, int* si3, int* sbag, float* ss) {
-    // len <= blockDim: thread k holds lookup k of the tile.  The keys (i1, i3, k) are
-    // distinct, so a key's rank is the number of smaller keys: every thread counts its
-    // own with broadcast shared-memory reads and writes its lookup at that rank.
-    const int k = threadIdx.x;
-    unsigned long long key = ~0ull;
-    int p1 = 0, p3 = 0, i1 = 0, i3 = 0, bag = 0;
-    float sc = 0.f;
-    if (k < len) {  // grouped-order copies: one coalesced pass, no dependent loads
-        p1 = P.g_p1[start + k];
-        p3 = P.g_p3[start + k];
-        i1 = P.g_i1[start + k];
-        i3 = P.g_i3[start + k];
-        bag = P.g_bag[start + k];
-        sc = P.g_s[start + k];
-        key = ((unsigned long long)i1 << (2 * kFieldBits)) | ((unsigned long long)i3 << kFieldBits) | (unsigned long long)k;
-        keys[k] = key;
-    }
-    __syncthreads();
-    if (k < len) {
-        int r = 0;
-        for (int j = 0; j < len; ++j) r += keys[j] < key ? 1 : 0;
-        sp1[r] = p1;
-        sp3[r] = p3;
-        si1[r] = i1;
-        si3[r] = i3;
-        sbag[r] = bag;
-        ss[r] = sc;
-    }
-    __syncthreads();
 }
 
 // Sum the dG1 (per tile-pair, over the column splits) or dG3 (per tile-row)
@@ -905,6 +869,7 @@ static cudaError_t launch_tile_bwd_split(const Params& P, cudaStream_t s) {
 }
 
 cudaError_t launch_tile_bwd(const Params& P, cudaStream_t s) {
+    if (P.bwd_tc) return launch_tile_bwd_tc(P, s);
     return P.split == 2 ? launch_tile_bwd_split<2>(P, s) : launch_tile_bwd_split<1>(P, s);
 }
 
@@ -933,6 +898,7 @@ cudaError_t set_bwd_attributes(int max_smem) {
     cudaError_t e = set_tile_attrs<1>(max_smem);
     if (e == cudaSuccess) e = set_tile_attrs<2>(max_smem);
     if (e == cudaSuccess) e = allow_max_dynamic_smem((const void*)k_reduce13, max_smem);
+    if (e == cudaSuccess) e = set_bwd_tc_attributes(max_smem);
     return e;
 }
 

@@ -95,6 +95,7 @@ struct Params {
     int fwd_split;                  // k_fwd_T blocks per (table, i2) group (1 or 2)
     int sms;                        // multiprocessors of the handle's device (grid sizes)
     unsigned wait_polls;            // polls before a bounded mbarrier wait gives up (tt_emb_set_wait_limit)
+    int bwd_tc;                     // 1: k_tile_bwd_tc (tensor cores) takes the backward tiles
     int g1s_floats, dts_floats;     // k_tile_bwd batch buffers (max over tables, this call's split)
     int g2s_floats;                 // k_tile_bwd G2 columns of one split, padded rows (max over tables)
     // call arguments
@@ -592,6 +593,10 @@ cudaError_t launch_fwd_T(const Params& P, cudaStream_t s);
 int fwd_tc_floats_of(int dclass, int r1, int N);
 cudaError_t launch_pool(const Params& P, cudaStream_t s);
 cudaError_t launch_tile_bwd(const Params& P, cudaStream_t s);
+cudaError_t launch_tile_bwd_tc(const Params& P, cudaStream_t s);
+bool bwd_tc_eligible(int dclass_all);  // the backward pair contractions run on the tensor cores
+int bwd_tc_cap();                      // lookups per tile of the tensor-core backward
+cudaError_t set_bwd_tc_attributes(int max_smem);
 cudaError_t launch_reduce13(const Params& P, cudaStream_t s);
 cudaError_t launch_cache_fill(const Params& P, cudaStream_t s);
 cudaError_t launch_cache_gmax(const Params& P, cudaStream_t s);
