@@ -309,53 +309,20 @@ __device__ void tile_bwd_body(const Params& P, const TableDev& T, const Dm dm, u
             }
         }
     }
-    // ---- gs: summed upstream gradient of every tile-row.  Each thread takes
-    // kGsUnroll (row, float4 column) items and loads the first lookup of all of
-    // them before summing; further lookups of a row (repeated rows) follow.
-    {
-        const int D4 = D >> 2;  // every compiled class and every D % 4 == 0 table; else scalar below
-        if ((D & 3) == 0) {
-            const int items = nrows * D4;
-            for (int e0 = threadIdx.x; e0 < items; e0 += kGsUnroll * kBwdThreads) {
-                float4 x[kGsUnroll];
-                int row[kGsUnroll], q4[kGsUnroll];
-#pragma unroll
-                for (int u = 0; u < kGsUnroll; ++u) {
-                    const int e = e0 + u * kBwdThreads;
-                    row[u] = e < items ? e / D4 : -1;
-                    q4[u] = e < items ? e - row[u] * D4 : 0;
-                    x[u] = make_float4(0.f, 0.f, 0.f, 0.f);
-                    if (row[u] >= 0) {
-                        const int kk = rowbeg[row[u]];
-                        x[u] = __ldg(reinterpret_cast<const float4*>(P.grad_out + (int64_t)sbag[kk] * D) + q4[u]);
-                    }
-                }
-#pragma unroll
-                for (int u = 0; u < kGsUnroll; ++u) {
-                    if (row[u] < 0) continue;
-                    const int kb = rowbeg[row[u]];
-                    const float s0 = ss[kb];
-                    float4 a = make_float4(s0 * x[u].x, s0 * x[u].y, s0 * x[u].z, s0 * x[u].w);
-                    for (int kk = kb + 1; kk < rowbeg[row[u] + 1]; ++kk) {
-                        const float4 y = __ldg(reinterpret_cast<const float4*>(P.grad_out + (int64_t)sbag[kk] * D) + q4[u]);
-                        const float sk = ss[kk];
-                        a.x = fmaf(sk, y.x, a.x); a.y = fmaf(sk, y.y, a.y);
-                        a.z = fmaf(sk, y.z, a.z); a.w = fmaf(sk, y.w, a.w);
-                    }
-                    *reinterpret_cast<float4*>(gs + row[u] * D + q4[u] * 4) = a;
-                }
-            }
-        } else {
-            for (int e = threadIdx.x; e < nrows * D; e += blockDim.x) {
-                const int row = e / D, j = e - row * D;
-                float acc = 0.f;
-                for (int kk = rowbeg[row]; kk < rowbeg[row + 1]; ++kk)
-                    acc = fmaf(ss[kk], __ldg(P.grad_out + (int64_t)sbag[kk] * D + j), acc);
-                gs[row * D + j] = acc;
-            }
+    // ---- gs: summed upstream gradient of every tile-row
+    if ((D & 3) == 0) {  // every compiled class and every D % 4 == 0 table
+        tile_gs(P, len, nrows, sbag, ss, rowbeg, gs, D);
+    } else {
+        __syncthreads();
+        for (int e = threadIdx.x; e < nrows * D; e += blockDim.x) {
+            const int row = e / D, j = e - row * D;
+            float acc = 0.f;
+            for (int kk = rowbeg[row]; kk < rowbeg[row + 1]; ++kk)
+                acc = fmaf(ss[kk], __ldg(P.grad_out + (int64_t)sbag[kk] * D + j), acc);
+            gs[row * D + j] = acc;
         }
+        __syncthreads();
     }
-    __syncthreads();
 
     // ---- dG3 partial per tile-row, columns c of this split: P3[c][j3] = sum_j12 T[j12][c] gs[j12 q3 + j3]
     if constexpr (Dm::kStatic) {

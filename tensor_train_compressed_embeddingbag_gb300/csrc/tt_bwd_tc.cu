@@ -335,39 +335,8 @@ __device__ void tile_bwd_tc_body(const Params& P, const TableDev& T, unsigned ch
     if (threadIdx.x == 32) mbar_init(bar, kTcBwdThreads / 32);  // one commit per issuing warp
     __syncthreads();  // rowid / pairid / rowbeg / pairbeg complete
 
-    // ---- gs: summed upstream gradient of every tile-row (float4 items, four in flight)
-    {
-        constexpr int D4 = D / 4;
-        const int items = nrows * D4;
-        for (int e0 = threadIdx.x; e0 < items; e0 += 4 * kTcBwdThreads) {
-            float4 x[4];
-            int row[4], q4[4];
-#pragma unroll
-            for (int u = 0; u < 4; ++u) {
-                const int e = e0 + u * kTcBwdThreads;
-                row[u] = e < items ? e / D4 : -1;
-                q4[u] = e < items ? e - row[u] * D4 : 0;
-                x[u] = make_float4(0.f, 0.f, 0.f, 0.f);
-                if (row[u] >= 0)
-                    x[u] = __ldg(reinterpret_cast<const float4*>(P.grad_out + (int64_t)sbag[rowbeg[row[u]]] * D) + q4[u]);
-            }
-#pragma unroll
-            for (int u = 0; u < 4; ++u) {
-                if (row[u] < 0) continue;
-                const int kb = rowbeg[row[u]];
-                const float s0 = ss[kb];
-                float4 a = make_float4(s0 * x[u].x, s0 * x[u].y, s0 * x[u].z, s0 * x[u].w);
-                for (int kk = kb + 1; kk < rowbeg[row[u] + 1]; ++kk) {
-                    const float4 y = __ldg(reinterpret_cast<const float4*>(P.grad_out + (int64_t)sbag[kk] * D) + q4[u]);
-                    const float sk = ss[kk];
-                    a.x = fmaf(sk, y.x, a.x); a.y = fmaf(sk, y.y, a.y);
-                    a.z = fmaf(sk, y.z, a.z); a.w = fmaf(sk, y.w, a.w);
-                }
-                *reinterpret_cast<float4*>(gs + row[u] * D + q4[u] * 4) = a;
-            }
-        }
-    }
-    __syncthreads();
+    // ---- gs: summed upstream gradient of every tile-row
+    tile_gs(P, len, nrows, sbag, ss, rowbeg, gs, D);
 
     // ---- batches of kTcBwdPairs pairs: dT and the G1 rows as pieces, then the MMAs
     constexpr uint32_t kIdescQ = tc_idesc_bf16(64, R, 0);

@@ -49,4 +49,57 @@ __device__ __forceinline__ void load_and_sort_tile(const Params& P, int start, i
     __syncthreads();
 }
 
+// Summed upstream gradient of every tile-row: gs[row] = sum over the row's lookups k
+// (a run of the sorted tile) of s_k grad_out[bag_k], D floats (D % 4 == 0).  First
+// every lookup's scaled gradient row goes to gs at the lookup's position (all loads in
+// flight at once: a hot row of many lookups is not a chain of dependent loads), then
+// each row's run is summed from shared memory, blockDim items (row, 4 columns) a
+// round, and written at the row's position.  A row's position is at most that of its
+// first lookup, so a round overwrites only positions that no later round reads.
+// Ends with the block synchronised; gs holds nrows rows.
+__device__ __forceinline__ void tile_gs(const Params& P, int len, int nrows, const int* sbag, const float* ss,
+                                        const int* rowbeg, float* gs, int D) {
+    const int D4 = D >> 2;
+    float4* g4 = reinterpret_cast<float4*>(gs);
+    const int n1 = len * D4;
+    for (int e0 = threadIdx.x; e0 < n1; e0 += 4 * blockDim.x) {
+        float4 x[4];
+        float sc[4];
+#pragma unroll
+        for (int u = 0; u < 4; ++u) {
+            const int e = e0 + u * blockDim.x;
+            x[u] = make_float4(0.f, 0.f, 0.f, 0.f);
+            sc[u] = 0.f;
+            if (e < n1) {
+                const int k = e / D4, q = e - k * D4;
+                sc[u] = ss[k];
+                x[u] = __ldg(reinterpret_cast<const float4*>(P.grad_out + (int64_t)sbag[k] * D) + q);
+            }
+        }
+#pragma unroll
+        for (int u = 0; u < 4; ++u) {
+            const int e = e0 + u * blockDim.x;
+            if (e < n1) g4[e] = make_float4(sc[u] * x[u].x, sc[u] * x[u].y, sc[u] * x[u].z, sc[u] * x[u].w);
+        }
+    }
+    __syncthreads();
+    const int n2 = nrows * D4;
+    for (int base = 0; base < n2; base += blockDim.x) {  // uniform trip count
+        const int e = base + threadIdx.x;
+        float4 a = make_float4(0.f, 0.f, 0.f, 0.f);
+        if (e < n2) {
+            const int row = e / D4, q = e - row * D4;
+            const int kb = rowbeg[row], ke = rowbeg[row + 1];
+            a = g4[kb * D4 + q];
+            for (int k = kb + 1; k < ke; ++k) {
+                const float4 y = g4[k * D4 + q];
+                a.x += y.x; a.y += y.y; a.z += y.z; a.w += y.w;
+            }
+        }
+        __syncthreads();
+        if (e < n2) g4[e] = a;
+    }
+    __syncthreads();
+}
+
 }  // namespace ttemb
