@@ -51,7 +51,8 @@ typedef enum {
     TT_ERR_CUDA = 4,    /* a CUDA runtime call failed */
     TT_ERR_STATE = 5,   /* call out of order, e.g. backward without a forward */
     TT_ERR_TIMEOUT = 6, /* a bounded device wait gave up */
-    TT_ERR_NOMEM = 7    /* device workspace allocation failed */
+    TT_ERR_NOMEM = 7,   /* device workspace allocation failed */
+    TT_ERR_BOUNDS = 8   /* debug build only (libttemb_debug.so): an internal index left its bound */
 } tt_status;
 
 typedef enum { TT_POOL_SUM = 0, TT_POOL_MEAN = 1 } tt_pool;

@@ -24,12 +24,17 @@ from typing import List, Optional, Sequence
 
 import torch
 
-from ._nvcc_build import LIB as _LIB_PATH
-from ._nvcc_build import build
+from ._nvcc_build import LIB as _LIB_RELEASE
+from ._nvcc_build import LIB_DEBUG as _LIB_DEBUG
+from ._nvcc_build import build, build_all
+
+# TTEMB_DEBUG=1 loads the debug library (index checks in the kernels, TT_ERR_BOUNDS)
+_LIB_PATH = _LIB_DEBUG if os.environ.get("TTEMB_DEBUG") == "1" else _LIB_RELEASE
 
 __all__ = [
     "TTError",
     "build",
+    "build_all",
     "suggested_tt_shapes",
     "tt_init_cores",
     "load_library",
@@ -68,7 +73,7 @@ __all__ = [
     "TableBatchedTTEmbeddingBag",
 ]
 
-TT_OK, TT_ERR_ARG, TT_ERR_SHAPE, TT_ERR_INDEX, TT_ERR_CUDA, TT_ERR_STATE, TT_ERR_TIMEOUT, TT_ERR_NOMEM = range(8)
+TT_OK, TT_ERR_ARG, TT_ERR_SHAPE, TT_ERR_INDEX, TT_ERR_CUDA, TT_ERR_STATE, TT_ERR_TIMEOUT, TT_ERR_NOMEM, TT_ERR_BOUNDS = range(9)
 TT_POOL_SUM, TT_POOL_MEAN = 0, 1
 TT_OPT_SGD, TT_OPT_ADAGRAD, TT_OPT_GRAD = 0, 1, 2
 

@@ -17,6 +17,8 @@ CSRC = os.path.join(HERE, "csrc")
 INCLUDE = os.path.join(os.path.dirname(HERE), "include")
 BUILD = os.path.join(HERE, "_build")
 LIB = os.path.join(HERE, "libttemb.so")
+# debug build: the kernels check their data-derived indices (-DTTEMB_DEBUG, see tt_internal.cuh)
+LIB_DEBUG = os.path.join(HERE, "libttemb_debug.so")
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 FLAGS = ["-O3", "-lineinfo", "-std=c++17", "-Xcompiler", "-fPIC", "-Xcompiler", "-O2",
          "-I" + INCLUDE, "-I" + CSRC]
@@ -37,25 +39,28 @@ def _deps():
     return _sources() + glob.glob(os.path.join(CSRC, "*.cuh")) + glob.glob(os.path.join(INCLUDE, "*.h")) + [__file__]
 
 
-def up_to_date() -> bool:
-    if not os.path.exists(LIB):
+def up_to_date(lib: str = LIB) -> bool:
+    if not os.path.exists(lib):
         return False
-    t = os.path.getmtime(LIB)
+    t = os.path.getmtime(lib)
     return all(os.path.getmtime(p) <= t for p in _deps())
 
 
-def build(force: bool = False, verbose: bool = False, extra_flags=()) -> str:
-    """Compile and link; returns the library path."""
-    if not force and up_to_date():
-        return LIB
-    os.makedirs(BUILD, exist_ok=True)
+def build(force: bool = False, verbose: bool = False, extra_flags=(), debug: bool = False) -> str:
+    """Compile and link; returns the library path (debug: libttemb_debug.so with -DTTEMB_DEBUG)."""
+    lib = LIB_DEBUG if debug else LIB
+    if not force and up_to_date(lib):
+        return lib
+    out = os.path.join(BUILD, "debug") if debug else BUILD
+    os.makedirs(out, exist_ok=True)
     cc = nvcc()
     srcs = _sources()
-    objs = [os.path.join(BUILD, os.path.basename(s)[:-3] + ".o") for s in srcs]
+    objs = [os.path.join(out, os.path.basename(s)[:-3] + ".o") for s in srcs]
+    flags = [*FLAGS, *extra_flags] + (["-DTTEMB_DEBUG"] if debug else [])
 
     def compile_one(src_obj):
         src, obj = src_obj
-        cmd = [cc, *ARCH, *FLAGS, *extra_flags, "-c", src, "-o", obj]
+        cmd = [cc, *ARCH, *flags, "-c", src, "-o", obj]
         r = subprocess.run(cmd, capture_output=True, text=True)
         if r.returncode != 0:
             raise RuntimeError(f"nvcc failed on {os.path.basename(src)}:\n{r.stderr}")
@@ -67,12 +72,19 @@ def build(force: bool = False, verbose: bool = False, extra_flags=()) -> str:
         for lg in logs:
             if lg.strip():
                 print(lg)
-    tmp = LIB + f".tmp{os.getpid()}"
+    tmp = lib + f".tmp{os.getpid()}"
     r = subprocess.run([cc, *ARCH, "-shared", "-o", tmp, *objs], capture_output=True, text=True)
     if r.returncode != 0:
         raise RuntimeError(f"link failed:\n{r.stderr}")
-    os.replace(tmp, LIB)
-    return LIB
+    os.replace(tmp, lib)
+    return lib
+
+
+def build_all() -> None:
+    """The release and the debug library, compiled concurrently."""
+    with cf.ThreadPoolExecutor(max_workers=2) as ex:
+        for f in [ex.submit(build), ex.submit(build, debug=True)]:
+            f.result()
 
 
 if __name__ == "__main__":

@@ -448,6 +448,7 @@ const char* tt_emb_status_string(tt_status s) {
         case TT_ERR_STATE: return "call out of order";
         case TT_ERR_TIMEOUT: return "bounded device wait gave up";
         case TT_ERR_NOMEM: return "device memory allocation failed";
+        case TT_ERR_BOUNDS: return "internal index out of bounds (debug build check)";
     }
     return "unknown status";
 }
@@ -989,6 +990,7 @@ tt_status tt_emb_get_last_error(tt_emb* h) {
     if (err & kErrIndex) return TT_ERR_INDEX;
     if (err & kErrOffsets) return TT_ERR_ARG;
     if (err & kErrTimeout) return TT_ERR_TIMEOUT;
+    if (err & kErrBounds) return TT_ERR_BOUNDS;
     return TT_OK;
 }
 

@@ -111,6 +111,9 @@ __device__ void reduce_slice(const Params& P, int bglob, int* slots, int* sh, fl
         while (base < end && nslot + (int)blockDim.x * nsub <= kReduceSlots) {
             const int kk = base + threadIdx.x;
             const int rv = kk < end ? rep[kk] : -1;
+#ifdef TTEMB_DEBUG
+            if (rv >= 0) TT_DCHECK(P, rv, P.nnz);
+#endif
             int tot;
             const int ex = block_scan_excl(rv >= 0 ? 1 : 0, sh, &tot);
             if (rv >= 0)
@@ -251,6 +254,14 @@ __device__ void tile_bwd_body(const Params& P, const TableDev& T, const Dm dm, u
 
     // ---- lookups of the tile, sorted by (i1, i3, position)
     load_and_sort_tile(P, start, len, keys, sp1, sp3, si1, si3, sbag, ss);
+#ifdef TTEMB_DEBUG
+    if ((int)threadIdx.x < len) {  // the tile's slices within the table, its group within the bins
+        si1[threadIdx.x] = TT_DCHECK(P, si1[threadIdx.x], T.p1);
+        si3[threadIdx.x] = TT_DCHECK(P, si3[threadIdx.x], T.p3);
+    }
+    if (threadIdx.x == 0) TT_DCHECK(P, i2, T.p2);
+    __syncthreads();
+#endif
     const int k = threadIdx.x;  // tile_cap <= blockDim
     int fr = 0, fp = 0;
     if (k < len) {

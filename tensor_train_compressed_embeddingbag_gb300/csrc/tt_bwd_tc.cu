@@ -294,6 +294,14 @@ __device__ void tile_bwd_tc_body(const Params& P, const TableDev& T, unsigned ch
 
     // ---- lookups of the tile, sorted by (i1, i3, position); rows and pairs
     load_and_sort_tile(P, start, len, keys, sp1, sp3, si1, si3, sbag, ss);
+#ifdef TTEMB_DEBUG
+    if ((int)threadIdx.x < len) {  // the tile's slices within the table, its group within the bins
+        si1[threadIdx.x] = TT_DCHECK(P, si1[threadIdx.x], T.p1);
+        si3[threadIdx.x] = TT_DCHECK(P, si3[threadIdx.x], T.p3);
+    }
+    if (threadIdx.x == 0) TT_DCHECK(P, i2, T.p2);
+    __syncthreads();
+#endif
     const int k = threadIdx.x;
     int fr = 0, fp = 0;
     if (k < len) {

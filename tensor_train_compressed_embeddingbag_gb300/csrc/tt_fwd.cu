@@ -424,6 +424,8 @@ __global__ void __launch_bounds__(kFwdThreads, 2) k_fwd_T(const __grid_constant_
 // ------------------------------------------------------------------ pooling
 
 __device__ __forceinline__ const float* t_of_pair(const Params& P, const TableDev& T, int i2, int i1) {
+    i2 = TT_DCHECK(P, i2, T.p2);
+    i1 = TT_DCHECK(P, i1, T.p1);
     return P.Tbuf + T.tbase + ((int64_t)i2 * T.p1 + i1) * (int64_t)(T.q1 * T.q2 * T.r2);
 }
 

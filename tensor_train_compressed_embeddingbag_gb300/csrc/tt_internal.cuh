@@ -52,7 +52,26 @@ constexpr int kSmallChunk = 256;        // small path: lookups per decode block 
 constexpr int kDecodeOffs = 1024;       // bag offsets staged per decode block
 constexpr int kMaxD = 256;              // largest q1 q2 q3
 
-enum ErrBits { kErrIndex = 1, kErrOffsets = 2, kErrTimeout = 4 };
+enum ErrBits { kErrIndex = 1, kErrOffsets = 2, kErrTimeout = 4, kErrBounds = 8 };
+
+// Debug build (compiled with -DTTEMB_DEBUG): every index below that is derived from
+// data (decoded slices, bag ids, positions in the sorted orders, tile ranges, partial
+// slots) is checked against its bound where it is used; an index outside [0, bound)
+// records kErrBounds (tt_emb_get_last_error: TT_ERR_BOUNDS) and is clamped into range,
+// so the access stays inside its buffer.  The release build compiles the checks away.
+#ifdef TTEMB_DEBUG
+template <class I>
+__device__ __forceinline__ I dcheck(int* err, I v, int64_t bound) {
+    if (v < 0 || (int64_t)v >= bound) {
+        atomicOr(err, kErrBounds);
+        return (I)(v < 0 ? 0 : (bound > 0 ? bound - 1 : 0));
+    }
+    return v;
+}
+#define TT_DCHECK(P, v, bound) ::ttemb::dcheck((P).err, (v), (int64_t)(bound))
+#else
+#define TT_DCHECK(P, v, bound) (v)
+#endif
 
 constexpr unsigned kTcWaitPolls = 1u << 24;  // default polls of a bounded mbarrier wait
 
@@ -429,10 +448,13 @@ __device__ __forceinline__ bool decode_lookup(const Params& P, int64_t n, int ba
         }
         P.lk_hit[n] = slot;
     }
+    i1 = TT_DCHECK(P, i1, T.p1);
+    i2 = TT_DCHECK(P, i2, T.p2);
+    i3 = TT_DCHECK(P, i3, T.p3);
     P.lk_i1[n] = i1;
     P.lk_i2[n] = i2;
     P.lk_i3[n] = i3;
-    P.lk_bag[n] = bag;
+    P.lk_bag[n] = TT_DCHECK(P, bag, P.nbags);
     P.lk_s[n] = s;
     if (CACHE && P.cache_train && P.lk_hit[n] >= 0) return false;
     P.tflag[T.fbase + (int64_t)i2 * T.p1 + i1] = epoch;
@@ -454,9 +476,9 @@ __device__ __forceinline__ void scatter_chunk(const Params& P, int c, int part) 
         if (excluded(P, n)) continue;
         const TableDev& T = P.tables[table_of_bag(P, P.lk_bag[n])];
         const int d1 = T.base1 + P.lk_i1[n], d2 = T.base2 + P.lk_i2[n], d3 = T.base3 + P.lk_i3[n];
-        const int p1 = P.H1[(int64_t)d1 * P.nch + c] + P.lr1[n];
-        const int p3 = P.H3[(int64_t)d3 * P.nch + c] + P.lr3[n];
-        const int pos = P.H2[(int64_t)d2 * P.nch + c] + P.lr2[n];
+        const int p1 = TT_DCHECK(P, P.H1[(int64_t)d1 * P.nch + c] + P.lr1[n], P.nnz);
+        const int p3 = TT_DCHECK(P, P.H3[(int64_t)d3 * P.nch + c] + P.lr3[n], P.nnz);
+        const int pos = TT_DCHECK(P, P.H2[(int64_t)d2 * P.nch + c] + P.lr2[n], P.nnz);
         P.pi1[p1] = (int)n;
         P.pi3[p3] = (int)n;
         P.pi21[pos] = (int)n;

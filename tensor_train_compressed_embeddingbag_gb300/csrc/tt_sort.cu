@@ -339,7 +339,7 @@ __global__ void __launch_bounds__(kSortThreads, 1) k_scatter13(const __grid_cons
         c, P.nnz, P.n1, cnt,
         [&](int64_t n) { return excluded(P, n) ? -1 : P.tables[table_of_bag(P, P.lk_bag[n])].base1 + P.lk_i1[n]; },
         [&](int64_t n, int d, int rank) {
-            const int pos = P.H1[(int64_t)d * P.nch + c] + rank;
+            const int pos = TT_DCHECK(P, P.H1[(int64_t)d * P.nch + c] + rank, P.nnz);
             P.pi1[pos] = (int)n;
             const int d2 = P.tables[table_of_bag(P, P.lk_bag[n])].base2 + P.lk_i2[n];
             atomicAdd(&P.H2[(int64_t)d2 * P.nch + pos / kChunk], 1);
@@ -349,7 +349,7 @@ __global__ void __launch_bounds__(kSortThreads, 1) k_scatter13(const __grid_cons
         c, P.nnz, P.n3, cnt,
         [&](int64_t n) { return excluded(P, n) ? -1 : P.tables[table_of_bag(P, P.lk_bag[n])].base3 + P.lk_i3[n]; },
         [&](int64_t n, int d, int rank) {
-            const int pos = P.H3[(int64_t)d * P.nch + c] + rank;
+            const int pos = TT_DCHECK(P, P.H3[(int64_t)d * P.nch + c] + rank, P.nnz);
             P.pi3[pos] = (int)n;
             P.inv3[n] = pos;
         });
@@ -368,7 +368,7 @@ __global__ void __launch_bounds__(kSortThreads, 1) k_scatter2(const __grid_const
             return P.tables[table_of_bag(P, P.lk_bag[n])].base2 + P.lk_i2[n];
         },
         [&](int64_t k, int d, int rank) {
-            const int n = P.pi1[k], pos = P.H2[(int64_t)d * P.nch + c] + rank;
+            const int n = TT_DCHECK(P, P.pi1[k], P.nnz), pos = TT_DCHECK(P, P.H2[(int64_t)d * P.nch + c] + rank, P.nnz);
             P.pi21[pos] = n;
             P.g_i1[pos] = P.lk_i1[n];
             P.g_i3[pos] = P.lk_i3[n];

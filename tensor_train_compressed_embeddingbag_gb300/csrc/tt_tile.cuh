@@ -26,12 +26,13 @@ __device__ __forceinline__ void load_and_sort_tile(const Params& P, int start, i
     int p1 = 0, p3 = 0, i1 = 0, i3 = 0, bag = 0;
     float sc = 0.f;
     if (k < len) {  // grouped-order copies: one coalesced pass, no dependent loads
-        p1 = P.g_p1[start + k];
-        p3 = P.g_p3[start + k];
-        i1 = P.g_i1[start + k];
-        i3 = P.g_i3[start + k];
-        bag = P.g_bag[start + k];
-        sc = P.g_s[start + k];
+        const int64_t at = TT_DCHECK(P, (int64_t)start + k, P.nnz);
+        p1 = TT_DCHECK(P, P.g_p1[at], P.nnz);
+        p3 = TT_DCHECK(P, P.g_p3[at], P.nnz);
+        i1 = P.g_i1[at];
+        i3 = P.g_i3[at];
+        bag = TT_DCHECK(P, P.g_bag[at], P.nbags);
+        sc = P.g_s[at];
         key = ((unsigned long long)i1 << (2 * kFieldBits)) | ((unsigned long long)i3 << kFieldBits) | (unsigned long long)k;
         keys[k] = key;
     }

@@ -37,6 +37,15 @@ def test_library_exports_every_declared_symbol(lib):
         assert getattr(lib, name)
 
 
+def test_debug_library_exports_the_same_symbols():
+    """libttemb_debug.so (the kernels' index checks compiled in) offers the same C ABI."""
+    path = tt.build(debug=True)
+    out = subprocess.run(["nm", "-D", "--defined-only", path], capture_output=True, text=True).stdout
+    exported = set(re.findall(r"\bT (tt_emb_\w+)$", out, flags=re.M))
+    for name in header_functions():
+        assert name in exported, name
+
+
 def test_build_targets_sm_103a_only():
     from tensor_train_compressed_embeddingbag_gb300 import _nvcc_build as b
 
@@ -44,10 +53,11 @@ def test_build_targets_sm_103a_only():
 
 
 def test_status_strings(lib):
-    for code in range(8):
+    for code in range(9):
         s = tt.tt_emb_status_string(code)
         assert isinstance(s, str) and s
     assert "index" in tt.tt_emb_status_string(tt.TT_ERR_INDEX)
+    assert "debug" in tt.tt_emb_status_string(tt.TT_ERR_BOUNDS)
 
 
 def _create(lib, E, p, q, r, cores=(256, 512, 768)):
