@@ -249,10 +249,10 @@ __device__ void tile_bwd_tc_body(const Params& P, const TableDev& T, unsigned ch
     using L = TcBwdLayout<R>;
     constexpr int N2 = L::N2, D = 64, KR = L::kRows;
     constexpr int G2I = R * (N2 / 8);                      // G2 items: (a, 8 columns)
-    constexpr int G2PER = (G2I + kTcBwdThreads - 1) / kTcBwdThreads;
     uint64_t* bar = reinterpret_cast<uint64_t*>(sm + L::ctl);
     uint32_t* tslot = reinterpret_cast<uint32_t*>(sm + L::ctl + 8);
     int* flag = reinterpret_cast<int*>(sm + L::ctl + 12);
+    uint64_t* gbar = reinterpret_cast<uint64_t*>(sm + L::ctl + 16);  // the G2 slice's bulk copy
     unsigned long long* keys = reinterpret_cast<unsigned long long*>(sm + L::keys);
     int* sp1 = reinterpret_cast<int*>(sm + L::ints);
     int* sp3 = sp1 + kTcBwdCap;
@@ -277,19 +277,13 @@ __device__ void tile_bwd_tc_body(const Params& P, const TableDev& T, unsigned ch
     const int t = P.ntab == 1 ? 0 : P.bin2_tab[g];
     const int lane = threadIdx.x & 31, w = threadIdx.x >> 5;
 
-    // G2 slice loads (they depend only on i2) are in flight during the tile sort
+    // The G2 slice (it depends only on i2) comes by one bulk copy into the dT piece
+    // region, which is free until the first batch; it is in flight during the tile sort.
     const float* g2src = T.G2 + (int64_t)i2 * R * N2;
-    float4 g2v[G2PER][2];
-#pragma unroll
-    for (int q = 0; q < G2PER; ++q) {
-        const int e = threadIdx.x + q * kTcBwdThreads;
-        const int a = (e & 7) + 8 * (e / (8 * (N2 / 8))), jc8 = (e >> 3) % (N2 / 8);
-        g2v[q][0] = g2v[q][1] = make_float4(0.f, 0.f, 0.f, 0.f);
-        if (e < G2I) {
-            const float4* src = reinterpret_cast<const float4*>(g2src + a * N2 + jc8 * 8);
-            g2v[q][0] = __ldg(src);
-            g2v[q][1] = __ldg(src + 1);
-        }
+    float* g2raw = reinterpret_cast<float*>(sm + L::dt);
+    if (threadIdx.x == 0) {
+        mbar_init(gbar, 1);
+        bulk_copy_g2s(g2raw, g2src, (uint32_t)(R * N2 * sizeof(float)), gbar);
     }
 
     // ---- lookups of the tile, sorted by (i1, i3, position); rows and pairs
@@ -329,16 +323,18 @@ __device__ void tile_bwd_tc_body(const Params& P, const TableDev& T, unsigned ch
 
     __syncthreads();  // rowbeg / pairbeg complete
     stage_g3<R>(T, rowbeg, si3, g3s, 0, nrows);  // the first batch's G3 slices
-    // ---- G2 as the B operand of Q: rows a, K = jc, three pieces
-#pragma unroll
-    for (int q = 0; q < G2PER; ++q) {
-        const int e = threadIdx.x + q * kTcBwdThreads;
-        if (e < G2I) {
-            const int a = (e & 7) + 8 * (e / (8 * (N2 / 8))), jc8 = (e >> 3) % (N2 / 8);
-            const float v[8] = {g2v[q][0].x, g2v[q][0].y, g2v[q][0].z, g2v[q][0].w,
-                                g2v[q][1].x, g2v[q][1].y, g2v[q][1].z, g2v[q][1].w};
-            store_pieces8(g2s, L::g2p, kmaj16(a, jc8 * 8, N2), v);
-        }
+    // ---- G2 as the B operand of Q: rows a, K = jc, three pieces (from the bulk copy)
+    if (threadIdx.x == 0 && !mbar_wait(gbar, 0, P.wait_polls)) {
+        atomicOr(P.err, kErrTimeout);
+        mbar_wait(gbar, 0, kTcWaitLimit);  // the copy writes shared memory: let it finish
+    }
+    __syncthreads();
+    for (int e = threadIdx.x; e < G2I; e += kTcBwdThreads) {
+        const int a = (e & 7) + 8 * (e / (8 * (N2 / 8))), jc8 = (e >> 3) % (N2 / 8);
+        const float4* src = reinterpret_cast<const float4*>(g2raw + a * N2 + jc8 * 8);
+        const float4 x = src[0], y = src[1];
+        const float v[8] = {x.x, x.y, x.z, x.w, y.x, y.y, y.z, y.w};
+        store_pieces8(g2s, L::g2p, kmaj16(a, jc8 * 8, N2), v);
     }
     if (threadIdx.x == 32) mbar_init(bar, kTcBwdThreads / 32);  // one commit per issuing warp
     __syncthreads();  // rowid / pairid / rowbeg / pairbeg complete

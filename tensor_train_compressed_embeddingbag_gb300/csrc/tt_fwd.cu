@@ -103,8 +103,8 @@ __device__ __forceinline__ void stage_g1_rows(float* g1s, const float* G1, const
 // up to kTcTiles x 32 pairs: A = their G1 slices as rows (u, j1) x r1 (128 rows per
 // tile), B = G2^T (q2 r2 rows x r1), D_t = A_t . B^T = 32 T blocks per tile in
 // tensor memory (columns [t N, t N + N)); three TF32 MMAs per K step (hi.hi +
-// hi.lo + lo.hi).  The G2 loads are issued before the touched-pair scan so that
-// the two latencies overlap.
+// hi.lo + lo.hi).  The G2 slice's bulk copy is issued before the touched-pair scan
+// so that the two latencies overlap.
 // The block's tensor memory (fwd_tc_cols columns) is allocated at kernel entry.
 template <int R1, int NN>
 __device__ void fwd_T_group_tc(const Params& P, const TableDev& T, int i2, int half, FwdSmem S) {
@@ -124,17 +124,14 @@ __device__ void fwd_T_group_tc(const Params& P, const TableDev& T, int i2, int h
     float* Bl = Bh + NN * R1;
     const int lane = threadIdx.x & 31, w = threadIdx.x >> 5;
 
-    // G2 of this i2, element (jc, a) of B = G2[i2][a][jc]: loads in flight during the scan
-    float bx[kBPer][4];
-    {
-        const float* src = T.G2 + (int64_t)i2 * R1 * NN;
-#pragma unroll
-        for (int q = 0; q < kBPer; ++q) {
-            const int e = threadIdx.x + q * kFwdThreads;
-            const int jc = e % NN, a4 = e / NN;
-#pragma unroll
-            for (int i = 0; i < 4; ++i) bx[q][i] = e < kBQ ? __ldg(src + (4 * a4 + i) * NN + jc) : 0.f;
-        }
+    // G2 of this i2 ([a][jc], contiguous) comes by one bulk copy into the A-lo tile, which
+    // is free until the first batch; the copy is in flight during the touched-pair scan.
+    // Element (jc, a) of B is G2[i2][a][jc].
+    uint64_t* gbar = reinterpret_cast<uint64_t*>(S.tc + 16);
+    const float* g2raw = Al;
+    if (threadIdx.x == 0) {
+        mbar_init(gbar, 1);
+        bulk_copy_g2s(Al, T.G2 + (int64_t)i2 * R1 * NN, (uint32_t)(R1 * NN * sizeof(float)), gbar);
     }
     bool staged = false, failed = false;
     int nbatch = 0;
@@ -148,18 +145,26 @@ __device__ void fwd_T_group_tc(const Params& P, const TableDev& T, int i2, int h
         }
         if (m == 0) continue;
         if (!staged) {
+            if (threadIdx.x == 0 && !mbar_wait(gbar, 0, P.wait_polls)) {
+                atomicOr(P.err, kErrTimeout);
+                mbar_wait(gbar, 0, kTcWaitLimit);  // the copy writes shared memory: let it finish
+            }
+            __syncthreads();
 #pragma unroll
             for (int q = 0; q < kBPer; ++q) {
                 const int e = threadIdx.x + q * kFwdThreads;
                 if (e < kBQ) {
                     const int jc = e % NN, a4 = e / NN;
-                    float hi[4];
+                    float x[4], hi[4];
 #pragma unroll
-                    for (int i = 0; i < 4; ++i) hi[i] = tf32_round(bx[q][i]);
+                    for (int i = 0; i < 4; ++i) {
+                        x[i] = g2raw[(4 * a4 + i) * NN + jc];
+                        hi[i] = tf32_round(x[i]);
+                    }
                     const int o = tc_off(jc, 4 * a4, R1);
                     *reinterpret_cast<float4*>(Bh + o) = make_float4(hi[0], hi[1], hi[2], hi[3]);
                     *reinterpret_cast<float4*>(Bl + o) =
-                        make_float4(bx[q][0] - hi[0], bx[q][1] - hi[1], bx[q][2] - hi[2], bx[q][3] - hi[3]);
+                        make_float4(x[0] - hi[0], x[1] - hi[1], x[2] - hi[2], x[3] - hi[3]);
                 }
             }
             if (threadIdx.x == 32) mbar_init(bar, 1);
@@ -264,6 +269,8 @@ __device__ void fwd_T_group_tc(const Params& P, const TableDev& T, int i2, int h
     // after a give-up the MMAs of that batch may still run: wait for them (full
     // limit) before the tensor memory is freed
     if (failed && threadIdx.x == 0) mbar_wait(bar, nbatch & 1, kTcWaitLimit);
+    // no touched pair: the G2 copy was never waited for; it must land before the block ends
+    if (!staged && threadIdx.x == 0 && !mbar_wait(gbar, 0, kTcWaitLimit)) atomicOr(P.err, kErrTimeout);
     tc_fence_before();
     __syncthreads();
     if (w == 0) tc_dealloc(*tslot, kTcTiles * NN);
