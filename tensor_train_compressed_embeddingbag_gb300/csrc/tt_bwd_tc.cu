@@ -33,11 +33,16 @@
 // (MN) byte offset 128.  dT's 8-row groups are 16 K + 16 bytes apart instead, which
 // puts the eight rows that one quarter-warp stores in distinct banks.
 // Accumulators: M = 128 puts row r in tensor-memory lane r; M = 64 puts row r in
-// lane 32 (r / 16) + r % 16.  Each contraction keeps four accumulators -- x1 y1,
-// the first-order terms x1 y2 + x2 y1, and the second-order terms x1 y3 + x2 y2 and
-// x3 y1 -- summed when read out (small terms first).  The eight accumulator chains
-// are issued by eight threads (lane 0 of every warp) at once: an MMA this small
-// costs more to issue than to run, so one issuing thread would be the bottleneck.
+// lane 32 (r / 16) + r % 16.  The three pieces of the B operand (R rows each) lie
+// one after another with the same 8-row stride, so [y1 | y2 | y3] and [y1 | y2] are
+// themselves B operands of N = 3R and 2R rows: one MMA x1 [y1 | y2 | y3] gives x1 y1,
+// x1 y2 and x1 y3 in three R-column accumulators, x2 [y1 | y2] adds x2 y1 and x2 y2
+// to the first two, and x3 y1 adds to the first.  Three MMAs per K step instead of
+// six, and each A piece (the large operand: dT) is read from shared memory once per
+// K step; the tensor core of these skinny products is bound by its shared-memory
+// operand reads.  The column blocks are summed when read out (small terms first).
+// Q runs as two chains (x1 [..] and x2 [..] + x3 y1, separate accumulators) and
+// dG2^T as one, each issued by its own thread (lane 0 of warps 0, 1, 2).
 #include "tt_dims.cuh"
 #include "tt_tc.cuh"
 #include "tt_tile.cuh"
@@ -48,11 +53,18 @@ constexpr int kTcBwdThreads = 256;
 constexpr int kTcBwdCap = 64;    // lookups per tile
 constexpr int kTcBwdPairs = 16;  // pairs per batch: Q has M = 16 x q1 = 64 rows
 constexpr int kTcBwdG3Rows = 16;  // G3 slices staged in shared memory per batch (its first rows)
-constexpr uint32_t kTcBwdCols = 256;  // tensor-memory columns: Q terms at 0, 32, 64, 96; dG2^T terms at 128 ..
+constexpr uint32_t kTcBwdCols = 256;  // tensor-memory columns (tc_cols_q1, tc_cols_q2, tc_cols_g below)
+constexpr int kTcBwdIssuers = 3;      // accumulator chains per batch, one commit each
 
 __host__ __device__ constexpr bool bwd_tc_class(int dclass) { return dclass == kQ444R32 || dclass == kQ444R16; }
 
 __host__ __device__ constexpr size_t al128(size_t x) { return (x + 127) & ~(size_t)127; }
+
+// Tensor-memory column of each accumulator (multiples of 32): Q's x1 chain (3R
+// columns), Q's x2 / x3 chain (2R), dG2^T (3R).
+__host__ __device__ constexpr uint32_t tc_cols_q2(int R) { return (3u * R + 31u) & ~31u; }
+__host__ __device__ constexpr uint32_t tc_cols_g(int R) { return tc_cols_q2(R) + ((2u * R + 31u) & ~31u); }
+static_assert(tc_cols_g(32) + 96 <= kTcBwdCols && tc_cols_g(16) + 48 <= kTcBwdCols, "accumulators fit");
 
 template <int R>
 struct TcBwdLayout {
@@ -116,20 +128,19 @@ __device__ __forceinline__ void tc_ld16(uint32_t taddr, float* v) {
     for (int i = 0; i < 16; ++i) v[i] = __uint_as_float(r[i]);
 }
 
-// 16 columns of the four accumulators of a contraction (at column offsets 0, 32,
-// 64, 96 from base: x1y1, first order, two second-order parts), summed small terms
-// first into v (t: scratch).
-__device__ __forceinline__ void tc_sum4x16(uint32_t base, float* v, float* t) {
-    tc_ld16(base + 96, v);
-    tc_ld16(base + 64, t);
+// 16 columns of a product's column blocks, summed last block first into v (t:
+// scratch): c[0] the block holding x1 y1, the others smaller terms.
+template <int NB>
+__device__ __forceinline__ void tc_sumx16(uint32_t lanebase, const uint32_t (&c)[NB], float* v, float* t) {
+    tc_ld16(lanebase + c[NB - 1], t);
 #pragma unroll
-    for (int a = 0; a < 16; ++a) t[a] += v[a];
-    tc_ld16(base + 32, v);
+    for (int b = NB - 2; b >= 0; --b) {
+        tc_ld16(lanebase + c[b], v);
 #pragma unroll
-    for (int a = 0; a < 16; ++a) t[a] += v[a];
-    tc_ld16(base, v);
+        for (int a = 0; a < 16; ++a) t[a] += v[a];
+    }
 #pragma unroll
-    for (int a = 0; a < 16; ++a) v[a] += t[a];
+    for (int a = 0; a < 16; ++a) v[a] = t[a];
 }
 
 // x rounded to a bf16 value (8-bit significand, ties away from zero), kept in fp32
@@ -336,17 +347,19 @@ __device__ void tile_bwd_tc_body(const Params& P, const TableDev& T, unsigned ch
         const float v[8] = {x.x, x.y, x.z, x.w, y.x, y.y, y.z, y.w};
         store_pieces8(g2s, L::g2p, kmaj16(a, jc8 * 8, N2), v);
     }
-    if (threadIdx.x == 32) mbar_init(bar, kTcBwdThreads / 32);  // one commit per issuing warp
+    if (threadIdx.x == 32) mbar_init(bar, kTcBwdIssuers);  // one commit per accumulator chain
     __syncthreads();  // rowid / pairid / rowbeg / pairbeg complete
 
     // ---- gs: summed upstream gradient of every tile-row
     tile_gs(P, len, nrows, sbag, ss, rowbeg, gs, D);
 
     // ---- batches of kTcBwdPairs pairs: dT and the G1 rows as pieces, then the MMAs
-    constexpr uint32_t kIdescQ = tc_idesc_bf16(64, R, 0);
-    constexpr uint32_t kIdescG = tc_idesc_bf16(N2, R, 1);
+    constexpr uint32_t kIdescQ3 = tc_idesc_bf16(64, 3 * R, 0), kIdescQ2 = tc_idesc_bf16(64, 2 * R, 0),
+                       kIdescQ1 = tc_idesc_bf16(64, R, 0);
+    constexpr uint32_t kIdescG3 = tc_idesc_bf16(N2, 3 * R, 1), kIdescG2 = tc_idesc_bf16(N2, 2 * R, 1),
+                       kIdescG1 = tc_idesc_bf16(N2, R, 1);
     constexpr uint32_t DTS = L::dts;
-    const uint32_t tq = *tslot, tg = *tslot + 128;  // three accumulators each, 32 columns apart
+    const uint32_t tq1 = *tslot, tq2 = *tslot + tc_cols_q2(R), tg = *tslot + tc_cols_g(R);
     // G1 item of this thread (row a, eight K positions (pair, j1)); the next batch's values
     // are loaded while the MMAs of the current one run
     const bool g1item = (int)threadIdx.x < R * (KR / 8);
@@ -415,29 +428,27 @@ __device__ void tile_bwd_tc_body(const Params& P, const TableDev& T, unsigned ch
         tc_fence_before();
         __syncthreads();
         tc_fence_after();
-        if (lane == 0) {
+        if (lane == 0 && w < kTcBwdIssuers) {
             // Q = dT G2^T (A = dT K-major rows (u, j1), B = G2 K-major rows a, K = jc) and
             // dG2^T += dT^T G1 (A = dT read MN-major rows jc, B = G1 K-major rows a, K = (u, j1)).
-            // Warp w's lane 0 issues accumulator chain w: warps 0-3 the Q terms x1y1, x1y2 + x2y1,
-            // x1y3 + x2y2, x3y1; warps 4-7 the same terms of dG2^T.  Each chain commits once.
+            // Warp 0: Q's x1 [y1 | y2 | y3]; warp 1: Q's x2 [y1 | y2] + x3 y1; warp 2: dG2^T's
+            // three MMAs per K step.  Each chain commits once.
             const uint32_t d0 = smem_addr(dts), g1b = smem_addr(g1s), g2a = smem_addr(g2s);
-            const int chain = w & 3;
-            if (w < 4) {
-                const uint32_t d = tq + 32 * chain;
+            if (w < 2) {
 #pragma unroll
                 for (int ks = 0; ks < N2 / 16; ++ks) {
                     const uint64_t a0 = tc_desc(d0 + ks * 256, 128, DTS);
                     const uint64_t b0 = tc_desc(g2a + ks * 256, 128, N2 * 16);
                     const uint64_t a1 = a0 + (L::dtp >> 4), a2 = a0 + 2 * (L::dtp >> 4);
-                    const uint64_t b1 = b0 + (L::g2p >> 4), b2 = b0 + 2 * (L::g2p >> 4);
                     const bool acc = ks > 0;
-                    if (chain == 0) tc_mma_f16(d, a0, b0, kIdescQ, acc);
-                    if (chain == 1) { tc_mma_f16(d, a0, b1, kIdescQ, acc); tc_mma_f16(d, a1, b0, kIdescQ, true); }
-                    if (chain == 2) { tc_mma_f16(d, a0, b2, kIdescQ, acc); tc_mma_f16(d, a1, b1, kIdescQ, true); }
-                    if (chain == 3) tc_mma_f16(d, a2, b0, kIdescQ, acc);
+                    if (w == 0) {
+                        tc_mma_f16(tq1, a0, b0, kIdescQ3, acc);
+                    } else {
+                        tc_mma_f16(tq2, a1, b0, kIdescQ2, acc);
+                        tc_mma_f16(tq2, a2, b0, kIdescQ1, true);
+                    }
                 }
             } else {
-                const uint32_t d = tg + 32 * chain;
                 const int NG = (4 * nb + 15) / 16;
 #pragma unroll
                 for (int ks = 0; ks < KR / 16; ++ks) {
@@ -445,12 +456,9 @@ __device__ void tile_bwd_tc_body(const Params& P, const TableDev& T, unsigned ch
                         const uint64_t a0 = tc_desc(d0 + ks * 2 * DTS, DTS, 128);
                         const uint64_t b0 = tc_desc(g1b + ks * 256, 128, KR * 16);
                         const uint64_t a1 = a0 + (L::dtp >> 4), a2 = a0 + 2 * (L::dtp >> 4);
-                        const uint64_t b1 = b0 + (L::g1p >> 4), b2 = b0 + 2 * (L::g1p >> 4);
-                        const bool acc = nbatch > 0 || ks > 0;
-                        if (chain == 0) tc_mma_f16(d, a0, b0, kIdescG, acc);
-                        if (chain == 1) { tc_mma_f16(d, a0, b1, kIdescG, acc); tc_mma_f16(d, a1, b0, kIdescG, true); }
-                        if (chain == 2) { tc_mma_f16(d, a0, b2, kIdescG, acc); tc_mma_f16(d, a1, b1, kIdescG, true); }
-                        if (chain == 3) tc_mma_f16(d, a2, b0, kIdescG, acc);
+                        tc_mma_f16(tg, a0, b0, kIdescG3, nbatch > 0 || ks > 0);
+                        tc_mma_f16(tg, a1, b0, kIdescG2, true);
+                        tc_mma_f16(tg, a2, b0, kIdescG1, true);
                     }
                 }
             }
@@ -475,7 +483,7 @@ __device__ void tile_bwd_tc_body(const Params& P, const TableDev& T, unsigned ch
             failed = true;
             break;
         }
-        // Q rows (u, j1): M = 64 puts row r in lane 32 (r / 16) + r % 16; Q = x1y1 + (first + second order)
+        // Q rows (u, j1): M = 64 puts row r in lane 32 (r / 16) + r % 16
         if (w < 4) {
             const int r = 16 * w + lane, u = r >> 2, j1 = r & 3;
             const bool live = lane < 16 && u < nb;
@@ -483,7 +491,8 @@ __device__ void tile_bwd_tc_body(const Params& P, const TableDev& T, unsigned ch
 #pragma unroll 1
             for (int c0 = 0; c0 < R; c0 += 16) {
                 float q[16], e[16];
-                tc_sum4x16(tq + ((uint32_t)(32 * w) << 16) + c0, q, e);
+                const uint32_t cq[5] = {tq1 + c0, tq2 + c0, tq1 + R + c0, tq2 + R + c0, tq1 + 2 * R + c0};
+                tc_sumx16<5>((uint32_t)(32 * w) << 16, cq, q, e);
                 if (live) {
 #pragma unroll
                     for (int a = 0; a < 16; a += 4)
@@ -516,7 +525,8 @@ __device__ void tile_bwd_tc_body(const Params& P, const TableDev& T, unsigned ch
 #pragma unroll 1
         for (int c0 = 0; c0 < R; c0 += 16) {
             float gv[16], ge[16];
-            tc_sum4x16(tg + ((uint32_t)(32 * w) << 16) + c0, gv, ge);
+            const uint32_t cg[3] = {tg + c0, tg + R + c0, tg + 2 * R + c0};
+            tc_sumx16<3>((uint32_t)(32 * w) << 16, cg, gv, ge);
             if (live) {
                 if (nt == 1) {
                     for (int a = 0; a < 16; ++a) core_update(P, G2p, A2p, (int64_t)(c0 + a) * N2 + jc, gv[a]);
