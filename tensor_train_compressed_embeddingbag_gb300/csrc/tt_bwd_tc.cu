@@ -196,6 +196,13 @@ __device__ __forceinline__ void store_pieces8(unsigned char* base, size_t stride
         *reinterpret_cast<uint4*>(base + p * stride + 2 * (size_t)off) = make_uint4(w[p][0], w[p][1], w[p][2], w[p][3]);
 }
 
+// 16 bytes from shared memory at a shared-window address (an explicit shared load).
+__device__ __forceinline__ float4 lds128(uint32_t a) {
+    float4 v;
+    asm volatile("ld.shared.v4.f32 {%0, %1, %2, %3}, [%4];" : "=f"(v.x), "=f"(v.y), "=f"(v.z), "=f"(v.w) : "r"(a));
+    return v;
+}
+
 // Asynchronous 16-byte global-to-shared copies (completion: cp_async_wait_all).
 __device__ __forceinline__ void cp_async16(void* dst, const void* src) {
     asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(smem_addr(dst)), "l"(src) : "memory");
@@ -400,22 +407,26 @@ __device__ void tile_bwd_tc_body(const Params& P, const TableDev& T, unsigned ch
                         if (kk != kb && rowid[kk] == rowid[kk - 1]) continue;  // once per tile-row
                         const float4 gv = *reinterpret_cast<const float4*>(gs + rowid[kk] * D + (j1 * 4 + j2) * 4);
                         const int rs = rowid[kk] - rowid[pairbeg[u0]];  // staged position of this row
-                        const float4* g3 = (rs < kTcBwdG3Rows
-                                                ? reinterpret_cast<const float4*>(g3s + rs * (R * 4))
-                                                : reinterpret_cast<const float4*>(T.G3 + (int64_t)si3[kk] * (R * 4))) + c0;
+                        // the G3 slice from shared memory (staged rows) or global memory, each
+                        // path with its own load form: a pointer that may be either would turn
+                        // every load into a slow generic one
+                        float4 y[CH];
+                        if (rs < kTcBwdG3Rows) {
+                            const uint32_t a0 = smem_addr(g3s + rs * (R * 4) + c0 * 4);
 #pragma unroll
-                        for (int h8 = 0; h8 < CH; h8 += 8) {
-                            float4 y[8];
+                            for (int i = 0; i < CH; ++i) y[i] = lds128(a0 + 16 * i);
+                        } else {
+                            const float4* g3 = reinterpret_cast<const float4*>(T.G3 + (int64_t)si3[kk] * (R * 4)) + c0;
 #pragma unroll
-                            for (int i = 0; i < 8; ++i) y[i] = g3[h8 + i];
+                            for (int i = 0; i < CH; ++i) y[i] = __ldg(g3 + i);
+                        }
 #pragma unroll
-                            for (int i = 0; i < 8; ++i) {
-                                float a = acc[h8 + i];
-                                a = fmaf(gv.x, y[i].x, a);
-                                a = fmaf(gv.y, y[i].y, a);
-                                a = fmaf(gv.z, y[i].z, a);
-                                acc[h8 + i] = fmaf(gv.w, y[i].w, a);
-                            }
+                        for (int i = 0; i < CH; ++i) {
+                            float a = acc[i];
+                            a = fmaf(gv.x, y[i].x, a);
+                            a = fmaf(gv.y, y[i].y, a);
+                            a = fmaf(gv.z, y[i].z, a);
+                            acc[i] = fmaf(gv.w, y[i].w, a);
                         }
                     }
                 }
