@@ -224,41 +224,39 @@ __device__ __forceinline__ void stage_g3(const TableDev& T, const int* rowbeg, c
     asm volatile("cp.async.commit_group;" ::: "memory");
 }
 
-// dG3 partial per tile-row, items [i0, i1) of nrows x R: P3[c][j3] = sum_j12 T[j12][c]
-// gs[j12 q3 + j3], T of the pair from the forward pass (PI items' loads in flight together).
+// dG3 partial per tile-row, items [i0, i1) of nrows x R/4 (a row and four columns c):
+// P3[c][j3] = sum_j12 T[j12][c] gs[j12 q3 + j3], T of the pair from the forward pass
+// (sixteen float4 loads of T in flight per item).  Items go to the highest threads
+// first: the low warps issue the MMAs and start late.
 template <int R>
 __device__ __forceinline__ void tile_p3(const Params& P, const TableDev& T, int i2, int start, const int* rowbeg,
                                         const int* si1, const float* gs, int i0, int i1) {
-    constexpr int PI = 3, D = 64;
-    for (int e0 = i0 + threadIdx.x; e0 < i1; e0 += PI * kTcBwdThreads) {
-        float tv[PI][16];
-        int rowv[PI], cv[PI];
+    constexpr int D = 64, C4 = R / 4;
+    for (int e = i0 + (kTcBwdThreads - 1 - (int)threadIdx.x); e < i1; e += kTcBwdThreads) {
+        const int row = e / C4, c4 = e - row * C4;
+        const int kk = rowbeg[row];
+        const float4* Tp = reinterpret_cast<const float4*>(
+                               P.Tbuf + T.tbase + ((int64_t)i2 * T.p1 + si1[kk]) * (int64_t)(16 * R)) + c4;
+        float4 tv[16];
 #pragma unroll
-        for (int v = 0; v < PI; ++v) {
-            const int e = e0 + v * kTcBwdThreads;
-            rowv[v] = e < i1 ? e / R : -1;
-            cv[v] = e < i1 ? e - rowv[v] * R : 0;
-            const int kk = rowv[v] >= 0 ? rowbeg[rowv[v]] : 0;
-            const float* Tp = P.Tbuf + T.tbase + ((int64_t)i2 * T.p1 + si1[kk]) * (int64_t)(16 * R) + cv[v];
+        for (int j12 = 0; j12 < 16; ++j12) tv[j12] = __ldg(Tp + j12 * C4);
+        const float* gr = gs + row * D;
+        float acc[4][4] = {};
 #pragma unroll
-            for (int j12 = 0; j12 < 16; ++j12) tv[v][j12] = rowv[v] >= 0 ? __ldg(Tp + j12 * R) : 0.f;
-        }
+        for (int j12 = 0; j12 < 16; ++j12) {
+            const float4 x = *reinterpret_cast<const float4*>(gr + j12 * 4);
+            const float t4[4] = {tv[j12].x, tv[j12].y, tv[j12].z, tv[j12].w};
 #pragma unroll
-        for (int v = 0; v < PI; ++v) {
-            if (rowv[v] < 0) continue;
-            const float* gr = gs + rowv[v] * D;
-            float acc[4] = {0.f, 0.f, 0.f, 0.f};
-#pragma unroll
-            for (int j12 = 0; j12 < 16; ++j12) {
-                const float4 x = *reinterpret_cast<const float4*>(gr + j12 * 4);
-                acc[0] = fmaf(tv[v][j12], x.x, acc[0]);
-                acc[1] = fmaf(tv[v][j12], x.y, acc[1]);
-                acc[2] = fmaf(tv[v][j12], x.z, acc[2]);
-                acc[3] = fmaf(tv[v][j12], x.w, acc[3]);
+            for (int c = 0; c < 4; ++c) {
+                acc[c][0] = fmaf(t4[c], x.x, acc[c][0]);
+                acc[c][1] = fmaf(t4[c], x.y, acc[c][1]);
+                acc[c][2] = fmaf(t4[c], x.z, acc[c][2]);
+                acc[c][3] = fmaf(t4[c], x.w, acc[c][3]);
             }
-            float* dst = P.Pbuf + (int64_t)(start + rowbeg[rowv[v]]) * P.ps_max + cv[v] * 4;
-            *reinterpret_cast<float4*>(dst) = make_float4(acc[0], acc[1], acc[2], acc[3]);
         }
+        float4* dst = reinterpret_cast<float4*>(P.Pbuf + (int64_t)(start + kk) * P.ps_max + c4 * 16);
+#pragma unroll
+        for (int c = 0; c < 4; ++c) dst[c] = make_float4(acc[c][0], acc[c][1], acc[c][2], acc[c][3]);
     }
 }
 
@@ -480,7 +478,7 @@ __device__ void tile_bwd_tc_body(const Params& P, const TableDev& T, unsigned ch
             stage_g3<R>(T, rowbeg, si3, g3s, rowid[pairbeg[u0 + kTcBwdPairs]], nrows);
         }
         {   // this batch's share of the dG3 partials, computed while the MMAs run
-            const int nbt = (npairs + kTcBwdPairs - 1) / kTcBwdPairs, items = nrows * R;
+            const int nbt = (npairs + kTcBwdPairs - 1) / kTcBwdPairs, items = nrows * (R / 4);
             const int per = (items + nbt - 1) / nbt;
             tile_p3<R>(P, T, i2, start, rowbeg, si1, gs, nbatch * per, min(items, (nbatch + 1) * per));
         }
