@@ -77,20 +77,25 @@ struct TcBwdLayout {
     static constexpr size_t sh = begs + 2 * 4 * (kTcBwdCap + 4);
     static constexpr size_t gs = al128(sh + 4 * 64);                 // [rows][64] fp32
     static constexpr size_t g2 = al128(gs + 4 * kTcBwdCap * 64);     // 3 pieces of [R][N2] bf16, K-major
-    static constexpr size_t g2p = 2 * (size_t)R * N2;               //   bytes per piece
+    static constexpr uint32_t g2sbo = 16 * N2 + 16;                   //   8-row group stride (bytes, padded)
+    static constexpr size_t g2p = (size_t)(R / 8) * g2sbo;          //   bytes per piece
     static constexpr size_t g1 = al128(g2 + 3 * g2p);                // 3 pieces of [R][kRows] bf16, K-major
-    static constexpr size_t g1p = 2 * (size_t)R * kRows;
+    static constexpr uint32_t g1sbo = 16 * kRows + 16;                //   8-row group stride (bytes, padded)
+    static constexpr size_t g1p = (size_t)(R / 8) * g1sbo;
     static constexpr size_t dt = al128(g1 + 3 * g1p);                // 3 pieces of [kRows][N2] bf16, K-major
     static constexpr uint32_t dts = 16 * N2 + 16;                     //   8-row group stride (bytes, padded)
     static constexpr size_t dtp = (size_t)(kRows / 8) * dts;
     static constexpr size_t g3 = dt + 3 * dtp;                       // G3 slices of a batch's first rows (fp32)
     static constexpr size_t total = g3 + 4 * (size_t)kTcBwdG3Rows * R * 4;
-    static_assert(g2p % 128 == 0 && g1p % 128 == 0 && dtp % 128 == 0, "pieces aligned");
+    static_assert(g2p % 16 == 0 && g1p % 16 == 0 && dtp % 16 == 0, "pieces 16-byte aligned");
+    // two blocks per SM: 228 KB of shared memory per SM, 1 KB of it reserved per block
+    static_assert(2 * (total + 1024) <= 228 * 1024, "two blocks per SM");
 };
 
-// K-major bf16 element offset of (row, k) in a tile whose K extent is K.
+// K-major bf16 element offset of (row, k) in a tile whose K extent is K, its 8-row
+// groups padded by 16 bytes (8 K + 8 elements apart).
 __device__ __forceinline__ int kmaj16(int row, int k, int K) {
-    return (row >> 3) * (K * 8) + (k >> 3) * 64 + (row & 7) * 8 + (k & 7);
+    return (row >> 3) * (K * 8 + 8) + (k >> 3) * 64 + (row & 7) * 8 + (k & 7);
 }
 
 // Byte offset of dT element (row, jc) in a piece: padded 8-row groups.
@@ -447,7 +452,7 @@ __device__ void tile_bwd_tc_body(const Params& P, const TableDev& T, unsigned ch
 #pragma unroll
                 for (int ks = 0; ks < N2 / 16; ++ks) {
                     const uint64_t a0 = tc_desc(d0 + ks * 256, 128, DTS);
-                    const uint64_t b0 = tc_desc(g2a + ks * 256, 128, N2 * 16);
+                    const uint64_t b0 = tc_desc(g2a + ks * 256, 128, L::g2sbo);
                     const uint64_t a1 = a0 + (L::dtp >> 4), a2 = a0 + 2 * (L::dtp >> 4);
                     const bool acc = ks > 0;
                     if (w == 0) {
@@ -463,7 +468,7 @@ __device__ void tile_bwd_tc_body(const Params& P, const TableDev& T, unsigned ch
                 for (int ks = 0; ks < KR / 16; ++ks) {
                     if (ks < NG) {
                         const uint64_t a0 = tc_desc(d0 + ks * 2 * DTS, DTS, 128);
-                        const uint64_t b0 = tc_desc(g1b + ks * 256, 128, KR * 16);
+                        const uint64_t b0 = tc_desc(g1b + ks * 256, 128, L::g1sbo);
                         const uint64_t a1 = a0 + (L::dtp >> 4), a2 = a0 + 2 * (L::dtp >> 4);
                         tc_mma_f16(tg, a0, b0, kIdescG3, nbatch > 0 || ks > 0);
                         tc_mma_f16(tg, a1, b0, kIdescG2, true);
