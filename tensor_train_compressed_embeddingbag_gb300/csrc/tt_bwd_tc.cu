@@ -85,8 +85,9 @@ struct TcBwdLayout {
     static constexpr size_t dt = al128(g1 + 3 * g1p);                // 3 pieces of [kRows][N2] bf16, K-major
     static constexpr uint32_t dts = 16 * N2 + 16;                     //   8-row group stride (bytes, padded)
     static constexpr size_t dtp = (size_t)(kRows / 8) * dts;
-    static constexpr size_t g3 = dt + 3 * dtp;                       // G3 slices of a batch's first rows (fp32)
-    static constexpr size_t total = g3 + 4 * (size_t)kTcBwdG3Rows * R * 4;
+    static constexpr size_t g3 = dt + 3 * dtp;                       // G3 slices of a batch's first rows (fp32,
+                                                                     //   R + 1 float4 a row: a gap between the halves)
+    static constexpr size_t total = g3 + 4 * (size_t)kTcBwdG3Rows * (R * 4 + 4);
     static_assert(g2p % 16 == 0 && g1p % 16 == 0 && dtp % 16 == 0, "pieces 16-byte aligned");
     // two blocks per SM: 228 KB of shared memory per SM, 1 KB of it reserved per block
     static_assert(2 * (total + 1024) <= 228 * 1024, "two blocks per SM");
@@ -216,7 +217,9 @@ __device__ __forceinline__ void cp_async_wait_all() {
     asm volatile("cp.async.commit_group;\n\tcp.async.wait_group 0;" ::: "memory");
 }
 
-// Start copying the G3 slices of tile-rows [r0, r0 + kTcBwdG3Rows) (clipped at nrows) into g3s.
+// Start copying the G3 slices of tile-rows [r0, r0 + kTcBwdG3Rows) (clipped at nrows) into g3s:
+// slice r at float4 r (R + 1), its second half one float4 further (the dT lanes of a
+// quarter-warp read both halves at once, now from different banks).
 template <int R>
 __device__ __forceinline__ void stage_g3(const TableDev& T, const int* rowbeg, const int* si3, float* g3s, int r0,
                                          int nrows) {
@@ -224,7 +227,7 @@ __device__ __forceinline__ void stage_g3(const TableDev& T, const int* rowbeg, c
     const int n = min(kTcBwdG3Rows, nrows - r0) * CH;
     for (int e = threadIdx.x; e < n; e += kTcBwdThreads) {
         const int r = e / CH, c = e - r * CH;
-        cp_async16(g3s + (r * CH + c) * 4, T.G3 + (int64_t)si3[rowbeg[r0 + r]] * (R * 4) + c * 4);
+        cp_async16(g3s + (r * (CH + 1) + c + (c >= CH / 2 ? 1 : 0)) * 4, T.G3 + (int64_t)si3[rowbeg[r0 + r]] * (R * 4) + c * 4);
     }
     asm volatile("cp.async.commit_group;" ::: "memory");
 }
@@ -298,13 +301,21 @@ __device__ void tile_bwd_tc_body(const Params& P, const TableDev& T, unsigned ch
     const int t = P.ntab == 1 ? 0 : P.bin2_tab[g];
     const int lane = threadIdx.x & 31, w = threadIdx.x >> 5;
 
-    // The G2 slice (it depends only on i2) comes by one bulk copy into the dT piece
-    // region, which is free until the first batch; it is in flight during the tile sort.
+    // The G2 slice (it depends only on i2) comes by bulk copies, one a row a, into the dT
+    // piece region (free until the first batch), rows N2 + 4 floats apart so that the
+    // eight rows one quarter-warp reads below lie in different banks; the copies are in
+    // flight during the tile sort.
     const float* g2src = T.G2 + (int64_t)i2 * R * N2;
     float* g2raw = reinterpret_cast<float*>(sm + L::dt);
-    if (threadIdx.x == 0) {
-        mbar_init(gbar, 1);
-        bulk_copy_g2s(g2raw, g2src, (uint32_t)(R * N2 * sizeof(float)), gbar);
+    static_assert(R * (N2 + 4) * 4 <= 3 * L::dtp, "raw G2 rows fit the dT region");
+    if (threadIdx.x < 32) {
+        if (threadIdx.x == 0) {
+            mbar_init(gbar, 1);
+            bulk_expect(gbar, (uint32_t)(R * N2 * sizeof(float)));
+        }
+        __syncwarp();
+        if ((int)threadIdx.x < R)
+            bulk_copy(g2raw + threadIdx.x * (N2 + 4), g2src + threadIdx.x * N2, (uint32_t)(N2 * sizeof(float)), gbar);
     }
 
     // ---- lookups of the tile, sorted by (i1, i3, position); rows and pairs
@@ -352,7 +363,7 @@ __device__ void tile_bwd_tc_body(const Params& P, const TableDev& T, unsigned ch
     __syncthreads();
     for (int e = threadIdx.x; e < G2I; e += kTcBwdThreads) {
         const int a = (e & 7) + 8 * (e / (8 * (N2 / 8))), jc8 = (e >> 3) % (N2 / 8);
-        const float4* src = reinterpret_cast<const float4*>(g2raw + a * N2 + jc8 * 8);
+        const float4* src = reinterpret_cast<const float4*>(g2raw + a * (N2 + 4) + jc8 * 8);
         const float4 x = src[0], y = src[1];
         const float v[8] = {x.x, x.y, x.z, x.w, y.x, y.y, y.z, y.w};
         store_pieces8(g2s, L::g2p, kmaj16(a, jc8 * 8, N2), v);
@@ -415,7 +426,7 @@ __device__ void tile_bwd_tc_body(const Params& P, const TableDev& T, unsigned ch
                         // every load into a slow generic one
                         float4 y[CH];
                         if (rs < kTcBwdG3Rows) {
-                            const uint32_t a0 = smem_addr(g3s + rs * (R * 4) + c0 * 4);
+                            const uint32_t a0 = smem_addr(g3s + (rs * (R + 1) + c0 + (c0 ? 1 : 0)) * 4);
 #pragma unroll
                             for (int i = 0; i < CH; ++i) y[i] = lds128(a0 + 16 * i);
                         } else {

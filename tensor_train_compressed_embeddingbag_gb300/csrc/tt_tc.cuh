@@ -109,17 +109,24 @@ __device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, uint32
     return false;
 }
 
-// Bulk asynchronous copy (the TMA's untiled form) of `bytes` contiguous bytes from
-// global to shared memory, completion signalled on `bar` as transaction bytes.  One
-// thread: announce the bytes on the mbarrier (its one arrival), then issue the copy.
-// Both addresses 16-byte aligned, bytes a multiple of 16.
-__device__ __forceinline__ void bulk_copy_g2s(void* dst, const void* src, uint32_t bytes, uint64_t* bar) {
+// Bulk asynchronous copies (the TMA's untiled form) from global to shared memory,
+// completion signalled on an mbarrier as transaction bytes.  One thread announces
+// the bytes of all the copies (its arrival, before any copy is issued); then any
+// thread issues copies of `bytes` contiguous bytes (both addresses 16-byte aligned,
+// bytes a multiple of 16).
+__device__ __forceinline__ void bulk_expect(uint64_t* bar, uint32_t bytes) {
     asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(smem_addr(bar)), "r"(bytes)
                  : "memory");
+}
+__device__ __forceinline__ void bulk_copy(void* dst, const void* src, uint32_t bytes, uint64_t* bar) {
     asm volatile("cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(
                      smem_addr(dst)),
                  "l"(src), "r"(bytes), "r"(smem_addr(bar))
                  : "memory");
+}
+__device__ __forceinline__ void bulk_copy_g2s(void* dst, const void* src, uint32_t bytes, uint64_t* bar) {
+    bulk_expect(bar, bytes);
+    bulk_copy(dst, src, bytes, bar);
 }
 
 // Warp-collective: 32 consecutive fp32 columns of this warp's 32 lanes (lane i of
