@@ -45,7 +45,7 @@ struct tt_emb {
     std::vector<TableDev> tabs;  // host copy
     TableDev* d_tables = nullptr;
     int* d_bins = nullptr;       // bin -> table for the three digits
-    int* d_fixed = nullptr;      // err, (spare x2), ntiles, epoch, dstep, nincl, scan_done, grp_done[2 n2]
+    int* d_fixed = nullptr;      // err, (spare x2), ntiles, epoch, dstep, nincl, scan_done, grp_done[2 n2], dec_done
     float* d_tbuf = nullptr;
     int64_t tbuf_floats = 0;
     int* d_tflag = nullptr;      // dense touched-pair flags
@@ -333,7 +333,7 @@ tt_status build_handle(tt_emb* h, int ntab, const tt_table_desc* d) {
     }
     if (cudaMalloc(&h->d_tables, sizeof(TableDev) * ntab) != cudaSuccess) return TT_ERR_NOMEM;
     if (cudaMalloc(&h->d_bins, sizeof(int) * bins.size()) != cudaSuccess) return TT_ERR_NOMEM;
-    const int nfixed = 8 + 2 * n2;
+    const int nfixed = 8 + 2 * n2 + kDecDoneSlots;
     if (cudaMalloc(&h->d_fixed, sizeof(int) * nfixed) != cudaSuccess) return TT_ERR_NOMEM;
     if (cudaMalloc(&h->d_tbuf, sizeof(float) * std::max<int64_t>(tb, 1)) != cudaSuccess) return TT_ERR_NOMEM;
     if (cudaMalloc(&h->d_tflag, sizeof(int) * std::max<int64_t>(fb, 1)) != cudaSuccess) return TT_ERR_NOMEM;
@@ -361,6 +361,7 @@ tt_status build_handle(tt_emb* h, int ntab, const tt_table_desc* d) {
     P.nincl = h->d_fixed + 6;
     P.scan_done = h->d_fixed + 7;
     P.grp_done = h->d_fixed + 8;
+    P.dec_done = h->d_fixed + 8 + 2 * n2;
     P.Tbuf = h->d_tbuf;
     P.tflag = h->d_tflag;
     return TT_OK;

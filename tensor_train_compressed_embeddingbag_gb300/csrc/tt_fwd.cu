@@ -68,7 +68,7 @@ __device__ __forceinline__ int touched_list(const Params& P, const TableDev& T, 
     int m = 0;
     for (int b = base; b < end; b += blockDim.x) {
         const int i1 = b + threadIdx.x;
-        const int f = (i1 < end) && (fl[i1] == epoch);
+        const int f = (i1 < end) && (__ldcg(fl + i1) == epoch);
         int tot;
         const int ex = block_scan_excl(f, sh, &tot);
         if (f) ulist[m + ex] = i1;
@@ -412,7 +412,12 @@ __global__ void __launch_bounds__(kFwdThreads, 2) k_fwd_T(const __grid_constant_
     // released at once.  (The previous kernels of the library hold no tensor memory.)
     const uint32_t tcols = fwd_tc_cols(DC >= 0 ? DC : T.dclass);
     if (tcols != 0 && threadIdx.x < 32) tc_alloc(reinterpret_cast<uint32_t*>(smraw + kFwdTcBase + 8), tcols);
-    pdl_entry();
+    if (P.small) {  // the decode blocks' touched flags, not the end of the decode grid
+        pdl_launch_dependents();
+        wait_decode_flags(P);
+    } else {
+        pdl_entry();
+    }
     FwdSmem S;
     S.ulist = (int*)smraw;
     S.sh = S.ulist + kListCap;

@@ -164,6 +164,8 @@ struct Params {
     int* grp_first;                 // [n2]
     int* grp_ntiles;                // [n2]
     int* grp_done;                  // [n2], zero between calls
+    int* dec_done;                  // [kDecDoneSlots]: small-path decode block c stores the pass's
+                                    // epoch once the touched flags of its lookups are written
     float* Tbuf;
     int* rep1;                      // [nnz] by position in pi1: partial slot of the tile-pair starting at that lookup, or -1
     int* rep3;                      // [nnz] by position in pi3: partial slot of the tile-row starting at that lookup, or -1
@@ -257,9 +259,29 @@ __device__ __forceinline__ void core_update_n(const Params& P, float* G, float* 
     }
 }
 
+__device__ __forceinline__ void pdl_launch_dependents() { asm volatile("griddepcontrol.launch_dependents;" ::: "memory"); }
+__device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
 __device__ __forceinline__ void pdl_entry() {
-    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
-    asm volatile("griddepcontrol.wait;" ::: "memory");
+    pdl_launch_dependents();
+    pdl_wait();
+}
+
+constexpr int kDecDoneSlots = 64;        // >= the small path's decode blocks
+constexpr int kDecodeFlagPolls = 256;    // polls of the decode stamps before the grid wait
+
+// Small path: the k_fwd_T blocks of the (table, i2) groups read only the touched flags
+// of the decode kernel just before them, not its histograms.  They wait for every decode
+// block's epoch stamp (bounded polls; then the whole-grid wait) instead of the grid's end.
+__device__ __forceinline__ void wait_decode_flags(const Params& P) {
+    const int epoch = *P.epoch;
+    bool ok = false;
+    for (int it = 0; it < kDecodeFlagPolls && !ok; ++it) {
+        const bool mine = (int)threadIdx.x >= P.nch || *(volatile const int*)(P.dec_done + threadIdx.x) == epoch;
+        ok = __syncthreads_and(mine);
+        if (!ok) __nanosleep(64);
+    }
+    if (!ok) pdl_wait();
+    __threadfence();
 }
 
 __device__ __forceinline__ unsigned lanemask_lt() {

@@ -422,6 +422,12 @@ __global__ void __launch_bounds__(kSmallChunk) k_decode_small(const __grid_const
             d[2] = T.base3 + i3;
         }
     }
+    // the touched flags of this block's lookups are stored: stamp the pass's epoch for the
+    // k_fwd_T blocks waiting on them
+    static_assert(kScanChunkMax <= kDecDoneSlots, "a decode stamp per block");
+    __threadfence();
+    __syncthreads();
+    if (threadIdx.x == 0) atomicExch(P.dec_done + c, epoch);
     const int lane = threadIdx.x & 31, w = threadIdx.x >> 5;
     const int nbs[3] = {P.n1, P.n2, P.n3};
     int* Hs[3] = {P.H1, P.H2, P.H3};
