@@ -328,6 +328,10 @@ __device__ void tile_bwd_tc_body(const Params& P, const TableDev& T, unsigned ch
     if (threadIdx.x == 0) TT_DCHECK(P, i2, T.p2);
     __syncthreads();
 #endif
+    // every lookup's gradient row: loads in flight during the scans and the G2 staging
+    static_assert(kTcBwdCap * 16 <= 4 * kTcBwdThreads, "gradient rows of a tile: four float4 a thread");
+    GsLoads gl;
+    tile_gs_issue(P, len, sbag, ss, D, gl);
     const int k = threadIdx.x;
     int fr = 0, fp = 0;
     if (k < len) {
@@ -355,6 +359,20 @@ __device__ void tile_bwd_tc_body(const Params& P, const TableDev& T, unsigned ch
 
     __syncthreads();  // rowbeg / pairbeg complete
     stage_g3<R>(T, rowbeg, si3, g3s, 0, nrows);  // the first batch's G3 slices
+    // G1 item of this thread (row a, eight K positions (pair, j1)); the next batch's values
+    // are loaded while the MMAs of the current one run
+    const bool g1item = (int)threadIdx.x < R * (KR / 8);
+    const int g1a = (threadIdx.x & 7) + 8 * (threadIdx.x / (8 * (KR / 8))), g1k8 = (threadIdx.x >> 3) % (KR / 8);
+    float g1v[8];
+    auto load_g1 = [&](int ub) {
+        const int nbb = min(kTcBwdPairs, npairs - ub);
+#pragma unroll
+        for (int i = 0; i < 8; ++i) {
+            const int u = 2 * g1k8 + (i >> 2), j1 = i & 3;
+            g1v[i] = (g1item && u < nbb) ? __ldg(T.G1 + (int64_t)si1[pairbeg[ub + u]] * (4 * R) + j1 * R + g1a) : 0.f;
+        }
+    };
+    load_g1(0);
     // ---- G2 as the B operand of Q: rows a, K = jc, three pieces (from the bulk copy)
     if (threadIdx.x == 0 && !mbar_wait(gbar, 0, P.wait_polls)) {
         atomicOr(P.err, kErrTimeout);
@@ -372,7 +390,7 @@ __device__ void tile_bwd_tc_body(const Params& P, const TableDev& T, unsigned ch
     __syncthreads();  // rowid / pairid / rowbeg / pairbeg complete
 
     // ---- gs: summed upstream gradient of every tile-row
-    tile_gs(P, len, nrows, sbag, ss, rowbeg, gs, D);
+    tile_gs_rows(gl, len, nrows, rowbeg, gs, D);
 
     // ---- batches of kTcBwdPairs pairs: dT and the G1 rows as pieces, then the MMAs
     constexpr uint32_t kIdescQ3 = tc_idesc_bf16(64, 3 * R, 0), kIdescQ2 = tc_idesc_bf16(64, 2 * R, 0),
@@ -381,20 +399,6 @@ __device__ void tile_bwd_tc_body(const Params& P, const TableDev& T, unsigned ch
                        kIdescG1 = tc_idesc_bf16(N2, R, 1);
     constexpr uint32_t DTS = L::dts;
     const uint32_t tq1 = *tslot, tq2 = *tslot + tc_cols_q2(R), tg = *tslot + tc_cols_g(R);
-    // G1 item of this thread (row a, eight K positions (pair, j1)); the next batch's values
-    // are loaded while the MMAs of the current one run
-    const bool g1item = (int)threadIdx.x < R * (KR / 8);
-    const int g1a = (threadIdx.x & 7) + 8 * (threadIdx.x / (8 * (KR / 8))), g1k8 = (threadIdx.x >> 3) % (KR / 8);
-    float g1v[8];
-    auto load_g1 = [&](int ub) {
-        const int nbb = min(kTcBwdPairs, npairs - ub);
-#pragma unroll
-        for (int i = 0; i < 8; ++i) {
-            const int u = 2 * g1k8 + (i >> 2), j1 = i & 3;
-            g1v[i] = (g1item && u < nbb) ? __ldg(T.G1 + (int64_t)si1[pairbeg[ub + u]] * (4 * R) + j1 * R + g1a) : 0.f;
-        }
-    };
-    load_g1(0);
     bool failed = false;
     int nbatch = 0;
     for (int u0 = 0; u0 < npairs; u0 += kTcBwdPairs, ++nbatch) {

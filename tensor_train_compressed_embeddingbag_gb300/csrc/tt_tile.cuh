@@ -103,4 +103,54 @@ __device__ __forceinline__ void tile_gs(const Params& P, int len, int nrows, con
     __syncthreads();
 }
 
+// tile_gs in two halves for tiles whose len D / 4 float4 items fit four a thread: the
+// loads of every lookup's gradient row are issued early (right after the tile sort) and
+// land while the block does other work; tile_gs_rows then stores and sums them.
+struct GsLoads {
+    float4 x[4];
+    float sc[4];
+};
+__device__ __forceinline__ void tile_gs_issue(const Params& P, int len, const int* sbag, const float* ss, int D,
+                                              GsLoads& g) {
+    const int D4 = D >> 2, n1 = len * D4;
+#pragma unroll
+    for (int u = 0; u < 4; ++u) {
+        const int e = threadIdx.x + u * blockDim.x;
+        g.x[u] = make_float4(0.f, 0.f, 0.f, 0.f);
+        g.sc[u] = 0.f;
+        if (e < n1) {
+            const int k = e / D4, q = e - k * D4;
+            g.sc[u] = ss[k];
+            g.x[u] = __ldg(reinterpret_cast<const float4*>(P.grad_out + (int64_t)sbag[k] * D) + q);
+        }
+    }
+}
+__device__ __forceinline__ void tile_gs_rows(const GsLoads& g, int len, int nrows, const int* rowbeg, float* gs, int D) {
+    const int D4 = D >> 2, n1 = len * D4;
+    float4* g4 = reinterpret_cast<float4*>(gs);
+#pragma unroll
+    for (int u = 0; u < 4; ++u) {
+        const int e = threadIdx.x + u * blockDim.x;
+        if (e < n1) g4[e] = make_float4(g.sc[u] * g.x[u].x, g.sc[u] * g.x[u].y, g.sc[u] * g.x[u].z, g.sc[u] * g.x[u].w);
+    }
+    __syncthreads();
+    const int n2 = nrows * D4;
+    for (int base = 0; base < n2; base += blockDim.x) {  // uniform trip count
+        const int e = base + threadIdx.x;
+        float4 a = make_float4(0.f, 0.f, 0.f, 0.f);
+        if (e < n2) {
+            const int row = e / D4, q = e - row * D4;
+            const int kb = rowbeg[row], ke = rowbeg[row + 1];
+            a = g4[kb * D4 + q];
+            for (int k = kb + 1; k < ke; ++k) {
+                const float4 y = g4[k * D4 + q];
+                a.x += y.x; a.y += y.y; a.z += y.z; a.w += y.w;
+            }
+        }
+        __syncthreads();
+        if (e < n2) g4[e] = a;
+    }
+    __syncthreads();
+}
+
 }  // namespace ttemb
