@@ -689,14 +689,22 @@ __device__ void tile_bwd_body(const Params& P, const TableDev& T, const Dm dm, u
         if (sh[42]) {
             __threadfence();
             const int first = P.grp_first[g];
-            for (int e = threadIdx.x; e < r1 * Ns; e += blockDim.x) {
-                float sum = 0.f;
-                for (int tt = 0; tt < nt; ++tt)
-                    sum += __ldcg(P.dG2part + ((int64_t)(first + tt) * SPLIT + sp) * P.s2_max + e);
-                const int a = e / Ns, jc = e - a * Ns;
-                const int j2 = jc / r2s, c = c0 + (jc - j2 * r2s);
-                const int ga = (a * q2 + j2) * r2 + c;
-                core_update(P, G2p, A2p, ga, sum);
+            for (int e0 = threadIdx.x; e0 < r1 * Ns; e0 += 4 * blockDim.x) {  // four elements a round
+                int ee[4], gidx[4];
+                float sum[4];
+#pragma unroll
+                for (int u = 0; u < 4; ++u) {
+                    const int e = e0 + u * blockDim.x;
+                    ee[u] = e < r1 * Ns ? e : -1;
+                    gidx[u] = -1;
+                    if (e < r1 * Ns) {
+                        const int a = e / Ns, jc = e - a * Ns;
+                        const int j2 = jc / r2s, c = c0 + (jc - j2 * r2s);
+                        gidx[u] = (a * q2 + j2) * r2 + c;
+                    }
+                }
+                sum_partials<4>(P.dG2part + ((int64_t)first * SPLIT + sp) * P.s2_max, (int64_t)SPLIT * P.s2_max, nt, ee, sum);
+                core_update_nm<4>(P, G2p, A2p, gidx, sum);  // then the four updates' loads together
             }
             if (threadIdx.x == 0) {
                 P.grp_done[g * SPLIT + sp] = 0;

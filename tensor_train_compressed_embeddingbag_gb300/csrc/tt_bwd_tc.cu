@@ -557,8 +557,11 @@ __device__ void tile_bwd_tc_body(const Params& P, const TableDev& T, unsigned ch
             const uint32_t cg[3] = {tg + c0, tg + R + c0, tg + 2 * R + c0};
             tc_sumx16<3>((uint32_t)(32 * w) << 16, cg, gv, ge);
             if (live) {
-                if (nt == 1) {
-                    for (int a = 0; a < 16; ++a) core_update(P, G2p, A2p, (int64_t)(c0 + a) * N2 + jc, gv[a]);
+                if (nt == 1) {  // sixteen loads in flight, then the stores
+                    int idx[16];
+#pragma unroll
+                    for (int a = 0; a < 16; ++a) idx[a] = (c0 + a) * N2 + jc;
+                    core_update_n<16>(P, G2p, A2p, idx, gv);
                 } else {
 #pragma unroll
                     for (int a = 0; a < 16; ++a) part[(c0 + a) * N2 + jc] = gv[a];
@@ -580,10 +583,13 @@ __device__ void tile_bwd_tc_body(const Params& P, const TableDev& T, unsigned ch
         if (sh[42]) {  // the group's last tile sums the dG2 partials in tile order
             __threadfence();
             const int first = P.grp_first[g];
-            for (int e = threadIdx.x; e < R * N2; e += kTcBwdThreads) {
-                float sum = 0.f;
-                for (int tt = 0; tt < nt; ++tt) sum += __ldcg(P.dG2part + (int64_t)(first + tt) * P.s2_max + e);
-                core_update(P, G2p, A2p, e, sum);
+            for (int e0 = threadIdx.x; e0 < R * N2; e0 += 8 * kTcBwdThreads) {  // eight elements a round
+                int idx[8];
+                float sum[8];
+#pragma unroll
+                for (int u = 0; u < 8; ++u) idx[u] = e0 + u * kTcBwdThreads < R * N2 ? e0 + u * kTcBwdThreads : -1;
+                sum_partials<8>(P.dG2part + (int64_t)first * P.s2_max, P.s2_max, nt, idx, sum);
+                core_update_nm<8>(P, G2p, A2p, idx, sum);  // then the eight updates' loads together
             }
             if (threadIdx.x == 0) {
                 P.grp_done[g] = 0;

@@ -259,6 +259,58 @@ __device__ __forceinline__ void core_update_n(const Params& P, float* G, float* 
     }
 }
 
+// sum[u] = the sum over tiles tt < nt, in tile order, of part[tt * stride + e[u]] for NE
+// elements (e[u] < 0: none); four tiles' loads of every element in flight at once.
+template <int NE>
+__device__ __forceinline__ void sum_partials(const float* part, int64_t stride, int nt, const int* e, float* sum) {
+#pragma unroll
+    for (int u = 0; u < NE; ++u) sum[u] = 0.f;
+    int tt = 0;
+    for (; tt + 4 <= nt; tt += 4) {
+        float x[NE][4];
+#pragma unroll
+        for (int u = 0; u < NE; ++u)
+#pragma unroll
+            for (int k = 0; k < 4; ++k) x[u][k] = e[u] >= 0 ? __ldcg(part + (int64_t)(tt + k) * stride + e[u]) : 0.f;
+#pragma unroll
+        for (int u = 0; u < NE; ++u)
+#pragma unroll
+            for (int k = 0; k < 4; ++k) sum[u] += x[u][k];
+    }
+    for (; tt < nt; ++tt)
+#pragma unroll
+        for (int u = 0; u < NE; ++u)
+            if (e[u] >= 0) sum[u] += __ldcg(part + (int64_t)tt * stride + e[u]);
+}
+
+// core_update_n where idx[i] < 0 marks an unused slot.
+template <int N>
+__device__ __forceinline__ void core_update_nm(const Params& P, float* G, float* aux, const int* idx, const float* g) {
+    if (P.opt == TT_OPT_GRAD) {
+#pragma unroll
+        for (int i = 0; i < N; ++i)
+            if (idx[i] >= 0) aux[idx[i]] = g[i];
+        return;
+    }
+    float w[N], st[N];
+#pragma unroll
+    for (int i = 0; i < N; ++i) w[i] = idx[i] >= 0 ? G[idx[i]] : 0.f;
+    if (P.opt == TT_OPT_ADAGRAD) {
+#pragma unroll
+        for (int i = 0; i < N; ++i) st[i] = idx[i] >= 0 ? fmaf(g[i], g[i], aux[idx[i]]) : 0.f;
+#pragma unroll
+        for (int i = 0; i < N; ++i) {
+            if (idx[i] < 0) continue;
+            aux[idx[i]] = st[i];
+            G[idx[i]] = w[i] - P.lr * g[i] / (sqrtf(st[i]) + P.eps);
+        }
+    } else {
+#pragma unroll
+        for (int i = 0; i < N; ++i)
+            if (idx[i] >= 0) G[idx[i]] = fmaf(-P.lr, g[i], w[i]);
+    }
+}
+
 __device__ __forceinline__ void pdl_launch_dependents() { asm volatile("griddepcontrol.launch_dependents;" ::: "memory"); }
 __device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
 __device__ __forceinline__ void pdl_entry() {
