@@ -144,6 +144,7 @@ size_t carve(tt_emb* h, void* base, int64_t nnz, bool assign) {
     float* g_s = A.take<float>(N);
     int* sigma = A.take<int>(N);
     int4* tiles = A.take<int4>(max_tiles);
+    int* tile_order = A.take<int>(max_tiles);
     int* grp_first = A.take<int>(P.n2);
     int* grp_ntiles = A.take<int>(P.n2);
     int* rep1 = A.take<int>(N);
@@ -162,7 +163,7 @@ size_t carve(tt_emb* h, void* base, int64_t nnz, bool assign) {
         P.H1 = H1; P.H3 = H3; P.H2 = H2;
         P.pi1 = pi1; P.pi3 = pi3; P.pi21 = pi21; P.sigma = sigma;
         P.g_i1 = g_i1; P.g_i3 = g_i3; P.g_bag = g_bag; P.g_s = g_s;
-        P.tiles = tiles; P.grp_first = grp_first; P.grp_ntiles = grp_ntiles;
+        P.tiles = tiles; P.tile_order = tile_order; P.grp_first = grp_first; P.grp_ntiles = grp_ntiles;
         P.rep1 = rep1; P.rep3 = rep3; P.g_p1 = g_p1; P.g_p3 = g_p3; P.inv3 = inv3; P.segsum = segsum;
         P.Qbuf = Qbuf; P.Pbuf = Pbuf; P.dG2part = dG2part;
     }

@@ -604,8 +604,8 @@ template <int DC>
 __global__ void __launch_bounds__(kTcBwdThreads, 2) k_tile_bwd_tc(const __grid_constant__ Params P) {
     pdl_entry();
     if (*P.err) return;  // a device error was recorded: leave every core unchanged
-    const int tile = blockIdx.x;
-    if (tile >= *P.ntiles) return;
+    if ((int)blockIdx.x >= *P.ntiles) return;
+    const int tile = P.small ? P.tile_order[blockIdx.x] : (int)blockIdx.x;  // longest tiles first
     extern __shared__ __align__(128) unsigned char smraw[];
     // tensor memory first, and the allocation permit released at once
     if (threadIdx.x < 32) tc_alloc(reinterpret_cast<uint32_t*>(smraw + 8), kTcBwdCols);
@@ -621,6 +621,7 @@ __global__ void __launch_bounds__(kTcBwdThreads, 2) k_tile_bwd_tc(const __grid_c
 
 bool bwd_tc_eligible(int dclass_all) { return bwd_tc_class(dclass_all); }
 int bwd_tc_cap() { return kTcBwdCap; }
+static_assert(kTcBwdCap <= kMaxTcTileCap, "the tile order's length buckets");
 
 static size_t tc_smem(int dclass) { return dclass == kQ444R32 ? TcBwdLayout<32>::total : TcBwdLayout<16>::total; }
 

@@ -158,6 +158,8 @@ struct Params {
     int* inv3;                      // [nnz] position of lookup n in pi3 (multi-CTA grouping)
     int* sigma;
     int4* tiles;                    // {start, len, group bin, tile index in group}
+    int* tile_order;                // small path with the tensor-core backward: tile ids in launch
+                                    // order, longest first (else the identity)
     int* tflag;                     // dense touched-pair flags, == *epoch when touched by this call
     int* epoch;                     // device counter: advanced by k_pool at the end of every forward pass
     int* ntiles;
@@ -572,6 +574,7 @@ __device__ __forceinline__ void scatter_chunk(const Params& P, int c, int part) 
 // block scans the bin totals, the thread rewrites its row as running prefixes,
 // and the rows go back with coalesced stores.  The i2 block then cuts every
 // (table, i2) group into tiles of <= tile_cap lookups.  sm: kScanSmemInts ints.
+constexpr int kMaxTcTileCap = 64;  // the tensor-core backward's tile cap
 constexpr int kScanChunkMax = 48;  // >= kSmallMaxNnz / kSmallChunk
 constexpr int kScanBlock = 256;    // threads of the scanning block
 constexpr int kScanSmemInts = 64 + kScanBlock * kScanChunkMax;
@@ -635,6 +638,27 @@ __device__ __forceinline__ void scan_digit_block(const Params& P, int k, int* sm
         __syncthreads();  // the next round reuses hs
     }
     if (k == 1 && threadIdx.x == 0) *P.ntiles = tcarry;
+    if (k == 1 && P.bwd_tc) {
+        // launch order of the tensor-core backward's tiles: longest first (a counting sort
+        // by length; the order within a length does not matter), so that the longest
+        // tiles are placed first, one to an SM
+        static_assert(kMaxTcTileCap + 1 <= kScanBlock, "a tile length per thread");
+        __syncthreads();
+        int* bucket = hs;  // [tile_cap + 1], the histogram rows are written back
+        const int cap = P.tile_cap;
+        for (int b = threadIdx.x; b <= cap; b += kScanBlock) bucket[b] = 0;
+        __syncthreads();
+        for (int i = threadIdx.x; i < tcarry; i += kScanBlock) atomicAdd(&bucket[__ldcg(&P.tiles[i].y)], 1);
+        __syncthreads();
+        const int len = cap - (int)threadIdx.x;  // thread t: length cap - t
+        const int cnt = len >= 0 ? bucket[len] : 0;
+        int total;
+        const int pos0 = block_scan_excl(cnt, sh, &total);
+        __syncthreads();
+        if (len >= 0) bucket[len] = pos0;
+        __syncthreads();
+        for (int i = threadIdx.x; i < tcarry; i += kScanBlock) P.tile_order[atomicAdd(&bucket[__ldcg(&P.tiles[i].y)], 1)] = i;
+    }
     if (k == 0 && threadIdx.x == 0) *P.nincl = carry;
 }
 
