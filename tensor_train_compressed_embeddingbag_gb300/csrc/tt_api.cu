@@ -45,7 +45,7 @@ struct tt_emb {
     std::vector<TableDev> tabs;  // host copy
     TableDev* d_tables = nullptr;
     int* d_bins = nullptr;       // bin -> table for the three digits
-    int* d_fixed = nullptr;      // err, (spare x2), ntiles, epoch, dstep, nincl, scan_done, grp_done[2 n2], dec_done
+    int* d_fixed = nullptr;      // err, (spare x2), ntiles, epoch, dstep, nincl, scan_done, grp_done[2 n2], dec_done, multi_count
     float* d_tbuf = nullptr;
     int64_t tbuf_floats = 0;
     int* d_tflag = nullptr;      // dense touched-pair flags
@@ -147,6 +147,7 @@ size_t carve(tt_emb* h, void* base, int64_t nnz, bool assign) {
     int* tile_order = A.take<int>(max_tiles);
     int* grp_first = A.take<int>(P.n2);
     int* grp_ntiles = A.take<int>(P.n2);
+    int* multi_groups = A.take<int>(P.n2);
     int* rep1 = A.take<int>(N);
     int* rep3 = A.take<int>(N);
     int* g_p1 = A.take<int>(N);
@@ -164,6 +165,7 @@ size_t carve(tt_emb* h, void* base, int64_t nnz, bool assign) {
         P.pi1 = pi1; P.pi3 = pi3; P.pi21 = pi21; P.sigma = sigma;
         P.g_i1 = g_i1; P.g_i3 = g_i3; P.g_bag = g_bag; P.g_s = g_s;
         P.tiles = tiles; P.tile_order = tile_order; P.grp_first = grp_first; P.grp_ntiles = grp_ntiles;
+        P.multi_groups = multi_groups;
         P.rep1 = rep1; P.rep3 = rep3; P.g_p1 = g_p1; P.g_p3 = g_p3; P.inv3 = inv3; P.segsum = segsum;
         P.Qbuf = Qbuf; P.Pbuf = Pbuf; P.dG2part = dG2part;
     }
@@ -334,7 +336,7 @@ tt_status build_handle(tt_emb* h, int ntab, const tt_table_desc* d) {
     }
     if (cudaMalloc(&h->d_tables, sizeof(TableDev) * ntab) != cudaSuccess) return TT_ERR_NOMEM;
     if (cudaMalloc(&h->d_bins, sizeof(int) * bins.size()) != cudaSuccess) return TT_ERR_NOMEM;
-    const int nfixed = 8 + 2 * n2 + kDecDoneSlots;
+    const int nfixed = 8 + 2 * n2 + kDecDoneSlots + 1;
     if (cudaMalloc(&h->d_fixed, sizeof(int) * nfixed) != cudaSuccess) return TT_ERR_NOMEM;
     if (cudaMalloc(&h->d_tbuf, sizeof(float) * std::max<int64_t>(tb, 1)) != cudaSuccess) return TT_ERR_NOMEM;
     if (cudaMalloc(&h->d_tflag, sizeof(int) * std::max<int64_t>(fb, 1)) != cudaSuccess) return TT_ERR_NOMEM;
@@ -363,6 +365,7 @@ tt_status build_handle(tt_emb* h, int ntab, const tt_table_desc* d) {
     P.scan_done = h->d_fixed + 7;
     P.grp_done = h->d_fixed + 8;
     P.dec_done = h->d_fixed + 8 + 2 * n2;
+    P.multi_count = h->d_fixed + 8 + 2 * n2 + kDecDoneSlots;
     P.Tbuf = h->d_tbuf;
     P.tflag = h->d_tflag;
     return TT_OK;

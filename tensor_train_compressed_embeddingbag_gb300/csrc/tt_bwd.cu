@@ -678,40 +678,8 @@ __device__ void tile_bwd_body(const Params& P, const TableDev& T, const Dm dm, u
         if (nt == 1 && P.slice_stamp && P.opt != TT_OPT_GRAD && threadIdx.x == 0 && t == 0) P.slice_stamp[T.p1 + i2] = *P.dstep + 1;
     }
 
-    // every partial of this block is written: publish them before any arrival count
-    __threadfence();
-    __syncthreads();
-    // several tiles in the group: the last one (per split) sums the dG2 partials in tile order
-    const int nt = P.grp_ntiles[g];
-    if (nt > 1) {
-        if (threadIdx.x == 0) sh[42] = (atomicAdd(&P.grp_done[g * SPLIT + sp], 1) == nt - 1);
-        __syncthreads();
-        if (sh[42]) {
-            __threadfence();
-            const int first = P.grp_first[g];
-            for (int e0 = threadIdx.x; e0 < r1 * Ns; e0 += 4 * blockDim.x) {  // four elements a round
-                int ee[4], gidx[4];
-                float sum[4];
-#pragma unroll
-                for (int u = 0; u < 4; ++u) {
-                    const int e = e0 + u * blockDim.x;
-                    ee[u] = e < r1 * Ns ? e : -1;
-                    gidx[u] = -1;
-                    if (e < r1 * Ns) {
-                        const int a = e / Ns, jc = e - a * Ns;
-                        const int j2 = jc / r2s, c = c0 + (jc - j2 * r2s);
-                        gidx[u] = (a * q2 + j2) * r2 + c;
-                    }
-                }
-                sum_partials<4>(P.dG2part + ((int64_t)first * SPLIT + sp) * P.s2_max, (int64_t)SPLIT * P.s2_max, nt, ee, sum);
-                core_update_nm<4>(P, G2p, A2p, gidx, sum);  // then the four updates' loads together
-            }
-            if (threadIdx.x == 0) {
-                P.grp_done[g * SPLIT + sp] = 0;
-                if (P.slice_stamp && P.opt != TT_OPT_GRAD && t == 0) P.slice_stamp[T.p1 + i2] = *P.dstep + 1;
-            }
-        }
-    }
+    // a group of several tiles: k_reduce13 sums its dG2 partials in tile order (a block
+    // per group and column half, so that a hot group's sum is not one tile's tail)
 }
 
 // Column-split kernels: three blocks per SM for the rank-16/32 classes (registers capped at 80), two otherwise.
@@ -734,13 +702,62 @@ __global__ void __launch_bounds__(kBwdThreads, SPLIT == 2 ? ((DC == kQ444R32 || 
 
 // Three blocks per SM (the slice count of the workloads fits one wave); without a minimum
 // the register target is so low that the partial loads of a thread no longer overlap.
+// FFMA backward: dG2 of the (table, i2) groups of several tiles, as work items of
+// kGrpChunk elements (group, column half, chunk): the sum of the group's per-tile
+// partials in tile order, then the update.  k_reduce13's first blocks (before those of
+// the G1 / G3 slices) take the items in turn, so that a hot group (thousands of tiles)
+// is spread over many blocks.
+constexpr int kGrpChunk = 4 * kBwdThreads;
+__device__ void reduce_group_items(const Params& P, int b0, int nblocks) {
+    const int SPLIT = P.split;
+    const int chunks = (P.s2_max / SPLIT + kGrpChunk - 1) / kGrpChunk;
+    const int items = *P.multi_count * SPLIT * chunks;
+    for (int item = b0; item < items; item += nblocks) {
+        const int gi = item / (SPLIT * chunks), rem = item - gi * (SPLIT * chunks);
+        const int sp = rem / chunks, ch = rem - sp * chunks;
+        const int g = P.multi_groups[gi];
+        const int nt = P.grp_ntiles[g];
+        const int t = P.ntab == 1 ? 0 : P.bin2_tab[g];
+        const TableDev& T = P.tables[t];
+        const int i2 = g - T.base2;
+        const int r1 = T.r1, q2 = T.q2, r2 = T.r2;
+        const int r2s = r2 / SPLIT, c0 = sp * r2s, Ns = q2 * r2s, n = r1 * Ns;
+        float* G2p = T.G2 + (int64_t)i2 * r1 * q2 * r2;
+        float* A2p = T.aux[1] ? T.aux[1] + (int64_t)i2 * r1 * q2 * r2 : nullptr;
+        int ee[4], gidx[4];
+        float sum[4];
+#pragma unroll
+        for (int u = 0; u < 4; ++u) {
+            const int e = ch * kGrpChunk + u * blockDim.x + threadIdx.x;
+            ee[u] = e < n ? e : -1;
+            gidx[u] = -1;
+            if (e < n) {
+                const int a = e / Ns, jc = e - a * Ns;
+                const int j2 = jc / r2s, c = c0 + (jc - j2 * r2s);
+                gidx[u] = (a * q2 + j2) * r2 + c;
+            }
+        }
+        sum_partials<4>(P.dG2part + ((int64_t)P.grp_first[g] * SPLIT + sp) * P.s2_max, (int64_t)SPLIT * P.s2_max, nt, ee,
+                        sum);
+        core_update_nm<4>(P, G2p, A2p, gidx, sum);  // then the four updates' loads together
+        if (sp == 0 && ch == 0 && threadIdx.x == 0 && P.slice_stamp && P.opt != TT_OPT_GRAD && t == 0)
+            P.slice_stamp[T.p1 + i2] = *P.dstep + 1;
+    }
+}
+
 __global__ void __launch_bounds__(kBwdThreads, 3) k_reduce13(const __grid_constant__ Params P) {
     pdl_entry();
     if (*P.err) return;  // a device error was recorded: leave every core unchanged
     __shared__ int slots[kReduceSlots];
     __shared__ int sh[40];
     extern __shared__ float sacc[];
-    const int b = blockIdx.x;
+    // the group blocks come first, so that they run beside the slice blocks
+    const int ngb = (int)gridDim.x - (P.n1 + P.n3);
+    if ((int)blockIdx.x < ngb) {
+        reduce_group_items(P, blockIdx.x, ngb);
+        return;
+    }
+    const int b = blockIdx.x - ngb;
     const int nb = b < P.n1 ? P.n1 : P.n3;
     const int bb = b < P.n1 ? b : b - P.n1;
     const int* H = b < P.n1 ? P.H1 : P.H3;
@@ -875,7 +892,9 @@ static cudaError_t set_tile_attrs(int max_smem) {
 cudaError_t launch_reduce13(const Params& P, cudaStream_t s) {
     // per-group sums: R S <= 4 kBwdThreads floats while one group's columns fit the block, else S
     const size_t smem = sizeof(float) * std::max<size_t>(4 * kBwdThreads, (size_t)std::max(P.qs_max, P.ps_max));
-    cudaError_t le = launch_pdl(k_reduce13, dim3(P.n1 + P.n3), dim3(kBwdThreads), smem, s, P);
+    // the FFMA backward leaves the dG2 sums of its multi-tile groups to blocks of this launch
+    const int groups = P.bwd_tc ? 0 : 2 * P.sms;
+    cudaError_t le = launch_pdl(k_reduce13, dim3(P.n1 + P.n3 + groups), dim3(kBwdThreads), smem, s, P);
     if (le != cudaSuccess) return le;
     return cudaGetLastError();
 }

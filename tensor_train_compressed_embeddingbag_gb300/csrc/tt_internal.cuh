@@ -166,6 +166,8 @@ struct Params {
     int* grp_first;                 // [n2]
     int* grp_ntiles;                // [n2]
     int* grp_done;                  // [n2], zero between calls
+    int* multi_groups;              // [n2]: the (table, i2) groups of several tiles, in group order
+    int* multi_count;               // their number (written by the tile cut)
     int* dec_done;                  // [kDecDoneSlots]: small-path decode block c stores the pass's
                                     // epoch once the touched flags of its lookups are written
     float* Tbuf;
@@ -584,7 +586,7 @@ __device__ __forceinline__ void scan_digit_block(const Params& P, int k, int* sm
     const int nb = k == 0 ? P.n1 : (k == 1 ? P.n2 : P.n3);
     int* H = k == 0 ? P.H1 : (k == 1 ? P.H2 : P.H3);
     const int nch = P.nch;  // <= kScanChunkMax on this path
-    int carry = 0, tcarry = 0;
+    int carry = 0, tcarry = 0, mcarry = 0;
     for (int b0 = 0; b0 < nb; b0 += kScanBlock) {
         const int nbr = min(kScanBlock, nb - b0);
         const int n = nbr * nch, n4 = n >> 2;
@@ -622,22 +624,29 @@ __device__ __forceinline__ void scan_digit_block(const Params& P, int k, int* sm
         if (k == 1) {  // tiles of the (table, i2) groups of this round of bins
             const int cap = P.tile_cap;
             const int nt = bl < nbr ? (tot + cap - 1) / cap : 0;
-            int ttot;
+            int ttot, mtot;
             const int first = tcarry + block_scan_excl(nt, sh, &ttot);
+            __syncthreads();
+            const int mpos = mcarry + block_scan_excl(nt > 1 ? 1 : 0, sh, &mtot);
             if (bl < nbr) {
                 P.grp_first[b] = first;
                 P.grp_ntiles[b] = nt;
                 for (int t = 0; t < nt; ++t)
                     P.tiles[first + t] = make_int4(start + t * cap, min(cap, tot - t * cap), b, t);
+                if (nt > 1) P.multi_groups[mpos] = b;
             }
             tcarry += ttot;
+            mcarry += mtot;
         }
         __syncthreads();
         for (int e = threadIdx.x; e < n4; e += kScanBlock) reinterpret_cast<int4*>(src)[e] = reinterpret_cast<const int4*>(hs)[e];
         for (int e = 4 * n4 + threadIdx.x; e < n; e += kScanBlock) src[e] = hs[e];
         __syncthreads();  // the next round reuses hs
     }
-    if (k == 1 && threadIdx.x == 0) *P.ntiles = tcarry;
+    if (k == 1 && threadIdx.x == 0) {
+        *P.ntiles = tcarry;
+        *P.multi_count = mcarry;
+    }
     if (k == 1 && P.bwd_tc) {
         // launch order of the tensor-core backward's tiles: longest first (a counting sort
         // by length; the order within a length does not matter), so that the longest

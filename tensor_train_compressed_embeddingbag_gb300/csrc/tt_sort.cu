@@ -255,7 +255,7 @@ __global__ void __launch_bounds__(kScanThreads) k_scan_apply(const __grid_consta
     __syncthreads();
     if (!last) return;
     __threadfence();
-    int carry = 0;
+    int carry = 0, mcarry = 0;
     for (int gb = 0; gb < P.n2; gb += blockDim.x) {
         const int g = gb + threadIdx.x;
         int start = 0, cnt = 0, nt = 0;
@@ -265,19 +265,24 @@ __global__ void __launch_bounds__(kScanThreads) k_scan_apply(const __grid_consta
             cnt = e - start;
             nt = (cnt + P.tile_cap - 1) / P.tile_cap;
         }
-        int total;
+        int total, mtot;
         const int first = carry + block_scan_excl(nt, sh, &total);
+        __syncthreads();
+        const int mpos = mcarry + block_scan_excl(nt > 1 ? 1 : 0, sh, &mtot);
         if (g < P.n2) {
             P.grp_first[g] = first;
             P.grp_ntiles[g] = nt;
             for (int k = 0; k < nt; ++k)
                 P.tiles[first + k] = make_int4(start + k * P.tile_cap, min(P.tile_cap, cnt - k * P.tile_cap), g, k);
+            if (nt > 1) P.multi_groups[mpos] = g;
         }
         carry += total;
+        mcarry += mtot;
         __syncthreads();
     }
     if (threadIdx.x == 0) {
         *P.ntiles = carry;
+        *P.multi_count = mcarry;
         *P.scan_done = 0;  // ready for the next pass
     }
 }
