@@ -106,17 +106,25 @@ def flops_per_lookup(spec):
     return A, Bc
 
 
+def touched_pairs(wl):
+    """Distinct (i1, i2) pairs of every table's lookups (i1 p2 + i2 = row div p3)."""
+    out = []
+    for t, spec in enumerate(wl.tables):
+        lo, hi = int(wl.offsets[t * wl.batch]), int(wl.offsets[(t + 1) * wl.batch])
+        rows = np.asarray(wl.indices[lo:hi], dtype=np.int64)
+        out.append(np.unique(rows // int(spec.p[2])).shape[0] if rows.size else 0)
+    return out
+
+
 def dedup_step_flops(wl):
     """Step FLOPs with the contractions shared per touched (table, i1, i2) pair, as the
     kernels do them: 6 A per pair (T = G1 G2 forward; Q and dG2 backward) plus 6 Bc
     per lookup (T G3 forward; dT and the dG3 partial backward)."""
     total = 0
-    for t, spec in enumerate(wl.tables):
-        lo, hi = int(wl.offsets[t * wl.batch]), int(wl.offsets[(t + 1) * wl.batch])
-        rows = np.asarray(wl.indices[lo:hi], dtype=np.int64)
-        pairs = np.unique(rows // int(spec.p[2])).shape[0] if rows.size else 0  # (i1, i2) = row div p3
+    for spec, pairs, t in zip(wl.tables, touched_pairs(wl), range(len(wl.tables))):
+        n = int(wl.offsets[(t + 1) * wl.batch] - wl.offsets[t * wl.batch])
         A, Bc = flops_per_lookup(spec)
-        total += 6 * A * pairs + 6 * Bc * rows.shape[0]
+        total += 6 * A * pairs + 6 * Bc * n
     return total
 
 
@@ -139,10 +147,11 @@ def tc_class(spec):
     return list(spec.q) == [4, 4, 4] and spec.ranks[0] == spec.ranks[1] and spec.ranks[0] in (16, 32)
 
 
-def kernel_parts(wl):
+def kernel_parts(wl, pairs=None):
     """Per kernel: [(algorithmic FLOPs per launch, pipe)] with the per-lookup counts of
     the path (A = q1 r1 q2 r2, Bc = q1 q2 r2 q3 per lookup): T = G1 G2 2A; row = T G3
-    2Bc; backward dT and the dG3 partial 4Bc, the dG1 partial and dG2 4A."""
+    2Bc; backward dT and the dG3 partial 4Bc, the dG1 partial and dG2 4A.  With `pairs`
+    (touched (i1, i2) pairs per table) the A terms count once per pair, as done."""
     out = {"fwd_T": [], "pool": [], "tile_bwd": []}
     acc = {}
     classes = {(tuple(s.q), tuple(s.ranks)) for s in wl.tables}
@@ -150,6 +159,8 @@ def kernel_parts(wl):
     for t, spec in enumerate(wl.tables):
         n = int(wl.offsets[(t + 1) * wl.batch] - wl.offsets[t * wl.batch])
         A, Bc = flops_per_lookup(spec)
+        if pairs is not None:
+            A = A * pairs[t] / max(n, 1)  # A per lookup, averaged over the shared pairs
         tc = tc_class(spec)
         for k, f, pp in (("fwd_T", 2 * A * n, "tensor" if tc else "fp32"), ("pool", 2 * Bc * n, "fp32"),
                          ("tile_bwd", 4 * A * n, "tensor" if bwd_tc else "fp32"), ("tile_bwd", 4 * Bc * n, "fp32")):
@@ -588,7 +599,14 @@ def run_gpu(args):
         value = total_lookups / (ms_total / 1e3)
         sm_mhz = float(pk.get("sm_max_mhz", SM_MAX_MHZ))
         pipe_peak = {"fp32": fp32_peak_tflops(sms, sm_mhz), "tensor": tf32x3_peak_tflops(pk)}
-        parts = kernel_parts(wl)
+        pairs = touched_pairs(wl)
+        parts_ns = kernel_parts(wl)
+        parts_dd = kernel_parts(wl, pairs)
+        # the roofline's FLOP count: per lookup (the metric's count), unless the lookups share
+        # their (i1, i2) pairs so much that it counts more than twice the work done; then per
+        # touched pair, with the per-lookup figure beside it
+        dedup_primary = sum(f for v in parts_dd.values() for f, _ in v) < 0.5 * sum(f for v in parts_ns.values() for f, _ in v)
+        parts = parts_dd if dedup_primary else parts_ns
         step_ms = ms_total / args.steps
         # ideal time of every kernel: its algorithmic FLOPs at the peak of the pipe that runs them
         ideal_ms = {k: sum(f / (pipe_peak[pp] * 1e12) for f, pp in v) * 1e3 for k, v in parts.items()}
@@ -599,10 +617,16 @@ def run_gpu(args):
             eff_peak = kflops[dom] / (ideal_ms[dom] * 1e-3) / 1e12
             pipes = sorted({pp for _, pp in parts[dom]})
             traffic, tnote = measured_traffic(dom)
+            other = parts_ns if dedup_primary else parts_dd
+            other_ideal = sum(f / (pipe_peak[pp] * 1e12) for f, pp in other[dom]) * 1e3
             roof = {"bound": "tensor" if pipes == ["tensor"] else "alu", "achieved": ach, "peak": eff_peak,
                     "unit": "TFLOP/s", "frac": ach / eff_peak, "traffic": traffic, "traffic_note": tnote,
                     "kernel": dom, "avg_ms": kavg[dom], "pipes": {pp: f for f, pp in parts[dom]},
-                    "peak_source": peak_source(parts[dom], pipe_peak, sms, sm_mhz, pk_kind)}
+                    "peak_source": peak_source(parts[dom], pipe_peak, sms, sm_mhz, pk_kind),
+                    "flop_count": ("per touched (i1, i2) pair for the pair contractions (the lookups share pairs: "
+                                   "the per-lookup count is more than twice the work done)" if dedup_primary else
+                                   "per lookup: 4 (q1 r1 q2 r2 + q1 q2 r2 q3) in the backward"),
+                    ("frac_per_lookup_count" if dedup_primary else "frac_per_pair_count"): other_ideal / kavg[dom]}
         else:
             roof = {"bound": "hbm", "achieved": None, "peak": pk["hbm_gbs"], "unit": "GB/s", "frac": None,
                     "traffic": None, "kernel": dom, "avg_ms": kavg[dom]}
@@ -660,8 +684,13 @@ def run_gpu(args):
                                                  "avg_ms": kavg.get(k), "pipes": {pp: f for f, pp in parts[k]}}
                                              for k in parts},
                               "fp32_frac_of_step": step_tf / pipe_peak["fp32"],
-                              "flop_formula": "6 (q1 r1 q2 r2 + q1 q2 r2 q3) per lookup",
+                              "flop_formula": "6 (q1 r1 q2 r2 + q1 q2 r2 q3) per lookup (flops_per_step); frac with "
+                                              + ("6 q1 r1 q2 r2 per touched pair + 6 q1 q2 r2 q3 per lookup"
+                                                 if dedup_primary else "the per-lookup count"),
                               "dedup_flops_per_step": dedup_flops,
+                              "dedup_frac": sum(sum(f / (pipe_peak[pp] * 1e12) for f, pp in v) * 1e3
+                                                for v in parts_dd.values()) / step_ms,
+                              "primary_count": "per touched pair" if dedup_primary else "per lookup",
                               "dedup_formula": "6 q1 r1 q2 r2 per touched (i1, i2) pair + 6 q1 q2 r2 q3 per lookup"},
             "peaks": {"sms": sms, "sm_mhz": sm_mhz, "fp32_tflops": pipe_peak["fp32"],
                       "tf32x3_tflops": pipe_peak["tensor"], "source": pk_kind,

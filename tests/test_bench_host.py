@@ -156,3 +156,19 @@ def test_traffic_record_voided_when_sources_change(tmp_path, monkeypatch):
     f.write_text(json.dumps(rec))
     assert bench.measured_traffic("k_x")[0] is None
     assert bench.measured_traffic("k_missing")[0] is None
+
+
+def test_pair_count_parts_match_dedup_flops():
+    """With the touched pairs, the per-kernel split adds up to 6 A per pair + 6 Bc per
+    lookup (the dedup count), and the pairs are counted from the decoded (i1, i2)."""
+    sys.path.insert(0, ROOT)
+    import bench
+    import oracle
+    from tt_inputs import config
+
+    wl = config(4, batch=128)
+    pairs = bench.touched_pairs(wl)
+    i1, i2, i3, bag = oracle.decode(wl.tables, wl.indices, wl.offsets, wl.batch)
+    assert pairs == [len(set(zip(i1.tolist(), i2.tolist())))]
+    parts = bench.kernel_parts(wl, pairs)
+    assert abs(sum(f for v in parts.values() for f, _ in v) - bench.dedup_step_flops(wl)) < 1e-6 * bench.dedup_step_flops(wl)
