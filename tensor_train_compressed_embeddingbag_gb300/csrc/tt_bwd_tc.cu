@@ -513,20 +513,20 @@ __device__ void tile_bwd_tc_body(const Params& P, const TableDev& T, unsigned ch
             break;
         }
         // Q rows (u, j1): M = 64 puts row r in lane 32 (r / 16) + r % 16
-        if (w < 4) {
-            const int r = 16 * w + lane, u = r >> 2, j1 = r & 3;
+        // warp w reads lane quarter w % 4 (the only lanes it may access) and, at R = 32, the
+        // 16-column half w / 4: every warp takes one 16-column chunk
+        if (R == 32 || w < 4) {
+            const int qw = w & 3, c0 = R == 32 ? 16 * (w >> 2) : 0;
+            const int r = 16 * qw + lane, u = r >> 2, j1 = r & 3;
             const bool live = lane < 16 && u < nb;
             float* dst = P.Qbuf + (int64_t)(start + (live ? pairbeg[u0 + u] : 0)) * P.qs_max + j1 * R;
-#pragma unroll 1
-            for (int c0 = 0; c0 < R; c0 += 16) {
-                float q[16], e[16];
-                const uint32_t cq[5] = {tq1 + c0, tq2 + c0, tq1 + R + c0, tq2 + R + c0, tq1 + 2 * R + c0};
-                tc_sumx16<5>((uint32_t)(32 * w) << 16, cq, q, e);
-                if (live) {
+            float q[16], e[16];
+            const uint32_t cq[5] = {tq1 + c0, tq2 + c0, tq1 + R + c0, tq2 + R + c0, tq1 + 2 * R + c0};
+            tc_sumx16<5>((uint32_t)(32 * qw) << 16, cq, q, e);
+            if (live) {
 #pragma unroll
-                    for (int a = 0; a < 16; a += 4)
-                        *reinterpret_cast<float4*>(dst + c0 + a) = make_float4(q[a], q[a + 1], q[a + 2], q[a + 3]);
-                }
+                for (int a = 0; a < 16; a += 4)
+                    *reinterpret_cast<float4*>(dst + c0 + a) = make_float4(q[a], q[a + 1], q[a + 2], q[a + 3]);
             }
         }
         tc_fence_before();
@@ -548,24 +548,22 @@ __device__ void tile_bwd_tc_body(const Params& P, const TableDev& T, unsigned ch
     float* A2p = T.aux[1] ? T.aux[1] + (int64_t)i2 * R * N2 : nullptr;
     const int nt = P.grp_ntiles[g];
     float* part = P.dG2part + (int64_t)tile * P.s2_max;
-    if (w < 4) {
-        const int jc = N2 == 128 ? 32 * w + lane : 16 * w + lane;
+    if (R == 32 || w < 4) {  // as for Q: warp w takes lane quarter w % 4 and one 16-column chunk
+        const int qw = w & 3, c0 = R == 32 ? 16 * (w >> 2) : 0;
+        const int jc = N2 == 128 ? 32 * qw + lane : 16 * qw + lane;
         const bool live = N2 == 128 || lane < 16;
-#pragma unroll 1
-        for (int c0 = 0; c0 < R; c0 += 16) {
-            float gv[16], ge[16];
-            const uint32_t cg[3] = {tg + c0, tg + R + c0, tg + 2 * R + c0};
-            tc_sumx16<3>((uint32_t)(32 * w) << 16, cg, gv, ge);
-            if (live) {
-                if (nt == 1) {  // sixteen loads in flight, then the stores
-                    int idx[16];
+        float gv[16], ge[16];
+        const uint32_t cg[3] = {tg + c0, tg + R + c0, tg + 2 * R + c0};
+        tc_sumx16<3>((uint32_t)(32 * qw) << 16, cg, gv, ge);
+        if (live) {
+            if (nt == 1) {  // sixteen loads in flight, then the stores
+                int idx[16];
 #pragma unroll
-                    for (int a = 0; a < 16; ++a) idx[a] = (c0 + a) * N2 + jc;
-                    core_update_n<16>(P, G2p, A2p, idx, gv);
-                } else {
+                for (int a = 0; a < 16; ++a) idx[a] = (c0 + a) * N2 + jc;
+                core_update_n<16>(P, G2p, A2p, idx, gv);
+            } else {
 #pragma unroll
-                    for (int a = 0; a < 16; ++a) part[(c0 + a) * N2 + jc] = gv[a];
-                }
+                for (int a = 0; a < 16; ++a) part[(c0 + a) * N2 + jc] = gv[a];
             }
         }
     }
