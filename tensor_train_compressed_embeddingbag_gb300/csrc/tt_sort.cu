@@ -412,10 +412,19 @@ __global__ void __launch_bounds__(kSmallChunk) k_decode_small(const __grid_const
     const int64_t row = n < hi ? P.idx[n] : 0;
     const float wv = (n < hi && P.w) ? P.w[n] : 1.0f;
     const int epoch = *P.epoch;
-    if (c == 0 && threadIdx.x == 64 && (P.off[0] != 0 || P.off[P.nbags] != P.nnz)) atomicOr(P.err, kErrOffsets);
-    for (int64_t g = (int64_t)c * blockDim.x + threadIdx.x; g < P.nbags; g += (int64_t)gridDim.x * blockDim.x)
-        if (P.off[g] > P.off[g + 1]) atomicOr(P.err, kErrOffsets);
+    if (threadIdx.x == 0) asm volatile("prefetch.global.L1 [%0];" ::"l"(P.tables));  // the decode reads it next
     const int nst = stage_bag_offsets(P, lo, hi, soff, sb, kDecodeOffs);
+    if (nst == P.nbags + 1) {  // every offset staged: block 0 checks them in shared memory
+        if (c == 0) {
+            if (threadIdx.x == 64 && (soff[0] != 0 || soff[P.nbags] != P.nnz)) atomicOr(P.err, kErrOffsets);
+            for (int64_t g = threadIdx.x; g < P.nbags; g += blockDim.x)
+                if (soff[g] > soff[g + 1]) atomicOr(P.err, kErrOffsets);
+        }
+    } else {
+        if (c == 0 && threadIdx.x == 64 && (P.off[0] != 0 || P.off[P.nbags] != P.nnz)) atomicOr(P.err, kErrOffsets);
+        for (int64_t g = (int64_t)c * blockDim.x + threadIdx.x; g < P.nbags; g += (int64_t)gridDim.x * blockDim.x)
+            if (P.off[g] > P.off[g + 1]) atomicOr(P.err, kErrOffsets);
+    }
     int d[3] = {-1, -1, -1};
     if (n < hi) {
         const int64_t bag = nst ? staged_bag(soff, sb[0], nst, n) : bag_of(P, n);

@@ -146,6 +146,18 @@ def test_groups_span_many_tiles():
     full_parity(synthetic([3, 2, 5], [2, 2, 2], [3, 5], rng.integers(0, 9, size=400), seed=1, weights=True))
 
 
+@pytest.mark.parametrize("r", [16, 32])
+def test_tensor_core_groups_span_many_tiles(r):
+    """The tensor-core backward (q = [4, 4, 4], r1 = r2 = 16 or 32) with p2 = 3: three
+    (i2) groups of ~300 lookups, each cut into several 64-lookup tiles of up to four
+    batches of pairs, tiles launched longest first, every group's dG2 summed by its
+    last tile; uniform rows and few distinct rows (long runs of one pair)."""
+    rng = np.random.default_rng(11)
+    lengths = rng.integers(1, 16, size=110)
+    full_parity(synthetic([40, 3, 30], [4, 4, 4], [r, r], lengths, seed=11, weights=True))
+    full_parity(synthetic([40, 3, 30], [4, 4, 4], [r, r], lengths, seed=12, dist="few", mode="mean"))
+
+
 def test_repeated_rows_span_tiles():
     rng = np.random.default_rng(2)
     full_parity(synthetic([7, 3, 4], [2, 4, 1], [6, 2], rng.integers(1, 30, size=100), seed=2, dist="few"))
