@@ -340,12 +340,12 @@ int tt_emb_last_launch_count(tt_emb* h, int which);
 
 /*
  * Bound of the handle's device waits.  The pages have no counterpart: the
- * tensor-core kernels wait for their own MMAs on an mbarrier, at most `polls`
- * polls (default 2^24, far longer than any MMA batch).  A wait that gives up
- * records TT_ERR_TIMEOUT (read by tt_emb_get_last_error), issues no further
- * MMA, waits with the default bound for the MMAs already in flight and frees
- * its tensor memory; the call's results are then undefined and a following
- * backward changes no core.  polls = 0 makes every such wait give up at once
+ * tensor-core kernels wait for their own MMAs and for the bulk copies of their
+ * G2 slices on mbarriers, at most `polls` polls (default 2^24, far longer than
+ * any MMA batch or copy).  A wait that gives up records TT_ERR_TIMEOUT (read by
+ * tt_emb_get_last_error), issues no further MMA, waits with the default bound
+ * for the MMAs or copies already in flight and frees its tensor memory; the
+ * call's results are then undefined and a following backward changes no core.  polls = 0 makes every such wait give up at once
  * (a test of that path).  Takes effect from the next call.  Returns
  * TT_ERR_ARG for a null handle.
  */
