@@ -582,7 +582,13 @@ tt_status tt_emb_forward(tt_emb* h, const int64_t* indices, int64_t nnz, const i
         q.run("pool", launch_pool);
     }
     st = q.finish();
-    if (st == TT_OK) h->has_fwd = true;
+    if (st == TT_OK) {
+        h->has_fwd = true;
+    } else if (small) {
+        // a pass cut short may not reach k_pool, which advances the epoch: clear the decode
+        // stamps so that the next pass's k_fwd_T blocks cannot take them for its own
+        cudaMemsetAsync(P.dec_done, 0, sizeof(int) * kDecDoneSlots, s);
+    }
     return st;
 }
 
