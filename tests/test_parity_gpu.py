@@ -337,3 +337,33 @@ def test_workspace_reuse_across_sizes(workloads):
     for k in range(3):
         assert_rows_close(got[k], ref_cores[k], f"G{k + 1} after three calls")
     run.close()
+
+
+@pytest.mark.parametrize("q,r", [([4, 4, 4], [32, 32]), ([2, 2, 2], [4, 4])])
+def test_consecutive_passes_new_lookups(q, r):
+    """Four forward + backward passes on one handle, every pass with new indices, bag
+    lengths, weights and upstream gradients (the small path, whose forward T blocks start
+    on the decode blocks' per-pass stamps): each pass against the oracle's chain of steps."""
+    rng = np.random.default_rng(21)
+    spec_wl = synthetic([40, 30, 25], q, r, [1], seed=21)
+    spec = spec_wl.tables[0]
+    run = GpuRun(spec_wl)
+    ref_cores = [c.astype(np.float64) for c in spec_wl.cores[0]]
+    for step in range(4):
+        lengths = rng.integers(0, 30, size=60)
+        wl = synthetic([40, 30, 25], q, r, lengths, seed=100 + step, weights=step % 2 == 0,
+                       mode="mean" if step == 1 else "sum")
+        out = torch.empty((wl.num_bags, spec.embedding_dim), dtype=torch.float32, device="cuda")
+        mode = tt.TT_POOL_MEAN if wl.mode == "mean" else tt.TT_POOL_SUM
+        w = None if wl.weights is None else dev(wl.weights)
+        tt.tt_emb_forward(run.h, dev(wl.indices), dev(wl.offsets), w, mode, out)
+        ref = oracle.forward(wl.tables, [ref_cores], wl.indices, wl.offsets, wl.weights, wl.mode, wl.batch)
+        assert_rows_close(out.cpu().numpy(), ref, f"pass {step} forward")
+        tt.tt_emb_backward(run.h, dev(wl.grad_out), wl.lr)
+        assert run.error() == tt.TT_OK
+        ref_cores = oracle.sgd_step(wl.tables, [ref_cores], wl.indices, wl.offsets, wl.grad_out, wl.lr,
+                                    wl.weights, wl.mode)[0]
+        got = run.cores_host()[0]
+        for k in range(3):
+            assert_rows_close(got[k], ref_cores[k], f"pass {step} G{k + 1}")
+    run.close()
