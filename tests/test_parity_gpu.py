@@ -367,3 +367,17 @@ def test_consecutive_passes_new_lookups(q, r):
         for k in range(3):
             assert_rows_close(got[k], ref_cores[k], f"pass {step} G{k + 1}")
     run.close()
+
+
+@pytest.mark.parametrize("cid,batch", [(2, 128), (3, 96), (3, 800)])
+def test_ffma_backward_on_tensor_core_classes(monkeypatch, cid, batch):
+    """TTEMB_BWD_FFMA=1 keeps the rank-16/32 classes on the FFMA backward (k_tile_bwd
+    with the column split): full parity on the 11M x 64 workload (small-batch path)
+    and the Zipf weighted-mean workload (small path; and at 800 bags, ~16k lookups,
+    the large-batch path)."""
+    monkeypatch.setenv("TTEMB_BWD_FFMA", "1")
+    wl = config(cid, batch=batch)
+    if wl.nnz > 12288:
+        sampled_parity(wl, nbags=128, per_core=8)
+    else:
+        full_parity(wl)
